@@ -1,0 +1,425 @@
+"""Plain CPU oracle for InfiniGen's per-layer decode-step speculation and sparse attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports, calls or links this module;
+only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may use it.
+It shares no code with the CUDA library: it is NumPy in float64, written step by step from
+the method's description, with no blocking, fusion or reordering beyond what that
+description states.
+
+Source: "InfiniGen: Efficient Generative Inference of Large Language Models with Dynamic KV
+Cache Management" (Lee, Lee, Seo, Sim; OSDI 2024, arXiv 2406.19707), as retold by the
+paper-graph summary page of that paper, section 3.4 ("Detailed, Sentence-Based Technical
+Breakdown").  Every function below names the part of that section it follows.
+
+Readings taken where the page is silent or garbled (each is listed in the design notes):
+  * score scale: speculated and real logits carry the 1/sqrt(d) factor, passed in as
+    ``scale`` (the page writes softmax(QK^T)V without one);
+  * the skew is per head: A_h is d x d (a full D x D rotation would mix heads);
+  * k = floor(ratio * d + 0.5) columns per head; the same columns serve every sequence;
+  * the column score sums the per-column absolute sums of W~_Q and K~ (the page's
+    element-wise sum of two differently shaped matrices cannot be taken literally);
+  * RoPE, when present, is applied before the skew: q~ = RoPE(q) A, k~ = RoPE(k) A;
+  * the current token's own key/value always join the attended set;
+  * the threshold test s_t > max - alpha is evaluated as max - s_t < alpha, so the maximum
+    is kept for every alpha > 0 even where max - alpha rounds back to max;
+  * multi-head averaging rounds the mean count half-up, with a minimum of one token;
+  * the transfer cap and the averaged count keep the best tokens by (score desc, index asc);
+  * pool counters are 8-bit, +1 per (layer, step) when any head selected the slot, halved
+    for the whole (layer, sequence) pool when one of them reaches 255; the victim is the
+    smallest counter, then the oldest insertion, then the lowest slot.
+
+Parity pins: every function here is pinned by a ``-m "not gpu"`` test (closed forms,
+values the page prints, brute force on tiny inputs).  Two choices are consistency-checked
+only ("parity unpinned"): the column choice on isotropic synthetic data (near ties), and the
+RoPE placement reading.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+SEL_THRESHOLD = 0
+SEL_HEAD_AVG = 1
+
+
+# ----------------------------------------------------------------------------------------
+# Hyper-parameters and accounting
+# ----------------------------------------------------------------------------------------
+def partial_columns(ratio: float, d: int) -> int:
+    """Number of partial columns per head, k = round(ratio * d) half-up.
+
+    Section 3.4, "Skewed Partial Weights" (k = 0.3 x D) applied per head of width d.
+    """
+    return int(math.floor(float(ratio) * d + 0.5))
+
+
+def cap_count(cap_frac: float, n_tokens: int) -> int:
+    """Per-layer transfer cap in tokens: round(cap_frac * n) half-up; cap_frac >= 1 means none.
+
+    Section 3.4, "Decoding Stage", Step 5 (up to 20 % of the KV cache).  The arithmetic is
+    done in float64 on the float32 value of ``cap_frac`` (the library takes a C float).
+    """
+    cf = float(np.float32(cap_frac))
+    if cf >= 1.0:
+        return int(n_tokens)
+    return int(math.floor(cf * float(n_tokens) + 0.5))
+
+
+def kv_bytes(layers: int, batch: int, tokens: int, hidden: int, elem_bytes: int = 2) -> int:
+    """Full KV cache size: keys and values of every token, layer and sequence (Fig 2 formula)."""
+    return layers * batch * tokens * hidden * 2 * elem_bytes
+
+
+# ----------------------------------------------------------------------------------------
+# RoPE (the rotate-half form, pairs (j, j + d/2))
+# ----------------------------------------------------------------------------------------
+def rope(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotary position embedding of the last axis of ``x`` (length d, even).
+
+    Pair j (j < d/2) is the plane (x_j, x_{j+d/2}), turned by the angle p * theta^(-2j/d).
+    ``positions`` broadcasts against ``x.shape[:-1]``.  The page names only
+    ``apply_rotary_pos_emb``/``rotate_half``; this is the standard half-split form.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    half = d // 2
+    j = np.arange(half, dtype=np.float64)
+    inv_freq = float(theta) ** (-2.0 * j / d)
+    ang = np.asarray(positions, dtype=np.float64)[..., None] * inv_freq
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = x[..., :half], x[..., half:]
+    return np.concatenate([lo * c - hi * s, lo * s + hi * c], axis=-1)
+
+
+# ----------------------------------------------------------------------------------------
+# Offline skew (section 3.4, "Skewed Partial Weights": Q = U S V^T, A = V, W~ = W A)
+# ----------------------------------------------------------------------------------------
+def canonical_signs(A: np.ndarray) -> np.ndarray:
+    """Flip each column of A so that its entry of largest magnitude is positive.
+
+    Ties go to the lowest row.  Any column sign is a valid SVD; this fixes one.
+    """
+    A = np.array(A, dtype=np.float64, copy=True)
+    for j in range(A.shape[1]):
+        r = int(np.argmax(np.abs(A[:, j])))
+        if A[r, j] < 0:
+            A[:, j] = -A[:, j]
+    return A
+
+
+def sample_queries(Xs: np.ndarray, Wq: np.ndarray, H: int, d: int, rope_theta: float = 0.0):
+    """Per-head sample query matrices Q_h = X_s W_Q,h (float64), post-RoPE at positions 0..Ns-1."""
+    X = np.asarray(Xs, dtype=np.float64)
+    W = np.asarray(Wq, dtype=np.float64)
+    Q = (X @ W).reshape(X.shape[0], H, d)
+    if rope_theta:
+        Q = rope(Q, np.arange(X.shape[0])[:, None], rope_theta)
+    return Q
+
+
+def skew(Xs, Wq, Wk, H: int, d: int, rope_theta: float = 0.0, Kprompt=None):
+    """Offline skewing controller.
+
+    For each head h: Q_h = X_s W_Q,h; SVD Q_h = U S V^T; A_h = V (columns in descending
+    singular value, signs canonical).  W~_Q,h = W_Q,h A_h and W~_K,h = W_K,h A_h, rounded once
+    to fp16.  If ``Kprompt`` ([N, H, d], unskewed, post-RoPE for RoPE models) is given, the
+    skewed prompt keys K~ = K A are returned too (rounded to fp16).
+
+    Returns (A [H,d,d] float64, sigma [H,d], Wq_skew fp16 [D,H*d], Wk_skew fp16 [D,H*d],
+    K_skew fp16 [N,H,d] or None).
+    """
+    Q = sample_queries(Xs, Wq, H, d, rope_theta)
+    Wq64 = np.asarray(Wq, dtype=np.float64)
+    Wk64 = np.asarray(Wk, dtype=np.float64)
+    D = Wq64.shape[0]
+    A = np.zeros((H, d, d))
+    sig = np.zeros((H, d))
+    Wq_s = np.zeros((D, H * d), dtype=np.float16)
+    Wk_s = np.zeros((D, H * d), dtype=np.float16)
+    for h in range(H):
+        _, s, vt = np.linalg.svd(Q[:, h, :], full_matrices=False)
+        A[h] = canonical_signs(vt.T)
+        sig[h] = s
+        Wq_s[:, h * d:(h + 1) * d] = (Wq64[:, h * d:(h + 1) * d] @ A[h]).astype(np.float16)
+        Wk_s[:, h * d:(h + 1) * d] = (Wk64[:, h * d:(h + 1) * d] @ A[h]).astype(np.float16)
+    Ks = None
+    if Kprompt is not None:
+        K64 = np.asarray(Kprompt, dtype=np.float64)
+        Ks = np.einsum("nhc,hcj->nhj", K64, A).astype(np.float16)
+    return A, sig, Wq_s, Wk_s, Ks
+
+
+def choose_columns(Wq_skew, K_skew, H: int, d: int, k: int) -> np.ndarray:
+    """Partial weight index generation (section 3.4, "Prefill Stage", Step 2, Fig 9).
+
+    colscore_h[c] = sum_r |W~_Q,h[r, c]| + sum_t |K~_h[t, c]| (t over every prompt key of every
+    sequence); keep the k largest (ties to the lower column), stored ascending.
+    ``K_skew`` is [..., H, d] (any leading token axes) or None.
+    Returns int32 [H, k].
+    """
+    W = np.abs(np.asarray(Wq_skew, dtype=np.float64))
+    cols = np.zeros((H, k), dtype=np.int32)
+    for h in range(H):
+        score = W[:, h * d:(h + 1) * d].sum(axis=0)
+        if K_skew is not None:
+            Kh = np.abs(np.asarray(K_skew, dtype=np.float64)[..., h, :]).reshape(-1, d)
+            score = score + Kh.sum(axis=0)
+        order = sorted(range(d), key=lambda c: (-score[c], c))
+        cols[h] = np.sort(np.array(order[:k], dtype=np.int32))
+    return cols
+
+
+def colscores(Wq_skew, K_skew, H: int, d: int) -> np.ndarray:
+    """The column scores used by :func:`choose_columns` ([H, d], float64)."""
+    W = np.abs(np.asarray(Wq_skew, dtype=np.float64))
+    out = np.zeros((H, d))
+    for h in range(H):
+        out[h] = W[:, h * d:(h + 1) * d].sum(axis=0)
+        if K_skew is not None:
+            out[h] += np.abs(np.asarray(K_skew, dtype=np.float64)[..., h, :]).reshape(-1, d).sum(axis=0)
+    return out
+
+
+def partial_weight(Wq_skew, cols, H: int, d: int) -> np.ndarray:
+    """Step 3 of the prefill stage: W~_Q^partial = the selected columns, head-contiguous.
+
+    Returns fp16 [D, H*k] whose column h*k + i is W~_Q[:, h*d + cols[h, i]].
+    """
+    k = cols.shape[1]
+    W = np.asarray(Wq_skew)
+    out = np.zeros((W.shape[0], H * k), dtype=W.dtype)
+    for h in range(H):
+        out[:, h * k:(h + 1) * k] = W[:, h * d + cols[h]]
+    return out
+
+
+def partial_key_cache(K_pool, cols) -> np.ndarray:
+    """Step 3 of the prefill stage: the partial key cache, the selected columns of each key.
+
+    K_pool [B, H, T, d] (skewed keys by slot) -> [B, H, k, T]: row c of head h holds
+    K~[b, h, :, cols[h, c]], token axis last (the layout the score step reads).
+    """
+    K = np.asarray(K_pool)
+    B, H, T, d = K.shape
+    k = cols.shape[1]
+    out = np.zeros((B, H, k, T), dtype=K.dtype)
+    for h in range(H):
+        for c in range(k):
+            out[:, h, c, :] = K[:, h, :, cols[h, c]]
+    return out
+
+
+# ----------------------------------------------------------------------------------------
+# Decode stage (section 3.4, "Decoding Stage: Speculative KV Selection and Prefetching")
+# ----------------------------------------------------------------------------------------
+def partial_query(x, Wq_part, H: int, k: int) -> np.ndarray:
+    """Step 1: q~p(i) = x_a(i-1) W~_Q^partial,(i).  x [B, D] fp16, W [D, H*k] -> [B, H, k] float64."""
+    q = np.asarray(x, dtype=np.float64) @ np.asarray(Wq_part, dtype=np.float64)
+    return q.reshape(q.shape[0], H, k)
+
+
+def partial_query_rope(x, Wq, A, cols, positions, theta: float) -> np.ndarray:
+    """Step 1 for RoPE models: q = x W_Q,h, rotated at the token's position, then q A_h[:, S_h].
+
+    x [B, D]; Wq [D, H*d] (unskewed); A [H, d, d]; cols [H, k]; positions [B].
+    Returns [B, H, k] float64.
+    """
+    H, d, _ = np.asarray(A).shape
+    B = np.asarray(x).shape[0]
+    q = (np.asarray(x, dtype=np.float64) @ np.asarray(Wq, dtype=np.float64)).reshape(B, H, d)
+    q = rope(q, np.asarray(positions)[:, None], theta)
+    k = cols.shape[1]
+    out = np.zeros((B, H, k))
+    for h in range(H):
+        out[:, h, :] = q[:, h, :] @ np.asarray(A[h], dtype=np.float64)[:, cols[h]]
+    return out
+
+
+def speculate(q_part, K_part, L_valid, scale) -> np.ndarray:
+    """Step 2: SpecScore = scale * q~p (K~p)^T over the resident tokens.
+
+    q_part [B, H, k] float; K_part [B, H, k, Lcap] fp16 (column-major per head, token axis
+    last); L_valid [B].  Slots t >= L_valid[b] get -inf.  ``scale`` is taken at float32
+    precision (it is a C float in the library) and applied in float64.
+    Returns [B, H, Lcap] float64.
+    """
+    q = np.asarray(q_part, dtype=np.float64)
+    K = np.asarray(K_part, dtype=np.float64)
+    B, H, k, Lcap = K.shape
+    sc = float(np.float32(scale))
+    s = np.full((B, H, Lcap), -np.inf)
+    for b in range(B):
+        L = int(L_valid[b])
+        s[b, :, :L] = sc * np.einsum("hc,hct->ht", q[b], K[b, :, :, :L])
+    return s
+
+
+def _best_first(s: np.ndarray, n: int) -> np.ndarray:
+    """Indices of the n best entries by (score desc, index asc), NaN never chosen, ascending."""
+    ok = [t for t in range(len(s)) if not np.isnan(s[t])]
+    ok.sort(key=lambda t: (-s[t], t))
+    return np.array(sorted(ok[:n]), dtype=np.int64)
+
+
+def select(scores, L_valid, alpha, policy: int = SEL_THRESHOLD, cap_frac: float = 1.0):
+    """Steps 3-4 (and the Step 5 cap): which tokens each head prefetches.
+
+    Threshold: I = {t : s_t > max(s) - alpha}, with max over the resident, non-NaN scores,
+    evaluated as (max(s) - s_t) < alpha; NaN scores are never selected.  The comparison is made in the dtype of ``scores``
+    (float64 end to end; float32 when the kernel's own scores are fed in), with
+    ``alpha`` taken at float32 precision.
+    Cap (cap_frac < 1): a head with more than cap_n = round(cap_frac * L) tokens keeps its
+    cap_n best by (score desc, index asc).
+    HEAD_AVG: cbar = max(1, round_half_up(mean_h |I_h|)), at most cap_n; every head then keeps
+    its cbar best (same order), regardless of the threshold.
+    Returns (idx list-of-lists [B][H] of ascending int arrays, cnt int32 [B, H],
+    used uint8 [B, Lcap] = 1 where any head of sequence b selected slot t).
+    """
+    s_all = np.asarray(scores)
+    dt = s_all.dtype.type
+    B, H, Lcap = s_all.shape
+    a = dt(np.float32(alpha))
+    idx = [[None] * H for _ in range(B)]
+    cnt = np.zeros((B, H), dtype=np.int32)
+    used = np.zeros((B, Lcap), dtype=np.uint8)
+    for b in range(B):
+        L = int(L_valid[b])
+        capn = cap_count(cap_frac, L)
+        for h in range(H):
+            s = s_all[b, h, :L]
+            finite = s[~np.isnan(s)]
+            if finite.size == 0:
+                idx[b][h] = np.zeros(0, dtype=np.int64)
+                continue
+            m = dt(finite.max())
+            # s_t > m - alpha, evaluated as the gap m - s_t < alpha so that the maximum
+            # itself (gap exactly 0) is kept for every alpha > 0
+            sel = np.array([t for t in range(L) if dt(m - s[t]) < a], dtype=np.int64)
+            if policy == SEL_THRESHOLD and sel.size > capn:
+                sel = _best_first(s, capn)
+            idx[b][h] = sel
+        if policy == SEL_HEAD_AVG:
+            tot = sum(len(idx[b][h]) for h in range(H))
+            cbar = max(1, (2 * tot + H) // (2 * H))
+            cbar = min(cbar, capn)
+            for h in range(H):
+                idx[b][h] = _best_first(s_all[b, h, :L], cbar)
+        for h in range(H):
+            cnt[b, h] = len(idx[b][h])
+            used[b, idx[b][h]] = 1
+    return idx, cnt, used
+
+
+def gather(K_pool, V_pool, idx, Lcap: int):
+    """Step 5: copy the selected full key/value rows out of the pool.
+
+    K_pool, V_pool: [B, H, Cap, d] (one layer).  Returns Kg, Vg [B, H, Lcap, d] with rows
+    j < cnt[b, h] filled (idx[b][h][j]) and the rest zero.
+    """
+    Kp = np.asarray(K_pool)
+    Vp = np.asarray(V_pool)
+    B, H, _, d = Kp.shape
+    Kg = np.zeros((B, H, Lcap, d), dtype=Kp.dtype)
+    Vg = np.zeros((B, H, Lcap, d), dtype=Vp.dtype)
+    for b in range(B):
+        for h in range(H):
+            ii = np.asarray(idx[b][h], dtype=np.int64)
+            Kg[b, h, :len(ii)] = Kp[b, h, ii]
+            Vg[b, h, :len(ii)] = Vp[b, h, ii]
+    return Kg, Vg
+
+
+def attend(q, Kg, Vg, cnt, scale, k_new=None, v_new=None) -> np.ndarray:
+    """Inference controller: attention over the prefetched rows (plus the current token).
+
+    z_j = scale * q . K_j over j < cnt[b, h] (and the current token's own key if given);
+    w = softmax(z); o = sum_j w_j V_j, all in float64.  Returns [B, H, d] float64.
+    """
+    q64 = np.asarray(q, dtype=np.float64)
+    K = np.asarray(Kg, dtype=np.float64)
+    V = np.asarray(Vg, dtype=np.float64)
+    B, H, _, d = K.shape
+    sc = float(np.float32(scale))
+    out = np.zeros((B, H, d))
+    for b in range(B):
+        for h in range(H):
+            c = int(cnt[b, h])
+            Ks, Vs = K[b, h, :c], V[b, h, :c]
+            if k_new is not None:
+                Ks = np.concatenate([Ks, np.asarray(k_new, dtype=np.float64)[b, h][None]], 0)
+                Vs = np.concatenate([Vs, np.asarray(v_new, dtype=np.float64)[b, h][None]], 0)
+            if Ks.shape[0] == 0:
+                continue
+            z = sc * (Ks @ q64[b, h])
+            w = np.exp(z - z.max())
+            w = w / w.sum()
+            out[b, h] = w @ Vs
+    return out
+
+
+# ----------------------------------------------------------------------------------------
+# KV cache pool (section 3.4, "KV Cache Pool Management Under Memory Pressure", Table 2)
+# ----------------------------------------------------------------------------------------
+@dataclass
+class CounterPool:
+    """One (layer, sequence) pool of ``cap`` slots with counter-based eviction.
+
+    Counters are 8-bit: +1 per update when the slot was used (saturating at 255); when any
+    counter reaches 255 every counter of the pool is halved.  Insertion fills free slots in
+    order; once full, the victim is the slot with the smallest counter, then the oldest
+    insertion, then the lowest index.  A new entry starts at counter 0.
+    """
+    cap: int
+    counter: np.ndarray = field(default=None)
+    seq: np.ndarray = field(default=None)
+    filled: int = 0
+    next_seq: int = 0
+
+    def __post_init__(self):
+        self.counter = np.zeros(self.cap, dtype=np.int64)
+        self.seq = np.zeros(self.cap, dtype=np.int64)
+
+    def update(self, used) -> None:
+        used = np.asarray(used)[: self.cap]
+        for s in range(self.filled):
+            if used[s]:
+                self.counter[s] = min(255, self.counter[s] + 1)
+        if self.filled and self.counter[: self.filled].max() >= 255:
+            self.counter[: self.filled] >>= 1
+
+    def insert(self) -> int:
+        if self.filled < self.cap:
+            slot = self.filled
+            self.filled += 1
+        else:
+            slot = min(range(self.cap), key=lambda s: (self.counter[s], self.seq[s], s))
+        self.counter[slot] = 0
+        self.seq[slot] = self.next_seq
+        self.next_seq += 1
+        return slot
+
+    def evict(self, used) -> int:
+        """One decode-step pool action: fold in this step's use, then place the new token."""
+        if used is not None:
+            self.update(used)
+        return self.insert()
+
+
+# ----------------------------------------------------------------------------------------
+# One layer-step, end to end
+# ----------------------------------------------------------------------------------------
+def decode_layer_step(x_prev, Wq_part, K_part, L_valid, q, K_pool, V_pool, *, H, k, scale,
+                      alpha, policy=SEL_THRESHOLD, cap_frac=1.0, k_new=None, v_new=None):
+    """Speculate layer i from layer i-1's input, select, gather, and attend at layer i.
+
+    Returns a dict with q_part, scores, idx, cnt, used, out (float64).
+    """
+    Lcap = np.asarray(K_part).shape[-1]
+    qp = partial_query(x_prev, Wq_part, H, k)
+    s = speculate(qp, K_part, L_valid, scale)
+    idx, cnt, used = select(s, L_valid, alpha, policy, cap_frac)
+    Kg, Vg = gather(K_pool, V_pool, idx, Lcap)
+    out = attend(q, Kg, Vg, cnt, scale, k_new, v_new)
+    return dict(q_part=qp, scores=s, idx=idx, cnt=cnt, used=used, out=out)

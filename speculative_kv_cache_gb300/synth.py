@@ -1,0 +1,179 @@
+"""Seeded synthetic inputs shaped like the OPT / Llama-2 decode workloads.
+
+This module draws random tensors and nothing else: it holds none of the method's
+arithmetic (no skew, no projection, no scoring, no selection, no attention).  Both the CUDA
+path and the CPU oracle take their inputs from here, so they see identical bytes.
+
+Recipe (trained weights and the PG-19 / WikiText-2 text are not available, so random-init
+stand-ins take their shapes):
+  * weights W ~ N(0, 0.02^2); layer inputs x ~ N(0, 1); sample inputs X_s ~ N(0, 1);
+  * consecutive layer inputs drift as x_l = (x_{l-1} + 0.4 eps) / sqrt(1.16), giving the
+    cos(x_l, x_{l-1}) ~ 0.93 that the paper's Table 1 reports between adjacent blocks;
+  * keys and values (already in the skewed basis) ~ N(0, (0.02 sqrt(D))^2), the law of x W
+    for isotropic x and W, which an orthogonal skew leaves unchanged;
+  * the OPT-30B-shaped workload plants high-norm keys: each (layer, seq, head, token) is
+    chosen with probability 2 % and its key row is scaled by gamma = 2, which makes the
+    attention skewed so that a few percent of the tokens pass the alpha threshold.
+"""
+from __future__ import annotations
+
+import math
+import zlib
+from dataclasses import dataclass, field
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    layers: int
+    heads: int
+    head_dim: int
+    hidden: int
+    batch: int
+    prompt: int
+    gen: int
+    ratio: float
+    alphas: tuple
+    rope_theta: float = 0.0
+    pool_frac: float = 1.0          # pool capacity as a fraction of prompt + gen
+    planted_p: float = 0.0
+    planted_gamma: float = 1.0
+    w_std: float = 0.02
+    kv_std: float | None = None     # None: 0.02 * sqrt(hidden)
+    sample_rows: int = 512          # rows of the offline skew sample X_s
+
+    @property
+    def context(self) -> int:
+        return self.prompt + self.gen
+
+    @property
+    def lcap(self) -> int:
+        """Slot capacity of the partial key cache: the pool size rounded up to 8 tokens."""
+        return (self.pool_cap + 7) // 8 * 8
+
+    @property
+    def pool_cap(self) -> int:
+        if self.pool_frac >= 1.0:
+            return self.context
+        return int(math.floor(self.pool_frac * self.context + 0.5))
+
+    @property
+    def k(self) -> int:
+        return int(math.floor(self.ratio * self.head_dim + 0.5))
+
+    @property
+    def key_std(self) -> float:
+        return self.kv_std if self.kv_std is not None else self.w_std * math.sqrt(self.hidden)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 4, 64, 256, 1, 256, 0, 0.25, (4.0,), kv_std=0.02, sample_rows=256),
+    "opt-6.7b": Workload("opt-6.7b", 32, 32, 128, 4096, 8, 1920, 128, 0.3, (4.0,)),
+    "llama-2-7b": Workload("llama-2-7b", 32, 32, 128, 4096, 4, 3968, 128, 0.3, (2.0, 4.0, 6.0),
+                           rope_theta=10000.0),
+    "llama-2-13b": Workload("llama-2-13b", 40, 40, 128, 5120, 8, 3968, 128, 0.3, (4.0,),
+                            rope_theta=10000.0, pool_frac=0.6),
+    "opt-30b": Workload("opt-30b", 48, 56, 128, 7168, 16, 1920, 128, 0.3, (4.0,),
+                        planted_p=0.02, planted_gamma=2.0),
+}
+
+
+def rng(workload: str, tensor: str, *idx: int, base_seed: int = 0) -> np.random.Generator:
+    """An independent, reproducible stream per (workload, tensor, indices)."""
+    key = [base_seed, zlib.crc32(workload.encode()), zlib.crc32(tensor.encode())] + [int(i) for i in idx]
+    return np.random.Generator(np.random.Philox(np.random.SeedSequence(key)))
+
+
+def normal_f16(g: np.random.Generator, shape, std: float) -> np.ndarray:
+    return (g.standard_normal(shape, dtype=np.float32) * np.float32(std)).astype(np.float16)
+
+
+# ---------------------------------------------------------------------------------------
+# Offline-skew inputs (one layer)
+# ---------------------------------------------------------------------------------------
+def skew_inputs(w: Workload, layer: int = 0, rows: int | None = None):
+    """Sample input X_s [Ns, D] fp16 ~ N(0,1) and the unskewed W_Q, W_K [D, H*d] fp16."""
+    ns = rows or w.sample_rows
+    D = w.hidden
+    Xs = normal_f16(rng(w.name, "Xs", layer), (ns, D), 1.0)
+    Wq = normal_f16(rng(w.name, "Wq", layer), (D, w.heads * w.head_dim), w.w_std)
+    Wk = normal_f16(rng(w.name, "Wk", layer), (D, w.heads * w.head_dim), w.w_std)
+    return Xs, Wq, Wk
+
+
+def prompt_keys_unskewed(w: Workload, layer: int = 0, tokens: int | None = None, std: float | None = None):
+    """Unskewed prompt keys [B, N, H, d] fp16 (the offline column choice reads them)."""
+    n = tokens or w.prompt
+    return normal_f16(rng(w.name, "Kraw", layer), (w.batch, n, w.heads, w.head_dim),
+                      w.key_std if std is None else std)
+
+
+# ---------------------------------------------------------------------------------------
+# Decode-step inputs
+# ---------------------------------------------------------------------------------------
+def layer_inputs(w: Workload, step: int = 0, layers: int | None = None) -> np.ndarray:
+    """Attention inputs of every layer at one decode step: x [L, B, D] fp16 with drift."""
+    nl = layers or w.layers
+    g = rng(w.name, "x", step)
+    x = np.zeros((nl, w.batch, w.hidden), dtype=np.float32)
+    x[0] = g.standard_normal((w.batch, w.hidden), dtype=np.float32)
+    for l in range(1, nl):
+        eps = g.standard_normal((w.batch, w.hidden), dtype=np.float32)
+        x[l] = (x[l - 1] + np.float32(0.4) * eps) / np.float32(math.sqrt(1.16))
+    return x.astype(np.float16)
+
+
+def pool_layer(w: Workload, layer: int, cap: int | None = None):
+    """Skewed keys and values of one layer's pool: K~, V [B, H, cap, d] fp16.
+
+    Planted high-norm rows (OPT-30B shape) scale the chosen key rows by gamma.
+    """
+    cap = cap or w.pool_cap
+    shape = (w.batch, w.heads, cap, w.head_dim)
+    K = rng(w.name, "K", layer).standard_normal(shape, dtype=np.float32) * np.float32(w.key_std)
+    if w.planted_p > 0:
+        m = rng(w.name, "plant", layer).random(shape[:3]) < w.planted_p
+        K[m] *= np.float32(w.planted_gamma)
+    V = normal_f16(rng(w.name, "V", layer), shape, w.key_std)
+    return K.astype(np.float16), V
+
+
+def skewed_partial_weight(w: Workload, layer: int) -> np.ndarray:
+    """W~_Q^partial [D, H*k] fp16 drawn directly in the skewed basis (same law as W A)."""
+    return normal_f16(rng(w.name, "Wqp", layer), (w.hidden, w.heads * w.k), w.w_std)
+
+
+def skewed_columns(w: Workload, layer: int) -> np.ndarray:
+    """A column set per head [H, k] int32, ascending (used with directly drawn skewed data)."""
+    g = rng(w.name, "cols", layer)
+    return np.stack([np.sort(g.permutation(w.head_dim)[: w.k]) for _ in range(w.heads)]).astype(np.int32)
+
+
+def token_inputs(w: Workload, layer: int, step: int = 0):
+    """The current token at one (layer, step): real query q~, key k~_new, value v_new [B, H, d] fp16."""
+    shape = (w.batch, w.heads, w.head_dim)
+    q = normal_f16(rng(w.name, "q", layer, step), shape, w.key_std)
+    kn = normal_f16(rng(w.name, "knew", layer, step), shape, w.key_std)
+    vn = normal_f16(rng(w.name, "vnew", layer, step), shape, w.key_std)
+    return q, kn, vn
+
+
+def valid_lengths(w: Workload, step: int = 0, ragged: bool = False) -> np.ndarray:
+    """Resident tokens per sequence at a decode step: prompt + step (capped at the pool).
+
+    ``ragged`` gives each sequence a different length (for edge-case tests).
+    """
+    L = np.full(w.batch, min(w.prompt + step, w.pool_cap), dtype=np.int32)
+    if ragged:
+        g = rng(w.name, "ragged", step)
+        L = np.minimum(L, g.integers(1, w.pool_cap + 1, size=w.batch)).astype(np.int32)
+    return L
+
+
+def scaled(w: Workload, **over) -> Workload:
+    """A smaller copy of a workload (same distributions) for fast tests."""
+    d = dict(w.__dict__)
+    d.update(over)
+    return Workload(**d)

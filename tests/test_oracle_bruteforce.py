@@ -1,0 +1,208 @@
+"""P4 and P13: the oracle against scalar-loop brute force on tiny inputs, and the pool rules.
+
+The brute-force versions below are written as explicit Python loops over single numbers,
+independently of the vectorised oracle, on inputs small enough (L <= 16, d <= 8) to check
+every entry.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import infinigen as ora
+
+
+def _bf_scores(qp, Kpart, L, scale):
+    B, H, k = qp.shape
+    out = {}
+    for b in range(B):
+        for h in range(H):
+            for t in range(L[b]):
+                acc = 0.0
+                for c in range(k):
+                    acc += float(qp[b, h, c]) * float(Kpart[b, h, c, t])
+                out[(b, h, t)] = float(np.float32(scale)) * acc
+    return out
+
+
+def _bf_threshold(vals, alpha):
+    m = max(vals)
+    return [t for t, v in enumerate(vals) if m - v < alpha]
+
+
+def _bf_topn(vals, n):
+    pairs = sorted([(-v, t) for t, v in enumerate(vals)])
+    return sorted(t for _, t in pairs[:n])
+
+
+def _bf_attend(q, rows_k, rows_v, scale):
+    z = []
+    for r in rows_k:
+        acc = 0.0
+        for c in range(len(q)):
+            acc += float(q[c]) * float(r[c])
+        z.append(float(np.float32(scale)) * acc)
+    m = max(z)
+    e = [math.exp(v - m) for v in z]
+    tot = sum(e)
+    out = [0.0] * len(rows_v[0])
+    for w, r in zip(e, rows_v):
+        for c in range(len(r)):
+            out[c] += (w / tot) * float(r[c])
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("policy,cap", [(ora.SEL_THRESHOLD, 1.0), (ora.SEL_THRESHOLD, 0.25),
+                                        (ora.SEL_HEAD_AVG, 1.0), (ora.SEL_HEAD_AVG, 0.3)])
+def test_p4_layer_step_brute_force(seed, policy, cap):
+    g = np.random.default_rng(seed)
+    B, H, d, D, k = 2, 3, 8, 12, 3
+    Lcap = 16
+    L = np.array([16, int(g.integers(1, 16))])
+    x = (g.standard_normal((B, D))).astype(np.float16)
+    Wqp = (g.standard_normal((D, H * k)) * 0.5).astype(np.float16)
+    Kpool = (g.standard_normal((B, H, Lcap, d))).astype(np.float16)
+    Vpool = (g.standard_normal((B, H, Lcap, d))).astype(np.float16)
+    cols = np.array([np.sort(g.permutation(d)[:k]) for _ in range(H)])
+    Kpart = ora.partial_key_cache(Kpool, cols)
+    q = (g.standard_normal((B, H, d))).astype(np.float16)
+    kn = (g.standard_normal((B, H, d))).astype(np.float16)
+    vn = (g.standard_normal((B, H, d))).astype(np.float16)
+    scale, alpha = 0.6, 1.3
+    r = ora.decode_layer_step(x, Wqp, Kpart, L, q, Kpool, Vpool, H=H, k=k, scale=scale, alpha=alpha,
+                              policy=policy, cap_frac=cap, k_new=kn, v_new=vn)
+    # partial query, scalar loops
+    qp = np.zeros((B, H, k))
+    for b in range(B):
+        for j in range(H * k):
+            acc = 0.0
+            for i in range(D):
+                acc += float(x[b, i]) * float(Wqp[i, j])
+            qp[b, j // k, j % k] = acc
+    assert np.allclose(r["q_part"], qp, rtol=1e-12, atol=1e-12)
+    # partial key rows must be the chosen columns of the full keys
+    for b in range(B):
+        for h in range(H):
+            for c in range(k):
+                for t in range(Lcap):
+                    assert Kpart[b, h, c, t] == Kpool[b, h, t, cols[h, c]]
+    bs = _bf_scores(qp, Kpart, L, scale)
+    for (b, h, t), v in bs.items():
+        assert abs(r["scores"][b, h, t] - v) <= 1e-12 * max(1.0, abs(v))
+    for b in range(B):
+        assert np.all(np.isneginf(r["scores"][b, :, L[b]:]))
+    # selection
+    for b in range(B):
+        capn = int(math.floor(float(np.float32(cap)) * L[b] + 0.5)) if cap < 1 else int(L[b])
+        sel = {}
+        for h in range(H):
+            vals = [bs[(b, h, t)] for t in range(L[b])]
+            s = _bf_threshold(vals, alpha)
+            if policy == ora.SEL_THRESHOLD and len(s) > capn:
+                s = _bf_topn(vals, capn)
+            sel[h] = s
+        if policy == ora.SEL_HEAD_AVG:
+            mean = sum(len(v) for v in sel.values()) / H
+            cbar = min(max(1, int(math.floor(mean + 0.5))), capn)
+            for h in range(H):
+                sel[h] = _bf_topn([bs[(b, h, t)] for t in range(L[b])], cbar)
+        for h in range(H):
+            assert list(r["idx"][b][h]) == sel[h]
+            assert r["cnt"][b, h] == len(sel[h])
+        for t in range(Lcap):
+            assert r["used"][b, t] == int(any(t in sel[h] for h in range(H)))
+        # attention over the selected rows plus the current token
+        for h in range(H):
+            rk = [Kpool[b, h, t] for t in sel[h]] + [kn[b, h]]
+            rv = [Vpool[b, h, t] for t in sel[h]] + [vn[b, h]]
+            o = _bf_attend(q[b, h], rk, rv, scale)
+            assert np.allclose(r["out"][b, h], o, rtol=0, atol=1e-12)
+
+
+def test_select_ignores_nan_and_handles_empty():
+    s = np.array([[[np.nan, 1.0, 0.5, np.nan], [np.nan] * 4]])
+    idx, cnt, used = ora.select(s, [4], 0.75)
+    assert list(idx[0][0]) == [1, 2] and cnt[0, 1] == 0
+    idx, cnt, used = ora.select(np.zeros((1, 2, 8)), [0], 4.0)
+    assert cnt.sum() == 0 and used.sum() == 0
+
+
+def test_gather_copies_rows_exactly():
+    g = np.random.default_rng(3)
+    Kp = g.standard_normal((2, 2, 9, 4)).astype(np.float16)
+    Vp = g.standard_normal((2, 2, 9, 4)).astype(np.float16)
+    idx = [[np.array([0, 8]), np.array([3])], [np.array([]), np.array([1, 2, 5])]]
+    Kg, Vg = ora.gather(Kp, Vp, idx, 9)
+    for b in range(2):
+        for h in range(2):
+            for j, t in enumerate(idx[b][h]):
+                assert Kg[b, h, j].tobytes() == Kp[b, h, int(t)].tobytes()
+                assert Vg[b, h, j].tobytes() == Vp[b, h, int(t)].tobytes()
+
+
+# --- P13: pool rules -------------------------------------------------------------------------
+def test_p13_pool_no_eviction_when_capacity_suffices():
+    p = ora.CounterPool(10)
+    assert [p.evict(None) for _ in range(10)] == list(range(10))
+
+
+def test_p13_pool_zero_counters_is_fifo():
+    p = ora.CounterPool(4)
+    slots = [p.evict(None) for _ in range(11)]
+    assert slots == [0, 1, 2, 3, 0, 1, 2, 3, 0, 1, 2]
+
+
+def test_p13_pool_evicts_smallest_counter_then_oldest():
+    p = ora.CounterPool(4)
+    for _ in range(4):
+        p.insert()
+    # slot 2 used twice, slot 0 once, slots 1 and 3 never
+    p.update([1, 0, 1, 0])
+    p.update([0, 0, 1, 0])
+    assert p.insert() == 1          # counters 1,0,2,0 -> smallest 0, oldest of {1, 3} is 1
+    assert p.insert() == 3          # slot 1 is new (counter 0, newest) -> slot 3 is older
+    assert p.counter.tolist() == [1, 0, 2, 0]
+
+
+def test_p13_pool_halving_keeps_order():
+    p = ora.CounterPool(3)
+    for _ in range(3):
+        p.insert()
+    for i in range(255):
+        p.update([1, 1 if i % 2 == 0 else 0, 0])
+    # slot 0 reached 255 and everything was halved once
+    assert p.counter.tolist() == [127, 64, 0]
+    assert p.counter[0] > p.counter[1] > p.counter[2]
+    assert p.insert() == 2
+
+
+def test_p13_pool_brute_force_against_slot_history():
+    g = np.random.default_rng(9)
+    cap, steps = 6, 60
+    p = ora.CounterPool(cap)
+    owner = {}
+    cnt = [0] * cap
+    seqs = [0] * cap
+    filled = 0
+    nxt = 0
+    for t in range(steps):
+        used = (g.random(cap) < 0.3).astype(np.uint8)
+        got = p.evict(used if t else None)
+        # brute force of the same rules
+        if t:
+            for s in range(filled):
+                if used[s]:
+                    cnt[s] = min(255, cnt[s] + 1)
+            if filled and max(cnt[:filled]) >= 255:
+                cnt = [c >> 1 for c in cnt]
+        if filled < cap:
+            want = filled
+            filled += 1
+        else:
+            want = min(range(cap), key=lambda s: (cnt[s], seqs[s], s))
+        cnt[want] = 0
+        seqs[want] = nxt
+        nxt += 1
+        owner[want] = t
+        assert got == want

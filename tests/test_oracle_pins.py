@@ -1,0 +1,299 @@
+"""Pins of the CPU oracle against what the InfiniGen pages and plain mathematics fix.
+
+None of these tests needs a GPU.  Each one is chosen so that a plausible slip in the oracle
+(a dropped term, a wrong sign or index, a transposed operand) makes it fail.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.special
+
+from oracle import infinigen as ora
+from speculative_kv_cache_gb300 import synth
+
+
+def _rand(seed, shape, std=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * std
+
+
+# --- P1: the skew is an orthogonal rotation, so rotated dot products are unchanged -------
+@pytest.mark.parametrize("theta", [0.0, 10000.0])
+def test_p1_skew_is_orthogonal_and_preserves_dot_products(theta):
+    H, d, D, Ns = 3, 16, 48, 64
+    Xs = _rand(1, (Ns, D)).astype(np.float16)
+    Wq = _rand(2, (D, H * d), 0.02).astype(np.float16)
+    Wk = _rand(3, (D, H * d), 0.02).astype(np.float16)
+    A, _, _, _, _ = ora.skew(Xs, Wq, Wk, H, d, rope_theta=theta)
+    for h in range(H):
+        assert np.abs(A[h].T @ A[h] - np.eye(d)).max() < 1e-12
+    # full-width rotated q.k equals unrotated q.k (float64, before any fp16 rounding)
+    x = _rand(4, (5, D))
+    y = _rand(5, (7, D))
+    q = (x @ Wq.astype(np.float64)).reshape(5, H, d)
+    kk = (y @ Wk.astype(np.float64)).reshape(7, H, d)
+    if theta:
+        q = ora.rope(q, np.arange(5)[:, None] + 100, theta)
+        kk = ora.rope(kk, np.arange(7)[:, None], theta)
+    for h in range(H):
+        ref = q[:, h] @ kk[:, h].T
+        rot = (q[:, h] @ A[h]) @ (kk[:, h] @ A[h]).T
+        assert np.abs(rot - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+# --- P2: Q A = U Sigma: columns orthogonal, norms are the singular values, descending -----
+def test_p2_skewed_sample_queries_are_u_sigma():
+    H, d, D, Ns = 2, 12, 40, 50
+    Xs = _rand(11, (Ns, D)).astype(np.float16)
+    Wq = _rand(12, (D, H * d), 0.02).astype(np.float16)
+    A, sig, _, _, _ = ora.skew(Xs, Wq, Wq, H, d)
+    Q = Xs.astype(np.float64) @ Wq.astype(np.float64)
+    for h in range(H):
+        Qh = Q[:, h * d:(h + 1) * d]
+        QA = Qh @ A[h]
+        G = QA.T @ QA
+        # singular values from an independent route: eigenvalues of the Gram matrix
+        ev = np.sort(scipy.linalg.eigvalsh(Qh.T @ Qh))[::-1]
+        assert np.allclose(np.sqrt(np.diag(G)), np.sqrt(np.maximum(ev, 0)), rtol=1e-10, atol=1e-12)
+        assert np.all(np.diff(np.diag(G)) <= 1e-9)
+        off = G - np.diag(np.diag(G))
+        assert np.abs(off).max() < 1e-9 * np.abs(G).max()
+        assert np.allclose(sig[h], np.sqrt(np.maximum(ev, 0)), rtol=1e-10)
+
+
+def test_p2_sign_canonicalisation():
+    A = np.array([[0.6, -0.8], [-0.8, -0.6]])
+    C = ora.canonical_signs(A)
+    assert np.array_equal(C, np.array([[-0.6, 0.8], [0.8, 0.6]]))
+    # ties go to the lowest row
+    T = ora.canonical_signs(np.array([[-0.5, 0.5], [0.5, 0.5]]))
+    assert T[0, 0] == 0.5 and T[1, 0] == -0.5
+
+
+# --- P3: ratio 1 and alpha = inf reproduce dense attention ---------------------------------
+@pytest.mark.parametrize("with_new", [False, True])
+def test_p3_full_ratio_infinite_alpha_is_dense_attention(with_new):
+    B, H, d, D, L, Ns = 2, 3, 8, 24, 20, 40
+    Xs = _rand(21, (Ns, D)).astype(np.float16)
+    Wq = _rand(22, (D, H * d), 0.05).astype(np.float16)
+    A, _, Wq_s, _, _ = ora.skew(Xs, Wq, Wq, H, d)
+    k = ora.partial_columns(1.0, d)
+    assert k == d
+    K = _rand(23, (B, H, L, d))
+    V = _rand(24, (B, H, L, d))
+    q = _rand(25, (B, H, d))
+    kn = _rand(26, (B, H, d))
+    vn = _rand(27, (B, H, d))
+    Kt = np.einsum("bhtc,hcj->bhtj", K, A)
+    qt = np.einsum("bhc,hcj->bhj", q, A)
+    knt = np.einsum("bhc,hcj->bhj", kn, A)
+    cols = ora.choose_columns(Wq_s, None, H, d, k)
+    assert np.array_equal(cols, np.tile(np.arange(d), (H, 1)))
+    Kpart = ora.partial_key_cache(Kt, cols)
+    Wqp = ora.partial_weight(Wq_s, cols, H, d)
+    x = _rand(28, (B, D)).astype(np.float16)
+    scale = 1 / math.sqrt(d)
+    r = ora.decode_layer_step(x, Wqp, Kpart, np.full(B, L), qt, Kt, V, H=H, k=k, scale=scale,
+                              alpha=np.inf, k_new=knt if with_new else None,
+                              v_new=vn if with_new else None)
+    assert np.all(r["cnt"] == L)
+    for b in range(B):
+        for h in range(H):
+            Kd, Vd = K[b, h], V[b, h]
+            if with_new:
+                Kd = np.vstack([Kd, kn[b, h]])
+                Vd = np.vstack([Vd, vn[b, h]])
+            w = scipy.special.softmax(np.float32(scale) * (Kd @ q[b, h]))
+            assert np.allclose(r["out"][b, h], w @ Vd, rtol=0, atol=1e-12)
+
+
+# --- P5: the page's worked number e^-5 ~ 0.0067 ~ 1/148.4 ----------------------------------
+def test_p5_alpha_five_weight_ratio(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "softmax_alpha5.json")))
+    d = 4
+    scale = 1.0  # the gap is stated in logit units
+    q = np.array([[[1.0, 0.0, 0.0, 0.0]]])
+    Kg = np.zeros((1, 1, 2, d))
+    Kg[0, 0, 0, 0] = 10.0
+    Kg[0, 0, 1, 0] = 10.0 - g["gap"]
+    Vg = np.zeros((1, 1, 2, d))
+    Vg[0, 0, 0, 1] = 1.0
+    Vg[0, 0, 1, 2] = 1.0
+    o = ora.attend(q, Kg, Vg, np.array([[2]]), scale)[0, 0]
+    ratio = o[2] / o[1]
+    assert round(ratio, g["weight_ratio_printed_digits"]) == g["weight_ratio"]
+    assert round(1 / ratio, g["inverse_printed_digits"]) == g["inverse"]
+
+
+# --- P6: partial weight / partial key cache fractions ---------------------------------------
+def test_p6_memory_fractions(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "memory_fraction.json")))
+    for s in g["shapes"]:
+        k = ora.partial_columns(g["ratio"], s["head_dim"])
+        kv_frac = 100.0 * k / (2 * s["head_dim"])          # k of 2d numbers per token and head
+        w_frac = 100.0 * s["heads"] * k * s["hidden"] / (g["params_per_block_over_hidden_sq"] * s["hidden"] ** 2)
+        assert abs(kv_frac - g["partial_key_cache_pct"]) <= g["printed_tolerance_pct"]
+        assert abs(w_frac - g["partial_weight_pct"]) <= g["printed_tolerance_pct"]
+    assert ora.partial_columns(0.3, 128) == 38
+    assert ora.partial_columns(0.25, 64) == 16
+
+
+# --- P7: cap rounding reproduces the page's 102 and 410 ------------------------------------
+def test_p7_cap_rounding(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "transfer_cap.json")))
+    for n, want in g["cases"]:
+        assert ora.cap_count(g["cap_frac"], n) == want
+    assert ora.cap_count(1.0, 77) == 77
+
+
+# --- P8: alpha -> 0+ keeps only the maximum (and exact ties) -------------------------------
+def test_p8_tiny_alpha_selects_argmax_and_ties():
+    s = np.array([[[0.5, 2.0, -1.0, 2.0, 1.999]]])
+    idx, cnt, used = ora.select(s, [5], 1e-30)
+    assert list(idx[0][0]) == [1, 3] and cnt[0, 0] == 2
+    assert list(used[0]) == [0, 1, 0, 1, 0]
+
+
+# --- P9: flipping a column sign of A changes nothing downstream ----------------------------
+def test_p9_sign_flip_invariance():
+    B, H, d, D, L, Ns = 2, 2, 16, 32, 30, 48
+    Xs = _rand(31, (Ns, D)).astype(np.float16)
+    Wq = _rand(32, (D, H * d), 0.05).astype(np.float16)
+    A, _, _, _, _ = ora.skew(Xs, Wq, Wq, H, d)
+    K = _rand(33, (B, H, L, d))
+    V = _rand(34, (B, H, L, d))
+    q = _rand(35, (B, H, d))
+    x = _rand(36, (B, D))
+    k = ora.partial_columns(0.3, d)
+    res = []
+    for flip in [None, 3]:
+        Af = A.copy()
+        if flip is not None:
+            Af[:, :, flip] *= -1
+        Wq_s = np.concatenate([Wq.astype(np.float64)[:, h * d:(h + 1) * d] @ Af[h] for h in range(H)], 1)
+        Kt = np.einsum("bhtc,hcj->bhtj", K, Af)
+        qt = np.einsum("bhc,hcj->bhj", q, Af)
+        cols = ora.choose_columns(Wq_s, np.transpose(Kt, (0, 2, 1, 3)), H, d, k)
+        Kpart = ora.partial_key_cache(Kt, cols)
+        r = ora.decode_layer_step(x, ora.partial_weight(Wq_s, cols, H, d), Kpart, np.full(B, L), qt, Kt, V,
+                                  H=H, k=k, scale=1 / math.sqrt(d), alpha=2.0)
+        res.append((cols, r))
+    (c0, r0), (c1, r1) = res
+    assert np.array_equal(c0, c1)
+    assert np.allclose(r0["scores"], r1["scores"], atol=1e-12)
+    assert all(np.array_equal(r0["idx"][b][h], r1["idx"][b][h]) for b in range(B) for h in range(H))
+    assert np.allclose(r0["out"], r1["out"], atol=1e-12)
+
+
+# --- P10: pool slot order is free ----------------------------------------------------------
+def test_p10_slot_permutation():
+    B, H, d, k, L = 2, 3, 8, 3, 25
+    Kt = _rand(41, (B, H, L, d))
+    V = _rand(42, (B, H, L, d))
+    q = _rand(43, (B, H, d))
+    qp = _rand(44, (B, H, k))
+    cols = np.array([[0, 2, 5]] * H)
+    perm = np.random.default_rng(45).permutation(L)
+    outs, sets = [], []
+    for P in [np.arange(L), perm]:
+        Kp, Vp = Kt[:, :, P], V[:, :, P]
+        Kpart = ora.partial_key_cache(Kp, cols)
+        s = ora.speculate(qp, Kpart, np.full(B, L), 0.7)
+        idx, cnt, _ = ora.select(s, np.full(B, L), 1.5)
+        Kg, Vg = ora.gather(Kp, Vp, idx, L)
+        outs.append(ora.attend(q, Kg, Vg, cnt, 0.35))
+        sets.append([[set(P[np.asarray(idx[b][h])].tolist()) for h in range(H)] for b in range(B)])
+    assert sets[0] == sets[1]
+    assert np.allclose(outs[0], outs[1], atol=1e-12)
+
+
+# --- P11: the selected count never drops as alpha grows ------------------------------------
+def test_p11_count_monotone_in_alpha():
+    s = _rand(51, (3, 4, 200))
+    prev = None
+    for a in [0.1, 0.5, 1, 2, 3, 4, 6, 9, np.inf]:
+        _, cnt, _ = ora.select(s, [200, 150, 17], a)
+        if prev is not None:
+            assert np.all(cnt >= prev)
+        prev = cnt
+    assert np.array_equal(prev, np.array([[200] * 4, [150] * 4, [17] * 4]))
+
+
+# --- P12: KV-cache bytes of the OPT-30B-shaped workload ------------------------------------
+def test_p12_kv_bytes():
+    w = synth.WORKLOADS["opt-30b"]
+    b = ora.kv_bytes(w.layers, w.batch, w.context, w.hidden)
+    assert b == 48 * 16 * 2048 * 7168 * 4
+    assert abs(b / 1e9 - 45.1) < 0.05
+
+
+# --- RoPE: reduces to complex rotation for d = 2; relative-position property -----------------
+def test_rope_two_dims_is_complex_rotation():
+    x = _rand(61, (7, 2))
+    p = np.arange(7) * 3 + 1
+    z = (x[:, 0] + 1j * x[:, 1]) * np.exp(1j * p)      # theta^0 = 1 for the only pair
+    r = ora.rope(x, p, 10000.0)
+    assert np.allclose(r[:, 0], z.real, atol=1e-13) and np.allclose(r[:, 1], z.imag, atol=1e-13)
+
+
+def test_rope_relative_position_and_norm():
+    d = 16
+    q = _rand(62, d)
+    kk = _rand(63, d)
+    a = ora.rope(q, 40, 10000.0) @ ora.rope(kk, 13, 10000.0)
+    b = ora.rope(q, 27, 10000.0) @ kk
+    assert abs(a - b) < 1e-12
+    assert abs(np.linalg.norm(ora.rope(q, 99, 500.0)) - np.linalg.norm(q)) < 1e-12
+    assert np.allclose(ora.rope(q, 0, 10000.0), q)
+    # pair j is (j, j + d/2), not (2j, 2j + 1): only dims 0 and 8 mix for the fastest pair
+    e0 = np.zeros(d)
+    e0[0] = 1.0
+    r = ora.rope(e0, 1, 10000.0)
+    assert np.count_nonzero(np.abs(r) > 1e-15) == 2 and abs(r[8] - math.sin(1.0)) < 1e-15
+
+
+def test_partial_query_rope_identity_skew_matches_rope_of_projection():
+    B, H, d, D = 2, 2, 8, 16
+    x = _rand(64, (B, D))
+    Wq = _rand(65, (D, H * d), 0.1)
+    A = np.stack([np.eye(d)] * H)
+    cols = np.tile(np.arange(d), (H, 1))
+    pos = np.array([5, 900])
+    got = ora.partial_query_rope(x, Wq, A, cols, pos, 10000.0)
+    q = (x @ Wq).reshape(B, H, d)
+    for b in range(B):
+        for h in range(H):
+            want = ora.rope(q[b, h], pos[b], 10000.0)
+            assert np.allclose(got[b, h], want, atol=1e-13)
+
+
+# --- column choice: the combined score keeps both kinds of outlier column -------------------
+def test_column_choice_combines_query_and_key_outliers(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "column_choice.json")))
+    W = np.array(g["Wq_skew"])
+    K = np.array(g["K_skew"])[:, None, :]
+    assert list(ora.choose_columns(W, K, 1, g["head_dim"], g["k"])[0]) == g["expected_cols"]
+    assert list(ora.choose_columns(W, None, 1, g["head_dim"], g["k"])[0]) == g["query_only_cols"]
+    assert list(ora.choose_columns(np.zeros_like(W), K, 1, g["head_dim"], g["k"])[0]) == g["key_only_cols"]
+
+
+# --- head averaging rounds half up, minimum one token ---------------------------------------
+def test_head_avg_count_rounding():
+    # counts per head 3, 5, 4, 6 -> mean 4.5 -> 5 tokens per head
+    s = np.full((1, 4, 10), -100.0)
+    for h, c in enumerate([3, 5, 4, 6]):
+        s[0, h, :c] = 0.0
+    s[0, :, 9] = -50.0
+    idx, cnt, _ = ora.select(s, [10], 1.0, ora.SEL_HEAD_AVG)
+    assert list(cnt[0]) == [5, 5, 5, 5]
+    # head 0 has three tied at 0, then takes the best of the rest: -50 at t = 9, then t = 3
+    assert list(idx[0][0]) == [0, 1, 2, 3, 9]
+    # mean 0.25 rounds to 0 but the minimum is one
+    s2 = np.zeros((1, 4, 6))
+    s2[0, 0, 2] = 10.0
+    s2[0, 1:, :] = np.nan
+    idx2, cnt2, _ = ora.select(s2, [6], 1.0, ora.SEL_HEAD_AVG)
+    assert list(cnt2[0]) == [1, 0, 0, 0] and list(idx2[0][0]) == [2]
