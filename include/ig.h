@@ -1,0 +1,241 @@
+/*
+ * ig.h — C ABI of the GB300 (sm_103a) InfiniGen decode hot path.
+ *
+ * InfiniGen ("InfiniGen: Efficient Generative Inference of Large Language Models with
+ * Dynamic KV Cache Management", OSDI 2024) speculates, one layer ahead, which keys and
+ * values the next attention layer needs, and fetches only those from a KV pool in host
+ * memory.  Citations below name the paper-graph summary page of that paper and the part of
+ * its section 3.4 ("Detailed, Sentence-Based Technical Breakdown") that defines each call.
+ *
+ * Conventions (every function):
+ *   - Returns ig_status: IG_OK (0) or a negative error.  ig_last_error() gives a message
+ *     for the calling thread.  Nothing aborts the process or traps the GPU.
+ *   - "dev" pointers are device memory (or, where stated, host memory the GPU can map);
+ *     "host" pointers are ordinary host memory.  The caller owns every buffer it passes.
+ *     The library owns only the pinned KV pool (ig_pool_create / ig_pool_destroy).
+ *   - Device calls are asynchronous on the caller's cudaStream_t, passed as void* (NULL =
+ *     legacy default stream).  Argument and launch errors are returned at once; a guard
+ *     that trips inside a kernel (an index out of range, a bounded wait that ran out) is
+ *     recorded in a device error word that ig_check() reads and clears.
+ *   - fp16 tensors are passed as uint16_t bit patterns; fp32 as float; indices as int32_t.
+ *   - All multi-dimensional arrays are dense, row-major, in the order written ([B][H][k]
+ *     means the last index is contiguous).
+ *   - No CPU fallback: with no usable GPU, device calls return IG_ERR_CUDA.
+ */
+#ifndef IG_H_
+#define IG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int ig_status;
+
+#define IG_OK 0
+#define IG_ERR_INVALID (-1)   /* bad argument: sizes, alignment, null pointer, alpha <= 0 ... */
+#define IG_ERR_CUDA (-2)      /* a CUDA runtime call or a launch failed                       */
+#define IG_ERR_OOM (-3)       /* pinned host allocation failed                                */
+#define IG_ERR_NUMERIC (-4)   /* the offline SVD did not converge                              */
+#define IG_ERR_TIMEOUT (-5)   /* a bounded in-kernel wait ran out (reported by ig_check)       */
+#define IG_ERR_CAPACITY (-6)  /* workspace or pool too small for the request                   */
+
+/* Selection policies for ig_select. */
+#define IG_SEL_THRESHOLD 0    /* each head keeps {t : s_t > max(s) - alpha}                   */
+#define IG_SEL_HEAD_AVG 1     /* each head keeps its top-cbar, cbar = mean count over heads    */
+
+/* Device error-word bits (ig_check maps them to a status). */
+#define IG_DEVERR_INDEX 1     /* an index or count was out of range; the access was skipped  */
+#define IG_DEVERR_TIMEOUT 2   /* a bounded wait on a copy ran out                              */
+
+/* Last error message of the calling thread ("" if none). */
+const char* ig_last_error(void);
+
+/* ABI version (major * 100 + minor). */
+int ig_version(void);
+
+/* Waits for `stream`, then reads and clears the device error word of the current device.
+ * Returns IG_OK, IG_ERR_INVALID (an index guard tripped), IG_ERR_TIMEOUT, or IG_ERR_CUDA. */
+ig_status ig_check(void* stream);
+
+/* ------------------------------------------------------------------------------------
+ * Offline skew and partial-column choice.
+ * Section 3.4, "Skewed Partial Weights" (Q = U S V^T, A = V, W~_Q = W_Q A, W~_K = W_K A) and
+ * "Prefill Stage", Step 2 (column score = column sums of |W~_Q| plus column sums of |K~|,
+ * top-k).  Per head h: Q_h = X_s W_Q,h (rotated by RoPE at positions 0..Ns-1 when
+ * rope_theta > 0), A_h = right singular vectors of Q_h in descending singular value
+ * (one-sided Jacobi SVD in float64), each column's largest-magnitude entry made positive.
+ * k = floor(ratio * d + 0.5).
+ *
+ *   Xs      host fp16 [Ns][D]            sample attention inputs
+ *   Wq, Wk  host fp16 [D][H*d]           unskewed query / key weights (head h = columns h*d..)
+ *   Kp      host fp16 [Nk][H][d] or NULL prompt keys in the unskewed basis (post-RoPE for
+ *                                        RoPE models); they join the column score
+ *   A       host fp32 [H][d][d]   out    skew matrices
+ *   Wq_skew host fp16 [D][H*d]    out    W_Q A (rounded once to nearest even); may be NULL
+ *   Wk_skew host fp16 [D][H*d]    out    W_K A; may be NULL
+ *   Kp_skew host fp16 [Nk][H][d]  out    Kp A; may be NULL (ignored when Kp is NULL)
+ *   cols    host int32 [H][k]     out    chosen columns per head, ascending
+ *   k_out   host int              out    k
+ * Host-only and synchronous; uses up to `threads` host threads (0 = all cores).
+ * Errors: IG_ERR_INVALID (d odd with RoPE, ratio outside (0,1], null required pointer),
+ *         IG_ERR_NUMERIC (Jacobi sweeps did not converge). */
+ig_status ig_skew_weights(int D, int H, int d, float ratio, float rope_theta,
+                          const uint16_t* Xs, int Ns, const uint16_t* Wq, const uint16_t* Wk,
+                          const uint16_t* Kp, int Nk, float* A, uint16_t* Wq_skew,
+                          uint16_t* Wk_skew, uint16_t* Kp_skew, int32_t* cols, int* k_out,
+                          int threads);
+
+/* ------------------------------------------------------------------------------------
+ * Speculation: partial query projection and speculated scores for layer i, from layer
+ * i-1's attention input.  Section 3.4, "Decoding Stage", Step 1 (q~p = x_a^(i-1) W~_Q^p,(i))
+ * and Step 2 (SpecScore = q~p (K~p)^T over the N+t resident tokens).
+ *
+ *   x        dev fp16 [B][D]          attention input of layer i-1
+ *   Wq_part  dev fp16 [D][H*k]        partial query weight of layer i, head-contiguous
+ *   Kpart    dev fp16 [B][H][k][Lcap] partial key cache of layer i, token index contiguous
+ *                                     (16-byte aligned; Lcap a multiple of 8)
+ *   L_valid  dev int32 [B]            resident slots per sequence (0 <= L_valid <= Lcap)
+ *   scores   dev fp32 [B][H][Lcap] out s[b][h][t] = score_scale * sum_c q~p[c] K~p[c][t]
+ *                                     for t < L_valid[b]; -inf for L_valid[b] <= t < Lcap
+ *   q_part   dev fp32 [B][H][k] out   the partial query (unscaled), or NULL
+ *   workspace dev, >= ig_speculate_workspace_bytes(B, D, H, k) bytes, 256-byte aligned
+ * Partial query: fp16 x fp16 products accumulated in fp32; scores in fp32. */
+size_t ig_speculate_workspace_bytes(int B, int D, int H, int k);
+ig_status ig_speculate(void* stream, int B, int D, int H, int k, int Lcap,
+                       const uint16_t* x, const uint16_t* Wq_part, const uint16_t* Kpart,
+                       const int32_t* L_valid, float score_scale, float* scores,
+                       float* q_part, void* workspace, size_t workspace_bytes);
+
+/* RoPE models (Llama-2): the skew has to follow the rotary embedding, so the partial query
+ * is q~p_h = RoPE_p(x W_Q,h) A_h[:, S_h] (the full per-head query, rotated at the current
+ * position, then projected on the chosen skewed columns).
+ *   Wq       dev fp16 [D][H*d]   unskewed query weight of layer i
+ *   A_cols   dev fp32 [H][d][k]  A_h[:, S_h]
+ *   positions dev int32 [B]      position of the current token of each sequence
+ * Other arguments as ig_speculate; workspace >= ig_speculate_rope_workspace_bytes(). */
+size_t ig_speculate_rope_workspace_bytes(int B, int D, int H, int d, int k);
+ig_status ig_speculate_rope(void* stream, int B, int D, int H, int d, int k, int Lcap,
+                            const uint16_t* x, const uint16_t* Wq, const float* A_cols,
+                            const int32_t* positions, float rope_theta,
+                            const uint16_t* Kpart, const int32_t* L_valid, float score_scale,
+                            float* scores, float* q_part, void* workspace,
+                            size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------------------
+ * Selection.  Section 3.4, "Decoding Stage", Step 3 ({t : s_t > max(s) - alpha}, evaluated
+ * as max(s) - s_t < alpha in fp32 so the maximum is always kept), Step 4 (multi-head
+ * averaging: cbar = max(1, round-half-up(mean_h count_h)), each head then keeps its cbar
+ * best) and Step 5 (a head keeps at most round-half-up(cap_frac * L_valid) tokens, the best
+ * by score then lower index; cap_frac >= 1 means no cap).  NaN scores are never chosen.
+ *
+ *   scores   dev fp32 [B][H][Lcap]
+ *   L_valid  dev int32 [B]
+ *   alpha    > 0 (may be +inf)
+ *   idx      dev int32 [B][H][Lcap] out  chosen slots, ascending, in idx[b][h][0..cnt)
+ *   cnt      dev int32 [B][H] out
+ *   used     dev uint8 [B][Lcap] out     1 where any head of b chose slot t; may be NULL
+ *   workspace dev, >= ig_select_workspace_bytes(B, H) bytes (HEAD_AVG only; else may be NULL) */
+size_t ig_select_workspace_bytes(int B, int H);
+ig_status ig_select(void* stream, int B, int H, int Lcap, const float* scores,
+                    const int32_t* L_valid, float alpha, int policy, float cap_frac,
+                    int32_t* idx, int32_t* cnt, uint8_t* used, void* workspace,
+                    size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------------------
+ * KV pool in pinned, mapped host memory: one pool per layer and sequence, `cap` slots, each
+ * holding the full key and value row of every head (section 3.4, "KV Cache Pool Management
+ * Under Memory Pressure").  Keys and values are in the skewed basis.  Layout per layer:
+ * K[B][H][cap][d] and V[B][H][cap][d] fp16, 16-byte aligned rows.  Each slot has an 8-bit
+ * access counter used by ig_pool_evict. */
+typedef struct ig_pool ig_pool;
+
+ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out);
+ig_status ig_pool_destroy(ig_pool* pool);
+
+/* Host pointers (also valid on the device) to one layer's K and V arrays. */
+ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V);
+
+/* Copies one layer's K and V ([B][H][cap][d] fp16 each, from device or host memory) into
+ * the pool, asynchronously on `stream`. */
+ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const uint16_t* K,
+                        const uint16_t* V);
+
+/* Host-side counter-based pool manager for one (layer, sequence), run once per decode step.
+ * Section 3.4, pool management (counter policy of Table 2): every slot that any head chose
+ * this step (used[slot] != 0) gains 1, saturating at 255; when a counter reaches 255 all
+ * counters of that pool are halved.  Then the new token gets a slot: the next free slot
+ * while the pool is not full, otherwise the victim with the smallest counter (then the
+ * oldest insertion, then the lowest slot).  The new slot's counter starts at 0.
+ *   used      host uint8 [cap] or NULL (no use to record, e.g. during prefill)
+ *   slot_out  host int32: the slot the new token must be written to (ig_append_kv)
+ *   filled_out host int32 or NULL: resident slots after the insertion */
+ig_status ig_pool_evict(ig_pool* pool, int layer, int b, const uint8_t* used,
+                        int32_t* slot_out, int32_t* filled_out);
+
+/* Reads one (layer, sequence)'s counters (host uint8 [cap]). */
+ig_status ig_pool_counters(const ig_pool* pool, int layer, int b, uint8_t* out);
+
+/* ------------------------------------------------------------------------------------
+ * Gather of the chosen full key/value rows from the host pool into HBM.  Section 3.4,
+ * "Decoding Stage", Step 5 (fetch the selected tokens' full keys and values, all d columns,
+ * asynchronously and overlapped with layer i-1's compute).  The kernel reads the mapped
+ * pinned pool directly (16-byte zero-copy loads over the host link); issue it on a side
+ * stream.  max_ctas bounds its grid (0 = library default) so that it leaves SMs to the
+ * compute stream.
+ *   idx, cnt  dev, from ig_select (slots must be < cap)
+ *   Kg, Vg    dev fp16 [B][H][Lcap][d] out  rows j < cnt[b][h] = pool rows idx[b][h][j] */
+ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, int B, int H, int d,
+                       int Lcap, const int32_t* idx, const int32_t* cnt, uint16_t* Kg,
+                       uint16_t* Vg, int max_ctas);
+
+/* ------------------------------------------------------------------------------------
+ * Attention over the gathered rows.  Section 3.4, Inference Controller (softmax(q K^T) V over
+ * the prefetched entries only).  o[b][h] = sum_j w_j V_j, w = softmax(scale * q . K_j) over
+ * rows j < cnt[b][h] plus, when k_new is given, the current token's own key/value.  fp32
+ * online softmax and accumulation.
+ *   q            dev fp16 [B][H][d]        query of layer i (skewed basis)
+ *   Kg, Vg       dev fp16 [B][H][Lcap][d]  (16-byte aligned)
+ *   cnt          dev int32 [B][H]
+ *   k_new, v_new dev fp16 [B][H][d] or NULL
+ *   out          dev fp32 [B][H][d] out
+ *   workspace    dev, >= ig_attend_workspace_bytes(B, H, d, Lcap) bytes, 256-byte aligned
+ * d must be 64 or 128. */
+size_t ig_attend_workspace_bytes(int B, int H, int d, int Lcap);
+ig_status ig_sparse_attend(void* stream, int B, int H, int d, int Lcap, float scale,
+                           const uint16_t* q, const uint16_t* Kg, const uint16_t* Vg,
+                           const int32_t* cnt, const uint16_t* k_new, const uint16_t* v_new,
+                           float* out, void* workspace, size_t workspace_bytes);
+
+/* Layer 0 (speculation starts at layer 1; section 3.4, "Why InfiniGen starts speculation from
+ * Layer 1"): dense attention over all L_valid[b] resident rows of an HBM-resident KV
+ * K, V [B][H][Lcap][d].  Same kernel and arguments as ig_sparse_attend, with the row count
+ * taken per sequence from L_valid [B]. */
+ig_status ig_dense_attend(void* stream, int B, int H, int d, int Lcap, float scale,
+                          const uint16_t* q, const uint16_t* K, const uint16_t* V,
+                          const int32_t* L_valid, const uint16_t* k_new,
+                          const uint16_t* v_new, float* out, void* workspace,
+                          size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------------------
+ * Append of the current token.  Section 3.4, "Partial Key Cache Updates During Decoding":
+ * the new token's full key and value go to the host pool, its k chosen columns to the
+ * partial key cache in HBM, at the slot given by ig_pool_evict.
+ *   slot     dev int32 [B]      slot per sequence (negative: skip that sequence)
+ *   cols     dev int32 [H][k]   chosen columns
+ *   k_new, v_new dev fp16 [B][H][d]
+ *   pool     written at (layer, b, h, slot) when not NULL
+ *   Kpart    dev fp16 [B][H][k][Lcap] or NULL
+ *   Kdense, Vdense dev fp16 [B][H][Lcap][d] or NULL (an HBM-resident KV, as for layer 0) */
+ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B, int H, int d, int k,
+                       int Lcap, const int32_t* slot, const int32_t* cols,
+                       const uint16_t* k_new, const uint16_t* v_new, uint16_t* Kpart,
+                       uint16_t* Kdense, uint16_t* Vdense);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IG_H_ */

@@ -1,0 +1,226 @@
+// KV cache pool in pinned, mapped host memory and its counter-based manager (InfiniGen
+// paper-graph summary, section 3.4, "KV Cache Pool Management Under Memory Pressure", counter
+// policy of Table 2), plus the append of the current token ("Partial Key Cache Updates
+// During Decoding").
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "ig_common.cuh"
+#include "pool_impl.h"
+
+namespace ig {
+namespace {
+
+// Host-side fault injection for tests: IG_FAULT=pool_alloc makes pool creation fail as if
+// the pinned allocation had been refused.
+bool fault_injected(const char* what) {
+  const char* f = getenv("IG_FAULT");
+  return f && strstr(f, what) != nullptr;
+}
+
+// K6: the current token of every (b, h): full key/value row to the pool slot (16-byte
+// zero-copy stores over the host link), the k chosen columns of the key to the partial key
+// cache, and optionally the full row to an HBM-resident KV.
+__global__ void k6_append(uint4* __restrict__ Kp, uint4* __restrict__ Vp, int cap, int H, int d,
+                          int k, int Lcap, const int32_t* __restrict__ slot,
+                          const int32_t* __restrict__ cols, const __half* __restrict__ k_new,
+                          const __half* __restrict__ v_new, __half* __restrict__ Kpart,
+                          uint4* __restrict__ Kd, uint4* __restrict__ Vd, int* err) {
+  const int bh = blockIdx.x, b = bh / H, h = bh % H;
+  const int sl = slot[b];
+  if (sl < 0) return;
+  const int vpr = d / 8;
+  const uint4* kn = reinterpret_cast<const uint4*>(k_new + (size_t)bh * d);
+  const uint4* vn = reinterpret_cast<const uint4*>(v_new + (size_t)bh * d);
+  if (Kp) {
+    if (sl >= cap) {
+      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_INDEX);
+      return;
+    }
+    for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
+      Kp[((size_t)bh * cap + sl) * vpr + v] = kn[v];
+      Vp[((size_t)bh * cap + sl) * vpr + v] = vn[v];
+    }
+  }
+  if (Kpart || Kd) {
+    if (sl >= Lcap) {
+      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_INDEX);
+      return;
+    }
+  }
+  if (Kd) {
+    for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
+      Kd[((size_t)bh * Lcap + sl) * vpr + v] = kn[v];
+      Vd[((size_t)bh * Lcap + sl) * vpr + v] = vn[v];
+    }
+  }
+  if (Kpart) {
+    for (int c = threadIdx.x; c < k; c += blockDim.x) {
+      int col = cols[h * k + c];
+      if (col < 0 || col >= d) {
+        raise_error(err, IG_DEVERR_INDEX);
+        continue;
+      }
+      Kpart[((size_t)bh * k + c) * Lcap + sl] = k_new[(size_t)bh * d + col];
+    }
+  }
+}
+
+}  // namespace
+}  // namespace ig
+
+using namespace ig;
+
+extern "C" ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out) {
+  IG_REQUIRE(out, "null out");
+  *out = nullptr;
+  IG_REQUIRE(layers > 0 && B > 0 && H > 0 && d > 0 && cap > 0, "pool sizes must be positive");
+  IG_REQUIRE(d % 8 == 0, "d must be a multiple of 8 (16-byte rows)");
+  const size_t elems = (size_t)layers * B * H * cap * d;
+  if (fault_injected("pool_alloc")) return fail(IG_ERR_OOM, "injected pinned-allocation failure");
+  ig_pool* p = new (std::nothrow) ig_pool();
+  if (!p) return fail(IG_ERR_OOM, "host allocation of the pool header failed");
+  p->layers = layers;
+  p->B = B;
+  p->H = H;
+  p->d = d;
+  p->cap = cap;
+  const unsigned flags = cudaHostAllocMapped | cudaHostAllocPortable;
+  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&p->K), elems * 2, flags);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&p->V), elems * 2, flags);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (p->K) cudaFreeHost(p->K);
+    delete p;
+    return fail(IG_ERR_OOM, "pinned allocation of 2 x %zu bytes failed: %s", elems * 2,
+                cudaGetErrorString(e));
+  }
+  void* kd = nullptr;
+  void* vd = nullptr;
+  e = cudaHostGetDevicePointer(&kd, p->K, 0);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(&vd, p->V, 0);
+  if (e != cudaSuccess) {
+    cudaFreeHost(p->K);
+    cudaFreeHost(p->V);
+    delete p;
+    return cuda_fail(e, "device pointer of the pinned pool");
+  }
+  p->Kdev = static_cast<uint16_t*>(kd);
+  p->Vdev = static_cast<uint16_t*>(vd);
+  try {
+    p->counter.assign((size_t)layers * B * cap, 0);
+    p->seq.assign((size_t)layers * B * cap, 0);
+    p->filled.assign((size_t)layers * B, 0);
+    p->next_seq.assign((size_t)layers * B, 0);
+  } catch (...) {
+    cudaFreeHost(p->K);
+    cudaFreeHost(p->V);
+    delete p;
+    return fail(IG_ERR_OOM, "host allocation of pool counters failed");
+  }
+  *out = p;
+  return IG_OK;
+}
+
+extern "C" ig_status ig_pool_destroy(ig_pool* pool) {
+  if (!pool) return IG_OK;
+  cudaError_t e1 = pool->K ? cudaFreeHost(pool->K) : cudaSuccess;
+  cudaError_t e2 = pool->V ? cudaFreeHost(pool->V) : cudaSuccess;
+  delete pool;
+  if (e1 != cudaSuccess) return cuda_fail(e1, "free pool keys");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "free pool values");
+  return IG_OK;
+}
+
+extern "C" ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V) {
+  IG_REQUIRE(pool && K && V, "null argument");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+  const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
+  *K = pool->K + (size_t)layer * le;
+  *V = pool->V + (size_t)layer * le;
+  return IG_OK;
+}
+
+extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const uint16_t* K,
+                                   const uint16_t* V) {
+  IG_REQUIRE(pool && K && V, "null argument");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+  const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = cudaMemcpyAsync(pool->K + (size_t)layer * le, K, le * 2, cudaMemcpyDefault, s);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(pool->V + (size_t)layer * le, V, le * 2, cudaMemcpyDefault, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pool write");
+  return IG_OK;
+}
+
+extern "C" ig_status ig_pool_evict(ig_pool* pool, int layer, int b, const uint8_t* used,
+                                   int32_t* slot_out, int32_t* filled_out) {
+  IG_REQUIRE(pool && slot_out, "null argument");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers && b >= 0 && b < pool->B, "layer/b out of range");
+  const size_t pb = (size_t)layer * pool->B + b;
+  const int cap = pool->cap;
+  uint8_t* cnt = pool->counter.data() + pb * cap;
+  uint32_t* seq = pool->seq.data() + pb * cap;
+  int32_t& filled = pool->filled[pb];
+  if (used) {
+    bool sat = false;
+    for (int s = 0; s < filled; ++s) {
+      if (used[s] && cnt[s] < 255) ++cnt[s];
+      sat |= (cnt[s] == 255);
+    }
+    if (sat)
+      for (int s = 0; s < filled; ++s) cnt[s] >>= 1;
+  }
+  int slot;
+  if (filled < cap) {
+    slot = filled++;
+  } else {
+    slot = 0;
+    for (int s = 1; s < cap; ++s) {
+      if (cnt[s] < cnt[slot] || (cnt[s] == cnt[slot] && seq[s] < seq[slot])) slot = s;
+    }
+  }
+  cnt[slot] = 0;
+  seq[slot] = pool->next_seq[pb]++;
+  *slot_out = slot;
+  if (filled_out) *filled_out = filled;
+  return IG_OK;
+}
+
+extern "C" ig_status ig_pool_counters(const ig_pool* pool, int layer, int b, uint8_t* out) {
+  IG_REQUIRE(pool && out, "null argument");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers && b >= 0 && b < pool->B, "layer/b out of range");
+  memcpy(out, pool->counter.data() + ((size_t)layer * pool->B + b) * pool->cap, pool->cap);
+  return IG_OK;
+}
+
+extern "C" ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B, int H, int d,
+                                  int k, int Lcap, const int32_t* slot, const int32_t* cols,
+                                  const uint16_t* k_new, const uint16_t* v_new, uint16_t* Kpart,
+                                  uint16_t* Kdense, uint16_t* Vdense) {
+  IG_REQUIRE(B > 0 && H > 0 && d > 0 && d % 8 == 0 && Lcap > 0, "bad sizes");
+  IG_REQUIRE(slot && k_new && v_new, "null slot, k_new or v_new");
+  IG_REQUIRE(!Kpart || (cols && k > 0 && k <= d), "Kpart needs cols and 0 < k <= d");
+  IG_REQUIRE((Kdense == nullptr) == (Vdense == nullptr), "Kdense and Vdense go together");
+  IG_REQUIRE(aligned(k_new, 16) && aligned(v_new, 16), "k_new, v_new must be 16-byte aligned");
+  IG_REQUIRE(!Kdense || (aligned(Kdense, 16) && aligned(Vdense, 16)), "dense KV must be 16-byte aligned");
+  uint4* Kp = nullptr;
+  uint4* Vp = nullptr;
+  int cap = 0;
+  if (pool) {
+    IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+    IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
+    const size_t le = (size_t)B * H * pool->cap * d;
+    Kp = reinterpret_cast<uint4*>(pool->Kdev + (size_t)layer * le);
+    Vp = reinterpret_cast<uint4*>(pool->Vdev + (size_t)layer * le);
+    cap = pool->cap;
+  }
+  k6_append<<<B * H, 64, 0, as_stream(stream)>>>(
+      Kp, Vp, cap, H, d, k, Lcap, slot, cols, reinterpret_cast<const __half*>(k_new),
+      reinterpret_cast<const __half*>(v_new), reinterpret_cast<__half*>(Kpart),
+      reinterpret_cast<uint4*>(Kdense), reinterpret_cast<uint4*>(Vdense), error_word());
+  IG_CHECK_LAUNCH("append launch");
+  return IG_OK;
+}

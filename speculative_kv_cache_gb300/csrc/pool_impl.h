@@ -1,0 +1,18 @@
+// Internal layout of the pinned host KV pool (opaque to ABI users).
+#pragma once
+
+#include <stdint.h>
+
+#include <vector>
+
+struct ig_pool {
+  int layers = 0, B = 0, H = 0, d = 0, cap = 0;
+  uint16_t* K = nullptr;     // pinned, mapped host memory [layers][B][H][cap][d]
+  uint16_t* V = nullptr;
+  uint16_t* Kdev = nullptr;  // the same memory as seen from the device
+  uint16_t* Vdev = nullptr;
+  std::vector<uint8_t> counter;   // [layers][B][cap]
+  std::vector<uint32_t> seq;      // insertion order per slot, [layers][B][cap]
+  std::vector<int32_t> filled;    // resident slots, [layers][B]
+  std::vector<uint32_t> next_seq; // [layers][B]
+};

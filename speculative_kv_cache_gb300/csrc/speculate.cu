@@ -1,0 +1,346 @@
+// Speculation for layer i from layer i-1's attention input (InfiniGen paper-graph summary,
+// section 3.4, "Decoding Stage", Steps 1-2):
+//   K1  partial query projection  q~p = x W~_Q^p       split-K, fp32 partial sums in workspace
+//   K1b RoPE epilogue (Llama)     q~p = RoPE(x W_Q) A[:, S]
+//   K2  speculated scores         s = scale q~p (K~p)^T, partial-key rows staged by bulk TMA
+#include <math.h>
+
+#include "ig_common.cuh"
+
+namespace ig {
+namespace {
+
+constexpr int kK1Threads = 256;      // 8 warps
+constexpr int kK1Cols = 128;         // columns per CTA: 32 lanes x 4
+constexpr int kK1XRows = 256;        // rows of x staged in shared memory at a time
+constexpr int kK1Unroll = 4;         // W rows in flight per warp
+constexpr int kMaxSplits = 16;
+
+// Number of K-splits of the projection for a given reduction length.
+inline int proj_splits(int D) {
+  int s = (D + 255) / 256;
+  return s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
+}
+
+// K1: part[s][b][n] = sum_{r in split s} x[b][r] * W[r][n] for one 128-column tile, one
+// split of the reduction axis and one chunk of BT batch rows.  Lane l owns 4 consecutive
+// columns (8-byte loads of W); the 8 warps stride over rows and are summed in a fixed tree,
+// so the result is deterministic.
+template <int BT, bool VEC>
+__global__ void __launch_bounds__(kK1Threads) k1_partial_q(const __half* __restrict__ x,
+                                                           const __half* __restrict__ W,
+                                                           float* __restrict__ part, int B, int D,
+                                                           int N, int rows_per_split) {
+  __shared__ float xs[BT][kK1XRows];
+  __shared__ float red[4][BT][kK1Cols];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c0 = blockIdx.x * kK1Cols + lane * 4;
+  const int s = blockIdx.y;
+  const int b0 = blockIdx.z * BT;
+  const int nb = min(BT, B - b0);
+  const int r_begin = s * rows_per_split;
+  const int r_end = min(D, r_begin + rows_per_split);
+
+  float acc[BT][4];
+#pragma unroll
+  for (int b = 0; b < BT; ++b)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[b][j] = 0.f;
+
+  for (int rc = r_begin; rc < r_end; rc += kK1XRows) {
+    const int nr = min(kK1XRows, r_end - rc);
+    __syncthreads();
+    for (int i = threadIdx.x; i < BT * kK1XRows; i += kK1Threads) {
+      int b = i / kK1XRows, r = i % kK1XRows;
+      xs[b][r] = (b < nb && r < nr) ? __half2float(x[(size_t)(b0 + b) * D + rc + r]) : 0.f;
+    }
+    __syncthreads();
+    for (int r = warp; r < nr; r += 8 * kK1Unroll) {
+      float w[kK1Unroll][4];
+#pragma unroll
+      for (int u = 0; u < kK1Unroll; ++u) {
+        const int rr = r + u * 8;
+        if (rr < nr) {
+          const __half* src = W + (size_t)(rc + rr) * N + c0;
+          if (VEC && c0 + 3 < N) {
+            uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+            float2 a = h2_to_f2(v.x), bq = h2_to_f2(v.y);
+            w[u][0] = a.x; w[u][1] = a.y; w[u][2] = bq.x; w[u][3] = bq.y;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) w[u][j] = (c0 + j < N) ? __half2float(src[j]) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) w[u][j] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kK1Unroll; ++u) {
+        const int rr = r + u * 8;
+        if (rr < nr) {
+#pragma unroll
+          for (int b = 0; b < BT; ++b) {
+            const float xv = xs[b][rr];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[b][j] = fmaf(xv, w[u][j], acc[b][j]);
+          }
+        }
+      }
+    }
+  }
+  // fixed-order tree over the 8 warps: (w + 4) -> w, (w + 2) -> w, 1 -> 0
+  for (int half = 4; half >= 1; half >>= 1) {
+    __syncthreads();
+    if (warp >= half && warp < 2 * half) {
+#pragma unroll
+      for (int b = 0; b < BT; ++b)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) red[warp - half][b][lane * 4 + j] = acc[b][j];
+    }
+    __syncthreads();
+    if (warp < half) {
+#pragma unroll
+      for (int b = 0; b < BT; ++b)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[b][j] += red[warp][b][lane * 4 + j];
+    }
+  }
+  if (warp == 0) {
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+      if (b < nb) {
+        float* dst = part + ((size_t)s * B + b0 + b) * N;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (c0 + j < N) dst[c0 + j] = acc[b][j];
+      }
+    }
+  }
+}
+
+template <int BT>
+ig_status launch_k1_bt(cudaStream_t st, const __half* x, const __half* W, float* part, int B,
+                       int D, int N, int S) {
+  const int rows = (D + S - 1) / S;
+  dim3 grid((N + kK1Cols - 1) / kK1Cols, S, (B + BT - 1) / BT);
+  const bool vec = (N % 4 == 0) && aligned(W, 8);
+  if (vec)
+    k1_partial_q<BT, true><<<grid, kK1Threads, 0, st>>>(x, W, part, B, D, N, rows);
+  else
+    k1_partial_q<BT, false><<<grid, kK1Threads, 0, st>>>(x, W, part, B, D, N, rows);
+  IG_CHECK_LAUNCH("partial query projection launch");
+  return IG_OK;
+}
+
+ig_status launch_k1(cudaStream_t st, const __half* x, const __half* W, float* part, int B, int D,
+                    int N, int S) {
+  if (B <= 1) return launch_k1_bt<1>(st, x, W, part, B, D, N, S);
+  if (B <= 2) return launch_k1_bt<2>(st, x, W, part, B, D, N, S);
+  if (B <= 4) return launch_k1_bt<4>(st, x, W, part, B, D, N, S);
+  if (B <= 8) return launch_k1_bt<8>(st, x, W, part, B, D, N, S);
+  return launch_k1_bt<16>(st, x, W, part, B, D, N, S);
+}
+
+// K1b: RoPE epilogue for one (b, h): q = sum of the split partials of x W_Q,h; rotate the
+// pairs (j, j + d/2) by p * theta^(-2j/d); then q~p[c] = sum_j q_rot[j] A[h][j][c].
+__global__ void k1b_rope_project(const float* __restrict__ part, int S, int B, int H, int d, int k,
+                                 const float* __restrict__ A_cols, const int* __restrict__ pos,
+                                 double theta, float* __restrict__ qp) {
+  extern __shared__ float sh[];
+  float* q = sh;           // d
+  float* qr = sh + d;      // d
+  const int bh = blockIdx.x, b = bh / H, h = bh % H;
+  const int N = H * d;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    float a = 0.f;
+    for (int s = 0; s < S; ++s) a += part[((size_t)s * B + b) * N + h * d + j];
+    q[j] = a;
+  }
+  __syncthreads();
+  const int half = d / 2;
+  const double p = (double)pos[b];
+  for (int j = threadIdx.x; j < half; j += blockDim.x) {
+    double inv = pow(theta, -2.0 * (double)j / (double)d);
+    double sn, cs;
+    sincos(p * inv, &sn, &cs);
+    const float lo = q[j], hi = q[j + half];
+    qr[j] = (float)((double)lo * cs - (double)hi * sn);
+    qr[j + half] = (float)((double)lo * sn + (double)hi * cs);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < k; c += blockDim.x) {
+    float a = 0.f;
+    const float* Ac = A_cols + (size_t)h * d * k + c;
+    for (int j = 0; j < d; ++j) a = fmaf(qr[j], Ac[(size_t)j * k], a);
+    qp[((size_t)b * H + h) * k + c] = a;
+  }
+}
+
+// K2: speculated scores for one (b, h) and a chunk of T tokens.  Thread 0 stages the k
+// partial-key rows of the chunk (T fp16 each, contiguous in the column-major cache) with k
+// bulk copies completing on one mbarrier; each thread then scores 4 tokens out of shared
+// memory.  The partial query is the sum of the S split partials, scaled once.
+__global__ void k2_scores(const float* __restrict__ qsrc, int S, int B, int H, int k,
+                          const __half* __restrict__ Kpart, const int* __restrict__ L_valid,
+                          int Lcap, int T, float scale, float* __restrict__ scores,
+                          float* __restrict__ q_out, int* err) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
+  float* qs = reinterpret_cast<float*>(smem + 16);
+  __half* Ks = reinterpret_cast<__half*>(smem + 16 + ((k * 4 + 127) & ~127));
+  const int bh = blockIdx.y, b = bh / H, h = bh % H;
+  const int t0 = blockIdx.x * T;
+  int L = L_valid[b];
+  if (L < 0 || L > Lcap) {
+    if (threadIdx.x == 0) raise_error(err, IG_DEVERR_INDEX);
+    L = L < 0 ? 0 : Lcap;
+  }
+  const int n_tok = max(0, min(T, L - t0));
+  const int n_copy = (n_tok + 7) & ~7;
+  const __half* rows = Kpart + ((size_t)bh * k) * Lcap + t0;
+  if (threadIdx.x == 0 && n_copy > 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(bar, (uint32_t)(k * n_copy * 2));
+    for (int c = 0; c < k; ++c) bulk_g2s(Ks + (size_t)c * T, rows + (size_t)c * Lcap, n_copy * 2, bar);
+  }
+  for (int c = threadIdx.x; c < k; c += blockDim.x) {
+    const int N = H * k;
+    float a = 0.f;
+    for (int s = 0; s < S; ++s) a += qsrc[((size_t)s * B + b) * N + h * k + c];
+    qs[c] = a * scale;
+    if (q_out && blockIdx.x == 0) q_out[(size_t)bh * k + c] = a;
+  }
+  __syncthreads();
+  const int tl = threadIdx.x * 4;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  if (n_copy > 0) {
+    if (!mbar_wait_bounded(bar, 0)) {
+      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
+      mbar_wait_bounded(bar, 0);  // give copies in flight one more bounded chance
+      return;
+    }
+    if (tl < n_tok) {
+      for (int c = 0; c < k; ++c) {
+        uint2 v = *reinterpret_cast<const uint2*>(Ks + (size_t)c * T + tl);
+        float2 f0 = h2_to_f2(v.x), f1 = h2_to_f2(v.y);
+        const float qc = qs[c];
+        acc[0] = fmaf(qc, f0.x, acc[0]);
+        acc[1] = fmaf(qc, f0.y, acc[1]);
+        acc[2] = fmaf(qc, f1.x, acc[2]);
+        acc[3] = fmaf(qc, f1.y, acc[3]);
+      }
+    }
+  }
+  const int t = t0 + tl;
+  if (tl < T && t < Lcap) {
+    float4 o;
+    o.x = (t + 0 < L) ? acc[0] : -INFINITY;
+    o.y = (t + 1 < L) ? acc[1] : -INFINITY;
+    o.z = (t + 2 < L) ? acc[2] : -INFINITY;
+    o.w = (t + 3 < L) ? acc[3] : -INFINITY;
+    *reinterpret_cast<float4*>(scores + (size_t)bh * Lcap + t) = o;
+  }
+}
+
+// Tokens per score CTA: as many as keep the staged rows within 80 KB (two or more CTAs per SM).
+inline int score_chunk(int k) {
+  int T = 512;
+  while (T > 64 && (size_t)k * T * 2 > 80 * 1024) T >>= 1;
+  return T;
+}
+
+inline size_t score_smem(int k, int T) { return 16 + round_up((size_t)k * 4, 128) + (size_t)k * T * 2; }
+
+ig_status launch_k2(cudaStream_t st, const float* qsrc, int S, int B, int H, int k,
+                    const uint16_t* Kpart, const int32_t* L_valid, int Lcap, float scale,
+                    float* scores, float* q_part) {
+  const int T = score_chunk(k);
+  const size_t sm = score_smem(k, T);
+  cudaError_t e = cudaFuncSetAttribute(k2_scores, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  if (e != cudaSuccess) return cuda_fail(e, "score kernel smem attribute");
+  dim3 grid((Lcap + T - 1) / T, B * H);
+  k2_scores<<<grid, T / 4, sm, st>>>(qsrc, S, B, H, k, reinterpret_cast<const __half*>(Kpart),
+                                     L_valid, Lcap, T, scale, scores, q_part, error_word());
+  IG_CHECK_LAUNCH("score kernel launch");
+  return IG_OK;
+}
+
+ig_status check_common(int B, int D, int H, int k, int Lcap, const void* x, const void* Kpart,
+                       const void* L_valid, const void* scores, const void* ws) {
+  IG_REQUIRE(B > 0 && D > 0 && H > 0 && k > 0, "B, D, H, k must be positive (got %d %d %d %d)", B, D, H, k);
+  IG_REQUIRE(Lcap > 0 && Lcap % 8 == 0, "Lcap must be a positive multiple of 8 (got %d)", Lcap);
+  IG_REQUIRE(x && Kpart && L_valid && scores && ws, "null pointer argument");
+  IG_REQUIRE(aligned(Kpart, 16), "Kpart must be 16-byte aligned");
+  IG_REQUIRE(aligned(scores, 16), "scores must be 16-byte aligned");
+  IG_REQUIRE(aligned(ws, 256), "workspace must be 256-byte aligned");
+  IG_REQUIRE((size_t)k * 4 <= 64 * 1024, "k too large");
+  return IG_OK;
+}
+
+}  // namespace
+}  // namespace ig
+
+using namespace ig;
+
+extern "C" size_t ig_speculate_workspace_bytes(int B, int D, int H, int k) {
+  if (B <= 0 || D <= 0 || H <= 0 || k <= 0) return 0;
+  return round_up((size_t)proj_splits(D) * B * H * k * sizeof(float), 256);
+}
+
+extern "C" ig_status ig_speculate(void* stream, int B, int D, int H, int k, int Lcap,
+                                  const uint16_t* x, const uint16_t* Wq_part,
+                                  const uint16_t* Kpart, const int32_t* L_valid,
+                                  float score_scale, float* scores, float* q_part,
+                                  void* workspace, size_t workspace_bytes) {
+  ig_status st = check_common(B, D, H, k, Lcap, x, Kpart, L_valid, scores, workspace);
+  if (st != IG_OK) return st;
+  IG_REQUIRE(Wq_part, "null Wq_part");
+  const size_t need = ig_speculate_workspace_bytes(B, D, H, k);
+  if (workspace_bytes < need)
+    return fail(IG_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  cudaStream_t s = as_stream(stream);
+  const int S = proj_splits(D);
+  float* part = static_cast<float*>(workspace);
+  st = launch_k1(s, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(Wq_part),
+                 part, B, D, H * k, S);
+  if (st != IG_OK) return st;
+  return launch_k2(s, part, S, B, H, k, Kpart, L_valid, Lcap, score_scale, scores, q_part);
+}
+
+extern "C" size_t ig_speculate_rope_workspace_bytes(int B, int D, int H, int d, int k) {
+  if (B <= 0 || D <= 0 || H <= 0 || d <= 0 || k <= 0) return 0;
+  return round_up((size_t)proj_splits(D) * B * H * d * sizeof(float), 256) +
+         round_up((size_t)B * H * k * sizeof(float), 256);
+}
+
+extern "C" ig_status ig_speculate_rope(void* stream, int B, int D, int H, int d, int k, int Lcap,
+                                       const uint16_t* x, const uint16_t* Wq,
+                                       const float* A_cols, const int32_t* positions,
+                                       float rope_theta, const uint16_t* Kpart,
+                                       const int32_t* L_valid, float score_scale,
+                                       float* scores, float* q_part, void* workspace,
+                                       size_t workspace_bytes) {
+  ig_status st = check_common(B, D, H, k, Lcap, x, Kpart, L_valid, scores, workspace);
+  if (st != IG_OK) return st;
+  IG_REQUIRE(Wq && A_cols && positions, "null Wq, A_cols or positions");
+  IG_REQUIRE(d > 0 && d % 2 == 0 && k <= d, "d must be even and k <= d (d=%d k=%d)", d, k);
+  IG_REQUIRE(rope_theta > 0.f, "rope_theta must be positive");
+  const size_t need = ig_speculate_rope_workspace_bytes(B, D, H, d, k);
+  if (workspace_bytes < need)
+    return fail(IG_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  cudaStream_t s = as_stream(stream);
+  const int S = proj_splits(D);
+  float* part = static_cast<float*>(workspace);
+  float* qp = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                       round_up((size_t)S * B * H * d * sizeof(float), 256));
+  st = launch_k1(s, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(Wq), part,
+                 B, D, H * d, S);
+  if (st != IG_OK) return st;
+  k1b_rope_project<<<B * H, 128, 2 * d * sizeof(float), s>>>(part, S, B, H, d, k, A_cols,
+                                                            positions, (double)rope_theta, qp);
+  IG_CHECK_LAUNCH("rope epilogue launch");
+  return launch_k2(s, qp, 1, B, H, k, Kpart, L_valid, Lcap, score_scale, scores, q_part);
+}

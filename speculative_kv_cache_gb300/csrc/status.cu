@@ -1,0 +1,80 @@
+// Status plumbing of the C ABI: per-thread error messages, the device error word, ig_check.
+#include <string.h>
+
+#include <mutex>
+
+#include "ig_common.cuh"
+
+namespace ig {
+
+namespace {
+thread_local char g_msg[512] = "";
+constexpr int kMaxDevices = 64;
+int* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+std::mutex g_mu;
+}  // namespace
+
+// One error word per device: bits IG_DEVERR_* set by guarded kernels.
+__device__ int g_device_error_word;
+
+ig_status fail(ig_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+ig_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(IG_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+}  // namespace ig
+
+extern "C" const char* ig_last_error(void) { return ig::g_msg; }
+
+extern "C" int ig_version(void) { return 100; }
+
+extern "C" ig_status ig_check(void* stream) {
+  cudaStream_t s = ig::as_stream(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return ig::cuda_fail(e, "ig_check: stream synchronize");
+  int* w = ig::error_word();
+  if (!w) return ig::fail(IG_ERR_CUDA, "ig_check: no device error word");
+  int v = 0;
+  e = cudaMemcpy(&v, w, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return ig::cuda_fail(e, "ig_check: read error word");
+  if (v) {
+    int zero = 0;
+    e = cudaMemcpy(w, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return ig::cuda_fail(e, "ig_check: clear error word");
+  }
+  if (v & IG_DEVERR_TIMEOUT) return ig::fail(IG_ERR_TIMEOUT, "a bounded in-kernel wait ran out (word 0x%x)", v);
+  if (v & IG_DEVERR_INDEX) return ig::fail(IG_ERR_INVALID, "an in-kernel index guard tripped (word 0x%x)", v);
+  return IG_OK;
+}

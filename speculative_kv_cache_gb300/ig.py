@@ -1,0 +1,241 @@
+"""Python binding of libig.so: the C ABI of include/ig.h, same names, argument marshalling only.
+
+Every function takes plain integers/floats for sizes and, for buffers, a torch tensor, a
+NumPy array, a raw integer address, or None (NULL).  Nothing here computes: each call goes
+straight to the library, and a non-zero status raises :class:`IGError`.  There is no fallback:
+if libig.so is missing or cannot load, importing this module fails.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import numpy as np
+
+try:  # torch provides the CUDA runtime that libig.so shares, and the tensors we pass
+    import torch
+except ImportError:  # pragma: no cover - torch is part of the environment
+    torch = None
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libig.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "ig.h")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is not built; run `python -m speculative_kv_cache_gb300.build`")
+_lib = C.CDLL(LIB_PATH)
+
+IG_OK = 0
+IG_ERR_INVALID = -1
+IG_ERR_CUDA = -2
+IG_ERR_OOM = -3
+IG_ERR_NUMERIC = -4
+IG_ERR_TIMEOUT = -5
+IG_ERR_CAPACITY = -6
+IG_SEL_THRESHOLD = 0
+IG_SEL_HEAD_AVG = 1
+
+_vp, _i, _f, _sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+
+
+class IGError(RuntimeError):
+    def __init__(self, status: int, fn: str):
+        self.status = status
+        msg = _lib.ig_last_error().decode(errors="replace")
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+
+
+def _sig(name, restype, *argtypes):
+    f = getattr(_lib, name)
+    f.restype = restype
+    f.argtypes = list(argtypes)
+    return f
+
+
+_sig("ig_last_error", C.c_char_p)
+_sig("ig_version", _i)
+_sig("ig_check", _i, _vp)
+_sig("ig_skew_weights", _i, _i, _i, _i, _f, _f, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp,
+     _vp, _vp, _i)
+_sig("ig_speculate_workspace_bytes", _sz, _i, _i, _i, _i)
+_sig("ig_speculate", _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _sz)
+_sig("ig_speculate_rope_workspace_bytes", _sz, _i, _i, _i, _i, _i)
+_sig("ig_speculate_rope", _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
+     _vp, _vp, _vp, _sz)
+_sig("ig_select_workspace_bytes", _sz, _i, _i)
+_sig("ig_select", _i, _vp, _i, _i, _i, _vp, _vp, _f, _i, _f, _vp, _vp, _vp, _vp, _sz)
+_sig("ig_pool_create", _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
+_sig("ig_pool_destroy", _i, _vp)
+_sig("ig_pool_kv", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_vp))
+_sig("ig_pool_write", _i, _vp, _vp, _i, _vp, _vp)
+_sig("ig_pool_evict", _i, _vp, _i, _i, _vp, C.POINTER(C.c_int32), C.POINTER(C.c_int32))
+_sig("ig_pool_counters", _i, _vp, _i, _i, _vp)
+_sig("ig_gather_kv", _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _i)
+_sig("ig_attend_workspace_bytes", _sz, _i, _i, _i, _i)
+_sig("ig_sparse_attend", _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz)
+_sig("ig_dense_attend", _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz)
+_sig("ig_append_kv", _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/ig.h declares."""
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b(ig_[a-z_0-9]+)\s*\(", txt)))
+
+
+def _p(x):
+    """Address of a buffer argument (tensor, ndarray, int, or None)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if torch is not None and isinstance(x, torch.Tensor):
+        if not x.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous")
+        return x.data_ptr()
+    if isinstance(x, np.ndarray):
+        if not x.flags["C_CONTIGUOUS"]:
+            raise ValueError("array arguments must be C-contiguous")
+        return x.ctypes.data
+    raise TypeError(f"unsupported buffer argument {type(x)}")
+
+
+def _s(stream):
+    """A cudaStream_t from a torch stream, an int handle, or None (torch's current stream)."""
+    if stream is None:
+        if torch is not None and torch.cuda.is_available():
+            return torch.cuda.current_stream().cuda_stream
+        return None
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ok(st: int, fn: str):
+    if st != IG_OK:
+        raise IGError(st, fn)
+
+
+def ig_version() -> int:
+    return _lib.ig_version()
+
+
+def ig_last_error() -> str:
+    return _lib.ig_last_error().decode(errors="replace")
+
+
+def ig_check(stream=None):
+    _ok(_lib.ig_check(_s(stream)), "ig_check")
+
+
+def ig_skew_weights(D, H, d, ratio, rope_theta, Xs, Ns, Wq, Wk, Kp, Nk, A, Wq_skew, Wk_skew,
+                    Kp_skew, cols, threads=0) -> int:
+    k = C.c_int(0)
+    _ok(_lib.ig_skew_weights(D, H, d, ratio, rope_theta, _p(Xs), Ns, _p(Wq), _p(Wk), _p(Kp), Nk,
+                             _p(A), _p(Wq_skew), _p(Wk_skew), _p(Kp_skew), _p(cols), C.byref(k),
+                             threads), "ig_skew_weights")
+    return k.value
+
+
+def ig_speculate_workspace_bytes(B, D, H, k) -> int:
+    return _lib.ig_speculate_workspace_bytes(B, D, H, k)
+
+
+def ig_speculate(stream, B, D, H, k, Lcap, x, Wq_part, Kpart, L_valid, score_scale, scores,
+                 q_part, workspace, workspace_bytes):
+    _ok(_lib.ig_speculate(_s(stream), B, D, H, k, Lcap, _p(x), _p(Wq_part), _p(Kpart), _p(L_valid),
+                          score_scale, _p(scores), _p(q_part), _p(workspace), workspace_bytes),
+        "ig_speculate")
+
+
+def ig_speculate_rope_workspace_bytes(B, D, H, d, k) -> int:
+    return _lib.ig_speculate_rope_workspace_bytes(B, D, H, d, k)
+
+
+def ig_speculate_rope(stream, B, D, H, d, k, Lcap, x, Wq, A_cols, positions, rope_theta, Kpart,
+                      L_valid, score_scale, scores, q_part, workspace, workspace_bytes):
+    _ok(_lib.ig_speculate_rope(_s(stream), B, D, H, d, k, Lcap, _p(x), _p(Wq), _p(A_cols),
+                               _p(positions), rope_theta, _p(Kpart), _p(L_valid), score_scale,
+                               _p(scores), _p(q_part), _p(workspace), workspace_bytes),
+        "ig_speculate_rope")
+
+
+def ig_select_workspace_bytes(B, H) -> int:
+    return _lib.ig_select_workspace_bytes(B, H)
+
+
+def ig_select(stream, B, H, Lcap, scores, L_valid, alpha, policy, cap_frac, idx, cnt, used,
+              workspace=None, workspace_bytes=0):
+    _ok(_lib.ig_select(_s(stream), B, H, Lcap, _p(scores), _p(L_valid), alpha, policy, cap_frac,
+                       _p(idx), _p(cnt), _p(used), _p(workspace), workspace_bytes), "ig_select")
+
+
+def ig_pool_create(layers, B, H, d, cap) -> int:
+    h = _vp()
+    _ok(_lib.ig_pool_create(layers, B, H, d, cap, C.byref(h)), "ig_pool_create")
+    return h.value
+
+
+def ig_pool_destroy(pool):
+    _ok(_lib.ig_pool_destroy(pool), "ig_pool_destroy")
+
+
+def ig_pool_kv(pool, layer):
+    """Host addresses (also valid on the device) of one layer's K and V arrays."""
+    k, v = _vp(), _vp()
+    _ok(_lib.ig_pool_kv(pool, layer, C.byref(k), C.byref(v)), "ig_pool_kv")
+    return k.value, v.value
+
+
+def ig_pool_write(pool, stream, layer, K, V):
+    _ok(_lib.ig_pool_write(pool, _s(stream), layer, _p(K), _p(V)), "ig_pool_write")
+
+
+def ig_pool_evict(pool, layer, b, used):
+    slot, filled = C.c_int32(0), C.c_int32(0)
+    _ok(_lib.ig_pool_evict(pool, layer, b, _p(used), C.byref(slot), C.byref(filled)), "ig_pool_evict")
+    return slot.value, filled.value
+
+
+def ig_pool_counters(pool, layer, b, out):
+    _ok(_lib.ig_pool_counters(pool, layer, b, _p(out)), "ig_pool_counters")
+
+
+def ig_gather_kv(stream, pool, layer, B, H, d, Lcap, idx, cnt, Kg, Vg, max_ctas=0):
+    _ok(_lib.ig_gather_kv(_s(stream), pool, layer, B, H, d, Lcap, _p(idx), _p(cnt), _p(Kg), _p(Vg),
+                          max_ctas), "ig_gather_kv")
+
+
+def ig_attend_workspace_bytes(B, H, d, Lcap) -> int:
+    return _lib.ig_attend_workspace_bytes(B, H, d, Lcap)
+
+
+def ig_sparse_attend(stream, B, H, d, Lcap, scale, q, Kg, Vg, cnt, k_new, v_new, out, workspace,
+                     workspace_bytes):
+    _ok(_lib.ig_sparse_attend(_s(stream), B, H, d, Lcap, scale, _p(q), _p(Kg), _p(Vg), _p(cnt),
+                              _p(k_new), _p(v_new), _p(out), _p(workspace), workspace_bytes),
+        "ig_sparse_attend")
+
+
+def ig_dense_attend(stream, B, H, d, Lcap, scale, q, K, V, L_valid, k_new, v_new, out, workspace,
+                    workspace_bytes):
+    _ok(_lib.ig_dense_attend(_s(stream), B, H, d, Lcap, scale, _p(q), _p(K), _p(V), _p(L_valid),
+                             _p(k_new), _p(v_new), _p(out), _p(workspace), workspace_bytes),
+        "ig_dense_attend")
+
+
+def ig_append_kv(stream, pool, layer, B, H, d, k, Lcap, slot, cols, k_new, v_new, Kpart, Kdense=None,
+                 Vdense=None):
+    _ok(_lib.ig_append_kv(_s(stream), pool, layer, B, H, d, k, Lcap, _p(slot), _p(cols), _p(k_new),
+                          _p(v_new), _p(Kpart), _p(Kdense), _p(Vdense)), "ig_append_kv")
+
+
+def pool_layer_view(pool, layer, B, H, cap, d):
+    """NumPy views (fp16) of one layer's K and V in the pinned pool: [B, H, cap, d] each."""
+    kp, vp = ig_pool_kv(pool, layer)
+    n = B * H * cap * d
+    K = np.ctypeslib.as_array(C.cast(kp, C.POINTER(C.c_uint16)), shape=(n,)).view(np.float16)
+    V = np.ctypeslib.as_array(C.cast(vp, C.POINTER(C.c_uint16)), shape=(n,)).view(np.float16)
+    return K.reshape(B, H, cap, d), V.reshape(B, H, cap, d)

@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads, and exports every function include/ig.h declares.
+
+No GPU is needed: these tests only load the library and exercise argument validation and
+host-side fault injection, which return before any CUDA call.
+"""
+import ctypes
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ig():
+    from speculative_kv_cache_gb300 import build
+
+    build.build()
+    from speculative_kv_cache_gb300 import ig as mod
+
+    return mod
+
+
+def test_every_declared_function_is_exported(ig):
+    names = ig.header_functions()
+    assert len(names) >= 20
+    for required in ["ig_skew_weights", "ig_speculate", "ig_select", "ig_gather_kv",
+                     "ig_sparse_attend", "ig_pool_evict", "ig_pool_create", "ig_pool_destroy",
+                     "ig_check"]:
+        assert required in names
+    lib = ctypes.CDLL(ig.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert hasattr(ig, n), f"binding lacks {n}"
+
+
+def test_version_and_error_string(ig):
+    assert ig.ig_version() == 100
+    assert isinstance(ig.ig_last_error(), str)
+
+
+def test_invalid_arguments_are_rejected_before_any_device_work(ig):
+    with pytest.raises(ig.IGError) as e:
+        ig.ig_select(0, 1, 1, 8, 16, 32, 0.0, ig.IG_SEL_THRESHOLD, 1.0, 48, 64, None)
+    assert e.value.status == ig.IG_ERR_INVALID and "alpha" in str(e.value)
+    with pytest.raises(ig.IGError) as e:
+        ig.ig_speculate(0, 1, 64, 1, 8, 12, 16, 16, 16, 16, 1.0, 16, None, 256, 1 << 20)
+    assert e.value.status == ig.IG_ERR_INVALID and "multiple of 8" in str(e.value)
+    with pytest.raises(ig.IGError) as e:
+        ig.ig_sparse_attend(0, 1, 1, 96, 8, 1.0, 16, 16, 16, 16, None, None, 16, None, 0)
+    assert e.value.status == ig.IG_ERR_INVALID
+
+
+def test_workspace_sizes(ig):
+    assert ig.ig_speculate_workspace_bytes(16, 7168, 56, 38) == 16 * 16 * 56 * 38 * 4
+    assert ig.ig_speculate_workspace_bytes(1, 256, 4, 16) == 256
+    assert ig.ig_select_workspace_bytes(16, 56) % 256 == 0
+    assert ig.ig_attend_workspace_bytes(1, 4, 64, 256) >= 4 * 4 * 66 * 4
+
+
+def test_injected_pinned_allocation_failure():
+    code = ("import os; os.environ['IG_FAULT']='pool_alloc';"
+            "from speculative_kv_cache_gb300 import ig;"
+            "import sys\n"
+            "try:\n ig.ig_pool_create(1, 1, 1, 8, 4)\n"
+            "except ig.IGError as e:\n sys.exit(0 if e.status == ig.IG_ERR_OOM else 3)\n"
+            "sys.exit(4)")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
