@@ -234,6 +234,97 @@ ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B, int H, int
                        const uint16_t* k_new, const uint16_t* v_new, uint16_t* Kpart,
                        uint16_t* Kdense, uint16_t* Vdense);
 
+/* ------------------------------------------------------------------------------------
+ * One decode step over every layer (native runtime of the calls above).  Section 3.2
+ * (architecture) and section 3.4, "Decoding Stage", Step 5 with Fig 8: while layer i-1
+ * attends, layer i is speculated from layer i-1's input and its rows are fetched on a side
+ * stream; layer 0 attends over its full, HBM-resident KV.  Order per step, compute stream S,
+ * fetch stream G:
+ *   S: dense attention + append of layer 0
+ *   for l = 1..L-1:  S: speculate(l), select(l)  ->  G: gather(l) into buffer l % 2
+ *                    S: wait gather(l-1), attention(l-1), append(l-1)
+ *   S: wait gather(L-1), attention(L-1), append(L-1); S finally waits for G.
+ * All buffers belong to the caller; the decoder holds only events.  The per-layer pointer
+ * arrays in ig_decoder_buffers are host arrays of device pointers, copied at creation. */
+typedef struct {
+  int layers, B, H, d, D, k, Lcap;
+  int policy;          /* IG_SEL_THRESHOLD or IG_SEL_HEAD_AVG */
+  float alpha;         /* > 0 */
+  float cap_frac;      /* >= 1: no cap */
+  float score_scale;   /* logit scale, e.g. 1/sqrt(d) */
+  float rope_theta;    /* 0: no RoPE (partial weight path); > 0: RoPE path */
+  int gather_ctas;     /* grid of the fetch kernel; 0 = library default */
+  int stage_timing;    /* 1: record timing events around each stage (ig_decoder_stage_ms) */
+} ig_decoder_config;
+
+typedef struct {
+  const uint16_t* const* Wq_part;  /* [layers] -> dev fp16 [D][H*k]       (no RoPE)        */
+  const uint16_t* const* Wq;       /* [layers] -> dev fp16 [D][H*d]       (RoPE)           */
+  const float* const* A_cols;      /* [layers] -> dev fp32 [H][d][k]      (RoPE)           */
+  uint16_t* const* Kpart;          /* [layers] -> dev fp16 [B][H][k][Lcap] (layer 0: may be NULL) */
+  const int32_t* const* cols;      /* [layers] -> dev int32 [H][k]                          */
+  uint16_t* K0;                    /* dev fp16 [B][H][Lcap][d]: layer 0's KV in HBM          */
+  uint16_t* V0;
+  float* scores;                   /* dev fp32 [B][H][Lcap]                                  */
+  int32_t* idx;                    /* dev int32 [2][B][H][Lcap]                              */
+  int32_t* cnt;                    /* dev int32 [layers][B][H]                               */
+  uint8_t* used;                   /* dev uint8 [layers][B][Lcap] or NULL                    */
+  uint16_t* Kg;                    /* dev fp16 [2][B][H][Lcap][d] (16-byte aligned)          */
+  uint16_t* Vg;
+  void* workspace;                 /* dev, >= ig_decoder_workspace_bytes(), 256-byte aligned */
+  size_t workspace_bytes;
+} ig_decoder_buffers;
+
+typedef struct {
+  const uint16_t* x;        /* dev fp16 [layers][B][D]    attention input of every layer       */
+  const uint16_t* q;        /* dev fp16 [layers][B][H][d] query of every layer (skewed basis)  */
+  const uint16_t* k_new;    /* dev fp16 [layers][B][H][d] current token's key                  */
+  const uint16_t* v_new;    /* dev fp16 [layers][B][H][d] current token's value                */
+  const int32_t* L_valid;   /* dev int32 [B] resident slots before this step's append          */
+  const int32_t* positions; /* dev int32 [B] current position (RoPE only)                     */
+  const int32_t* slot;      /* dev int32 [layers][B] append slot per layer, or NULL: no append */
+  float* out;               /* dev fp32 [layers][B][H][d] attention output of every layer     */
+} ig_step_io;
+
+typedef struct ig_decoder ig_decoder;
+
+size_t ig_decoder_workspace_bytes(const ig_decoder_config* cfg);
+ig_status ig_decoder_create(const ig_decoder_config* cfg, const ig_decoder_buffers* buffers,
+                            ig_pool* pool, ig_decoder** out);
+ig_status ig_decoder_destroy(ig_decoder* dec);
+/* Enqueues one step on `stream` (compute) and `side_stream` (fetch); returns at once. */
+ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void* stream, void* side_stream);
+
+/* Pool counters only: folds one step's use of (layer, b) into its counters, without placing a
+ * token (ig_pool_evict does both).  While the pool is not full the two orders agree, so a
+ * runtime may fold use in late, off the critical path. */
+ig_status ig_pool_update(ig_pool* pool, int layer, int b, const uint8_t* used);
+
+/* Prefill: inserts n_tokens prompt tokens into every (layer, sequence) pool exactly as
+ * n_tokens calls of ig_pool_evict(used = NULL) would (the free slots in order, then, with all
+ * counters at 0, the oldest slot first).  slots_out: host int32 [n_tokens] or NULL, the slot
+ * of each prompt token (the same for every layer and sequence). */
+ig_status ig_pool_prefill(ig_pool* pool, int n_tokens, int32_t* slots_out);
+
+/* One decode step of the pool manager for every (layer, sequence) at once.
+ *   used      host uint8 [layers][B][Lcap] (first `cap` entries of each row are read) or NULL
+ *   slots_out host int32 [layers][B] or NULL
+ * With `used`, folds that step's use into the counters (as ig_pool_update); with `slots_out`,
+ * then places the next token (as ig_pool_evict(used = NULL)).  ig_pool_full() tells whether
+ * any pool is full, i.e. whether placement depends on the counters. */
+ig_status ig_pool_step(ig_pool* pool, const uint8_t* used, int Lcap, int32_t* slots_out);
+ig_status ig_pool_full(const ig_pool* pool, int* any_full);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t ig_launch_count(void);
+
+/* Stage timing of a recent ig_decode_step (steps_back = 0: the last one, 1: the one before),
+ * when the decoder was created with config.stage_timing = 1: ms_out[0] = sum of gather kernel
+ * times (fetch stream), ms_out[1] = speculate + select, ms_out[2] = attention + append
+ * (compute stream); counts_out[0..2] = the number of timed intervals of each.  Waits for that
+ * step to finish; reading step t-1 while step t is queued keeps the GPU busy. */
+ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float* ms_out, int* counts_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,287 @@
+// One decode step over every layer, pipelined as InfiniGen's KV selection controller and
+// inference controller are (paper-graph summary, section 3.2 architecture and section 3.4,
+// "Decoding Stage", Step 5 and Fig 8): while layer i-1 computes, layer i is speculated from
+// layer i-1's input and its selected rows are fetched on a side stream; layer 0 attends over
+// its full, HBM-resident KV.
+//
+// Per step, on the compute stream S and the fetch stream G:
+//   S: dense attention of layer 0, append of layer 0
+//   for l = 1 .. L-1:
+//     S: speculate(l), select(l), record sel[l]
+//     G: wait sel[l] (and att[l-2], which frees gather buffer l % 2), gather(l), record got[l]
+//     S: (l >= 2) wait got[l-1], attention(l-1), append(l-1), record att[l-1]
+//   S: wait got[L-1], attention(L-1), append(L-1)
+#include <vector>
+
+#include "ig_common.cuh"
+#include "pool_impl.h"
+
+struct ig_decoder {
+  ig_decoder_config cfg{};
+  ig_decoder_buffers buf{};
+  std::vector<const uint16_t*> Wq_part, Wq;
+  std::vector<const float*> A_cols;
+  std::vector<uint16_t*> Kpart;
+  std::vector<const int32_t*> cols;
+  ig_pool* pool = nullptr;
+  std::vector<cudaEvent_t> ev_sel, ev_got, ev_att;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  // stage timing (optional): [layer] start/end of gather (G), speculate+select and
+  // attention+append (S)
+  // attention+append (S); two sets, alternating by step, indexed [parity * layers + layer]
+  std::vector<cudaEvent_t> tg0, tg1, ts0, ts1, ta0, ta1;
+  long long steps = 0;  // decode steps enqueued so far
+};
+
+namespace {
+
+size_t sz_scores(const ig_decoder_config& c) { return (size_t)c.B * c.H * c.Lcap; }
+size_t sz_kv(const ig_decoder_config& c) { return (size_t)c.B * c.H * c.Lcap * c.d; }
+
+void destroy_events(ig_decoder* d) {
+  for (auto* v : {&d->ev_sel, &d->ev_got, &d->ev_att, &d->tg0, &d->tg1, &d->ts0, &d->ts1, &d->ta0,
+                  &d->ta1})
+    for (cudaEvent_t e : *v)
+      if (e) cudaEventDestroy(e);
+  if (d->ev_fork) cudaEventDestroy(d->ev_fork);
+  if (d->ev_join) cudaEventDestroy(d->ev_join);
+}
+
+}  // namespace
+
+using namespace ig;
+
+extern "C" size_t ig_decoder_workspace_bytes(const ig_decoder_config* c) {
+  if (!c) return 0;
+  size_t a = c->rope_theta > 0.f ? ig_speculate_rope_workspace_bytes(c->B, c->D, c->H, c->d, c->k)
+                                  : ig_speculate_workspace_bytes(c->B, c->D, c->H, c->k);
+  size_t b = ig_attend_workspace_bytes(c->B, c->H, c->d, c->Lcap);
+  size_t s = ig_select_workspace_bytes(c->B, c->H);
+  size_t m = a > b ? a : b;
+  return m + round_up(s, 256);
+}
+
+extern "C" ig_status ig_decoder_create(const ig_decoder_config* cfg, const ig_decoder_buffers* buf,
+                                       ig_pool* pool, ig_decoder** out) {
+  IG_REQUIRE(cfg && buf && out, "null argument");
+  *out = nullptr;
+  const ig_decoder_config& c = *cfg;
+  IG_REQUIRE(c.layers >= 1 && c.B > 0 && c.H > 0 && c.d > 0 && c.D > 0 && c.k > 0 && c.k <= c.d,
+             "bad decoder sizes");
+  IG_REQUIRE(c.Lcap > 0 && c.Lcap % 8 == 0, "Lcap must be a positive multiple of 8");
+  IG_REQUIRE(c.alpha > 0.f, "alpha must be > 0");
+  IG_REQUIRE(pool && pool->layers == c.layers && pool->B == c.B && pool->H == c.H && pool->d == c.d,
+             "pool does not match the decoder");
+  IG_REQUIRE(pool->cap <= c.Lcap, "pool capacity %d exceeds Lcap %d", pool->cap, c.Lcap);
+  IG_REQUIRE(buf->Kpart && buf->cols && buf->K0 && buf->V0 && buf->scores && buf->idx && buf->cnt &&
+                 buf->Kg && buf->Vg && buf->workspace,
+             "missing decoder buffer");
+  if (c.rope_theta > 0.f)
+    IG_REQUIRE(buf->Wq && buf->A_cols, "RoPE decoding needs Wq and A_cols");
+  else
+    IG_REQUIRE(buf->Wq_part, "decoding needs Wq_part");
+  IG_REQUIRE(buf->workspace_bytes >= ig_decoder_workspace_bytes(cfg), "decoder workspace too small");
+  ig_decoder* d = new ig_decoder();
+  d->cfg = c;
+  d->buf = *buf;
+  d->pool = pool;
+  const int L = c.layers;
+  for (int l = 0; l < L; ++l) {
+    d->Kpart.push_back(buf->Kpart[l]);
+    d->cols.push_back(buf->cols[l]);
+    d->Wq_part.push_back(buf->Wq_part ? buf->Wq_part[l] : nullptr);
+    d->Wq.push_back(buf->Wq ? buf->Wq[l] : nullptr);
+    d->A_cols.push_back(buf->A_cols ? buf->A_cols[l] : nullptr);
+  }
+  d->buf.Wq_part = nullptr;  // the host arrays belong to the caller; we keep our copies
+  d->buf.Wq = nullptr;
+  d->buf.A_cols = nullptr;
+  d->buf.Kpart = nullptr;
+  d->buf.cols = nullptr;
+  d->ev_sel.assign(L, nullptr);
+  d->ev_got.assign(L, nullptr);
+  d->ev_att.assign(L, nullptr);
+  cudaError_t e = cudaSuccess;
+  for (int l = 0; l < L && e == cudaSuccess; ++l) {
+    e = cudaEventCreateWithFlags(&d->ev_sel[l], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->ev_got[l], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->ev_att[l], cudaEventDisableTiming);
+  }
+  if (c.stage_timing) {
+    for (auto* v : {&d->tg0, &d->tg1, &d->ts0, &d->ts1, &d->ta0, &d->ta1}) {
+      v->assign(2 * L, nullptr);
+      for (int l = 0; l < 2 * L && e == cudaSuccess; ++l) e = cudaEventCreate(&(*v)[l]);
+    }
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->ev_fork, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->ev_join, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    destroy_events(d);
+    delete d;
+    return cuda_fail(e, "decoder events");
+  }
+  if (!error_word()) {  // resolve the error word now, outside any stream capture
+    destroy_events(d);
+    delete d;
+    return fail(IG_ERR_CUDA, "no device error word");
+  }
+  *out = d;
+  return IG_OK;
+}
+
+extern "C" ig_status ig_decoder_destroy(ig_decoder* d) {
+  if (!d) return IG_OK;
+  destroy_events(d);
+  delete d;
+  return IG_OK;
+}
+
+extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void* stream,
+                                    void* side_stream) {
+  IG_REQUIRE(dec && io, "null argument");
+  IG_REQUIRE(io->x && io->q && io->k_new && io->v_new && io->L_valid && io->out, "missing step input");
+  const ig_decoder_config& c = dec->cfg;
+  const ig_decoder_buffers& b = dec->buf;
+  IG_REQUIRE(!(c.rope_theta > 0.f) || io->positions, "RoPE decoding needs positions");
+  cudaStream_t S = as_stream(stream), G = as_stream(side_stream);
+  IG_REQUIRE(S != G, "the fetch stream must differ from the compute stream");
+  const int L = c.layers, B = c.B, H = c.H, d = c.d, D = c.D, k = c.k, Lc = c.Lcap;
+  const size_t xs = (size_t)B * D, ts = (size_t)B * H * d;
+  char* ws = static_cast<char*>(b.workspace);
+  const size_t spec_att_ws = b.workspace_bytes - round_up(ig_select_workspace_bytes(B, H), 256);
+  void* sel_ws = ws + spec_att_ws;
+  const size_t sel_ws_bytes = round_up(ig_select_workspace_bytes(B, H), 256);
+  ig_status st;
+  cudaError_t e;
+
+  // G joins S's work so far (the caller's uploads), so it never runs ahead of its inputs
+  e = cudaEventRecord(dec->ev_fork, S);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(G, dec->ev_fork, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "decode step fork");
+
+  auto attend_append = [&](int l) -> ig_status {
+    const size_t buf = (size_t)(l & 1);
+    const int32_t* slot = io->slot ? io->slot + (size_t)l * B : nullptr;
+    ig_status r;
+    if (l == 0) {
+      r = ig_dense_attend(S, B, H, d, Lc, c.score_scale, io->q, b.K0, b.V0, io->L_valid, io->k_new,
+                          io->v_new, io->out, ws, spec_att_ws);
+    } else {
+      r = ig_sparse_attend(S, B, H, d, Lc, c.score_scale, io->q + (size_t)l * ts,
+                           b.Kg + buf * sz_kv(c), b.Vg + buf * sz_kv(c), b.cnt + (size_t)l * B * H,
+                           io->k_new + (size_t)l * ts, io->v_new + (size_t)l * ts,
+                           io->out + (size_t)l * ts, ws, spec_att_ws);
+    }
+    if (r != IG_OK || !slot) return r;
+    if (l == 0)
+      return ig_append_kv(S, nullptr, 0, B, H, d, k, Lc, slot, dec->cols[0], io->k_new, io->v_new,
+                          dec->Kpart[0], b.K0, b.V0);
+    return ig_append_kv(S, dec->pool, l, B, H, d, k, Lc, slot, dec->cols[l],
+                        io->k_new + (size_t)l * ts, io->v_new + (size_t)l * ts, dec->Kpart[l],
+                        nullptr, nullptr);
+  };
+
+  const bool timing = c.stage_timing != 0;
+  const int tset = (int)(dec->steps & 1) * L;
+  auto rec = [&](std::vector<cudaEvent_t>& v, int l, cudaStream_t s) -> cudaError_t {
+    return timing ? cudaEventRecord(v[tset + l], s) : cudaSuccess;
+  };
+  auto timed_attend = [&](int l) -> ig_status {
+    cudaError_t te = rec(dec->ta0, l, S);
+    if (te != cudaSuccess) return cuda_fail(te, "timing event");
+    ig_status r = attend_append(l);
+    if (r != IG_OK) return r;
+    te = rec(dec->ta1, l, S);
+    return te == cudaSuccess ? IG_OK : cuda_fail(te, "timing event");
+  };
+  dec->steps += 1;
+
+  st = timed_attend(0);
+  if (st != IG_OK) return st;
+  for (int l = 1; l < L; ++l) {
+    float* sc = b.scores;
+    int32_t* idx = b.idx + (size_t)(l & 1) * sz_scores(c);
+    int32_t* cnt = b.cnt + (size_t)l * B * H;
+    uint8_t* used = b.used ? b.used + (size_t)l * B * Lc : nullptr;
+    e = rec(dec->ts0, l, S);
+    if (e != cudaSuccess) return cuda_fail(e, "timing event");
+    if (c.rope_theta > 0.f) {
+      const int32_t* pos = io->positions;
+      st = ig_speculate_rope(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq[l],
+                             dec->A_cols[l], pos, c.rope_theta, dec->Kpart[l], io->L_valid,
+                             c.score_scale, sc, nullptr, ws, spec_att_ws);
+    } else {
+      st = ig_speculate(S, B, D, H, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq_part[l],
+                        dec->Kpart[l], io->L_valid, c.score_scale, sc, nullptr, ws, spec_att_ws);
+    }
+    if (st != IG_OK) return st;
+    st = ig_select(S, B, H, Lc, sc, io->L_valid, c.alpha, c.policy, c.cap_frac, idx, cnt, used,
+                   sel_ws, sel_ws_bytes);
+    if (st != IG_OK) return st;
+    e = rec(dec->ts1, l, S);
+    if (e == cudaSuccess) e = cudaEventRecord(dec->ev_sel[l], S);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(G, dec->ev_sel[l], 0);
+    if (e == cudaSuccess && l >= 3) e = cudaStreamWaitEvent(G, dec->ev_att[l - 2], 0);
+    if (e == cudaSuccess) e = rec(dec->tg0, l, G);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step events (select)");
+    const size_t buf = (size_t)(l & 1);
+    st = ig_gather_kv(G, dec->pool, l, B, H, d, Lc, idx, cnt, b.Kg + buf * sz_kv(c),
+                      b.Vg + buf * sz_kv(c), c.gather_ctas);
+    if (st != IG_OK) return st;
+    e = rec(dec->tg1, l, G);
+    if (e == cudaSuccess) e = cudaEventRecord(dec->ev_got[l], G);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step events (gather)");
+    if (l >= 2) {
+      e = cudaStreamWaitEvent(S, dec->ev_got[l - 1], 0);
+      if (e != cudaSuccess) return cuda_fail(e, "decode step wait");
+      st = timed_attend(l - 1);
+      if (st != IG_OK) return st;
+      e = cudaEventRecord(dec->ev_att[l - 1], S);
+      if (e != cudaSuccess) return cuda_fail(e, "decode step events (attend)");
+    }
+  }
+  if (L >= 2) {
+    e = cudaStreamWaitEvent(S, dec->ev_got[L - 1], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step wait");
+    st = timed_attend(L - 1);
+    if (st != IG_OK) return st;
+  }
+  // S ends after everything G did, so the caller can treat S alone as the step's stream
+  e = cudaEventRecord(dec->ev_join, G);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(S, dec->ev_join, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "decode step join");
+  return IG_OK;
+}
+
+extern "C" ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float* ms_out,
+                                         int* counts_out) {
+  IG_REQUIRE(dec && ms_out, "null argument");
+  IG_REQUIRE(steps_back == 0 || steps_back == 1, "steps_back must be 0 or 1");
+  IG_REQUIRE(dec->cfg.stage_timing && dec->steps > steps_back, "stage timing is off or no such step");
+  const int L = dec->cfg.layers;
+  const int tset = (int)((dec->steps - 1 - steps_back) & 1) * L;
+  double sums[3] = {0, 0, 0};
+  int counts[3] = {0, 0, 0};
+  auto span = [&](cudaEvent_t a, cudaEvent_t b, int which) -> cudaError_t {
+    cudaError_t e = cudaEventSynchronize(b);
+    if (e != cudaSuccess) return e;
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, a, b);
+    if (e != cudaSuccess) return e;
+    sums[which] += ms;
+    counts[which] += 1;
+    return cudaSuccess;
+  };
+  cudaError_t e = cudaSuccess;
+  for (int l = 0; l < L && e == cudaSuccess; ++l) {
+    if (l >= 1) e = span(dec->tg0[tset + l], dec->tg1[tset + l], 0);
+    if (e == cudaSuccess && l >= 1) e = span(dec->ts0[tset + l], dec->ts1[tset + l], 1);
+    if (e == cudaSuccess) e = span(dec->ta0[tset + l], dec->ta1[tset + l], 2);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "stage timing");
+  for (int i = 0; i < 3; ++i) {
+    ms_out[i] = (float)sums[i];
+    if (counts_out) counts_out[i] = counts[i];
+  }
+  return IG_OK;
+}

@@ -31,10 +31,14 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Counts one kernel launch of this library (ig_launch_count).
+void count_launch();
+
 #define IG_CHECK_LAUNCH(what)                                   \
   do {                                                          \
     cudaError_t e_ = cudaGetLastError();                        \
     if (e_ != cudaSuccess) return ::ig::cuda_fail(e_, what);    \
+    ::ig::count_launch();                                       \
   } while (0)
 
 #define IG_REQUIRE(cond, ...)                                   \

@@ -155,37 +155,91 @@ extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const
   return IG_OK;
 }
 
+namespace {
+void fold_use(ig_pool* pool, size_t pb, const uint8_t* used) {
+  const int cap = pool->cap;
+  uint8_t* cnt = pool->counter.data() + pb * cap;
+  const int filled = pool->filled[pb];
+  bool sat = false;
+  for (int s = 0; s < filled; ++s) {
+    if (used[s] && cnt[s] < 255) ++cnt[s];
+    sat |= (cnt[s] == 255);
+  }
+  if (sat)
+    for (int s = 0; s < filled; ++s) cnt[s] >>= 1;
+}
+}  // namespace
+
+extern "C" ig_status ig_pool_update(ig_pool* pool, int layer, int b, const uint8_t* used) {
+  IG_REQUIRE(pool && used, "null argument");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers && b >= 0 && b < pool->B, "layer/b out of range");
+  fold_use(pool, (size_t)layer * pool->B + b, used);
+  return IG_OK;
+}
+
+namespace {
+int place(ig_pool* pool, size_t pb);
+}  // namespace
+
 extern "C" ig_status ig_pool_evict(ig_pool* pool, int layer, int b, const uint8_t* used,
                                    int32_t* slot_out, int32_t* filled_out) {
   IG_REQUIRE(pool && slot_out, "null argument");
   IG_REQUIRE(layer >= 0 && layer < pool->layers && b >= 0 && b < pool->B, "layer/b out of range");
   const size_t pb = (size_t)layer * pool->B + b;
+  if (used) fold_use(pool, pb, used);
+  *slot_out = place(pool, pb);
+  if (filled_out) *filled_out = pool->filled[pb];
+  return IG_OK;
+}
+
+namespace {
+int place(ig_pool* pool, size_t pb) {
   const int cap = pool->cap;
   uint8_t* cnt = pool->counter.data() + pb * cap;
   uint32_t* seq = pool->seq.data() + pb * cap;
   int32_t& filled = pool->filled[pb];
-  if (used) {
-    bool sat = false;
-    for (int s = 0; s < filled; ++s) {
-      if (used[s] && cnt[s] < 255) ++cnt[s];
-      sat |= (cnt[s] == 255);
-    }
-    if (sat)
-      for (int s = 0; s < filled; ++s) cnt[s] >>= 1;
-  }
   int slot;
   if (filled < cap) {
     slot = filled++;
   } else {
     slot = 0;
-    for (int s = 1; s < cap; ++s) {
+    for (int s = 1; s < cap; ++s)
       if (cnt[s] < cnt[slot] || (cnt[s] == cnt[slot] && seq[s] < seq[slot])) slot = s;
-    }
   }
   cnt[slot] = 0;
   seq[slot] = pool->next_seq[pb]++;
-  *slot_out = slot;
-  if (filled_out) *filled_out = filled;
+  return slot;
+}
+}  // namespace
+
+extern "C" ig_status ig_pool_prefill(ig_pool* pool, int n_tokens, int32_t* slots_out) {
+  IG_REQUIRE(pool && n_tokens >= 0, "bad argument");
+  const size_t npb = (size_t)pool->layers * pool->B;
+  for (size_t pb = 0; pb < npb; ++pb) {
+    for (int t = 0; t < n_tokens; ++t) {
+      const int s = place(pool, pb);
+      if (pb == 0 && slots_out) slots_out[t] = s;
+    }
+  }
+  return IG_OK;
+}
+
+extern "C" ig_status ig_pool_step(ig_pool* pool, const uint8_t* used, int Lcap, int32_t* slots_out) {
+  IG_REQUIRE(pool, "null pool");
+  IG_REQUIRE(!used || Lcap >= pool->cap, "Lcap must cover the pool capacity");
+  const size_t npb = (size_t)pool->layers * pool->B;
+  if (used)
+    for (size_t pb = 0; pb < npb; ++pb) fold_use(pool, pb, used + pb * (size_t)Lcap);
+  if (slots_out)
+    for (size_t pb = 0; pb < npb; ++pb) slots_out[pb] = place(pool, pb);
+  return IG_OK;
+}
+
+extern "C" ig_status ig_pool_full(const ig_pool* pool, int* any_full) {
+  IG_REQUIRE(pool && any_full, "null argument");
+  *any_full = 0;
+  for (int32_t f : pool->filled)
+    if (f >= pool->cap) *any_full = 1;
   return IG_OK;
 }
 

@@ -1,6 +1,7 @@
 // Status plumbing of the C ABI: per-thread error messages, the device error word, ig_check.
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "ig_common.cuh"
@@ -54,7 +55,15 @@ int sm_count() {
   return g_sms[dev];
 }
 
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace ig
+
+extern "C" uint64_t ig_launch_count(void) { return ig::g_launches.load(); }
 
 extern "C" const char* ig_last_error(void) { return ig::g_msg; }
 

@@ -1,0 +1,194 @@
+"""Decoder: the user-facing decode engine over the C ABI (buffers, streams, pool manager).
+
+It owns the pinned KV pool, the HBM-resident partial key caches and layer-0 KV, the working
+buffers of one step, a compute stream and a fetch stream.  ``step`` runs one decode step of
+every layer through ``ig_decode_step`` (all arithmetic is in libig.so's kernels), then hands
+the step's "used" flags to the host-side counter pool manager.
+
+Pool-manager ordering (section 3.4, "KV Cache Pool Management Under Memory Pressure"): the new
+token of step t goes to a slot chosen after folding step t-1's use into the counters.  While
+no pool is full the slot does not depend on the counters, so the decoder places the token
+first and folds step t-1's use while step t runs on the GPU; once a pool is full it folds
+first, which makes the host wait for step t-1 before launching step t.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import ig
+
+
+class Decoder:
+    def __init__(self, *, layers, B, H, d, D, k, Lcap, pool_cap, alpha, policy=ig.IG_SEL_THRESHOLD,
+                 cap_frac=1.0, score_scale=None, rope_theta=0.0, gather_ctas=0, stage_timing=False,
+                 device="cuda:0"):
+        if pool_cap > Lcap or Lcap % 8:
+            raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
+        self.layers, self.B, self.H, self.d, self.D, self.k, self.Lcap = layers, B, H, d, D, k, Lcap
+        self.pool_cap = pool_cap
+        self.rope = rope_theta > 0
+        self.dev = torch.device(device)
+        torch.cuda.set_device(self.dev)
+        f16, i32 = torch.float16, torch.int32
+        e = lambda *s, dt=f16: torch.empty(*s, dtype=dt, device=self.dev)  # noqa: E731
+        self.pool = ig.ig_pool_create(layers, B, H, d, pool_cap)
+        self.cfg = ig.DecoderConfig(layers, B, H, d, D, k, Lcap, policy, float(alpha), float(cap_frac),
+                                    float(score_scale if score_scale is not None else 1.0 / math.sqrt(d)),
+                                    float(rope_theta), int(gather_ctas), int(bool(stage_timing)))
+        # per-layer state: partial query weight (or full W_Q and A[:, S] for RoPE), columns,
+        # partial key cache; layer 0 keeps its full KV in HBM instead
+        self.Wq_part = [None] + [e(D, H * k) for _ in range(1, layers)] if not self.rope else None
+        self.Wq = [None] + [e(D, H * d) for _ in range(1, layers)] if self.rope else None
+        self.A_cols = [None] + [e(H, d, k, dt=torch.float32) for _ in range(1, layers)] if self.rope else None
+        self.cols = [torch.zeros(H, k, dtype=i32, device=self.dev) for _ in range(layers)]
+        self.Kpart = [None] + [e(B, H, k, Lcap) for _ in range(1, layers)]
+        self.K0, self.V0 = e(B, H, Lcap, d), e(B, H, Lcap, d)
+        self.scores = e(B, H, Lcap, dt=torch.float32)
+        self.idx = e(2, B, H, Lcap, dt=i32)
+        self.cnt = torch.zeros(layers, B, H, dtype=i32, device=self.dev)
+        self.used = torch.zeros(layers, B, Lcap, dtype=torch.uint8, device=self.dev)
+        self.Kg, self.Vg = e(2, B, H, Lcap, d), e(2, B, H, Lcap, d)
+        self.ws = torch.empty(ig.ig_decoder_workspace_bytes(self.cfg), dtype=torch.uint8, device=self.dev)
+        # control data of a step (double-buffered pinned host + device)
+        self.L_host = [torch.zeros(B, dtype=i32).pin_memory() for _ in range(2)]
+        self.pos_host = [torch.zeros(B, dtype=i32).pin_memory() for _ in range(2)]
+        self.slot_host = [torch.zeros(layers, B, dtype=i32).pin_memory() for _ in range(2)]
+        self.L_dev, self.pos_dev = e(B, dt=i32), e(B, dt=i32)
+        self.slot_dev = e(layers, B, dt=i32)
+        self.used_host = [torch.zeros(layers, B, Lcap, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        self.S = torch.cuda.Stream(self.dev)
+        self.G = torch.cuda.Stream(self.dev)
+        self._keep = self._make_buffers()
+        self.handle = ig.ig_decoder_create(self.cfg, self._keep[0], self.pool)
+        self.filled = 0
+        self.t = 0
+        self._pending = None  # (buffer index, event) of the last step's used flags
+
+    def _make_buffers(self):
+        arrs = {}
+        if self.rope:
+            arrs["Wq"] = ig._ptr_array([0] + self.Wq[1:])
+            arrs["A_cols"] = ig._ptr_array([0] + self.A_cols[1:])
+        else:
+            arrs["Wq_part"] = ig._ptr_array([0] + self.Wq_part[1:])
+        arrs["Kpart"] = ig._ptr_array([0] + self.Kpart[1:])
+        arrs["cols"] = ig._ptr_array(self.cols)
+        b = ig.DecoderBuffers()
+        for name, a in arrs.items():
+            setattr(b, name, a)
+        b.K0, b.V0 = self.K0.data_ptr(), self.V0.data_ptr()
+        b.scores, b.idx, b.cnt = self.scores.data_ptr(), self.idx.data_ptr(), self.cnt.data_ptr()
+        b.used = self.used.data_ptr()
+        b.Kg, b.Vg = self.Kg.data_ptr(), self.Vg.data_ptr()
+        b.workspace, b.workspace_bytes = self.ws.data_ptr(), self.ws.numel()
+        return b, arrs
+
+    # ------------------------------------------------------------------ setup (not timed)
+    def load_layer(self, l, K, V, cols, Wq_part=None, Wq=None, A_cols=None):
+        """Installs layer l: skewed keys K and values V [B, H, pool_cap, d] (device fp16), the
+        chosen columns [H, k], and the partial query weight (or W_Q and A[:, S] for RoPE)."""
+        # the inputs may still be in flight on the caller's stream
+        self.S.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(self.S):
+            self.cols[l].copy_(torch.as_tensor(cols, dtype=torch.int32))
+            if l == 0:
+                self.K0[:, :, : self.pool_cap].copy_(K)
+                self.V0[:, :, : self.pool_cap].copy_(V)
+            else:
+                # the partial key cache: the chosen columns of every key, token index last
+                ci = self.cols[l].long()
+                part = torch.stack([K[:, h][..., ci[h]] for h in range(self.H)], dim=1)
+                self.Kpart[l].zero_()
+                self.Kpart[l][..., : self.pool_cap].copy_(part.transpose(-1, -2))
+                if self.rope:
+                    self.Wq[l].copy_(Wq)
+                    self.A_cols[l].copy_(A_cols)
+                else:
+                    self.Wq_part[l].copy_(Wq_part)
+            ig.ig_pool_write(self.pool, self.S, l, K.contiguous(), V.contiguous())
+        self.S.synchronize()
+
+    def prefill(self, n_tokens):
+        """Marks n_tokens prompt tokens resident in every pool (their KV is already loaded)."""
+        ig.ig_pool_prefill(self.pool, n_tokens)
+        self.filled = min(n_tokens, self.pool_cap)
+
+    # ------------------------------------------------------------------ decode
+    def _fold_pending(self):
+        if self._pending is None:
+            return
+        i, ev = self._pending
+        ev.synchronize()
+        ig.ig_pool_step(self.pool, self.used_host[i], self.Lcap, None)
+        self._pending = None
+
+    def step(self, x, q, k_new, v_new, out, positions=None):
+        """One decode step of every layer on device tensors; returns at once (asynchronous).
+
+        x [L, B, D], q / k_new / v_new [L, B, H, d] fp16; out [L, B, H, d] fp32.
+        positions [B] (RoPE): the current token's position; defaults to the resident count.
+        The step runs on the decoder's stream ``S`` after the caller's current stream's work;
+        read ``out`` after ``finish()`` or after making your stream wait for ``S``.
+        """
+        i = self.t % 2
+        full = ig.ig_pool_full(self.pool)
+        if full:
+            self._fold_pending()
+        L_now = self.filled
+        slots = self.slot_host[i]
+        ig.ig_pool_step(self.pool, None, self.Lcap, slots.numpy())
+        self.filled = min(self.filled + 1, self.pool_cap)
+        self.L_host[i].fill_(L_now)
+        if positions is None:
+            self.pos_host[i].fill_(L_now)
+        else:
+            self.pos_host[i].copy_(torch.as_tensor(positions, dtype=torch.int32))
+        self.S.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(self.S):
+            self.L_dev.copy_(self.L_host[i], non_blocking=True)
+            self.pos_dev.copy_(self.pos_host[i], non_blocking=True)
+            self.slot_dev.copy_(slots, non_blocking=True)
+        io = ig.StepIO(x.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), self.L_dev.data_ptr(),
+                       self.pos_dev.data_ptr(), self.slot_dev.data_ptr(), out.data_ptr())
+        ig.ig_decode_step(self.handle, io, self.S, self.G)
+        with torch.cuda.stream(self.S):
+            self.used_host[i].copy_(self.used, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(self.S)
+        if not full:
+            self._fold_pending()  # step t-1's use, while step t runs
+        self._pending = (i, ev)
+        self.t += 1
+        return L_now
+
+    def stage_ms(self, steps_back=0):
+        """Per-stage device times of a recent step (see ig_decoder_stage_ms); waits for it."""
+        return ig.ig_decoder_stage_ms(self.handle, steps_back)
+
+    def finish(self):
+        self.S.synchronize()
+        self._fold_pending()
+
+    def close(self):
+        if getattr(self, "handle", None):
+            self.S.synchronize()
+            ig.ig_decoder_destroy(self.handle)
+            self.handle = None
+        if getattr(self, "pool", None):
+            ig.ig_pool_destroy(self.pool)
+            self.pool = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def pool_counters(dec: Decoder, layer: int, b: int) -> np.ndarray:
+    out = np.zeros(dec.pool_cap, dtype=np.uint8)
+    ig.ig_pool_counters(dec.pool, layer, b, out)
+    return out

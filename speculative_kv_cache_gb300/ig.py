@@ -239,3 +239,88 @@ def pool_layer_view(pool, layer, B, H, cap, d):
     K = np.ctypeslib.as_array(C.cast(kp, C.POINTER(C.c_uint16)), shape=(n,)).view(np.float16)
     V = np.ctypeslib.as_array(C.cast(vp, C.POINTER(C.c_uint16)), shape=(n,)).view(np.float16)
     return K.reshape(B, H, cap, d), V.reshape(B, H, cap, d)
+
+
+# ---------------------------------------------------------------------------------------
+# Decoder (one step over every layer) and the batched pool manager
+# ---------------------------------------------------------------------------------------
+class DecoderConfig(C.Structure):
+    _fields_ = [("layers", _i), ("B", _i), ("H", _i), ("d", _i), ("D", _i), ("k", _i), ("Lcap", _i),
+                ("policy", _i), ("alpha", _f), ("cap_frac", _f), ("score_scale", _f),
+                ("rope_theta", _f), ("gather_ctas", _i), ("stage_timing", _i)]
+
+
+class DecoderBuffers(C.Structure):
+    _fields_ = [("Wq_part", C.POINTER(_vp)), ("Wq", C.POINTER(_vp)), ("A_cols", C.POINTER(_vp)),
+                ("Kpart", C.POINTER(_vp)), ("cols", C.POINTER(_vp)), ("K0", _vp), ("V0", _vp),
+                ("scores", _vp), ("idx", _vp), ("cnt", _vp), ("used", _vp), ("Kg", _vp), ("Vg", _vp),
+                ("workspace", _vp), ("workspace_bytes", _sz)]
+
+
+class StepIO(C.Structure):
+    _fields_ = [("x", _vp), ("q", _vp), ("k_new", _vp), ("v_new", _vp), ("L_valid", _vp),
+                ("positions", _vp), ("slot", _vp), ("out", _vp)]
+
+
+_sig("ig_decoder_workspace_bytes", _sz, C.POINTER(DecoderConfig))
+_sig("ig_decoder_create", _i, C.POINTER(DecoderConfig), C.POINTER(DecoderBuffers), _vp, C.POINTER(_vp))
+_sig("ig_decoder_destroy", _i, _vp)
+_sig("ig_decode_step", _i, _vp, C.POINTER(StepIO), _vp, _vp)
+_sig("ig_decoder_stage_ms", _i, _vp, _i, C.POINTER(_f), C.POINTER(_i))
+_sig("ig_pool_update", _i, _vp, _i, _i, _vp)
+_sig("ig_pool_prefill", _i, _vp, _i, _vp)
+_sig("ig_pool_step", _i, _vp, _vp, _i, _vp)
+_sig("ig_pool_full", _i, _vp, C.POINTER(_i))
+_sig("ig_launch_count", C.c_uint64)
+
+
+def _ptr_array(items):
+    arr = (_vp * len(items))(*[_p(t) for t in items])
+    return arr
+
+
+def ig_decoder_workspace_bytes(cfg: DecoderConfig) -> int:
+    return _lib.ig_decoder_workspace_bytes(C.byref(cfg))
+
+
+def ig_decoder_create(cfg: DecoderConfig, bufs: DecoderBuffers, pool) -> int:
+    h = _vp()
+    _ok(_lib.ig_decoder_create(C.byref(cfg), C.byref(bufs), pool, C.byref(h)), "ig_decoder_create")
+    return h.value
+
+
+def ig_decoder_destroy(dec):
+    _ok(_lib.ig_decoder_destroy(dec), "ig_decoder_destroy")
+
+
+def ig_decode_step(dec, io: StepIO, stream, side_stream):
+    _ok(_lib.ig_decode_step(dec, C.byref(io), _s(stream), _s(side_stream)), "ig_decode_step")
+
+
+def ig_decoder_stage_ms(dec, steps_back=0):
+    ms = (_f * 3)()
+    cnt = (_i * 3)()
+    _ok(_lib.ig_decoder_stage_ms(dec, steps_back, ms, cnt), "ig_decoder_stage_ms")
+    return list(ms), list(cnt)
+
+
+def ig_pool_update(pool, layer, b, used):
+    _ok(_lib.ig_pool_update(pool, layer, b, _p(used)), "ig_pool_update")
+
+
+def ig_pool_prefill(pool, n_tokens, slots_out=None):
+    _ok(_lib.ig_pool_prefill(pool, n_tokens, _p(slots_out)), "ig_pool_prefill")
+
+
+def ig_pool_step(pool, used, Lcap, slots_out):
+    _ok(_lib.ig_pool_step(pool, _p(used), Lcap, _p(slots_out)), "ig_pool_step")
+
+
+def ig_pool_full(pool) -> bool:
+    f = _i(0)
+    _ok(_lib.ig_pool_full(pool, C.byref(f)), "ig_pool_full")
+    return bool(f.value)
+
+
+def ig_launch_count() -> int:
+    return _lib.ig_launch_count()
