@@ -109,6 +109,26 @@ ig_status ig_speculate(void* stream, int B, int D, int H, int k, int Lcap,
                        const int32_t* L_valid, float score_scale, float* scores,
                        float* q_part, void* workspace, size_t workspace_bytes);
 
+/* ig_speculate without a workspace argument, for callers that cannot allocate device memory
+ * (the paper has no counterpart; this is an interface convenience).  Some embedders hand
+ * all device memory to their own allocator up front, so a stray cudaMalloc either fails or
+ * breaks their accounting, and some cannot afford the implicit synchronisation an allocation
+ * may bring.  Here the projection's split partial sums live in a 4 MiB array inside the
+ * library (a file-scope __device__ array, held on every GPU that loads the library until the
+ * process exits); nothing is allocated, by this call or by anything it calls.
+ *   - Limit: ig_speculate_workspace_bytes(B, D, H, k) must be <= 4 MiB (4194304 bytes), else
+ *     IG_ERR_CAPACITY with a message; e.g. B = 16, D = 7168, H * k = 2128 needs 2.2 MB.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     and caches it; make that first call before any stream capture.
+ *   - Every call on a device shares the one array and leaves its partial sums there (each call
+ *     overwrites all it reads, so nothing needs clearing); calls whose work overlaps on the GPU
+ *     (different streams, or other threads) race on it and must be serialised by the caller.
+ * Arguments and results are those of ig_speculate. */
+ig_status ig_speculate_static(void* stream, int B, int D, int H, int k, int Lcap,
+                              const uint16_t* x, const uint16_t* Wq_part, const uint16_t* Kpart,
+                              const int32_t* L_valid, float score_scale, float* scores,
+                              float* q_part);
+
 /* RoPE models (Llama-2): the skew has to follow the rotary embedding, so the partial query
  * is q~p_h = RoPE_p(x W_Q,h) A_h[:, S_h] (the full per-head query, rotated at the current
  * position, then projected on the chosen skewed columns).

@@ -5,6 +5,8 @@
 //   K2  speculated scores         s = scale q~p (K~p)^T, partial-key rows staged by bulk TMA
 #include <math.h>
 
+#include <mutex>
+
 #include "ig_common.cuh"
 
 namespace ig {
@@ -343,4 +345,61 @@ extern "C" ig_status ig_speculate_rope(void* stream, int B, int D, int H, int d,
                                                             positions, (double)rope_theta, qp);
   IG_CHECK_LAUNCH("rope epilogue launch");
   return launch_k2(s, qp, 1, B, H, k, Kpart, L_valid, Lcap, score_scale, scores, q_part);
+}
+
+// ---------------------------------------------------------------------------------------
+// ig_speculate_static: ig_speculate for callers that must not allocate device memory.
+// The split-K partial sums live in this file-scope array instead of a caller workspace.
+// The array's name is only a host-side stand-in in host code: its device address is looked
+// up once per device with cudaGetSymbolAddress and handed to the kernels.
+// ---------------------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kStaticScratchBytes = 4u << 20;  // 4 MiB on every device that loads the library
+static __device__ __align__(256) float g_speculate_scratch[kStaticScratchBytes / sizeof(float)];
+
+std::mutex g_static_mu;
+float* g_static_ptr[64] = {};
+
+// Device address of the scratch array on the current device (looked up on first use).
+ig_status static_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "ig_speculate_static: current device");
+  if (dev < 0 || dev >= 64) return fail(IG_ERR_INVALID, "ig_speculate_static: device %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_speculate_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "ig_speculate_static: scratch address");
+    g_static_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return IG_OK;
+}
+
+}  // namespace
+
+extern "C" ig_status ig_speculate_static(void* stream, int B, int D, int H, int k, int Lcap,
+                                         const uint16_t* x, const uint16_t* Wq_part,
+                                         const uint16_t* Kpart, const int32_t* L_valid,
+                                         float score_scale, float* scores, float* q_part) {
+  float* part = nullptr;
+  ig_status st = static_scratch(&part);
+  if (st != IG_OK) return st;
+  st = check_common(B, D, H, k, Lcap, x, Kpart, L_valid, scores, part);
+  if (st != IG_OK) return st;
+  IG_REQUIRE(Wq_part, "null Wq_part");
+  const size_t need = ig_speculate_workspace_bytes(B, D, H, k);
+  if (need > kStaticScratchBytes)
+    return fail(IG_ERR_CAPACITY,
+                "ig_speculate_static needs %zu bytes of scratch for B=%d, H*k=%d, D=%d; its static "
+                "scratch holds %zu bytes (use ig_speculate with a workspace)",
+                need, B, H * k, D, kStaticScratchBytes);
+  cudaStream_t s = as_stream(stream);
+  const int S = proj_splits(D);
+  st = launch_k1(s, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(Wq_part),
+                 part, B, D, H * k, S);
+  if (st != IG_OK) return st;
+  return launch_k2(s, part, S, B, H, k, Kpart, L_valid, Lcap, score_scale, scores, q_part);
 }

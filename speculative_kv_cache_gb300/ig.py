@@ -60,6 +60,7 @@ _sig("ig_skew_weights", _i, _i, _i, _i, _f, _f, _vp, _i, _vp, _vp, _vp, _i, _vp,
      _vp, _vp, _i)
 _sig("ig_speculate_workspace_bytes", _sz, _i, _i, _i, _i)
 _sig("ig_speculate", _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _sz)
+_sig("ig_speculate_static", _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp)
 _sig("ig_speculate_rope_workspace_bytes", _sz, _i, _i, _i, _i, _i)
 _sig("ig_speculate_rope", _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
      _vp, _vp, _vp, _sz)
@@ -148,6 +149,14 @@ def ig_speculate(stream, B, D, H, k, Lcap, x, Wq_part, Kpart, L_valid, score_sca
     _ok(_lib.ig_speculate(_s(stream), B, D, H, k, Lcap, _p(x), _p(Wq_part), _p(Kpart), _p(L_valid),
                           score_scale, _p(scores), _p(q_part), _p(workspace), workspace_bytes),
         "ig_speculate")
+
+
+def ig_speculate_static(stream, B, D, H, k, Lcap, x, Wq_part, Kpart, L_valid, score_scale, scores,
+                        q_part):
+    """ig_speculate with the library's own static scratch: no workspace, nothing allocated."""
+    _ok(_lib.ig_speculate_static(_s(stream), B, D, H, k, Lcap, _p(x), _p(Wq_part), _p(Kpart),
+                                 _p(L_valid), score_scale, _p(scores), _p(q_part)),
+        "ig_speculate_static")
 
 
 def ig_speculate_rope_workspace_bytes(B, D, H, d, k) -> int:
