@@ -47,7 +47,9 @@ def parse_args(argv=None):
     p.add_argument("--gather-ctas", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-layers", type=int, default=0, help="oracle sample: layers (0 = all)")
+    p.add_argument("--cpu-layers", type=int, default=0, help="oracle sample: layers (0 = default)")
+    p.add_argument("--layers", type=int, default=0,
+                   help="override the workload's layer count (small cases for profiling)")
     return p.parse_args(argv)
 
 
@@ -441,7 +443,9 @@ def run_ours(args, w, alpha):
 def main(argv=None):
     args = parse_args(argv)
     w = synth.WORKLOADS[args.workload]
-    alpha = args.alpha if args.alpha is not None else (4.0 if 4.0 in w.alphas else w.alphas[0])
+    if args.layers:
+        w = synth.scaled(w, layers=args.layers)
+    alpha =args.alpha if args.alpha is not None else (4.0 if 4.0 in w.alphas else w.alphas[0])
     if args.impl == "reference":
         return run_reference(args, w, alpha)
     return run_ours(args, w, alpha)

@@ -394,7 +394,8 @@ class CounterPool:
             slot = self.filled
             self.filled += 1
         else:
-            slot = min(range(self.cap), key=lambda s: (self.counter[s], self.seq[s], s))
+            # smallest counter, then oldest insertion, then lowest slot (lexsort: last key first)
+            slot = int(np.lexsort((np.arange(self.cap), self.seq, self.counter))[0])
         self.counter[slot] = 0
         self.seq[slot] = self.next_seq
         self.next_seq += 1

@@ -6,6 +6,11 @@
 // a row is 256 B and 16 lanes fetch it together; each lane keeps 2 x kUnroll loads in flight
 // (keys and values).  The grid is kept small (a fraction of the SMs): the host link saturates
 // with a few dozen CTAs, and the rest of the GPU stays free for the compute stream.
+//
+// Balance: the rows to fetch, over all (b, h) units, are numbered 0..R-1 in unit order (an
+// exclusive scan of the per-unit counts, which every CTA computes in shared memory), and CTA c
+// fetches rows [c R / G, (c + 1) R / G).  Every CTA therefore moves the same number of bytes,
+// whatever the spread of the per-head counts, without atomics or scratch memory.
 #include "ig_common.cuh"
 #include "pool_impl.h"
 
@@ -14,50 +19,96 @@ namespace {
 
 constexpr int kGatherThreads = 256;
 constexpr int kUnroll = 4;
+constexpr int kMaxGatherUnits = 32768;  // (units + 1) ints of shared memory: 128 KB
 
 __global__ void __launch_bounds__(kGatherThreads) k4_gather(
     const uint4* __restrict__ Kp, const uint4* __restrict__ Vp, int units, int cap, int vpr,
     int Lcap, const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt,
     uint4* __restrict__ Kg, uint4* __restrict__ Vg, int* err) {
-  const int rpp = kGatherThreads / vpr;  // rows fetched in parallel per CTA
-  const int v = threadIdx.x % vpr, rg = threadIdx.x / vpr;
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+  extern __shared__ int pre[];  // pre[u] = rows of units < u; pre[units] = R
+  __shared__ int wsum[kGatherThreads / 32];
+  // --- exclusive scan of the clamped counts, in chunks of `per` units per thread
+  const int per = (units + kGatherThreads - 1) / kGatherThreads;
+  const int u0 = threadIdx.x * per;
+  int local = 0;
+  for (int u = u0; u < min(units, u0 + per); ++u) {
     int c = cnt[u];
     if (c < 0 || c > Lcap) {
-      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_INDEX);
+      raise_error(err, IG_DEVERR_INDEX);
       c = c < 0 ? 0 : Lcap;
     }
-    const int32_t* ii = idx + (size_t)u * Lcap;
-    const uint4* ksrc = Kp + (size_t)u * cap * vpr;
-    const uint4* vsrc = Vp + (size_t)u * cap * vpr;
-    uint4* kdst = Kg + (size_t)u * Lcap * vpr;
-    uint4* vdst = Vg + (size_t)u * Lcap * vpr;
-    for (int j = rg; j < c; j += rpp * kUnroll) {
-      uint4 kv[kUnroll], vv[kUnroll];
-      int slot[kUnroll];
+    pre[u + 1] = c;  // temporarily the count
+    local += c;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = local;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int base = 0;
+  for (int w = 0; w < warp; ++w) base += wsum[w];
+  int run = base + incl - local;  // rows before this thread's chunk
+  if (threadIdx.x == 0) pre[0] = 0;
+  for (int u = u0; u < min(units, u0 + per); ++u) {
+    const int c = pre[u + 1];
+    run += c;
+    pre[u + 1] = run;
+  }
+  __syncthreads();
+  const long long R = pre[units];
+  const int r0 = (int)(R * blockIdx.x / gridDim.x);
+  const int r1 = (int)(R * (blockIdx.x + 1) / gridDim.x);
+
+  // --- fetch rows [r0, r1): row-group rg takes rows r0 + rg, r0 + rg + rpp, ...
+  const int rpp = kGatherThreads / vpr;
+  const int v = threadIdx.x % vpr, rg = threadIdx.x / vpr;
+  int u = 0;  // unit of the row-group's current row; rows only grow, so u only advances
+  {
+    int lo = 0, hi = units;  // first unit whose end is past r0 (upper bound of r0 in pre)
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid + 1] <= r0) lo = mid + 1; else hi = mid;
+    }
+    u = lo;
+  }
+  for (int r = r0 + rg; r < r1; r += rpp * kUnroll) {
+    uint4 kv[kUnroll], vv[kUnroll];
+    int unit[kUnroll], row[kUnroll], slot[kUnroll];
 #pragma unroll
-      for (int q = 0; q < kUnroll; ++q) {
-        const int jj = j + q * rpp;
-        slot[q] = (jj < c) ? ii[jj] : -1;
-        if (jj < c && (slot[q] < 0 || slot[q] >= cap)) {
+    for (int q = 0; q < kUnroll; ++q) {
+      const int rr = r + q * rpp;
+      slot[q] = -1;
+      unit[q] = 0;
+      row[q] = 0;
+      if (rr < r1) {
+        while (pre[u + 1] <= rr) ++u;
+        unit[q] = u;
+        row[q] = rr - pre[u];
+        const int sl = idx[(size_t)u * Lcap + row[q]];
+        if (sl < 0 || sl >= cap) {
           raise_error(err, IG_DEVERR_INDEX);
-          slot[q] = -1;
+        } else {
+          slot[q] = sl;
         }
       }
+    }
 #pragma unroll
-      for (int q = 0; q < kUnroll; ++q) {
-        if (slot[q] >= 0) {
-          kv[q] = ld_nc_v4(ksrc + (size_t)slot[q] * vpr + v);
-          vv[q] = ld_nc_v4(vsrc + (size_t)slot[q] * vpr + v);
-        }
+    for (int q = 0; q < kUnroll; ++q) {
+      if (slot[q] >= 0) {
+        const size_t src = ((size_t)unit[q] * cap + slot[q]) * vpr + v;
+        kv[q] = ld_nc_v4(Kp + src);
+        vv[q] = ld_nc_v4(Vp + src);
       }
+    }
 #pragma unroll
-      for (int q = 0; q < kUnroll; ++q) {
-        const int jj = j + q * rpp;
-        if (slot[q] >= 0) {
-          kdst[(size_t)jj * vpr + v] = kv[q];
-          vdst[(size_t)jj * vpr + v] = vv[q];
-        }
+    for (int q = 0; q < kUnroll; ++q) {
+      if (slot[q] >= 0) {
+        const size_t dst = ((size_t)unit[q] * Lcap + row[q]) * vpr + v;
+        Kg[dst] = kv[q];
+        Vg[dst] = vv[q];
       }
     }
   }
@@ -80,13 +131,21 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
   const int vpr = d * 2 / 16;
   IG_REQUIRE(kGatherThreads % vpr == 0, "unsupported d %d", d);
   const int units = B * H;
-  int grid = max_ctas > 0 ? max_ctas : sm_count() / 2;
-  if (grid > units) grid = units;
+  IG_REQUIRE(units <= kMaxGatherUnits, "B*H = %d exceeds %d", units, kMaxGatherUnits);
+  IG_REQUIRE((long long)units * Lcap < (1ll << 31), "B*H*Lcap must stay below 2^31 rows");
+  // a quarter of the SMs (38 on a GB300) already moves ~185 GB/s over the host link while
+  // the compute stream runs beside it; more CTAs only slow that stream down
+  int grid = max_ctas > 0 ? max_ctas : sm_count() / 4;
   if (grid < 1) grid = 1;
+  const size_t smem = (size_t)(units + 1) * sizeof(int);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k4_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "gather smem attribute");
+  }
   const size_t layer_elems = (size_t)B * H * pool->cap * d;
   const uint4* Kp = reinterpret_cast<const uint4*>(pool->Kdev + (size_t)layer * layer_elems);
   const uint4* Vp = reinterpret_cast<const uint4*>(pool->Vdev + (size_t)layer * layer_elems);
-  k4_gather<<<grid, kGatherThreads, 0, as_stream(stream)>>>(
+  k4_gather<<<grid, kGatherThreads, smem, as_stream(stream)>>>(
       Kp, Vp, units, pool->cap, vpr, Lcap, idx, cnt, reinterpret_cast<uint4*>(Kg),
       reinterpret_cast<uint4*>(Vg), error_word());
   IG_CHECK_LAUNCH("gather launch");

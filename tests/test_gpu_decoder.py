@@ -1,10 +1,10 @@
 """The pipelined multi-layer decode step (ig_decode_step via Decoder) against the oracle.
 
-Several decode steps of a small OPT-shaped model (and a RoPE, Llama-shaped one) run through
-the native runtime; the oracle replays every layer of every step on its own copy of the pool
-and partial key caches.  Layer outputs must agree within 2e-3; a (sequence, head) whose oracle
-scores put a token within 1e-3 of the threshold is compared only for validity (the stated
-exemption), and such heads must be rare.  With a capped pool, the slots the runtime evicts
+Several decode steps of small OPT-shaped and Llama-shaped models run through the native
+runtime; the oracle replays every layer of every step on its own copy of the pool and partial
+key caches.  The GPU's index sets must equal the oracle's except tokens whose oracle score lies
+within 1e-3 of the threshold (the stated exemption); layer outputs must agree within 2e-3 with
+the oracle's attention over the GPU's sets.  With a capped pool, the slots the runtime evicts
 must be the ones the oracle's counter pool picks from the same use flags.
 """
 import math
@@ -16,6 +16,7 @@ torch = pytest.importorskip("torch")
 
 from oracle import infinigen as ora  # noqa: E402
 from speculative_kv_cache_gb300 import synth  # noqa: E402
+from gpu_util import index_sets_ok  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -41,17 +42,6 @@ def _layer_data(w, l, cap, rope):
         Wq = synth.normal_f16(synth.rng(w.name, "Wq", l), (w.hidden, w.heads * w.head_dim), w.w_std)
         return dict(K=K, V=V, cols=cols, A=A.astype(np.float32), Wq=Wq)
     return dict(K=K, V=V, cols=cols, Wqp=synth.skewed_partial_weight(w, l))
-
-
-def _band_heads(s, L, alpha, band=1e-3):
-    out = set()
-    B, H, _ = s.shape
-    for b in range(B):
-        for h in range(H):
-            x = s[b, h, :L]
-            if np.any(np.abs(x - (x.max() - alpha)) <= band):
-                out.add((b, h))
-    return out
 
 
 def _run(mods, w, steps, rope=False, check_slots=False):
@@ -107,6 +97,7 @@ def _run(mods, w, steps, rope=False, check_slots=False):
                 assert np.array_equal(dec.slot_host[s % 2].numpy(), want_slots)
             used = dec.used_host[s % 2].numpy().copy()
             cnt = dec.cnt.cpu().numpy()
+            idx_buf = dec.idx.cpu().numpy()
             o = out.cpu().numpy()
             Lv = np.full(w.batch, L_now, dtype=np.int32)
             # layer 0: dense attention over the resident tokens plus the new one
@@ -120,20 +111,21 @@ def _run(mods, w, steps, rope=False, check_slots=False):
                     qp = ora.partial_query(x[l - 1], dd["Wqp"], w.heads, w.k)
                 Kpart = ora.partial_key_cache(oK[l], dd["cols"])
                 sc = ora.speculate(qp, Kpart, Lv, scale)
-                idx, oc, oused = ora.select(sc, Lv, alpha)
-                Kg, Vg = ora.gather(oK[l], oV[l], idx, Lcap)
-                ol = ora.attend(q[l], Kg, Vg, oc, scale, kn[l], vn[l])
-                band = _band_heads(sc, L_now, alpha)
+                # the GPU's own index sets (both gather buffers survive a step of <= 3 layers):
+                # equal to the oracle's except tokens within 1e-3 of the threshold
+                gi = idx_buf[l % 2]
+                exempt = index_sets_ok(gi, cnt[l], sc, Lv, alpha)
+                skipped += exempt
+                sets = [[gi[b, h, :cnt[l, b, h]] for h in range(w.heads)] for b in range(w.batch)]
+                checked += int(cnt[l].sum())
+                Kg, Vg = ora.gather(oK[l], oV[l], sets, Lcap)
+                ol = ora.attend(q[l], Kg, Vg, cnt[l], scale, kn[l], vn[l])
+                assert np.abs(o[l] - ol).max() <= 2e-3
+                want_used = np.zeros((w.batch, Lcap), dtype=np.uint8)
                 for b in range(w.batch):
                     for h in range(w.heads):
-                        if (b, h) in band:
-                            skipped += 1
-                            continue
-                        checked += 1
-                        assert cnt[l, b, h] == oc[b, h]
-                        assert np.abs(o[l, b, h] - ol[b, h]).max() <= 2e-3
-                    if not any((b, h) in band for h in range(w.heads)):
-                        assert np.array_equal(used[l, b, :L_now], oused[b, :L_now])
+                        want_used[b, sets[b][h]] = 1
+                assert np.array_equal(used[l, :, :L_now], want_used[:, :L_now])
             # the oracle appends the new token at the slots the pool chose
             for l in range(w.layers):
                 for b in range(w.batch):
@@ -141,7 +133,7 @@ def _run(mods, w, steps, rope=False, check_slots=False):
                     oK[l][b, :, sl] = kn[l, b]
                     oV[l][b, :, sl] = vn[l, b]
             prev_used = used
-        assert checked > 0 and skipped <= 0.02 * (checked + skipped)
+        assert checked > 0 and skipped <= 0.01 * checked
         # the device-side appends landed in the pinned pool and the partial caches
         for l in range(1, w.layers):
             Kp, Vp = ig.pool_layer_view(dec.pool, l, w.batch, w.heads, cap, w.head_dim)
@@ -153,7 +145,7 @@ def _run(mods, w, steps, rope=False, check_slots=False):
 
 
 def test_decoder_opt_shaped_steps(mods):
-    w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-opt", layers=4, batch=3, heads=6, hidden=768,
+    w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-opt", layers=3, batch=3, heads=6, hidden=768,
                      prompt=300, gen=8)
     _run(mods, w, steps=3)
 
@@ -169,3 +161,11 @@ def test_decoder_rope_steps(mods):
     w = synth.scaled(synth.WORKLOADS["llama-2-7b"], name="dec-rope", layers=3, batch=2, heads=4,
                      hidden=512, prompt=260, gen=8)
     _run(mods, w, steps=2, rope=True)
+
+
+def test_decoder_llama13b_width_capped_pool(mods):
+    """Llama-2-13B-shaped layers at full width and context (pool capped at 60 %, RoPE):
+    eviction happens at every step."""
+    w = synth.scaled(synth.WORKLOADS["llama-2-13b"], name="dec-13b", layers=3)
+    assert w.pool_cap == 2458 and w.pool_cap < w.prompt
+    _run(mods, w, steps=3, rope=True, check_slots=True)

@@ -310,3 +310,54 @@ def test_layer_step_end_to_end(ig, pools, name):
     if name == "opt-30b":
         f = cnt_g.sum() / (B * H * c["L"][0])
         assert 0.005 < f < 0.15, f"planted structure should keep a few percent, got {f:.4f}"
+
+
+@functools.lru_cache(maxsize=1)
+def rope_case():
+    """One Llama-2-7B-shaped layer at full size: RoPE, context 3968 + 1, the oracle's own skew."""
+    w = synth.WORKLOADS["llama-2-7b"]
+    Lcap = 4096
+    L = np.full(w.batch, w.prompt + 1, dtype=np.int32)
+    Xs, Wq, Wk = synth.skew_inputs(w, layer=1)
+    A, _, _, _, _ = ora.skew(Xs, Wq, Wk, w.heads, w.head_dim, rope_theta=w.rope_theta)
+    K, V = synth.pool_layer(w, 1, cap=Lcap)
+    cols = synth.skewed_columns(w, 1)
+    x = synth.layer_inputs(w, step=1, layers=1)[0]
+    q, kn, vn = synth.token_inputs(w, 1, 1)
+    A_cols = np.stack([A[h][:, cols[h]] for h in range(w.heads)]).astype(np.float32)
+    return dict(w=w, Lcap=Lcap, L=L, A=A.astype(np.float32), A_cols=A_cols, Wq=Wq, K=K, V=V, cols=cols, x=x,
+                q=q, kn=kn, vn=vn, Kpart=ora.partial_key_cache(K, cols), pos=L.copy(),
+                scale=np.float32(1.0 / math.sqrt(w.head_dim)))
+
+
+@pytest.mark.parametrize("alpha", [2.0, 4.0, 6.0])
+def test_rope_layer_step_end_to_end(ig, pools, alpha):
+    c = rope_case()
+    w = c["w"]
+    B, H, d, k, D, Lcap = w.batch, w.heads, w.head_dim, w.k, w.hidden, c["Lcap"]
+    pool = _pool_for(ig, pools, c, "llama-2-7b")
+    scores = empty((B, H, Lcap), torch.float32)
+    qp = empty((B, H, k), torch.float32)
+    ws = workspace(max(ig.ig_speculate_rope_workspace_bytes(B, D, H, d, k), ig.ig_attend_workspace_bytes(B, H, d, Lcap)))
+    ig.ig_speculate_rope(None, B, D, H, d, k, Lcap, dev(c["x"]), dev(c["Wq"]), dev(c["A_cols"]), dev(c["pos"]),
+                         w.rope_theta, dev(c["Kpart"]), dev(c["L"]), float(c["scale"]), scores, qp, ws, ws.numel())
+    idx = empty((B, H, Lcap), torch.int32)
+    cnt = empty((B, H), torch.int32)
+    ig.ig_select(None, B, H, Lcap, scores, dev(c["L"]), alpha, 0, 1.0, idx, cnt, None)
+    Kg = empty((B, H, Lcap, d), torch.float16)
+    Vg = empty((B, H, Lcap, d), torch.float16)
+    ig.ig_gather_kv(None, pool, 0, B, H, d, Lcap, idx, cnt, Kg, Vg, 0)
+    out = empty((B, H, d), torch.float32)
+    ig.ig_sparse_attend(None, B, H, d, Lcap, float(c["scale"]), dev(c["q"]), Kg, Vg, cnt, dev(c["kn"]),
+                        dev(c["vn"]), out, ws, ws.numel())
+    ig.ig_check()
+    qp_o = ora.partial_query_rope(c["x"], c["Wq"], c["A"], c["cols"], c["pos"], w.rope_theta)
+    assert np.abs(host(qp) - qp_o).max() <= 1e-4 * max(1.0, np.abs(qp_o).max())
+    s_o = ora.speculate(qp_o, c["Kpart"], c["L"], c["scale"])
+    assert score_ok(host(scores), s_o, c["L"]) <= SCORE_TOL
+    idx_g, cnt_g = host(idx), host(cnt)
+    index_sets_ok(idx_g, cnt_g, s_o, c["L"], alpha)
+    sets = [[idx_g[b, h, :cnt_g[b, h]] for h in range(H)] for b in range(B)]
+    Kg_o, Vg_o = ora.gather(c["K"], c["V"], sets, Lcap)
+    o = ora.attend(c["q"], Kg_o, Vg_o, cnt_g, c["scale"], c["kn"], c["vn"])
+    assert np.abs(host(out) - o).max() <= OUT_TOL
