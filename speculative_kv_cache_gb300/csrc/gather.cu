@@ -18,7 +18,7 @@ namespace ig {
 namespace {
 
 constexpr int kGatherThreads = 256;
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;  // 8 rows x (K, V) in flight per lane: 205 GB/s alone at 38 CTAs
 constexpr int kMaxGatherUnits = 32768;  // (units + 1) ints of shared memory: 128 KB
 
 __global__ void __launch_bounds__(kGatherThreads) k4_gather(

@@ -60,7 +60,9 @@ class Decoder:
         self.slot_dev = e(layers, B, dt=i32)
         self.used_host = [torch.zeros(layers, B, Lcap, dtype=torch.uint8).pin_memory() for _ in range(2)]
         self.S = torch.cuda.Stream(self.dev)
-        self.G = torch.cuda.Stream(self.dev)
+        # the fetch stream gets the highest priority: its few CTAs are dispatched ahead of the
+        # compute stream's large grids, so the host link never waits for free SMs
+        self.G = torch.cuda.Stream(self.dev, priority=-100)
         self._keep = self._make_buffers()
         self.handle = ig.ig_decoder_create(self.cfg, self._keep[0], self.pool)
         self.filled = 0
