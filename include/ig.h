@@ -94,7 +94,8 @@ ig_status ig_skew_weights(int D, int H, int d, float ratio, float rope_theta,
  * and Step 2 (SpecScore = q~p (K~p)^T over the N+t resident tokens).
  *
  *   x        dev fp16 [B][D]          attention input of layer i-1
- *   Wq_part  dev fp16 [D][H*k]        partial query weight of layer i, head-contiguous
+ *   Wq_part  dev fp16 [H*k][D]        partial query weight of layer i, stored transposed: row
+ *                                     h*k + c holds the D weights of head h's component c
  *   Kpart    dev fp16 [B][H][k][Lcap] partial key cache of layer i, token index contiguous
  *                                     (16-byte aligned; Lcap a multiple of 8)
  *   L_valid  dev int32 [B]            resident slots per sequence (0 <= L_valid <= Lcap)
@@ -102,7 +103,8 @@ ig_status ig_skew_weights(int D, int H, int d, float ratio, float rope_theta,
  *                                     for t < L_valid[b]; -inf for L_valid[b] <= t < Lcap
  *   q_part   dev fp32 [B][H][k] out   the partial query (unscaled), or NULL
  *   workspace dev, >= ig_speculate_workspace_bytes(B, D, H, k) bytes, 256-byte aligned
- * Partial query: fp16 x fp16 products accumulated in fp32; scores in fp32. */
+ * Partial query: fp16 x fp16 products on the tensor cores (tcgen05), fp32 accumulation; scores
+ * in fp32.  D must be a multiple of 8; x and Wq_part 16-byte aligned. */
 size_t ig_speculate_workspace_bytes(int B, int D, int H, int k);
 ig_status ig_speculate(void* stream, int B, int D, int H, int k, int Lcap,
                        const uint16_t* x, const uint16_t* Wq_part, const uint16_t* Kpart,
@@ -132,7 +134,7 @@ ig_status ig_speculate_static(void* stream, int B, int D, int H, int k, int Lcap
 /* RoPE models (Llama-2): the skew has to follow the rotary embedding, so the partial query
  * is q~p_h = RoPE_p(x W_Q,h) A_h[:, S_h] (the full per-head query, rotated at the current
  * position, then projected on the chosen skewed columns).
- *   Wq       dev fp16 [D][H*d]   unskewed query weight of layer i
+ *   Wq       dev fp16 [H*d][D]   unskewed query weight of layer i, transposed (row h*d + j)
  *   A_cols   dev fp32 [H][d][k]  A_h[:, S_h]
  *   positions dev int32 [B]      position of the current token of each sequence
  * Other arguments as ig_speculate; workspace >= ig_speculate_rope_workspace_bytes(). */
@@ -278,8 +280,8 @@ typedef struct {
 } ig_decoder_config;
 
 typedef struct {
-  const uint16_t* const* Wq_part;  /* [layers] -> dev fp16 [D][H*k]       (no RoPE)        */
-  const uint16_t* const* Wq;       /* [layers] -> dev fp16 [D][H*d]       (RoPE)           */
+  const uint16_t* const* Wq_part;  /* [layers] -> dev fp16 [H*k][D]       (no RoPE)        */
+  const uint16_t* const* Wq;       /* [layers] -> dev fp16 [H*d][D]       (RoPE)           */
   const float* const* A_cols;      /* [layers] -> dev fp32 [H][d][k]      (RoPE)           */
   uint16_t* const* Kpart;          /* [layers] -> dev fp16 [B][H][k][Lcap] (layer 0: may be NULL) */
   const int32_t* const* cols;      /* [layers] -> dev int32 [H][k]                          */

@@ -1,6 +1,7 @@
 // Speculation for layer i from layer i-1's attention input (InfiniGen paper-graph summary,
 // section 3.4, "Decoding Stage", Steps 1-2):
-//   K1  partial query projection  q~p = x W~_Q^p       split-K, fp32 partial sums in workspace
+//   K1  partial query projection  q~p = x W~_Q^p       tcgen05 tensor cores (proj_tc.cu), split-K,
+//                                                       fp32 partial sums in workspace
 //   K1b RoPE epilogue (Llama)     q~p = RoPE(x W_Q) A[:, S]
 //   K2  speculated scores         s = scale q~p (K~p)^T, partial-key rows staged by bulk TMA
 #include <math.h>
@@ -10,12 +11,10 @@
 #include "ig_common.cuh"
 
 namespace ig {
+ig_status launch_partial_q_tc(cudaStream_t st, const __half* x, const __half* Wt, float* part, int B,
+                              int D, int N, int S, int* s_eff);
 namespace {
 
-constexpr int kK1Threads = 256;      // 8 warps
-constexpr int kK1Cols = 128;         // columns per CTA: 32 lanes x 4
-constexpr int kK1XRows = 256;        // rows of x staged in shared memory at a time
-constexpr int kK1Unroll = 4;         // W rows in flight per warp
 constexpr int kMaxSplits = 16;
 
 // Number of K-splits of the projection for a given reduction length.
@@ -24,125 +23,13 @@ inline int proj_splits(int D) {
   return s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
 }
 
-// K1: part[s][b][n] = sum_{r in split s} x[b][r] * W[r][n] for one 128-column tile, one
-// split of the reduction axis and one chunk of BT batch rows.  Lane l owns 4 consecutive
-// columns (8-byte loads of W); the 8 warps stride over rows and are summed in a fixed tree,
-// so the result is deterministic.
-template <int BT, bool VEC>
-__global__ void __launch_bounds__(kK1Threads) k1_partial_q(const __half* __restrict__ x,
-                                                           const __half* __restrict__ W,
-                                                           float* __restrict__ part, int B, int D,
-                                                           int N, int rows_per_split) {
-  __shared__ float xs[BT][kK1XRows];
-  __shared__ float red[4][BT][kK1Cols];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c0 = blockIdx.x * kK1Cols + lane * 4;
-  const int s = blockIdx.y;
-  const int b0 = blockIdx.z * BT;
-  const int nb = min(BT, B - b0);
-  const int r_begin = s * rows_per_split;
-  const int r_end = min(D, r_begin + rows_per_split);
-
-  float acc[BT][4];
-#pragma unroll
-  for (int b = 0; b < BT; ++b)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[b][j] = 0.f;
-
-  for (int rc = r_begin; rc < r_end; rc += kK1XRows) {
-    const int nr = min(kK1XRows, r_end - rc);
-    __syncthreads();
-    for (int i = threadIdx.x; i < BT * kK1XRows; i += kK1Threads) {
-      int b = i / kK1XRows, r = i % kK1XRows;
-      xs[b][r] = (b < nb && r < nr) ? __half2float(x[(size_t)(b0 + b) * D + rc + r]) : 0.f;
-    }
-    __syncthreads();
-    for (int r = warp; r < nr; r += 8 * kK1Unroll) {
-      float w[kK1Unroll][4];
-#pragma unroll
-      for (int u = 0; u < kK1Unroll; ++u) {
-        const int rr = r + u * 8;
-        if (rr < nr) {
-          const __half* src = W + (size_t)(rc + rr) * N + c0;
-          if (VEC && c0 + 3 < N) {
-            uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
-            float2 a = h2_to_f2(v.x), bq = h2_to_f2(v.y);
-            w[u][0] = a.x; w[u][1] = a.y; w[u][2] = bq.x; w[u][3] = bq.y;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 4; ++j) w[u][j] = (c0 + j < N) ? __half2float(src[j]) : 0.f;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) w[u][j] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kK1Unroll; ++u) {
-        const int rr = r + u * 8;
-        if (rr < nr) {
-#pragma unroll
-          for (int b = 0; b < BT; ++b) {
-            const float xv = xs[b][rr];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[b][j] = fmaf(xv, w[u][j], acc[b][j]);
-          }
-        }
-      }
-    }
-  }
-  // fixed-order tree over the 8 warps: (w + 4) -> w, (w + 2) -> w, 1 -> 0
-  for (int half = 4; half >= 1; half >>= 1) {
-    __syncthreads();
-    if (warp >= half && warp < 2 * half) {
-#pragma unroll
-      for (int b = 0; b < BT; ++b)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) red[warp - half][b][lane * 4 + j] = acc[b][j];
-    }
-    __syncthreads();
-    if (warp < half) {
-#pragma unroll
-      for (int b = 0; b < BT; ++b)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[b][j] += red[warp][b][lane * 4 + j];
-    }
-  }
-  if (warp == 0) {
-#pragma unroll
-    for (int b = 0; b < BT; ++b) {
-      if (b < nb) {
-        float* dst = part + ((size_t)s * B + b0 + b) * N;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (c0 + j < N) dst[c0 + j] = acc[b][j];
-      }
-    }
-  }
+// K1: the partial query projection runs on the tensor cores (proj_tc.cu); part holds S_eff
+// split partials [S_eff][B][N] of x W (W given transposed, [N][D]).
+ig_status launch_k1(cudaStream_t st, const __half* x, const __half* Wt, float* part, int B, int D,
+                    int N, int S, int* s_eff) {
+  return launch_partial_q_tc(st, x, Wt, part, B, D, N, S, s_eff);
 }
 
-template <int BT>
-ig_status launch_k1_bt(cudaStream_t st, const __half* x, const __half* W, float* part, int B,
-                       int D, int N, int S) {
-  const int rows = (D + S - 1) / S;
-  dim3 grid((N + kK1Cols - 1) / kK1Cols, S, (B + BT - 1) / BT);
-  const bool vec = (N % 4 == 0) && aligned(W, 8);
-  if (vec)
-    k1_partial_q<BT, true><<<grid, kK1Threads, 0, st>>>(x, W, part, B, D, N, rows);
-  else
-    k1_partial_q<BT, false><<<grid, kK1Threads, 0, st>>>(x, W, part, B, D, N, rows);
-  IG_CHECK_LAUNCH("partial query projection launch");
-  return IG_OK;
-}
-
-ig_status launch_k1(cudaStream_t st, const __half* x, const __half* W, float* part, int B, int D,
-                    int N, int S) {
-  if (B <= 1) return launch_k1_bt<1>(st, x, W, part, B, D, N, S);
-  if (B <= 2) return launch_k1_bt<2>(st, x, W, part, B, D, N, S);
-  if (B <= 4) return launch_k1_bt<4>(st, x, W, part, B, D, N, S);
-  if (B <= 8) return launch_k1_bt<8>(st, x, W, part, B, D, N, S);
-  return launch_k1_bt<16>(st, x, W, part, B, D, N, S);
-}
 
 // K1b: RoPE epilogue for one (b, h): q = sum of the split partials of x W_Q,h; rotate the
 // pairs (j, j + d/2) by p * theta^(-2j/d); then q~p[c] = sum_j q_rot[j] A[h][j][c].
@@ -304,10 +191,10 @@ extern "C" ig_status ig_speculate(void* stream, int B, int D, int H, int k, int 
   if (workspace_bytes < need)
     return fail(IG_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
   cudaStream_t s = as_stream(stream);
-  const int S = proj_splits(D);
+  int S = proj_splits(D);
   float* part = static_cast<float*>(workspace);
   st = launch_k1(s, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(Wq_part),
-                 part, B, D, H * k, S);
+                 part, B, D, H * k, S, &S);
   if (st != IG_OK) return st;
   return launch_k2(s, part, S, B, H, k, Kpart, L_valid, Lcap, score_scale, scores, q_part);
 }
@@ -334,12 +221,12 @@ extern "C" ig_status ig_speculate_rope(void* stream, int B, int D, int H, int d,
   if (workspace_bytes < need)
     return fail(IG_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
   cudaStream_t s = as_stream(stream);
-  const int S = proj_splits(D);
+  int S = proj_splits(D);
   float* part = static_cast<float*>(workspace);
   float* qp = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                        round_up((size_t)S * B * H * d * sizeof(float), 256));
   st = launch_k1(s, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(Wq), part,
-                 B, D, H * d, S);
+                 B, D, H * d, S, &S);
   if (st != IG_OK) return st;
   k1b_rope_project<<<B * H, 128, 2 * d * sizeof(float), s>>>(part, S, B, H, d, k, A_cols,
                                                             positions, (double)rope_theta, qp);
@@ -397,9 +284,9 @@ extern "C" ig_status ig_speculate_static(void* stream, int B, int D, int H, int 
                 "scratch holds %zu bytes (use ig_speculate with a workspace)",
                 need, B, H * k, D, kStaticScratchBytes);
   cudaStream_t s = as_stream(stream);
-  const int S = proj_splits(D);
+  int S = proj_splits(D);
   st = launch_k1(s, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(Wq_part),
-                 part, B, D, H * k, S);
+                 part, B, D, H * k, S, &S);
   if (st != IG_OK) return st;
   return launch_k2(s, part, S, B, H, k, Kpart, L_valid, Lcap, score_scale, scores, q_part);
 }

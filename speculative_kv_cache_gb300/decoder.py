@@ -40,8 +40,8 @@ class Decoder:
                                     float(rope_theta), int(gather_ctas), int(bool(stage_timing)))
         # per-layer state: partial query weight (or full W_Q and A[:, S] for RoPE), columns,
         # partial key cache; layer 0 keeps its full KV in HBM instead
-        self.Wq_part = [None] + [e(D, H * k) for _ in range(1, layers)] if not self.rope else None
-        self.Wq = [None] + [e(D, H * d) for _ in range(1, layers)] if self.rope else None
+        self.Wq_part = [None] + [e(H * k, D) for _ in range(1, layers)] if not self.rope else None
+        self.Wq = [None] + [e(H * d, D) for _ in range(1, layers)] if self.rope else None
         self.A_cols = [None] + [e(H, d, k, dt=torch.float32) for _ in range(1, layers)] if self.rope else None
         self.cols = [torch.zeros(H, k, dtype=i32, device=self.dev) for _ in range(layers)]
         self.Kpart = [None] + [e(B, H, k, Lcap) for _ in range(1, layers)]
@@ -91,7 +91,8 @@ class Decoder:
     # ------------------------------------------------------------------ setup (not timed)
     def load_layer(self, l, K, V, cols, Wq_part=None, Wq=None, A_cols=None):
         """Installs layer l: skewed keys K and values V [B, H, pool_cap, d] (device fp16), the
-        chosen columns [H, k], and the partial query weight (or W_Q and A[:, S] for RoPE)."""
+        chosen columns [H, k], and the partial query weight [D, H*k] (or W_Q [D, H*d] and
+        A[:, S] [H, d, k] for RoPE); the weights are stored transposed for the tensor cores."""
         # the inputs may still be in flight on the caller's stream
         self.S.wait_stream(torch.cuda.current_stream(self.dev))
         with torch.cuda.stream(self.S):
@@ -106,10 +107,10 @@ class Decoder:
                 self.Kpart[l].zero_()
                 self.Kpart[l][..., : self.pool_cap].copy_(part.transpose(-1, -2))
                 if self.rope:
-                    self.Wq[l].copy_(Wq)
+                    self.Wq[l].copy_(Wq.t())  # stored transposed: [H*d, D]
                     self.A_cols[l].copy_(A_cols)
                 else:
-                    self.Wq_part[l].copy_(Wq_part)
+                    self.Wq_part[l].copy_(Wq_part.t())  # stored transposed: [H*k, D]
             ig.ig_pool_write(self.pool, self.S, l, K.contiguous(), V.contiguous())
         self.S.synchronize()
 

@@ -67,7 +67,7 @@ def gpu_speculate(ig, c):
     scores = empty((B, H, Lcap), torch.float32)
     qp = empty((B, H, k), torch.float32)
     ws = workspace(ig.ig_speculate_workspace_bytes(B, D, H, k))
-    ig.ig_speculate(None, B, D, H, k, Lcap, dev(c["x"]), dev(c["Wqp"]), dev(c["Kpart"]), dev(c["L"]),
+    ig.ig_speculate(None, B, D, H, k, Lcap, dev(c["x"]), dev(c["Wqp"].T), dev(c["Kpart"]), dev(c["L"]),
                     float(c["scale"]), scores, qp, ws, ws.numel())
     ig.ig_check()
     return host(scores), host(qp)
@@ -284,7 +284,7 @@ def test_layer_step_end_to_end(ig, pools, name):
     pool = _pool_for(ig, pools, c, name)
     scores = empty((B, H, Lcap), torch.float32)
     ws = workspace(max(ig.ig_speculate_workspace_bytes(B, D, H, k), ig.ig_attend_workspace_bytes(B, H, d, Lcap)))
-    ig.ig_speculate(None, B, D, H, k, Lcap, dev(c["x"]), dev(c["Wqp"]), dev(c["Kpart"]), dev(c["L"]),
+    ig.ig_speculate(None, B, D, H, k, Lcap, dev(c["x"]), dev(c["Wqp"].T), dev(c["Kpart"]), dev(c["L"]),
                     float(c["scale"]), scores, None, ws, ws.numel())
     idx = empty((B, H, Lcap), torch.int32)
     cnt = empty((B, H), torch.int32)
@@ -339,7 +339,7 @@ def test_rope_layer_step_end_to_end(ig, pools, alpha):
     scores = empty((B, H, Lcap), torch.float32)
     qp = empty((B, H, k), torch.float32)
     ws = workspace(max(ig.ig_speculate_rope_workspace_bytes(B, D, H, d, k), ig.ig_attend_workspace_bytes(B, H, d, Lcap)))
-    ig.ig_speculate_rope(None, B, D, H, d, k, Lcap, dev(c["x"]), dev(c["Wq"]), dev(c["A_cols"]), dev(c["pos"]),
+    ig.ig_speculate_rope(None, B, D, H, d, k, Lcap, dev(c["x"]), dev(c["Wq"].T), dev(c["A_cols"]), dev(c["pos"]),
                          w.rope_theta, dev(c["Kpart"]), dev(c["L"]), float(c["scale"]), scores, qp, ws, ws.numel())
     idx = empty((B, H, Lcap), torch.int32)
     cnt = empty((B, H), torch.int32)

@@ -38,7 +38,7 @@ def _case(w, Lcap, layer):
     cols = synth.skewed_columns(w, layer)
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to("cuda:0")  # noqa: E731
     L = np.array([min(w.prompt, Lcap) - (3 * b) % 17 for b in range(w.batch)], dtype=np.int32)
-    return dict(x=dev(synth.layer_inputs(w, layers=layer)[layer - 1]), W=dev(synth.skewed_partial_weight(w, layer)),
+    return dict(x=dev(synth.layer_inputs(w, layers=layer)[layer - 1]), W=dev(synth.skewed_partial_weight(w, layer).T),
                 Kpart=dev(ora.partial_key_cache(K, cols)), L=dev(L), Lh=L)
 
 
