@@ -195,6 +195,22 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def gather_traffic_bytes():
+    """DRAM bytes per launch of the fetch kernel from the committed ncu summary, or None when
+    the kernel source has changed since those counters were taken."""
+    import hashlib
+
+    prof = os.path.join(ROOT, "profiles", "k4_gather_opt30b_4layer.md")
+    src = os.path.join(ROOT, "speculative_kv_cache_gb300", "csrc", "gather.cu")
+    try:
+        vals = dict(ln.split(":", 1) for ln in open(prof).read().splitlines() if ln.startswith("traffic_"))
+        if vals["traffic_source_sha1"].strip() != hashlib.sha1(open(src, "rb").read()).hexdigest():
+            return None
+        return float(vals["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def link_peak_gbs(torch) -> float:
     """Pinned host -> device copy bandwidth (best of 5 x 1 GiB, CUDA events)."""
     n = 1 << 30
@@ -421,7 +437,9 @@ def run_ours(args, w, alpha):
             "gpu_launches": int(launches),
             "roofline": {"kernel": "k4_gather (zero-copy fetch of the selected K/V rows)",
                          "bound": "host-link", "achieved": achieved, "peak": link,
-                         "unit": "GB/s", "frac": achieved / link, "traffic": None,
+                         "unit": "GB/s", "frac": achieved / link, "traffic": gather_traffic_bytes(),
+                         "traffic_note": "DRAM read+write bytes per launch (ncu, same per-layer shape); "
+                                         "the kernel's algorithmic bytes cross the host link, not DRAM",
                          "peak_source": "measured in this run: pinned host->device copy, best of 5 x 1 GiB",
                          "algorithmic_bytes_per_launch": G_per_launch,
                          "launch_ms": gather_ms_per_launch},

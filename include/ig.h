@@ -262,9 +262,8 @@ ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B, int H, int
  * attends, layer i is speculated from layer i-1's input and its rows are fetched on a side
  * stream; layer 0 attends over its full, HBM-resident KV.  Order per step, compute stream S,
  * fetch stream G:
- *   S: dense attention + append of layer 0
  *   for l = 1..L-1:  S: speculate(l), select(l)  ->  G: gather(l) into buffer l % 2
- *                    S: wait gather(l-1), attention(l-1), append(l-1)
+ *                    S: (wait gather(l-1)) attention(l-1), append(l-1)   [l-1 = 0: dense]
  *   S: wait gather(L-1), attention(L-1), append(L-1); S finally waits for G.
  * All buffers belong to the caller; the decoder holds only events.  The per-layer pointer
  * arrays in ig_decoder_buffers are host arrays of device pointers, copied at creation. */

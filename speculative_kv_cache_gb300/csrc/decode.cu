@@ -5,12 +5,13 @@
 // its full, HBM-resident KV.
 //
 // Per step, on the compute stream S and the fetch stream G:
-//   S: dense attention of layer 0, append of layer 0
 //   for l = 1 .. L-1:
-//     S: speculate(l), select(l), record sel[l]
+//     S: speculate(l) from layer l-1's input, select(l), record sel[l]
 //     G: wait sel[l] (and att[l-2], which frees gather buffer l % 2), gather(l), record got[l]
-//     S: (l >= 2) wait got[l-1], attention(l-1), append(l-1), record att[l-1]
+//     S: (l >= 2: wait got[l-1]) attention(l-1), append(l-1), record att[l-1]
+//        (attention(0) is the dense layer-0 attention, which needs no fetch)
 //   S: wait got[L-1], attention(L-1), append(L-1)
+// so layer 1 is speculated and its fetch starts before layer 0 attends.
 #include <vector>
 
 #include "ig_common.cuh"
@@ -26,9 +27,8 @@ struct ig_decoder {
   ig_pool* pool = nullptr;
   std::vector<cudaEvent_t> ev_sel, ev_got, ev_att;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-  // stage timing (optional): [layer] start/end of gather (G), speculate+select and
-  // attention+append (S)
-  // attention+append (S); two sets, alternating by step, indexed [parity * layers + layer]
+  // stage timing (optional): start/end of gather (G), speculate+select and attention+append
+  // (S); two sets, alternating by step, indexed [parity * layers + layer]
   std::vector<cudaEvent_t> tg0, tg1, ts0, ts1, ta0, ta1;
   long long steps = 0;  // decode steps enqueued so far
 };
@@ -196,8 +196,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
   };
   dec->steps += 1;
 
-  st = timed_attend(0);
-  if (st != IG_OK) return st;
+  if (L == 1) return timed_attend(0);
   for (int l = 1; l < L; ++l) {
     float* sc = b.scores;
     int32_t* idx = b.idx + (size_t)(l & 1) * sz_scores(c);
@@ -231,14 +230,15 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     e = rec(dec->tg1, l, G);
     if (e == cudaSuccess) e = cudaEventRecord(dec->ev_got[l], G);
     if (e != cudaSuccess) return cuda_fail(e, "decode step events (gather)");
+    // layer l-1 attends while layer l is fetched (layer 0 needs no fetch)
     if (l >= 2) {
       e = cudaStreamWaitEvent(S, dec->ev_got[l - 1], 0);
       if (e != cudaSuccess) return cuda_fail(e, "decode step wait");
-      st = timed_attend(l - 1);
-      if (st != IG_OK) return st;
-      e = cudaEventRecord(dec->ev_att[l - 1], S);
-      if (e != cudaSuccess) return cuda_fail(e, "decode step events (attend)");
     }
+    st = timed_attend(l - 1);
+    if (st != IG_OK) return st;
+    e = cudaEventRecord(dec->ev_att[l - 1], S);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step events (attend)");
   }
   if (L >= 2) {
     e = cudaStreamWaitEvent(S, dec->ev_got[L - 1], 0);
