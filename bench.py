@@ -77,14 +77,20 @@ def oracle_sample(w: synth.Workload, n_layers: int, alpha: float):
     """Inputs of one decode step for ONE sequence and n_layers layers (same recipe)."""
     w1 = synth.scaled(w, batch=1)
     Lcap = w1.lcap
-    L = np.array([w1.prompt], dtype=np.int32)
+    L = np.array([min(w1.prompt, w1.pool_cap)], dtype=np.int32)  # resident slots
     xs = synth.layer_inputs(w1, step=0, layers=n_layers + 1)
     layers = []
     for l in range(1, n_layers + 1):
         K, V = synth.pool_layer(w1, l, cap=Lcap)
         cols = synth.skewed_columns(w1, l)
         q, kn, vn = synth.token_inputs(w1, l, 0)
-        layers.append((xs[l - 1], synth.skewed_partial_weight(w1, l), K, V, cols, q, kn, vn))
+        if w1.rope_theta:  # RoPE models project with the full W_Q, rotate, then take A[:, S]
+            g = np.random.default_rng(l)
+            A = np.stack([np.linalg.qr(g.standard_normal((w1.head_dim, w1.head_dim)))[0] for _ in range(w1.heads)])
+            W = (synth.normal_f16(synth.rng(w1.name, "Wq", l), (w1.hidden, w1.heads * w1.head_dim), w1.w_std), A)
+        else:
+            W = synth.skewed_partial_weight(w1, l)
+        layers.append((xs[l - 1], W, K, V, cols, q, kn, vn))
     return w1, L, layers
 
 
@@ -93,10 +99,16 @@ def time_oracle(w1, L, layers, alpha) -> float:
 
     scale = 1.0 / math.sqrt(w1.head_dim)
     t0 = time.perf_counter()
-    for x, Wqp, K, V, cols, q, kn, vn in layers:
+    for x, W, K, V, cols, q, kn, vn in layers:
         Kpart = ora.partial_key_cache(K, cols)
-        ora.decode_layer_step(x, Wqp, Kpart, L, q, K, V, H=w1.heads, k=w1.k, scale=scale, alpha=alpha,
-                              k_new=kn, v_new=vn)
+        if w1.rope_theta:
+            qp = ora.partial_query_rope(x, W[0], W[1], cols, L, w1.rope_theta)
+        else:
+            qp = ora.partial_query(x, W, w1.heads, w1.k)
+        s = ora.speculate(qp, Kpart, L, scale)
+        idx, cnt, _ = ora.select(s, L, alpha)
+        Kg, Vg = ora.gather(K, V, idx, K.shape[2])
+        ora.attend(q, Kg, Vg, cnt, scale, kn, vn)
     return time.perf_counter() - t0
 
 
@@ -342,8 +354,8 @@ def run_ours(args, w, alpha):
     dec.finish()
     ig.ig_check(dec.S)
 
-    stage = [0.0, 0.0, 0.0]
-    stage_n = [0, 0, 0]
+    stage = [0.0, 0.0, 0.0, 0.0]
+    stage_n = [0, 0, 0, 0]
     barrier()
     launches0 = ig.ig_launch_count()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -355,14 +367,14 @@ def run_ours(args, w, alpha):
                 cnt_host[i].copy_(dec.cnt, non_blocking=True)
             if i > 0:  # the previous step's stage times, while this step is queued
                 ms, n = dec.stage_ms(steps_back=1)
-                for j in range(3):
+                for j in range(4):
                     stage[j] += ms[j]
                     stage_n[j] += n[j]
             s += 1
         t1.record(dec.S)
         t1.synchronize()
         ms, n = dec.stage_ms(steps_back=0)
-        for j in range(3):
+        for j in range(4):
             stage[j] += ms[j]
             stage_n[j] += n[j]
     barrier()
@@ -389,6 +401,7 @@ def run_ours(args, w, alpha):
     t_roof_s = float(np.maximum(hbm_l / (hbm_peak * 1e9), link_l / (link * 1e9)).sum())
     t_roof_s += w.batch * w.heads * ctx.mean() * w.head_dim * 2 * 2 / (hbm_peak * 1e9)
     ms_per_step = elapsed_max / args.steps
+    hbm_gbs_alg = float(hbm_l.sum() + w.batch * w.heads * ctx.mean() * w.head_dim * 4) / (ms_per_step * 1e-3) / 1e9
 
     # end to end through host buffers (pinned): inputs up, outputs down, every step
     e2e = None
@@ -430,7 +443,10 @@ def run_ours(args, w, alpha):
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "selected_fraction": float(f),
             "link_gbs": G_total / args.steps / (ms_per_step * 1e-3) / 1e9,
-            "hbm_alg_gbs": float(hbm_l.sum() + w.batch * w.heads * ctx.mean() * w.head_dim * 4) / (ms_per_step * 1e-3) / 1e9,
+            "hbm_alg_gbs": hbm_gbs_alg,
+            "us_per_speculative_layer_step": 1000 * (ms_per_step - stage[3] / args.steps) / max(1, w.layers - 1),
+            "layer0_ms_per_step": stage[3] / args.steps,
+            "hbm_alg_frac": {"of_measured": hbm_gbs_alg / hbm_peak, "of_nominal_8000": hbm_gbs_alg / 8000.0},
             "stage_ms_per_step": {"gather": stage[0] / args.steps, "speculate_select": stage[1] / args.steps,
                                   "attend_append": stage[2] / args.steps},
             "e2e": e2e,

@@ -341,8 +341,9 @@ uint64_t ig_launch_count(void);
 
 /* Stage timing of a recent ig_decode_step (steps_back = 0: the last one, 1: the one before),
  * when the decoder was created with config.stage_timing = 1: ms_out[0] = sum of gather kernel
- * times (fetch stream), ms_out[1] = speculate + select, ms_out[2] = attention + append
- * (compute stream); counts_out[0..2] = the number of timed intervals of each.  Waits for that
+ * times (fetch stream), ms_out[1] = speculate + select, ms_out[2] = attention + append of
+ * layers 1.. (compute stream), ms_out[3] = layer 0's dense attention + append; counts_out[0..3]
+ * = the number of timed intervals of each (both arrays hold 4 entries).  Waits for that
  * step to finish; reading step t-1 while step t is queued keeps the GPU busy. */
 ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float* ms_out, int* counts_out);
 

@@ -260,8 +260,8 @@ extern "C" ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float*
   IG_REQUIRE(dec->cfg.stage_timing && dec->steps > steps_back, "stage timing is off or no such step");
   const int L = dec->cfg.layers;
   const int tset = (int)((dec->steps - 1 - steps_back) & 1) * L;
-  double sums[3] = {0, 0, 0};
-  int counts[3] = {0, 0, 0};
+  double sums[4] = {0, 0, 0, 0};
+  int counts[4] = {0, 0, 0, 0};
   auto span = [&](cudaEvent_t a, cudaEvent_t b, int which) -> cudaError_t {
     cudaError_t e = cudaEventSynchronize(b);
     if (e != cudaSuccess) return e;
@@ -276,10 +276,10 @@ extern "C" ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float*
   for (int l = 0; l < L && e == cudaSuccess; ++l) {
     if (l >= 1) e = span(dec->tg0[tset + l], dec->tg1[tset + l], 0);
     if (e == cudaSuccess && l >= 1) e = span(dec->ts0[tset + l], dec->ts1[tset + l], 1);
-    if (e == cudaSuccess) e = span(dec->ta0[tset + l], dec->ta1[tset + l], 2);
+    if (e == cudaSuccess) e = span(dec->ta0[tset + l], dec->ta1[tset + l], l == 0 ? 3 : 2);
   }
   if (e != cudaSuccess) return cuda_fail(e, "stage timing");
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < 4; ++i) {
     ms_out[i] = (float)sums[i];
     if (counts_out) counts_out[i] = counts[i];
   }

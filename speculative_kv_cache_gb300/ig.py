@@ -307,8 +307,8 @@ def ig_decode_step(dec, io: StepIO, stream, side_stream):
 
 
 def ig_decoder_stage_ms(dec, steps_back=0):
-    ms = (_f * 3)()
-    cnt = (_i * 3)()
+    ms = (_f * 4)()
+    cnt = (_i * 4)()
     _ok(_lib.ig_decoder_stage_ms(dec, steps_back, ms, cnt), "ig_decoder_stage_ms")
     return list(ms), list(cnt)
 
