@@ -45,6 +45,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="opt-30b", choices=sorted(synth.WORKLOADS))
     p.add_argument("--alpha", type=float, default=None)
     p.add_argument("--gather-ctas", type=int, default=0)
+    p.add_argument("--graph", type=int, default=1, help="1: replay each step from a CUDA graph")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-layers", type=int, default=0, help="oracle sample: layers (0 = default)")
@@ -240,13 +241,13 @@ def link_peak_gbs(torch) -> float:
     return n / (best * 1e-3) / 1e9
 
 
-def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total):
+def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False):
     from speculative_kv_cache_gb300.decoder import Decoder
 
     Lcap = w.lcap
     dec = Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=Lcap,
                   pool_cap=w.pool_cap, alpha=alpha, rope_theta=w.rope_theta, gather_ctas=gather_ctas,
-                  stage_timing=True, device=device)
+                  stage_timing=True, graph=bool(graph), device=device)
     gen = torch.Generator(device=device)
     shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
@@ -261,8 +262,9 @@ def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total):
                             for _ in range(w.heads)]).int()
         if w.rope_theta:
             Wq = (torch.randn((w.hidden, w.heads * w.head_dim), generator=gen, device=device) * w.w_std).half()
-            A = torch.linalg.qr(torch.randn((w.heads, w.head_dim, w.head_dim), generator=gen, device=device,
-                                            dtype=torch.float64))[0].float()
+            g = np.random.default_rng(1_000_003 * (l + 1))  # orthogonal skew stand-in, built on the host
+            A = torch.from_numpy(np.stack([np.linalg.qr(g.standard_normal((w.head_dim, w.head_dim)))[0]
+                                           for _ in range(w.heads)]).astype(np.float32)).to(device)
             A_cols = torch.stack([A[h][:, cols[h].long()] for h in range(w.heads)]).contiguous()
             dec.load_layer(l, K, V, cols, Wq=Wq, A_cols=A_cols)
         else:
@@ -343,7 +345,7 @@ def run_ours(args, w, alpha):
     steps_total = args.warmup + args.steps + n_e2e
     if w.prompt + steps_total > w.context:
         raise SystemExit(f"warmup + steps (+ e2e steps) must stay within the {w.gen} generated tokens")
-    dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total)
+    dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph)
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
@@ -439,7 +441,7 @@ def run_ours(args, w, alpha):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp16 storage, fp32 accumulate", "data": "synthetic (seeded, random-init weights)",
-            "config": workload_config(w, alpha),
+            "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph)),
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "selected_fraction": float(f),
             "link_gbs": G_total / args.steps / (ms_per_step * 1e-3) / 1e9,

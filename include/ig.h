@@ -316,6 +316,17 @@ ig_status ig_decoder_destroy(ig_decoder* dec);
 /* Enqueues one step on `stream` (compute) and `side_stream` (fetch); returns at once. */
 ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void* stream, void* side_stream);
 
+/* CUDA-graph form of ig_decode_step: captures the whole step (both streams, with the pointers
+ * in `io`, which must stay valid and in place) into graphs, so later steps replay it with one
+ * launch instead of a few hundred.  Capture once, then per step: update the contents of the io
+ * buffers (inputs, L_valid, slots) on `stream`, then ig_decoder_graph_launch.  Capture runs
+ * nothing on the GPU; call it after one eager ig_decode_step (which sets kernel attributes).
+ * Two graphs are kept when stage timing is on (one per timing-event set).
+ * ig_decoder_graph_launch counts the step's kernels in ig_launch_count. */
+ig_status ig_decoder_graph_capture(ig_decoder* dec, const ig_step_io* io, void* stream,
+                                   void* side_stream);
+ig_status ig_decoder_graph_launch(ig_decoder* dec, void* stream);
+
 /* Pool counters only: folds one step's use of (layer, b) into its counters, without placing a
  * token (ig_pool_evict does both).  While the pool is not full the two orders agree, so a
  * runtime may fold use in late, off the critical path. */

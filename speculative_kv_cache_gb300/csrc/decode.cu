@@ -31,6 +31,9 @@ struct ig_decoder {
   // (S); two sets, alternating by step, indexed [parity * layers + layer]
   std::vector<cudaEvent_t> tg0, tg1, ts0, ts1, ta0, ta1;
   long long steps = 0;  // decode steps enqueued so far
+  // captured steps (ig_decoder_graph_capture), one per timing-event set
+  cudaGraphExec_t graph[2] = {nullptr, nullptr};
+  uint64_t graph_kernels = 0;  // kernels in one captured step
 };
 
 namespace {
@@ -45,6 +48,11 @@ void destroy_events(ig_decoder* d) {
       if (e) cudaEventDestroy(e);
   if (d->ev_fork) cudaEventDestroy(d->ev_fork);
   if (d->ev_join) cudaEventDestroy(d->ev_join);
+  for (cudaGraphExec_t& g : d->graph)
+    if (g) {
+      cudaGraphExecDestroy(g);
+      g = nullptr;
+    }
 }
 
 }  // namespace
@@ -183,8 +191,17 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
 
   const bool timing = c.stage_timing != 0;
   const int tset = (int)(dec->steps & 1) * L;
+  // inside a stream capture the timing events are recorded as external events, which become
+  // event-record nodes of the graph (a plain record there would only express a dependency and
+  // never fire on replay); outside a capture they are plain records
+  cudaStreamCaptureStatus cap_status = cudaStreamCaptureStatusNone;
+  if (timing) {
+    e = cudaStreamIsCapturing(S, &cap_status);
+    if (e != cudaSuccess) return cuda_fail(e, "capture status");
+  }
+  const unsigned rec_flags = cap_status == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0u;
   auto rec = [&](std::vector<cudaEvent_t>& v, int l, cudaStream_t s) -> cudaError_t {
-    return timing ? cudaEventRecord(v[tset + l], s) : cudaSuccess;
+    return timing ? cudaEventRecordWithFlags(v[tset + l], s, rec_flags) : cudaSuccess;
   };
   auto timed_attend = [&](int l) -> ig_status {
     cudaError_t te = rec(dec->ta0, l, S);
@@ -283,5 +300,58 @@ extern "C" ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float*
     ms_out[i] = (float)sums[i];
     if (counts_out) counts_out[i] = counts[i];
   }
+  return IG_OK;
+}
+
+extern "C" ig_status ig_decoder_graph_capture(ig_decoder* dec, const ig_step_io* io, void* stream,
+                                              void* side_stream) {
+  IG_REQUIRE(dec && io, "null argument");
+  cudaStream_t S = as_stream(stream);
+  IG_REQUIRE(S != nullptr, "graph capture needs a created (non-default) compute stream");
+  for (cudaGraphExec_t& g : dec->graph)
+    if (g) {
+      cudaGraphExecDestroy(g);
+      g = nullptr;
+    }
+  const long long saved = dec->steps;
+  const int n = dec->cfg.stage_timing ? 2 : 1;
+  for (int p = 0; p < n; ++p) {
+    dec->steps = p;  // selects timing-event set p
+    const uint64_t k0 = ig_launch_count();
+    cudaError_t e = cudaStreamBeginCapture(S, cudaStreamCaptureModeRelaxed);
+    if (e != cudaSuccess) {
+      dec->steps = saved;
+      return cuda_fail(e, "begin capture");
+    }
+    const ig_status st = ig_decode_step(dec, io, stream, side_stream);
+    cudaGraph_t graph = nullptr;
+    e = cudaStreamEndCapture(S, &graph);
+    const uint64_t captured = ig_launch_count() - k0;
+    count_launches(-(int64_t)captured);  // captured launches have not run
+    if (st != IG_OK || e != cudaSuccess) {
+      if (graph) cudaGraphDestroy(graph);
+      dec->steps = saved;
+      return st != IG_OK ? st : cuda_fail(e, "end capture");
+    }
+    e = cudaGraphInstantiate(&dec->graph[p], graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) {
+      dec->steps = saved;
+      return cuda_fail(e, "graph instantiate");
+    }
+    dec->graph_kernels = captured;
+  }
+  dec->steps = saved;
+  return IG_OK;
+}
+
+extern "C" ig_status ig_decoder_graph_launch(ig_decoder* dec, void* stream) {
+  IG_REQUIRE(dec, "null decoder");
+  const int p = dec->cfg.stage_timing ? (int)(dec->steps & 1) : 0;
+  IG_REQUIRE(dec->graph[p], "no captured step (call ig_decoder_graph_capture first)");
+  cudaError_t e = cudaGraphLaunch(dec->graph[p], as_stream(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "graph launch");
+  dec->steps += 1;
+  count_launches((int64_t)dec->graph_kernels);
   return IG_OK;
 }

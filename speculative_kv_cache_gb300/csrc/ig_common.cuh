@@ -31,8 +31,10 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Counts one kernel launch of this library (ig_launch_count).
+// Counts one kernel launch of this library (ig_launch_count); count_launches adds n (n may be
+// negative: launches recorded into a graph have not run).
 void count_launch();
+void count_launches(int64_t n);
 
 #define IG_CHECK_LAUNCH(what)                                   \
   do {                                                          \

@@ -32,13 +32,15 @@ ig_status launch_k1(cudaStream_t st, const __half* x, const __half* Wt, float* p
 
 
 // K1b: RoPE epilogue for one (b, h): q = sum of the split partials of x W_Q,h; rotate the
-// pairs (j, j + d/2) by p * theta^(-2j/d); then q~p[c] = sum_j q_rot[j] A[h][j][c].
+// pairs (j, j + d/2) by p * theta^(-2j/d) (angle in float64); then q~p[c] = sum_j q_rot[j] A[h][j][c]
+// with A[h][:, S_h] staged in shared memory by coalesced loads and one warp per output c.
 __global__ void k1b_rope_project(const float* __restrict__ part, int S, int B, int H, int d, int k,
                                  const float* __restrict__ A_cols, const int* __restrict__ pos,
                                  double theta, float* __restrict__ qp) {
   extern __shared__ float sh[];
   float* q = sh;           // d
   float* qr = sh + d;      // d
+  float* As = sh + 2 * d;  // d * k
   const int bh = blockIdx.x, b = bh / H, h = bh % H;
   const int N = H * d;
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
@@ -46,6 +48,8 @@ __global__ void k1b_rope_project(const float* __restrict__ part, int S, int B, i
     for (int s = 0; s < S; ++s) a += part[((size_t)s * B + b) * N + h * d + j];
     q[j] = a;
   }
+  const float* Ah = A_cols + (size_t)h * d * k;
+  for (int i = threadIdx.x; i < d * k; i += blockDim.x) As[i] = Ah[i];
   __syncthreads();
   const int half = d / 2;
   const double p = (double)pos[b];
@@ -58,11 +62,12 @@ __global__ void k1b_rope_project(const float* __restrict__ part, int S, int B, i
     qr[j + half] = (float)((double)lo * sn + (double)hi * cs);
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < k; c += blockDim.x) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int c = warp; c < k; c += nw) {
     float a = 0.f;
-    const float* Ac = A_cols + (size_t)h * d * k + c;
-    for (int j = 0; j < d; ++j) a = fmaf(qr[j], Ac[(size_t)j * k], a);
-    qp[((size_t)b * H + h) * k + c] = a;
+    for (int j = lane; j < d; j += 32) a = fmaf(qr[j], As[j * k + c], a);
+    for (int o = 16; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (lane == 0) qp[((size_t)b * H + h) * k + c] = a;
   }
 }
 
@@ -228,7 +233,13 @@ extern "C" ig_status ig_speculate_rope(void* stream, int B, int D, int H, int d,
   st = launch_k1(s, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(Wq), part,
                  B, D, H * d, S, &S);
   if (st != IG_OK) return st;
-  k1b_rope_project<<<B * H, 128, 2 * d * sizeof(float), s>>>(part, S, B, H, d, k, A_cols,
+  const size_t rope_smem = (size_t)(2 * d + d * k) * sizeof(float);
+  if (rope_smem > 48 * 1024) {
+    cudaError_t ae = cudaFuncSetAttribute(k1b_rope_project, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)rope_smem);
+    if (ae != cudaSuccess) return cuda_fail(ae, "rope epilogue smem attribute");
+  }
+  k1b_rope_project<<<B * H, 128, rope_smem, s>>>(part, S, B, H, d, k, A_cols,
                                                             positions, (double)rope_theta, qp);
   IG_CHECK_LAUNCH("rope epilogue launch");
   return launch_k2(s, qp, 1, B, H, k, Kpart, L_valid, Lcap, score_scale, scores, q_part);

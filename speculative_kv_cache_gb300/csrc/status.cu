@@ -60,6 +60,7 @@ std::atomic<uint64_t> g_launches{0};
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+void count_launches(int64_t n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 }  // namespace ig
 

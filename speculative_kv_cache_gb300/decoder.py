@@ -24,7 +24,7 @@ from . import ig
 class Decoder:
     def __init__(self, *, layers, B, H, d, D, k, Lcap, pool_cap, alpha, policy=ig.IG_SEL_THRESHOLD,
                  cap_frac=1.0, score_scale=None, rope_theta=0.0, gather_ctas=0, stage_timing=False,
-                 device="cuda:0"):
+                 graph=False, device="cuda:0"):
         if pool_cap > Lcap or Lcap % 8:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
         self.layers, self.B, self.H, self.d, self.D, self.k, self.Lcap = layers, B, H, d, D, k, Lcap
@@ -68,6 +68,14 @@ class Decoder:
         self.filled = 0
         self.t = 0
         self._pending = None  # (buffer index, event) of the last step's used flags
+        # graph mode: the step reads fixed input buffers and writes a fixed output buffer, is
+        # run once eagerly, then captured into CUDA graphs and replayed
+        self.graph = graph
+        self._captured = False
+        if graph:
+            self.in_x = e(layers, B, D)
+            self.in_q, self.in_k, self.in_v = (e(layers, B, H, d) for _ in range(3))
+            self.out_buf = e(layers, B, H, d, dt=torch.float32)
 
     def _make_buffers(self):
         arrs = {}
@@ -154,9 +162,27 @@ class Decoder:
             self.L_dev.copy_(self.L_host[i], non_blocking=True)
             self.pos_dev.copy_(self.pos_host[i], non_blocking=True)
             self.slot_dev.copy_(slots, non_blocking=True)
-        io = ig.StepIO(x.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), self.L_dev.data_ptr(),
-                       self.pos_dev.data_ptr(), self.slot_dev.data_ptr(), out.data_ptr())
-        ig.ig_decode_step(self.handle, io, self.S, self.G)
+        if self.graph:
+            with torch.cuda.stream(self.S):
+                for dst, src in ((self.in_x, x), (self.in_q, q), (self.in_k, k_new), (self.in_v, v_new)):
+                    if src.data_ptr() != dst.data_ptr():
+                        dst.copy_(src, non_blocking=True)
+            io = ig.StepIO(self.in_x.data_ptr(), self.in_q.data_ptr(), self.in_k.data_ptr(), self.in_v.data_ptr(),
+                           self.L_dev.data_ptr(), self.pos_dev.data_ptr(), self.slot_dev.data_ptr(),
+                           self.out_buf.data_ptr())
+            if self._captured:
+                ig.ig_decoder_graph_launch(self.handle, self.S)
+            else:  # one eager step, then capture the same step for replay
+                ig.ig_decode_step(self.handle, io, self.S, self.G)
+                ig.ig_decoder_graph_capture(self.handle, io, self.S, self.G)
+                self._captured = True
+            if out.data_ptr() != self.out_buf.data_ptr():
+                with torch.cuda.stream(self.S):
+                    out.copy_(self.out_buf, non_blocking=True)
+        else:
+            io = ig.StepIO(x.data_ptr(), q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), self.L_dev.data_ptr(),
+                           self.pos_dev.data_ptr(), self.slot_dev.data_ptr(), out.data_ptr())
+            ig.ig_decode_step(self.handle, io, self.S, self.G)
         with torch.cuda.stream(self.S):
             self.used_host[i].copy_(self.used, non_blocking=True)
             ev = torch.cuda.Event()

@@ -281,6 +281,8 @@ _sig("ig_pool_prefill", _i, _vp, _i, _vp)
 _sig("ig_pool_step", _i, _vp, _vp, _i, _vp)
 _sig("ig_pool_full", _i, _vp, C.POINTER(_i))
 _sig("ig_launch_count", C.c_uint64)
+_sig("ig_decoder_graph_capture", _i, _vp, C.POINTER(StepIO), _vp, _vp)
+_sig("ig_decoder_graph_launch", _i, _vp, _vp)
 
 
 def _ptr_array(items):
@@ -304,6 +306,14 @@ def ig_decoder_destroy(dec):
 
 def ig_decode_step(dec, io: StepIO, stream, side_stream):
     _ok(_lib.ig_decode_step(dec, C.byref(io), _s(stream), _s(side_stream)), "ig_decode_step")
+
+
+def ig_decoder_graph_capture(dec, io: StepIO, stream, side_stream):
+    _ok(_lib.ig_decoder_graph_capture(dec, C.byref(io), _s(stream), _s(side_stream)), "ig_decoder_graph_capture")
+
+
+def ig_decoder_graph_launch(dec, stream):
+    _ok(_lib.ig_decoder_graph_launch(dec, _s(stream)), "ig_decoder_graph_launch")
 
 
 def ig_decoder_stage_ms(dec, steps_back=0):

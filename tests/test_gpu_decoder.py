@@ -169,3 +169,41 @@ def test_decoder_llama13b_width_capped_pool(mods):
     w = synth.scaled(synth.WORKLOADS["llama-2-13b"], name="dec-13b", layers=3)
     assert w.pool_cap == 2458 and w.pool_cap < w.prompt
     _run(mods, w, steps=3, rope=True, check_slots=True)
+
+
+def test_graph_replay_matches_eager_step(mods):
+    """The CUDA-graph form of the step gives the same bytes as the eager step, step after step."""
+    ig, decoder = mods
+    w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-graph", layers=3, batch=2, heads=4, hidden=512,
+                     prompt=200, gen=10, pool_frac=0.95)
+    dev = "cuda:0"
+    outs = {}
+    for graph in (False, True):
+        dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k,
+                              Lcap=w.lcap, pool_cap=w.pool_cap, alpha=4.0, graph=graph, stage_timing=graph,
+                              device=dev)
+        try:
+            for l in range(w.layers):
+                dd = _layer_data(w, l, w.pool_cap, False)
+                t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+                dec.load_layer(l, t(dd["K"]), t(dd["V"]), dd["cols"], Wq_part=t(dd["Wqp"]))
+            dec.prefill(w.prompt)
+            res = []
+            for s in range(5):  # crosses the capture step and eviction (the pool is full)
+                x = torch.from_numpy(synth.layer_inputs(w, step=s)).to(dev)
+                qkv = [synth.token_inputs(w, l, s) for l in range(w.layers)]
+                q, kn, vn = (torch.from_numpy(np.stack([a[i] for a in qkv])).to(dev) for i in range(3))
+                out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=dev)
+                dec.step(x, q, kn, vn, out)
+                dec.finish()
+                ig.ig_check(dec.S)
+                res.append((out.cpu().numpy(), dec.cnt.cpu().numpy(), dec.slot_host[s % 2].numpy().copy()))
+                if graph and s >= 1:
+                    ms, n = dec.stage_ms()
+                    assert n[0] == w.layers - 1 and ms[0] > 0
+            outs[graph] = res
+        finally:
+            dec.close()
+    for (o0, c0, s0), (o1, c1, s1) in zip(outs[False], outs[True]):
+        assert np.array_equal(s0, s1) and np.array_equal(c0, c1)
+        assert np.array_equal(o0, o1)
