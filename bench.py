@@ -46,6 +46,7 @@ def parse_args(argv=None):
     p.add_argument("--alpha", type=float, default=None)
     p.add_argument("--gather-ctas", type=int, default=0)
     p.add_argument("--graph", type=int, default=1, help="1: replay each step from a CUDA graph")
+    p.add_argument("--fused-select", type=int, default=1, help="1: fused cluster score+select kernel")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-layers", type=int, default=0, help="oracle sample: layers (0 = default)")
@@ -241,13 +242,13 @@ def link_peak_gbs(torch) -> float:
     return n / (best * 1e-3) / 1e9
 
 
-def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False):
+def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True):
     from speculative_kv_cache_gb300.decoder import Decoder
 
     Lcap = w.lcap
     dec = Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=Lcap,
                   pool_cap=w.pool_cap, alpha=alpha, rope_theta=w.rope_theta, gather_ctas=gather_ctas,
-                  stage_timing=True, graph=bool(graph), device=device)
+                  stage_timing=True, graph=bool(graph), fused_select=bool(fused_select), device=device)
     gen = torch.Generator(device=device)
     shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
@@ -345,7 +346,8 @@ def run_ours(args, w, alpha):
     steps_total = args.warmup + args.steps + n_e2e
     if w.prompt + steps_total > w.context:
         raise SystemExit(f"warmup + steps (+ e2e steps) must stay within the {w.gen} generated tokens")
-    dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph)
+    dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph,
+                                          args.fused_select)
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
@@ -441,7 +443,8 @@ def run_ours(args, w, alpha):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp16 storage, fp32 accumulate", "data": "synthetic (seeded, random-init weights)",
-            "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph)),
+            "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph),
+                           fused_select=bool(args.fused_select)),
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "selected_fraction": float(f),
             "link_gbs": G_total / args.steps / (ms_per_step * 1e-3) / 1e9,

@@ -119,7 +119,7 @@ ig_status ig_speculate(void* stream, int B, int D, int H, int k, int Lcap,
  * library (a file-scope __device__ array, held on every GPU that loads the library until the
  * process exits); nothing is allocated, by this call or by anything it calls.
  *   - Limit: ig_speculate_workspace_bytes(B, D, H, k) must be <= 4 MiB (4194304 bytes), else
- *     IG_ERR_CAPACITY with a message; e.g. B = 16, D = 7168, H * k = 2128 needs 2.2 MB.
+ *     IG_ERR_CAPACITY with a message; e.g. B = 16, D = 7168, H * k = 2128 needs 3.8 MB.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *     and caches it; make that first call before any stream capture.
  *   - Every call on a device shares the one array and leaves its partial sums there (each call
@@ -165,6 +165,27 @@ ig_status ig_select(void* stream, int B, int H, int Lcap, const float* scores,
                     const int32_t* L_valid, float alpha, int policy, float cap_frac,
                     int32_t* idx, int32_t* cnt, uint8_t* used, void* workspace,
                     size_t workspace_bytes);
+
+/* ------------------------------------------------------------------------------------
+ * Fused speculation + threshold selection: ig_speculate followed by ig_select with
+ * IG_SEL_THRESHOLD and no cap, with the scores kept on chip.  Section 3.4, "Decoding Stage",
+ * Steps 1-3.  One thread-block cluster per (sequence, head) and one CTA per 512-token chunk;
+ * the head's maximum and the compaction offsets cross the cluster through distributed
+ * shared memory.  Identical results to the two calls (same fp32 operations).
+ *   Wq        dev fp16 [H*k][D] (rope_theta == 0) or [H*d][D] (RoPE: then A_cols [H][d][k] and
+ *             positions [B] are required, as in ig_speculate_rope)
+ *   idx, cnt, used   as ig_select (used may be NULL)
+ *   scores    dev fp32 [B][H][Lcap] or NULL: the scores, written only when asked for
+ *   q_part    dev fp32 [B][H][k] or NULL
+ *   workspace >= ig_speculate_select_workspace_bytes(B, D, H, d, k, rope != 0)
+ * Lcap must be <= 4096 (at most 8 chunks per cluster); else IG_ERR_INVALID. */
+size_t ig_speculate_select_workspace_bytes(int B, int D, int H, int d, int k, int rope);
+ig_status ig_speculate_select(void* stream, int B, int D, int H, int d, int k, int Lcap,
+                              const uint16_t* x, const uint16_t* Wq, const float* A_cols,
+                              const int32_t* positions, float rope_theta, const uint16_t* Kpart,
+                              const int32_t* L_valid, float score_scale, float alpha,
+                              int32_t* idx, int32_t* cnt, uint8_t* used, float* scores,
+                              float* q_part, void* workspace, size_t workspace_bytes);
 
 /* ------------------------------------------------------------------------------------
  * KV pool in pinned, mapped host memory: one pool per layer and sequence, `cap` slots, each
@@ -276,6 +297,8 @@ typedef struct {
   float rope_theta;    /* 0: no RoPE (partial weight path); > 0: RoPE path */
   int gather_ctas;     /* grid of the fetch kernel; 0 = library default */
   int stage_timing;    /* 1: record timing events around each stage (ig_decoder_stage_ms) */
+  int fused_select;    /* 1: use ig_speculate_select when policy = IG_SEL_THRESHOLD, cap_frac >= 1
+                          and Lcap <= 4096 (scores stay on chip); 0: separate calls */
 } ig_decoder_config;
 
 typedef struct {

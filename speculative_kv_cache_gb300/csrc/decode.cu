@@ -221,7 +221,14 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     uint8_t* used = b.used ? b.used + (size_t)l * B * Lc : nullptr;
     e = rec(dec->ts0, l, S);
     if (e != cudaSuccess) return cuda_fail(e, "timing event");
-    if (c.rope_theta > 0.f) {
+    const bool fused = c.fused_select && c.policy == IG_SEL_THRESHOLD && c.cap_frac >= 1.f && Lc <= 4096;
+    if (fused) {
+      const bool rope = c.rope_theta > 0.f;
+      st = ig_speculate_select(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs,
+                               rope ? dec->Wq[l] : dec->Wq_part[l], rope ? dec->A_cols[l] : nullptr,
+                               rope ? io->positions : nullptr, c.rope_theta, dec->Kpart[l], io->L_valid,
+                               c.score_scale, c.alpha, idx, cnt, used, nullptr, nullptr, ws, spec_att_ws);
+    } else if (c.rope_theta > 0.f) {
       const int32_t* pos = io->positions;
       st = ig_speculate_rope(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq[l],
                              dec->A_cols[l], pos, c.rope_theta, dec->Kpart[l], io->L_valid,
@@ -231,9 +238,11 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
                         dec->Kpart[l], io->L_valid, c.score_scale, sc, nullptr, ws, spec_att_ws);
     }
     if (st != IG_OK) return st;
-    st = ig_select(S, B, H, Lc, sc, io->L_valid, c.alpha, c.policy, c.cap_frac, idx, cnt, used,
-                   sel_ws, sel_ws_bytes);
-    if (st != IG_OK) return st;
+    if (!fused) {
+      st = ig_select(S, B, H, Lc, sc, io->L_valid, c.alpha, c.policy, c.cap_frac, idx, cnt, used,
+                     sel_ws, sel_ws_bytes);
+      if (st != IG_OK) return st;
+    }
     e = rec(dec->ts1, l, S);
     if (e == cudaSuccess) e = cudaEventRecord(dec->ev_sel[l], S);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(G, dec->ev_sel[l], 0);

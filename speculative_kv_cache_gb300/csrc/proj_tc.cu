@@ -60,9 +60,9 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kTcThreads, 1) k1_partial_q_tc(
+__global__ void __launch_bounds__(kTcThreads) k1_partial_q_tc(
     const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-    float* __restrict__ part, int B, int D, int N, int split_k, int* err) {
+    float* __restrict__ part, int B, int D, int N, int split_k, int max_st, int* err) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled stages
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -72,11 +72,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k1_partial_q_tc(
   const int b0 = blockIdx.z * kTcN;
   const int k_begin = s * split_k;
   const int k_end = min(D, k_begin + split_k);
-  const int nst = (k_end - k_begin + kTcBK - 1) / kTcBK;  // 1..kTcMaxStages
-  unsigned char* sA = smem;
-  unsigned char* sB = smem + kTcMaxStages * kStageA;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kTcMaxStages * kStageB);
-  uint64_t* done = full + kTcMaxStages;
+  const int nst = (k_end - k_begin + kTcBK - 1) / kTcBK;  // 1..max_st stages of this CTA
+  unsigned char* sA = smem;                              // max_st weight stages
+  unsigned char* sB = smem + max_st * kStageA;           // max_st x stages
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + max_st * kStageB);
+  uint64_t* done = full + max_st;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -202,7 +202,9 @@ ig_status make_map(CUtensorMap* m, const void* base, int rows, int cols, int box
   return IG_OK;
 }
 
-size_t tc_smem_bytes() { return 1024 + kTcMaxStages * (kStageA + kStageB) + (kTcMaxStages + 1) * 8 + 16; }
+// shared memory for max_st stages (sized per launch: 4 stages of a 256-wide split take 73 KB, so
+// three CTAs share an SM)
+size_t tc_smem_bytes(int max_st) { return 1024 + max_st * (kStageA + kStageB) + (max_st + 1) * 8 + 16; }
 
 }  // namespace
 
@@ -227,11 +229,12 @@ ig_status launch_partial_q_tc(cudaStream_t st, const __half* x, const __half* Wt
   if (r != IG_OK) return r;
   r = make_map(&mx, x, B, D, kTcN);
   if (r != IG_OK) return r;
-  cudaError_t ae = cudaFuncSetAttribute(k1_partial_q_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)tc_smem_bytes());
+  const int max_st = split_k / kTcBK;
+  const size_t smem = tc_smem_bytes(max_st);
+  cudaError_t ae = cudaFuncSetAttribute(k1_partial_q_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ae != cudaSuccess) return cuda_fail(ae, "tensor-core projection smem attribute");
   dim3 grid((N + kTcM - 1) / kTcM, se, (B + kTcN - 1) / kTcN);
-  k1_partial_q_tc<<<grid, kTcThreads, tc_smem_bytes(), st>>>(mw, mx, part, B, D, N, split_k, error_word());
+  k1_partial_q_tc<<<grid, kTcThreads, smem, st>>>(mw, mx, part, B, D, N, split_k, max_st, error_word());
   IG_CHECK_LAUNCH("tensor-core projection launch");
   *s_eff = se;
   return IG_OK;

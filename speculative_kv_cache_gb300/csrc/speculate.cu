@@ -15,9 +15,10 @@ ig_status launch_partial_q_tc(cudaStream_t st, const __half* x, const __half* Wt
                               int D, int N, int S, int* s_eff);
 namespace {
 
-constexpr int kMaxSplits = 16;
+constexpr int kMaxSplits = 32;
 
-// Number of K-splits of the projection for a given reduction length.
+// Number of K-splits of the projection for a given reduction length: 256-wide pieces (four
+// 64-wide tensor-core stages each), at most 32.
 inline int proj_splits(int D) {
   int s = (D + 255) / 256;
   return s < 1 ? 1 : (s > kMaxSplits ? kMaxSplits : s);
@@ -175,6 +176,22 @@ ig_status check_common(int B, int D, int H, int k, int Lcap, const void* x, cons
 }
 
 }  // namespace
+
+int projection_splits(int D) { return proj_splits(D); }
+
+ig_status launch_rope_project(cudaStream_t st, const float* part, int S, int B, int H, int d, int k,
+                              const float* A_cols, const int* pos, float theta, float* qp) {
+  const size_t rope_smem = (size_t)(2 * d + d * k) * sizeof(float);
+  if (rope_smem > 48 * 1024) {
+    cudaError_t ae = cudaFuncSetAttribute(k1b_rope_project, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)rope_smem);
+    if (ae != cudaSuccess) return cuda_fail(ae, "rope epilogue smem attribute");
+  }
+  k1b_rope_project<<<B * H, 128, rope_smem, st>>>(part, S, B, H, d, k, A_cols, pos, (double)theta, qp);
+  IG_CHECK_LAUNCH("rope epilogue launch");
+  return IG_OK;
+}
+
 }  // namespace ig
 
 using namespace ig;
@@ -233,15 +250,8 @@ extern "C" ig_status ig_speculate_rope(void* stream, int B, int D, int H, int d,
   st = launch_k1(s, reinterpret_cast<const __half*>(x), reinterpret_cast<const __half*>(Wq), part,
                  B, D, H * d, S, &S);
   if (st != IG_OK) return st;
-  const size_t rope_smem = (size_t)(2 * d + d * k) * sizeof(float);
-  if (rope_smem > 48 * 1024) {
-    cudaError_t ae = cudaFuncSetAttribute(k1b_rope_project, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)rope_smem);
-    if (ae != cudaSuccess) return cuda_fail(ae, "rope epilogue smem attribute");
-  }
-  k1b_rope_project<<<B * H, 128, rope_smem, s>>>(part, S, B, H, d, k, A_cols,
-                                                            positions, (double)rope_theta, qp);
-  IG_CHECK_LAUNCH("rope epilogue launch");
+  st = launch_rope_project(s, part, S, B, H, d, k, A_cols, positions, rope_theta, qp);
+  if (st != IG_OK) return st;
   return launch_k2(s, qp, 1, B, H, k, Kpart, L_valid, Lcap, score_scale, scores, q_part);
 }
 

@@ -24,7 +24,7 @@ from . import ig
 class Decoder:
     def __init__(self, *, layers, B, H, d, D, k, Lcap, pool_cap, alpha, policy=ig.IG_SEL_THRESHOLD,
                  cap_frac=1.0, score_scale=None, rope_theta=0.0, gather_ctas=0, stage_timing=False,
-                 graph=False, device="cuda:0"):
+                 graph=False, fused_select=True, device="cuda:0"):
         if pool_cap > Lcap or Lcap % 8:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
         self.layers, self.B, self.H, self.d, self.D, self.k, self.Lcap = layers, B, H, d, D, k, Lcap
@@ -37,7 +37,8 @@ class Decoder:
         self.pool = ig.ig_pool_create(layers, B, H, d, pool_cap)
         self.cfg = ig.DecoderConfig(layers, B, H, d, D, k, Lcap, policy, float(alpha), float(cap_frac),
                                     float(score_scale if score_scale is not None else 1.0 / math.sqrt(d)),
-                                    float(rope_theta), int(gather_ctas), int(bool(stage_timing)))
+                                    float(rope_theta), int(gather_ctas), int(bool(stage_timing)),
+                                    int(bool(fused_select)))
         # per-layer state: partial query weight (or full W_Q and A[:, S] for RoPE), columns,
         # partial key cache; layer 0 keeps its full KV in HBM instead
         self.Wq_part = [None] + [e(H * k, D) for _ in range(1, layers)] if not self.rope else None

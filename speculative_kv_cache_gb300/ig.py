@@ -65,6 +65,9 @@ _sig("ig_speculate_rope_workspace_bytes", _sz, _i, _i, _i, _i, _i)
 _sig("ig_speculate_rope", _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f,
      _vp, _vp, _vp, _sz)
 _sig("ig_select_workspace_bytes", _sz, _i, _i)
+_sig("ig_speculate_select_workspace_bytes", _sz, _i, _i, _i, _i, _i, _i)
+_sig("ig_speculate_select", _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp, _f, _f, _vp, _vp,
+     _vp, _vp, _vp, _vp, _sz)
 _sig("ig_select", _i, _vp, _i, _i, _i, _vp, _vp, _f, _i, _f, _vp, _vp, _vp, _vp, _sz)
 _sig("ig_pool_create", _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_destroy", _i, _vp)
@@ -181,6 +184,18 @@ def ig_select(stream, B, H, Lcap, scores, L_valid, alpha, policy, cap_frac, idx,
                        _p(idx), _p(cnt), _p(used), _p(workspace), workspace_bytes), "ig_select")
 
 
+def ig_speculate_select_workspace_bytes(B, D, H, d, k, rope) -> int:
+    return _lib.ig_speculate_select_workspace_bytes(B, D, H, d, k, int(bool(rope)))
+
+
+def ig_speculate_select(stream, B, D, H, d, k, Lcap, x, Wq, A_cols, positions, rope_theta, Kpart, L_valid,
+                        score_scale, alpha, idx, cnt, used, scores, q_part, workspace, workspace_bytes):
+    _ok(_lib.ig_speculate_select(_s(stream), B, D, H, d, k, Lcap, _p(x), _p(Wq), _p(A_cols), _p(positions),
+                                 rope_theta, _p(Kpart), _p(L_valid), score_scale, alpha, _p(idx), _p(cnt),
+                                 _p(used), _p(scores), _p(q_part), _p(workspace), workspace_bytes),
+        "ig_speculate_select")
+
+
 def ig_pool_create(layers, B, H, d, cap) -> int:
     h = _vp()
     _ok(_lib.ig_pool_create(layers, B, H, d, cap, C.byref(h)), "ig_pool_create")
@@ -256,7 +271,7 @@ def pool_layer_view(pool, layer, B, H, cap, d):
 class DecoderConfig(C.Structure):
     _fields_ = [("layers", _i), ("B", _i), ("H", _i), ("d", _i), ("D", _i), ("k", _i), ("Lcap", _i),
                 ("policy", _i), ("alpha", _f), ("cap_frac", _f), ("score_scale", _f),
-                ("rope_theta", _f), ("gather_ctas", _i), ("stage_timing", _i)]
+                ("rope_theta", _f), ("gather_ctas", _i), ("stage_timing", _i), ("fused_select", _i)]
 
 
 class DecoderBuffers(C.Structure):

@@ -54,7 +54,7 @@ def test_invalid_arguments_are_rejected_before_any_device_work(ig):
 
 
 def test_workspace_sizes(ig):
-    assert ig.ig_speculate_workspace_bytes(16, 7168, 56, 38) == 16 * 16 * 56 * 38 * 4
+    assert ig.ig_speculate_workspace_bytes(16, 7168, 56, 38) == 28 * 16 * 56 * 38 * 4
     assert ig.ig_speculate_workspace_bytes(1, 256, 4, 16) == 256
     assert ig.ig_select_workspace_bytes(16, 56) % 256 == 0
     assert ig.ig_attend_workspace_bytes(1, 4, 64, 256) >= 4 * 4 * 66 * 4

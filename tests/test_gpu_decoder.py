@@ -44,7 +44,7 @@ def _layer_data(w, l, cap, rope):
     return dict(K=K, V=V, cols=cols, Wqp=synth.skewed_partial_weight(w, l))
 
 
-def _run(mods, w, steps, rope=False, check_slots=False):
+def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True):
     ig, decoder = mods
     dev = "cuda:0"
     Lcap = w.lcap
@@ -52,7 +52,8 @@ def _run(mods, w, steps, rope=False, check_slots=False):
     scale = np.float32(1.0 / math.sqrt(w.head_dim))
     alpha = 4.0
     dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k,
-                          Lcap=Lcap, pool_cap=cap, alpha=alpha, rope_theta=w.rope_theta, device=dev)
+                          Lcap=Lcap, pool_cap=cap, alpha=alpha, rope_theta=w.rope_theta,
+                          fused_select=fused_select, device=dev)
     try:
         data = [_layer_data(w, l, cap, rope) for l in range(w.layers)]
         for l, dd in enumerate(data):
@@ -144,10 +145,11 @@ def _run(mods, w, steps, rope=False, check_slots=False):
         dec.close()
 
 
-def test_decoder_opt_shaped_steps(mods):
+@pytest.mark.parametrize("fused", [True, False])
+def test_decoder_opt_shaped_steps(mods, fused):
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-opt", layers=3, batch=3, heads=6, hidden=768,
                      prompt=300, gen=8)
-    _run(mods, w, steps=3)
+    _run(mods, w, steps=3, fused_select=fused)
 
 
 def test_decoder_capped_pool_evicts_like_the_oracle(mods):

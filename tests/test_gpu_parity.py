@@ -361,3 +361,56 @@ def test_rope_layer_step_end_to_end(ig, pools, alpha):
     Kg_o, Vg_o = ora.gather(c["K"], c["V"], sets, Lcap)
     o = ora.attend(c["q"], Kg_o, Vg_o, cnt_g, c["scale"], c["kn"], c["vn"])
     assert np.abs(host(out) - o).max() <= OUT_TOL
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("alpha", [1e-6, 4.0, float("inf")])
+def test_fused_speculate_select_equals_separate_calls(ig, name, alpha):
+    """The cluster-fused score+select gives the same bytes as ig_speculate then ig_select."""
+    c = make_case(name)
+    w = c["w"]
+    B, H, d, k, D, Lcap = w.batch, w.heads, w.head_dim, w.k, w.hidden, c["Lcap"]
+    args = (dev(c["x"]), dev(c["Wqp"].T))
+    ws = workspace(ig.ig_speculate_select_workspace_bytes(B, D, H, d, k, 0))
+    s1 = empty((B, H, Lcap), torch.float32)
+    ig.ig_speculate(None, B, D, H, k, Lcap, *args, dev(c["Kpart"]), dev(c["L"]), float(c["scale"]), s1, None, ws,
+                    ws.numel())
+    i1, c1, u1 = empty((B, H, Lcap), torch.int32), empty((B, H), torch.int32), empty((B, Lcap), torch.uint8)
+    ig.ig_select(None, B, H, Lcap, s1, dev(c["L"]), alpha, 0, 1.0, i1, c1, u1)
+    s2 = empty((B, H, Lcap), torch.float32)
+    i2, c2, u2 = empty((B, H, Lcap), torch.int32), empty((B, H), torch.int32), empty((B, Lcap), torch.uint8)
+    ig.ig_speculate_select(None, B, D, H, d, k, Lcap, *args, None, None, 0.0, dev(c["Kpart"]), dev(c["L"]),
+                           float(c["scale"]), alpha, i2, c2, u2, s2, None, ws, ws.numel())
+    ig.ig_check()
+    assert np.array_equal(host(s1), host(s2))
+    cn1, cn2 = host(c1), host(c2)
+    assert np.array_equal(cn1, cn2)
+    a1, a2 = host(i1), host(i2)
+    for b in range(B):
+        for h in range(H):
+            assert np.array_equal(a1[b, h, :cn1[b, h]], a2[b, h, :cn2[b, h]])
+    assert np.array_equal(host(u1), host(u2))
+
+
+@pytest.mark.parametrize("alpha", [2.0, 6.0])
+def test_fused_speculate_select_rope(ig, alpha):
+    c = rope_case()
+    w = c["w"]
+    B, H, d, k, D, Lcap = w.batch, w.heads, w.head_dim, w.k, w.hidden, c["Lcap"]
+    ws = workspace(ig.ig_speculate_select_workspace_bytes(B, D, H, d, k, 1))
+    s1 = empty((B, H, Lcap), torch.float32)
+    common = (dev(c["x"]), dev(c["Wq"].T), dev(c["A_cols"]), dev(c["pos"]), w.rope_theta)
+    ig.ig_speculate_rope(None, B, D, H, d, k, Lcap, *common, dev(c["Kpart"]), dev(c["L"]), float(c["scale"]), s1,
+                         None, ws, ws.numel())
+    i1, c1 = empty((B, H, Lcap), torch.int32), empty((B, H), torch.int32)
+    ig.ig_select(None, B, H, Lcap, s1, dev(c["L"]), alpha, 0, 1.0, i1, c1, None)
+    i2, c2 = empty((B, H, Lcap), torch.int32), empty((B, H), torch.int32)
+    ig.ig_speculate_select(None, B, D, H, d, k, Lcap, *common, dev(c["Kpart"]), dev(c["L"]), float(c["scale"]),
+                           alpha, i2, c2, None, None, None, ws, ws.numel())
+    ig.ig_check()
+    cn1, cn2 = host(c1), host(c2)
+    assert np.array_equal(cn1, cn2)
+    a1, a2 = host(i1), host(i2)
+    for b in range(B):
+        for h in range(H):
+            assert np.array_equal(a1[b, h, :cn1[b, h]], a2[b, h, :cn2[b, h]])

@@ -80,7 +80,7 @@ def test_static_scratch_matches_workspace_version_on_two_calls(ig):
 
 
 def test_static_scratch_refuses_requests_beyond_its_size(ig):
-    # 16 splits x B x H*k floats beyond 4 MiB: 16 * 64 * 56 * 38 * 4 = 8.7 MB
+    # 28 splits x B x H*k floats beyond 4 MiB: 28 * 64 * 56 * 38 * 4 = 15 MB
     B, D, H, k, Lcap = 64, 7168, 56, 38, 8
     assert ig.ig_speculate_workspace_bytes(B, D, H, k) > 4 << 20
     t = torch.zeros(16, dtype=torch.float32, device="cuda:0")
