@@ -47,6 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--gather-ctas", type=int, default=0)
     p.add_argument("--graph", type=int, default=1, help="1: replay each step from a CUDA graph")
     p.add_argument("--fused-select", type=int, default=1, help="1: fused cluster score+select kernel")
+    p.add_argument("--fused-fetch", type=int, default=0,
+                   help="1: layers 1.. attend straight from the pinned pool on the fetch stream (no staging)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-layers", type=int, default=0, help="oracle sample: layers (0 = default)")
@@ -242,13 +244,15 @@ def link_peak_gbs(torch) -> float:
     return n / (best * 1e-3) / 1e9
 
 
-def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True):
+def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True,
+                  fused_fetch=False):
     from speculative_kv_cache_gb300.decoder import Decoder
 
     Lcap = w.lcap
     dec = Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=Lcap,
                   pool_cap=w.pool_cap, alpha=alpha, rope_theta=w.rope_theta, gather_ctas=gather_ctas,
-                  stage_timing=True, graph=bool(graph), fused_select=bool(fused_select), device=device)
+                  stage_timing=True, graph=bool(graph), fused_select=bool(fused_select),
+                  fused_fetch=bool(fused_fetch), device=device)
     gen = torch.Generator(device=device)
     shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
@@ -346,8 +350,9 @@ def run_ours(args, w, alpha):
     steps_total = args.warmup + args.steps + n_e2e
     if w.prompt + steps_total > w.context:
         raise SystemExit(f"warmup + steps (+ e2e steps) must stay within the {w.gen} generated tokens")
+    fused_fetch = bool(args.fused_fetch)
     dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph,
-                                          args.fused_select)
+                                          args.fused_select, fused_fetch)
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
@@ -400,7 +405,8 @@ def run_ours(args, w, alpha):
     # whole-step roofline: per layer the slower of HBM bytes at HBM peak and gathered bytes at
     # the link peak; layer 0 reads its full KV from HBM
     pk_bytes = w.batch * w.heads * w.k * ctx.mean() * 2
-    hbm_l = pk_bytes + cnts[:, 1:].sum(axis=(2, 3)).mean(axis=0) * 2 * w.head_dim * 2
+    # staged: the fetched rows are written to and read back from HBM once; fused: not at all
+    hbm_l = pk_bytes + (0 if fused_fetch else cnts[:, 1:].sum(axis=(2, 3)).mean(axis=0) * 2 * w.head_dim * 2)
     link_l = cnts[:, 1:].sum(axis=(2, 3)).mean(axis=0) * 2 * w.head_dim * 2
     t_roof_s = float(np.maximum(hbm_l / (hbm_peak * 1e9), link_l / (link * 1e9)).sum())
     t_roof_s += w.batch * w.heads * ctx.mean() * w.head_dim * 2 * 2 / (hbm_peak * 1e9)
@@ -444,7 +450,7 @@ def run_ours(args, w, alpha):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp16 storage, fp32 accumulate", "data": "synthetic (seeded, random-init weights)",
             "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph),
-                           fused_select=bool(args.fused_select)),
+                           fused_select=bool(args.fused_select), fused_fetch=fused_fetch),
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "selected_fraction": float(f),
             "link_gbs": G_total / args.steps / (ms_per_step * 1e-3) / 1e9,
@@ -452,13 +458,16 @@ def run_ours(args, w, alpha):
             "us_per_speculative_layer_step": 1000 * (ms_per_step - stage[3] / args.steps) / max(1, w.layers - 1),
             "layer0_ms_per_step": stage[3] / args.steps,
             "hbm_alg_frac": {"of_measured": hbm_gbs_alg / hbm_peak, "of_nominal_8000": hbm_gbs_alg / 8000.0},
-            "stage_ms_per_step": {"gather": stage[0] / args.steps, "speculate_select": stage[1] / args.steps,
-                                  "attend_append": stage[2] / args.steps},
+            "stage_ms_per_step": {("fetch_attend" if fused_fetch else "gather"): stage[0] / args.steps,
+                                  "speculate_select": stage[1] / args.steps,
+                                  ("append" if fused_fetch else "attend_append"): stage[2] / args.steps},
             "e2e": e2e,
             "gpu_launches": int(launches),
-            "roofline": {"kernel": "k4_gather (zero-copy fetch of the selected K/V rows)",
+            "roofline": {"kernel": ("k5_fetch_attend + combine (fused zero-copy fetch + attention)"
+                                    if fused_fetch else "k4_gather (zero-copy fetch of the selected K/V rows)"),
                          "bound": "host-link", "achieved": achieved, "peak": link,
-                         "unit": "GB/s", "frac": achieved / link, "traffic": gather_traffic_bytes(),
+                         "unit": "GB/s", "frac": achieved / link,
+                         "traffic": None if fused_fetch else gather_traffic_bytes(),
                          "traffic_note": "DRAM read+write bytes per launch (ncu, same per-layer shape); "
                                          "the kernel's algorithmic bytes cross the host link, not DRAM",
                          "peak_source": "measured in this run: pinned host->device copy, best of 5 x 1 GiB",

@@ -262,6 +262,28 @@ ig_status ig_dense_attend(void* stream, int B, int H, int d, int Lcap, float sca
                           const uint16_t* v_new, float* out, void* workspace,
                           size_t workspace_bytes);
 
+/* Fused fetch + attention.  The same result as ig_gather_kv followed by ig_sparse_attend,
+ * up to fp32 summation order, without staging the rows in HBM: the kernel loads each selected
+ * row straight from the pinned pool (16-byte zero-copy loads over the host link) through idx
+ * and folds it into a per-head online softmax.  This is the prefetch of section 3.4
+ * (Inference Controller) with the copy and the attention that consumes it in one pass; the
+ * pages stage the rows in GPU memory first.  Issue it on a side stream; max_ctas bounds the
+ * grid (0 = library default, a quarter of the SMs; at most 256).
+ *   pool, layer        as for ig_gather_kv (B, H, d must match the pool)
+ *   q                  dev fp16 [B][H][d]
+ *   idx, cnt           dev, from ig_select (slots must be < the pool's capacity; a slot
+ *                      out of range is skipped and raises IG_DEVERR_INDEX)
+ *   k_new, v_new       dev fp16 [B][H][d] or NULL (the current token, always attended)
+ *   out                dev fp32 [B][H][d] out
+ *   workspace          dev, >= ig_gather_attend_workspace_bytes(B, H, d, Lcap) bytes,
+ *                      256-byte aligned (per-head partials of the kernel's lane groups)
+ * d must be 64 or 128. */
+size_t ig_gather_attend_workspace_bytes(int B, int H, int d, int Lcap);
+ig_status ig_gather_attend(void* stream, const ig_pool* pool, int layer, int B, int H, int d,
+                           int Lcap, float scale, const uint16_t* q, const int32_t* idx,
+                           const int32_t* cnt, const uint16_t* k_new, const uint16_t* v_new,
+                           float* out, void* workspace, size_t workspace_bytes, int max_ctas);
+
 /* ------------------------------------------------------------------------------------
  * Append of the current token.  Section 3.4, "Partial Key Cache Updates During Decoding":
  * the new token's full key and value go to the host pool, its k chosen columns to the
@@ -299,6 +321,9 @@ typedef struct {
   int stage_timing;    /* 1: record timing events around each stage (ig_decoder_stage_ms) */
   int fused_select;    /* 1: use ig_speculate_select when policy = IG_SEL_THRESHOLD, cap_frac >= 1
                           and Lcap <= 4096 (scores stay on chip); 0: separate calls */
+  int fused_fetch;     /* 1: layers 1.. attend straight from the pool on the fetch stream
+                          (ig_gather_attend), no staging in HBM, Kg/Vg unused (may be NULL);
+                          0: gather into Kg/Vg on the fetch stream, attend on the compute stream */
 } ig_decoder_config;
 
 typedef struct {
@@ -313,7 +338,8 @@ typedef struct {
   int32_t* idx;                    /* dev int32 [2][B][H][Lcap]                              */
   int32_t* cnt;                    /* dev int32 [layers][B][H]                               */
   uint8_t* used;                   /* dev uint8 [layers][B][Lcap] or NULL                    */
-  uint16_t* Kg;                    /* dev fp16 [2][B][H][Lcap][d] (16-byte aligned)          */
+  uint16_t* Kg;                    /* dev fp16 [2][B][H][Lcap][d] (16-byte aligned); NULL
+                                      allowed with fused_fetch                                */
   uint16_t* Vg;
   void* workspace;                 /* dev, >= ig_decoder_workspace_bytes(), 256-byte aligned */
   size_t workspace_bytes;
@@ -375,9 +401,10 @@ uint64_t ig_launch_count(void);
 
 /* Stage timing of a recent ig_decode_step (steps_back = 0: the last one, 1: the one before),
  * when the decoder was created with config.stage_timing = 1: ms_out[0] = sum of gather kernel
- * times (fetch stream), ms_out[1] = speculate + select, ms_out[2] = attention + append of
- * layers 1.. (compute stream), ms_out[3] = layer 0's dense attention + append; counts_out[0..3]
- * = the number of timed intervals of each (both arrays hold 4 entries).  Waits for that
+ * times (fetch stream; with fused_fetch, of fetch + attention), ms_out[1] = speculate +
+ * select, ms_out[2] = attention + append of layers 1.. (compute stream; with fused_fetch, the
+ * appends alone), ms_out[3] = layer 0's dense attention + append; counts_out[0..3] = the
+ * number of timed intervals of each (both arrays hold 4 entries).  Waits for that
  * step to finish; reading step t-1 while step t is queued keeps the GPU busy. */
 ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float* ms_out, int* counts_out);
 

@@ -16,6 +16,7 @@
 #include <math.h>
 
 #include "ig_common.cuh"
+#include "pool_impl.h"
 
 namespace ig {
 namespace {
@@ -24,6 +25,12 @@ constexpr int kAttThreads = 128;
 constexpr int kAttUnroll = 4;
 constexpr int kMaxAttCtas = 1024;   // upper bound of the balanced grid (sizes the workspace)
 constexpr int kMaxAttUnits = 16384; // (units + 1) ints of shared memory for the scan
+constexpr int kFaThreads = 256;     // fused fetch + attention: as the gather (host-link bound)
+constexpr int kFaUnroll = 6;        // rows per batch and lane group (two batches in flight)
+constexpr int kMaxFaCtas = 256;     // upper bound of its grid (sizes its workspace)
+// a partial in the workspace: [max, sum, -, -, unnormalised output[D]] (D + 4 floats, so
+// that the output part of every partial starts on a 16-byte boundary)
+constexpr int kPartHead = 4;
 
 __device__ __forceinline__ float lane_dot(const float (&q)[8], uint4 kv) {
   float2 a = h2_to_f2(kv.x), b = h2_to_f2(kv.y), c = h2_to_f2(kv.z), e = h2_to_f2(kv.w);
@@ -60,9 +67,10 @@ __device__ __forceinline__ void online_add(float z, uint4 vv, float& m, float& l
 
 // Exclusive scan of the clamped per-unit row counts into pre[0..units] (pre[units] = R).
 // cnt_per_seq: the count of unit u is cnt[u / H] (dense attention) instead of cnt[u].
+template <int THREADS>
 __device__ void scan_counts(const int32_t* cnt, int cnt_per_seq, int H, int units, int Lcap, int* pre,
                             int* wsum, int* err) {
-  const int per = (units + kAttThreads - 1) / kAttThreads;
+  const int per = (units + THREADS - 1) / THREADS;
   const int u0 = threadIdx.x * per;
   int local = 0;
   for (int u = u0; u < min(units, u0 + per); ++u) {
@@ -96,7 +104,7 @@ template <int D>
 __global__ void __launch_bounds__(kAttThreads) k5_attend(
     const __half* __restrict__ q, const __half* __restrict__ Kg, const __half* __restrict__ Vg,
     const int32_t* __restrict__ cnt, int cnt_per_seq, int H, int Lcap, int units, float scale,
-    float* __restrict__ ws, int* err) {
+    float* __restrict__ ws, int* __restrict__ gpre, int* err) {
   constexpr int VPR = D / 8;                    // lanes per row
   constexpr int RPW = 32 / VPR;                 // rows per warp step
   constexpr int NG = (kAttThreads / 32) * RPW;  // lane groups per CTA
@@ -104,7 +112,9 @@ __global__ void __launch_bounds__(kAttThreads) k5_attend(
   __shared__ int wsum[kAttThreads / 32];
   __shared__ float sm_m[NG], sm_l[NG];
   __shared__ float sm_acc[NG][D];
-  scan_counts(cnt, cnt_per_seq, H, units, Lcap, pre, wsum, err);
+  scan_counts<kAttThreads>(cnt, cnt_per_seq, H, units, Lcap, pre, wsum, err);
+  if (blockIdx.x == 0)  // the row prefix, for the combine
+    for (int i = threadIdx.x; i <= units; i += kAttThreads) gpre[i] = pre[i];
   const long long R = pre[units];
   int r0 = (int)(R * blockIdx.x / gridDim.x);
   const int r1 = (int)(R * (blockIdx.x + 1) / gridDim.x);
@@ -165,12 +175,12 @@ __global__ void __launch_bounds__(kAttThreads) k5_attend(
     __syncthreads();
     float M = -INFINITY;
     for (int i = 0; i < NG; ++i) M = fmaxf(M, sm_m[i]);
-    float* w = ws + ((size_t)u + blockIdx.x) * (D + 2);
+    float* w = ws + ((size_t)u + blockIdx.x) * (D + kPartHead);
     for (int dd = threadIdx.x; dd < D; dd += kAttThreads) {
       float o = 0.f;
       for (int i = 0; i < NG; ++i)
         if (sm_m[i] != -INFINITY) o += sm_acc[i][dd] * __expf(sm_m[i] - M);
-      w[2 + dd] = o;
+      w[kPartHead + dd] = o;
     }
     if (threadIdx.x == 0) {
       float Ls = 0.f;
@@ -185,6 +195,132 @@ __global__ void __launch_bounds__(kAttThreads) k5_attend(
   }
 }
 
+// Fused fetch + attention straight from the pinned pool.  The CTA's rows (the same balanced
+// split as above) are streamed as in the gather, without stopping at head boundaries: lane
+// group g takes rows start + g, start + g + NG, ..., kFaUnroll of them in flight, each with
+// its head's query chunk (loaded where the head changes), and keeps one online softmax for its
+// current head.  When its next
+// row belongs to another head it writes its partial to ws[(head + CTA) * NG + g] and starts
+// afresh, so a group writes one partial per head it touches and no CTA-wide barrier sits on
+// the load path.  Every slot is range-checked; a bad one is skipped and flagged.
+template <int D>
+__global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
+    const __half* __restrict__ q, const uint4* __restrict__ Kp, const uint4* __restrict__ Vp,
+    const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int H, int Lcap, int units,
+    int cap, float scale, float* __restrict__ ws, int* __restrict__ gpre, int* err) {
+  constexpr int VPR = D / 8;                  // lanes per row
+  constexpr int RPW = 32 / VPR;               // rows per warp step
+  constexpr int NG = (kFaThreads / 32) * RPW; // lane groups per CTA
+  extern __shared__ int pre[];                // [units + 1]
+  __shared__ int wsum[kFaThreads / 32];
+  scan_counts<kFaThreads>(cnt, 0, H, units, Lcap, pre, wsum, err);
+  if (blockIdx.x == 0)  // the row prefix, for the combine
+    for (int i = threadIdx.x; i <= units; i += kFaThreads) gpre[i] = pre[i];
+  const long long R = pre[units];
+  const int r0 = (int)(R * blockIdx.x / gridDim.x);
+  const int r1 = (int)(R * (blockIdx.x + 1) / gridDim.x);
+  if (r0 >= r1) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int v = lane % VPR, sub = lane / VPR, g = warp * RPW + sub;
+  int u;
+  {
+    int lo = 0, hi = units;  // first unit whose rows end after r0
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid + 1] <= r0) lo = mid + 1; else hi = mid;
+    }
+    u = lo;
+  }
+  int cur = -1;  // head of the running partial (and of qf)
+  float m = -INFINITY, l = 0.f, acc[8], qf[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = qf[i] = 0.f;
+  auto flush = [&]() {
+    // 16-byte aligned: ws is 256-byte aligned and (D + kPartHead) floats is a multiple of 16 B
+    float* w = ws + ((size_t)(cur + blockIdx.x) * NG + g) * (D + kPartHead);
+    *reinterpret_cast<float4*>(w + kPartHead + v * 8) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(w + kPartHead + 4 + v * 8) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (v == 0) {
+      w[0] = m;
+      w[1] = l;
+    }
+  };
+  // Software pipeline over batches of kFaUnroll rows per group: the loads of batch n + 1
+  // (index, then pool rows and, where the head changes, the query chunk) are issued before
+  // batch n is folded in, so the host link always has this group's rows in flight.
+  auto prepare = [&](int rw, int (&hu)[kFaUnroll], int (&slot)[kFaUnroll]) {
+#pragma unroll
+    for (int x = 0; x < kFaUnroll; ++x) {
+      const int rr = rw + sub + x * NG;
+      hu[x] = -1;
+      slot[x] = -1;
+      if (rr < r1) {
+        while (pre[u + 1] <= rr) ++u;
+        hu[x] = u;
+        const int sl = idx[(size_t)u * Lcap + (rr - pre[u])];
+        if (sl < 0 || sl >= cap) raise_error(err, IG_DEVERR_INDEX);
+        else slot[x] = sl;
+      }
+    }
+  };
+  // the query chunk is loaded only where the head changes (a group's rows mostly share one)
+  auto issue = [&](const int (&hu)[kFaUnroll], const int (&slot)[kFaUnroll], int prev, uint4 (&kv)[kFaUnroll],
+                   uint4 (&vv)[kFaUnroll], uint4 (&qv)[kFaUnroll]) {
+#pragma unroll
+    for (int x = 0; x < kFaUnroll; ++x) {
+      kv[x] = vv[x] = qv[x] = make_uint4(0, 0, 0, 0);
+      if (hu[x] >= 0 && hu[x] != (x == 0 ? prev : hu[x - 1]))
+        qv[x] = *reinterpret_cast<const uint4*>(q + (size_t)hu[x] * D + v * 8);
+      if (slot[x] >= 0) {
+        const size_t src = ((size_t)hu[x] * cap + slot[x]) * VPR + v;
+        kv[x] = ld_nc_v4(Kp + src);
+        vv[x] = ld_nc_v4(Vp + src);
+      }
+    }
+  };
+  int hu[kFaUnroll], slot[kFaUnroll], hn[kFaUnroll], sn[kFaUnroll];
+  uint4 kv[kFaUnroll], vv[kFaUnroll], qv[kFaUnroll], kn[kFaUnroll], vn[kFaUnroll], qn[kFaUnroll];
+  int rw = r0 + warp * RPW;
+  prepare(rw, hu, slot);
+  issue(hu, slot, -1, kv, vv, qv);
+  // warp-uniform trip count (the shuffles take the full mask); rows past the end compute on
+  // zeros and change nothing
+  while (rw < r1) {
+    const int rnext = rw + NG * kFaUnroll;
+    int last = cur;  // head of the last row of this batch (the query in use when the next starts)
+#pragma unroll
+    for (int x = 0; x < kFaUnroll; ++x) last = hu[x] >= 0 ? hu[x] : last;
+    prepare(rnext, hn, sn);
+    issue(hn, sn, last, kn, vn, qn);
+#pragma unroll
+    for (int x = 0; x < kFaUnroll; ++x) {
+      if (hu[x] >= 0 && hu[x] != cur) {  // a new head: hand over the previous one's partial
+        if (cur >= 0) flush();
+        cur = hu[x];
+        m = -INFINITY;
+        l = 0.f;
+        float2 a = h2_to_f2(qv[x].x), b = h2_to_f2(qv[x].y), c = h2_to_f2(qv[x].z), e = h2_to_f2(qv[x].w);
+        qf[0] = a.x * scale; qf[1] = a.y * scale; qf[2] = b.x * scale; qf[3] = b.y * scale;
+        qf[4] = c.x * scale; qf[5] = c.y * scale; qf[6] = e.x * scale; qf[7] = e.y * scale;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      }
+      const float z = group_sum<VPR>(lane_dot(qf, kv[x]));
+      if (slot[x] >= 0) online_add(z, vv[x], m, l, acc);
+    }
+#pragma unroll
+    for (int x = 0; x < kFaUnroll; ++x) {
+      hu[x] = hn[x];
+      slot[x] = sn[x];
+      kv[x] = kn[x];
+      vv[x] = vn[x];
+      qv[x] = qn[x];
+    }
+    rw = rnext;
+  }
+  if (cur >= 0) flush();
+}
+
 // CTA of the balanced grid whose row range holds row r (the last c with start(c) <= r).
 __device__ __forceinline__ int cta_of(long long r, long long R, int G) {
   int c = (int)((r * G) / R);
@@ -194,62 +330,43 @@ __device__ __forceinline__ int cta_of(long long r, long long R, int G) {
 }
 
 // One CTA (d threads) per head: merges the partials of the CTAs that covered its rows, adds
-// the current token, normalises.
-template <int D>
-__global__ void __launch_bounds__(D) k5_combine(const float* __restrict__ ws, const int32_t* __restrict__ cnt,
-                                                int cnt_per_seq, int H, int Lcap, int units, int G,
-                                                const __half* __restrict__ q,
+// the current token, normalises.  NGP partials per (head, CTA): 1 for the staged attention;
+// the lane-group count for the fused fetch, where group g of CTA cc holds a partial for the
+// head iff one of the head's rows in that CTA's range is g's (rows go round-robin to groups).
+template <int D, int NGP>
+__global__ void __launch_bounds__(D) k5_combine(const float* __restrict__ ws, const int* __restrict__ gpre,
+                                                int units, int G, const __half* __restrict__ q,
                                                 const __half* __restrict__ k_new,
                                                 const __half* __restrict__ v_new, float scale,
                                                 float* __restrict__ out) {
   __shared__ float red[D / 32];
-  __shared__ long long sh_lo, sh_R;
   const int u = blockIdx.x, dd = threadIdx.x;
-  // rows before this head and in total (clamped counts, as in the main kernel)
-  long long before = 0, total = 0;
-  for (int x = threadIdx.x; x < units; x += D) {
-    int c = cnt_per_seq ? cnt[x / H] : cnt[x];
-    c = c < 0 ? 0 : (c > Lcap ? Lcap : c);
-    total += c;
-    if (x < u) before += c;
-  }
-  for (int o = 16; o; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    total += __shfl_xor_sync(0xffffffffu, total, o);
-  }
-  __shared__ long long sb[D / 32], st[D / 32];
-  if ((threadIdx.x & 31) == 0) {
-    sb[threadIdx.x >> 5] = before;
-    st[threadIdx.x >> 5] = total;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    long long b = 0, t = 0;
-    for (int i = 0; i < D / 32; ++i) {
-      b += sb[i];
-      t += st[i];
-    }
-    sh_lo = b;
-    sh_R = t;
-  }
-  __syncthreads();
-  const long long lo = sh_lo, R = sh_R;
-  int c = cnt_per_seq ? cnt[u / H] : cnt[u];
-  c = c < 0 ? 0 : (c > Lcap ? Lcap : c);
+  // rows before this head, its rows and all rows (the main kernel's clamped prefix)
+  const long long lo = gpre[u], R = gpre[units];
+  const int c = gpre[u + 1] - gpre[u];
   float M = -INFINITY, Ls = 0.f, o = 0.f;
   if (c > 0) {
     // CTAs c0..c1 cover this head's rows; those with an empty range (fewer rows than CTAs)
     // wrote nothing and are skipped
     const int c0 = cta_of(lo, R, G), c1 = cta_of(lo + c - 1, R, G);
-    for (int cc = c0; cc <= c1; ++cc)
-      if ((R * cc) / G < (R * (cc + 1)) / G) M = fmaxf(M, ws[((size_t)u + cc) * (D + 2)]);
-    for (int cc = c0; cc <= c1; ++cc) {
-      if ((R * cc) / G == (R * (cc + 1)) / G) continue;
-      const float* w = ws + ((size_t)u + cc) * (D + 2);
-      if (w[0] == -INFINITY) continue;
-      const float f = __expf(w[0] - M);
-      Ls += w[1] * f;
-      o += w[2 + dd] * f;
+    for (int pass = 0; pass < 2; ++pass) {
+      for (int cc = c0; cc <= c1; ++cc) {
+        const long long s0 = (R * cc) / G, s1 = (R * (cc + 1)) / G;
+        if (s0 == s1) continue;
+        const long long a = lo > s0 ? lo : s0, e = (lo + c) < s1 ? (lo + c) : s1;
+        const long long n = e - a, off = (a - s0) % NGP;
+        for (int gi = 0; gi < NGP; ++gi) {
+          if (NGP > 1 && n < NGP && (gi - off + NGP) % NGP >= n) continue;
+          const float* w = ws + (((size_t)u + cc) * NGP + gi) * (D + kPartHead);
+          if (pass == 0) {
+            M = fmaxf(M, w[0]);
+          } else if (w[0] != -INFINITY) {
+            const float f = __expf(w[0] - M);
+            Ls += w[1] * f;
+            o += w[kPartHead + dd] * f;
+          }
+        }
+      }
     }
   }
   if (k_new) {
@@ -270,6 +387,18 @@ __global__ void __launch_bounds__(D) k5_combine(const float* __restrict__ ws, co
   out[(size_t)u * D + dd] = Ls > 0.f ? o / Ls : 0.f;
 }
 
+// workspace: the partials, then the row prefix [units + 1] ints
+inline size_t att_part_bytes(int B, int H, int d) {
+  return round_up((size_t)(B * H + kMaxAttCtas) * (d + kPartHead) * sizeof(float), 256);
+}
+template <int D>
+constexpr int fa_groups() { return (kFaThreads / 32) * (32 / (D / 8)); }
+inline size_t fa_part_bytes(int B, int H, int d) {
+  const int ng = d == 64 ? fa_groups<64>() : fa_groups<128>();
+  return round_up((size_t)(B * H + kMaxFaCtas) * ng * (d + kPartHead) * sizeof(float), 256);
+}
+inline size_t prefix_bytes(int B, int H) { return round_up((size_t)(B * H + 1) * sizeof(int), 256); }
+
 inline int att_grid() {
   int g = 4 * sm_count();
   return g > kMaxAttCtas ? kMaxAttCtas : g;
@@ -286,21 +415,43 @@ ig_status launch_attend(cudaStream_t st, int B, int H, int Lcap, float scale, co
     cudaError_t e = cudaFuncSetAttribute(k5_attend<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "attention smem attribute");
   }
-  k5_attend<D><<<G, kAttThreads, smem, st>>>(
-      reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(K),
-      reinterpret_cast<const __half*>(V), cnt, per_seq, H, Lcap, units, scale, static_cast<float*>(ws),
-      error_word());
+  int* gpre = reinterpret_cast<int*>(static_cast<char*>(ws) + att_part_bytes(B, H, D));
+  k5_attend<D><<<G, kAttThreads, smem, st>>>(reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(K),
+                                            reinterpret_cast<const __half*>(V), cnt, per_seq, H, Lcap, units,
+                                            scale, static_cast<float*>(ws), gpre, error_word());
   IG_CHECK_LAUNCH("attention launch");
-  k5_combine<D><<<units, D, 0, st>>>(static_cast<const float*>(ws), cnt, per_seq, H, Lcap, units, G,
-                                     reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(kn),
-                                     reinterpret_cast<const __half*>(vn), scale, out);
+  k5_combine<D, 1><<<units, D, 0, st>>>(static_cast<const float*>(ws), gpre, units, G,
+                                        reinterpret_cast<const __half*>(q), reinterpret_cast<const __half*>(kn),
+                                        reinterpret_cast<const __half*>(vn), scale, out);
   IG_CHECK_LAUNCH("attention combine launch");
   return IG_OK;
 }
 
-size_t attend_ws_bytes(int B, int H, int d) {
-  return round_up((size_t)(B * H + kMaxAttCtas) * (d + 2) * sizeof(float), 256);
+template <int D>
+ig_status launch_fetch_attend(cudaStream_t st, int B, int H, int Lcap, int cap, float scale, const uint16_t* q,
+                              const uint16_t* Kp, const uint16_t* Vp, const int32_t* idx, const int32_t* cnt,
+                              const uint16_t* kn, const uint16_t* vn, float* out, void* ws, int grid) {
+  const int units = B * H;
+  const size_t smem = (size_t)(units + 1) * sizeof(int);
+  if (smem > 32 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k5_fetch_attend<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "fetch-attention smem attribute");
+  }
+  int* gpre = reinterpret_cast<int*>(static_cast<char*>(ws) + fa_part_bytes(B, H, D));
+  k5_fetch_attend<D><<<grid, kFaThreads, smem, st>>>(
+      reinterpret_cast<const __half*>(q), reinterpret_cast<const uint4*>(Kp), reinterpret_cast<const uint4*>(Vp),
+      idx, cnt, H, Lcap, units, cap, scale, static_cast<float*>(ws), gpre, error_word());
+  IG_CHECK_LAUNCH("fetch-attention launch");
+  k5_combine<D, fa_groups<D>()><<<units, D, 0, st>>>(
+      static_cast<const float*>(ws), gpre, units, grid, reinterpret_cast<const __half*>(q),
+      reinterpret_cast<const __half*>(kn), reinterpret_cast<const __half*>(vn), scale, out);
+  IG_CHECK_LAUNCH("fetch-attention combine launch");
+  return IG_OK;
 }
+
+size_t fetch_attend_ws_bytes(int B, int H, int d) { return fa_part_bytes(B, H, d) + prefix_bytes(B, H); }
+
+size_t attend_ws_bytes(int B, int H, int d) { return att_part_bytes(B, H, d) + prefix_bytes(B, H); }
 
 ig_status attend_common(void* stream, int B, int H, int d, int Lcap, float scale,
                         const uint16_t* q, const uint16_t* K, const uint16_t* V,
@@ -348,4 +499,45 @@ extern "C" ig_status ig_dense_attend(void* stream, int B, int H, int d, int Lcap
                                      size_t workspace_bytes) {
   return attend_common(stream, B, H, d, Lcap, scale, q, K, V, L_valid, 1, k_new, v_new, out,
                        workspace, workspace_bytes);
+}
+
+extern "C" size_t ig_gather_attend_workspace_bytes(int B, int H, int d, int Lcap) {
+  if (B <= 0 || H <= 0 || (d != 64 && d != 128) || Lcap <= 0) return 0;
+  return fetch_attend_ws_bytes(B, H, d);
+}
+
+extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int layer, int B, int H,
+                                      int d, int Lcap, float scale, const uint16_t* q,
+                                      const int32_t* idx, const int32_t* cnt,
+                                      const uint16_t* k_new, const uint16_t* v_new, float* out,
+                                      void* workspace, size_t workspace_bytes, int max_ctas) {
+  IG_REQUIRE(pool, "null pool");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+  IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
+  IG_REQUIRE(B > 0 && H > 0 && Lcap > 0, "B, H, Lcap must be positive");
+  IG_REQUIRE(d == 64 || d == 128, "d must be 64 or 128 (got %d)", d);
+  IG_REQUIRE(B * H <= kMaxAttUnits, "B*H = %d exceeds %d", B * H, kMaxAttUnits);
+  IG_REQUIRE((long long)B * H * Lcap < (1ll << 31), "B*H*Lcap must stay below 2^31 rows");
+  IG_REQUIRE(q && idx && cnt && out, "null pointer argument");
+  IG_REQUIRE((k_new == nullptr) == (v_new == nullptr), "k_new and v_new go together");
+  IG_REQUIRE(aligned(q, 16), "q must be 16-byte aligned");
+  IG_REQUIRE(!k_new || (aligned(k_new, 16) && aligned(v_new, 16)), "k_new, v_new must be 16-byte aligned");
+  IG_REQUIRE(max_ctas >= 0 && max_ctas <= kMaxFaCtas, "max_ctas must be in [0, %d]", kMaxFaCtas);
+  const size_t need = fetch_attend_ws_bytes(B, H, d);
+  if (!workspace || workspace_bytes < need)
+    return fail(IG_ERR_CAPACITY, "fused fetch + attention needs %zu workspace bytes", need);
+  IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
+  // the same default as the gather: a quarter of the SMs saturates the host link
+  int grid = max_ctas > 0 ? max_ctas : sm_count() / 4;
+  if (grid < 1) grid = 1;
+  if (grid > kMaxFaCtas) grid = kMaxFaCtas;
+  const size_t layer_elems = (size_t)B * H * pool->cap * d;
+  const uint16_t* Kp = pool->Kdev + (size_t)layer * layer_elems;
+  const uint16_t* Vp = pool->Vdev + (size_t)layer * layer_elems;
+  cudaStream_t s = as_stream(stream);
+  if (d == 128)
+    return launch_fetch_attend<128>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, idx, cnt, k_new, v_new, out,
+                                    workspace, grid);
+  return launch_fetch_attend<64>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, idx, cnt, k_new, v_new, out,
+                                 workspace, grid);
 }

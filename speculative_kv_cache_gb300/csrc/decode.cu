@@ -12,6 +12,17 @@
 //        (attention(0) is the dense layer-0 attention, which needs no fetch)
 //   S: wait got[L-1], attention(L-1), append(L-1)
 // so layer 1 is speculated and its fetch starts before layer 0 attends.
+//
+// With config.fused_fetch the selected rows are not staged in HBM: the fetch stream runs the
+// attention itself, reading the rows from the pinned pool (ig_gather_attend):
+//   for l = 1 .. L-1:
+//     S: (l >= 3: wait att[l-2], the attention that yields layer l-1's input; append(l-2))
+//        speculate(l), select(l), record sel[l]
+//     G: wait sel[l], fetch + attention(l), record att[l]
+//     S: (l == 1) dense attention(0), append(0)
+//   S: wait att[L-2], append(L-2); wait att[L-1], append(L-1)
+// so the fetch stream does nothing but fetch and attend.  Selection l reuses index buffer
+// l % 2 only after attention(l-2) has finished with it.
 #include <vector>
 
 #include "ig_common.cuh"
@@ -26,6 +37,7 @@ struct ig_decoder {
   std::vector<const int32_t*> cols;
   ig_pool* pool = nullptr;
   std::vector<cudaEvent_t> ev_sel, ev_got, ev_att;
+  size_t ws_main = 0, ws_sel = 0, ws_fetch = 0;  // workspace regions: S, selection, G (fused fetch)
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // stage timing (optional): start/end of gather (G), speculate+select and attention+append
   // (S); two sets, alternating by step, indexed [parity * layers + layer]
@@ -59,14 +71,28 @@ void destroy_events(ig_decoder* d) {
 
 using namespace ig;
 
-extern "C" size_t ig_decoder_workspace_bytes(const ig_decoder_config* c) {
-  if (!c) return 0;
+namespace {
+
+// workspace regions: [main: speculation / selection-fused / S's attention][selection][fetch
+// stream's attention, fused fetch only]
+void ws_regions(const ig_decoder_config* c, size_t* main, size_t* sel, size_t* fetch) {
   size_t a = c->rope_theta > 0.f ? ig_speculate_rope_workspace_bytes(c->B, c->D, c->H, c->d, c->k)
                                   : ig_speculate_workspace_bytes(c->B, c->D, c->H, c->k);
-  size_t b = ig_attend_workspace_bytes(c->B, c->H, c->d, c->Lcap);
-  size_t s = ig_select_workspace_bytes(c->B, c->H);
-  size_t m = a > b ? a : b;
-  return m + round_up(s, 256);
+  const size_t f = ig_speculate_select_workspace_bytes(c->B, c->D, c->H, c->d, c->k, c->Lcap);
+  if (f > a) a = f;
+  const size_t b = ig_attend_workspace_bytes(c->B, c->H, c->d, c->Lcap);
+  *main = round_up(a > b ? a : b, 256);
+  *sel = round_up(ig_select_workspace_bytes(c->B, c->H), 256);
+  *fetch = c->fused_fetch ? round_up(ig_gather_attend_workspace_bytes(c->B, c->H, c->d, c->Lcap), 256) : 0;
+}
+
+}  // namespace
+
+extern "C" size_t ig_decoder_workspace_bytes(const ig_decoder_config* c) {
+  if (!c) return 0;
+  size_t m, s, f;
+  ws_regions(c, &m, &s, &f);
+  return m + s + f;
 }
 
 extern "C" ig_status ig_decoder_create(const ig_decoder_config* cfg, const ig_decoder_buffers* buf,
@@ -82,8 +108,10 @@ extern "C" ig_status ig_decoder_create(const ig_decoder_config* cfg, const ig_de
              "pool does not match the decoder");
   IG_REQUIRE(pool->cap <= c.Lcap, "pool capacity %d exceeds Lcap %d", pool->cap, c.Lcap);
   IG_REQUIRE(buf->Kpart && buf->cols && buf->K0 && buf->V0 && buf->scores && buf->idx && buf->cnt &&
-                 buf->Kg && buf->Vg && buf->workspace,
+                 buf->workspace,
              "missing decoder buffer");
+  IG_REQUIRE(c.fused_fetch || (buf->Kg && buf->Vg), "staged fetch needs Kg and Vg");
+  IG_REQUIRE(!c.fused_fetch || (c.d == 64 || c.d == 128), "fused fetch needs d = 64 or 128");
   if (c.rope_theta > 0.f)
     IG_REQUIRE(buf->Wq && buf->A_cols, "RoPE decoding needs Wq and A_cols");
   else
@@ -93,6 +121,7 @@ extern "C" ig_status ig_decoder_create(const ig_decoder_config* cfg, const ig_de
   d->cfg = c;
   d->buf = *buf;
   d->pool = pool;
+  ws_regions(&c, &d->ws_main, &d->ws_sel, &d->ws_fetch);
   const int L = c.layers;
   for (int l = 0; l < L; ++l) {
     d->Kpart.push_back(buf->Kpart[l]);
@@ -156,9 +185,10 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
   const int L = c.layers, B = c.B, H = c.H, d = c.d, D = c.D, k = c.k, Lc = c.Lcap;
   const size_t xs = (size_t)B * D, ts = (size_t)B * H * d;
   char* ws = static_cast<char*>(b.workspace);
-  const size_t spec_att_ws = b.workspace_bytes - round_up(ig_select_workspace_bytes(B, H), 256);
-  void* sel_ws = ws + spec_att_ws;
-  const size_t sel_ws_bytes = round_up(ig_select_workspace_bytes(B, H), 256);
+  const size_t spec_att_ws = dec->ws_main;
+  void* sel_ws = ws + dec->ws_main;
+  const size_t sel_ws_bytes = dec->ws_sel;
+  void* fetch_ws = ws + dec->ws_main + dec->ws_sel;
   ig_status st;
   cudaError_t e;
 
@@ -213,40 +243,96 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
   };
   dec->steps += 1;
 
-  if (L == 1) return timed_attend(0);
-  for (int l = 1; l < L; ++l) {
+  // speculation + selection of layer l on S; G then waits for it
+  auto spec_select = [&](int l) -> ig_status {
     float* sc = b.scores;
     int32_t* idx = b.idx + (size_t)(l & 1) * sz_scores(c);
     int32_t* cnt = b.cnt + (size_t)l * B * H;
     uint8_t* used = b.used ? b.used + (size_t)l * B * Lc : nullptr;
-    e = rec(dec->ts0, l, S);
-    if (e != cudaSuccess) return cuda_fail(e, "timing event");
+    cudaError_t se = rec(dec->ts0, l, S);
+    if (se != cudaSuccess) return cuda_fail(se, "timing event");
     const bool fused = c.fused_select && c.policy == IG_SEL_THRESHOLD && c.cap_frac >= 1.f && Lc <= 4096;
+    ig_status r;
     if (fused) {
       const bool rope = c.rope_theta > 0.f;
-      st = ig_speculate_select(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs,
-                               rope ? dec->Wq[l] : dec->Wq_part[l], rope ? dec->A_cols[l] : nullptr,
-                               rope ? io->positions : nullptr, c.rope_theta, dec->Kpart[l], io->L_valid,
-                               c.score_scale, c.alpha, idx, cnt, used, nullptr, nullptr, ws, spec_att_ws);
+      r = ig_speculate_select(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs,
+                              rope ? dec->Wq[l] : dec->Wq_part[l], rope ? dec->A_cols[l] : nullptr,
+                              rope ? io->positions : nullptr, c.rope_theta, dec->Kpart[l], io->L_valid,
+                              c.score_scale, c.alpha, idx, cnt, used, nullptr, nullptr, ws, spec_att_ws);
     } else if (c.rope_theta > 0.f) {
-      const int32_t* pos = io->positions;
-      st = ig_speculate_rope(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq[l],
-                             dec->A_cols[l], pos, c.rope_theta, dec->Kpart[l], io->L_valid,
-                             c.score_scale, sc, nullptr, ws, spec_att_ws);
+      r = ig_speculate_rope(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq[l],
+                            dec->A_cols[l], io->positions, c.rope_theta, dec->Kpart[l], io->L_valid,
+                            c.score_scale, sc, nullptr, ws, spec_att_ws);
     } else {
-      st = ig_speculate(S, B, D, H, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq_part[l],
-                        dec->Kpart[l], io->L_valid, c.score_scale, sc, nullptr, ws, spec_att_ws);
+      r = ig_speculate(S, B, D, H, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq_part[l],
+                       dec->Kpart[l], io->L_valid, c.score_scale, sc, nullptr, ws, spec_att_ws);
     }
-    if (st != IG_OK) return st;
+    if (r != IG_OK) return r;
     if (!fused) {
-      st = ig_select(S, B, H, Lc, sc, io->L_valid, c.alpha, c.policy, c.cap_frac, idx, cnt, used,
-                     sel_ws, sel_ws_bytes);
+      r = ig_select(S, B, H, Lc, sc, io->L_valid, c.alpha, c.policy, c.cap_frac, idx, cnt, used,
+                    sel_ws, sel_ws_bytes);
+      if (r != IG_OK) return r;
+    }
+    se = rec(dec->ts1, l, S);
+    if (se == cudaSuccess) se = cudaEventRecord(dec->ev_sel[l], S);
+    if (se == cudaSuccess) se = cudaStreamWaitEvent(G, dec->ev_sel[l], 0);
+    return se == cudaSuccess ? IG_OK : cuda_fail(se, "decode step events (select)");
+  };
+
+  if (L == 1) return timed_attend(0);
+  if (c.fused_fetch) {
+    // append(l) on S once the fetch stream's attention(l) has read the pool (the new token may
+    // overwrite an evicted slot) and speculation(l) has read the partial cache
+    auto append_after_fetch = [&](int l) -> ig_status {
+      cudaError_t ae = cudaStreamWaitEvent(S, dec->ev_att[l], 0);
+      if (ae == cudaSuccess) ae = rec(dec->ta0, l, S);
+      if (ae != cudaSuccess) return cuda_fail(ae, "decode step wait");
+      if (io->slot) {
+        const size_t off = (size_t)l * ts;
+        ig_status r = ig_append_kv(S, dec->pool, l, B, H, d, k, Lc, io->slot + (size_t)l * B, dec->cols[l],
+                                   io->k_new + off, io->v_new + off, dec->Kpart[l], nullptr, nullptr);
+        if (r != IG_OK) return r;
+      }
+      ae = rec(dec->ta1, l, S);
+      return ae == cudaSuccess ? IG_OK : cuda_fail(ae, "timing event");
+    };
+    for (int l = 1; l < L; ++l) {
+      if (l >= 3) {  // attention(l-2) yields layer l-1's input, which speculation(l) reads
+        st = append_after_fetch(l - 2);
+        if (st != IG_OK) return st;
+      }
+      st = spec_select(l);
+      if (st != IG_OK) return st;
+      e = rec(dec->tg0, l, G);
+      if (e != cudaSuccess) return cuda_fail(e, "timing event");
+      const size_t off = (size_t)l * ts;
+      st = ig_gather_attend(G, dec->pool, l, B, H, d, Lc, c.score_scale, io->q + off,
+                            b.idx + (size_t)(l & 1) * sz_scores(c), b.cnt + (size_t)l * B * H,
+                            io->k_new + off, io->v_new + off, io->out + off, fetch_ws, dec->ws_fetch,
+                            c.gather_ctas);
+      if (st != IG_OK) return st;
+      e = rec(dec->tg1, l, G);
+      if (e == cudaSuccess) e = cudaEventRecord(dec->ev_att[l], G);
+      if (e != cudaSuccess) return cuda_fail(e, "decode step events (fetch)");
+      if (l == 1) {
+        st = timed_attend(0);
+        if (st != IG_OK) return st;
+      }
+    }
+    for (int l = L - 2 > 1 ? L - 2 : 1; l < L; ++l) {
+      st = append_after_fetch(l);
       if (st != IG_OK) return st;
     }
-    e = rec(dec->ts1, l, S);
-    if (e == cudaSuccess) e = cudaEventRecord(dec->ev_sel[l], S);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(G, dec->ev_sel[l], 0);
-    if (e == cudaSuccess && l >= 3) e = cudaStreamWaitEvent(G, dec->ev_att[l - 2], 0);
+    e = cudaEventRecord(dec->ev_join, G);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(S, dec->ev_join, 0);
+    return e == cudaSuccess ? IG_OK : cuda_fail(e, "decode step join");
+  }
+  for (int l = 1; l < L; ++l) {
+    st = spec_select(l);
+    if (st != IG_OK) return st;
+    const int32_t* idx = b.idx + (size_t)(l & 1) * sz_scores(c);
+    const int32_t* cnt = b.cnt + (size_t)l * B * H;
+    if (l >= 3) e = cudaStreamWaitEvent(G, dec->ev_att[l - 2], 0);
     if (e == cudaSuccess) e = rec(dec->tg0, l, G);
     if (e != cudaSuccess) return cuda_fail(e, "decode step events (select)");
     const size_t buf = (size_t)(l & 1);

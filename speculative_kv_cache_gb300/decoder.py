@@ -24,7 +24,7 @@ from . import ig
 class Decoder:
     def __init__(self, *, layers, B, H, d, D, k, Lcap, pool_cap, alpha, policy=ig.IG_SEL_THRESHOLD,
                  cap_frac=1.0, score_scale=None, rope_theta=0.0, gather_ctas=0, stage_timing=False,
-                 graph=False, fused_select=True, device="cuda:0"):
+                 graph=False, fused_select=True, fused_fetch=False, device="cuda:0"):
         if pool_cap > Lcap or Lcap % 8:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
         self.layers, self.B, self.H, self.d, self.D, self.k, self.Lcap = layers, B, H, d, D, k, Lcap
@@ -38,7 +38,7 @@ class Decoder:
         self.cfg = ig.DecoderConfig(layers, B, H, d, D, k, Lcap, policy, float(alpha), float(cap_frac),
                                     float(score_scale if score_scale is not None else 1.0 / math.sqrt(d)),
                                     float(rope_theta), int(gather_ctas), int(bool(stage_timing)),
-                                    int(bool(fused_select)))
+                                    int(bool(fused_select)), int(bool(fused_fetch)))
         # per-layer state: partial query weight (or full W_Q and A[:, S] for RoPE), columns,
         # partial key cache; layer 0 keeps its full KV in HBM instead
         self.Wq_part = [None] + [e(H * k, D) for _ in range(1, layers)] if not self.rope else None
@@ -51,7 +51,8 @@ class Decoder:
         self.idx = e(2, B, H, Lcap, dt=i32)
         self.cnt = torch.zeros(layers, B, H, dtype=i32, device=self.dev)
         self.used = torch.zeros(layers, B, Lcap, dtype=torch.uint8, device=self.dev)
-        self.Kg, self.Vg = e(2, B, H, Lcap, d), e(2, B, H, Lcap, d)
+        # staging buffers of the fetched rows (none when the fetch stream attends from the pool)
+        self.Kg, self.Vg = (None, None) if fused_fetch else (e(2, B, H, Lcap, d), e(2, B, H, Lcap, d))
         self.ws = torch.empty(ig.ig_decoder_workspace_bytes(self.cfg), dtype=torch.uint8, device=self.dev)
         # control data of a step (double-buffered pinned host + device)
         self.L_host = [torch.zeros(B, dtype=i32).pin_memory() for _ in range(2)]
@@ -93,7 +94,8 @@ class Decoder:
         b.K0, b.V0 = self.K0.data_ptr(), self.V0.data_ptr()
         b.scores, b.idx, b.cnt = self.scores.data_ptr(), self.idx.data_ptr(), self.cnt.data_ptr()
         b.used = self.used.data_ptr()
-        b.Kg, b.Vg = self.Kg.data_ptr(), self.Vg.data_ptr()
+        b.Kg = self.Kg.data_ptr() if self.Kg is not None else None
+        b.Vg = self.Vg.data_ptr() if self.Vg is not None else None
         b.workspace, b.workspace_bytes = self.ws.data_ptr(), self.ws.numel()
         return b, arrs
 

@@ -78,6 +78,8 @@ _sig("ig_pool_counters", _i, _vp, _i, _i, _vp)
 _sig("ig_gather_kv", _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _i)
 _sig("ig_attend_workspace_bytes", _sz, _i, _i, _i, _i)
 _sig("ig_sparse_attend", _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz)
+_sig("ig_gather_attend_workspace_bytes", _sz, _i, _i, _i, _i)
+_sig("ig_gather_attend", _i, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i)
 _sig("ig_dense_attend", _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz)
 _sig("ig_append_kv", _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 
@@ -243,6 +245,17 @@ def ig_sparse_attend(stream, B, H, d, Lcap, scale, q, Kg, Vg, cnt, k_new, v_new,
         "ig_sparse_attend")
 
 
+def ig_gather_attend_workspace_bytes(B, H, d, Lcap):
+    return _lib.ig_gather_attend_workspace_bytes(B, H, d, Lcap)
+
+
+def ig_gather_attend(stream, pool, layer, B, H, d, Lcap, scale, q, idx, cnt, k_new, v_new, out,
+                     workspace, workspace_bytes, max_ctas=0):
+    _ok(_lib.ig_gather_attend(_s(stream), pool, layer, B, H, d, Lcap, scale, _p(q), _p(idx), _p(cnt),
+                              _p(k_new), _p(v_new), _p(out), _p(workspace), workspace_bytes, max_ctas),
+        "ig_gather_attend")
+
+
 def ig_dense_attend(stream, B, H, d, Lcap, scale, q, K, V, L_valid, k_new, v_new, out, workspace,
                     workspace_bytes):
     _ok(_lib.ig_dense_attend(_s(stream), B, H, d, Lcap, scale, _p(q), _p(K), _p(V), _p(L_valid),
@@ -271,7 +284,8 @@ def pool_layer_view(pool, layer, B, H, cap, d):
 class DecoderConfig(C.Structure):
     _fields_ = [("layers", _i), ("B", _i), ("H", _i), ("d", _i), ("D", _i), ("k", _i), ("Lcap", _i),
                 ("policy", _i), ("alpha", _f), ("cap_frac", _f), ("score_scale", _f),
-                ("rope_theta", _f), ("gather_ctas", _i), ("stage_timing", _i), ("fused_select", _i)]
+                ("rope_theta", _f), ("gather_ctas", _i), ("stage_timing", _i), ("fused_select", _i),
+                ("fused_fetch", _i)]
 
 
 class DecoderBuffers(C.Structure):

@@ -51,6 +51,21 @@ def test_invalid_arguments_are_rejected_before_any_device_work(ig):
     with pytest.raises(ig.IGError) as e:
         ig.ig_sparse_attend(0, 1, 1, 96, 8, 1.0, 16, 16, 16, 16, None, None, 16, None, 0)
     assert e.value.status == ig.IG_ERR_INVALID
+    with pytest.raises(ig.IGError) as e:
+        ig.ig_gather_attend(0, None, 0, 1, 1, 64, 8, 1.0, 16, 16, 16, None, None, 16, None, 0)
+    assert e.value.status == ig.IG_ERR_INVALID and "pool" in str(e.value)
+
+
+def test_decoder_fused_fetch_needs_no_staging_buffers_and_a_fetch_workspace(ig):
+    base = dict(layers=2, B=2, H=4, d=64, D=256, k=16, Lcap=64, policy=0, alpha=4.0, cap_frac=1.0,
+                score_scale=0.125, rope_theta=0.0, gather_ctas=0, stage_timing=0, fused_select=1)
+    staged = ig.ig_decoder_workspace_bytes(ig.DecoderConfig(**base, fused_fetch=0))
+    fused = ig.ig_decoder_workspace_bytes(ig.DecoderConfig(**base, fused_fetch=1))
+    # the fetch stream's attention gets a region of its own
+    assert fused - staged == ig.ig_gather_attend_workspace_bytes(2, 4, 64, 64)
+    # per-head partials of every lane group: (B*H + 256 CTAs) x 32 groups x (d + 2) floats
+    assert ig.ig_gather_attend_workspace_bytes(2, 4, 64, 64) >= (8 + 256) * 32 * 66 * 4
+    assert ig.ig_gather_attend_workspace_bytes(2, 4, 96, 64) == 0
 
 
 def test_workspace_sizes(ig):

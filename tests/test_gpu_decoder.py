@@ -44,7 +44,7 @@ def _layer_data(w, l, cap, rope):
     return dict(K=K, V=V, cols=cols, Wqp=synth.skewed_partial_weight(w, l))
 
 
-def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True):
+def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True, fused_fetch=False, graph=False):
     ig, decoder = mods
     dev = "cuda:0"
     Lcap = w.lcap
@@ -53,7 +53,7 @@ def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True):
     alpha = 4.0
     dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k,
                           Lcap=Lcap, pool_cap=cap, alpha=alpha, rope_theta=w.rope_theta,
-                          fused_select=fused_select, device=dev)
+                          fused_select=fused_select, fused_fetch=fused_fetch, graph=graph, device=dev)
     try:
         data = [_layer_data(w, l, cap, rope) for l in range(w.layers)]
         for l, dd in enumerate(data):
@@ -146,23 +146,33 @@ def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True):
 
 
 @pytest.mark.parametrize("fused", [True, False])
-def test_decoder_opt_shaped_steps(mods, fused):
+@pytest.mark.parametrize("fetch", ["staged", "fused"])
+def test_decoder_opt_shaped_steps(mods, fused, fetch):
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-opt", layers=3, batch=3, heads=6, hidden=768,
                      prompt=300, gen=8)
-    _run(mods, w, steps=3, fused_select=fused)
+    _run(mods, w, steps=3, fused_select=fused, fused_fetch=fetch == "fused")
 
 
-def test_decoder_capped_pool_evicts_like_the_oracle(mods):
+@pytest.mark.parametrize("fetch", ["staged", "fused"])
+def test_decoder_capped_pool_evicts_like_the_oracle(mods, fetch):
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-cap", layers=3, batch=2, heads=4, hidden=512,
                      prompt=200, gen=10, pool_frac=0.95)
     assert w.pool_cap < w.prompt + 10
-    _run(mods, w, steps=8, check_slots=True)
+    _run(mods, w, steps=8, check_slots=True, fused_fetch=fetch == "fused")
 
 
-def test_decoder_rope_steps(mods):
+@pytest.mark.parametrize("fetch", ["staged", "fused"])
+def test_decoder_rope_steps(mods, fetch):
     w = synth.scaled(synth.WORKLOADS["llama-2-7b"], name="dec-rope", layers=3, batch=2, heads=4,
                      hidden=512, prompt=260, gen=8)
-    _run(mods, w, steps=2, rope=True)
+    _run(mods, w, steps=2, rope=True, fused_fetch=fetch == "fused")
+
+
+def test_decoder_fused_fetch_graph_replay(mods):
+    """Fused fetch + attention under CUDA-graph replay, with eviction, against the oracle."""
+    w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-ffg", layers=3, batch=2, heads=4, hidden=512,
+                     prompt=200, gen=10, pool_frac=0.95)
+    _run(mods, w, steps=4, check_slots=True, fused_fetch=True, graph=True)
 
 
 def test_decoder_llama13b_width_capped_pool(mods):
@@ -173,7 +183,8 @@ def test_decoder_llama13b_width_capped_pool(mods):
     _run(mods, w, steps=3, rope=True, check_slots=True)
 
 
-def test_graph_replay_matches_eager_step(mods):
+@pytest.mark.parametrize("fused_fetch", [False, True])
+def test_graph_replay_matches_eager_step(mods, fused_fetch):
     """The CUDA-graph form of the step gives the same bytes as the eager step, step after step."""
     ig, decoder = mods
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-graph", layers=3, batch=2, heads=4, hidden=512,
@@ -183,7 +194,7 @@ def test_graph_replay_matches_eager_step(mods):
     for graph in (False, True):
         dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k,
                               Lcap=w.lcap, pool_cap=w.pool_cap, alpha=4.0, graph=graph, stage_timing=graph,
-                              device=dev)
+                              fused_fetch=fused_fetch, device=dev)
         try:
             for l in range(w.layers):
                 dd = _layer_data(w, l, w.pool_cap, False)

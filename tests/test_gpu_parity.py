@@ -209,6 +209,69 @@ def test_sparse_attend_matches_oracle(ig, name, with_new):
     assert err <= OUT_TOL, err
 
 
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("with_new", [True, False])
+@pytest.mark.parametrize("max_ctas", [0, 5, 256])
+def test_gather_attend_matches_oracle_and_staged_path(ig, pools, name, with_new, max_ctas):
+    """Fused fetch + attention straight from the pinned pool: the oracle's attention over the
+    selected rows, and the staged path (gather, then attention over the staged rows) up to
+    fp32 summation order."""
+    c = make_case(name)
+    w = c["w"]
+    B, H, d, Lcap = w.batch, w.heads, w.head_dim, c["Lcap"]
+    pool = _pool_for(ig, pools, c, name)
+    s32 = _quantised_scores(7, B, H, Lcap)
+    oi, oc, _ = ora.select(s32, c["L"], 1.5)
+    idx = np.zeros((B, H, Lcap), dtype=np.int32)
+    for b in range(B):
+        for h in range(H):
+            idx[b, h, :oc[b, h]] = oi[b][h]
+    kn = dev(c["kn"]) if with_new else None
+    vn = dev(c["vn"]) if with_new else None
+    ws = workspace(max(ig.ig_attend_workspace_bytes(B, H, d, Lcap), ig.ig_gather_attend_workspace_bytes(B, H, d, Lcap)))
+    out = empty((B, H, d), torch.float32)
+    q, idx_d, cnt_d = dev(c["q"]), dev(idx), dev(oc)
+    ig.ig_gather_attend(None, pool, 0, B, H, d, Lcap, float(c["scale"]), q, idx_d, cnt_d, kn, vn, out, ws,
+                        ws.numel(), max_ctas)
+    ig.ig_check()
+    Kg_o, Vg_o = ora.gather(c["K"], c["V"], oi, Lcap)
+    o = ora.attend(c["q"], Kg_o, Vg_o, oc, c["scale"], c["kn"] if with_new else None,
+                   c["vn"] if with_new else None)
+    got = host(out)
+    assert np.abs(got - o).max() <= OUT_TOL
+    Kg = torch.zeros((B, H, Lcap, d), dtype=torch.float16, device="cuda")
+    Vg = torch.zeros_like(Kg)
+    ig.ig_gather_kv(None, pool, 0, B, H, d, Lcap, idx_d, cnt_d, Kg, Vg, 0)
+    staged = empty((B, H, d), torch.float32)
+    ig.ig_sparse_attend(None, B, H, d, Lcap, float(c["scale"]), q, Kg, Vg, cnt_d, kn, vn, staged, ws,
+                        ws.numel())
+    ig.ig_check()
+    assert np.abs(got - host(staged)).max() <= 1e-5
+    # heads with nothing selected and no current token attend to nothing: exactly 0
+    if not with_new:
+        assert np.all(got[oc == 0] == 0.0)
+
+
+def test_gather_attend_guard_reports_out_of_range_slot(ig, pools):
+    c = make_case("tiny")
+    w = c["w"]
+    B, H, d, Lcap = w.batch, w.heads, w.head_dim, c["Lcap"]
+    pool = _pool_for(ig, pools, c, "tiny")
+    idx = np.zeros((B, H, Lcap), dtype=np.int32)
+    idx[0, 0, 1] = Lcap + 5  # beyond the pool: checked, skipped, flagged
+    cnt = np.full((B, H), 2, dtype=np.int32)
+    ws = workspace(ig.ig_gather_attend_workspace_bytes(B, H, d, Lcap))
+    out = empty((B, H, d), torch.float32)
+    ig.ig_gather_attend(None, pool, 0, B, H, d, Lcap, float(c["scale"]), dev(c["q"]), dev(idx), dev(cnt),
+                        None, None, out, ws, ws.numel(), 0)
+    with pytest.raises(ig.IGError) as e:
+        ig.ig_check()
+    assert e.value.status == ig.IG_ERR_INVALID
+    ig.ig_check()
+    # the head with the bad slot attended to its one valid row (slot 0) only: out = V[slot 0]
+    assert np.abs(host(out)[0, 0] - c["V"][0, 0, 0].astype(np.float32)).max() <= 1e-3
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged", "opt-30b"])
 def test_dense_attend_is_full_attention(ig, name):
     c = make_case(name)
