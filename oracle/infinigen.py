@@ -26,7 +26,12 @@ Readings taken where the page is silent or garbled (each is listed in the design
   * the transfer cap and the averaged count keep the best tokens by (score desc, index asc);
   * pool counters are 8-bit, +1 per (layer, step) when any head selected the slot, halved
     for the whole (layer, sequence) pool when one of them reaches 255; the victim is the
-    smallest counter, then the oldest insertion, then the lowest slot.
+    smallest counter, then the oldest insertion, then the lowest slot;
+  * FIFO evicts the oldest insertion; LRU evicts the slot whose last selection (by any head)
+    is oldest, where entering the pool counts as a selection at that moment, ties going to
+    the oldest insertion;
+  * an eviction miss is a token that selection over every token seen so far would pick but
+    that the pool no longer holds.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test (closed forms,
 values the page prints, brute force on tiny inputs).  Two choices are consistency-checked
@@ -406,6 +411,114 @@ class CounterPool:
         if used is not None:
             self.update(used)
         return self.insert()
+
+
+class FifoPool:
+    """One (layer, sequence) pool with first-in-first-out eviction.
+
+    Section 3.4, "KV Cache Pool Management Under Memory Pressure" (the FIFO policy of
+    Table 2): the victim is the entry that has been in the pool longest.  Use does not
+    matter, so ``update`` only checks its argument.
+    """
+
+    def __init__(self, cap: int):
+        self.cap = cap
+        self.seq = np.zeros(cap, dtype=np.int64)
+        self.filled = 0
+        self.next_seq = 0
+
+    def update(self, used) -> None:
+        np.asarray(used)
+
+    def insert(self) -> int:
+        if self.filled < self.cap:
+            slot = self.filled
+            self.filled += 1
+        else:
+            slot = int(np.argmin(self.seq))  # insertion numbers are unique
+        self.seq[slot] = self.next_seq
+        self.next_seq += 1
+        return slot
+
+    def evict(self, used) -> int:
+        if used is not None:
+            self.update(used)
+        return self.insert()
+
+
+class LruPool:
+    """One (layer, sequence) pool with least-recently-used eviction.
+
+    Section 3.4, "KV Cache Pool Management Under Memory Pressure" (the LRU policy of
+    Table 2): the victim is the entry selected for prefetching least recently by any head.
+    Time advances by one per update; a slot used in an update takes that time, a new entry
+    takes the time of its insertion; the victim has the oldest time, then the oldest
+    insertion, then the lowest slot.
+    """
+
+    def __init__(self, cap: int):
+        self.cap = cap
+        self.last = np.zeros(cap, dtype=np.int64)
+        self.seq = np.zeros(cap, dtype=np.int64)
+        self.clock = 0
+        self.filled = 0
+        self.next_seq = 0
+
+    def update(self, used) -> None:
+        used = np.asarray(used)[: self.cap]
+        self.clock += 1
+        for s in range(self.filled):
+            if used[s]:
+                self.last[s] = self.clock
+
+    def insert(self) -> int:
+        if self.filled < self.cap:
+            slot = self.filled
+            self.filled += 1
+        else:
+            slot = int(np.lexsort((np.arange(self.cap), self.seq, self.last))[0])
+        self.last[slot] = self.clock
+        self.seq[slot] = self.next_seq
+        self.next_seq += 1
+        return slot
+
+    def evict(self, used) -> int:
+        if used is not None:
+            self.update(used)
+        return self.insert()
+
+
+POOL_COUNTER, POOL_FIFO, POOL_LRU = 0, 1, 2
+
+
+def make_pool(cap: int, policy: int):
+    """The pool model for one of the three victim policies of Table 2."""
+    return {POOL_COUNTER: CounterPool, POOL_FIFO: FifoPool, POOL_LRU: LruPool}[policy](cap)
+
+
+def eviction_misses(scores, idx, cnt, resident):
+    """Selections of tokens the pool no longer holds (diagnostic, not a step of the method).
+
+    ``scores`` [B, H, T] are speculated scores over every token seen so far (token index t),
+    ``idx``/``cnt`` the selection over them, ``resident`` [B, T] whether token t is in the pool.
+    Returns (miss count [B, H], miss mass [B, H]): the mass is the share of the selected
+    tokens' softmax weight, exp(s_t - m) over the selected set, that falls on missed tokens.
+    """
+    scores = np.asarray(scores, dtype=np.float64)
+    B, H = np.asarray(cnt).shape
+    n_miss = np.zeros((B, H), dtype=np.int64)
+    mass = np.zeros((B, H), dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            sel = [int(t) for t in idx[b][h][: cnt[b][h]]]
+            if not sel:
+                continue
+            m = max(scores[b, h, t] for t in sel)
+            w = {t: math.exp(scores[b, h, t] - m) for t in sel}
+            missed = [t for t in sel if not resident[b][t]]
+            n_miss[b, h] = len(missed)
+            mass[b, h] = sum(w[t] for t in missed) / sum(w.values())
+    return n_miss, mass
 
 
 # ----------------------------------------------------------------------------------------

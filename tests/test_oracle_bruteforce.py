@@ -206,3 +206,84 @@ def test_p13_pool_brute_force_against_slot_history():
         nxt += 1
         owner[want] = t
         assert got == want
+
+
+# --- pool policies of Table 2: FIFO and LRU ---------------------------------------------------
+def test_fifo_pool_cycles_the_slots_and_keeps_the_newest():
+    p = ora.FifoPool(5)
+    slots = [p.evict(np.ones(5, np.uint8)) for _ in range(17)]
+    # free slots in order, then the oldest entry: slot t mod 5 whatever the use
+    assert slots == [t % 5 for t in range(17)]
+    # the resident tokens are the last 5 inserted (token numbers 12..16)
+    assert sorted(p.seq.tolist()) == list(range(12, 17))
+
+
+def _lru_list_model(cap, steps, use_prob, seed):
+    """Textbook LRU with an ordered list (least recent first): a use moves the entry to the
+    most-recent end, an insertion appends there, the victim is the first entry.  Entries used
+    in the same update move in insertion order, so the newest of them ends most recent."""
+    g = np.random.default_rng(seed)
+    order = []          # token numbers, least recent first
+    slot_of = {}        # token -> slot
+    free = list(range(cap))
+    out = []
+    for t in range(steps):
+        used = (g.random(cap) < use_prob).astype(np.uint8)
+        if t:
+            tokens_used = sorted(tok for tok, s in slot_of.items() if used[s])
+            for tok in tokens_used:
+                order.remove(tok)
+                order.append(tok)
+        if free:
+            s = free.pop(0)
+        else:
+            victim = order.pop(0)
+            s = slot_of.pop(victim)
+        slot_of[t] = s
+        order.append(t)
+        out.append((s, used if t else None))
+    return out
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("cap,use_prob", [(4, 0.3), (7, 0.1), (9, 0.6)])
+def test_lru_pool_equals_the_textbook_list_lru(seed, cap, use_prob):
+    hist = _lru_list_model(cap, 80, use_prob, seed)
+    p = ora.LruPool(cap)
+    for want, used in hist:
+        assert p.evict(used) == want
+
+
+def test_lru_keeps_a_hot_entry_that_fifo_drops():
+    lru, fifo = ora.LruPool(3), ora.FifoPool(3)
+    for _ in range(3):
+        lru.insert(), fifo.insert()
+    # slot 0 (the oldest token) is used at every step
+    for _ in range(6):
+        u = np.array([1, 0, 0], np.uint8)
+        s_l, s_f = lru.evict(u), fifo.evict(u)
+        assert s_l != 0
+    assert 0 in lru.seq.tolist() and 0 not in fifo.seq.tolist()
+
+
+def test_make_pool_dispatch():
+    assert isinstance(ora.make_pool(3, ora.POOL_COUNTER), ora.CounterPool)
+    assert isinstance(ora.make_pool(3, ora.POOL_FIFO), ora.FifoPool)
+    assert isinstance(ora.make_pool(3, ora.POOL_LRU), ora.LruPool)
+
+
+def test_eviction_misses_closed_form():
+    # one head, tokens 0..3 selected with scores 0, -1, -2, -3; tokens 1 and 3 are gone
+    scores = np.array([[[0.0, -1.0, -2.0, -3.0]]])
+    idx = [[np.array([0, 1, 2, 3])]]
+    cnt = np.array([[4]])
+    resident = np.array([[1, 0, 1, 0]], bool)
+    n, mass = ora.eviction_misses(scores, idx, cnt, resident)
+    e = np.exp(-np.arange(4.0))
+    assert n[0, 0] == 2
+    assert mass[0, 0] == pytest.approx((e[1] + e[3]) / e.sum(), rel=1e-15)
+    # nothing evicted, or nothing selected: no misses
+    n, mass = ora.eviction_misses(scores, idx, cnt, np.ones((1, 4), bool))
+    assert n[0, 0] == 0 and mass[0, 0] == 0.0
+    n, mass = ora.eviction_misses(scores, idx, np.array([[0]]), resident)
+    assert n[0, 0] == 0 and mass[0, 0] == 0.0
