@@ -47,6 +47,8 @@ def parse_args(argv=None):
     p.add_argument("--gather-ctas", type=int, default=0)
     p.add_argument("--graph", type=int, default=1, help="1: replay each step from a CUDA graph")
     p.add_argument("--fused-select", type=int, default=1, help="1: fused cluster score+select kernel")
+    p.add_argument("--pool-policy", default="counter", choices=["counter", "fifo", "lru"],
+                   help="victim policy of a capacity-limited pool (workloads with pool_frac < 1)")
     p.add_argument("--fused-fetch", type=int, default=0,
                    help="1: layers 1.. attend straight from the pinned pool on the fetch stream (no staging)")
     p.add_argument("--no-e2e", action="store_true")
@@ -245,14 +247,14 @@ def link_peak_gbs(torch) -> float:
 
 
 def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True,
-                  fused_fetch=False):
+                  fused_fetch=False, pool_policy=0):
     from speculative_kv_cache_gb300.decoder import Decoder
 
     Lcap = w.lcap
     dec = Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=Lcap,
                   pool_cap=w.pool_cap, alpha=alpha, rope_theta=w.rope_theta, gather_ctas=gather_ctas,
                   stage_timing=True, graph=bool(graph), fused_select=bool(fused_select),
-                  fused_fetch=bool(fused_fetch), device=device)
+                  fused_fetch=bool(fused_fetch), pool_policy=pool_policy, device=device)
     gen = torch.Generator(device=device)
     shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
@@ -351,8 +353,9 @@ def run_ours(args, w, alpha):
     if w.prompt + steps_total > w.context:
         raise SystemExit(f"warmup + steps (+ e2e steps) must stay within the {w.gen} generated tokens")
     fused_fetch = bool(args.fused_fetch)
+    pool_policy = {"counter": ig.IG_POOL_COUNTER, "fifo": ig.IG_POOL_FIFO, "lru": ig.IG_POOL_LRU}[args.pool_policy]
     dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph,
-                                          args.fused_select, fused_fetch)
+                                          args.fused_select, fused_fetch, pool_policy)
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
@@ -450,7 +453,8 @@ def run_ours(args, w, alpha):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "fp16 storage, fp32 accumulate", "data": "synthetic (seeded, random-init weights)",
             "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph),
-                           fused_select=bool(args.fused_select), fused_fetch=fused_fetch),
+                           fused_select=bool(args.fused_select), fused_fetch=fused_fetch,
+                           pool_policy=args.pool_policy if w.pool_frac < 1 else None),
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "selected_fraction": float(f),
             "link_gbs": G_total / args.steps / (ms_per_step * 1e-3) / 1e9,

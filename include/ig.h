@@ -195,7 +195,25 @@ ig_status ig_speculate_select(void* stream, int B, int D, int H, int d, int k, i
  * access counter used by ig_pool_evict. */
 typedef struct ig_pool ig_pool;
 
+/* Victim policies (section 3.4, pool management, and the three policies of Table 2).
+ * Ties always go to the oldest insertion, then the lowest slot.
+ *   IG_POOL_COUNTER  smallest 8-bit use counter (the policy InfiniGen uses; the default)
+ *   IG_POOL_FIFO     oldest insertion
+ *   IG_POOL_LRU      oldest last use by any head; a new entry counts as used when it is
+ *                    inserted, and each folded step advances the pool's time by one */
+#define IG_POOL_COUNTER 0
+#define IG_POOL_FIFO 1
+#define IG_POOL_LRU 2
+/* ig_pool_create_ex flags.  IG_POOL_NO_STORAGE: the slot manager alone (no pinned K/V rows,
+ * H and d ignored; needs no GPU), for host-side simulation of a policy; the calls that move
+ * rows (ig_pool_kv, ig_pool_write, ig_gather_kv, ig_gather_attend, ig_append_kv with this
+ * pool) then return IG_ERR_INVALID. */
+#define IG_POOL_NO_STORAGE 1
+
 ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out);
+/* ig_pool_create with a victim policy (IG_POOL_*) and flags (0 or IG_POOL_NO_STORAGE). */
+ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap, int policy, int flags,
+                            ig_pool** out);
 ig_status ig_pool_destroy(ig_pool* pool);
 
 /* Host pointers (also valid on the device) to one layer's K and V arrays. */
@@ -206,12 +224,13 @@ ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V)
 ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const uint16_t* K,
                         const uint16_t* V);
 
-/* Host-side counter-based pool manager for one (layer, sequence), run once per decode step.
- * Section 3.4, pool management (counter policy of Table 2): every slot that any head chose
- * this step (used[slot] != 0) gains 1, saturating at 255; when a counter reaches 255 all
- * counters of that pool are halved.  Then the new token gets a slot: the next free slot
- * while the pool is not full, otherwise the victim with the smallest counter (then the
- * oldest insertion, then the lowest slot).  The new slot's counter starts at 0.
+/* Host-side pool manager for one (layer, sequence), run once per decode step.  Section 3.4,
+ * pool management (counter policy of Table 2): every slot that any head chose this step
+ * (used[slot] != 0) gains 1, saturating at 255; when a counter reaches 255 all counters of
+ * that pool are halved; the slot's last-use time becomes the current step (for LRU).  Then
+ * the new token gets a slot: the next free slot while the pool is not full, otherwise the
+ * victim of the pool's policy (the smallest counter by default; see IG_POOL_*).  The new
+ * slot's counter starts at 0.
  *   used      host uint8 [cap] or NULL (no use to record, e.g. during prefill)
  *   slot_out  host int32: the slot the new token must be written to (ig_append_kv)
  *   filled_out host int32 or NULL: resident slots after the insertion */
@@ -220,6 +239,14 @@ ig_status ig_pool_evict(ig_pool* pool, int layer, int b, const uint8_t* used,
 
 /* Reads one (layer, sequence)'s counters (host uint8 [cap]). */
 ig_status ig_pool_counters(const ig_pool* pool, int layer, int b, uint8_t* out);
+
+/* Which token each slot of one (layer, sequence) holds: out host int32 [cap], the token's
+ * insertion number (prompt tokens 0..n-1 in prefill order, then one per decode step, so the
+ * token's position when every step inserts one token), -1 for a free slot. */
+ig_status ig_pool_slot_tokens(const ig_pool* pool, int layer, int b, int32_t* out);
+
+/* Number of placements into a full (layer, sequence) pool so far (host int64). */
+ig_status ig_pool_evictions(const ig_pool* pool, int layer, int b, int64_t* out);
 
 /* ------------------------------------------------------------------------------------
  * Gather of the chosen full key/value rows from the host pool into HBM.  Section 3.4,
@@ -395,6 +422,23 @@ ig_status ig_pool_prefill(ig_pool* pool, int n_tokens, int32_t* slots_out);
  * any pool is full, i.e. whether placement depends on the counters. */
 ig_status ig_pool_step(ig_pool* pool, const uint8_t* used, int Lcap, int32_t* slots_out);
 ig_status ig_pool_full(const ig_pool* pool, int* any_full);
+
+/* Diagnostic of a capacity-limited pool (not a step of the method; section 3.4, pool
+ * management): how much of a selection falls on tokens the pool has evicted.  Selection runs
+ * over every token seen so far, indexed by token number t (a partial key cache that keeps
+ * every token, scored by ig_speculate and selected by ig_select); the pool's slot -> token
+ * map (ig_pool_slot_tokens) gives `resident`.  Per (b, h):
+ *   miss_cnt  = |{ j < cnt : resident[b][idx_j] == 0 }|
+ *   miss_mass = sum over missed j of exp(s_j - m) / sum over all j < cnt of exp(s_j - m),
+ *               m = the largest selected score (0 when nothing is selected)
+ *   scores    dev fp32 [B][H][Lcap]  by token number
+ *   idx, cnt  dev int32 [B][H][Lcap], [B][H]  (token numbers < Lcap; others raise
+ *             IG_DEVERR_INDEX and are skipped)
+ *   resident  dev uint8 [B][Lcap]
+ *   miss_cnt  dev int32 [B][H] out;  miss_mass dev fp32 [B][H] out */
+ig_status ig_eviction_misses(void* stream, int B, int H, int Lcap, const float* scores,
+                             const int32_t* idx, const int32_t* cnt, const uint8_t* resident,
+                             int32_t* miss_cnt, float* miss_mass);
 
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t ig_launch_count(void);

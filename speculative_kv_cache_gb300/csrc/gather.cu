@@ -123,6 +123,7 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
                                   int d, int Lcap, const int32_t* idx, const int32_t* cnt,
                                   uint16_t* Kg, uint16_t* Vg, int max_ctas) {
   IG_REQUIRE(pool, "null pool");
+  IG_REQUIRE(pool->storage, "the pool was created without storage");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
   IG_REQUIRE(Lcap > 0 && idx && cnt && Kg && Vg, "bad Lcap or null pointer");

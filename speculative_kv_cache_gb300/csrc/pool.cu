@@ -1,7 +1,7 @@
-// KV cache pool in pinned, mapped host memory and its counter-based manager (InfiniGen
-// paper-graph summary, section 3.4, "KV Cache Pool Management Under Memory Pressure", counter
-// policy of Table 2), plus the append of the current token ("Partial Key Cache Updates
-// During Decoding").
+// KV cache pool in pinned, mapped host memory and its slot manager (InfiniGen paper-graph
+// summary, section 3.4, "KV Cache Pool Management Under Memory Pressure"): the counter policy
+// InfiniGen uses and the FIFO and LRU policies it is compared with in Table 2, plus the
+// append of the current token ("Partial Key Cache Updates During Decoding").
 #include <stdlib.h>
 #include <string.h>
 
@@ -73,55 +73,73 @@ __global__ void k6_append(uint4* __restrict__ Kp, uint4* __restrict__ Vp, int ca
 
 using namespace ig;
 
-extern "C" ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out) {
+extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap, int policy,
+                                        int flags, ig_pool** out) {
   IG_REQUIRE(out, "null out");
   *out = nullptr;
-  IG_REQUIRE(layers > 0 && B > 0 && H > 0 && d > 0 && cap > 0, "pool sizes must be positive");
-  IG_REQUIRE(d % 8 == 0, "d must be a multiple of 8 (16-byte rows)");
-  const size_t elems = (size_t)layers * B * H * cap * d;
+  IG_REQUIRE(policy == IG_POOL_COUNTER || policy == IG_POOL_FIFO || policy == IG_POOL_LRU,
+             "unknown pool policy %d", policy);
+  IG_REQUIRE((flags & ~IG_POOL_NO_STORAGE) == 0, "unknown pool flags 0x%x", flags);
+  const bool storage = !(flags & IG_POOL_NO_STORAGE);
+  IG_REQUIRE(layers > 0 && B > 0 && cap > 0, "pool sizes must be positive");
+  IG_REQUIRE(!storage || (H > 0 && d > 0), "a pool with storage needs H, d > 0");
+  IG_REQUIRE(!storage || d % 8 == 0, "d must be a multiple of 8 (16-byte rows)");
   if (fault_injected("pool_alloc")) return fail(IG_ERR_OOM, "injected pinned-allocation failure");
   ig_pool* p = new (std::nothrow) ig_pool();
   if (!p) return fail(IG_ERR_OOM, "host allocation of the pool header failed");
   p->layers = layers;
   p->B = B;
-  p->H = H;
-  p->d = d;
+  p->H = storage ? H : 0;
+  p->d = storage ? d : 0;
   p->cap = cap;
-  const unsigned flags = cudaHostAllocMapped | cudaHostAllocPortable;
-  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&p->K), elems * 2, flags);
-  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&p->V), elems * 2, flags);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    if (p->K) cudaFreeHost(p->K);
-    delete p;
-    return fail(IG_ERR_OOM, "pinned allocation of 2 x %zu bytes failed: %s", elems * 2,
-                cudaGetErrorString(e));
+  p->policy = policy;
+  p->storage = storage;
+  if (storage) {
+    const size_t elems = (size_t)layers * B * H * cap * d;
+    const unsigned hflags = cudaHostAllocMapped | cudaHostAllocPortable;
+    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&p->K), elems * 2, hflags);
+    if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&p->V), elems * 2, hflags);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      if (p->K) cudaFreeHost(p->K);
+      delete p;
+      return fail(IG_ERR_OOM, "pinned allocation of 2 x %zu bytes failed: %s", elems * 2,
+                  cudaGetErrorString(e));
+    }
+    void* kd = nullptr;
+    void* vd = nullptr;
+    e = cudaHostGetDevicePointer(&kd, p->K, 0);
+    if (e == cudaSuccess) e = cudaHostGetDevicePointer(&vd, p->V, 0);
+    if (e != cudaSuccess) {
+      cudaFreeHost(p->K);
+      cudaFreeHost(p->V);
+      delete p;
+      return cuda_fail(e, "device pointer of the pinned pool");
+    }
+    p->Kdev = static_cast<uint16_t*>(kd);
+    p->Vdev = static_cast<uint16_t*>(vd);
   }
-  void* kd = nullptr;
-  void* vd = nullptr;
-  e = cudaHostGetDevicePointer(&kd, p->K, 0);
-  if (e == cudaSuccess) e = cudaHostGetDevicePointer(&vd, p->V, 0);
-  if (e != cudaSuccess) {
-    cudaFreeHost(p->K);
-    cudaFreeHost(p->V);
-    delete p;
-    return cuda_fail(e, "device pointer of the pinned pool");
-  }
-  p->Kdev = static_cast<uint16_t*>(kd);
-  p->Vdev = static_cast<uint16_t*>(vd);
   try {
-    p->counter.assign((size_t)layers * B * cap, 0);
-    p->seq.assign((size_t)layers * B * cap, 0);
-    p->filled.assign((size_t)layers * B, 0);
-    p->next_seq.assign((size_t)layers * B, 0);
+    const size_t npb = (size_t)layers * B;
+    p->counter.assign(npb * cap, 0);
+    p->seq.assign(npb * cap, 0);
+    p->filled.assign(npb, 0);
+    p->next_seq.assign(npb, 0);
+    p->last_use.assign(npb * cap, 0);
+    p->clock.assign(npb, 0);
+    p->evictions.assign(npb, 0);
   } catch (...) {
-    cudaFreeHost(p->K);
-    cudaFreeHost(p->V);
+    if (p->K) cudaFreeHost(p->K);
+    if (p->V) cudaFreeHost(p->V);
     delete p;
-    return fail(IG_ERR_OOM, "host allocation of pool counters failed");
+    return fail(IG_ERR_OOM, "host allocation of the pool manager failed");
   }
   *out = p;
   return IG_OK;
+}
+
+extern "C" ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out) {
+  return ig_pool_create_ex(layers, B, H, d, cap, IG_POOL_COUNTER, 0, out);
 }
 
 extern "C" ig_status ig_pool_destroy(ig_pool* pool) {
@@ -136,6 +154,7 @@ extern "C" ig_status ig_pool_destroy(ig_pool* pool) {
 
 extern "C" ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V) {
   IG_REQUIRE(pool && K && V, "null argument");
+  IG_REQUIRE(pool->storage, "the pool was created without storage");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
   *K = pool->K + (size_t)layer * le;
@@ -146,107 +165,13 @@ extern "C" ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, ui
 extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const uint16_t* K,
                                    const uint16_t* V) {
   IG_REQUIRE(pool && K && V, "null argument");
+  IG_REQUIRE(pool->storage, "the pool was created without storage");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
   cudaStream_t s = as_stream(stream);
   cudaError_t e = cudaMemcpyAsync(pool->K + (size_t)layer * le, K, le * 2, cudaMemcpyDefault, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(pool->V + (size_t)layer * le, V, le * 2, cudaMemcpyDefault, s);
   if (e != cudaSuccess) return cuda_fail(e, "pool write");
-  return IG_OK;
-}
-
-namespace {
-void fold_use(ig_pool* pool, size_t pb, const uint8_t* used) {
-  const int cap = pool->cap;
-  uint8_t* cnt = pool->counter.data() + pb * cap;
-  const int filled = pool->filled[pb];
-  bool sat = false;
-  for (int s = 0; s < filled; ++s) {
-    if (used[s] && cnt[s] < 255) ++cnt[s];
-    sat |= (cnt[s] == 255);
-  }
-  if (sat)
-    for (int s = 0; s < filled; ++s) cnt[s] >>= 1;
-}
-}  // namespace
-
-extern "C" ig_status ig_pool_update(ig_pool* pool, int layer, int b, const uint8_t* used) {
-  IG_REQUIRE(pool && used, "null argument");
-  IG_REQUIRE(layer >= 0 && layer < pool->layers && b >= 0 && b < pool->B, "layer/b out of range");
-  fold_use(pool, (size_t)layer * pool->B + b, used);
-  return IG_OK;
-}
-
-namespace {
-int place(ig_pool* pool, size_t pb);
-}  // namespace
-
-extern "C" ig_status ig_pool_evict(ig_pool* pool, int layer, int b, const uint8_t* used,
-                                   int32_t* slot_out, int32_t* filled_out) {
-  IG_REQUIRE(pool && slot_out, "null argument");
-  IG_REQUIRE(layer >= 0 && layer < pool->layers && b >= 0 && b < pool->B, "layer/b out of range");
-  const size_t pb = (size_t)layer * pool->B + b;
-  if (used) fold_use(pool, pb, used);
-  *slot_out = place(pool, pb);
-  if (filled_out) *filled_out = pool->filled[pb];
-  return IG_OK;
-}
-
-namespace {
-int place(ig_pool* pool, size_t pb) {
-  const int cap = pool->cap;
-  uint8_t* cnt = pool->counter.data() + pb * cap;
-  uint32_t* seq = pool->seq.data() + pb * cap;
-  int32_t& filled = pool->filled[pb];
-  int slot;
-  if (filled < cap) {
-    slot = filled++;
-  } else {
-    slot = 0;
-    for (int s = 1; s < cap; ++s)
-      if (cnt[s] < cnt[slot] || (cnt[s] == cnt[slot] && seq[s] < seq[slot])) slot = s;
-  }
-  cnt[slot] = 0;
-  seq[slot] = pool->next_seq[pb]++;
-  return slot;
-}
-}  // namespace
-
-extern "C" ig_status ig_pool_prefill(ig_pool* pool, int n_tokens, int32_t* slots_out) {
-  IG_REQUIRE(pool && n_tokens >= 0, "bad argument");
-  const size_t npb = (size_t)pool->layers * pool->B;
-  for (size_t pb = 0; pb < npb; ++pb) {
-    for (int t = 0; t < n_tokens; ++t) {
-      const int s = place(pool, pb);
-      if (pb == 0 && slots_out) slots_out[t] = s;
-    }
-  }
-  return IG_OK;
-}
-
-extern "C" ig_status ig_pool_step(ig_pool* pool, const uint8_t* used, int Lcap, int32_t* slots_out) {
-  IG_REQUIRE(pool, "null pool");
-  IG_REQUIRE(!used || Lcap >= pool->cap, "Lcap must cover the pool capacity");
-  const size_t npb = (size_t)pool->layers * pool->B;
-  if (used)
-    for (size_t pb = 0; pb < npb; ++pb) fold_use(pool, pb, used + pb * (size_t)Lcap);
-  if (slots_out)
-    for (size_t pb = 0; pb < npb; ++pb) slots_out[pb] = place(pool, pb);
-  return IG_OK;
-}
-
-extern "C" ig_status ig_pool_full(const ig_pool* pool, int* any_full) {
-  IG_REQUIRE(pool && any_full, "null argument");
-  *any_full = 0;
-  for (int32_t f : pool->filled)
-    if (f >= pool->cap) *any_full = 1;
-  return IG_OK;
-}
-
-extern "C" ig_status ig_pool_counters(const ig_pool* pool, int layer, int b, uint8_t* out) {
-  IG_REQUIRE(pool && out, "null argument");
-  IG_REQUIRE(layer >= 0 && layer < pool->layers && b >= 0 && b < pool->B, "layer/b out of range");
-  memcpy(out, pool->counter.data() + ((size_t)layer * pool->B + b) * pool->cap, pool->cap);
   return IG_OK;
 }
 
@@ -264,6 +189,7 @@ extern "C" ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B,
   uint4* Vp = nullptr;
   int cap = 0;
   if (pool) {
+    IG_REQUIRE(pool->storage, "the pool was created without storage");
     IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
     IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
     const size_t le = (size_t)B * H * pool->cap * d;

@@ -7,6 +7,8 @@
 
 struct ig_pool {
   int layers = 0, B = 0, H = 0, d = 0, cap = 0;
+  int policy = 0;            // IG_POOL_COUNTER, IG_POOL_FIFO or IG_POOL_LRU
+  bool storage = true;       // false: the slot manager only, no K/V rows
   uint16_t* K = nullptr;     // pinned, mapped host memory [layers][B][H][cap][d]
   uint16_t* V = nullptr;
   uint16_t* Kdev = nullptr;  // the same memory as seen from the device
@@ -15,4 +17,7 @@ struct ig_pool {
   std::vector<uint32_t> seq;      // insertion order per slot, [layers][B][cap]
   std::vector<int32_t> filled;    // resident slots, [layers][B]
   std::vector<uint32_t> next_seq; // [layers][B]
+  std::vector<uint32_t> last_use; // LRU time of each slot, [layers][B][cap]
+  std::vector<uint32_t> clock;    // LRU time (updates folded so far), [layers][B]
+  std::vector<int64_t> evictions; // placements into a full pool, [layers][B]
 };

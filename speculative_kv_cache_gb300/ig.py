@@ -35,6 +35,10 @@ IG_ERR_TIMEOUT = -5
 IG_ERR_CAPACITY = -6
 IG_SEL_THRESHOLD = 0
 IG_SEL_HEAD_AVG = 1
+IG_POOL_COUNTER = 0
+IG_POOL_FIFO = 1
+IG_POOL_LRU = 2
+IG_POOL_NO_STORAGE = 1
 
 _vp, _i, _f, _sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
 
@@ -70,6 +74,10 @@ _sig("ig_speculate_select", _i, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp,
      _vp, _vp, _vp, _vp, _sz)
 _sig("ig_select", _i, _vp, _i, _i, _i, _vp, _vp, _f, _i, _f, _vp, _vp, _vp, _vp, _sz)
 _sig("ig_pool_create", _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
+_sig("ig_pool_create_ex", _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
+_sig("ig_pool_slot_tokens", _i, _vp, _i, _i, _vp)
+_sig("ig_pool_evictions", _i, _vp, _i, _i, C.POINTER(C.c_int64))
+_sig("ig_eviction_misses", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_pool_destroy", _i, _vp)
 _sig("ig_pool_kv", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_vp))
 _sig("ig_pool_write", _i, _vp, _vp, _i, _vp, _vp)
@@ -204,6 +212,12 @@ def ig_pool_create(layers, B, H, d, cap) -> int:
     return h.value
 
 
+def ig_pool_create_ex(layers, B, H, d, cap, policy=IG_POOL_COUNTER, flags=0) -> int:
+    h = _vp()
+    _ok(_lib.ig_pool_create_ex(layers, B, H, d, cap, policy, flags, C.byref(h)), "ig_pool_create_ex")
+    return h.value
+
+
 def ig_pool_destroy(pool):
     _ok(_lib.ig_pool_destroy(pool), "ig_pool_destroy")
 
@@ -227,6 +241,21 @@ def ig_pool_evict(pool, layer, b, used):
 
 def ig_pool_counters(pool, layer, b, out):
     _ok(_lib.ig_pool_counters(pool, layer, b, _p(out)), "ig_pool_counters")
+
+
+def ig_pool_slot_tokens(pool, layer, b, out):
+    _ok(_lib.ig_pool_slot_tokens(pool, layer, b, _p(out)), "ig_pool_slot_tokens")
+
+
+def ig_pool_evictions(pool, layer, b) -> int:
+    n = C.c_int64()
+    _ok(_lib.ig_pool_evictions(pool, layer, b, C.byref(n)), "ig_pool_evictions")
+    return n.value
+
+
+def ig_eviction_misses(stream, B, H, Lcap, scores, idx, cnt, resident, miss_cnt, miss_mass):
+    _ok(_lib.ig_eviction_misses(_s(stream), B, H, Lcap, _p(scores), _p(idx), _p(cnt), _p(resident),
+                                _p(miss_cnt), _p(miss_mass)), "ig_eviction_misses")
 
 
 def ig_gather_kv(stream, pool, layer, B, H, d, Lcap, idx, cnt, Kg, Vg, max_ctas=0):

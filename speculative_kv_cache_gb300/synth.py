@@ -125,6 +125,25 @@ def layer_inputs(w: Workload, step: int = 0, layers: int | None = None) -> np.nd
     return x.astype(np.float16)
 
 
+def layer_inputs_over_steps(w: Workload, steps: int, layers: int | None = None) -> np.ndarray:
+    """Attention inputs of every layer for ``steps`` consecutive decode steps, [steps, L, B, D]
+    fp16, drifting across steps as they drift across layers: layer 0's input at step s + 1 is
+    (x_s + 0.4 eps) / sqrt(1.16) of step s's (cos ~ 0.93), each step's layers drift from it as
+    in ``layer_inputs``.  Used where a study needs attention that persists across steps."""
+    nl = layers or w.layers
+    g = rng(w.name, "xsteps", steps)
+    out = np.zeros((steps, nl, w.batch, w.hidden), dtype=np.float32)
+    x0 = g.standard_normal((w.batch, w.hidden), dtype=np.float32)
+    c = np.float32(math.sqrt(1.16))
+    for s in range(steps):
+        if s:
+            x0 = (x0 + np.float32(0.4) * g.standard_normal((w.batch, w.hidden), dtype=np.float32)) / c
+        out[s, 0] = x0
+        for l in range(1, nl):
+            out[s, l] = (out[s, l - 1] + np.float32(0.4) * g.standard_normal((w.batch, w.hidden), dtype=np.float32)) / c
+    return out.astype(np.float16)
+
+
 def pool_layer(w: Workload, layer: int, cap: int | None = None):
     """Skewed keys and values of one layer's pool: K~, V [B, H, cap, d] fp16.
 
