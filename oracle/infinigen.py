@@ -31,7 +31,10 @@ Readings taken where the page is silent or garbled (each is listed in the design
     is oldest, where entering the pool counts as a selection at that moment, ties going to
     the oldest insertion;
   * an eviction miss is a token that selection over every token seen so far would pick but
-    that the pool no longer holds.
+    that the pool no longer holds;
+  * speculation fidelity: recall@c counts the speculated tokens whose real score is at least
+    the c-th largest real score (c = the speculated count; ties at that score count as hits);
+    the captured fraction is the share of sum_t sum_c |q_c k_tc| that the partial columns hold.
 
 Parity pins: every function here is pinned by a ``-m "not gpu"`` test (closed forms,
 values the page prints, brute force on tiny inputs).  Two choices are consistency-checked
@@ -519,6 +522,64 @@ def eviction_misses(scores, idx, cnt, resident):
             n_miss[b, h] = len(missed)
             mass[b, h] = sum(w[t] for t in missed) / sum(w.values())
     return n_miss, mass
+
+
+# ----------------------------------------------------------------------------------------
+# Speculation fidelity (diagnostics the summary's critique asks for; not steps of the method)
+# ----------------------------------------------------------------------------------------
+def real_scores(q, K, L_valid, scale):
+    """Layer i's actual attention logits z[b,h,t] = scale * q[b,h] . K[b,h,t], t < L (else -inf)."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    B, H, T, _ = K.shape
+    z = np.full((B, H, T), -np.inf)
+    for b in range(B):
+        n = int(L_valid[b])
+        z[b, :, :n] = float(scale) * np.einsum("hd,htd->ht", q[b], K[b, :, :n])
+    return z
+
+
+def speculation_recall(z, idx, cnt, L_valid):
+    """How well a speculated set matches the real attention of its layer.
+
+    For each (b, h) with c = cnt > 0 speculated tokens: recall = |{t in I : z_t >= z_(c)}| / c,
+    z_(c) the c-th largest real score among the L resident tokens (ties at z_(c) are hits); and
+    weight = sum_{t in I} softmax(z)_t over the resident tokens.  Heads with c = 0 give 0, 0.
+    """
+    z = np.asarray(z, dtype=np.float64)
+    B, H = np.asarray(cnt).shape
+    rec = np.zeros((B, H))
+    wt = np.zeros((B, H))
+    for b in range(B):
+        n = int(L_valid[b])
+        for h in range(H):
+            c = int(cnt[b][h])
+            if c == 0 or n == 0:
+                continue
+            zz = z[b, h, :n]
+            thr = np.sort(zz)[::-1][min(c, n) - 1]
+            sel = [int(t) for t in idx[b][h][:c]]
+            rec[b, h] = sum(1 for t in sel if zz[t] >= thr) / c
+            e = np.exp(zz - zz.max())
+            wt[b, h] = e[sel].sum() / e.sum()
+    return rec, wt
+
+
+def captured_fraction(q, K, L_valid, cols):
+    """Share of the dot-product magnitude that the partial columns hold, per (b, h):
+    sum_t sum_{c in S_h} |q_c K_tc| / sum_t sum_c |q_c K_tc| over the resident tokens t < L."""
+    q = np.abs(np.asarray(q, dtype=np.float64))
+    K = np.abs(np.asarray(K, dtype=np.float64))
+    cols = np.asarray(cols)
+    B, H = q.shape[:2]
+    out = np.zeros((B, H))
+    for b in range(B):
+        n = int(L_valid[b])
+        for h in range(H):
+            prod = q[b, h][None, :] * K[b, h, :n]
+            tot = prod.sum()
+            out[b, h] = prod[:, cols[h]].sum() / tot if tot > 0 else 0.0
+    return out
 
 
 # ----------------------------------------------------------------------------------------

@@ -297,3 +297,51 @@ def test_head_avg_count_rounding():
     s2[0, 1:, :] = np.nan
     idx2, cnt2, _ = ora.select(s2, [6], 1.0, ora.SEL_HEAD_AVG)
     assert list(cnt2[0]) == [1, 0, 0, 0] and list(idx2[0][0]) == [2]
+
+
+# --- speculation fidelity diagnostics ----------------------------------------------------------
+def test_recall_is_one_when_speculation_is_the_real_query_and_all_columns():
+    """Ratio 1 (every column) and the real query as the speculation query: the speculated
+    scores are the real ones, so the threshold set is a top set and recall is exactly 1."""
+    g = np.random.default_rng(3)
+    B, H, T, d = 2, 3, 50, 16
+    q = g.standard_normal((B, H, d))
+    K = g.standard_normal((B, H, T, d))
+    L = np.array([50, 31])
+    z = ora.real_scores(q, K, L, 0.25)
+    idx, cnt, _ = ora.select(z, L, 1.0)
+    rec, wt = ora.speculation_recall(z, idx, cnt, L)
+    assert np.all(rec == 1.0)
+    # weight recall: the softmax mass of the selected set, computed directly
+    for b in range(B):
+        for h in range(H):
+            e = np.exp(z[b, h, :L[b]] - z[b, h, :L[b]].max())
+            assert wt[b, h] == pytest.approx(e[list(idx[b][h])].sum() / e.sum(), rel=1e-12)
+    # alpha = inf selects everything: all the weight
+    idx, cnt, _ = ora.select(z, L, float("inf"))
+    _, wt = ora.speculation_recall(z, idx, cnt, L)
+    assert np.allclose(wt, 1.0, rtol=1e-14)
+
+
+def test_recall_closed_form_and_ties():
+    z = np.array([[[5.0, 4.0, 3.0, 2.0, 1.0]]])
+    L = np.array([5])
+    # speculated {0, 3}: top-2 real = {0, 1}; token 3 is not among them -> 1/2
+    rec, _ = ora.speculation_recall(z, [[np.array([0, 3])]], np.array([[2]]), L)
+    assert rec[0, 0] == 0.5
+    # ties at the c-th score count as hits
+    z2 = np.array([[[5.0, 4.0, 4.0, 1.0]]])
+    rec, _ = ora.speculation_recall(z2, [[np.array([0, 2])]], np.array([[2]]), np.array([4]))
+    assert rec[0, 0] == 1.0
+    rec, wt = ora.speculation_recall(z2, [[np.array([], int)]], np.array([[0]]), np.array([4]))
+    assert rec[0, 0] == 0.0 and wt[0, 0] == 0.0
+
+
+def test_captured_fraction_closed_forms():
+    q = np.array([[[1.0, -2.0, 3.0, 0.0]]])
+    K = np.array([[[[1.0, 1.0, -1.0, 5.0], [2.0, 0.0, 1.0, 1.0]]]])
+    L = np.array([2])
+    # |q_c K_tc|: token 0 -> 1, 2, 3, 0; token 1 -> 2, 0, 3, 0; total 11
+    assert ora.captured_fraction(q, K, L, np.array([[0, 2]]))[0, 0] == pytest.approx(9 / 11, rel=1e-15)
+    assert ora.captured_fraction(q, K, L, np.array([[0, 1, 2, 3]]))[0, 0] == 1.0
+    assert ora.captured_fraction(q, K, np.array([1]), np.array([[1]]))[0, 0] == pytest.approx(2 / 6, rel=1e-15)
