@@ -440,6 +440,36 @@ ig_status ig_eviction_misses(void* stream, int B, int H, int Lcap, const float* 
                              const int32_t* idx, const int32_t* cnt, const uint8_t* resident,
                              int32_t* miss_cnt, float* miss_mass);
 
+/* Speculation fidelity (diagnostic, not a step of the method; section 3.4, "Decoding Stage",
+ * and the skew ablation of Fig 13): how well a speculated set matches the real attention of
+ * its layer.  Per (b, h), with the real logits z_t = scale q . K_t over the L_valid[b]
+ * resident rows and c = cnt[b][h] speculated tokens idx[b][h][0..c):
+ *   recall = |{ j < c : z_{idx_j} >= z_(c) }| / c, z_(c) the c-th largest real logit (ties at
+ *            z_(c) count as hits; c is capped at L for the threshold);
+ *   weight = sum_{j < c} exp(z_{idx_j} - M) / sum_{t < L} exp(z_t - M), M = max_t z_t
+ *            (the share of the real softmax weight the speculated set holds);
+ * both 0 when c = 0 or L = 0.
+ *   q          dev fp16 [B][H][d]        the layer's real query (16-byte aligned)
+ *   K          dev fp16 [B][H][Lcap][d]  its keys (16-byte aligned), HBM
+ *   L_valid    dev int32 [B];  idx, cnt dev int32 [B][H][Lcap], [B][H] (from ig_select)
+ *   recall, weight  dev fp32 [B][H] out
+ * d must be 64 or 128; Lcap <= 16384. */
+ig_status ig_attention_recall(void* stream, int B, int H, int d, int Lcap, float scale,
+                              const uint16_t* q, const uint16_t* K, const int32_t* L_valid,
+                              const int32_t* idx, const int32_t* cnt, float* recall,
+                              float* weight);
+
+/* Captured dot-product fraction of a column set (diagnostic; the skew's purpose in section
+ * 3.4, "Skewed Partial Weights"): per (b, h),
+ *   frac = sum_{t < L} sum_{c in cols[h]} |q_c K_tc| / sum_{t < L} sum_c |q_c K_tc|
+ * for a query and keys in any basis (skewed, with the skewed columns, or unskewed, with
+ * columns chosen there), so the two can be compared.
+ *   q dev fp16 [B][H][d], K dev fp16 [B][H][Lcap][d] (16-byte aligned), L_valid dev int32 [B],
+ *   cols dev int32 [H][k], frac dev fp32 [B][H] out.  d must be 64 or 128. */
+ig_status ig_captured_fraction(void* stream, int B, int H, int d, int k, int Lcap,
+                               const uint16_t* q, const uint16_t* K, const int32_t* L_valid,
+                               const int32_t* cols, float* frac);
+
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t ig_launch_count(void);
 

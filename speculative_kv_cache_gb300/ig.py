@@ -78,6 +78,8 @@ _sig("ig_pool_create_ex", _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_slot_tokens", _i, _vp, _i, _i, _vp)
 _sig("ig_pool_evictions", _i, _vp, _i, _i, C.POINTER(C.c_int64))
 _sig("ig_eviction_misses", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp)
+_sig("ig_attention_recall", _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
+_sig("ig_captured_fraction", _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_pool_destroy", _i, _vp)
 _sig("ig_pool_kv", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_vp))
 _sig("ig_pool_write", _i, _vp, _vp, _i, _vp, _vp)
@@ -256,6 +258,16 @@ def ig_pool_evictions(pool, layer, b) -> int:
 def ig_eviction_misses(stream, B, H, Lcap, scores, idx, cnt, resident, miss_cnt, miss_mass):
     _ok(_lib.ig_eviction_misses(_s(stream), B, H, Lcap, _p(scores), _p(idx), _p(cnt), _p(resident),
                                 _p(miss_cnt), _p(miss_mass)), "ig_eviction_misses")
+
+
+def ig_attention_recall(stream, B, H, d, Lcap, scale, q, K, L_valid, idx, cnt, recall, weight):
+    _ok(_lib.ig_attention_recall(_s(stream), B, H, d, Lcap, scale, _p(q), _p(K), _p(L_valid), _p(idx), _p(cnt),
+                                 _p(recall), _p(weight)), "ig_attention_recall")
+
+
+def ig_captured_fraction(stream, B, H, d, k, Lcap, q, K, L_valid, cols, frac):
+    _ok(_lib.ig_captured_fraction(_s(stream), B, H, d, k, Lcap, _p(q), _p(K), _p(L_valid), _p(cols), _p(frac)),
+        "ig_captured_fraction")
 
 
 def ig_gather_kv(stream, pool, layer, B, H, d, Lcap, idx, cnt, Kg, Vg, max_ctas=0):

@@ -159,6 +159,34 @@ def pool_layer(w: Workload, layer: int, cap: int | None = None):
     return K.astype(np.float16), V
 
 
+def structured_qk_weights(w: Workload, layer: int, decay: float = 0.5):
+    """Unskewed W_Q, W_K [D, H*d] fp16 with the low-rank structure of trained attention weights.
+
+    Per head: W = G diag(sigma) R^T with G ~ N(0, w_std^2) [D, d], sigma_i proportional to
+    (i + 1)^(-decay) (mean sigma^2 = 1), and a random orthogonal R [d, d] shared by W_Q and W_K
+    of the head, so queries and keys put their energy in the same few directions, which the
+    columns do not line up with.  Random i.i.d. weights have a flat spectrum, which would leave
+    nothing for the skew to concentrate.
+    """
+    D, H, d = w.hidden, w.heads, w.head_dim
+    g = rng(w.name, "structured", layer)
+    sig = (np.arange(1, d + 1, dtype=np.float64)) ** (-float(decay))
+    sig /= math.sqrt(float(np.mean(sig * sig)))
+    Wq = np.zeros((D, H * d), dtype=np.float32)
+    Wk = np.zeros((D, H * d), dtype=np.float32)
+    for h in range(H):
+        R, _ = np.linalg.qr(g.standard_normal((d, d)))
+        for W in (Wq, Wk):
+            G = g.standard_normal((D, d)) * w.w_std
+            W[:, h * d:(h + 1) * d] = (G * sig[None, :]) @ R.T
+    return Wq.astype(np.float16), Wk.astype(np.float16)
+
+
+def hidden_states(w: Workload, layer: int, tokens: int) -> np.ndarray:
+    """Token hidden states X [B, tokens, D] fp16 ~ N(0, 1) (prompt and generated tokens)."""
+    return normal_f16(rng(w.name, "hidden", layer), (w.batch, tokens, w.hidden), 1.0)
+
+
 def skewed_partial_weight(w: Workload, layer: int) -> np.ndarray:
     """W~_Q^partial [D, H*k] fp16 drawn directly in the skewed basis (same law as W A)."""
     return normal_f16(rng(w.name, "Wqp", layer), (w.hidden, w.heads * w.k), w.w_std)
