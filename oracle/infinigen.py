@@ -50,6 +50,7 @@ import numpy as np
 
 SEL_THRESHOLD = 0
 SEL_HEAD_AVG = 1
+SEL_NORMALIZED = 2
 
 
 # ----------------------------------------------------------------------------------------
@@ -282,6 +283,9 @@ def select(scores, L_valid, alpha, policy: int = SEL_THRESHOLD, cap_frac: float 
     cap_n best by (score desc, index asc).
     HEAD_AVG: cbar = max(1, round_half_up(mean_h |I_h|)), at most cap_n; every head then keeps
     its cbar best (same order), regardless of the threshold.
+    NORMALIZED (the portable threshold alpha' = alpha / sigma proposed as follow-up work, read
+    per head): I = {t : max - s_t < alpha * sigma} plus the ties of the maximum, sigma the
+    population standard deviation of the head's resident, non-NaN scores; the cap as above.
     Returns (idx list-of-lists [B][H] of ascending int arrays, cnt int32 [B, H],
     used uint8 [B, Lcap] = 1 where any head of sequence b selected slot t).
     """
@@ -302,10 +306,18 @@ def select(scores, L_valid, alpha, policy: int = SEL_THRESHOLD, cap_frac: float 
                 idx[b][h] = np.zeros(0, dtype=np.int64)
                 continue
             m = dt(finite.max())
-            # s_t > m - alpha, evaluated as the gap m - s_t < alpha so that the maximum
-            # itself (gap exactly 0) is kept for every alpha > 0
-            sel = np.array([t for t in range(L) if dt(m - s[t]) < a], dtype=np.int64)
-            if policy == SEL_THRESHOLD and sel.size > capn:
+            if policy == SEL_NORMALIZED:
+                # alpha in units of the head's score spread; the maximum and its ties are
+                # kept even when the spread is 0
+                sigma = float(np.std(finite.astype(np.float64)))
+                ah = dt(np.float32(alpha) * dt(sigma))
+                sel = np.array([t for t in range(L) if not np.isnan(s[t])
+                                and (dt(m - s[t]) < ah or dt(m - s[t]) == 0)], dtype=np.int64)
+            else:
+                # s_t > m - alpha, evaluated as the gap m - s_t < alpha so that the maximum
+                # itself (gap exactly 0) is kept for every alpha > 0
+                sel = np.array([t for t in range(L) if dt(m - s[t]) < a], dtype=np.int64)
+            if policy in (SEL_THRESHOLD, SEL_NORMALIZED) and sel.size > capn:
                 sel = _best_first(s, capn)
             idx[b][h] = sel
         if policy == SEL_HEAD_AVG:

@@ -345,3 +345,37 @@ def test_captured_fraction_closed_forms():
     assert ora.captured_fraction(q, K, L, np.array([[0, 2]]))[0, 0] == pytest.approx(9 / 11, rel=1e-15)
     assert ora.captured_fraction(q, K, L, np.array([[0, 1, 2, 3]]))[0, 0] == 1.0
     assert ora.captured_fraction(q, K, np.array([1]), np.array([[1]]))[0, 0] == pytest.approx(2 / 6, rel=1e-15)
+
+
+# --- normalized threshold (alpha in units of the head's score spread) ----------------------------
+def test_normalized_threshold_closed_form():
+    s = np.array([[[0.0, 1.0, 2.0, 3.0]]])
+    L = np.array([4])
+    sigma = math.sqrt(1.25)  # population std of 0, 1, 2, 3
+    for alpha, want in [(0.5, [3]), (1.0, [2, 3]), (2.0, [1, 2, 3]), (3.0, [0, 1, 2, 3])]:
+        idx, cnt, _ = ora.select(s, L, alpha, ora.SEL_NORMALIZED)
+        assert list(idx[0][0]) == want, (alpha, alpha * sigma)
+    # the cap still applies
+    idx, cnt, _ = ora.select(s, L, 3.0, ora.SEL_NORMALIZED, cap_frac=0.5)
+    assert list(idx[0][0]) == [2, 3]
+
+
+def test_normalized_threshold_is_scale_and_shift_invariant():
+    g = np.random.default_rng(5)
+    s = g.standard_normal((2, 3, 40))
+    L = np.array([40, 17])
+    base, _, _ = ora.select(s, L, 2.0, ora.SEL_NORMALIZED)
+    for a, c in [(7.0, 0.0), (0.01, 3.0), (1.0, -50.0)]:
+        got, _, _ = ora.select(a * s + c, L, 2.0, ora.SEL_NORMALIZED)
+        for b in range(2):
+            for h in range(3):
+                assert list(got[b][h]) == list(base[b][h])
+    # a plain threshold is not scale invariant: scaling the scores down selects more
+    plain, _, _ = ora.select(0.01 * s, L, 2.0)
+    assert sum(len(x) for r in plain for x in r) > sum(len(x) for r in base for x in r)
+
+
+def test_normalized_threshold_zero_spread_keeps_all_ties():
+    s = np.full((1, 1, 5), 2.5)
+    idx, cnt, _ = ora.select(s, np.array([5]), 1.0, ora.SEL_NORMALIZED)
+    assert cnt[0, 0] == 5
