@@ -32,6 +32,10 @@ Readings taken where the page is silent or garbled (each is listed in the design
     the oldest insertion;
   * an eviction miss is a token that selection over every token seen so far would pick but
     that the pool no longer holds;
+  * the FP8 pool (follow-up work: selective prefetch of a quantized pool): every (token, head)
+    row of keys and values is stored as e4m3 codes with one float32 scale, amax / 448, the
+    codes being round-to-nearest-even e4m3 (saturating at 448) of x * (448 / amax) in float32;
+    a row of zeros keeps scale 0; the partial key cache stays float16;
   * speculation fidelity: recall@c counts the speculated tokens whose real score is at least
     the c-th largest real score (c = the speculated count; ties at that score count as hits);
     the captured fraction is the share of sum_t sum_c |q_c k_tc| that the partial columns hold.
@@ -534,6 +538,72 @@ def eviction_misses(scores, idx, cnt, resident):
             n_miss[b, h] = len(missed)
             mass[b, h] = sum(w[t] for t in missed) / sum(w.values())
     return n_miss, mass
+
+
+# ----------------------------------------------------------------------------------------
+# FP8 (e4m3) pool rows (a follow-up of the method: selective prefetch of a quantized pool)
+# ----------------------------------------------------------------------------------------
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of an e4m3 byte: sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent 0 is
+    subnormal (m/8 * 2^-6); S.1111.111 is NaN and there is no infinity."""
+    sgn = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return sgn * (m / 8.0) * 2.0 ** -6
+    return sgn * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def e4m3_encode(x: float) -> int:
+    """Nearest e4m3 byte to x (ties to the even mantissa), magnitudes above 448 saturating."""
+    x = float(x)
+    sign = 0x80 if (x < 0 or (x == 0 and math.copysign(1.0, x) < 0)) else 0
+    a = abs(x)
+    if a >= E4M3_MAX:
+        return sign | 0x7E
+    # spacing of the representable values around a: 2^-9 below the normal range, else 2^(e-3)
+    e = -6 if a < 2.0 ** -6 else math.floor(math.log2(a))
+    step = 2.0 ** (e - 3)
+    q = float(np.rint(a / step)) * step          # round half to even on the quotient
+    if q >= E4M3_MAX:
+        return sign | 0x7E
+    if q == 0:
+        return sign
+    if q < 2.0 ** -6:
+        return sign | int(round(q / 2.0 ** -9))
+    ee = math.floor(math.log2(q))
+    mm = int(round((q / 2.0 ** ee - 1.0) * 8))
+    return sign | ((ee + 7) << 3) | mm
+
+
+def fp8_quantize_rows(X):
+    """Rows (last axis) of float16 X -> (e4m3 codes uint8, float32 scales)."""
+    X = np.asarray(X, dtype=np.float16).astype(np.float32)
+    flat = X.reshape(-1, X.shape[-1])
+    codes = np.zeros(flat.shape, dtype=np.uint8)
+    scales = np.zeros(flat.shape[0], dtype=np.float32)
+    for r in range(flat.shape[0]):
+        amax = np.float32(np.abs(flat[r]).max())
+        if amax == 0:
+            continue
+        inv = np.float32(np.float32(E4M3_MAX) / amax)
+        scales[r] = np.float32(amax / np.float32(E4M3_MAX))
+        for i in range(flat.shape[1]):
+            codes[r, i] = e4m3_encode(float(np.float32(flat[r, i] * inv)))
+    return codes.reshape(X.shape), scales.reshape(X.shape[:-1])
+
+
+def fp8_dequantize_rows(codes, scales):
+    """float16 rows: float32(e4m3 value) * scale, rounded to float16."""
+    codes = np.asarray(codes)
+    table = np.array([0.0 if (c & 0x7F) == 0x7F else e4m3_decode(c) for c in range(256)], dtype=np.float32)
+    vals = table[codes] * np.asarray(scales, dtype=np.float32)[..., None]
+    return vals.astype(np.float32).astype(np.float16)
 
 
 # ----------------------------------------------------------------------------------------

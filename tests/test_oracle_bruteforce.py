@@ -287,3 +287,48 @@ def test_eviction_misses_closed_form():
     assert n[0, 0] == 0 and mass[0, 0] == 0.0
     n, mass = ora.eviction_misses(scores, idx, np.array([[0]]), resident)
     assert n[0, 0] == 0 and mass[0, 0] == 0.0
+
+
+# --- FP8 (e4m3) pool rows -----------------------------------------------------------------------
+def test_e4m3_known_codes_and_round_trip():
+    assert ora.e4m3_encode(0.0) == 0x00 and ora.e4m3_encode(-0.0) == 0x80
+    assert ora.e4m3_encode(1.0) == 0x38 and ora.e4m3_encode(-1.0) == 0xB8
+    assert ora.e4m3_encode(448.0) == 0x7E and ora.e4m3_encode(1e6) == 0x7E and ora.e4m3_encode(-500) == 0xFE
+    assert ora.e4m3_encode(2.0 ** -9) == 0x01           # smallest subnormal
+    assert ora.e4m3_encode(2.0 ** -10) == 0x00          # halfway to 0: ties to even
+    assert ora.e4m3_encode(3 * 2.0 ** -10) == 0x02      # halfway between 1 and 2 (x 2^-9): even
+    assert ora.e4m3_encode(1.0625) == 0x38              # halfway between 1 and 1.125: even (1)
+    assert ora.e4m3_encode(1.1875) == 0x3A              # halfway between 1.125 and 1.25: even (1.25)
+    assert ora.e4m3_decode(0x7E) == 448.0 and math.isnan(ora.e4m3_decode(0x7F))
+    # every finite code decodes and encodes back to itself (-0 to 0x80)
+    for c in range(256):
+        v = ora.e4m3_decode(c)
+        if math.isnan(v):
+            continue
+        assert ora.e4m3_encode(v) == c, hex(c)
+
+
+def test_e4m3_encode_is_the_nearest_value():
+    finite = sorted({ora.e4m3_decode(c) for c in range(256)} - {float("nan")})
+    finite = [v for v in finite if not math.isnan(v)]
+    g = np.random.default_rng(0)
+    for x in np.concatenate([g.standard_normal(2000) * 30, g.standard_normal(500) * 0.01]):
+        got = ora.e4m3_decode(ora.e4m3_encode(x))
+        best = min(abs(v - x) for v in finite)
+        assert abs(got - x) == best
+
+
+def test_fp8_rows_scale_and_error_bound():
+    g = np.random.default_rng(1)
+    X = (g.standard_normal((3, 5, 64)) * 2).astype(np.float16)
+    X[0, 0] = 0
+    codes, scales = ora.fp8_quantize_rows(X)
+    assert scales[0, 0] == 0 and not codes[0, 0].any()
+    Y = ora.fp8_dequantize_rows(codes, scales)
+    Xf, Yf = X.astype(np.float32), Y.astype(np.float32)
+    amax = np.abs(Xf).max(-1, keepdims=True)
+    # the largest element maps to +-448 exactly; e4m3 keeps 3 mantissa bits: relative error
+    # <= 2^-4 for normal values, absolute <= 2^-10 * scale below the normal range
+    assert np.all(np.abs(Yf - Xf) <= np.maximum(np.abs(Xf) * 2.0 ** -4, amax / 448 * 2.0 ** -9) + 1e-3 * amax + 1e-6)
+    r = np.unravel_index(np.abs(Xf[1, 2]).argmax(), (64,))
+    assert ora.e4m3_decode(codes[1, 2][r]) in (448.0, -448.0)
