@@ -47,8 +47,12 @@ def parse_args(argv=None):
     p.add_argument("--gather-ctas", type=int, default=0)
     p.add_argument("--graph", type=int, default=1, help="1: replay each step from a CUDA graph")
     p.add_argument("--fused-select", type=int, default=1, help="1: fused cluster score+select kernel")
+    p.add_argument("--policy", default="threshold", choices=["threshold", "head_avg", "normalized"],
+                   help="selection policy (normalized: alpha in units of each head's score std)")
     p.add_argument("--pool-policy", default="counter", choices=["counter", "fifo", "lru"],
                    help="victim policy of a capacity-limited pool (workloads with pool_frac < 1)")
+    p.add_argument("--pool-fp8", type=int, default=0,
+                   help="1: the host pool holds e4m3 rows with a per-row scale (d + 4 bytes per row)")
     p.add_argument("--fused-fetch", type=int, default=0,
                    help="1: layers 1.. attend straight from the pinned pool on the fetch stream (no staging)")
     p.add_argument("--no-e2e", action="store_true")
@@ -247,14 +251,15 @@ def link_peak_gbs(torch) -> float:
 
 
 def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True,
-                  fused_fetch=False, pool_policy=0):
+                  fused_fetch=False, pool_policy=0, policy=0, pool_fp8=False):
     from speculative_kv_cache_gb300.decoder import Decoder
 
     Lcap = w.lcap
     dec = Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=Lcap,
                   pool_cap=w.pool_cap, alpha=alpha, rope_theta=w.rope_theta, gather_ctas=gather_ctas,
                   stage_timing=True, graph=bool(graph), fused_select=bool(fused_select),
-                  fused_fetch=bool(fused_fetch), pool_policy=pool_policy, device=device)
+                  fused_fetch=bool(fused_fetch), pool_policy=pool_policy, policy=policy,
+                  pool_fp8=bool(pool_fp8), device=device)
     gen = torch.Generator(device=device)
     shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
@@ -354,8 +359,10 @@ def run_ours(args, w, alpha):
         raise SystemExit(f"warmup + steps (+ e2e steps) must stay within the {w.gen} generated tokens")
     fused_fetch = bool(args.fused_fetch)
     pool_policy = {"counter": ig.IG_POOL_COUNTER, "fifo": ig.IG_POOL_FIFO, "lru": ig.IG_POOL_LRU}[args.pool_policy]
+    policy = {"threshold": ig.IG_SEL_THRESHOLD, "head_avg": ig.IG_SEL_HEAD_AVG,
+              "normalized": ig.IG_SEL_NORMALIZED}[args.policy]
     dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph,
-                                          args.fused_select, fused_fetch, pool_policy)
+                                          args.fused_select, fused_fetch, pool_policy, policy, args.pool_fp8)
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
@@ -401,7 +408,8 @@ def run_ours(args, w, alpha):
     sel_rows = cnts[:, 1:].sum()                                          # layers 1.. gather
     ctx = np.array([w.prompt + args.warmup + i for i in range(args.steps)], dtype=np.float64)
     f = sel_rows / (args.steps * (w.layers - 1) * w.batch * w.heads * ctx.mean())
-    G_total = sel_rows * 2 * w.head_dim * 2                               # K + V rows over the link
+    row_link = 2 * (w.head_dim + 4) if args.pool_fp8 else 2 * w.head_dim * 2  # K + V bytes of a row
+    G_total = sel_rows * row_link                                         # over the link
     gather_ms_per_launch = stage[0] / max(stage_n[0], 1)
     G_per_launch = G_total / max(stage_n[0], 1)
     achieved = G_per_launch / (gather_ms_per_launch * 1e-3) / 1e9
@@ -410,7 +418,7 @@ def run_ours(args, w, alpha):
     pk_bytes = w.batch * w.heads * w.k * ctx.mean() * 2
     # staged: the fetched rows are written to and read back from HBM once; fused: not at all
     hbm_l = pk_bytes + (0 if fused_fetch else cnts[:, 1:].sum(axis=(2, 3)).mean(axis=0) * 2 * w.head_dim * 2)
-    link_l = cnts[:, 1:].sum(axis=(2, 3)).mean(axis=0) * 2 * w.head_dim * 2
+    link_l = cnts[:, 1:].sum(axis=(2, 3)).mean(axis=0) * row_link
     t_roof_s = float(np.maximum(hbm_l / (hbm_peak * 1e9), link_l / (link * 1e9)).sum())
     t_roof_s += w.batch * w.heads * ctx.mean() * w.head_dim * 2 * 2 / (hbm_peak * 1e9)
     ms_per_step = elapsed_max / args.steps
@@ -454,6 +462,7 @@ def run_ours(args, w, alpha):
             "dtype": "fp16 storage, fp32 accumulate", "data": "synthetic (seeded, random-init weights)",
             "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph),
                            fused_select=bool(args.fused_select), fused_fetch=fused_fetch,
+                           selection=args.policy, pool_dtype="fp8-e4m3 + fp32 row scale" if args.pool_fp8 else "fp16",
                            pool_policy=args.pool_policy if w.pool_frac < 1 else None),
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "selected_fraction": float(f),

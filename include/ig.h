@@ -45,6 +45,10 @@ typedef int ig_status;
 /* Selection policies for ig_select. */
 #define IG_SEL_THRESHOLD 0    /* each head keeps {t : s_t > max(s) - alpha}                   */
 #define IG_SEL_HEAD_AVG 1     /* each head keeps its top-cbar, cbar = mean count over heads    */
+#define IG_SEL_NORMALIZED 2   /* each head keeps {t : max(s) - s_t < alpha * sigma} and the ties
+                                 of the maximum; sigma = population std of the head's resident
+                                 scores (the portable threshold alpha' = alpha / sigma proposed
+                                 as follow-up work; ig_select only)                            */
 
 /* Device error-word bits (ig_check maps them to a status). */
 #define IG_DEVERR_INDEX 1     /* an index or count was out of range; the access was skipped  */
@@ -152,6 +156,8 @@ ig_status ig_speculate_rope(void* stream, int B, int D, int H, int d, int k, int
  * averaging: cbar = max(1, round-half-up(mean_h count_h)), each head then keeps its cbar
  * best) and Step 5 (a head keeps at most round-half-up(cap_frac * L_valid) tokens, the best
  * by score then lower index; cap_frac >= 1 means no cap).  NaN scores are never chosen.
+ * policy IG_SEL_NORMALIZED: the threshold is alpha times the head's score standard deviation
+ * (computed in fp32 over the resident, non-NaN scores); the cap applies as for the threshold.
  *
  *   scores   dev fp32 [B][H][Lcap]
  *   L_valid  dev int32 [B]
@@ -209,9 +215,19 @@ typedef struct ig_pool ig_pool;
  * rows (ig_pool_kv, ig_pool_write, ig_gather_kv, ig_gather_attend, ig_append_kv with this
  * pool) then return IG_ERR_INVALID. */
 #define IG_POOL_NO_STORAGE 1
+/* IG_POOL_FP8: rows stored as e4m3 codes [layers][B][H][cap][d] with one fp32 scale per row
+ * [layers][B][H][cap] (the combination of a quantized pool with selective prefetch proposed as
+ * follow-up work).  Each row is quantized on its way in (ig_pool_write, ig_append_kv): scale =
+ * amax / 448, codes = round-to-nearest-even e4m3 of x * (448 / amax) in fp32, saturating; a row
+ * of zeros has scale 0.  ig_gather_kv dequantizes (code value x scale, rounded to fp16) into the
+ * usual fp16 staging rows, so the link carries d + 4 bytes per row instead of 2d; the partial key
+ * cache (speculation) stays fp16.  d must be 64 or 128; ig_pool_kv and ig_gather_attend refuse
+ * fp8 pools (use ig_pool_kv8). */
+#define IG_POOL_FP8 2
 
 ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out);
-/* ig_pool_create with a victim policy (IG_POOL_*) and flags (0 or IG_POOL_NO_STORAGE). */
+/* ig_pool_create with a victim policy (IG_POOL_COUNTER/FIFO/LRU) and flags (0, IG_POOL_NO_STORAGE
+ * or IG_POOL_FP8). */
 ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap, int policy, int flags,
                             ig_pool** out);
 ig_status ig_pool_destroy(ig_pool* pool);
@@ -219,8 +235,14 @@ ig_status ig_pool_destroy(ig_pool* pool);
 /* Host pointers (also valid on the device) to one layer's K and V arrays. */
 ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V);
 
+/* fp8 pools: host pointers (also valid on the device) to one layer's codes
+ * ([B][H][cap][d] uint8) and row scales ([B][H][cap] fp32). */
+ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** K8, uint8_t** V8, float** Ks,
+                      float** Vs);
+
 /* Copies one layer's K and V ([B][H][cap][d] fp16 each, from device or host memory) into
- * the pool, asynchronously on `stream`. */
+ * the pool, asynchronously on `stream`.  An fp8 pool quantizes them in a kernel, so for it the
+ * source must be device memory or pinned host memory. */
 ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const uint16_t* K,
                         const uint16_t* V);
 
@@ -339,7 +361,7 @@ ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B, int H, int
  * arrays in ig_decoder_buffers are host arrays of device pointers, copied at creation. */
 typedef struct {
   int layers, B, H, d, D, k, Lcap;
-  int policy;          /* IG_SEL_THRESHOLD or IG_SEL_HEAD_AVG */
+  int policy;          /* IG_SEL_THRESHOLD, IG_SEL_HEAD_AVG or IG_SEL_NORMALIZED */
   float alpha;         /* > 0 */
   float cap_frac;      /* >= 1: no cap */
   float score_scale;   /* logit scale, e.g. 1/sqrt(d) */

@@ -11,6 +11,8 @@
 // exclusive scan of the per-unit counts, which every CTA computes in shared memory), and CTA c
 // fetches rows [c R / G, (c + 1) R / G).  Every CTA therefore moves the same number of bytes,
 // whatever the spread of the per-head counts, without atomics or scratch memory.
+#include <cuda_fp8.h>
+
 #include "ig_common.cuh"
 #include "pool_impl.h"
 
@@ -114,6 +116,113 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather(
   }
 }
 
+// FP8 pool (rows of e4m3 codes + one fp32 scale): the same balanced row split; 16 codes per
+// lane (d/16 lanes per row, so a 128-wide row is 128 B + 4 B over the link instead of 256 B),
+// dequantized to fp16 (code value x scale, rounded to nearest) into the same staging layout.
+__global__ void __launch_bounds__(kGatherThreads) k4_gather_fp8(
+    const uint4* __restrict__ K8, const uint4* __restrict__ V8, const float* __restrict__ Ks,
+    const float* __restrict__ Vs, int units, int cap, int vpr, int Lcap, const int32_t* __restrict__ idx,
+    const int32_t* __restrict__ cnt, uint4* __restrict__ Kg, uint4* __restrict__ Vg, int* err) {
+  extern __shared__ int pre[];
+  __shared__ int wsum[kGatherThreads / 32];
+  const int per = (units + kGatherThreads - 1) / kGatherThreads;
+  const int u0 = threadIdx.x * per;
+  int local = 0;
+  for (int u = u0; u < min(units, u0 + per); ++u) {
+    int c = cnt[u];
+    if (c < 0 || c > Lcap) {
+      raise_error(err, IG_DEVERR_INDEX);
+      c = c < 0 ? 0 : Lcap;
+    }
+    pre[u + 1] = c;
+    local += c;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = local;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  int run = incl - local;
+  for (int w = 0; w < warp; ++w) run += wsum[w];
+  if (threadIdx.x == 0) pre[0] = 0;
+  for (int u = u0; u < min(units, u0 + per); ++u) {
+    run += pre[u + 1];
+    pre[u + 1] = run;
+  }
+  __syncthreads();
+  const long long R = pre[units];
+  const int r0 = (int)(R * blockIdx.x / gridDim.x);
+  const int r1 = (int)(R * (blockIdx.x + 1) / gridDim.x);
+  const int rpp = kGatherThreads / vpr;
+  const int v = threadIdx.x % vpr, rg = threadIdx.x / vpr;
+  int u = 0;
+  {
+    int lo = 0, hi = units;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (pre[mid + 1] <= r0) lo = mid + 1; else hi = mid;
+    }
+    u = lo;
+  }
+  for (int r = r0 + rg; r < r1; r += rpp * kUnroll) {
+    uint4 kv[kUnroll], vv[kUnroll];
+    float ks[kUnroll], vs[kUnroll];
+    int unit[kUnroll], row[kUnroll], slot[kUnroll];
+#pragma unroll
+    for (int q = 0; q < kUnroll; ++q) {
+      const int rr = r + q * rpp;
+      slot[q] = -1;
+      unit[q] = 0;
+      row[q] = 0;
+      if (rr < r1) {
+        while (pre[u + 1] <= rr) ++u;
+        unit[q] = u;
+        row[q] = rr - pre[u];
+        const int sl = idx[(size_t)u * Lcap + row[q]];
+        if (sl < 0 || sl >= cap) raise_error(err, IG_DEVERR_INDEX);
+        else slot[q] = sl;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kUnroll; ++q) {
+      if (slot[q] >= 0) {
+        const size_t rowi = (size_t)unit[q] * cap + slot[q];
+        kv[q] = ld_nc_v4(K8 + rowi * vpr + v);
+        vv[q] = ld_nc_v4(V8 + rowi * vpr + v);
+        ks[q] = __ldg(Ks + rowi);
+        vs[q] = __ldg(Vs + rowi);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kUnroll; ++q) {
+      if (slot[q] < 0) continue;
+      const size_t dst = ((size_t)unit[q] * Lcap + row[q]) * (2 * vpr) + 2 * v;
+      for (int kvsel = 0; kvsel < 2; ++kvsel) {
+        const uint4 c = kvsel ? vv[q] : kv[q];
+        const float sc = kvsel ? vs[q] : ks[q];
+        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          // two codes at a time: exact fp16 values of the codes, then x scale in fp32
+          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] & 0xffffu), __NV_E4M3);
+          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] >> 16), __NV_E4M3);
+          const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+          const __half2 ra = __floats2half2_rn(a.x * sc, a.y * sc), rb = __floats2half2_rn(b.x * sc, b.y * sc);
+          o[2 * i] = *reinterpret_cast<const uint32_t*>(&ra);
+          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&rb);
+        }
+        uint4* out = kvsel ? Vg : Kg;
+        out[dst] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[dst + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+    }
+  }
+}
+
 }  // namespace
 }  // namespace ig
 
@@ -142,6 +251,20 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k4_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "gather smem attribute");
+  }
+  if (pool->fp8) {
+    const int vpr8 = d / 16;  // lanes per fp8 row (16 codes each)
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(k4_gather_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_fail(e, "gather smem attribute");
+    }
+    const size_t rows = (size_t)B * H * pool->cap, r0 = (size_t)layer * rows;
+    k4_gather_fp8<<<grid, kGatherThreads, smem, as_stream(stream)>>>(
+        reinterpret_cast<const uint4*>(pool->K8 + r0 * d), reinterpret_cast<const uint4*>(pool->V8 + r0 * d),
+        pool->Ks + r0, pool->Vs + r0, units, pool->cap, vpr8, Lcap, idx, cnt, reinterpret_cast<uint4*>(Kg),
+        reinterpret_cast<uint4*>(Vg), error_word());
+    IG_CHECK_LAUNCH("fp8 gather launch");
+    return IG_OK;
   }
   const size_t layer_elems = (size_t)B * H * pool->cap * d;
   const uint4* Kp = reinterpret_cast<const uint4*>(pool->Kdev + (size_t)layer * layer_elems);

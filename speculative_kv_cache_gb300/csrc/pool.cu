@@ -5,6 +5,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <cuda_fp8.h>
+
 #include <new>
 
 #include "ig_common.cuh"
@@ -68,6 +70,63 @@ __global__ void k6_append(uint4* __restrict__ Kp, uint4* __restrict__ Vp, int ca
   }
 }
 
+// One warp quantizes one row of d fp16 values (d = 32 * PER) to e4m3 codes with the row's
+// scale amax / 448: codes = RN-even e4m3, saturating, of x * (448 / amax) in fp32; a row of
+// zeros gets scale 0 and zero codes.
+template <int PER>
+__device__ void quantize_row(const __half* __restrict__ x, uint8_t* __restrict__ codes, float* __restrict__ scale) {
+  const int lane = threadIdx.x & 31;
+  float v[PER];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    v[i] = __half2float(x[lane * PER + i]);
+    amax = fmaxf(amax, fabsf(v[i]));
+  }
+  for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  uint32_t packed = 0;
+  if (amax > 0.f) {
+    const float inv = 448.f / amax;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      packed |= (uint32_t)__nv_cvt_float_to_fp8(v[i] * inv, __NV_SATFINITE, __NV_E4M3) << (8 * i);
+  }
+  if (PER == 4) reinterpret_cast<uint32_t*>(codes)[lane] = packed;
+  else reinterpret_cast<uint16_t*>(codes)[lane] = (uint16_t)packed;
+  if (lane == 0) *scale = amax > 0.f ? amax / 448.f : 0.f;
+}
+
+// Pool write of an fp8 pool: rows [rows][d] fp16 (device-accessible) -> codes + scales.
+template <int PER>
+__global__ void k_quantize_rows(const __half* __restrict__ K, const __half* __restrict__ V, size_t rows,
+                                uint8_t* __restrict__ K8, uint8_t* __restrict__ V8, float* __restrict__ Ks,
+                                float* __restrict__ Vs) {
+  constexpr int D = 32 * PER;
+  const size_t r = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  quantize_row<PER>(K + r * D, K8 + r * D, Ks + r);
+  quantize_row<PER>(V + r * D, V8 + r * D, Vs + r);
+}
+
+// Append into an fp8 pool: one warp per (b, h) quantizes the current token's key and value.
+template <int PER>
+__global__ void k6_append_fp8(uint8_t* __restrict__ K8, uint8_t* __restrict__ V8, float* __restrict__ Ks,
+                              float* __restrict__ Vs, int units, int cap, int H, const int32_t* __restrict__ slot,
+                              const __half* __restrict__ k_new, const __half* __restrict__ v_new, int* err) {
+  constexpr int D = 32 * PER;
+  const int bh = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (bh >= units) return;
+  const int sl = slot[bh / H];
+  if (sl < 0) return;
+  if (sl >= cap) {
+    if ((threadIdx.x & 31) == 0) raise_error(err, IG_DEVERR_INDEX);
+    return;
+  }
+  const size_t row = (size_t)bh * cap + sl;
+  quantize_row<PER>(k_new + (size_t)bh * D, K8 + row * D, Ks + row);
+  quantize_row<PER>(v_new + (size_t)bh * D, V8 + row * D, Vs + row);
+}
+
 }  // namespace
 }  // namespace ig
 
@@ -79,8 +138,10 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
   *out = nullptr;
   IG_REQUIRE(policy == IG_POOL_COUNTER || policy == IG_POOL_FIFO || policy == IG_POOL_LRU,
              "unknown pool policy %d", policy);
-  IG_REQUIRE((flags & ~IG_POOL_NO_STORAGE) == 0, "unknown pool flags 0x%x", flags);
+  IG_REQUIRE((flags & ~(IG_POOL_NO_STORAGE | IG_POOL_FP8)) == 0, "unknown pool flags 0x%x", flags);
   const bool storage = !(flags & IG_POOL_NO_STORAGE);
+  const bool fp8 = storage && (flags & IG_POOL_FP8);
+  IG_REQUIRE(!fp8 || d == 64 || d == 128, "an fp8 pool needs d = 64 or 128");
   IG_REQUIRE(layers > 0 && B > 0 && cap > 0, "pool sizes must be positive");
   IG_REQUIRE(!storage || (H > 0 && d > 0), "a pool with storage needs H, d > 0");
   IG_REQUIRE(!storage || d % 8 == 0, "d must be a multiple of 8 (16-byte rows)");
@@ -96,28 +157,49 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
   p->storage = storage;
   if (storage) {
     const size_t elems = (size_t)layers * B * H * cap * d;
+    const size_t nrows = (size_t)layers * B * H * cap;
     const unsigned hflags = cudaHostAllocMapped | cudaHostAllocPortable;
-    cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&p->K), elems * 2, hflags);
-    if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&p->V), elems * 2, hflags);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      if (p->K) cudaFreeHost(p->K);
-      delete p;
-      return fail(IG_ERR_OOM, "pinned allocation of 2 x %zu bytes failed: %s", elems * 2,
-                  cudaGetErrorString(e));
+    // with mapped pinned memory on this platform the host address is also the device address;
+    // it is still obtained through cudaHostGetDevicePointer below for the fp16 rows
+    auto alloc = [&](void** p, size_t bytes) { return cudaHostAlloc(p, bytes, hflags); };
+    cudaError_t e;
+    if (fp8) {
+      p->fp8 = true;
+      e = alloc(reinterpret_cast<void**>(&p->K8), elems);
+      if (e == cudaSuccess) e = alloc(reinterpret_cast<void**>(&p->V8), elems);
+      if (e == cudaSuccess) e = alloc(reinterpret_cast<void**>(&p->Ks), nrows * sizeof(float));
+      if (e == cudaSuccess) e = alloc(reinterpret_cast<void**>(&p->Vs), nrows * sizeof(float));
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        for (void* q : {(void*)p->K8, (void*)p->V8, (void*)p->Ks, (void*)p->Vs})
+          if (q) cudaFreeHost(q);
+        delete p;
+        return fail(IG_ERR_OOM, "pinned allocation of the fp8 pool (2 x %zu + 2 x %zu bytes) failed: %s", elems,
+                    nrows * sizeof(float), cudaGetErrorString(e));
+      }
+    } else {
+      e = alloc(reinterpret_cast<void**>(&p->K), elems * 2);
+      if (e == cudaSuccess) e = alloc(reinterpret_cast<void**>(&p->V), elems * 2);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        if (p->K) cudaFreeHost(p->K);
+        delete p;
+        return fail(IG_ERR_OOM, "pinned allocation of 2 x %zu bytes failed: %s", elems * 2,
+                    cudaGetErrorString(e));
+      }
+      void* kd = nullptr;
+      void* vd = nullptr;
+      e = cudaHostGetDevicePointer(&kd, p->K, 0);
+      if (e == cudaSuccess) e = cudaHostGetDevicePointer(&vd, p->V, 0);
+      if (e != cudaSuccess) {
+        cudaFreeHost(p->K);
+        cudaFreeHost(p->V);
+        delete p;
+        return cuda_fail(e, "device pointer of the pinned pool");
+      }
+      p->Kdev = static_cast<uint16_t*>(kd);
+      p->Vdev = static_cast<uint16_t*>(vd);
     }
-    void* kd = nullptr;
-    void* vd = nullptr;
-    e = cudaHostGetDevicePointer(&kd, p->K, 0);
-    if (e == cudaSuccess) e = cudaHostGetDevicePointer(&vd, p->V, 0);
-    if (e != cudaSuccess) {
-      cudaFreeHost(p->K);
-      cudaFreeHost(p->V);
-      delete p;
-      return cuda_fail(e, "device pointer of the pinned pool");
-    }
-    p->Kdev = static_cast<uint16_t*>(kd);
-    p->Vdev = static_cast<uint16_t*>(vd);
   }
   try {
     const size_t npb = (size_t)layers * B;
@@ -129,8 +211,8 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
     p->clock.assign(npb, 0);
     p->evictions.assign(npb, 0);
   } catch (...) {
-    if (p->K) cudaFreeHost(p->K);
-    if (p->V) cudaFreeHost(p->V);
+    for (void* q : {(void*)p->K, (void*)p->V, (void*)p->K8, (void*)p->V8, (void*)p->Ks, (void*)p->Vs})
+      if (q) cudaFreeHost(q);
     delete p;
     return fail(IG_ERR_OOM, "host allocation of the pool manager failed");
   }
@@ -144,21 +226,38 @@ extern "C" ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig
 
 extern "C" ig_status ig_pool_destroy(ig_pool* pool) {
   if (!pool) return IG_OK;
-  cudaError_t e1 = pool->K ? cudaFreeHost(pool->K) : cudaSuccess;
-  cudaError_t e2 = pool->V ? cudaFreeHost(pool->V) : cudaSuccess;
+  cudaError_t first = cudaSuccess;
+  for (void* q : {(void*)pool->K, (void*)pool->V, (void*)pool->K8, (void*)pool->V8, (void*)pool->Ks, (void*)pool->Vs}) {
+    if (!q) continue;
+    const cudaError_t e = cudaFreeHost(q);
+    if (first == cudaSuccess) first = e;
+  }
   delete pool;
-  if (e1 != cudaSuccess) return cuda_fail(e1, "free pool keys");
-  if (e2 != cudaSuccess) return cuda_fail(e2, "free pool values");
+  if (first != cudaSuccess) return cuda_fail(first, "free pool memory");
   return IG_OK;
 }
 
 extern "C" ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V) {
   IG_REQUIRE(pool && K && V, "null argument");
   IG_REQUIRE(pool->storage, "the pool was created without storage");
+  IG_REQUIRE(!pool->fp8, "an fp8 pool has no fp16 rows (use ig_pool_kv8)");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
   *K = pool->K + (size_t)layer * le;
   *V = pool->V + (size_t)layer * le;
+  return IG_OK;
+}
+
+extern "C" ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** K8, uint8_t** V8, float** Ks,
+                                 float** Vs) {
+  IG_REQUIRE(pool && K8 && V8 && Ks && Vs, "null argument");
+  IG_REQUIRE(pool->fp8, "not an fp8 pool");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+  const size_t rows = (size_t)pool->B * pool->H * pool->cap;
+  *K8 = pool->K8 + (size_t)layer * rows * pool->d;
+  *V8 = pool->V8 + (size_t)layer * rows * pool->d;
+  *Ks = pool->Ks + (size_t)layer * rows;
+  *Vs = pool->Vs + (size_t)layer * rows;
   return IG_OK;
 }
 
@@ -169,6 +268,31 @@ extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
   cudaStream_t s = as_stream(stream);
+  if (pool->fp8) {
+    // the rows are quantized by a kernel, so they must be readable by the device
+    for (const void* src : {(const void*)K, (const void*)V}) {
+      cudaPointerAttributes at{};
+      const cudaError_t e = cudaPointerGetAttributes(&at, src);
+      if (e != cudaSuccess || at.type == cudaMemoryTypeUnregistered) {
+        cudaGetLastError();
+        return fail(IG_ERR_INVALID, "writing an fp8 pool needs device or pinned source rows");
+      }
+    }
+    const size_t rows = (size_t)pool->B * pool->H * pool->cap;
+    const size_t r0 = (size_t)layer * rows;
+    const int wpb = 8;  // rows (warps) per block
+    const unsigned blocks = (unsigned)((rows + wpb - 1) / wpb);
+    auto Kh = reinterpret_cast<const __half*>(K);
+    auto Vh = reinterpret_cast<const __half*>(V);
+    if (pool->d == 128)
+      k_quantize_rows<4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, pool->K8 + r0 * 128, pool->V8 + r0 * 128,
+                                                     pool->Ks + r0, pool->Vs + r0);
+    else
+      k_quantize_rows<2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, pool->K8 + r0 * 64, pool->V8 + r0 * 64,
+                                                     pool->Ks + r0, pool->Vs + r0);
+    IG_CHECK_LAUNCH("fp8 pool write launch");
+    return IG_OK;
+  }
   cudaError_t e = cudaMemcpyAsync(pool->K + (size_t)layer * le, K, le * 2, cudaMemcpyDefault, s);
   if (e == cudaSuccess) e = cudaMemcpyAsync(pool->V + (size_t)layer * le, V, le * 2, cudaMemcpyDefault, s);
   if (e != cudaSuccess) return cuda_fail(e, "pool write");
@@ -192,10 +316,27 @@ extern "C" ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B,
     IG_REQUIRE(pool->storage, "the pool was created without storage");
     IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
     IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
-    const size_t le = (size_t)B * H * pool->cap * d;
-    Kp = reinterpret_cast<uint4*>(pool->Kdev + (size_t)layer * le);
-    Vp = reinterpret_cast<uint4*>(pool->Vdev + (size_t)layer * le);
-    cap = pool->cap;
+    if (pool->fp8) {  // the quantized row goes to the pool here; the kernel below does the rest
+      const size_t rows = (size_t)B * H * pool->cap, r0 = (size_t)layer * rows;
+      const int units = B * H, wpb = 8;
+      auto kn = reinterpret_cast<const __half*>(k_new);
+      auto vn = reinterpret_cast<const __half*>(v_new);
+      if (d == 128)
+        k6_append_fp8<4><<<(units + wpb - 1) / wpb, 32 * wpb, 0, as_stream(stream)>>>(
+            pool->K8 + r0 * d, pool->V8 + r0 * d, pool->Ks + r0, pool->Vs + r0, units, pool->cap, H, slot, kn, vn,
+            error_word());
+      else
+        k6_append_fp8<2><<<(units + wpb - 1) / wpb, 32 * wpb, 0, as_stream(stream)>>>(
+            pool->K8 + r0 * d, pool->V8 + r0 * d, pool->Ks + r0, pool->Vs + r0, units, pool->cap, H, slot, kn, vn,
+            error_word());
+      IG_CHECK_LAUNCH("fp8 append launch");
+      if (!Kpart && !Kdense) return IG_OK;
+    } else {
+      const size_t le = (size_t)B * H * pool->cap * d;
+      Kp = reinterpret_cast<uint4*>(pool->Kdev + (size_t)layer * le);
+      Vp = reinterpret_cast<uint4*>(pool->Vdev + (size_t)layer * le);
+      cap = pool->cap;
+    }
   }
   k6_append<<<B * H, 64, 0, as_stream(stream)>>>(
       Kp, Vp, cap, H, d, k, Lcap, slot, cols, reinterpret_cast<const __half*>(k_new),

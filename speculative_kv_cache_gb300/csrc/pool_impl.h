@@ -9,6 +9,11 @@ struct ig_pool {
   int layers = 0, B = 0, H = 0, d = 0, cap = 0;
   int policy = 0;            // IG_POOL_COUNTER, IG_POOL_FIFO or IG_POOL_LRU
   bool storage = true;       // false: the slot manager only, no K/V rows
+  bool fp8 = false;          // rows stored as e4m3 codes with one fp32 scale per row
+  uint8_t* K8 = nullptr;     // fp8 pools: pinned, mapped codes [layers][B][H][cap][d]
+  uint8_t* V8 = nullptr;
+  float* Ks = nullptr;       // fp8 pools: pinned, mapped row scales [layers][B][H][cap]
+  float* Vs = nullptr;
   uint16_t* K = nullptr;     // pinned, mapped host memory [layers][B][H][cap][d]
   uint16_t* V = nullptr;
   uint16_t* Kdev = nullptr;  // the same memory as seen from the device

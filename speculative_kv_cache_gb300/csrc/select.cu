@@ -1,5 +1,6 @@
 // Selection of the tokens each head prefetches (InfiniGen paper-graph summary, section 3.4,
-// "Decoding Stage", Step 3 threshold, Step 4 multi-head averaging, Step 5 transfer cap).
+// "Decoding Stage", Step 3 threshold, Step 4 multi-head averaging, Step 5 transfer cap; and
+// the normalized threshold alpha' = alpha / sigma its follow-up work proposes).
 //
 // One CTA per (sequence, head).  The per-head maximum is a warp-shuffle reduction followed by
 // a reduction over warps; the chosen tokens are compacted in ascending order with a warp
@@ -55,6 +56,17 @@ __device__ int block_sum(int v, SelShared& sh) {
   return r;
 }
 
+__device__ float block_fsum(float v, SelShared& sh) {
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) sh.fred[warp] = v;
+  __syncthreads();
+  float r = 0.f;
+  for (int w = 0; w < kSelWarps; ++w) r += sh.fred[w];
+  return r;
+}
+
 // Finds the n-th largest key among valid tokens (n >= 1, n <= number of valid tokens).
 // Returns the key; *need_eq = how many tokens holding exactly that key are to be kept
 // (the lowest-index ones).
@@ -98,8 +110,9 @@ __device__ uint32_t radix_select(const float* s, int L, int n, int* need_eq, Sel
   return sh.prefix;
 }
 
-// Ordered compaction.  mode 0: keep valid tokens with (m - s) < alpha.  mode 1: keep valid
-// tokens with key > kstar, plus the first need_eq tokens with key == kstar.
+// Ordered compaction.  mode 0: keep valid tokens with (m - s) < alpha or s tied with the
+// maximum.  mode 1: keep valid tokens with key > kstar, plus the first need_eq tokens with
+// key == kstar.
 __device__ int compact(const float* s, int L, int mode, float m, float alpha, uint32_t kstar,
                        int need_eq, int32_t* idx_out, uint8_t* used_b, SelShared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -112,7 +125,7 @@ __device__ int compact(const float* s, int L, int mode, float m, float alpha, ui
       const float v = s[t];
       if (!isnan(v)) {
         if (mode == 0) {
-          f = (m - v) < alpha;
+          f = (m - v) < alpha || (m - v) == 0.f;
         } else {
           const uint32_t kk = fkey(v);
           f = kk > kstar;
@@ -156,9 +169,11 @@ __device__ int compact(const float* s, int L, int mode, float m, float alpha, ui
 }
 
 // pass: 0 = threshold (+ optional cap) and write; 1 = head-avg counting only; 2 = head-avg write.
+// normalized (pass 0): the threshold is alpha times the head's score standard deviation.
 __global__ void __launch_bounds__(kSelThreads) k3_select(const float* __restrict__ scores,
                                                          const int* __restrict__ L_valid, int H,
-                                                         int Lcap, float alpha, double cap_frac,
+                                                         int Lcap, float alpha, int normalized,
+                                                         double cap_frac,
                                                          int pass, int32_t* __restrict__ idx,
                                                          int32_t* __restrict__ cnt,
                                                          uint8_t* __restrict__ used,
@@ -204,12 +219,26 @@ __global__ void __launch_bounds__(kSelThreads) k3_select(const float* __restrict
     return;
   }
 
+  if (normalized && nv > 0) {  // alpha in units of the population std of the valid scores
+    float a = 0.f;
+    for (int t = threadIdx.x; t < L; t += kSelThreads) {
+      const float v = s[t];
+      if (!isnan(v)) a += v;
+    }
+    const float mean = block_fsum(a, sh) / (float)nv;
+    float q = 0.f;
+    for (int t = threadIdx.x; t < L; t += kSelThreads) {
+      const float v = s[t];
+      if (!isnan(v)) q = fmaf(v - mean, v - mean, q);
+    }
+    alpha = alpha * sqrtf(block_fsum(q, sh) / (float)nv);
+  }
   int nthr = 0;
   if (nv > 0) {
     int c = 0;
     for (int t = threadIdx.x; t < L; t += kSelThreads) {
       const float v = s[t];
-      if (!isnan(v) && (m - v) < alpha) ++c;
+      if (!isnan(v) && ((m - v) < alpha || (m - v) == 0.f)) ++c;
     }
     nthr = block_sum(c, sh);
   }
@@ -248,7 +277,8 @@ extern "C" ig_status ig_select(void* stream, int B, int H, int Lcap, const float
   IG_REQUIRE(scores && L_valid && idx && cnt, "null pointer argument");
   IG_REQUIRE(alpha > 0.f, "alpha must be > 0 (got %g)", (double)alpha);
   IG_REQUIRE(!(cap_frac < 0.f) && !isnan(cap_frac), "cap_frac must be >= 0");
-  IG_REQUIRE(policy == IG_SEL_THRESHOLD || policy == IG_SEL_HEAD_AVG, "unknown policy %d", policy);
+  IG_REQUIRE(policy == IG_SEL_THRESHOLD || policy == IG_SEL_HEAD_AVG || policy == IG_SEL_NORMALIZED,
+             "unknown policy %d", policy);
   cudaStream_t s = as_stream(stream);
   int* err = error_word();
   if (used) {
@@ -256,9 +286,9 @@ extern "C" ig_status ig_select(void* stream, int B, int H, int Lcap, const float
     if (e != cudaSuccess) return cuda_fail(e, "clear used flags");
   }
   const double cf = (double)cap_frac;
-  if (policy == IG_SEL_THRESHOLD) {
-    k3_select<<<B * H, kSelThreads, 0, s>>>(scores, L_valid, H, Lcap, alpha, cf, 0, idx, cnt, used,
-                                            nullptr, err);
+  if (policy == IG_SEL_THRESHOLD || policy == IG_SEL_NORMALIZED) {
+    k3_select<<<B * H, kSelThreads, 0, s>>>(scores, L_valid, H, Lcap, alpha, policy == IG_SEL_NORMALIZED, cf, 0,
+                                            idx, cnt, used, nullptr, err);
     IG_CHECK_LAUNCH("select launch");
     return IG_OK;
   }
@@ -266,10 +296,10 @@ extern "C" ig_status ig_select(void* stream, int B, int H, int Lcap, const float
   if (!workspace || workspace_bytes < need)
     return fail(IG_ERR_CAPACITY, "head-averaged selection needs %zu workspace bytes", need);
   int32_t* counts = static_cast<int32_t*>(workspace);
-  k3_select<<<B * H, kSelThreads, 0, s>>>(scores, L_valid, H, Lcap, alpha, cf, 1, idx, cnt, used,
+  k3_select<<<B * H, kSelThreads, 0, s>>>(scores, L_valid, H, Lcap, alpha, 0, cf, 1, idx, cnt, used,
                                           counts, err);
   IG_CHECK_LAUNCH("select (count) launch");
-  k3_select<<<B * H, kSelThreads, 0, s>>>(scores, L_valid, H, Lcap, alpha, cf, 2, idx, cnt, used,
+  k3_select<<<B * H, kSelThreads, 0, s>>>(scores, L_valid, H, Lcap, alpha, 0, cf, 2, idx, cnt, used,
                                           counts, err);
   IG_CHECK_LAUNCH("select (head-avg) launch");
   return IG_OK;

@@ -35,10 +35,12 @@ IG_ERR_TIMEOUT = -5
 IG_ERR_CAPACITY = -6
 IG_SEL_THRESHOLD = 0
 IG_SEL_HEAD_AVG = 1
+IG_SEL_NORMALIZED = 2
 IG_POOL_COUNTER = 0
 IG_POOL_FIFO = 1
 IG_POOL_LRU = 2
 IG_POOL_NO_STORAGE = 1
+IG_POOL_FP8 = 2
 
 _vp, _i, _f, _sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
 
@@ -76,6 +78,7 @@ _sig("ig_select", _i, _vp, _i, _i, _i, _vp, _vp, _f, _i, _f, _vp, _vp, _vp, _vp,
 _sig("ig_pool_create", _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_create_ex", _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_slot_tokens", _i, _vp, _i, _i, _vp)
+_sig("ig_pool_kv8", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp))
 _sig("ig_pool_evictions", _i, _vp, _i, _i, C.POINTER(C.c_int64))
 _sig("ig_eviction_misses", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_attention_recall", _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
@@ -243,6 +246,23 @@ def ig_pool_evict(pool, layer, b, used):
 
 def ig_pool_counters(pool, layer, b, out):
     _ok(_lib.ig_pool_counters(pool, layer, b, _p(out)), "ig_pool_counters")
+
+
+def ig_pool_kv8(pool, layer):
+    """fp8 pools: host addresses (also valid on the device) of one layer's codes and scales."""
+    k, v, ks, vs = _vp(), _vp(), _vp(), _vp()
+    _ok(_lib.ig_pool_kv8(pool, layer, C.byref(k), C.byref(v), C.byref(ks), C.byref(vs)), "ig_pool_kv8")
+    return k.value, v.value, ks.value, vs.value
+
+
+def pool_layer_view_fp8(pool, layer, B, H, cap, d):
+    """NumPy views of one layer of an fp8 pool: codes [B, H, cap, d] uint8 (K, V) and scales
+    [B, H, cap] float32 (K, V)."""
+    k, v, ks, vs = ig_pool_kv8(pool, layer)
+    n, r = B * H * cap * d, B * H * cap
+    arr = lambda p, t, m, shp: np.ctypeslib.as_array(C.cast(p, C.POINTER(t)), shape=(m,)).reshape(shp)  # noqa: E731
+    return (arr(k, C.c_uint8, n, (B, H, cap, d)), arr(v, C.c_uint8, n, (B, H, cap, d)),
+            arr(ks, C.c_float, r, (B, H, cap)), arr(vs, C.c_float, r, (B, H, cap)))
 
 
 def ig_pool_slot_tokens(pool, layer, b, out):

@@ -125,6 +125,36 @@ def test_select_is_bit_exact_on_shared_fp32_scores(ig, name, policy, cap, alpha,
         assert np.array_equal(used_g[b, :l], ou[b, :l])
 
 
+@pytest.mark.parametrize("name", ["tiny", "ragged", "opt-30b"])
+@pytest.mark.parametrize("alpha,cap", [(0.5, 1.0), (2.0, 1.0), (3.0, 0.1), (1e-6, 1.0)])
+@pytest.mark.parametrize("source", ["kernel", "ties"])
+def test_normalized_select_matches_oracle(ig, name, alpha, cap, source):
+    """alpha in units of each head's score std: equal index sets except tokens whose gap to
+    the maximum lies within 1e-5 of alpha * sigma (sigma is summed in fp32 on the GPU)."""
+    c = make_case(name)
+    w = c["w"]
+    B, H, Lcap = w.batch, w.heads, c["Lcap"]
+    s32 = gpu_speculate(ig, c)[0] if source == "kernel" else _quantised_scores(11, B, H, Lcap)
+    idx = empty((B, H, Lcap), torch.int32)
+    cnt = empty((B, H), torch.int32)
+    ig.ig_select(None, B, H, Lcap, dev(s32), dev(c["L"]), alpha, ig.IG_SEL_NORMALIZED, cap, idx, cnt, None)
+    ig.ig_check()
+    idx_g, cnt_g = host(idx), host(cnt)
+    oi, oc, _ = ora.select(s32, c["L"], alpha, ora.SEL_NORMALIZED, cap)
+    for b in range(B):
+        L = int(c["L"][b])
+        for h in range(H):
+            g_set = set(idx_g[b, h, :cnt_g[b, h]].tolist())
+            o_set = set(int(t) for t in oi[b][h])
+            if g_set == o_set:
+                continue
+            sv = s32[b, h, :L].astype(np.float64)
+            fin = sv[~np.isnan(sv)]
+            m, a = fin.max(), alpha * fin.std()
+            for t in g_set ^ o_set:
+                assert abs((m - sv[t]) - a) <= 1e-5 * (1 + a), (b, h, t)
+
+
 @pytest.fixture(scope="module")
 def pools(ig):
     made = {}
