@@ -224,6 +224,32 @@ def partial_key_cache(K_pool, cols) -> np.ndarray:
     return out
 
 
+def prefill_layer(X, Wq_skew, Wk_skew, Wv, H: int, d: int, k: int, cap: int):
+    """Prefill Stage, Steps 1-3, for one layer (no RoPE).
+
+    Step 1: the prompt's skewed keys K~ = X W~_K and values V = X W_V (float64, rounded once to
+    float16), stored in the pool: the pool places prompt tokens as the counter pool does
+    (token t at slot t mod cap; with more tokens than slots the last cap stay).  Step 2: the
+    columns, from W~_Q and the keys of every prompt token of every sequence.  Step 3: the
+    partial query weight and the partial key cache of the resident slots.
+
+    X [B, N, D] fp16; W~_Q, W~_K, W_V [D, H*d] fp16.  Returns a dict: K, V [B, N, H, d] fp16,
+    cols [H, k], Wq_part [D, H*k] fp16, K_pool, V_pool [B, H, cap, d] fp16, K_part [B, H, k, cap].
+    """
+    X64 = np.asarray(X, dtype=np.float64)
+    B, N, _ = X64.shape
+    Kt = (X64 @ np.asarray(Wk_skew, dtype=np.float64)).astype(np.float16).reshape(B, N, H, d)
+    Vt = (X64 @ np.asarray(Wv, dtype=np.float64)).astype(np.float16).reshape(B, N, H, d)
+    cols = choose_columns(Wq_skew, Kt, H, d, k)
+    Kp = np.zeros((B, H, cap, d), dtype=np.float16)
+    Vp = np.zeros((B, H, cap, d), dtype=np.float16)
+    for t in range(max(0, N - cap), N):
+        Kp[:, :, t % cap] = Kt[:, t]
+        Vp[:, :, t % cap] = Vt[:, t]
+    return dict(K=Kt, V=Vt, cols=cols, Wq_part=partial_weight(Wq_skew, cols, H, d), K_pool=Kp, V_pool=Vp,
+                K_part=partial_key_cache(Kp, cols))
+
+
 # ----------------------------------------------------------------------------------------
 # Decode stage (section 3.4, "Decoding Stage: Speculative KV Selection and Prefetching")
 # ----------------------------------------------------------------------------------------

@@ -379,3 +379,43 @@ def test_normalized_threshold_zero_spread_keeps_all_ties():
     s = np.full((1, 1, 5), 2.5)
     idx, cnt, _ = ora.select(s, np.array([5]), 1.0, ora.SEL_NORMALIZED)
     assert cnt[0, 0] == 5
+
+
+# --- prefill stage (Steps 1-3) -------------------------------------------------------------------
+def test_prefill_keys_are_the_skewed_prompt_keys():
+    """X (W_K A) is (X W_K) A: the prefill's keys from the skewed weight equal the skew's own
+    rotation of the unskewed prompt keys, up to the two fp16 roundings."""
+    w = synth.scaled(synth.WORKLOADS["tiny"], name="pf", heads=2, hidden=256, batch=2, prompt=24)
+    H, d, k = w.heads, w.head_dim, w.k
+    Xs, Wq, Wk = synth.skew_inputs(w)
+    X = synth.hidden_states(w, 0, w.prompt)
+    Kraw = (X.astype(np.float64) @ Wk.astype(np.float64)).astype(np.float16).reshape(-1, H, d)
+    A, _, Wq_s, Wk_s, K_s = ora.skew(Xs, Wq, Wk, H, d, Kprompt=Kraw)
+    Wv = synth.normal_f16(synth.rng(w.name, "Wv", 0), Wq.shape, w.w_std)
+    out = ora.prefill_layer(X, Wq_s, Wk_s, Wv, H, d, k, cap=w.prompt)
+    got = out["K"].reshape(-1, H, d).astype(np.float64)
+    want = K_s.astype(np.float64)
+    assert np.abs(got - want).max() <= 4e-3 * np.abs(want).max()
+    # the columns come from W~_Q and these keys: the same as the oracle's column choice on the
+    # skew's own keys unless the two roundings flip a near tie
+    sc = ora.colscores(Wq_s, out["K"], H, d)
+    for h in range(H):
+        s_sorted = np.sort(sc[h])[::-1]
+        if s_sorted[k - 1] - s_sorted[k] > 1e-3 * s_sorted[k - 1]:
+            assert np.array_equal(out["cols"][h], ora.choose_columns(Wq_s, K_s, H, d, k)[h])
+
+
+def test_prefill_pool_placement_is_the_counter_pool_prefill():
+    g = np.random.default_rng(3)
+    B, N, D, H, d, k, cap = 1, 11, 32, 2, 8, 3, 4
+    X = g.standard_normal((B, N, D)).astype(np.float16)
+    W = [(g.standard_normal((D, H * d)) * 0.1).astype(np.float16) for _ in range(3)]
+    out = ora.prefill_layer(X, W[0], W[1], W[2], H, d, k, cap)
+    pool = ora.CounterPool(cap)
+    owner = {}
+    for t in range(N):
+        owner[pool.insert()] = t
+    for s_, t in owner.items():
+        assert np.array_equal(out["K_pool"][:, :, s_], out["K"][:, t])
+        assert np.array_equal(out["V_pool"][:, :, s_], out["V"][:, t])
+    assert np.array_equal(out["K_part"], ora.partial_key_cache(out["K_pool"], out["cols"]))
