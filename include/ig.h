@@ -492,6 +492,41 @@ ig_status ig_captured_fraction(void* stream, int B, int H, int d, int k, int Lca
                                const uint16_t* q, const uint16_t* K, const int32_t* L_valid,
                                const int32_t* cols, float* frac);
 
+/* ------------------------------------------------------------------------------------
+ * Prefill stage (section 3.4, "Prefill Stage: Partial Weight Index Generation", Steps 1-3;
+ * models without RoPE).  For one layer and a prompt of N tokens per sequence:
+ *   Step 1  K~ = X W~_K and V = X W_V on the tensor cores (fp16 in, fp32 accumulate, fp16
+ *           out); the rows of the tokens the pool keeps go to it, token t at slot t mod cap
+ *           (the pool's own prefill placement: call ig_pool_prefill(pool, N, ...) for the
+ *           slot manager; with N > cap the first N - cap tokens are dropped);
+ *   Step 2  cols[h] = the k columns of head h with the largest sum of |W~_Q| over its rows
+ *           plus |K~| over every prompt token of every sequence (float64 sums in a fixed
+ *           order; ties to the lower column), ascending;
+ *   Step 3  Wq_part_t = those rows of W~_Q^T (the partial query weight as ig_speculate takes
+ *           it) and Kpart = the chosen columns of the resident keys, at their slots.
+ *   X             dev fp16 [B][N][D]         the layer's attention input for the prompt
+ *   Wq_t, Wk_t    dev fp16 [H*d][D]          W~_Q^T and W~_K^T (skewed, transposed)
+ *   Wv_t          dev fp16 [H*d][D]          W_V^T
+ *   cols          dev int32 [H][k] out
+ *   Wq_part_t     dev fp16 [H*k][D] out
+ *   Kpart         dev fp16 [B][H][k][Lcap] out (resident slots written; others untouched)
+ *   workspace     dev, >= ig_prefill_workspace_bytes(B, N, H, d), 256-byte aligned (holds
+ *                 K~ and V, 4 B N H d bytes, and per-tile column sums)
+ * The pool must have storage and fp16 rows; d must be 64 or 128; D a multiple of 8. */
+size_t ig_prefill_workspace_bytes(int B, int N, int H, int d);
+ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,
+                           int d, int k, int Lcap, const uint16_t* X, const uint16_t* Wq_t,
+                           const uint16_t* Wk_t, const uint16_t* Wv_t, int32_t* cols,
+                           uint16_t* Wq_part_t, uint16_t* Kpart, void* workspace,
+                           size_t workspace_bytes);
+
+/* The prefill's tensor-core GEMM on its own: C[M][N] = A[M][K] Bt[N][K]^T, fp16 operands
+ * (both K-major), fp32 accumulation, fp16 result (row-major).  With colpart (dev fp32
+ * [ceil(M/128)][N]) it also writes, per 128-row tile, the column sums of |C| as stored (fp16).
+ * N must be a multiple of 32, K of 8; A, Bt, C 16-byte aligned. */
+ig_status ig_gemm_tn(void* stream, int M, int N, int K, const uint16_t* A, const uint16_t* Bt,
+                     uint16_t* C, float* colpart);
+
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t ig_launch_count(void);
 

@@ -1,0 +1,388 @@
+// Prefill stage on the GPU (InfiniGen paper-graph summary, section 3.4, "Prefill Stage:
+// Partial Weight Index Generation", Steps 1-3; no RoPE):
+//   Step 1  K~ = X W~_K and V = X W_V for every prompt token (a tcgen05 GEMM), the rows of the
+//           tokens the pool keeps written to the pinned pool, token t at slot t mod cap;
+//   Step 2  column score = column sums of |W~_Q| plus column sums of |K~| over every prompt
+//           token, top-k per head;
+//   Step 3  the partial query weight (the chosen rows of W~_Q^T) and the partial key cache.
+//
+// The GEMM C[M][N] = A[M][K] . Bt[N][K]^T (both K-major, fp16 in, fp32 accumulate, fp16 out):
+// one 128 x 256 output tile per CTA, a ring of 4 TMA stages of 64-wide K (48 KB each), one
+// thread issuing the loads and another the tcgen05 MMAs (128x256x16, accumulator in 256 TMEM
+// columns), each stage released by a tcgen05.commit onto its "empty" mbarrier.  The epilogue
+// reads the accumulator with tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = rows), stores
+// fp16 rows, and, when asked, reduces |C| down each column of the tile (a shuffle transpose-
+// reduce in each warp, then the four warps in a fixed order) into per-tile partial sums, so the
+// column score is deterministic.
+#include <cuda.h>
+
+#include "ig_common.cuh"
+#include "pool_impl.h"
+#include "tc_common.cuh"
+
+namespace ig {
+namespace {
+
+constexpr int kGM = 128;        // tile rows (tcgen05 M = TMEM lanes)
+constexpr int kGN = 256;        // tile columns (tcgen05 N = TMEM columns)
+constexpr int kGK = 64;         // K per stage: one 128-byte swizzle atom of fp16
+constexpr int kGStages = 4;
+constexpr int kGThreads = 128;
+constexpr uint32_t kGStageA = kGM * kGK * 2;  // 16 KB
+constexpr uint32_t kGStageB = kGN * kGK * 2;  // 32 KB
+constexpr uint32_t kGTmemCols = 256;
+// kind::f16, D fp32, A/B fp16 K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28
+constexpr uint32_t kGIdesc = (1u << 4) | ((uint32_t)(kGN >> 3) << 17) | ((uint32_t)(kGM >> 4) << 24);
+
+size_t gemm_smem_bytes() {
+  return 1024 + kGStages * (kGStageA + kGStageB) + (2 * kGStages + 1) * 8 + 32 + 4 * kGN * sizeof(float);
+}
+
+__global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant__ CUtensorMap map_a,
+                                                           const __grid_constant__ CUtensorMap map_b,
+                                                           __half* __restrict__ C, int M, int N, int K,
+                                                           float* __restrict__ colpart, int* err) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* sA = smem;
+  unsigned char* sB = smem + kGStages * kGStageA;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kGStages * kGStageB);
+  uint64_t* empty = full + kGStages;
+  uint64_t* done = empty + kGStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  float* csum = reinterpret_cast<float*>(abort_flag + 3);  // [4][kGN] (scalar accesses only)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kGN, m0 = blockIdx.y * kGM;
+  const int nk = (K + kGK - 1) / kGK;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kGStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                 "r"(kGTmemCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (threadIdx.x == 0) {
+    // producer: stage kb % S of round kb / S is free once the MMAs of the previous round on it
+    // have completed (their commit arrives on empty[stage])
+    for (int kb = 0; kb < nk; ++kb) {
+      const int st = kb % kGStages, r = kb / kGStages;
+      if (r > 0 && !mbar_wait_bounded(&empty[st], (uint32_t)((r - 1) & 1))) {
+        *abort_flag = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[st], kGStageA + kGStageB);
+      tma_load_2d(sA + st * kGStageA, &map_a, kb * kGK, m0, &full[st]);
+      tma_load_2d(sB + st * kGStageB, &map_b, kb * kGK, n0, &full[st]);
+    }
+  } else if (threadIdx.x == 32) {
+    // MMA issuer
+    bool ok = true;
+    for (int kb = 0; kb < nk; ++kb) {
+      const int st = kb % kGStages, r = kb / kGStages;
+      if (!mbar_wait_bounded(&full[st], (uint32_t)(r & 1))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a0 = smem_addr(sA + st * kGStageA), b0 = smem_addr(sB + st * kGStageB);
+#pragma unroll
+      for (int kk = 0; kk < kGK / 16; ++kk) {
+        const uint64_t ad = sw128_desc(a0 + kk * 32), bd = sw128_desc(b0 + kk * 32);
+        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
+            "l"(ad), "l"(bd), "r"(kGIdesc), "r"(acc));
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_addr(&empty[st]))
+                   : "memory");
+    }
+    if (ok)
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_addr(done))
+                   : "memory");
+    else
+      *abort_flag = 1;
+  }
+  __syncthreads();
+  const bool aborted = *abort_flag != 0;
+  // every thread takes the same branch: the TMEM loads below are warp-collective
+  const bool landed = __syncthreads_and((!aborted && mbar_wait_bounded(done, 0)) ? 1 : 0) != 0;
+  if (!landed) {
+    if (threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
+    if (aborted && threadIdx.x == 0) {
+      // let the loads already issued land before the shared memory is released
+      for (int i = 0; i < kGStages; ++i) mbar_wait_bounded(&full[i], 0, 1u << 16);
+    }
+  } else {
+    tc_fence_after();
+    const int row = m0 + warp * 32 + lane;
+    for (int ch = 0; ch < kGN / 32; ++ch) {
+      const int c0 = n0 + ch * 32;
+      uint32_t r[32];
+      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ch * 32);
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+          "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+            "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+            "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+            "=r"(r[30]), "=r"(r[31])
+          : "r"(taddr));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      if (c0 >= N) continue;  // warp-uniform: N is a multiple of 32
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      if (row < M) {
+        uint32_t h[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+          h[i] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(C + (size_t)row * N + c0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+      }
+      if (colpart) {
+        // |C| of the stored fp16 values (rows past M are zero: the A tile is zero-filled there);
+        // transpose-reduce: after the steps 16, 8, 4, 2, 1 lane j holds column j's sum
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = row < M ? fabsf(__half2float(__float2half_rn(v[i]))) : 0.f;
+#pragma unroll
+        for (int s = 16; s >= 1; s >>= 1) {
+          const bool up = (lane & s) != 0;
+#pragma unroll
+          for (int i = 0; i < s; ++i) {
+            const float send = up ? v[i] : v[i + s];
+            const float keep = up ? v[i + s] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+          }
+        }
+        csum[warp * kGN + ch * 32 + lane] = v[0];
+      }
+    }
+  }
+  __syncthreads();
+  if (landed && colpart) {
+    for (int c = threadIdx.x; c < kGN; c += kGThreads) {
+      if (n0 + c >= N) continue;
+      colpart[(size_t)blockIdx.y * N + n0 + c] = ((csum[c] + csum[kGN + c]) + csum[2 * kGN + c]) + csum[3 * kGN + c];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGTmemCols));
+  }
+}
+
+// Step 2: one CTA (d threads) per head: score[c] = sum_r |Wq_t[h d + c][r]| (float64) + the
+// key column partials summed over the row tiles in order; the k best (ties to the lower
+// column) written ascending.
+__global__ void k_choose_cols(const __half* __restrict__ Wq_t, int D, int H, int d, int k,
+                              const float* __restrict__ colpart, int mtiles, int32_t* __restrict__ cols,
+                              double* __restrict__ score_out) {
+  extern __shared__ double sc[];  // [d]
+  const int h = blockIdx.x, c = threadIdx.x;
+  const int n = h * d + c;
+  // the weight row sum: one warp per row would be faster; this runs once per prompt
+  const __half* w = Wq_t + (size_t)n * D;
+  double a = 0.0;
+  for (int r = 0; r < D; ++r) a += fabs((double)__half2float(w[r]));
+  double kc = 0.0;
+  for (int t = 0; t < mtiles; ++t) kc += (double)colpart[(size_t)t * H * d + n];
+  sc[c] = a + kc;
+  if (score_out) score_out[n] = a + kc;
+  __syncthreads();
+  int rank = 0;
+  for (int o = 0; o < d; ++o) rank += (sc[o] > sc[c] || (sc[o] == sc[c] && o < c)) ? 1 : 0;
+  const bool keep = rank < k;
+  __syncthreads();
+  // ascending compaction of the kept columns
+  int* flag = reinterpret_cast<int*>(sc);
+  flag[c] = keep ? 1 : 0;
+  __syncthreads();
+  if (keep) {
+    int pos = 0;
+    for (int o = 0; o < c; ++o) pos += flag[o];
+    cols[h * k + pos] = c;
+  }
+}
+
+// Step 3a: the partial query weight, rows h k + j = Wq_t[h d + cols[h][j]] (16-byte copies).
+__global__ void k_extract_rows(const uint4* __restrict__ Wq_t, int D, int d, int k, const int32_t* __restrict__ cols,
+                               uint4* __restrict__ out, int* err) {
+  const int hk = blockIdx.x, h = hk / k;
+  const int c = cols[hk];
+  if (c < 0 || c >= d) {
+    if (threadIdx.x == 0) raise_error(err, IG_DEVERR_INDEX);
+    return;
+  }
+  const int v16 = D / 8;
+  const uint4* src = Wq_t + (size_t)(h * d + c) * v16;
+  for (int i = threadIdx.x; i < v16; i += blockDim.x) out[(size_t)hk * v16 + i] = src[i];
+}
+
+// Step 1 (store) and 3b: for (b, h) and a tile of 64 prompt tokens, the rows of the tokens the
+// pool keeps (t >= N - cap) go to slot t mod cap of the pinned pool (16-byte zero-copy stores)
+// and their chosen columns to the partial key cache.
+constexpr int kScTok = 64;
+__global__ void k_prefill_scatter(const __half* __restrict__ Kt, const __half* __restrict__ Vt, int N, int H,
+                                  int d, int k, int cap, int Lcap, const int32_t* __restrict__ cols,
+                                  uint4* __restrict__ Kp, uint4* __restrict__ Vp, __half* __restrict__ Kpart,
+                                  int* err) {
+  extern __shared__ __align__(16) unsigned char sraw[];
+  __half* sk = reinterpret_cast<__half*>(sraw);  // [kScTok][d]
+  const int t0 = blockIdx.x * kScTok, h = blockIdx.y, b = blockIdx.z;
+  const int first = N > cap ? N - cap : 0;
+  const int vpr = d / 8;
+  const size_t bh = (size_t)b * H + h;
+  for (int i = threadIdx.x; i < kScTok * vpr; i += blockDim.x) {
+    const int tt = i / vpr, v = i % vpr, t = t0 + tt;
+    if (t >= N) continue;
+    const size_t src = ((size_t)b * N + t) * H * d + (size_t)h * d;  // halves
+    const uint4 kv = *reinterpret_cast<const uint4*>(Kt + src + v * 8);
+    reinterpret_cast<uint4*>(sk)[tt * vpr + v] = kv;
+    if (t < first) continue;
+    const int slot = t % cap;
+    Kp[(bh * cap + slot) * vpr + v] = kv;
+    Vp[(bh * cap + slot) * vpr + v] = *reinterpret_cast<const uint4*>(Vt + src + v * 8);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < k * kScTok; i += blockDim.x) {
+    const int c = i / kScTok, tt = i % kScTok, t = t0 + tt;
+    if (t >= N || t < first) continue;
+    const int col = cols[h * k + c];
+    if (col < 0 || col >= d) {
+      raise_error(err, IG_DEVERR_INDEX);
+      continue;
+    }
+    Kpart[(bh * k + c) * Lcap + t % cap] = sk[tt * d + col];
+  }
+}
+
+}  // namespace
+}  // namespace ig
+
+using namespace ig;
+
+namespace {
+
+size_t rup(size_t x) { return round_up(x, 256); }
+
+// workspace: K~ [B N][H d] fp16, V [B N][H d] fp16, column partials [ceil(B N / 128)][H d] fp32
+void prefill_layout(int B, int N, int H, int d, size_t* off_v, size_t* off_cp, size_t* total) {
+  const size_t M = (size_t)B * N, Nn = (size_t)H * d;
+  const size_t mt = (M + kGM - 1) / kGM;
+  *off_v = rup(M * Nn * 2);
+  *off_cp = *off_v + rup(M * Nn * 2);
+  *total = *off_cp + rup(mt * Nn * sizeof(float));
+}
+
+ig_status gemm(cudaStream_t st, const uint16_t* A, const uint16_t* Bt, uint16_t* C, int M, int N, int K,
+               float* colpart) {
+  CUtensorMap ma, mb;
+  ig_status r = make_map(&ma, A, M, K, kGM);
+  if (r != IG_OK) return r;
+  r = make_map(&mb, Bt, N, K, kGN);
+  if (r != IG_OK) return r;
+  const size_t smem = gemm_smem_bytes();
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_tn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill GEMM smem attribute");
+  dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM);
+  k_gemm_tn<<<grid, kGThreads, smem, st>>>(ma, mb, reinterpret_cast<__half*>(C), M, N, K, colpart, error_word());
+  IG_CHECK_LAUNCH("prefill GEMM launch");
+  return IG_OK;
+}
+
+}  // namespace
+
+extern "C" ig_status ig_gemm_tn(void* stream, int M, int N, int K, const uint16_t* A, const uint16_t* Bt,
+                                uint16_t* C, float* colpart) {
+  IG_REQUIRE(M > 0 && N > 0 && K > 0, "M, N, K must be positive");
+  IG_REQUIRE(N % 32 == 0 && K % 8 == 0, "N must be a multiple of 32 and K of 8");
+  IG_REQUIRE((long long)(M + kGM - 1) / kGM <= 65535, "M too large for one launch");
+  IG_REQUIRE(A && Bt && C, "null pointer argument");
+  IG_REQUIRE(aligned(A, 16) && aligned(Bt, 16) && aligned(C, 16), "A, Bt, C must be 16-byte aligned");
+  return gemm(as_stream(stream), A, Bt, C, M, N, K, colpart);
+}
+
+extern "C" size_t ig_prefill_workspace_bytes(int B, int N, int H, int d) {
+  if (B <= 0 || N <= 0 || H <= 0 || d <= 0) return 0;
+  size_t ov, oc, tot;
+  prefill_layout(B, N, H, d, &ov, &oc, &tot);
+  return tot;
+}
+
+extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H, int d,
+                                      int k, int Lcap, const uint16_t* X, const uint16_t* Wq_t, const uint16_t* Wk_t,
+                                      const uint16_t* Wv_t, int32_t* cols, uint16_t* Wq_part_t, uint16_t* Kpart,
+                                      void* workspace, size_t workspace_bytes) {
+  IG_REQUIRE(pool, "null pool");
+  IG_REQUIRE(pool->storage && !pool->fp8, "the prefill writes an fp16 pool with storage");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+  IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
+  IG_REQUIRE(N > 0 && D > 0 && D % 8 == 0, "N > 0 and D a positive multiple of 8");
+  IG_REQUIRE(d == 64 || d == 128, "d must be 64 or 128");
+  IG_REQUIRE(k > 0 && k <= d, "0 < k <= d");
+  IG_REQUIRE(Lcap >= pool->cap && Lcap % 8 == 0, "Lcap must cover the pool and be a multiple of 8");
+  IG_REQUIRE(X && Wq_t && Wk_t && Wv_t && cols && Wq_part_t && Kpart, "null pointer argument");
+  IG_REQUIRE(aligned(X, 16) && aligned(Wq_t, 16) && aligned(Wk_t, 16) && aligned(Wv_t, 16) &&
+                 aligned(Wq_part_t, 16),
+             "X and the weights must be 16-byte aligned");
+  size_t ov, oc, tot;
+  prefill_layout(B, N, H, d, &ov, &oc, &tot);
+  if (!workspace || workspace_bytes < tot)
+    return fail(IG_ERR_CAPACITY, "the prefill needs %zu workspace bytes", tot);
+  IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
+  cudaStream_t st = as_stream(stream);
+  char* ws = static_cast<char*>(workspace);
+  uint16_t* Kt = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* Vt = reinterpret_cast<uint16_t*>(ws + ov);
+  float* colpart = reinterpret_cast<float*>(ws + oc);
+  const int M = B * N, Nn = H * d;
+  const int mtiles = (M + kGM - 1) / kGM;
+  IG_REQUIRE(mtiles <= 65535, "B*N too large for one launch");
+  // Step 1: K~ (with the per-tile column partials of |K~|) and V
+  ig_status r = gemm(st, X, Wk_t, Kt, M, Nn, D, colpart);
+  if (r != IG_OK) return r;
+  r = gemm(st, X, Wv_t, Vt, M, Nn, D, nullptr);
+  if (r != IG_OK) return r;
+  // Step 2: the columns
+  k_choose_cols<<<H, d, d * sizeof(double), st>>>(reinterpret_cast<const __half*>(Wq_t), D, H, d, k, colpart, mtiles,
+                                                  cols, nullptr);
+  IG_CHECK_LAUNCH("column choice launch");
+  // Step 3: the partial weight, then the pool rows and the partial key cache
+  k_extract_rows<<<H * k, 128, 0, st>>>(reinterpret_cast<const uint4*>(Wq_t), D, d, k, cols,
+                                        reinterpret_cast<uint4*>(Wq_part_t), error_word());
+  IG_CHECK_LAUNCH("partial weight launch");
+  const size_t le = (size_t)B * H * pool->cap * d;
+  dim3 sg((N + kScTok - 1) / kScTok, H, B);
+  k_prefill_scatter<<<sg, 256, kScTok * d * 2, st>>>(
+      reinterpret_cast<const __half*>(Kt), reinterpret_cast<const __half*>(Vt), N, H, d, k, pool->cap, Lcap, cols,
+      reinterpret_cast<uint4*>(pool->Kdev + (size_t)layer * le), reinterpret_cast<uint4*>(pool->Vdev + (size_t)layer * le),
+      reinterpret_cast<__half*>(Kpart), error_word());
+  IG_CHECK_LAUNCH("prefill scatter launch");
+  return IG_OK;
+}

@@ -81,6 +81,9 @@ _sig("ig_pool_slot_tokens", _i, _vp, _i, _i, _vp)
 _sig("ig_pool_kv8", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp))
 _sig("ig_pool_evictions", _i, _vp, _i, _i, C.POINTER(C.c_int64))
 _sig("ig_eviction_misses", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp)
+_sig("ig_prefill_workspace_bytes", _sz, _i, _i, _i, _i)
+_sig("ig_prefill_layer", _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz)
+_sig("ig_gemm_tn", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp)
 _sig("ig_attention_recall", _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_captured_fraction", _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_pool_destroy", _i, _vp)
@@ -278,6 +281,21 @@ def ig_pool_evictions(pool, layer, b) -> int:
 def ig_eviction_misses(stream, B, H, Lcap, scores, idx, cnt, resident, miss_cnt, miss_mass):
     _ok(_lib.ig_eviction_misses(_s(stream), B, H, Lcap, _p(scores), _p(idx), _p(cnt), _p(resident),
                                 _p(miss_cnt), _p(miss_mass)), "ig_eviction_misses")
+
+
+def ig_prefill_workspace_bytes(B, N, H, d):
+    return _lib.ig_prefill_workspace_bytes(B, N, H, d)
+
+
+def ig_prefill_layer(stream, pool, layer, B, N, D, H, d, k, Lcap, X, Wq_t, Wk_t, Wv_t, cols, Wq_part_t, Kpart,
+                     workspace, workspace_bytes):
+    _ok(_lib.ig_prefill_layer(_s(stream), pool, layer, B, N, D, H, d, k, Lcap, _p(X), _p(Wq_t), _p(Wk_t), _p(Wv_t),
+                              _p(cols), _p(Wq_part_t), _p(Kpart), _p(workspace), workspace_bytes),
+        "ig_prefill_layer")
+
+
+def ig_gemm_tn(stream, M, N, K, A, Bt, C, colpart=None):
+    _ok(_lib.ig_gemm_tn(_s(stream), M, N, K, _p(A), _p(Bt), _p(C), _p(colpart)), "ig_gemm_tn")
 
 
 def ig_attention_recall(stream, B, H, d, Lcap, scale, q, K, L_valid, idx, cnt, recall, weight):
