@@ -164,6 +164,23 @@ def skew(Xs, Wq, Wk, H: int, d: int, rope_theta: float = 0.0, Kprompt=None):
     return A, sig, Wq_s, Wk_s, Ks
 
 
+def energy_k(sigma, energy: float) -> int:
+    """Per-layer partial width from the skewed query's spectrum (the per-layer ratio proposed
+    as follow-up work): the smallest k in [1, d] whose captured energy, the mean over heads of
+    sum_{i<k} sigma_i^2 / sum_i sigma_i^2 (singular values in descending order), reaches
+    ``energy``; a head with no energy counts as fully captured."""
+    sig = np.asarray(sigma, dtype=np.float64)
+    H, d = sig.shape
+    e2 = sig * sig
+    tot = e2.sum(axis=1)
+    frac = np.where(tot[:, None] > 0, np.cumsum(e2, axis=1) / np.where(tot > 0, tot, 1.0)[:, None], 1.0)
+    mean = frac.mean(axis=0)
+    for kk in range(1, d + 1):
+        if mean[kk - 1] >= energy:
+            return kk
+    return d
+
+
 def choose_columns(Wq_skew, K_skew, H: int, d: int, k: int) -> np.ndarray:
     """Partial weight index generation (section 3.4, "Prefill Stage", Step 2, Fig 9).
 

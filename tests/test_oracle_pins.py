@@ -419,3 +419,35 @@ def test_prefill_pool_placement_is_the_counter_pool_prefill():
         assert np.array_equal(out["K_pool"][:, :, s_], out["K"][:, t])
         assert np.array_equal(out["V_pool"][:, :, s_], out["V"][:, t])
     assert np.array_equal(out["K_part"], ora.partial_key_cache(out["K_pool"], out["cols"]))
+
+
+# --- per-layer partial width from the spectrum ---------------------------------------------------
+def test_energy_k_closed_forms():
+    flat = np.ones((3, 128))
+    for e in (0.1, 0.3, 0.5, 0.9, 1.0):
+        assert ora.energy_k(flat, e) == math.ceil(e * 128 - 1e-9)
+    spike = np.zeros((2, 64))
+    spike[:, 0] = 5.0
+    assert ora.energy_k(spike, 0.99) == 1
+    # sigma_i^2 = 2^-i: captured fraction after k is (1 - 2^-k) / (1 - 2^-d)
+    geo = np.sqrt(2.0 ** -np.arange(32))[None, :]
+    assert ora.energy_k(geo, 0.9) == 4 and ora.energy_k(geo, 0.99) == 7
+    # non-decreasing in the energy target; the mean over heads
+    g = np.random.default_rng(2)
+    s = np.sort(g.random((4, 128)), axis=1)[:, ::-1]
+    ks = [ora.energy_k(s, e) for e in np.linspace(0.05, 1.0, 20)]
+    assert ks == sorted(ks)
+    two = np.stack([np.ones(10), np.r_[1.0, np.zeros(9)]])  # head means 0.1 k and 1.0
+    assert ora.energy_k(two, 0.6) == 2  # (0.2 + 1) / 2 = 0.6
+
+
+def test_skew_spectrum_is_the_svd_of_the_sample_queries():
+    w = synth.scaled(synth.WORKLOADS["tiny"], name="spec", heads=2, hidden=256)
+    Xs, Wq, Wk = synth.skew_inputs(w)
+    A, sig, _, _, _ = ora.skew(Xs, Wq, Wk, w.heads, w.head_dim)
+    Q = Xs.astype(np.float64) @ Wq.astype(np.float64)
+    for h in range(w.heads):
+        Qh = Q[:, h * w.head_dim:(h + 1) * w.head_dim]
+        # singular values: the column norms of Q_h A_h, descending
+        assert np.allclose(np.linalg.norm(Qh @ A[h], axis=0), sig[h], rtol=1e-10)
+        assert np.all(np.diff(sig[h]) <= 0)
