@@ -92,6 +92,18 @@ ig_status ig_skew_weights(int D, int H, int d, float ratio, float rope_theta,
                           uint16_t* Wk_skew, uint16_t* Kp_skew, int32_t* cols, int* k_out,
                           int threads);
 
+/* The singular values of each head's sample queries Q_h = X_s W_Q,h (RoPE-rotated when
+ * rope_theta > 0), descending: sigma host fp32 [H][d] out.  The same SVD as ig_skew_weights
+ * (whose A_h are the matching right singular vectors). */
+ig_status ig_skew_spectrum(int D, int H, int d, float rope_theta, const uint16_t* Xs, int Ns,
+                           const uint16_t* Wq, float* sigma, int threads);
+
+/* A layer's partial width from that spectrum (the per-layer ratio proposed as follow-up work:
+ * layers whose singular values decay faster need fewer columns): the smallest k in [1, d]
+ * whose captured energy, the mean over heads of sum_{i<k} sigma_i^2 / sum_i sigma_i^2, reaches
+ * `energy` (in (0, 1]); heads with no energy count as fully captured.  Host only. */
+ig_status ig_ratio_from_spectrum(int H, int d, const float* sigma, float energy, int* k_out);
+
 /* ------------------------------------------------------------------------------------
  * Speculation: partial query projection and speculated scores for layer i, from layer
  * i-1's attention input.  Section 3.4, "Decoding Stage", Step 1 (q~p = x_a^(i-1) W~_Q^p,(i))
@@ -392,6 +404,9 @@ typedef struct {
   uint16_t* Vg;
   void* workspace;                 /* dev, >= ig_decoder_workspace_bytes(), 256-byte aligned */
   size_t workspace_bytes;
+  const int* ks;                   /* host int [layers]: each layer's partial width (1..config
+                                      k; the arrays above sized with it), or NULL: config k for
+                                      every layer (the per-layer ratio of ig_ratio_from_spectrum) */
 } ig_decoder_buffers;
 
 typedef struct {

@@ -35,6 +35,7 @@ struct ig_decoder {
   std::vector<const float*> A_cols;
   std::vector<uint16_t*> Kpart;
   std::vector<const int32_t*> cols;
+  std::vector<int> ks;  // partial width of each layer (config k when none is given)
   ig_pool* pool = nullptr;
   std::vector<cudaEvent_t> ev_sel, ev_got, ev_att;
   size_t ws_main = 0, ws_sel = 0, ws_fetch = 0;  // workspace regions: S, selection, G (fused fetch)
@@ -124,6 +125,12 @@ extern "C" ig_status ig_decoder_create(const ig_decoder_config* cfg, const ig_de
   ws_regions(&c, &d->ws_main, &d->ws_sel, &d->ws_fetch);
   const int L = c.layers;
   for (int l = 0; l < L; ++l) {
+    const int kl = buf->ks ? buf->ks[l] : c.k;
+    if (kl < 1 || kl > c.k) {
+      delete d;
+      return fail(IG_ERR_INVALID, "layer %d width %d outside [1, config k = %d]", l, kl, c.k);
+    }
+    d->ks.push_back(kl);
     d->Kpart.push_back(buf->Kpart[l]);
     d->cols.push_back(buf->cols[l]);
     d->Wq_part.push_back(buf->Wq_part ? buf->Wq_part[l] : nullptr);
@@ -135,6 +142,7 @@ extern "C" ig_status ig_decoder_create(const ig_decoder_config* cfg, const ig_de
   d->buf.A_cols = nullptr;
   d->buf.Kpart = nullptr;
   d->buf.cols = nullptr;
+  d->buf.ks = nullptr;
   d->ev_sel.assign(L, nullptr);
   d->ev_got.assign(L, nullptr);
   d->ev_att.assign(L, nullptr);
@@ -182,7 +190,8 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
   IG_REQUIRE(!(c.rope_theta > 0.f) || io->positions, "RoPE decoding needs positions");
   cudaStream_t S = as_stream(stream), G = as_stream(side_stream);
   IG_REQUIRE(S != G, "the fetch stream must differ from the compute stream");
-  const int L = c.layers, B = c.B, H = c.H, d = c.d, D = c.D, k = c.k, Lc = c.Lcap;
+  const int L = c.layers, B = c.B, H = c.H, d = c.d, D = c.D, Lc = c.Lcap;
+  const std::vector<int>& ks = dec->ks;
   const size_t xs = (size_t)B * D, ts = (size_t)B * H * d;
   char* ws = static_cast<char*>(b.workspace);
   const size_t spec_att_ws = dec->ws_main;
@@ -212,9 +221,9 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     }
     if (r != IG_OK || !slot) return r;
     if (l == 0)
-      return ig_append_kv(S, nullptr, 0, B, H, d, k, Lc, slot, dec->cols[0], io->k_new, io->v_new,
+      return ig_append_kv(S, nullptr, 0, B, H, d, ks[0], Lc, slot, dec->cols[0], io->k_new, io->v_new,
                           dec->Kpart[0], b.K0, b.V0);
-    return ig_append_kv(S, dec->pool, l, B, H, d, k, Lc, slot, dec->cols[l],
+    return ig_append_kv(S, dec->pool, l, B, H, d, ks[l], Lc, slot, dec->cols[l],
                         io->k_new + (size_t)l * ts, io->v_new + (size_t)l * ts, dec->Kpart[l],
                         nullptr, nullptr);
   };
@@ -255,16 +264,16 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     ig_status r;
     if (fused) {
       const bool rope = c.rope_theta > 0.f;
-      r = ig_speculate_select(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs,
+      r = ig_speculate_select(S, B, D, H, d, ks[l], Lc, io->x + (size_t)(l - 1) * xs,
                               rope ? dec->Wq[l] : dec->Wq_part[l], rope ? dec->A_cols[l] : nullptr,
                               rope ? io->positions : nullptr, c.rope_theta, dec->Kpart[l], io->L_valid,
                               c.score_scale, c.alpha, idx, cnt, used, nullptr, nullptr, ws, spec_att_ws);
     } else if (c.rope_theta > 0.f) {
-      r = ig_speculate_rope(S, B, D, H, d, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq[l],
+      r = ig_speculate_rope(S, B, D, H, d, ks[l], Lc, io->x + (size_t)(l - 1) * xs, dec->Wq[l],
                             dec->A_cols[l], io->positions, c.rope_theta, dec->Kpart[l], io->L_valid,
                             c.score_scale, sc, nullptr, ws, spec_att_ws);
     } else {
-      r = ig_speculate(S, B, D, H, k, Lc, io->x + (size_t)(l - 1) * xs, dec->Wq_part[l],
+      r = ig_speculate(S, B, D, H, ks[l], Lc, io->x + (size_t)(l - 1) * xs, dec->Wq_part[l],
                        dec->Kpart[l], io->L_valid, c.score_scale, sc, nullptr, ws, spec_att_ws);
     }
     if (r != IG_OK) return r;
@@ -289,7 +298,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
       if (ae != cudaSuccess) return cuda_fail(ae, "decode step wait");
       if (io->slot) {
         const size_t off = (size_t)l * ts;
-        ig_status r = ig_append_kv(S, dec->pool, l, B, H, d, k, Lc, io->slot + (size_t)l * B, dec->cols[l],
+        ig_status r = ig_append_kv(S, dec->pool, l, B, H, d, ks[l], Lc, io->slot + (size_t)l * B, dec->cols[l],
                                    io->k_new + off, io->v_new + off, dec->Kpart[l], nullptr, nullptr);
         if (r != IG_OK) return r;
       }

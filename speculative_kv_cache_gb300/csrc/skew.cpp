@@ -71,6 +71,8 @@ struct SkewJob {
   uint16_t* Wk_skew;
   uint16_t* Kp_skew;
   int32_t* cols;
+  float* sigma = nullptr;      // [H][d] singular values, descending (optional)
+  bool spectrum_only = false;  // stop after the SVD
   std::atomic<int> failed{0};
 };
 
@@ -159,6 +161,9 @@ void skew_head(SkewJob& J, int h) {
   std::vector<int> ord(d);
   for (int j = 0; j < d; ++j) ord[j] = j;
   std::stable_sort(ord.begin(), ord.end(), [&](int x, int y) { return nrm[x] > nrm[y]; });
+  if (J.sigma)
+    for (int j = 0; j < d; ++j) J.sigma[(size_t)h * d + j] = (float)sqrt(nrm[ord[j]]);
+  if (J.spectrum_only) return;
   std::vector<double> Ah((size_t)d * d);  // row-major A_h[i][j]
   for (int j = 0; j < d; ++j) {
     const double* v = &V[(size_t)ord[j] * d];
@@ -255,6 +260,61 @@ extern "C" ig_status ig_skew_weights(int D, int H, int d, float ratio, float rop
   worker();
   for (auto& t : pool) t.join();
   if (J.failed) return ig::fail(IG_ERR_NUMERIC, "Jacobi SVD did not converge");
+  *k_out = k;
+  return IG_OK;
+}
+
+extern "C" ig_status ig_skew_spectrum(int D, int H, int d, float rope_theta, const uint16_t* Xs, int Ns,
+                                      const uint16_t* Wq, float* sigma, int threads) {
+  if (D <= 0 || H <= 0 || d <= 0 || Ns <= 0) return ig::fail(IG_ERR_INVALID, "sizes must be positive");
+  if (!Xs || !Wq || !sigma) return ig::fail(IG_ERR_INVALID, "null required pointer");
+  if (rope_theta < 0.f || (rope_theta > 0.f && d % 2)) return ig::fail(IG_ERR_INVALID, "RoPE needs even d and theta > 0");
+  std::vector<double> X((size_t)Ns * D);
+  for (size_t i = 0; i < X.size(); ++i) X[i] = half_to_double(Xs[i]);
+  SkewJob J;
+  J.D = D; J.H = H; J.d = d; J.Ns = Ns; J.Nk = 0; J.k = 1;
+  J.theta = rope_theta;
+  J.X = X.data(); J.Wq = Wq; J.Wk = nullptr; J.Kp = nullptr;
+  std::vector<float> A((size_t)H * d * d);
+  J.A = A.data(); J.Wq_skew = nullptr; J.Wk_skew = nullptr; J.Kp_skew = nullptr;
+  std::vector<int32_t> cols(H);
+  J.cols = cols.data();
+  J.sigma = sigma;
+  J.spectrum_only = true;
+  int nt = threads > 0 ? threads : (int)std::thread::hardware_concurrency();
+  if (nt < 1) nt = 1;
+  if (nt > H) nt = H;
+  std::atomic<int> next{0};
+  auto worker = [&]() {
+    for (int h = next++; h < H; h = next++) skew_head(J, h);
+  };
+  std::vector<std::thread> pool;
+  for (int i = 1; i < nt; ++i) pool.emplace_back(worker);
+  worker();
+  for (auto& t : pool) t.join();
+  if (J.failed) return ig::fail(IG_ERR_NUMERIC, "Jacobi SVD did not converge");
+  return IG_OK;
+}
+
+extern "C" ig_status ig_ratio_from_spectrum(int H, int d, const float* sigma, float energy, int* k_out) {
+  if (H <= 0 || d <= 0 || !sigma || !k_out) return ig::fail(IG_ERR_INVALID, "bad argument");
+  if (!(energy > 0.f && energy <= 1.f)) return ig::fail(IG_ERR_INVALID, "energy must be in (0, 1]");
+  std::vector<double> mean(d, 0.0);
+  for (int h = 0; h < H; ++h) {
+    double tot = 0;
+    for (int j = 0; j < d; ++j) tot += (double)sigma[(size_t)h * d + j] * sigma[(size_t)h * d + j];
+    double run = 0;
+    for (int j = 0; j < d; ++j) {
+      run += (double)sigma[(size_t)h * d + j] * sigma[(size_t)h * d + j];
+      mean[j] += tot > 0 ? run / tot : 1.0;
+    }
+  }
+  int k = d;
+  for (int j = 0; j < d; ++j)
+    if (mean[j] / H >= (double)energy) {
+      k = j + 1;
+      break;
+    }
   *k_out = k;
   return IG_OK;
 }

@@ -30,6 +30,12 @@ class Decoder:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
         if pool_fp8 and fused_fetch:
             raise ValueError("the fused fetch + attention reads fp16 pools only")
+        # k: one partial width for every layer, or one per layer (e.g. from ig_ratio_from_spectrum)
+        ks = [int(x) for x in k] if hasattr(k, "__len__") else [int(k)] * layers
+        if len(ks) != layers:
+            raise ValueError("one partial width per layer")
+        k = max(ks)
+        self.ks = ks
         self.layers, self.B, self.H, self.d, self.D, self.k, self.Lcap = layers, B, H, d, D, k, Lcap
         self.pool_cap = pool_cap
         self.rope = rope_theta > 0
@@ -46,11 +52,11 @@ class Decoder:
                                     int(bool(fused_select)), int(bool(fused_fetch)))
         # per-layer state: partial query weight (or full W_Q and A[:, S] for RoPE), columns,
         # partial key cache; layer 0 keeps its full KV in HBM instead
-        self.Wq_part = [None] + [e(H * k, D) for _ in range(1, layers)] if not self.rope else None
+        self.Wq_part = [None] + [e(H * ks[l], D) for l in range(1, layers)] if not self.rope else None
         self.Wq = [None] + [e(H * d, D) for _ in range(1, layers)] if self.rope else None
-        self.A_cols = [None] + [e(H, d, k, dt=torch.float32) for _ in range(1, layers)] if self.rope else None
-        self.cols = [torch.zeros(H, k, dtype=i32, device=self.dev) for _ in range(layers)]
-        self.Kpart = [None] + [e(B, H, k, Lcap) for _ in range(1, layers)]
+        self.A_cols = [None] + [e(H, d, ks[l], dt=torch.float32) for l in range(1, layers)] if self.rope else None
+        self.cols = [torch.zeros(H, ks[l], dtype=i32, device=self.dev) for l in range(layers)]
+        self.Kpart = [None] + [e(B, H, ks[l], Lcap) for l in range(1, layers)]
         self.K0, self.V0 = e(B, H, Lcap, d), e(B, H, Lcap, d)
         self.scores = e(B, H, Lcap, dt=torch.float32)
         self.idx = e(2, B, H, Lcap, dt=i32)
@@ -102,6 +108,8 @@ class Decoder:
         b.Kg = self.Kg.data_ptr() if self.Kg is not None else None
         b.Vg = self.Vg.data_ptr() if self.Vg is not None else None
         b.workspace, b.workspace_bytes = self.ws.data_ptr(), self.ws.numel()
+        arrs["ks"] = (ig.C.c_int * self.layers)(*self.ks)
+        b.ks = ig.C.cast(arrs["ks"], ig.C.POINTER(ig.C.c_int))
         return b, arrs
 
     # ------------------------------------------------------------------ setup (not timed)

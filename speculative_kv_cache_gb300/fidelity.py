@@ -60,12 +60,17 @@ class _Basis:
         self.Kpart[..., :T] = part.transpose(-1, -2)
 
 
-def run(w: synth.Workload, alpha: float = 4.0, steps: int = 4, decay: float = 0.5, device: str = "cuda:0") -> list:
+def run(w: synth.Workload, alpha: float = 4.0, steps: int = 4, decay=0.5, device: str = "cuda:0",
+        energy: float | None = None) -> list:
     """Per layer >= 1: mean recall, weight recall, selected fraction and captured fraction for
-    the three variants (skew / no skew, speculating from layer i-1's or layer i's input)."""
+    the three variants (skew / no skew, speculating from layer i-1's or layer i's input).
+
+    ``decay``: the spectral decay of the synthetic weights, one value or one per layer.
+    ``energy``: choose each layer's partial width from its skewed query's spectrum
+    (``ig_skew_spectrum`` + ``ig_ratio_from_spectrum``) instead of the workload's ratio."""
     dev = torch.device(device)
     B, H, d, D, L, T = w.batch, w.heads, w.head_dim, w.hidden, w.layers, w.prompt
-    k = w.k
+    decays = list(decay) if hasattr(decay, "__len__") else [decay] * L
     Lcap = (T + 7) // 8 * 8
     scale = 1.0 / math.sqrt(d)
     f32, i32, u8 = torch.float32, torch.int32, torch.uint8
@@ -76,12 +81,18 @@ def run(w: synth.Workload, alpha: float = 4.0, steps: int = 4, decay: float = 0.
     rec = torch.empty((B, H), dtype=f32, device=dev)
     wt = torch.empty((B, H), dtype=f32, device=dev)
     frac = torch.empty((B, H), dtype=f32, device=dev)
-    ws = torch.empty(max(ig.ig_speculate_workspace_bytes(B, D, H, k), 256), dtype=u8, device=dev)
+    ws = torch.empty(max(ig.ig_speculate_workspace_bytes(B, D, H, d), 256), dtype=u8, device=dev)
     sws = torch.empty(max(ig.ig_select_workspace_bytes(B, H), 256), dtype=u8, device=dev)
     st = torch.cuda.current_stream(dev)
     rows = []
     for l in range(1, L):
-        Wq_np, Wk_np = synth.structured_qk_weights(w, l, decay)
+        Wq_np, Wk_np = synth.structured_qk_weights(w, l, decays[l])
+        k = w.k
+        if energy is not None:
+            Xs0, _, _ = synth.skew_inputs(w, l)
+            sig = np.zeros((H, d), np.float32)
+            ig.ig_skew_spectrum(D, H, d, 0.0, Xs0, Xs0.shape[0], Wq_np, sig)
+            k = ig.ig_ratio_from_spectrum(H, d, sig, energy)
         X = torch.from_numpy(synth.hidden_states(w, l, T)).to(dev)
         Wq, Wk = torch.from_numpy(Wq_np).to(dev), torch.from_numpy(Wk_np).to(dev)
         K = (X.float() @ Wk.float()).half()                                # [B, T, H*d] unskewed
@@ -93,8 +104,9 @@ def run(w: synth.Workload, alpha: float = 4.0, steps: int = 4, decay: float = 0.
         Kp = K.view(B * T, H, d).cpu().numpy()
         Kp_skew = np.zeros_like(Kp)
         # ig_skew_weights forms Q_s = X_s W_Q from the sample input itself (float64)
-        ig.ig_skew_weights(D, H, d, w.ratio, 0.0, Xs, Xs.shape[0], Wq_np, Wk_np, Kp, B * T, A, Wq_skew, None,
-                           Kp_skew, cols_s)
+        kk = ig.ig_skew_weights(D, H, d, k / d, 0.0, Xs, Xs.shape[0], Wq_np, Wk_np, Kp, B * T, A, Wq_skew, None,
+                                Kp_skew, cols_s)
+        assert kk == k
         skew = _Basis(torch.from_numpy(Wq_skew).to(dev), torch.from_numpy(Kp_skew).to(dev).view(B, T, H * d),
                       torch.from_numpy(cols_s).to(dev), H, d, k, Lcap, dev)
         raw = _Basis(Wq, K, _raw_columns(Wq, K, H, d, k), H, d, k, Lcap, dev)
@@ -116,7 +128,7 @@ def run(w: synth.Workload, alpha: float = 4.0, steps: int = 4, decay: float = 0.
                 a["selected"].append(cnt.cpu().numpy() / T)
                 a["captured"].append(frac.cpu().numpy().copy())
         ig.ig_check(st)
-        row = dict(layer=l)
+        row = dict(layer=l, k=k, decay=decays[l])
         for name, a in acc.items():
             row[name] = {m: float(np.mean(v)) for m, v in a.items()}
         rows.append(row)
@@ -144,7 +156,9 @@ def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--alpha", type=float, default=4.0)
     p.add_argument("--steps", type=int, default=4)
-    p.add_argument("--decay", type=float, default=0.5)
+    p.add_argument("--decay", default="0.5", help="one value, or one per layer (comma-separated)")
+    p.add_argument("--energy", type=float, default=None,
+                   help="choose each layer's width from its spectrum (captured-energy target)")
     p.add_argument("--layers", type=int, default=4)
     p.add_argument("--batch", type=int, default=2)
     p.add_argument("--heads", type=int, default=8)
@@ -152,7 +166,9 @@ def main(argv=None):
     p.add_argument("--prompt", type=int, default=2048)
     a = p.parse_args(argv)
     w = fidelity_workload(a.layers, a.batch, a.heads, a.hidden, a.prompt)
-    for row in run(w, a.alpha, a.steps, a.decay):
+    decay = [float(x) for x in a.decay.split(",")]
+    decay = decay[0] if len(decay) == 1 else decay
+    for row in run(w, a.alpha, a.steps, decay, energy=a.energy):
         print(json.dumps(row), flush=True)
 
 

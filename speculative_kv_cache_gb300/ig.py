@@ -64,6 +64,8 @@ _sig("ig_version", _i)
 _sig("ig_check", _i, _vp)
 _sig("ig_skew_weights", _i, _i, _i, _i, _f, _f, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp,
      _vp, _vp, _i)
+_sig("ig_skew_spectrum", _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _i)
+_sig("ig_ratio_from_spectrum", _i, _i, _i, _vp, _f, C.POINTER(_i))
 _sig("ig_speculate_workspace_bytes", _sz, _i, _i, _i, _i)
 _sig("ig_speculate", _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp, _vp, _sz)
 _sig("ig_speculate_static", _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp)
@@ -158,6 +160,16 @@ def ig_skew_weights(D, H, d, ratio, rope_theta, Xs, Ns, Wq, Wk, Kp, Nk, A, Wq_sk
     _ok(_lib.ig_skew_weights(D, H, d, ratio, rope_theta, _p(Xs), Ns, _p(Wq), _p(Wk), _p(Kp), Nk,
                              _p(A), _p(Wq_skew), _p(Wk_skew), _p(Kp_skew), _p(cols), C.byref(k),
                              threads), "ig_skew_weights")
+    return k.value
+
+
+def ig_skew_spectrum(D, H, d, rope_theta, Xs, Ns, Wq, sigma, threads=0):
+    _ok(_lib.ig_skew_spectrum(D, H, d, rope_theta, _p(Xs), Ns, _p(Wq), _p(sigma), threads), "ig_skew_spectrum")
+
+
+def ig_ratio_from_spectrum(H, d, sigma, energy) -> int:
+    k = C.c_int(0)
+    _ok(_lib.ig_ratio_from_spectrum(H, d, _p(sigma), energy, C.byref(k)), "ig_ratio_from_spectrum")
     return k.value
 
 
@@ -371,7 +383,7 @@ class DecoderBuffers(C.Structure):
     _fields_ = [("Wq_part", C.POINTER(_vp)), ("Wq", C.POINTER(_vp)), ("A_cols", C.POINTER(_vp)),
                 ("Kpart", C.POINTER(_vp)), ("cols", C.POINTER(_vp)), ("K0", _vp), ("V0", _vp),
                 ("scores", _vp), ("idx", _vp), ("cnt", _vp), ("used", _vp), ("Kg", _vp), ("Vg", _vp),
-                ("workspace", _vp), ("workspace_bytes", _sz)]
+                ("workspace", _vp), ("workspace_bytes", _sz), ("ks", C.POINTER(_i))]
 
 
 class StepIO(C.Structure):

@@ -28,7 +28,7 @@ def prefill_decoder_layer(dec, l: int, X, Wq_t, Wk_t, Wv_t, workspace=None):
     dec.S.wait_stream(torch.cuda.current_stream(X.device))
     with torch.cuda.stream(dec.S):
         dec.Kpart[l].zero_()
-        ig.ig_prefill_layer(dec.S, dec.pool, l, B, N, D, dec.H, dec.d, dec.k, dec.Lcap, X, Wq_t, Wk_t, Wv_t,
+        ig.ig_prefill_layer(dec.S, dec.pool, l, B, N, D, dec.H, dec.d, dec.ks[l], dec.Lcap, X, Wq_t, Wk_t, Wv_t,
                             dec.cols[l], dec.Wq_part[l], dec.Kpart[l], workspace, workspace.numel())
     dec.S.synchronize()
     return workspace

@@ -33,7 +33,9 @@ def mods():
     return ig, decoder
 
 
-def _layer_data(w, l, cap, rope):
+def _layer_data(w, l, cap, rope, ratio=None):
+    if ratio is not None:  # this layer's own partial width
+        w = synth.scaled(w, ratio=ratio)
     K, V = synth.pool_layer(w, l, cap=cap)
     cols = synth.skewed_columns(w, l)
     if rope:
@@ -44,18 +46,20 @@ def _layer_data(w, l, cap, rope):
     return dict(K=K, V=V, cols=cols, Wqp=synth.skewed_partial_weight(w, l))
 
 
-def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True, fused_fetch=False, graph=False):
+def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True, fused_fetch=False, graph=False,
+         ratios=None):
     ig, decoder = mods
     dev = "cuda:0"
     Lcap = w.lcap
     cap = w.pool_cap
     scale = np.float32(1.0 / math.sqrt(w.head_dim))
     alpha = 4.0
-    dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k,
+    ks = [synth.scaled(w, ratio=r).k for r in ratios] if ratios else [w.k] * w.layers
+    dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=ks if ratios else w.k,
                           Lcap=Lcap, pool_cap=cap, alpha=alpha, rope_theta=w.rope_theta,
                           fused_select=fused_select, fused_fetch=fused_fetch, graph=graph, device=dev)
     try:
-        data = [_layer_data(w, l, cap, rope) for l in range(w.layers)]
+        data = [_layer_data(w, l, cap, rope, ratios[l] if ratios else None) for l in range(w.layers)]
         for l, dd in enumerate(data):
             t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
             if rope:
@@ -109,7 +113,7 @@ def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True, fused
                 if rope:
                     qp = ora.partial_query_rope(x[l - 1], dd["Wq"], dd["A"], dd["cols"], pos, w.rope_theta)
                 else:
-                    qp = ora.partial_query(x[l - 1], dd["Wqp"], w.heads, w.k)
+                    qp = ora.partial_query(x[l - 1], dd["Wqp"], w.heads, ks[l])
                 Kpart = ora.partial_key_cache(oK[l], dd["cols"])
                 sc = ora.speculate(qp, Kpart, Lv, scale)
                 # the GPU's own index sets (both gather buffers survive a step of <= 3 layers):
@@ -166,6 +170,14 @@ def test_decoder_rope_steps(mods, fetch):
     w = synth.scaled(synth.WORKLOADS["llama-2-7b"], name="dec-rope", layers=3, batch=2, heads=4,
                      hidden=512, prompt=260, gen=8)
     _run(mods, w, steps=2, rope=True, fused_fetch=fetch == "fused")
+
+
+@pytest.mark.parametrize("rope", [False, True])
+def test_decoder_per_layer_widths(mods, rope):
+    """Each layer with its own partial width (the per-layer ratio), fused and plain paths."""
+    base = synth.WORKLOADS["llama-2-7b"] if rope else synth.WORKLOADS["opt-30b"]
+    w = synth.scaled(base, name="dec-ks", layers=4, batch=2, heads=4, hidden=512, prompt=220, gen=8)
+    _run(mods, w, steps=2, rope=rope, ratios=[0.3, 0.125, 0.5, 0.25])
 
 
 def test_decoder_fused_fetch_graph_replay(mods):

@@ -101,3 +101,12 @@ def test_fidelity_study_small(mods):
             assert 0.0 <= r[name][m] <= 1.0
     # the skew concentrates the dot product in the chosen columns
     assert r["skew"]["captured"] > r["no_skew"]["captured"] + 0.15
+
+
+def test_fidelity_per_layer_width_from_spectrum(mods):
+    ig, fidelity = mods
+    w = fidelity.fidelity_workload(layers=3, batch=1, heads=2, hidden=512, prompt=256)
+    rows = fidelity.run(w, alpha=4.0, steps=1, decay=[0.5, 0.2, 1.2], energy=0.8)
+    ks = [r["k"] for r in rows if "layer" in r]
+    # a faster-decaying spectrum needs fewer columns for the same captured energy
+    assert ks[1] < ks[0] and all(1 <= k <= w.head_dim for k in ks)

@@ -81,3 +81,22 @@ def test_skew_rejects_bad_arguments(ig):
     with pytest.raises(ig.IGError):
         ig.ig_skew_weights(8, 1, 7, 0.5, 10000.0, z, 8, z, z, None, 0, np.zeros(64, np.float32), None, None,
                            None, np.zeros(8, np.int32))
+
+
+def test_spectrum_and_energy_k_match_oracle():
+    """ig_skew_spectrum equals the oracle's singular values; ig_ratio_from_spectrum equals the
+    oracle's energy_k on the same spectrum, at several targets."""
+    from oracle import infinigen as ora
+    from speculative_kv_cache_gb300 import ig, synth
+
+    w = synth.scaled(synth.WORKLOADS["tiny"], name="spec2", heads=3, hidden=256)
+    H, d = w.heads, w.head_dim
+    Xs, Wq, Wk = synth.skew_inputs(w)
+    Wq_s, _ = synth.structured_qk_weights(w, 0, 0.7)
+    for W in (Wq, Wq_s):
+        sig = np.zeros((H, d), np.float32)
+        ig.ig_skew_spectrum(w.hidden, H, d, 0.0, Xs, Xs.shape[0], W, sig)
+        _, want, _, _, _ = ora.skew(Xs, W, Wk, H, d)
+        assert np.allclose(sig, want, rtol=1e-5, atol=1e-6 * want.max())
+        for e in (0.3, 0.5, 0.8, 0.95):
+            assert ig.ig_ratio_from_spectrum(H, d, sig, e) == ora.energy_k(sig.astype(np.float64), e)
