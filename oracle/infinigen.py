@@ -267,6 +267,34 @@ def prefill_layer(X, Wq_skew, Wk_skew, Wv, H: int, d: int, k: int, cap: int):
                 K_part=partial_key_cache(Kp, cols))
 
 
+def prefill_layer_rope(X, Wq_skew, Wk, Wv, A, theta: float, H: int, d: int, k: int, cap: int):
+    """Prefill Stage, Steps 1-3, for one layer of a RoPE model.
+
+    The keys are rotated before the skew, so the skew cannot live in W_K: K = X W_K (rounded
+    once to float16, as a projection stores it), then K~_h = RoPE_t(K_h) A_h at the token's
+    position t (float64, rounded once to float16).  V = X W_V.  The columns come from W~_Q =
+    W_Q A and the keys; the decode stage of a RoPE model takes A_h[:, S_h] instead of a partial
+    weight.  Pool placement and the partial key cache as in :func:`prefill_layer`.
+
+    Returns a dict as :func:`prefill_layer` with A_cols [H, d, k] (float64) for Wq_part.
+    """
+    X64 = np.asarray(X, dtype=np.float64)
+    B, N, _ = X64.shape
+    Kraw = (X64 @ np.asarray(Wk, dtype=np.float64)).astype(np.float16).reshape(B, N, H, d)
+    Kr = rope(Kraw.astype(np.float64), np.arange(N)[None, :, None], theta)
+    A64 = np.asarray(A, dtype=np.float64)
+    Kt = np.einsum("bnhi,hij->bnhj", Kr, A64).astype(np.float16)
+    Vt = (X64 @ np.asarray(Wv, dtype=np.float64)).astype(np.float16).reshape(B, N, H, d)
+    cols = choose_columns(Wq_skew, Kt, H, d, k)
+    Kp = np.zeros((B, H, cap, d), dtype=np.float16)
+    Vp = np.zeros((B, H, cap, d), dtype=np.float16)
+    for t in range(max(0, N - cap), N):
+        Kp[:, :, t % cap] = Kt[:, t]
+        Vp[:, :, t % cap] = Vt[:, t]
+    A_cols = np.stack([A64[h][:, cols[h]] for h in range(H)])
+    return dict(K=Kt, V=Vt, cols=cols, A_cols=A_cols, K_pool=Kp, V_pool=Vp, K_part=partial_key_cache(Kp, cols))
+
+
 # ----------------------------------------------------------------------------------------
 # Decode stage (section 3.4, "Decoding Stage: Speculative KV Selection and Prefetching")
 # ----------------------------------------------------------------------------------------

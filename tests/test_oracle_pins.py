@@ -451,3 +451,30 @@ def test_skew_spectrum_is_the_svd_of_the_sample_queries():
         # singular values: the column norms of Q_h A_h, descending
         assert np.allclose(np.linalg.norm(Qh @ A[h], axis=0), sig[h], rtol=1e-10)
         assert np.all(np.diff(sig[h]) <= 0)
+
+
+def test_prefill_rope_keys_are_the_skews_rotated_prompt_keys():
+    """RoPE prefill: RoPE_t(X W_K) A equals what the skew produces from the post-RoPE prompt
+    keys (ora.skew with Kprompt), and the partial key of slot t scored with the partial RoPE
+    query equals the full rotated dot product restricted to the columns (the identity the
+    decode stage relies on)."""
+    w = synth.scaled(synth.WORKLOADS["llama-2-7b"], name="pfr", heads=2, hidden=256, batch=1, prompt=40,
+                     head_dim=64, sample_rows=256)
+    H, d, k, th = w.heads, w.head_dim, w.k, w.rope_theta
+    Xs, Wq, Wk = synth.skew_inputs(w)
+    X = synth.hidden_states(w, 0, w.prompt)
+    Kraw = (X.astype(np.float64) @ Wk.astype(np.float64)).astype(np.float16).reshape(1, -1, H, d)
+    Kpost = ora.rope(Kraw.astype(np.float64), np.arange(w.prompt)[None, :, None], th).reshape(-1, H, d)
+    A, _, Wq_s, _, K_s = ora.skew(Xs, Wq, Wk, H, d, rope_theta=th, Kprompt=Kpost)
+    Wv = synth.normal_f16(synth.rng(w.name, "Wv", 0), Wq.shape, w.w_std)
+    o = ora.prefill_layer_rope(X, Wq_s, Wk, Wv, A, th, H, d, k, cap=w.prompt)
+    assert np.abs(o["K"].reshape(-1, H, d).astype(np.float64) - K_s.astype(np.float64)).max() <= \
+        2e-3 * np.abs(K_s.astype(np.float64)).max()
+    # decode identity: q A[:, S] . K~[:, S] with the rotated query
+    x = synth.normal_f16(synth.rng(w.name, "xq", 0), (1, w.hidden), 1.0)
+    pos = np.array([w.prompt])
+    qp = ora.partial_query_rope(x, Wq, A, o["cols"], pos, th)  # [1, H, k]
+    for h in range(H):
+        kp = o["K_part"][0, h].astype(np.float64)  # [k, cap]
+        assert np.allclose(qp[0, h] @ kp, qp[0, h] @ o["K"][0, :, h][:, o["cols"][h]].T.astype(np.float64))
+        assert np.array_equal(o["A_cols"][h], A[h][:, o["cols"][h]])
