@@ -509,7 +509,7 @@ ig_status ig_captured_fraction(void* stream, int B, int H, int d, int k, int Lca
 
 /* ------------------------------------------------------------------------------------
  * Prefill stage (section 3.4, "Prefill Stage: Partial Weight Index Generation", Steps 1-3;
- * models without RoPE).  For one layer and a prompt of N tokens per sequence:
+ * models without RoPE; ig_prefill_layer_rope below for RoPE models).  For one layer and a prompt of N tokens per sequence:
  *   Step 1  K~ = X W~_K and V = X W_V on the tensor cores (fp16 in, fp32 accumulate, fp16
  *           out); the rows of the tokens the pool keeps go to it, token t at slot t mod cap
  *           (the pool's own prefill placement: call ig_pool_prefill(pool, N, ...) for the
@@ -526,7 +526,7 @@ ig_status ig_captured_fraction(void* stream, int B, int H, int d, int k, int Lca
  *   Wq_part_t     dev fp16 [H*k][D] out
  *   Kpart         dev fp16 [B][H][k][Lcap] out (resident slots written; others untouched)
  *   workspace     dev, >= ig_prefill_workspace_bytes(B, N, H, d), 256-byte aligned (holds
- *                 K~ and V, 4 B N H d bytes, and per-tile column sums)
+ *                 K~ and V, 4 B N H d bytes, per-tile column sums and a RoPE table)
  * The pool must have storage and fp16 rows; d must be 64 or 128; D a multiple of 8. */
 size_t ig_prefill_workspace_bytes(int B, int N, int H, int d);
 ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,
@@ -534,6 +534,23 @@ ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, int B, int N,
                            const uint16_t* Wk_t, const uint16_t* Wv_t, int32_t* cols,
                            uint16_t* Wq_part_t, uint16_t* Kpart, void* workspace,
                            size_t workspace_bytes);
+
+/* The prefill of a RoPE model's layer.  The keys are rotated before the skew, so the skew is
+ * not in the key weight: K = X W_K (tensor cores, rounded to fp16), then each row of head h
+ * becomes K~ = RoPE_t(K_h) A_h (token t of the prompt at position t; angles in float64, the
+ * rest in fp32, rounded to fp16).  The columns, the pool rows and the partial key cache as in
+ * ig_prefill_layer; instead of a partial weight the decode stage of a RoPE model takes
+ * A_cols = A_h[:, cols[h]] (ig_speculate_rope).
+ *   Wq_t   dev fp16 [H*d][D]  W~_Q^T = (W_Q A)^T (skewed; it enters the column score only)
+ *   Wk_t   dev fp16 [H*d][D]  W_K^T (unskewed);  Wv_t dev fp16 [H*d][D]  W_V^T
+ *   A      dev fp32 [H][d][d] the skew matrices (ig_skew_weights)
+ *   A_cols dev fp32 [H][d][k] out
+ * Workspace: ig_prefill_workspace_bytes(B, N, H, d) (the same query). */
+ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,
+                                int d, int k, int Lcap, float rope_theta, const uint16_t* X,
+                                const uint16_t* Wq_t, const uint16_t* Wk_t, const uint16_t* Wv_t,
+                                const float* A, int32_t* cols, float* A_cols, uint16_t* Kpart,
+                                void* workspace, size_t workspace_bytes);
 
 /* The prefill's tensor-core GEMM on its own: C[M][N] = A[M][K] Bt[N][K]^T, fp16 operands
  * (both K-major), fp32 accumulation, fp16 result (row-major).  With colpart (dev fp32

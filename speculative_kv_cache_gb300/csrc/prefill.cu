@@ -1,5 +1,6 @@
 // Prefill stage on the GPU (InfiniGen paper-graph summary, section 3.4, "Prefill Stage:
-// Partial Weight Index Generation", Steps 1-3; no RoPE):
+// Partial Weight Index Generation", Steps 1-3; RoPE models rotate each key before the skew, so
+// for them K = X W_K is followed by a kernel computing K~_h = RoPE_t(K_h) A_h):
 //   Step 1  K~ = X W~_K and V = X W_V for every prompt token (a tcgen05 GEMM), the rows of the
 //           tokens the pool keeps written to the pinned pool, token t at slot t mod cap;
 //   Step 2  column score = column sums of |W~_Q| plus column sums of |K~| over every prompt
@@ -282,6 +283,88 @@ __global__ void k_prefill_scatter(const __half* __restrict__ Kt, const __half* _
   }
 }
 
+// RoPE: cos and sin of t * theta^(-2j/d) for t < N, j < d/2 (angles in float64).
+__global__ void k_rope_table(int N, int half, int d, double theta, float* __restrict__ cs) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= N * half) return;
+  const int t = i / half, j = i % half;
+  double sn, c;
+  sincos((double)t * pow(theta, -2.0 * (double)j / (double)d), &sn, &c);
+  cs[2 * (size_t)i] = (float)c;
+  cs[2 * (size_t)i + 1] = (float)sn;
+}
+
+// K~ rows of a RoPE model, in place: row m (token t = m mod N) of head h becomes
+// RoPE_t(K_h) A_h, rounded to fp16.  One CTA per (64 rows, head): A_h and the rotated rows in
+// shared memory (fp32), thread (j, r0) computes column j of rows r0, r0 + 2, ...; the column
+// sums of |K~| of the tile go to colpart[tile][h d + j] (two row halves added in order).
+constexpr int kRsRows = 64;
+template <int D>
+__global__ void __launch_bounds__(256) k_rope_skew(__half* __restrict__ K, int M, int N, int H,
+                                                  const float* __restrict__ A, const float* __restrict__ cs,
+                                                  float* __restrict__ colpart) {
+  extern __shared__ float smf[];
+  float* sA = smf;                 // [D][D]
+  float* sR = smf + D * D;         // [kRsRows][D]
+  float* sC = sR + kRsRows * D;    // [2][D]
+  const int h = blockIdx.y, m0 = blockIdx.x * kRsRows;
+  const int Hd = H * D, half = D / 2;
+  for (int i = threadIdx.x; i < D * D; i += 256) sA[i] = A[(size_t)h * D * D + i];
+  for (int i = threadIdx.x; i < kRsRows * half; i += 256) {
+    const int r = i / half, j = i % half, m = m0 + r;
+    float lo = 0.f, hi = 0.f, c = 1.f, sn = 0.f;
+    if (m < M) {
+      const int t = m % N;
+      lo = __half2float(K[(size_t)m * Hd + h * D + j]);
+      hi = __half2float(K[(size_t)m * Hd + h * D + j + half]);
+      c = cs[2 * ((size_t)t * half + j)];
+      sn = cs[2 * ((size_t)t * half + j) + 1];
+    }
+    sR[r * D + j] = lo * c - hi * sn;
+    sR[r * D + j + half] = lo * sn + hi * c;
+  }
+  __syncthreads();
+  constexpr int TPC = 256 / D;  // threads per column (2 for D = 128, 4 for D = 64)
+  const int j = threadIdx.x % D, r0 = threadIdx.x / D;
+  float csum = 0.f;
+  for (int r = r0; r < kRsRows; r += TPC) {
+    float acc = 0.f;
+#pragma unroll 8
+    for (int i = 0; i < D; ++i) acc = fmaf(sR[r * D + i], sA[i * D + j], acc);
+    const int m = m0 + r;
+    const __half o = __float2half_rn(acc);
+    if (m < M) {
+      K[(size_t)m * Hd + h * D + j] = o;
+      csum += fabsf(__half2float(o));
+    }
+  }
+  if (TPC == 2) {
+    sC[r0 * D + j] = csum;
+    __syncthreads();
+    if (r0 == 0) colpart[(size_t)blockIdx.x * Hd + h * D + j] = sC[j] + sC[D + j];
+  } else {
+    __shared__ float sc4[4][D];
+    sc4[r0][j] = csum;
+    __syncthreads();
+    if (r0 == 0) colpart[(size_t)blockIdx.x * Hd + h * D + j] = ((sc4[0][j] + sc4[1][j]) + sc4[2][j]) + sc4[3][j];
+  }
+}
+
+// A_cols[h][i][j] = A[h][i][cols[h][j]] (the decode stage's partial skew for RoPE models).
+__global__ void k_extract_acols(const float* __restrict__ A, int d, int k, const int32_t* __restrict__ cols,
+                                float* __restrict__ out, int* err) {
+  const int h = blockIdx.x;
+  for (int e = threadIdx.x; e < d * k; e += blockDim.x) {
+    const int i = e / k, j = e % k;
+    const int c = cols[h * k + j];
+    if (c < 0 || c >= d) {
+      raise_error(err, IG_DEVERR_INDEX);
+      continue;
+    }
+    out[((size_t)h * d + i) * k + j] = A[((size_t)h * d + i) * d + c];
+  }
+}
+
 }  // namespace
 }  // namespace ig
 
@@ -291,13 +374,15 @@ namespace {
 
 size_t rup(size_t x) { return round_up(x, 256); }
 
-// workspace: K~ [B N][H d] fp16, V [B N][H d] fp16, column partials [ceil(B N / 128)][H d] fp32
-void prefill_layout(int B, int N, int H, int d, size_t* off_v, size_t* off_cp, size_t* total) {
+// workspace: K~ [B N][H d] fp16, V [B N][H d] fp16, column partials [ceil(B N / 64)][H d] fp32
+// (128-row tiles use the first half), the RoPE cos/sin table [N][d/2][2] fp32
+void prefill_layout(int B, int N, int H, int d, size_t* off_v, size_t* off_cp, size_t* off_tab, size_t* total) {
   const size_t M = (size_t)B * N, Nn = (size_t)H * d;
-  const size_t mt = (M + kGM - 1) / kGM;
+  const size_t mt = (M + kRsRows - 1) / kRsRows;
   *off_v = rup(M * Nn * 2);
   *off_cp = *off_v + rup(M * Nn * 2);
-  *total = *off_cp + rup(mt * Nn * sizeof(float));
+  *off_tab = *off_cp + rup(mt * Nn * sizeof(float));
+  *total = *off_tab + rup((size_t)N * d * sizeof(float));
 }
 
 ig_status gemm(cudaStream_t st, const uint16_t* A, const uint16_t* Bt, uint16_t* C, int M, int N, int K,
@@ -330,8 +415,8 @@ extern "C" ig_status ig_gemm_tn(void* stream, int M, int N, int K, const uint16_
 
 extern "C" size_t ig_prefill_workspace_bytes(int B, int N, int H, int d) {
   if (B <= 0 || N <= 0 || H <= 0 || d <= 0) return 0;
-  size_t ov, oc, tot;
-  prefill_layout(B, N, H, d, &ov, &oc, &tot);
+  size_t ov, oc, ot, tot;
+  prefill_layout(B, N, H, d, &ov, &oc, &ot, &tot);
   return tot;
 }
 
@@ -351,8 +436,8 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   IG_REQUIRE(aligned(X, 16) && aligned(Wq_t, 16) && aligned(Wk_t, 16) && aligned(Wv_t, 16) &&
                  aligned(Wq_part_t, 16),
              "X and the weights must be 16-byte aligned");
-  size_t ov, oc, tot;
-  prefill_layout(B, N, H, d, &ov, &oc, &tot);
+  size_t ov, oc, ot, tot;
+  prefill_layout(B, N, H, d, &ov, &oc, &ot, &tot);
   if (!workspace || workspace_bytes < tot)
     return fail(IG_ERR_CAPACITY, "the prefill needs %zu workspace bytes", tot);
   IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
@@ -377,6 +462,75 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   k_extract_rows<<<H * k, 128, 0, st>>>(reinterpret_cast<const uint4*>(Wq_t), D, d, k, cols,
                                         reinterpret_cast<uint4*>(Wq_part_t), error_word());
   IG_CHECK_LAUNCH("partial weight launch");
+  const size_t le = (size_t)B * H * pool->cap * d;
+  dim3 sg((N + kScTok - 1) / kScTok, H, B);
+  k_prefill_scatter<<<sg, 256, kScTok * d * 2, st>>>(
+      reinterpret_cast<const __half*>(Kt), reinterpret_cast<const __half*>(Vt), N, H, d, k, pool->cap, Lcap, cols,
+      reinterpret_cast<uint4*>(pool->Kdev + (size_t)layer * le), reinterpret_cast<uint4*>(pool->Vdev + (size_t)layer * le),
+      reinterpret_cast<__half*>(Kpart), error_word());
+  IG_CHECK_LAUNCH("prefill scatter launch");
+  return IG_OK;
+}
+
+extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,
+                                           int d, int k, int Lcap, float rope_theta, const uint16_t* X,
+                                           const uint16_t* Wq_t, const uint16_t* Wk_t, const uint16_t* Wv_t,
+                                           const float* A, int32_t* cols, float* A_cols, uint16_t* Kpart,
+                                           void* workspace, size_t workspace_bytes) {
+  IG_REQUIRE(pool, "null pool");
+  IG_REQUIRE(pool->storage && !pool->fp8, "the prefill writes an fp16 pool with storage");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+  IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
+  IG_REQUIRE(N > 0 && D > 0 && D % 8 == 0, "N > 0 and D a positive multiple of 8");
+  IG_REQUIRE(d == 64 || d == 128, "d must be 64 or 128");
+  IG_REQUIRE(k > 0 && k <= d, "0 < k <= d");
+  IG_REQUIRE(rope_theta > 0.f, "rope_theta must be > 0");
+  IG_REQUIRE(Lcap >= pool->cap && Lcap % 8 == 0, "Lcap must cover the pool and be a multiple of 8");
+  IG_REQUIRE(X && Wq_t && Wk_t && Wv_t && A && cols && A_cols && Kpart, "null pointer argument");
+  IG_REQUIRE(aligned(X, 16) && aligned(Wq_t, 16) && aligned(Wk_t, 16) && aligned(Wv_t, 16),
+             "X and the weights must be 16-byte aligned");
+  size_t ov, oc, ot, tot;
+  prefill_layout(B, N, H, d, &ov, &oc, &ot, &tot);
+  if (!workspace || workspace_bytes < tot)
+    return fail(IG_ERR_CAPACITY, "the prefill needs %zu workspace bytes", tot);
+  IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
+  cudaStream_t st = as_stream(stream);
+  char* ws = static_cast<char*>(workspace);
+  uint16_t* Kt = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* Vt = reinterpret_cast<uint16_t*>(ws + ov);
+  float* colpart = reinterpret_cast<float*>(ws + oc);
+  float* tab = reinterpret_cast<float*>(ws + ot);
+  const int M = B * N, Nn = H * d;
+  IG_REQUIRE((M + kGM - 1) / kGM <= 65535, "B*N too large for one launch");
+  // Step 1: K = X W_K, rotated and skewed row by row (with the column partials), and V
+  ig_status r = gemm(st, X, Wk_t, Kt, M, Nn, D, nullptr);
+  if (r != IG_OK) return r;
+  const int half = d / 2;
+  k_rope_table<<<(N * half + 255) / 256, 256, 0, st>>>(N, half, d, (double)rope_theta, tab);
+  IG_CHECK_LAUNCH("RoPE table launch");
+  const int mt = (M + kRsRows - 1) / kRsRows;
+  const size_t smem = ((size_t)d * d + (size_t)kRsRows * d + 2 * d) * sizeof(float);
+  dim3 rg(mt, H);
+  cudaError_t e;
+  if (d == 128) {
+    e = cudaFuncSetAttribute(k_rope_skew<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "rope-skew smem attribute");
+    k_rope_skew<128><<<rg, 256, smem, st>>>(reinterpret_cast<__half*>(Kt), M, N, H, A, tab, colpart);
+  } else {
+    e = cudaFuncSetAttribute(k_rope_skew<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "rope-skew smem attribute");
+    k_rope_skew<64><<<rg, 256, smem, st>>>(reinterpret_cast<__half*>(Kt), M, N, H, A, tab, colpart);
+  }
+  IG_CHECK_LAUNCH("rope-skew launch");
+  r = gemm(st, X, Wv_t, Vt, M, Nn, D, nullptr);
+  if (r != IG_OK) return r;
+  // Step 2: the columns (W~_Q from Wq_t, the keys' partials over 64-row tiles)
+  k_choose_cols<<<H, d, d * sizeof(double), st>>>(reinterpret_cast<const __half*>(Wq_t), D, H, d, k, colpart, mt,
+                                                  cols, nullptr);
+  IG_CHECK_LAUNCH("column choice launch");
+  // Step 3: A[:, S], then the pool rows and the partial key cache
+  k_extract_acols<<<H, 256, 0, st>>>(A, d, k, cols, A_cols, error_word());
+  IG_CHECK_LAUNCH("partial skew launch");
   const size_t le = (size_t)B * H * pool->cap * d;
   dim3 sg((N + kScTok - 1) / kScTok, H, B);
   k_prefill_scatter<<<sg, 256, kScTok * d * 2, st>>>(

@@ -86,6 +86,8 @@ _sig("ig_eviction_misses", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_prefill_workspace_bytes", _sz, _i, _i, _i, _i)
 _sig("ig_prefill_layer", _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz)
 _sig("ig_gemm_tn", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp)
+_sig("ig_prefill_layer_rope", _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+     _vp, _vp, _sz)
 _sig("ig_attention_recall", _i, _vp, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_captured_fraction", _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_pool_destroy", _i, _vp)
@@ -304,6 +306,13 @@ def ig_prefill_layer(stream, pool, layer, B, N, D, H, d, k, Lcap, X, Wq_t, Wk_t,
     _ok(_lib.ig_prefill_layer(_s(stream), pool, layer, B, N, D, H, d, k, Lcap, _p(X), _p(Wq_t), _p(Wk_t), _p(Wv_t),
                               _p(cols), _p(Wq_part_t), _p(Kpart), _p(workspace), workspace_bytes),
         "ig_prefill_layer")
+
+
+def ig_prefill_layer_rope(stream, pool, layer, B, N, D, H, d, k, Lcap, rope_theta, X, Wq_t, Wk_t, Wv_t, A, cols,
+                          A_cols, Kpart, workspace, workspace_bytes):
+    _ok(_lib.ig_prefill_layer_rope(_s(stream), pool, layer, B, N, D, H, d, k, Lcap, rope_theta, _p(X), _p(Wq_t),
+                                   _p(Wk_t), _p(Wv_t), _p(A), _p(cols), _p(A_cols), _p(Kpart), _p(workspace),
+                                   workspace_bytes), "ig_prefill_layer_rope")
 
 
 def ig_gemm_tn(stream, M, N, K, A, Bt, C, colpart=None):

@@ -34,6 +34,23 @@ def prefill_decoder_layer(dec, l: int, X, Wq_t, Wk_t, Wv_t, workspace=None):
     return workspace
 
 
+def prefill_decoder_layer_rope(dec, l: int, X, Wq_skew_t, Wk_t, Wv_t, A, workspace=None):
+    """As :func:`prefill_decoder_layer` for a RoPE decoder: W~_Q^T (skewed, column score only),
+    W_K^T and W_V^T (unskewed) [H*d, D] fp16 and the skew A [H, d, d] fp32, all on the device."""
+    B, N, D = X.shape
+    if workspace is None:
+        workspace = torch.empty(ig.ig_prefill_workspace_bytes(B, N, dec.H, dec.d), dtype=torch.uint8,
+                                device=X.device)
+    dec.S.wait_stream(torch.cuda.current_stream(X.device))
+    with torch.cuda.stream(dec.S):
+        dec.Kpart[l].zero_()
+        ig.ig_prefill_layer_rope(dec.S, dec.pool, l, B, N, D, dec.H, dec.d, dec.ks[l], dec.Lcap, dec.cfg.rope_theta,
+                                 X, Wq_skew_t, Wk_t, Wv_t, A, dec.cols[l], dec.A_cols[l], dec.Kpart[l], workspace,
+                                 workspace.numel())
+    dec.S.synchronize()
+    return workspace
+
+
 def time_layer(w: synth.Workload, reps: int = 3, device: str = "cuda:0") -> dict:
     """Device time of one layer's prefill at the workload's shape, and of its parts."""
     dev = torch.device(device)

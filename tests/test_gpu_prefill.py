@@ -163,3 +163,113 @@ def test_decoder_built_by_the_library_prefill(ig):
             assert cnt[l].sum() > 0
     finally:
         dec.close()
+
+
+@pytest.mark.parametrize("d,cap", [(128, 320), (64, 250)])
+def test_prefill_layer_rope_matches_oracle(ig, d, cap):
+    """RoPE prefill: keys within one fp16 ulp plus the fp32 bound of the oracle's RoPE_t(X W_K) A,
+    columns as the oracle's (but near ties), A_cols exactly A[:, cols], pool rows and partial
+    keys exactly the kernel's own keys at the oracle's slots."""
+    B, N, D, H, k, theta = 2, 300, 512, 4, 38 if d == 128 else 16, 10000.0
+    Lcap = (cap + 7) // 8 * 8
+    g = np.random.default_rng(7 + d)
+    X = g.standard_normal((B, N, D)).astype(np.float16)
+    Wq, Wk, Wv = ((g.standard_normal((D, H * d)) * 0.02 * (1 + np.arange(H * d) % 5)).astype(np.float16)
+                  for _ in range(3))
+    A = np.stack([np.linalg.qr(g.standard_normal((d, d)))[0] for _ in range(H)])
+    Wq_s = np.zeros_like(Wq)
+    for h in range(H):
+        Wq_s[:, h * d:(h + 1) * d] = (Wq[:, h * d:(h + 1) * d].astype(np.float64) @ A[h]).astype(np.float16)
+    pool = ig.ig_pool_create(1, B, H, d, cap)
+    try:
+        cols = empty((H, k), torch.int32)
+        Ac = empty((H, d, k), torch.float32)
+        Kpart = torch.zeros((B, H, k, Lcap), dtype=torch.float16, device="cuda")
+        ws = workspace(ig.ig_prefill_workspace_bytes(B, N, H, d))
+        t = lambda a: dev(np.ascontiguousarray(a.T))  # noqa: E731
+        ig.ig_prefill_layer_rope(None, pool, 0, B, N, D, H, d, k, Lcap, theta, dev(X), t(Wq_s), t(Wk), t(Wv),
+                                 dev(A.astype(np.float32)), cols, Ac, Kpart, ws, ws.numel())
+        ig.ig_check()
+        o = ora.prefill_layer_rope(X, Wq_s, Wk, Wv, A.astype(np.float32).astype(np.float64), theta, H, d, k, cap)
+        Kg = host(ws[: B * N * H * d * 2].view(torch.float16)).reshape(B, N, H, d).astype(np.float64)
+        Kw = o["K"].astype(np.float64)
+        # the unskewed key is rounded to fp16 on both sides, then rotated and skewed; the
+        # projection's fp32 accumulation can move that rounding by an ulp, which the skew spreads
+        X64 = np.abs(X.astype(np.float64))
+        pre = D * 2.0 ** -23 * (X64 @ np.abs(Wk.astype(np.float64))).reshape(B, N, H, d)
+        Kraw = (X.astype(np.float64) @ Wk.astype(np.float64)).reshape(B, N, H, d)
+        braw = _ulp16(Kraw) + pre
+        brot = braw + np.roll(braw, d // 2, axis=-1)  # a rotation mixes each pair (j, j + d/2)
+        spread = np.einsum("bnhi,hij->bnhj", brot, np.abs(A))
+        assert np.all(np.abs(Kg - Kw) <= _ulp16(Kw) + spread + 1e-6 * np.abs(Kw).max())
+        got_cols = host(cols)
+        sc = ora.colscores(Wq_s, o["K"], H, d)
+        for h in range(H):
+            s_sorted = np.sort(sc[h])[::-1]
+            near = s_sorted[k - 1] - s_sorted[k] <= 1e-3 * s_sorted[k - 1]
+            assert np.array_equal(got_cols[h], o["cols"][h]) or near, h
+            assert np.array_equal(host(Ac)[h], A[h].astype(np.float32)[:, got_cols[h]])
+        Kp, _ = ig.pool_layer_view(pool, 0, B, H, cap, d)
+        kp = host(Kpart)
+        for tt in range(max(0, N - cap), N):
+            assert np.array_equal(Kp[:, :, tt % cap].astype(np.float64), Kg[:, tt])
+            for h in range(H):
+                assert np.array_equal(kp[:, h, :, tt % cap].astype(np.float64), Kg[:, tt, h][:, got_cols[h]])
+    finally:
+        ig.ig_pool_destroy(pool)
+
+
+def test_rope_decoder_built_by_the_library_prefill(ig):
+    """A RoPE decoder whose layers >= 1 are filled by ig_prefill_layer_rope, then one decode
+    step against the oracle's attention over its own prefilled rows, on the GPU's index sets."""
+    import math
+
+    from speculative_kv_cache_gb300 import decoder, prefill
+
+    L, B, H, d, D, N, k, theta = 3, 2, 4, 128, 512, 200, 38, 10000.0
+    cap = Lcap = N + 8
+    g = np.random.default_rng(9)
+    dec = decoder.Decoder(layers=L, B=B, H=H, d=d, D=D, k=k, Lcap=Lcap, pool_cap=cap, alpha=4.0, rope_theta=theta,
+                          device="cuda:0")
+    try:
+        orc = {}
+        for l in range(L):
+            X = g.standard_normal((B, N, D)).astype(np.float16)
+            Wq, Wk, Wv = ((g.standard_normal((D, H * d)) * 0.05 * (1 + np.arange(H * d) % 5)).astype(np.float16)
+                          for _ in range(3))
+            A = np.stack([np.linalg.qr(g.standard_normal((d, d)))[0] for _ in range(H)]).astype(np.float32)
+            Wq_s = np.concatenate([(Wq[:, h * d:(h + 1) * d].astype(np.float64) @ A[h]).astype(np.float16)
+                                   for h in range(H)], axis=1)
+            o = ora.prefill_layer_rope(X, Wq_s, Wk, Wv, A.astype(np.float64), theta, H, d, k, cap)
+            orc[l] = (o, Wq, A)
+            if l == 0:
+                Kb = np.zeros((B, H, cap, d), np.float16)
+                Vb = np.zeros_like(Kb)
+                Kb[:, :, :N] = o["K"].transpose(0, 2, 1, 3)
+                Vb[:, :, :N] = o["V"].transpose(0, 2, 1, 3)
+                dec.load_layer(0, dev(Kb), dev(Vb), o["cols"], Wq=dev(Wq), A_cols=dev(o["A_cols"].astype(np.float32)))
+            else:
+                t = lambda a: dev(np.ascontiguousarray(a.T))  # noqa: E731
+                dec.Wq[l].copy_(dev(Wq).t())  # the decode stage projects with the unskewed W_Q
+                prefill.prefill_decoder_layer_rope(dec, l, dev(X), t(Wq_s), t(Wk), t(Wv), dev(A))
+        dec.prefill(N)
+        x = g.standard_normal((L, B, D)).astype(np.float16)
+        q, kn, vn = (g.standard_normal((L, B, H, d)).astype(np.float16) for _ in range(3))
+        out = torch.empty((L, B, H, d), dtype=torch.float32, device="cuda")
+        dec.step(dev(x), dev(q), dev(kn), dev(vn), out, positions=np.full(B, N, np.int32))
+        dec.finish()
+        ig.ig_check(dec.S)
+        o_gpu, cnt, idx_buf = host(out), host(dec.cnt), host(dec.idx)
+        scale = np.float32(1.0 / math.sqrt(d))
+        for l in range(1, L):
+            gi = idx_buf[l % 2]
+            sets = [[gi[b, h, :cnt[l, b, h]] for h in range(H)] for b in range(B)]
+            o = orc[l][0]
+            Kg, Vg = ora.gather(o["K_pool"], o["V_pool"], sets, Lcap)
+            want = ora.attend(q[l], Kg, Vg, cnt[l], scale, kn[l], vn[l])
+            # the oracle attends over its own keys, which differ from the kernels' by the
+            # projection's rounding twice over (before and after the rotation): a relative term
+            assert np.abs(o_gpu[l] - want).max() <= 2e-3 + 5e-4 * np.abs(want).max()
+            assert cnt[l].sum() > 0
+    finally:
+        dec.close()
