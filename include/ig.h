@@ -345,6 +345,21 @@ ig_status ig_gather_attend(void* stream, const ig_pool* pool, int layer, int B, 
                            const int32_t* cnt, const uint16_t* k_new, const uint16_t* v_new,
                            float* out, void* workspace, size_t workspace_bytes, int max_ctas);
 
+/* The appends of every layer's current token in one launch (the same rows as ig_append_kv
+ * called per layer), for a step whose fetches are done.  Layer 0 goes to Kdense/Vdense when
+ * they are given (an HBM-resident layer 0), else to the pool like the others.
+ *   ks      host int [layers]: partial width of each layer (0 where Kpart[l] is NULL)
+ *   slot    dev int32 [layers][B]: slot per (layer, sequence); negative: skip
+ *   cols    host array [layers] of dev int32 [H][ks[l]] (entries may be NULL with Kpart[l])
+ *   k_new, v_new  dev fp16 [layers][B][H][d]
+ *   Kpart   host array [layers] of dev fp16 [B][H][ks[l]][Lcap] or NULL entries; may be NULL
+ * At most 128 layers per call; fp8 pools quantize the rows as ig_append_kv does. */
+ig_status ig_append_kv_layers(void* stream, ig_pool* pool, int layers, int B, int H, int d,
+                              const int* ks, int Lcap, const int32_t* slot,
+                              const int32_t* const* cols, const uint16_t* k_new,
+                              const uint16_t* v_new, uint16_t* const* Kpart, uint16_t* Kdense,
+                              uint16_t* Vdense);
+
 /* ------------------------------------------------------------------------------------
  * Append of the current token.  Section 3.4, "Partial Key Cache Updates During Decoding":
  * the new token's full key and value go to the host pool, its k chosen columns to the
@@ -385,6 +400,9 @@ typedef struct {
   int fused_fetch;     /* 1: layers 1.. attend straight from the pool on the fetch stream
                           (ig_gather_attend), no staging in HBM, Kg/Vg unused (may be NULL);
                           0: gather into Kg/Vg on the fetch stream, attend on the compute stream */
+  int batched_append;  /* 1: every layer's new token is appended in one launch at the end of the
+                          step (ig_append_kv_layers), after the fetches; 0: each layer's append
+                          follows its attention */
 } ig_decoder_config;
 
 typedef struct {

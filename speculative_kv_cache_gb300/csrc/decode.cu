@@ -219,7 +219,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
                            io->k_new + (size_t)l * ts, io->v_new + (size_t)l * ts,
                            io->out + (size_t)l * ts, ws, spec_att_ws);
     }
-    if (r != IG_OK || !slot) return r;
+    if (r != IG_OK || !slot || c.batched_append) return r;
     if (l == 0)
       return ig_append_kv(S, nullptr, 0, B, H, d, ks[0], Lc, slot, dec->cols[0], io->k_new, io->v_new,
                           dec->Kpart[0], b.K0, b.V0);
@@ -288,7 +288,19 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     return se == cudaSuccess ? IG_OK : cuda_fail(se, "decode step events (select)");
   };
 
-  if (L == 1) return timed_attend(0);
+  // with batched appends, every layer's token is written in one launch once the step's fetches
+  // are done (the fetch stream has joined): the pool rows it may overwrite have been read, and
+  // the link carries no fetch while the appends cross it
+  auto batched_tail = [&]() -> ig_status {
+    if (!c.batched_append || !io->slot) return IG_OK;
+    return ig_append_kv_layers(S, dec->pool, L, B, H, d, ks.data(), Lc, io->slot, dec->cols.data(), io->k_new,
+                               io->v_new, dec->Kpart.data(), b.K0, b.V0);
+  };
+
+  if (L == 1) {
+    st = timed_attend(0);
+    return st != IG_OK ? st : batched_tail();
+  }
   if (c.fused_fetch) {
     // append(l) on S once the fetch stream's attention(l) has read the pool (the new token may
     // overwrite an evicted slot) and speculation(l) has read the partial cache
@@ -296,7 +308,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
       cudaError_t ae = cudaStreamWaitEvent(S, dec->ev_att[l], 0);
       if (ae == cudaSuccess) ae = rec(dec->ta0, l, S);
       if (ae != cudaSuccess) return cuda_fail(ae, "decode step wait");
-      if (io->slot) {
+      if (io->slot && !c.batched_append) {
         const size_t off = (size_t)l * ts;
         ig_status r = ig_append_kv(S, dec->pool, l, B, H, d, ks[l], Lc, io->slot + (size_t)l * B, dec->cols[l],
                                    io->k_new + off, io->v_new + off, dec->Kpart[l], nullptr, nullptr);
@@ -334,7 +346,8 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     }
     e = cudaEventRecord(dec->ev_join, G);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(S, dec->ev_join, 0);
-    return e == cudaSuccess ? IG_OK : cuda_fail(e, "decode step join");
+    if (e != cudaSuccess) return cuda_fail(e, "decode step join");
+    return batched_tail();
   }
   for (int l = 1; l < L; ++l) {
     st = spec_select(l);
@@ -371,7 +384,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
   e = cudaEventRecord(dec->ev_join, G);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(S, dec->ev_join, 0);
   if (e != cudaSuccess) return cuda_fail(e, "decode step join");
-  return IG_OK;
+  return batched_tail();
 }
 
 extern "C" ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float* ms_out,

@@ -113,6 +113,19 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
+// Sum of S (<= 32) split partials p[0], p[stride], ... added in that order (the same fp32 sum
+// as a plain loop): every load is issued before the first add, so the loads overlap.
+__device__ __forceinline__ float sum_splits(const float* __restrict__ p, size_t stride, int S) {
+  float v[32];
+#pragma unroll
+  for (int s = 0; s < 32; ++s) v[s] = s < S ? __ldg(p + (size_t)s * stride) : 0.f;
+  float a = 0.f;
+#pragma unroll
+  for (int s = 0; s < 32; ++s)
+    if (s < S) a += v[s];
+  return a;
+}
+
 __device__ __forceinline__ float2 h2_to_f2(uint32_t v) {
   __half2 h = *reinterpret_cast<__half2*>(&v);
   return __half22float2(h);

@@ -127,6 +127,74 @@ __global__ void k6_append_fp8(uint8_t* __restrict__ K8, uint8_t* __restrict__ V8
   quantize_row<PER>(v_new + (size_t)bh * D, V8 + row * D, Vs + row);
 }
 
+// Appends of every layer's current token in one launch (grid: (b, h) x layer), run once the
+// step's fetches are done: layer 0 to the dense rows when given, other layers to the pool
+// (Q = 0: fp16 rows by 16-byte copies; Q = 2 or 4: fp8 rows quantized by the first two warps),
+// and each layer's chosen columns to its partial key cache.
+constexpr int kMaxAppendLayers = 128;
+struct AppendLayers {
+  __half* Kpart[kMaxAppendLayers];
+  const int32_t* cols[kMaxAppendLayers];
+  int k[kMaxAppendLayers];
+};
+
+template <int Q>
+__global__ void __launch_bounds__(64) k6_append_layers(
+    const AppendLayers P, uint4* __restrict__ Kp, uint4* __restrict__ Vp, uint8_t* __restrict__ K8,
+    uint8_t* __restrict__ V8, float* __restrict__ Ks, float* __restrict__ Vs, int cap, int H, int d, int Lcap,
+    int units, const int32_t* __restrict__ slot, const __half* __restrict__ k_new,
+    const __half* __restrict__ v_new, uint4* __restrict__ Kd, uint4* __restrict__ Vd, int* err) {
+  const int bh = blockIdx.x, l = blockIdx.y, b = bh / H, h = bh % H;
+  const int sl = slot[l * (units / H) + b];
+  if (sl < 0) return;
+  const __half* kn = k_new + ((size_t)l * units + bh) * d;
+  const __half* vn = v_new + ((size_t)l * units + bh) * d;
+  const int vpr = d / 8;
+  if (l == 0 && Kd) {
+    if (sl >= Lcap) {
+      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_INDEX);
+      return;
+    }
+    for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
+      Kd[((size_t)bh * Lcap + sl) * vpr + v] = reinterpret_cast<const uint4*>(kn)[v];
+      Vd[((size_t)bh * Lcap + sl) * vpr + v] = reinterpret_cast<const uint4*>(vn)[v];
+    }
+  } else {
+    if (sl >= cap) {
+      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_INDEX);
+      return;
+    }
+    const size_t row = ((size_t)l * units + bh) * cap + sl;
+    if (Q == 0) {
+      for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
+        Kp[row * vpr + v] = reinterpret_cast<const uint4*>(kn)[v];
+        Vp[row * vpr + v] = reinterpret_cast<const uint4*>(vn)[v];
+      }
+    } else {
+      constexpr int PER = Q > 0 ? Q : 1;
+      if (threadIdx.x < 32) quantize_row<PER>(kn, K8 + row * d, Ks + row);
+      else quantize_row<PER>(vn, V8 + row * d, Vs + row);
+    }
+  }
+  __half* kp = P.Kpart[l];
+  if (kp) {
+    if (sl >= Lcap) {
+      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_INDEX);
+      return;
+    }
+    const int k = P.k[l];
+    const int32_t* cl = P.cols[l];
+    for (int c = threadIdx.x; c < k; c += blockDim.x) {
+      const int col = cl[h * k + c];
+      if (col < 0 || col >= d) {
+        raise_error(err, IG_DEVERR_INDEX);
+        continue;
+      }
+      kp[((size_t)bh * k + c) * Lcap + sl] = kn[col];
+    }
+  }
+}
+
 }  // namespace
 }  // namespace ig
 
@@ -343,5 +411,46 @@ extern "C" ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B,
       reinterpret_cast<const __half*>(v_new), reinterpret_cast<__half*>(Kpart),
       reinterpret_cast<uint4*>(Kdense), reinterpret_cast<uint4*>(Vdense), error_word());
   IG_CHECK_LAUNCH("append launch");
+  return IG_OK;
+}
+
+extern "C" ig_status ig_append_kv_layers(void* stream, ig_pool* pool, int layers, int B, int H, int d,
+                                         const int* ks, int Lcap, const int32_t* slot,
+                                         const int32_t* const* cols, const uint16_t* k_new,
+                                         const uint16_t* v_new, uint16_t* const* Kpart, uint16_t* Kdense,
+                                         uint16_t* Vdense) {
+  IG_REQUIRE(pool && pool->storage, "a pool with storage is needed");
+  IG_REQUIRE(layers >= 1 && layers <= pool->layers && layers <= kMaxAppendLayers, "bad layer count %d", layers);
+  IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
+  IG_REQUIRE(Lcap > 0 && slot && k_new && v_new, "bad Lcap or null pointer");
+  IG_REQUIRE((Kdense == nullptr) == (Vdense == nullptr), "Kdense and Vdense go together");
+  IG_REQUIRE(aligned(k_new, 16) && aligned(v_new, 16), "k_new, v_new must be 16-byte aligned");
+  IG_REQUIRE(!Kdense || (aligned(Kdense, 16) && aligned(Vdense, 16)), "dense rows must be 16-byte aligned");
+  AppendLayers P{};
+  for (int l = 0; l < layers; ++l) {
+    P.Kpart[l] = Kpart ? reinterpret_cast<__half*>(Kpart[l]) : nullptr;
+    P.cols[l] = cols ? cols[l] : nullptr;
+    P.k[l] = ks ? ks[l] : 0;
+    IG_REQUIRE(!P.Kpart[l] || (P.cols[l] && P.k[l] > 0 && P.k[l] <= d), "layer %d: Kpart needs cols and 0 < k <= d", l);
+  }
+  const int units = B * H;
+  dim3 grid(units, layers);
+  cudaStream_t st = as_stream(stream);
+  auto kn = reinterpret_cast<const __half*>(k_new);
+  auto vn = reinterpret_cast<const __half*>(v_new);
+  auto Kd = reinterpret_cast<uint4*>(Kdense);
+  auto Vd = reinterpret_cast<uint4*>(Vdense);
+  if (!pool->fp8) {
+    k6_append_layers<0><<<grid, 64, 0, st>>>(P, reinterpret_cast<uint4*>(pool->Kdev), reinterpret_cast<uint4*>(pool->Vdev),
+                                            nullptr, nullptr, nullptr, nullptr, pool->cap, H, d, Lcap, units, slot, kn, vn,
+                                            Kd, Vd, error_word());
+  } else if (d == 128) {
+    k6_append_layers<4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->K8, pool->V8, pool->Ks, pool->Vs, pool->cap, H,
+                                            d, Lcap, units, slot, kn, vn, Kd, Vd, error_word());
+  } else {
+    k6_append_layers<2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->K8, pool->V8, pool->Ks, pool->Vs, pool->cap, H,
+                                            d, Lcap, units, slot, kn, vn, Kd, Vd, error_word());
+  }
+  IG_CHECK_LAUNCH("batched append launch");
   return IG_OK;
 }

@@ -67,8 +67,7 @@ __global__ void __launch_bounds__(kFThreads) k23_score_select(
   }
   for (int c = threadIdx.x; c < k; c += blockDim.x) {
     const int N = H * k;
-    float a = 0.f;
-    for (int s = 0; s < S; ++s) a += qsrc[((size_t)s * B + b) * N + h * k + c];
+    const float a = sum_splits(qsrc + (size_t)b * N + h * k + c, (size_t)B * N, S);
     qs[c] = a * scale;
     if (q_out && rank == 0) q_out[(size_t)bh * k + c] = a;
   }

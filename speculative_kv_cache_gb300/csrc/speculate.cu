@@ -45,9 +45,7 @@ __global__ void k1b_rope_project(const float* __restrict__ part, int S, int B, i
   const int bh = blockIdx.x, b = bh / H, h = bh % H;
   const int N = H * d;
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
-    float a = 0.f;
-    for (int s = 0; s < S; ++s) a += part[((size_t)s * B + b) * N + h * d + j];
-    q[j] = a;
+    q[j] = sum_splits(part + (size_t)b * N + h * d + j, (size_t)B * N, S);
   }
   const float* Ah = A_cols + (size_t)h * d * k;
   for (int i = threadIdx.x; i < d * k; i += blockDim.x) As[i] = Ah[i];
@@ -103,8 +101,7 @@ __global__ void k2_scores(const float* __restrict__ qsrc, int S, int B, int H, i
   }
   for (int c = threadIdx.x; c < k; c += blockDim.x) {
     const int N = H * k;
-    float a = 0.f;
-    for (int s = 0; s < S; ++s) a += qsrc[((size_t)s * B + b) * N + h * k + c];
+    const float a = sum_splits(qsrc + (size_t)b * N + h * k + c, (size_t)B * N, S);
     qs[c] = a * scale;
     if (q_out && blockIdx.x == 0) q_out[(size_t)bh * k + c] = a;
   }

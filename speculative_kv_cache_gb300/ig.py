@@ -82,6 +82,7 @@ _sig("ig_pool_create_ex", _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_slot_tokens", _i, _vp, _i, _i, _vp)
 _sig("ig_pool_kv8", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp))
 _sig("ig_pool_evictions", _i, _vp, _i, _i, C.POINTER(C.c_int64))
+_sig("ig_append_kv_layers", _i, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_eviction_misses", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_prefill_workspace_bytes", _sz, _i, _i, _i, _i)
 _sig("ig_prefill_layer", _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz)
@@ -369,6 +370,18 @@ def ig_append_kv(stream, pool, layer, B, H, d, k, Lcap, slot, cols, k_new, v_new
                           _p(v_new), _p(Kpart), _p(Kdense), _p(Vdense)), "ig_append_kv")
 
 
+def ig_append_kv_layers(stream, pool, layers, B, H, d, ks, Lcap, slot, cols, k_new, v_new, Kpart, Kdense=None,
+                        Vdense=None):
+    """ks: list of ints; cols, Kpart: lists of device tensors (or None entries)."""
+    ks_a = (C.c_int * layers)(*[int(x) for x in ks])
+    cols_a = _ptr_array(cols)
+    kp_a = _ptr_array(Kpart) if Kpart is not None else None
+    _ok(_lib.ig_append_kv_layers(_s(stream), pool, layers, B, H, d, C.cast(ks_a, _vp), Lcap, _p(slot),
+                                 C.cast(cols_a, _vp), _p(k_new), _p(v_new),
+                                 C.cast(kp_a, _vp) if kp_a is not None else None, _p(Kdense), _p(Vdense)),
+        "ig_append_kv_layers")
+
+
 def pool_layer_view(pool, layer, B, H, cap, d):
     """NumPy views (fp16) of one layer's K and V in the pinned pool: [B, H, cap, d] each."""
     kp, vp = ig_pool_kv(pool, layer)
@@ -385,7 +398,7 @@ class DecoderConfig(C.Structure):
     _fields_ = [("layers", _i), ("B", _i), ("H", _i), ("d", _i), ("D", _i), ("k", _i), ("Lcap", _i),
                 ("policy", _i), ("alpha", _f), ("cap_frac", _f), ("score_scale", _f),
                 ("rope_theta", _f), ("gather_ctas", _i), ("stage_timing", _i), ("fused_select", _i),
-                ("fused_fetch", _i)]
+                ("fused_fetch", _i), ("batched_append", _i)]
 
 
 class DecoderBuffers(C.Structure):
