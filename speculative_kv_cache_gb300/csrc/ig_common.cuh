@@ -113,16 +113,18 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
-// Sum of S (<= 32) split partials p[0], p[stride], ... added in that order (the same fp32 sum
-// as a plain loop): every load is issued before the first add, so the loads overlap.
+// Sum of S split partials p[0], p[stride], ... added in that order (the same fp32 sum as a
+// plain loop): the loads are issued 8 at a time before their adds, so they overlap.
 __device__ __forceinline__ float sum_splits(const float* __restrict__ p, size_t stride, int S) {
-  float v[32];
-#pragma unroll
-  for (int s = 0; s < 32; ++s) v[s] = s < S ? __ldg(p + (size_t)s * stride) : 0.f;
   float a = 0.f;
+  for (int s0 = 0; s0 < S; s0 += 8) {
+    float v[8];
 #pragma unroll
-  for (int s = 0; s < 32; ++s)
-    if (s < S) a += v[s];
+    for (int i = 0; i < 8; ++i) v[i] = s0 + i < S ? __ldg(p + (size_t)(s0 + i) * stride) : 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (s0 + i < S) a += v[i];
+  }
   return a;
 }
 
