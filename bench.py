@@ -53,6 +53,8 @@ def parse_args(argv=None):
                    help="victim policy of a capacity-limited pool (workloads with pool_frac < 1)")
     p.add_argument("--batched-append", type=int, default=0,
                    help="1: all layers' new tokens appended in one launch after the step's fetches")
+    p.add_argument("--append-on-fetch", type=int, default=0,
+                   help="1: each layer's append runs on the fetch stream right after its gather")
     p.add_argument("--pool-fp8", type=int, default=0,
                    help="1: the host pool holds e4m3 rows with a per-row scale (d + 4 bytes per row)")
     p.add_argument("--fused-fetch", type=int, default=0,
@@ -253,7 +255,8 @@ def link_peak_gbs(torch) -> float:
 
 
 def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True,
-                  fused_fetch=False, pool_policy=0, policy=0, pool_fp8=False, batched_append=False):
+                  fused_fetch=False, pool_policy=0, policy=0, pool_fp8=False, batched_append=False,
+                  append_on_fetch=False):
     from speculative_kv_cache_gb300.decoder import Decoder
 
     Lcap = w.lcap
@@ -261,7 +264,8 @@ def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False
                   pool_cap=w.pool_cap, alpha=alpha, rope_theta=w.rope_theta, gather_ctas=gather_ctas,
                   stage_timing=True, graph=bool(graph), fused_select=bool(fused_select),
                   fused_fetch=bool(fused_fetch), pool_policy=pool_policy, policy=policy,
-                  pool_fp8=bool(pool_fp8), batched_append=bool(batched_append), device=device)
+                  pool_fp8=bool(pool_fp8), batched_append=bool(batched_append),
+                  append_on_fetch=bool(append_on_fetch), device=device)
     gen = torch.Generator(device=device)
     shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
@@ -365,7 +369,7 @@ def run_ours(args, w, alpha):
               "normalized": ig.IG_SEL_NORMALIZED}[args.policy]
     dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph,
                                           args.fused_select, fused_fetch, pool_policy, policy, args.pool_fp8,
-                                          args.batched_append)
+                                          args.batched_append, args.append_on_fetch)
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
@@ -465,7 +469,8 @@ def run_ours(args, w, alpha):
             "dtype": "fp16 storage, fp32 accumulate", "data": "synthetic (seeded, random-init weights)",
             "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph),
                            fused_select=bool(args.fused_select), fused_fetch=fused_fetch,
-                           selection=args.policy, batched_append=bool(args.batched_append), pool_dtype="fp8-e4m3 + fp32 row scale" if args.pool_fp8 else "fp16",
+                           selection=args.policy, batched_append=bool(args.batched_append),
+                           append_on_fetch=bool(args.append_on_fetch), pool_dtype="fp8-e4m3 + fp32 row scale" if args.pool_fp8 else "fp16",
                            pool_policy=args.pool_policy if w.pool_frac < 1 else None),
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "selected_fraction": float(f),

@@ -403,6 +403,9 @@ typedef struct {
   int batched_append;  /* 1: every layer's new token is appended in one launch at the end of the
                           step (ig_append_kv_layers), after the fetches; 0: each layer's append
                           follows its attention */
+  int append_on_fetch; /* staged fetch, batched_append = 0: 1: layer l >= 1's append runs on the
+                          fetch stream right after its gather (spares the compute stream where
+                          that is the critical path); 0: on the compute stream after attention */
 } ig_decoder_config;
 
 typedef struct {

@@ -219,7 +219,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
                            io->k_new + (size_t)l * ts, io->v_new + (size_t)l * ts,
                            io->out + (size_t)l * ts, ws, spec_att_ws);
     }
-    if (r != IG_OK || !slot || c.batched_append) return r;
+    if (r != IG_OK || !slot || c.batched_append || (l > 0 && c.append_on_fetch)) return r;
     if (l == 0)
       return ig_append_kv(S, nullptr, 0, B, H, d, ks[0], Lc, slot, dec->cols[0], io->k_new, io->v_new,
                           dec->Kpart[0], b.K0, b.V0);
@@ -364,6 +364,13 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     e = rec(dec->tg1, l, G);
     if (e == cudaSuccess) e = cudaEventRecord(dec->ev_got[l], G);
     if (e != cudaSuccess) return cuda_fail(e, "decode step events (gather)");
+    if (c.append_on_fetch && !c.batched_append && io->slot) {
+      // the fetch stream writes layer l's new token right after reading layer l's rows: no fetch
+      // of its own is in flight then, and the compute stream is spared the host stores
+      st = ig_append_kv(G, dec->pool, l, B, H, d, ks[l], Lc, io->slot + (size_t)l * B, dec->cols[l],
+                        io->k_new + (size_t)l * ts, io->v_new + (size_t)l * ts, dec->Kpart[l], nullptr, nullptr);
+      if (st != IG_OK) return st;
+    }
     // layer l-1 attends while layer l is fetched (layer 0 needs no fetch)
     if (l >= 2) {
       e = cudaStreamWaitEvent(S, dec->ev_got[l - 1], 0);

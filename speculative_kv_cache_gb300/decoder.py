@@ -25,7 +25,7 @@ class Decoder:
     def __init__(self, *, layers, B, H, d, D, k, Lcap, pool_cap, alpha, policy=ig.IG_SEL_THRESHOLD,
                  cap_frac=1.0, score_scale=None, rope_theta=0.0, gather_ctas=0, stage_timing=False,
                  graph=False, fused_select=True, fused_fetch=False, pool_policy=ig.IG_POOL_COUNTER,
-                 pool_fp8=False, batched_append=False, device="cuda:0"):
+                 pool_fp8=False, batched_append=False, append_on_fetch=False, device="cuda:0"):
         if pool_cap > Lcap or Lcap % 8:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
         if pool_fp8 and fused_fetch:
@@ -49,7 +49,8 @@ class Decoder:
         self.cfg = ig.DecoderConfig(layers, B, H, d, D, k, Lcap, policy, float(alpha), float(cap_frac),
                                     float(score_scale if score_scale is not None else 1.0 / math.sqrt(d)),
                                     float(rope_theta), int(gather_ctas), int(bool(stage_timing)),
-                                    int(bool(fused_select)), int(bool(fused_fetch)), int(bool(batched_append)))
+                                    int(bool(fused_select)), int(bool(fused_fetch)), int(bool(batched_append)),
+                                    int(bool(append_on_fetch)))
         # per-layer state: partial query weight (or full W_Q and A[:, S] for RoPE), columns,
         # partial key cache; layer 0 keeps its full KV in HBM instead
         self.Wq_part = [None] + [e(H * ks[l], D) for l in range(1, layers)] if not self.rope else None

@@ -398,7 +398,7 @@ class DecoderConfig(C.Structure):
     _fields_ = [("layers", _i), ("B", _i), ("H", _i), ("d", _i), ("D", _i), ("k", _i), ("Lcap", _i),
                 ("policy", _i), ("alpha", _f), ("cap_frac", _f), ("score_scale", _f),
                 ("rope_theta", _f), ("gather_ctas", _i), ("stage_timing", _i), ("fused_select", _i),
-                ("fused_fetch", _i), ("batched_append", _i)]
+                ("fused_fetch", _i), ("batched_append", _i), ("append_on_fetch", _i)]
 
 
 class DecoderBuffers(C.Structure):

@@ -47,7 +47,7 @@ def _layer_data(w, l, cap, rope, ratio=None):
 
 
 def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True, fused_fetch=False, graph=False,
-         ratios=None, batched_append=False):
+         ratios=None, batched_append=False, append_on_fetch=False):
     ig, decoder = mods
     dev = "cuda:0"
     Lcap = w.lcap
@@ -58,7 +58,7 @@ def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True, fused
     dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=ks if ratios else w.k,
                           Lcap=Lcap, pool_cap=cap, alpha=alpha, rope_theta=w.rope_theta,
                           fused_select=fused_select, fused_fetch=fused_fetch, graph=graph,
-                          batched_append=batched_append, device=dev)
+                          batched_append=batched_append, append_on_fetch=append_on_fetch, device=dev)
     try:
         data = [_layer_data(w, l, cap, rope, ratios[l] if ratios else None) for l in range(w.layers)]
         for l, dd in enumerate(data):
@@ -159,12 +159,13 @@ def test_decoder_opt_shaped_steps(mods, fused, fetch):
 
 
 @pytest.mark.parametrize("fetch", ["staged", "fused"])
-@pytest.mark.parametrize("batched", [True, False])
-def test_decoder_capped_pool_evicts_like_the_oracle(mods, fetch, batched):
+@pytest.mark.parametrize("append", ["per-layer", "batched", "on-fetch"])
+def test_decoder_capped_pool_evicts_like_the_oracle(mods, fetch, append):
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-cap", layers=3, batch=2, heads=4, hidden=512,
                      prompt=200, gen=10, pool_frac=0.95)
     assert w.pool_cap < w.prompt + 10
-    _run(mods, w, steps=8, check_slots=True, fused_fetch=fetch == "fused", batched_append=batched)
+    _run(mods, w, steps=8, check_slots=True, fused_fetch=fetch == "fused", batched_append=append == "batched",
+         append_on_fetch=append == "on-fetch")
 
 
 @pytest.mark.parametrize("fetch", ["staged", "fused"])
