@@ -120,9 +120,12 @@ def time_gemm(n: int = 8192, reps: int = 5, device: str = "cuda:0") -> dict:
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--workload", default="opt-30b")
+    p.add_argument("--gemm-only", action="store_true", help="time the n^3 GEMM alone")
+    p.add_argument("--n", type=int, default=8192)
     a = p.parse_args(argv)
-    print(json.dumps(time_gemm()), flush=True)
-    print(json.dumps(time_layer(synth.WORKLOADS[a.workload])), flush=True)
+    print(json.dumps(time_gemm(a.n)), flush=True)
+    if not a.gemm_only:
+        print(json.dumps(time_layer(synth.WORKLOADS[a.workload])), flush=True)
 
 
 if __name__ == "__main__":
