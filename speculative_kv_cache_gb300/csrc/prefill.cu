@@ -17,6 +17,8 @@
 // column score is deterministic.
 #include <cuda.h>
 
+#include <mutex>
+
 #include "ig_common.cuh"
 #include "pool_impl.h"
 #include "tc_common.cuh"
@@ -32,6 +34,7 @@ constexpr int kGThreads = 128;
 constexpr uint32_t kGStageA = kGM * kGK * 2;  // 16 KB
 constexpr uint32_t kGStageB = kGN * kGK * 2;  // 32 KB
 constexpr uint32_t kGTmemCols = 256;
+constexpr int kGGroup = 16;     // row tiles per group of the tile order
 // kind::f16, D fp32, A/B fp16 K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28
 constexpr uint32_t kGIdesc = (1u << 4) | ((uint32_t)(kGN >> 3) << 17) | ((uint32_t)(kGM >> 4) << 24);
 
@@ -55,7 +58,15 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant_
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   float* csum = reinterpret_cast<float*>(abort_flag + 3);  // [4][kGN] (scalar accesses only)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kGN, m0 = blockIdx.y * kGM;
+  // grouped tile order: runs of kGGroup row tiles take each column tile in turn, so a B tile is
+  // reused by consecutive CTAs and the group's A tiles stay in L2 while the group sweeps N
+  const int tiles_n = (N + kGN - 1) / kGN, tiles_m = (M + kGM - 1) / kGM;
+  const int per_group = kGGroup * tiles_n;
+  const int gi = (int)blockIdx.x / per_group, within = (int)blockIdx.x % per_group;
+  const int first_m = gi * kGGroup;
+  const int gsize = min(tiles_m - first_m, kGGroup);
+  const int mt = first_m + within % gsize, ntile = within / gsize;
+  const int n0 = ntile * kGN, m0 = mt * kGM;
   const int nk = (K + kGK - 1) / kGK;
 
   if (threadIdx.x == 0) {
@@ -187,7 +198,7 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant_
   if (landed && colpart) {
     for (int c = threadIdx.x; c < kGN; c += kGThreads) {
       if (n0 + c >= N) continue;
-      colpart[(size_t)blockIdx.y * N + n0 + c] = ((csum[c] + csum[kGN + c]) + csum[2 * kGN + c]) + csum[3 * kGN + c];
+      colpart[(size_t)mt * N + n0 + c] = ((csum[c] + csum[kGN + c]) + csum[2 * kGN + c]) + csum[3 * kGN + c];
     }
   }
   tc_fence_before();
@@ -245,14 +256,34 @@ __global__ void k_extract_rows(const uint4* __restrict__ Wq_t, int D, int d, int
   for (int i = threadIdx.x; i < v16; i += blockDim.x) out[(size_t)hk * v16 + i] = src[i];
 }
 
-// Step 1 (store) and 3b: for (b, h) and a tile of 64 prompt tokens, the rows of the tokens the
-// pool keeps (t >= N - cap) go to slot t mod cap of the pinned pool (16-byte zero-copy stores)
-// and their chosen columns to the partial key cache.
+// Step 1 (store): rows of the tokens the pool keeps (t >= N - cap) to slot t mod cap of the
+// pinned pool, 16-byte zero-copy stores; src [B][N][H][d], one warp per (b, t, h) row.  It needs
+// no shared memory, so it runs beside the projection GEMM (on a side stream).
+__global__ void __launch_bounds__(256) k_pool_rows(const uint4* __restrict__ src, int B, int N, int H, int d, int cap,
+                                                  uint4* __restrict__ pool) {
+  const int vpr = d / 8;
+  const int first = N > cap ? N - cap : 0;
+  const long long keep = (long long)B * (N - first) * H;
+  const long long w0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const long long nw = (long long)gridDim.x * blockDim.x / 32;
+  const int lane = threadIdx.x & 31;
+  for (long long r = w0; r < keep; r += nw) {
+    const int h = (int)(r % H);
+    const long long bt = r / H;
+    const int t = first + (int)(bt % (N - first));
+    const int b = (int)(bt / (N - first));
+    const uint4* s = src + (((size_t)b * N + t) * H + h) * vpr;
+    uint4* dst = pool + (((size_t)b * H + h) * cap + t % cap) * vpr;
+    for (int v = lane; v < vpr; v += 32) dst[v] = s[v];
+  }
+}
+
+// Step 3b: for (b, h) and a tile of 64 prompt tokens, the chosen columns of the keys the pool
+// keeps go to the partial key cache at their slots (rows staged in shared memory, coalesced
+// writes along the token axis).
 constexpr int kScTok = 64;
-__global__ void k_prefill_scatter(const __half* __restrict__ Kt, const __half* __restrict__ Vt, int N, int H,
-                                  int d, int k, int cap, int Lcap, const int32_t* __restrict__ cols,
-                                  uint4* __restrict__ Kp, uint4* __restrict__ Vp, __half* __restrict__ Kpart,
-                                  int* err) {
+__global__ void k_partial_keys(const __half* __restrict__ Kt, int N, int H, int d, int k, int cap, int Lcap,
+                               const int32_t* __restrict__ cols, __half* __restrict__ Kpart, int* err) {
   extern __shared__ __align__(16) unsigned char sraw[];
   __half* sk = reinterpret_cast<__half*>(sraw);  // [kScTok][d]
   const int t0 = blockIdx.x * kScTok, h = blockIdx.y, b = blockIdx.z;
@@ -261,14 +292,9 @@ __global__ void k_prefill_scatter(const __half* __restrict__ Kt, const __half* _
   const size_t bh = (size_t)b * H + h;
   for (int i = threadIdx.x; i < kScTok * vpr; i += blockDim.x) {
     const int tt = i / vpr, v = i % vpr, t = t0 + tt;
-    if (t >= N) continue;
+    if (t >= N || t < first) continue;
     const size_t src = ((size_t)b * N + t) * H * d + (size_t)h * d;  // halves
-    const uint4 kv = *reinterpret_cast<const uint4*>(Kt + src + v * 8);
-    reinterpret_cast<uint4*>(sk)[tt * vpr + v] = kv;
-    if (t < first) continue;
-    const int slot = t % cap;
-    Kp[(bh * cap + slot) * vpr + v] = kv;
-    Vp[(bh * cap + slot) * vpr + v] = *reinterpret_cast<const uint4*>(Vt + src + v * 8);
+    reinterpret_cast<uint4*>(sk)[tt * vpr + v] = *reinterpret_cast<const uint4*>(Kt + src + v * 8);
   }
   __syncthreads();
   for (int i = threadIdx.x; i < k * kScTok; i += blockDim.x) {
@@ -374,6 +400,51 @@ namespace {
 
 size_t rup(size_t x) { return round_up(x, 256); }
 
+// The side stream and events that let the pool writes run beside the projections (one set per
+// device, created on first use; the enqueue sequence of a call is serialised by a mutex).
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+};
+std::mutex g_side_mu;
+SideStream g_side[64];
+
+ig_status side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "current device");
+  if (dev < 0 || dev >= 64) return fail(IG_ERR_INVALID, "device %d out of range", dev);
+  SideStream& ss = g_side[dev];
+  if (!ss.s) {
+    int lo = 0, hi = 0;
+    e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&ss.s, cudaStreamNonBlocking, hi);
+    for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventCreateWithFlags(&ss.ev[i], cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill side stream");
+  }
+  *out = &ss;
+  return IG_OK;
+}
+
+// Writes the kept rows of src to the pool on the side stream once `st`'s work so far is done.
+ig_status fork_pool_rows(cudaStream_t st, SideStream* ss, int which, const uint16_t* src, int B, int N, int H,
+                         int d, int cap, uint16_t* pool) {
+  cudaError_t e = cudaEventRecord(ss->ev[which], st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->s, ss->ev[which], 0);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill fork");
+  k_pool_rows<<<2 * sm_count(), 256, 0, ss->s>>>(reinterpret_cast<const uint4*>(src), B, N, H, d, cap,
+                                                 reinterpret_cast<uint4*>(pool));
+  IG_CHECK_LAUNCH("pool rows launch");
+  return IG_OK;
+}
+
+// `st` continues after everything the side stream was given.
+ig_status join_side(cudaStream_t st, SideStream* ss) {
+  cudaError_t e = cudaEventRecord(ss->ev[2], ss->s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->ev[2], 0);
+  return e == cudaSuccess ? IG_OK : cuda_fail(e, "prefill join");
+}
+
 // workspace: K~ [B N][H d] fp16, V [B N][H d] fp16, column partials [ceil(B N / 64)][H d] fp32
 // (128-row tiles use the first half), the RoPE cos/sin table [N][d/2][2] fp32
 void prefill_layout(int B, int N, int H, int d, size_t* off_v, size_t* off_cp, size_t* off_tab, size_t* total) {
@@ -395,8 +466,9 @@ ig_status gemm(cudaStream_t st, const uint16_t* A, const uint16_t* Bt, uint16_t*
   const size_t smem = gemm_smem_bytes();
   cudaError_t e = cudaFuncSetAttribute(k_gemm_tn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return cuda_fail(e, "prefill GEMM smem attribute");
-  dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-  k_gemm_tn<<<grid, kGThreads, smem, st>>>(ma, mb, reinterpret_cast<__half*>(C), M, N, K, colpart, error_word());
+  const long long tiles = (long long)((N + kGN - 1) / kGN) * ((M + kGM - 1) / kGM);
+  IG_REQUIRE(tiles < (1ll << 31), "GEMM too large for one launch");
+  k_gemm_tn<<<(unsigned)tiles, kGThreads, smem, st>>>(ma, mb, reinterpret_cast<__half*>(C), M, N, K, colpart, error_word());
   IG_CHECK_LAUNCH("prefill GEMM launch");
   return IG_OK;
 }
@@ -449,27 +521,34 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   const int M = B * N, Nn = H * d;
   const int mtiles = (M + kGM - 1) / kGM;
   IG_REQUIRE(mtiles <= 65535, "B*N too large for one launch");
-  // Step 1: K~ (with the per-tile column partials of |K~|) and V
-  ig_status r = gemm(st, X, Wk_t, Kt, M, Nn, D, colpart);
+  SideStream* ss = nullptr;
+  ig_status r = side_stream(&ss);
+  if (r != IG_OK) return r;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  const size_t le = (size_t)B * H * pool->cap * d;
+  // Step 1: K~ (with the per-tile column partials of |K~|); its pool rows go out on the side
+  // stream while V is projected, then V's while the columns are chosen
+  r = gemm(st, X, Wk_t, Kt, M, Nn, D, colpart);
+  if (r != IG_OK) return r;
+  r = fork_pool_rows(st, ss, 0, Kt, B, N, H, d, pool->cap, pool->Kdev + (size_t)layer * le);
   if (r != IG_OK) return r;
   r = gemm(st, X, Wv_t, Vt, M, Nn, D, nullptr);
+  if (r != IG_OK) return r;
+  r = fork_pool_rows(st, ss, 1, Vt, B, N, H, d, pool->cap, pool->Vdev + (size_t)layer * le);
   if (r != IG_OK) return r;
   // Step 2: the columns
   k_choose_cols<<<H, d, d * sizeof(double), st>>>(reinterpret_cast<const __half*>(Wq_t), D, H, d, k, colpart, mtiles,
                                                   cols, nullptr);
   IG_CHECK_LAUNCH("column choice launch");
-  // Step 3: the partial weight, then the pool rows and the partial key cache
+  // Step 3: the partial weight and the partial key cache; then wait for the pool rows
   k_extract_rows<<<H * k, 128, 0, st>>>(reinterpret_cast<const uint4*>(Wq_t), D, d, k, cols,
                                         reinterpret_cast<uint4*>(Wq_part_t), error_word());
   IG_CHECK_LAUNCH("partial weight launch");
-  const size_t le = (size_t)B * H * pool->cap * d;
   dim3 sg((N + kScTok - 1) / kScTok, H, B);
-  k_prefill_scatter<<<sg, 256, kScTok * d * 2, st>>>(
-      reinterpret_cast<const __half*>(Kt), reinterpret_cast<const __half*>(Vt), N, H, d, k, pool->cap, Lcap, cols,
-      reinterpret_cast<uint4*>(pool->Kdev + (size_t)layer * le), reinterpret_cast<uint4*>(pool->Vdev + (size_t)layer * le),
-      reinterpret_cast<__half*>(Kpart), error_word());
-  IG_CHECK_LAUNCH("prefill scatter launch");
-  return IG_OK;
+  k_partial_keys<<<sg, 256, kScTok * d * 2, st>>>(reinterpret_cast<const __half*>(Kt), N, H, d, k, pool->cap, Lcap,
+                                                 cols, reinterpret_cast<__half*>(Kpart), error_word());
+  IG_CHECK_LAUNCH("partial keys launch");
+  return join_side(st, ss);
 }
 
 extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,
@@ -502,8 +581,14 @@ extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int laye
   float* tab = reinterpret_cast<float*>(ws + ot);
   const int M = B * N, Nn = H * d;
   IG_REQUIRE((M + kGM - 1) / kGM <= 65535, "B*N too large for one launch");
-  // Step 1: K = X W_K, rotated and skewed row by row (with the column partials), and V
-  ig_status r = gemm(st, X, Wk_t, Kt, M, Nn, D, nullptr);
+  SideStream* ss = nullptr;
+  ig_status r = side_stream(&ss);
+  if (r != IG_OK) return r;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  const size_t le = (size_t)B * H * pool->cap * d;
+  // Step 1: K = X W_K, rotated and skewed row by row (with the column partials); its pool rows
+  // go out on the side stream while V is projected
+  r = gemm(st, X, Wk_t, Kt, M, Nn, D, nullptr);
   if (r != IG_OK) return r;
   const int half = d / 2;
   k_rope_table<<<(N * half + 255) / 256, 256, 0, st>>>(N, half, d, (double)rope_theta, tab);
@@ -522,21 +607,22 @@ extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int laye
     k_rope_skew<64><<<rg, 256, smem, st>>>(reinterpret_cast<__half*>(Kt), M, N, H, A, tab, colpart);
   }
   IG_CHECK_LAUNCH("rope-skew launch");
+  r = fork_pool_rows(st, ss, 0, Kt, B, N, H, d, pool->cap, pool->Kdev + (size_t)layer * le);
+  if (r != IG_OK) return r;
   r = gemm(st, X, Wv_t, Vt, M, Nn, D, nullptr);
+  if (r != IG_OK) return r;
+  r = fork_pool_rows(st, ss, 1, Vt, B, N, H, d, pool->cap, pool->Vdev + (size_t)layer * le);
   if (r != IG_OK) return r;
   // Step 2: the columns (W~_Q from Wq_t, the keys' partials over 64-row tiles)
   k_choose_cols<<<H, d, d * sizeof(double), st>>>(reinterpret_cast<const __half*>(Wq_t), D, H, d, k, colpart, mt,
                                                   cols, nullptr);
   IG_CHECK_LAUNCH("column choice launch");
-  // Step 3: A[:, S], then the pool rows and the partial key cache
+  // Step 3: A[:, S] and the partial key cache; then wait for the pool rows
   k_extract_acols<<<H, 256, 0, st>>>(A, d, k, cols, A_cols, error_word());
   IG_CHECK_LAUNCH("partial skew launch");
-  const size_t le = (size_t)B * H * pool->cap * d;
   dim3 sg((N + kScTok - 1) / kScTok, H, B);
-  k_prefill_scatter<<<sg, 256, kScTok * d * 2, st>>>(
-      reinterpret_cast<const __half*>(Kt), reinterpret_cast<const __half*>(Vt), N, H, d, k, pool->cap, Lcap, cols,
-      reinterpret_cast<uint4*>(pool->Kdev + (size_t)layer * le), reinterpret_cast<uint4*>(pool->Vdev + (size_t)layer * le),
-      reinterpret_cast<__half*>(Kpart), error_word());
-  IG_CHECK_LAUNCH("prefill scatter launch");
-  return IG_OK;
+  k_partial_keys<<<sg, 256, kScTok * d * 2, st>>>(reinterpret_cast<const __half*>(Kt), N, H, d, k, pool->cap, Lcap,
+                                                 cols, reinterpret_cast<__half*>(Kpart), error_word());
+  IG_CHECK_LAUNCH("partial keys launch");
+  return join_side(st, ss);
 }
