@@ -227,14 +227,15 @@ typedef struct ig_pool ig_pool;
  * rows (ig_pool_kv, ig_pool_write, ig_gather_kv, ig_gather_attend, ig_append_kv with this
  * pool) then return IG_ERR_INVALID. */
 #define IG_POOL_NO_STORAGE 1
-/* IG_POOL_FP8: rows stored as e4m3 codes [layers][B][H][cap][d] with one fp32 scale per row
- * [layers][B][H][cap] (the combination of a quantized pool with selective prefetch proposed as
- * follow-up work).  Each row is quantized on its way in (ig_pool_write, ig_append_kv): scale =
- * amax / 448, codes = round-to-nearest-even e4m3 of x * (448 / amax) in fp32, saturating; a row
- * of zeros has scale 0.  ig_gather_kv dequantizes (code value x scale, rounded to fp16) into the
- * usual fp16 staging rows, so the link carries d + 4 bytes per row instead of 2d; the partial key
- * cache (speculation) stays fp16.  d must be 64 or 128; ig_pool_kv and ig_gather_attend refuse
- * fp8 pools (use ig_pool_kv8). */
+/* IG_POOL_FP8: each (token, head) row stored as one record of 2d + 16 bytes: the key's d e4m3
+ * codes, the value's d codes, the key's and the value's fp32 scale, 8 bytes of padding (the
+ * combination of a quantized pool with selective prefetch proposed as follow-up work).  Each
+ * row is quantized on its way in (ig_pool_write, ig_append_kv): scale = amax / 448, codes =
+ * round-to-nearest-even e4m3 of x * (448 / amax) in fp32, saturating; a row of zeros has scale
+ * 0.  ig_gather_kv reads one contiguous record per selected row and dequantizes it (code value x
+ * scale, rounded to fp16) into the usual fp16 staging rows, so the link carries 2d + 16 bytes
+ * per row instead of 4d; the partial key cache (speculation) stays fp16.  d must be 64 or 128;
+ * ig_pool_kv and ig_gather_attend refuse fp8 pools (use ig_pool_kv8). */
 #define IG_POOL_FP8 2
 
 ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out);
@@ -247,10 +248,9 @@ ig_status ig_pool_destroy(ig_pool* pool);
 /* Host pointers (also valid on the device) to one layer's K and V arrays. */
 ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V);
 
-/* fp8 pools: host pointers (also valid on the device) to one layer's codes
- * ([B][H][cap][d] uint8) and row scales ([B][H][cap] fp32). */
-ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** K8, uint8_t** V8, float** Ks,
-                      float** Vs);
+/* fp8 pools: host pointer (also valid on the device) to one layer's records
+ * [B][H][cap][record_bytes] (layout under IG_POOL_FP8) and the record size (2d + 16). */
+ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** records, int* record_bytes);
 
 /* Copies one layer's K and V ([B][H][cap][d] fp16 each, from device or host memory) into
  * the pool, asynchronously on `stream`.  An fp8 pool quantizes them in a kernel, so for it the

@@ -21,6 +21,7 @@ namespace {
 
 constexpr int kGatherThreads = 256;
 constexpr int kUnroll = 8;  // 8 rows x (K, V) in flight per lane: 205 GB/s alone at 38 CTAs
+constexpr int kUnroll8 = 16;  // fp8 records: one 16-byte load per lane and row, so twice the rows
 constexpr int kMaxGatherUnits = 32768;  // (units + 1) ints of shared memory: 128 KB
 
 __global__ void __launch_bounds__(kGatherThreads) k4_gather(
@@ -116,12 +117,13 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather(
   }
 }
 
-// FP8 pool (rows of e4m3 codes + one fp32 scale): the same balanced row split; 16 codes per
-// lane (d/16 lanes per row, so a 128-wide row is 128 B + 4 B over the link instead of 256 B),
-// dequantized to fp16 (code value x scale, rounded to nearest) into the same staging layout.
+// FP8 pool (one record per (token, head): K codes, V codes, their two fp32 scales): the same
+// balanced row split; a row is one contiguous record of 2d + 16 bytes, read by 2d/16 lanes (16
+// codes each: the first d/16 lanes the key, the rest the value) plus each lane's 4-byte scale
+// from the same record, and dequantized to fp16 (code value x scale, rounded to nearest) into
+// the usual staging layout.
 __global__ void __launch_bounds__(kGatherThreads) k4_gather_fp8(
-    const uint4* __restrict__ K8, const uint4* __restrict__ V8, const float* __restrict__ Ks,
-    const float* __restrict__ Vs, int units, int cap, int vpr, int Lcap, const int32_t* __restrict__ idx,
+    const uint8_t* __restrict__ Rec, int rec, int units, int cap, int vpr, int Lcap, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ cnt, uint4* __restrict__ Kg, uint4* __restrict__ Vg, int* err) {
   extern __shared__ int pre[];
   __shared__ int wsum[kGatherThreads / 32];
@@ -167,12 +169,16 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather_fp8(
     }
     u = lo;
   }
-  for (int r = r0 + rg; r < r1; r += rpp * kUnroll) {
-    uint4 kv[kUnroll], vv[kUnroll];
-    float ks[kUnroll], vs[kUnroll];
-    int unit[kUnroll], row[kUnroll], slot[kUnroll];
+  const int half = vpr / 2;            // lanes of the key codes
+  const bool is_v = v >= half;
+  const int cv = is_v ? v - half : v;   // chunk of 16 codes within K or V
+  uint4* out = is_v ? Vg : Kg;
+  for (int r = r0 + rg; r < r1; r += rpp * kUnroll8) {
+    uint4 cd[kUnroll8];
+    float sc[kUnroll8];
+    int unit[kUnroll8], row[kUnroll8], slot[kUnroll8];
 #pragma unroll
-    for (int q = 0; q < kUnroll; ++q) {
+    for (int q = 0; q < kUnroll8; ++q) {
       const int rr = r + q * rpp;
       slot[q] = -1;
       unit[q] = 0;
@@ -187,38 +193,31 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather_fp8(
       }
     }
 #pragma unroll
-    for (int q = 0; q < kUnroll; ++q) {
+    for (int q = 0; q < kUnroll8; ++q) {
       if (slot[q] >= 0) {
-        const size_t rowi = (size_t)unit[q] * cap + slot[q];
-        kv[q] = ld_nc_v4(K8 + rowi * vpr + v);
-        vv[q] = ld_nc_v4(V8 + rowi * vpr + v);
-        ks[q] = __ldg(Ks + rowi);
-        vs[q] = __ldg(Vs + rowi);
+        const uint8_t* rp = Rec + ((size_t)unit[q] * cap + slot[q]) * rec;
+        cd[q] = ld_nc_v4(rp + (size_t)v * 16);
+        sc[q] = __ldg(reinterpret_cast<const float*>(rp + 2 * 16 * half) + (is_v ? 1 : 0));
       }
     }
 #pragma unroll
-    for (int q = 0; q < kUnroll; ++q) {
+    for (int q = 0; q < kUnroll8; ++q) {
       if (slot[q] < 0) continue;
-      const size_t dst = ((size_t)unit[q] * Lcap + row[q]) * (2 * vpr) + 2 * v;
-      for (int kvsel = 0; kvsel < 2; ++kvsel) {
-        const uint4 c = kvsel ? vv[q] : kv[q];
-        const float sc = kvsel ? vs[q] : ks[q];
-        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-        uint32_t o[8];
+      const size_t dst = ((size_t)unit[q] * Lcap + row[q]) * (2 * half) + 2 * cv;
+      const uint32_t w4[4] = {cd[q].x, cd[q].y, cd[q].z, cd[q].w};
+      uint32_t o[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          // two codes at a time: exact fp16 values of the codes, then x scale in fp32
-          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] & 0xffffu), __NV_E4M3);
-          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] >> 16), __NV_E4M3);
-          const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
-          const __half2 ra = __floats2half2_rn(a.x * sc, a.y * sc), rb = __floats2half2_rn(b.x * sc, b.y * sc);
-          o[2 * i] = *reinterpret_cast<const uint32_t*>(&ra);
-          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&rb);
-        }
-        uint4* out = kvsel ? Vg : Kg;
-        out[dst] = make_uint4(o[0], o[1], o[2], o[3]);
-        out[dst + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+      for (int i = 0; i < 4; ++i) {
+        // two codes at a time: exact fp16 values of the codes, then x scale in fp32
+        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] & 0xffffu), __NV_E4M3);
+        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] >> 16), __NV_E4M3);
+        const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+        const __half2 ra = __floats2half2_rn(a.x * sc[q], a.y * sc[q]), rb = __floats2half2_rn(b.x * sc[q], b.y * sc[q]);
+        o[2 * i] = *reinterpret_cast<const uint32_t*>(&ra);
+        o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&rb);
       }
+      out[dst] = make_uint4(o[0], o[1], o[2], o[3]);
+      out[dst + 1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
   }
 }
@@ -253,15 +252,14 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
     if (e != cudaSuccess) return cuda_fail(e, "gather smem attribute");
   }
   if (pool->fp8) {
-    const int vpr8 = d / 16;  // lanes per fp8 row (16 codes each)
+    const int vpr8 = 2 * d / 16;  // lanes per fp8 record (16 codes each: K, then V)
     if (smem > 48 * 1024) {
       cudaError_t e = cudaFuncSetAttribute(k4_gather_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return cuda_fail(e, "gather smem attribute");
     }
     const size_t rows = (size_t)B * H * pool->cap, r0 = (size_t)layer * rows;
     k4_gather_fp8<<<grid, kGatherThreads, smem, as_stream(stream)>>>(
-        reinterpret_cast<const uint4*>(pool->K8 + r0 * d), reinterpret_cast<const uint4*>(pool->V8 + r0 * d),
-        pool->Ks + r0, pool->Vs + r0, units, pool->cap, vpr8, Lcap, idx, cnt, reinterpret_cast<uint4*>(Kg),
+        pool->R + r0 * pool->rec, pool->rec, units, pool->cap, vpr8, Lcap, idx, cnt, reinterpret_cast<uint4*>(Kg),
         reinterpret_cast<uint4*>(Vg), error_word());
     IG_CHECK_LAUNCH("fp8 gather launch");
     return IG_OK;

@@ -96,23 +96,26 @@ __device__ void quantize_row(const __half* __restrict__ x, uint8_t* __restrict__
   if (lane == 0) *scale = amax > 0.f ? amax / 448.f : 0.f;
 }
 
-// Pool write of an fp8 pool: rows [rows][d] fp16 (device-accessible) -> codes + scales.
+// Pool write of an fp8 pool: rows [rows][d] fp16 (device-accessible) -> records (K and V codes,
+// then their scales).
 template <int PER>
 __global__ void k_quantize_rows(const __half* __restrict__ K, const __half* __restrict__ V, size_t rows,
-                                uint8_t* __restrict__ K8, uint8_t* __restrict__ V8, float* __restrict__ Ks,
-                                float* __restrict__ Vs) {
+                                uint8_t* __restrict__ R, int rec) {
   constexpr int D = 32 * PER;
   const size_t r = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (r >= rows) return;
-  quantize_row<PER>(K + r * D, K8 + r * D, Ks + r);
-  quantize_row<PER>(V + r * D, V8 + r * D, Vs + r);
+  uint8_t* rr = R + r * rec;
+  float* sc = reinterpret_cast<float*>(rr + 2 * D);
+  quantize_row<PER>(K + r * D, rr, sc);
+  quantize_row<PER>(V + r * D, rr + D, sc + 1);
 }
 
-// Append into an fp8 pool: one warp per (b, h) quantizes the current token's key and value.
+// Append into an fp8 pool: one warp per (b, h) quantizes the current token's key and value into
+// its record.
 template <int PER>
-__global__ void k6_append_fp8(uint8_t* __restrict__ K8, uint8_t* __restrict__ V8, float* __restrict__ Ks,
-                              float* __restrict__ Vs, int units, int cap, int H, const int32_t* __restrict__ slot,
-                              const __half* __restrict__ k_new, const __half* __restrict__ v_new, int* err) {
+__global__ void k6_append_fp8(uint8_t* __restrict__ R, int rec, int units, int cap, int H,
+                              const int32_t* __restrict__ slot, const __half* __restrict__ k_new,
+                              const __half* __restrict__ v_new, int* err) {
   constexpr int D = 32 * PER;
   const int bh = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (bh >= units) return;
@@ -122,9 +125,10 @@ __global__ void k6_append_fp8(uint8_t* __restrict__ K8, uint8_t* __restrict__ V8
     if ((threadIdx.x & 31) == 0) raise_error(err, IG_DEVERR_INDEX);
     return;
   }
-  const size_t row = (size_t)bh * cap + sl;
-  quantize_row<PER>(k_new + (size_t)bh * D, K8 + row * D, Ks + row);
-  quantize_row<PER>(v_new + (size_t)bh * D, V8 + row * D, Vs + row);
+  uint8_t* rr = R + ((size_t)bh * cap + sl) * rec;
+  float* sc = reinterpret_cast<float*>(rr + 2 * D);
+  quantize_row<PER>(k_new + (size_t)bh * D, rr, sc);
+  quantize_row<PER>(v_new + (size_t)bh * D, rr + D, sc + 1);
 }
 
 // Appends of every layer's current token in one launch (grid: (b, h) x layer), run once the
@@ -140,8 +144,8 @@ struct AppendLayers {
 
 template <int Q>
 __global__ void __launch_bounds__(64) k6_append_layers(
-    const AppendLayers P, uint4* __restrict__ Kp, uint4* __restrict__ Vp, uint8_t* __restrict__ K8,
-    uint8_t* __restrict__ V8, float* __restrict__ Ks, float* __restrict__ Vs, int cap, int H, int d, int Lcap,
+    const AppendLayers P, uint4* __restrict__ Kp, uint4* __restrict__ Vp, uint8_t* __restrict__ R, int rec,
+    int cap, int H, int d, int Lcap,
     int units, const int32_t* __restrict__ slot, const __half* __restrict__ k_new,
     const __half* __restrict__ v_new, uint4* __restrict__ Kd, uint4* __restrict__ Vd, int* err) {
   const int bh = blockIdx.x, l = blockIdx.y, b = bh / H, h = bh % H;
@@ -172,8 +176,10 @@ __global__ void __launch_bounds__(64) k6_append_layers(
       }
     } else {
       constexpr int PER = Q > 0 ? Q : 1;
-      if (threadIdx.x < 32) quantize_row<PER>(kn, K8 + row * d, Ks + row);
-      else quantize_row<PER>(vn, V8 + row * d, Vs + row);
+      uint8_t* rr = R + row * rec;
+      float* sc = reinterpret_cast<float*>(rr + 2 * d);
+      if (threadIdx.x < 32) quantize_row<PER>(kn, rr, sc);
+      else quantize_row<PER>(vn, rr + d, sc + 1);
     }
   }
   __half* kp = P.Kpart[l];
@@ -233,17 +239,13 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
     cudaError_t e;
     if (fp8) {
       p->fp8 = true;
-      e = alloc(reinterpret_cast<void**>(&p->K8), elems);
-      if (e == cudaSuccess) e = alloc(reinterpret_cast<void**>(&p->V8), elems);
-      if (e == cudaSuccess) e = alloc(reinterpret_cast<void**>(&p->Ks), nrows * sizeof(float));
-      if (e == cudaSuccess) e = alloc(reinterpret_cast<void**>(&p->Vs), nrows * sizeof(float));
+      p->rec = 2 * d + 16;
+      e = alloc(reinterpret_cast<void**>(&p->R), nrows * (size_t)p->rec);
       if (e != cudaSuccess) {
         cudaGetLastError();
-        for (void* q : {(void*)p->K8, (void*)p->V8, (void*)p->Ks, (void*)p->Vs})
-          if (q) cudaFreeHost(q);
         delete p;
-        return fail(IG_ERR_OOM, "pinned allocation of the fp8 pool (2 x %zu + 2 x %zu bytes) failed: %s", elems,
-                    nrows * sizeof(float), cudaGetErrorString(e));
+        return fail(IG_ERR_OOM, "pinned allocation of the fp8 pool (%zu bytes) failed: %s", nrows * (size_t)p->rec,
+                    cudaGetErrorString(e));
       }
     } else {
       e = alloc(reinterpret_cast<void**>(&p->K), elems * 2);
@@ -279,7 +281,7 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
     p->clock.assign(npb, 0);
     p->evictions.assign(npb, 0);
   } catch (...) {
-    for (void* q : {(void*)p->K, (void*)p->V, (void*)p->K8, (void*)p->V8, (void*)p->Ks, (void*)p->Vs})
+    for (void* q : {(void*)p->K, (void*)p->V, (void*)p->R})
       if (q) cudaFreeHost(q);
     delete p;
     return fail(IG_ERR_OOM, "host allocation of the pool manager failed");
@@ -295,7 +297,7 @@ extern "C" ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig
 extern "C" ig_status ig_pool_destroy(ig_pool* pool) {
   if (!pool) return IG_OK;
   cudaError_t first = cudaSuccess;
-  for (void* q : {(void*)pool->K, (void*)pool->V, (void*)pool->K8, (void*)pool->V8, (void*)pool->Ks, (void*)pool->Vs}) {
+  for (void* q : {(void*)pool->K, (void*)pool->V, (void*)pool->R}) {
     if (!q) continue;
     const cudaError_t e = cudaFreeHost(q);
     if (first == cudaSuccess) first = e;
@@ -316,16 +318,13 @@ extern "C" ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, ui
   return IG_OK;
 }
 
-extern "C" ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** K8, uint8_t** V8, float** Ks,
-                                 float** Vs) {
-  IG_REQUIRE(pool && K8 && V8 && Ks && Vs, "null argument");
+extern "C" ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** records, int* record_bytes) {
+  IG_REQUIRE(pool && records && record_bytes, "null argument");
   IG_REQUIRE(pool->fp8, "not an fp8 pool");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t rows = (size_t)pool->B * pool->H * pool->cap;
-  *K8 = pool->K8 + (size_t)layer * rows * pool->d;
-  *V8 = pool->V8 + (size_t)layer * rows * pool->d;
-  *Ks = pool->Ks + (size_t)layer * rows;
-  *Vs = pool->Vs + (size_t)layer * rows;
+  *records = pool->R + (size_t)layer * rows * pool->rec;
+  *record_bytes = pool->rec;
   return IG_OK;
 }
 
@@ -352,12 +351,11 @@ extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const
     const unsigned blocks = (unsigned)((rows + wpb - 1) / wpb);
     auto Kh = reinterpret_cast<const __half*>(K);
     auto Vh = reinterpret_cast<const __half*>(V);
+    uint8_t* R0 = pool->R + r0 * pool->rec;
     if (pool->d == 128)
-      k_quantize_rows<4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, pool->K8 + r0 * 128, pool->V8 + r0 * 128,
-                                                     pool->Ks + r0, pool->Vs + r0);
+      k_quantize_rows<4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
     else
-      k_quantize_rows<2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, pool->K8 + r0 * 64, pool->V8 + r0 * 64,
-                                                     pool->Ks + r0, pool->Vs + r0);
+      k_quantize_rows<2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
     IG_CHECK_LAUNCH("fp8 pool write launch");
     return IG_OK;
   }
@@ -389,14 +387,13 @@ extern "C" ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B,
       const int units = B * H, wpb = 8;
       auto kn = reinterpret_cast<const __half*>(k_new);
       auto vn = reinterpret_cast<const __half*>(v_new);
+      uint8_t* R0 = pool->R + r0 * pool->rec;
       if (d == 128)
-        k6_append_fp8<4><<<(units + wpb - 1) / wpb, 32 * wpb, 0, as_stream(stream)>>>(
-            pool->K8 + r0 * d, pool->V8 + r0 * d, pool->Ks + r0, pool->Vs + r0, units, pool->cap, H, slot, kn, vn,
-            error_word());
+        k6_append_fp8<4><<<(units + wpb - 1) / wpb, 32 * wpb, 0, as_stream(stream)>>>(R0, pool->rec, units, pool->cap,
+                                                                                     H, slot, kn, vn, error_word());
       else
-        k6_append_fp8<2><<<(units + wpb - 1) / wpb, 32 * wpb, 0, as_stream(stream)>>>(
-            pool->K8 + r0 * d, pool->V8 + r0 * d, pool->Ks + r0, pool->Vs + r0, units, pool->cap, H, slot, kn, vn,
-            error_word());
+        k6_append_fp8<2><<<(units + wpb - 1) / wpb, 32 * wpb, 0, as_stream(stream)>>>(R0, pool->rec, units, pool->cap,
+                                                                                     H, slot, kn, vn, error_word());
       IG_CHECK_LAUNCH("fp8 append launch");
       if (!Kpart && !Kdense) return IG_OK;
     } else {
@@ -442,14 +439,13 @@ extern "C" ig_status ig_append_kv_layers(void* stream, ig_pool* pool, int layers
   auto Vd = reinterpret_cast<uint4*>(Vdense);
   if (!pool->fp8) {
     k6_append_layers<0><<<grid, 64, 0, st>>>(P, reinterpret_cast<uint4*>(pool->Kdev), reinterpret_cast<uint4*>(pool->Vdev),
-                                            nullptr, nullptr, nullptr, nullptr, pool->cap, H, d, Lcap, units, slot, kn, vn,
-                                            Kd, Vd, error_word());
+                                            nullptr, 0, pool->cap, H, d, Lcap, units, slot, kn, vn, Kd, Vd, error_word());
   } else if (d == 128) {
-    k6_append_layers<4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->K8, pool->V8, pool->Ks, pool->Vs, pool->cap, H,
-                                            d, Lcap, units, slot, kn, vn, Kd, Vd, error_word());
+    k6_append_layers<4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+                                            slot, kn, vn, Kd, Vd, error_word());
   } else {
-    k6_append_layers<2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->K8, pool->V8, pool->Ks, pool->Vs, pool->cap, H,
-                                            d, Lcap, units, slot, kn, vn, Kd, Vd, error_word());
+    k6_append_layers<2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+                                            slot, kn, vn, Kd, Vd, error_word());
   }
   IG_CHECK_LAUNCH("batched append launch");
   return IG_OK;

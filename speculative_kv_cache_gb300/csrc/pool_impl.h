@@ -10,10 +10,8 @@ struct ig_pool {
   int policy = 0;            // IG_POOL_COUNTER, IG_POOL_FIFO or IG_POOL_LRU
   bool storage = true;       // false: the slot manager only, no K/V rows
   bool fp8 = false;          // rows stored as e4m3 codes with one fp32 scale per row
-  uint8_t* K8 = nullptr;     // fp8 pools: pinned, mapped codes [layers][B][H][cap][d]
-  uint8_t* V8 = nullptr;
-  float* Ks = nullptr;       // fp8 pools: pinned, mapped row scales [layers][B][H][cap]
-  float* Vs = nullptr;
+  uint8_t* R = nullptr;      // fp8 pools: pinned, mapped records [layers][B][H][cap][rec]:
+  int rec = 0;               //   K codes [d], V codes [d], K scale, V scale (fp32), 8 B pad
   uint16_t* K = nullptr;     // pinned, mapped host memory [layers][B][H][cap][d]
   uint16_t* V = nullptr;
   uint16_t* Kdev = nullptr;  // the same memory as seen from the device

@@ -80,7 +80,7 @@ _sig("ig_select", _i, _vp, _i, _i, _i, _vp, _vp, _f, _i, _f, _vp, _vp, _vp, _vp,
 _sig("ig_pool_create", _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_create_ex", _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_slot_tokens", _i, _vp, _i, _i, _vp)
-_sig("ig_pool_kv8", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp))
+_sig("ig_pool_kv8", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_i))
 _sig("ig_pool_evictions", _i, _vp, _i, _i, C.POINTER(C.c_int64))
 _sig("ig_append_kv_layers", _i, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_eviction_misses", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp)
@@ -267,20 +267,19 @@ def ig_pool_counters(pool, layer, b, out):
 
 
 def ig_pool_kv8(pool, layer):
-    """fp8 pools: host addresses (also valid on the device) of one layer's codes and scales."""
-    k, v, ks, vs = _vp(), _vp(), _vp(), _vp()
-    _ok(_lib.ig_pool_kv8(pool, layer, C.byref(k), C.byref(v), C.byref(ks), C.byref(vs)), "ig_pool_kv8")
-    return k.value, v.value, ks.value, vs.value
+    """fp8 pools: host address (also valid on the device) of one layer's records, and their size."""
+    r, n = _vp(), _i(0)
+    _ok(_lib.ig_pool_kv8(pool, layer, C.byref(r), C.byref(n)), "ig_pool_kv8")
+    return r.value, n.value
 
 
 def pool_layer_view_fp8(pool, layer, B, H, cap, d):
     """NumPy views of one layer of an fp8 pool: codes [B, H, cap, d] uint8 (K, V) and scales
-    [B, H, cap] float32 (K, V)."""
-    k, v, ks, vs = ig_pool_kv8(pool, layer)
-    n, r = B * H * cap * d, B * H * cap
-    arr = lambda p, t, m, shp: np.ctypeslib.as_array(C.cast(p, C.POINTER(t)), shape=(m,)).reshape(shp)  # noqa: E731
-    return (arr(k, C.c_uint8, n, (B, H, cap, d)), arr(v, C.c_uint8, n, (B, H, cap, d)),
-            arr(ks, C.c_float, r, (B, H, cap)), arr(vs, C.c_float, r, (B, H, cap)))
+    [B, H, cap] float32 (K, V), all views into the records."""
+    r, rec = ig_pool_kv8(pool, layer)
+    raw = np.ctypeslib.as_array(C.cast(r, C.POINTER(C.c_uint8)), shape=(B * H * cap * rec,)).reshape(B, H, cap, rec)
+    sc = raw[..., 2 * d:2 * d + 8].view(np.float32)
+    return raw[..., :d], raw[..., d:2 * d], sc[..., 0], sc[..., 1]
 
 
 def ig_pool_slot_tokens(pool, layer, b, out):
