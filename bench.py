@@ -62,6 +62,7 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-layers", type=int, default=0, help="oracle sample: layers (0 = default)")
+    p.add_argument("--oracle-layer-step", default=None, help=argparse.SUPPRESS)
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (small cases for profiling)")
     return p.parse_args(argv)
@@ -87,11 +88,11 @@ def workload_config(w: synth.Workload, alpha: float) -> dict:
 # ---------------------------------------------------------------------------------------
 # CPU oracle (the baseline and the reference arm)
 # ---------------------------------------------------------------------------------------
-def oracle_sample(w: synth.Workload, n_layers: int, alpha: float):
-    """Inputs of one decode step for ONE sequence and n_layers layers (same recipe)."""
-    w1 = synth.scaled(w, batch=1)
+def oracle_sample(w: synth.Workload, n_layers: int, alpha: float, batch: int = 1):
+    """Inputs of one decode step for ``batch`` sequences and n_layers layers (same recipe)."""
+    w1 = synth.scaled(w, batch=batch)
     Lcap = w1.lcap
-    L = np.array([min(w1.prompt, w1.pool_cap)], dtype=np.int32)  # resident slots
+    L = np.full(batch, min(w1.prompt, w1.pool_cap), dtype=np.int32)  # resident slots
     xs = synth.layer_inputs(w1, step=0, layers=n_layers + 1)
     layers = []
     for l in range(1, n_layers + 1):
@@ -124,6 +125,41 @@ def time_oracle(w1, L, layers, alpha) -> float:
         Kg, Vg = ora.gather(K, V, idx, K.shape[2])
         ora.attend(q, Kg, Vg, cnt, scale, kn, vn)
     return time.perf_counter() - t0
+
+
+ONE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def oracle_layer_step_child(names, alpha) -> int:
+    """(child process, BLAS pinned to one thread) one layer-step of each named workload, all its
+    sequences: print {"name": seconds, ...}."""
+    out = {}
+    for name in names:
+        w = synth.WORKLOADS[name]
+        a = alpha if alpha in w.alphas else w.alphas[0]
+        w1, L, layers = oracle_sample(w, 1, a, batch=w.batch)
+        time_oracle(w1, L, layers, a)  # warm
+        out[name] = time_oracle(w1, L, layers, a)
+    print(json.dumps(out), flush=True)
+    return 0
+
+
+def oracle_one_thread(w: synth.Workload, alpha: float) -> dict | None:
+    """One-thread oracle time of one layer-step (every sequence) of this workload and of the
+    one-layer tiny workload, in a child process whose BLAS pool is held to one thread."""
+    names = [w.name] + (["tiny"] if w.name != "tiny" else [])
+    if w.name not in synth.WORKLOADS or synth.WORKLOADS[w.name] != w:
+        return None  # a resized workload (--layers): its layer-step is the named one's
+    env = dict(os.environ, **{k: "1" for k in ONE_THREAD_ENV})
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-layer-step", ",".join(names),
+                            "--alpha", str(alpha)], env=env, capture_output=True, text=True, timeout=600)
+        secs = json.loads(r.stdout.strip().splitlines()[-1])
+    except (subprocess.SubprocessError, ValueError, IndexError):
+        return None
+    return {name: {"layer_step_s": t, "sample": f"one decode layer-step of all {synth.WORKLOADS[name].batch} "
+                                                f"sequences (layer 1), one BLAS thread"}
+            for name, t in secs.items()}
 
 
 def run_reference(args, w, alpha):
@@ -210,6 +246,31 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def fetch_stream_summary(timelines, fused_fetch: bool) -> dict | None:
+    """How busy the fetch stream was, from per-step timelines ([L, 6]: fetch, speculate+select,
+    attend+append start/end in ms).  A gap before fetch l is charged to its selection when
+    selection l ended after fetch l-1 did, else (staged fetch) to the gather buffer when the
+    attention of layer l-2 that frees it ended after fetch l-1, else to launch latency."""
+    if not timelines or timelines[0].shape[0] < 3:
+        return None
+    busy, span, gaps, by_sel, by_buf = 0.0, 0.0, [], 0, 0
+    for T in timelines:
+        L = T.shape[0]
+        busy += float((T[1:, 1] - T[1:, 0]).sum())
+        span += float(T[L - 1, 1] - T[1, 0])
+        for l in range(2, L):
+            prev_end = T[l - 1, 1]
+            gaps.append(float(T[l, 0] - prev_end))
+            if T[l, 3] > prev_end:
+                by_sel += 1
+            elif not fused_fetch and l >= 2 and T[l - 2, 5] > prev_end:
+                by_buf += 1
+    n = len(gaps)
+    return {"busy_frac": busy / span if span > 0 else None, "gap_us_mean": 1e3 * sum(gaps) / n,
+            "gated_by_select_frac": by_sel / n, "gated_by_buffer_frac": by_buf / n,
+            "steps": len(timelines)}
 
 
 def measured_peaks():
@@ -356,6 +417,9 @@ def run_ours(args, w, alpha):
                "sample": f"1 of {w.batch} sequences, {nl} of {w.layers} layers, one decode step "
                          f"({t_cpu:.1f} s of NumPy float64)"}
         del sample
+        one = oracle_one_thread(w, alpha)
+        if one is not None:
+            cpu["one_thread"] = one
 
     link = link_peak_gbs(torch)
     hbm_peak, hbm_src = measured_peaks()
@@ -382,6 +446,7 @@ def run_ours(args, w, alpha):
 
     stage = [0.0, 0.0, 0.0, 0.0]
     stage_n = [0, 0, 0, 0]
+    timelines = []
     barrier()
     launches0 = ig.ig_launch_count()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -396,6 +461,7 @@ def run_ours(args, w, alpha):
                 for j in range(4):
                     stage[j] += ms[j]
                     stage_n[j] += n[j]
+                timelines.append(dec.timeline(steps_back=1))
             s += 1
         t1.record(dec.S)
         t1.synchronize()
@@ -403,6 +469,7 @@ def run_ours(args, w, alpha):
         for j in range(4):
             stage[j] += ms[j]
             stage_n[j] += n[j]
+        timelines.append(dec.timeline(steps_back=0))
     barrier()
     launches = ig.ig_launch_count() - launches0
     elapsed = t0.elapsed_time(t1)
@@ -479,6 +546,7 @@ def run_ours(args, w, alpha):
             "us_per_speculative_layer_step": 1000 * (ms_per_step - stage[3] / args.steps) / max(1, w.layers - 1),
             "layer0_ms_per_step": stage[3] / args.steps,
             "hbm_alg_frac": {"of_measured": hbm_gbs_alg / hbm_peak, "of_nominal_8000": hbm_gbs_alg / 8000.0},
+            "fetch_stream": fetch_stream_summary(timelines, fused_fetch),
             "stage_ms_per_step": {("fetch_attend" if fused_fetch else "gather"): stage[0] / args.steps,
                                   "speculate_select": stage[1] / args.steps,
                                   ("append" if fused_fetch else "attend_append"): stage[2] / args.steps},
@@ -511,6 +579,8 @@ def run_ours(args, w, alpha):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.oracle_layer_step:
+        return oracle_layer_step_child(args.oracle_layer_step.split(","), args.alpha or 4.0)
     w = synth.WORKLOADS[args.workload]
     if args.layers:
         w = synth.scaled(w, layers=args.layers)

@@ -592,6 +592,16 @@ uint64_t ig_launch_count(void);
  * step to finish; reading step t-1 while step t is queued keeps the GPU busy. */
 ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float* ms_out, int* counts_out);
 
+/* The same step's stages as a timeline (a trace of the two streams): t_out (host float
+ * [layers][6]) receives, per layer, the device times in ms of the start and end of its fetch
+ * (fetch stream), of its speculation + selection and of its attention + append (compute
+ * stream; the roles of ig_decoder_stage_ms's intervals), all relative to the start of the
+ * step's first timed stage (layer 1's speculation; layer 0's attention when there is one
+ * layer).  Layer 0 has no fetch or speculation: NaN there.  The InfiniGen paper-graph summary
+ * draws this overlap of the prefetch with the previous layer's compute (section 3.2, Fig 8);
+ * the timeline shows it.  Needs config.stage_timing = 1; waits for that step to finish. */
+ig_status ig_decoder_timeline(ig_decoder* dec, int steps_back, float* t_out);
+
 #ifdef __cplusplus
 }
 #endif

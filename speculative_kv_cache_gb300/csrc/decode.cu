@@ -23,6 +23,7 @@
 //   S: wait att[L-2], append(L-2); wait att[L-1], append(L-1)
 // so the fetch stream does nothing but fetch and attend.  Selection l reuses index buffer
 // l % 2 only after attention(l-2) has finished with it.
+#include <limits>
 #include <vector>
 
 #include "ig_common.cuh"
@@ -425,6 +426,36 @@ extern "C" ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float*
     if (counts_out) counts_out[i] = counts[i];
   }
   return IG_OK;
+}
+
+extern "C" ig_status ig_decoder_timeline(ig_decoder* dec, int steps_back, float* t_out) {
+  IG_REQUIRE(dec && t_out, "null argument");
+  IG_REQUIRE(steps_back == 0 || steps_back == 1, "steps_back must be 0 or 1");
+  IG_REQUIRE(dec->cfg.stage_timing && dec->steps > steps_back, "stage timing is off or no such step");
+  const int L = dec->cfg.layers;
+  const int tset = (int)((dec->steps - 1 - steps_back) & 1) * L;
+  // the step's first timed stage: speculation of layer 1 (layer 0's attention when L == 1)
+  cudaEvent_t t0 = L > 1 ? dec->ts0[tset + 1] : dec->ta0[tset];
+  const float nan = std::numeric_limits<float>::quiet_NaN();
+  cudaError_t e = cudaSuccess;
+  auto at = [&](cudaEvent_t ev, float* out) -> cudaError_t {
+    cudaError_t r = cudaEventSynchronize(ev);
+    if (r == cudaSuccess) r = cudaEventElapsedTime(out, t0, ev);
+    return r;
+  };
+  for (int l = 0; l < L && e == cudaSuccess; ++l) {
+    float* row = t_out + (size_t)l * 6;
+    for (int j = 0; j < 4; ++j) row[j] = nan;
+    if (l >= 1) {
+      e = at(dec->tg0[tset + l], &row[0]);
+      if (e == cudaSuccess) e = at(dec->tg1[tset + l], &row[1]);
+      if (e == cudaSuccess) e = at(dec->ts0[tset + l], &row[2]);
+      if (e == cudaSuccess) e = at(dec->ts1[tset + l], &row[3]);
+    }
+    if (e == cudaSuccess) e = at(dec->ta0[tset + l], &row[4]);
+    if (e == cudaSuccess) e = at(dec->ta1[tset + l], &row[5]);
+  }
+  return e == cudaSuccess ? IG_OK : cuda_fail(e, "stage timeline");
 }
 
 extern "C" ig_status ig_decoder_graph_capture(ig_decoder* dec, const ig_step_io* io, void* stream,

@@ -214,6 +214,10 @@ class Decoder:
         """Per-stage device times of a recent step (see ig_decoder_stage_ms); waits for it."""
         return ig.ig_decoder_stage_ms(self.handle, steps_back)
 
+    def timeline(self, steps_back=0):
+        """The stages of a recent step on the two streams (see ig_decoder_timeline); waits for it."""
+        return ig.ig_decoder_timeline(self.handle, self.layers, steps_back)
+
     def finish(self):
         self.S.synchronize()
         self._fold_pending()

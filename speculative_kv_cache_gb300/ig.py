@@ -417,6 +417,7 @@ _sig("ig_decoder_create", _i, C.POINTER(DecoderConfig), C.POINTER(DecoderBuffers
 _sig("ig_decoder_destroy", _i, _vp)
 _sig("ig_decode_step", _i, _vp, C.POINTER(StepIO), _vp, _vp)
 _sig("ig_decoder_stage_ms", _i, _vp, _i, C.POINTER(_f), C.POINTER(_i))
+_sig("ig_decoder_timeline", _i, _vp, _i, C.POINTER(_f))
 _sig("ig_pool_update", _i, _vp, _i, _i, _vp)
 _sig("ig_pool_prefill", _i, _vp, _i, _vp)
 _sig("ig_pool_step", _i, _vp, _vp, _i, _vp)
@@ -462,6 +463,14 @@ def ig_decoder_stage_ms(dec, steps_back=0):
     cnt = (_i * 4)()
     _ok(_lib.ig_decoder_stage_ms(dec, steps_back, ms, cnt), "ig_decoder_stage_ms")
     return list(ms), list(cnt)
+
+
+def ig_decoder_timeline(dec, layers, steps_back=0):
+    """[layers, 6] float32: fetch start/end, speculate+select start/end, attend+append
+    start/end (ms from the step's first timed stage; NaN where a layer has no such stage)."""
+    t = np.zeros((layers, 6), dtype=np.float32)
+    _ok(_lib.ig_decoder_timeline(dec, steps_back, t.ctypes.data_as(C.POINTER(_f))), "ig_decoder_timeline")
+    return t
 
 
 def ig_pool_update(pool, layer, b, used):

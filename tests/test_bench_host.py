@@ -59,3 +59,33 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--steps", "1", "--warmup", "0"], cwd=ROOT, capture_output=True, text=True,
                        timeout=300, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_one_thread_oracle_layer_step_runs_in_a_child():
+    import bench
+    from speculative_kv_cache_gb300 import synth
+
+    got = bench.oracle_one_thread(synth.WORKLOADS["tiny"], 4.0)
+    assert set(got) == {"tiny"}
+    assert got["tiny"]["layer_step_s"] > 0 and "one BLAS thread" in got["tiny"]["sample"]
+    # a resized workload has no layer-step of its own name
+    assert bench.oracle_one_thread(synth.scaled(synth.WORKLOADS["tiny"], layers=3), 4.0) is None
+
+
+def test_fetch_stream_summary_charges_gaps():
+    import numpy as np
+
+    import bench
+
+    nan = float("nan")
+    # 4 layers; fetch l runs [f0, f1], select [s0, s1], attend [a0, a1] (ms)
+    T = np.array([[nan, nan, nan, nan, 0.0, 0.1],
+                  [0.0, 1.0, 0.0, 0.2, 0.2, 0.3],   # fetch 1
+                  [1.5, 2.5, 0.3, 1.4, 1.6, 1.7],   # fetch 2 waited for select 2 (ended 1.4 > 1.0)
+                  [2.6, 3.6, 1.7, 1.9, 2.5, 2.6]],  # fetch 3: select ended at 1.9 < 2.5; att(1) ended 0.3
+                 dtype=np.float32)
+    got = bench.fetch_stream_summary([T], fused_fetch=False)
+    assert abs(got["busy_frac"] - 3.0 / 3.6) < 1e-6
+    assert abs(got["gap_us_mean"] - 1e3 * (0.5 + 0.1) / 2) < 1e-3
+    assert got["gated_by_select_frac"] == 0.5 and got["gated_by_buffer_frac"] == 0.0
+    assert bench.fetch_stream_summary([T[:2]], fused_fetch=False) is None

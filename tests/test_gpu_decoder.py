@@ -198,6 +198,21 @@ def test_decoder_llama13b_width_capped_pool(mods):
     _run(mods, w, steps=3, rope=True, check_slots=True)
 
 
+def _check_timeline(T, L, fused_fetch, eps=2e-3):
+    """The stage timeline honours the step's dependencies (ms; event resolution ~0.5 us)."""
+    assert T.shape == (L, 6)
+    assert np.isnan(T[0, :4]).all() and np.isfinite(T[0, 4:]).all() and np.isfinite(T[1:]).all()
+    assert T[1, 2] == 0.0  # the reference point: layer 1's speculation starts the step
+    for j in (0, 2, 4):
+        ok = ~np.isnan(T[:, j])
+        assert (T[ok, j] <= T[ok, j + 1] + eps).all()
+    for l in range(1, L):
+        assert T[l, 0] >= T[l, 3] - eps  # the fetch waits for its selection
+        assert T[l, 4] >= T[l, 1] - eps  # attention (staged) / append (fused) waits for the fetch
+        if l >= 2:
+            assert T[l, 0] >= T[l - 1, 1] - eps  # one fetch stream: fetches in layer order
+
+
 @pytest.mark.parametrize("fused_fetch", [False, True])
 def test_graph_replay_matches_eager_step(mods, fused_fetch):
     """The CUDA-graph form of the step gives the same bytes as the eager step, step after step."""
@@ -229,6 +244,7 @@ def test_graph_replay_matches_eager_step(mods, fused_fetch):
                 if graph and s >= 1:
                     ms, n = dec.stage_ms()
                     assert n[0] == w.layers - 1 and ms[0] > 0
+                    _check_timeline(dec.timeline(), w.layers, fused_fetch)
             outs[graph] = res
         finally:
             dec.close()

@@ -367,10 +367,12 @@ def test_pool_evict_matches_oracle_counter_policy(ig):
         ig.ig_pool_destroy(pool)
 
 
+@pytest.mark.parametrize("step", [0, 127])
 @pytest.mark.parametrize("name", list(SHAPES))
-def test_layer_step_end_to_end(ig, pools, name):
-    """speculate -> select -> gather -> attend on the GPU against the oracle in float64."""
-    c = make_case(name, step=3)
+def test_layer_step_end_to_end(ig, pools, name, step):
+    """speculate -> select -> gather -> attend on the GPU against the oracle in float64, at the
+    first and the last (128th) generated token: the context grows from prompt + 1 to prompt + 128."""
+    c = make_case(name, step=step)
     w = c["w"]
     B, H, d, k, D, Lcap = w.batch, w.heads, w.head_dim, w.k, w.hidden, c["Lcap"]
     alpha = w.alphas[0]
@@ -406,29 +408,32 @@ def test_layer_step_end_to_end(ig, pools, name):
 
 
 @functools.lru_cache(maxsize=1)
-def rope_case():
-    """One Llama-2-7B-shaped layer at full size: RoPE, context 3968 + 1, the oracle's own skew."""
-    w = synth.WORKLOADS["llama-2-7b"]
-    Lcap = 4096
-    L = np.full(w.batch, w.prompt + 1, dtype=np.int32)
+def rope_case(name="llama-2-7b", step=1):
+    """One RoPE layer at full size (Llama-2-7B: context 3968 + step + 1; Llama-2-13B: its pool
+    holds 2458 rows, the current token sits at position 3968 + step), the oracle's own skew."""
+    w = synth.WORKLOADS[name]
+    Lcap = w.lcap
+    L = np.full(w.batch, min(w.prompt + step, w.pool_cap), dtype=np.int32)
     Xs, Wq, Wk = synth.skew_inputs(w, layer=1)
     A, _, _, _, _ = ora.skew(Xs, Wq, Wk, w.heads, w.head_dim, rope_theta=w.rope_theta)
     K, V = synth.pool_layer(w, 1, cap=Lcap)
     cols = synth.skewed_columns(w, 1)
-    x = synth.layer_inputs(w, step=1, layers=1)[0]
-    q, kn, vn = synth.token_inputs(w, 1, 1)
+    x = synth.layer_inputs(w, step=step, layers=1)[0]
+    q, kn, vn = synth.token_inputs(w, 1, step)
     A_cols = np.stack([A[h][:, cols[h]] for h in range(w.heads)]).astype(np.float32)
+    pos = np.full(w.batch, w.prompt + step, dtype=np.int32)
     return dict(w=w, Lcap=Lcap, L=L, A=A.astype(np.float32), A_cols=A_cols, Wq=Wq, K=K, V=V, cols=cols, x=x,
-                q=q, kn=kn, vn=vn, Kpart=ora.partial_key_cache(K, cols), pos=L.copy(),
+                q=q, kn=kn, vn=vn, Kpart=ora.partial_key_cache(K, cols), pos=pos,
                 scale=np.float32(1.0 / math.sqrt(w.head_dim)))
 
 
-@pytest.mark.parametrize("alpha", [2.0, 4.0, 6.0])
-def test_rope_layer_step_end_to_end(ig, pools, alpha):
-    c = rope_case()
+@pytest.mark.parametrize("name,step,alpha", [("llama-2-7b", 1, a) for a in (2.0, 4.0, 6.0)] +
+                         [("llama-2-7b", 127, 4.0), ("llama-2-13b", 0, 4.0), ("llama-2-13b", 127, 4.0)])
+def test_rope_layer_step_end_to_end(ig, pools, name, step, alpha):
+    c = rope_case(name, step)
     w = c["w"]
     B, H, d, k, D, Lcap = w.batch, w.heads, w.head_dim, w.k, w.hidden, c["Lcap"]
-    pool = _pool_for(ig, pools, c, "llama-2-7b")
+    pool = _pool_for(ig, pools, c, name)
     scores = empty((B, H, Lcap), torch.float32)
     qp = empty((B, H, k), torch.float32)
     ws = workspace(max(ig.ig_speculate_rope_workspace_bytes(B, D, H, d, k), ig.ig_attend_workspace_bytes(B, H, d, Lcap)))
