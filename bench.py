@@ -59,6 +59,8 @@ def parse_args(argv=None):
                    help="1: the host pool holds e4m3 rows with a per-row scale (d + 4 bytes per row)")
     p.add_argument("--fused-fetch", type=int, default=0,
                    help="1: layers 1.. attend straight from the pinned pool on the fetch stream (no staging)")
+    p.add_argument("--sm-split", type=int, default=0,
+                   help="N > 0: the fetch stream on N SMs of its own (green contexts), compute on the rest")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-layers", type=int, default=0, help="oracle sample: layers (0 = default)")
@@ -317,7 +319,7 @@ def link_peak_gbs(torch) -> float:
 
 def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True,
                   fused_fetch=False, pool_policy=0, policy=0, pool_fp8=False, batched_append=False,
-                  append_on_fetch=False):
+                  append_on_fetch=False, sm_split=0):
     from speculative_kv_cache_gb300.decoder import Decoder
 
     Lcap = w.lcap
@@ -326,7 +328,7 @@ def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False
                   stage_timing=True, graph=bool(graph), fused_select=bool(fused_select),
                   fused_fetch=bool(fused_fetch), pool_policy=pool_policy, policy=policy,
                   pool_fp8=bool(pool_fp8), batched_append=bool(batched_append),
-                  append_on_fetch=bool(append_on_fetch), device=device)
+                  append_on_fetch=bool(append_on_fetch), sm_split=sm_split, device=device)
     gen = torch.Generator(device=device)
     shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
@@ -433,7 +435,7 @@ def run_ours(args, w, alpha):
               "normalized": ig.IG_SEL_NORMALIZED}[args.policy]
     dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph,
                                           args.fused_select, fused_fetch, pool_policy, policy, args.pool_fp8,
-                                          args.batched_append, args.append_on_fetch)
+                                          args.batched_append, args.append_on_fetch, args.sm_split)
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
@@ -538,7 +540,9 @@ def run_ours(args, w, alpha):
                            fused_select=bool(args.fused_select), fused_fetch=fused_fetch,
                            selection=args.policy, batched_append=bool(args.batched_append),
                            append_on_fetch=bool(args.append_on_fetch), pool_dtype="fp8-e4m3 + fp32 row scale" if args.pool_fp8 else "fp16",
-                           pool_policy=args.pool_policy if w.pool_frac < 1 else None),
+                           pool_policy=args.pool_policy if w.pool_frac < 1 else None,
+                           sm_split=({"fetch_sms": dec.fetch_sms, "compute_sms": dec.compute_sms}
+                                     if args.sm_split else None)),
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "selected_fraction": float(f),
             "link_gbs": G_total / args.steps / (ms_per_step * 1e-3) / 1e9,

@@ -580,6 +580,26 @@ ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int layer, int B, i
 ig_status ig_gemm_tn(void* stream, int M, int N, int K, const uint16_t* A, const uint16_t* Bt,
                      uint16_t* C, float* colpart);
 
+/* A spatial split of one GPU between two streams: two green contexts over disjoint sets of
+ * SMs, each with one stream.  The decode step's host-link fetch (whose loads wait microseconds
+ * on the link) and its HBM-bound speculation and attention then never share an SM; sharing
+ * them, compute CTAs beside fetch CTAs run slower and hold back kernels that split their work
+ * evenly over their CTAs.  fetch_sms is rounded up to the device's partition granularity (8 on
+ * sm_90 and later); the compute stream gets the remaining SMs.  On success *compute_stream and
+ * *fetch_stream (cudaStream_t, owned by the split; the fetch stream at the highest priority)
+ * take work like any stream of the device: pass them to ig_decode_step and the per-stage calls.
+ * Kernels launched on them size their grids by their partition (the attention by its SM count;
+ * the fetch kernels, by default, two CTAs per fetch SM).  *compute_sms and *fetch_sms_out (may
+ * be NULL) receive the sizes.  IG_ERR_CUDA when the driver has no green contexts;
+ * IG_ERR_INVALID when the split leaves no SM for the compute stream.  Not part of the method:
+ * the InfiniGen paper-graph summary overlaps the prefetch with compute (section 3.2, Fig 8)
+ * on a GPU whose copy engine does the transfer. */
+typedef struct ig_sm_split ig_sm_split;
+ig_status ig_sm_split_create(int device, int fetch_sms, ig_sm_split** out, void** compute_stream,
+                             void** fetch_stream, int* compute_sms, int* fetch_sms_out);
+/* Destroys the streams and green contexts (after all work on them has finished).  NULL is a no-op. */
+ig_status ig_sm_split_destroy(ig_sm_split* split);
+
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t ig_launch_count(void);
 

@@ -399,8 +399,8 @@ inline size_t fa_part_bytes(int B, int H, int d) {
 }
 inline size_t prefix_bytes(int B, int H) { return round_up((size_t)(B * H + 1) * sizeof(int), 256); }
 
-inline int att_grid() {
-  int g = 4 * sm_count();
+inline int att_grid(cudaStream_t st) {
+  int g = 4 * sm_count(st);
   return g > kMaxAttCtas ? kMaxAttCtas : g;
 }
 
@@ -409,7 +409,7 @@ ig_status launch_attend(cudaStream_t st, int B, int H, int Lcap, float scale, co
                         const uint16_t* K, const uint16_t* V, const int32_t* cnt, int per_seq,
                         const uint16_t* kn, const uint16_t* vn, float* out, void* ws) {
   const int units = B * H;
-  const int G = att_grid();
+  const int G = att_grid(st);
   const size_t smem = (size_t)(units + 1) * sizeof(int);
   if (smem > 32 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k5_attend<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -529,8 +529,8 @@ extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int lay
   if (!workspace || workspace_bytes < need)
     return fail(IG_ERR_CAPACITY, "fused fetch + attention needs %zu workspace bytes", need);
   IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
-  // the same default as the gather: a quarter of the SMs saturates the host link
-  int grid = max_ctas > 0 ? max_ctas : sm_count() / 4;
+  // the same default as the gather
+  int grid = max_ctas > 0 ? max_ctas : fetch_grid(as_stream(stream));
   if (grid < 1) grid = 1;
   if (grid > kMaxFaCtas) grid = kMaxFaCtas;
   const size_t layer_elems = (size_t)B * H * pool->cap * d;

@@ -242,9 +242,7 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
   const int units = B * H;
   IG_REQUIRE(units <= kMaxGatherUnits, "B*H = %d exceeds %d", units, kMaxGatherUnits);
   IG_REQUIRE((long long)units * Lcap < (1ll << 31), "B*H*Lcap must stay below 2^31 rows");
-  // a quarter of the SMs (38 on a GB300) already moves ~185 GB/s over the host link while
-  // the compute stream runs beside it; more CTAs only slow that stream down
-  int grid = max_ctas > 0 ? max_ctas : sm_count() / 4;
+  int grid = max_ctas > 0 ? max_ctas : fetch_grid(as_stream(stream));
   if (grid < 1) grid = 1;
   const size_t smem = (size_t)(units + 1) * sizeof(int);
   if (smem > 48 * 1024) {

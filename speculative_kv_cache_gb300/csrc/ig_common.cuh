@@ -25,6 +25,16 @@ int* error_word();
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Number of SMs work on `st` may use: the size of its SM partition when the stream belongs to
+// one (ig_sm_split_create), else the device's count.  Grids are sized by it.
+int sm_count(cudaStream_t st);
+// SMs of the partition `st` belongs to, 0 when it has none.
+int stream_sms(cudaStream_t st);
+// Default grid of the host-link fetch kernels launched on `st`.
+int fetch_grid(cudaStream_t st);
+void register_stream_sms(cudaStream_t st, int sms);
+void unregister_stream_sms(cudaStream_t st);
+
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

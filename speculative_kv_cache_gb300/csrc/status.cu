@@ -3,6 +3,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "ig_common.cuh"
 
@@ -14,6 +15,9 @@ constexpr int kMaxDevices = 64;
 int* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 std::mutex g_mu;
+// streams bound to a subset of the SMs (a green context), with that subset's size
+std::vector<std::pair<cudaStream_t, int>> g_stream_sms;
+std::atomic<int> g_n_stream_sms{0};
 }  // namespace
 
 // One error word per device: bits IG_DEVERR_* set by guarded kernels.
@@ -53,6 +57,44 @@ int sm_count() {
     g_sms[dev] = n;
   }
   return g_sms[dev];
+}
+
+int stream_sms(cudaStream_t st) {
+  if (st && g_n_stream_sms.load(std::memory_order_acquire) > 0) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (const auto& e : g_stream_sms)
+      if (e.first == st) return e.second;
+  }
+  return 0;
+}
+
+int sm_count(cudaStream_t st) {
+  const int n = stream_sms(st);
+  return n > 0 ? n : sm_count();
+}
+
+int fetch_grid(cudaStream_t st) {
+  // on a stream of its own SM partition the fetch takes two CTAs on every SM of it; sharing
+  // all SMs with the compute stream, a quarter of them (38 on a GB300) already moves ~185 GB/s
+  // over the host link, and more CTAs only slow the compute stream down
+  const int n = stream_sms(st);
+  return n > 0 ? 2 * n : (sm_count() / 4 > 0 ? sm_count() / 4 : 1);
+}
+
+void register_stream_sms(cudaStream_t st, int sms) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_stream_sms.emplace_back(st, sms);
+  g_n_stream_sms.store((int)g_stream_sms.size(), std::memory_order_release);
+}
+
+void unregister_stream_sms(cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (size_t i = 0; i < g_stream_sms.size(); ++i)
+    if (g_stream_sms[i].first == st) {
+      g_stream_sms.erase(g_stream_sms.begin() + (long)i);
+      break;
+    }
+  g_n_stream_sms.store((int)g_stream_sms.size(), std::memory_order_release);
 }
 
 namespace {

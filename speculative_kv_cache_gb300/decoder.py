@@ -21,11 +21,23 @@ import torch
 from . import ig
 
 
+# SM splits by (device, fetch SMs), shared by the decoders that ask for one and kept for the
+# life of the process: torch's allocator may still touch their streams while it shuts down
+_SPLITS = {}
+
+
+def _sm_split(device: int, fetch_sms: int):
+    key = (device, fetch_sms)
+    if key not in _SPLITS:
+        _SPLITS[key] = ig.ig_sm_split_create(device, fetch_sms)
+    return _SPLITS[key]
+
+
 class Decoder:
     def __init__(self, *, layers, B, H, d, D, k, Lcap, pool_cap, alpha, policy=ig.IG_SEL_THRESHOLD,
                  cap_frac=1.0, score_scale=None, rope_theta=0.0, gather_ctas=0, stage_timing=False,
                  graph=False, fused_select=True, fused_fetch=False, pool_policy=ig.IG_POOL_COUNTER,
-                 pool_fp8=False, batched_append=False, append_on_fetch=False, device="cuda:0"):
+                 pool_fp8=False, batched_append=False, append_on_fetch=False, sm_split=0, device="cuda:0"):
         if pool_cap > Lcap or Lcap % 8:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
         if pool_fp8 and fused_fetch:
@@ -73,10 +85,16 @@ class Decoder:
         self.L_dev, self.pos_dev = e(B, dt=i32), e(B, dt=i32)
         self.slot_dev = e(layers, B, dt=i32)
         self.used_host = [torch.zeros(layers, B, Lcap, dtype=torch.uint8).pin_memory() for _ in range(2)]
-        self.S = torch.cuda.Stream(self.dev)
-        # the fetch stream gets the highest priority: its few CTAs are dispatched ahead of the
-        # compute stream's large grids, so the host link never waits for free SMs
-        self.G = torch.cuda.Stream(self.dev, priority=-100)
+        if sm_split:
+            # the fetch stream on sm_split SMs of its own, the compute stream on the rest
+            _, cs, fs, self.compute_sms, self.fetch_sms = _sm_split(self.dev.index or 0, int(sm_split))
+            self.S = torch.cuda.ExternalStream(cs, device=self.dev)
+            self.G = torch.cuda.ExternalStream(fs, device=self.dev)
+        else:
+            self.S = torch.cuda.Stream(self.dev)
+            # the fetch stream gets the highest priority: its few CTAs are dispatched ahead of
+            # the compute stream's large grids, so the host link never waits for free SMs
+            self.G = torch.cuda.Stream(self.dev, priority=-100)
         self._keep = self._make_buffers()
         self.handle = ig.ig_decoder_create(self.cfg, self._keep[0], self.pool)
         self.filled = 0

@@ -423,6 +423,8 @@ _sig("ig_pool_prefill", _i, _vp, _i, _vp)
 _sig("ig_pool_step", _i, _vp, _vp, _i, _vp)
 _sig("ig_pool_full", _i, _vp, C.POINTER(_i))
 _sig("ig_launch_count", C.c_uint64)
+_sig("ig_sm_split_create", _i, _i, _i, C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_vp), C.POINTER(_i), C.POINTER(_i))
+_sig("ig_sm_split_destroy", _i, _vp)
 _sig("ig_decoder_graph_capture", _i, _vp, C.POINTER(StepIO), _vp, _vp)
 _sig("ig_decoder_graph_launch", _i, _vp, _vp)
 
@@ -493,3 +495,16 @@ def ig_pool_full(pool) -> bool:
 
 def ig_launch_count() -> int:
     return _lib.ig_launch_count()
+
+
+def ig_sm_split_create(device: int, fetch_sms: int):
+    """(split handle, compute stream handle, fetch stream handle, compute SMs, fetch SMs)."""
+    h, cs, fs = _vp(), _vp(), _vp()
+    nc, nf = _i(), _i()
+    _ok(_lib.ig_sm_split_create(device, fetch_sms, C.byref(h), C.byref(cs), C.byref(fs), C.byref(nc), C.byref(nf)),
+        "ig_sm_split_create")
+    return h.value, cs.value, fs.value, nc.value, nf.value
+
+
+def ig_sm_split_destroy(split):
+    _ok(_lib.ig_sm_split_destroy(split), "ig_sm_split_destroy")

@@ -47,7 +47,7 @@ def _layer_data(w, l, cap, rope, ratio=None):
 
 
 def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True, fused_fetch=False, graph=False,
-         ratios=None, batched_append=False, append_on_fetch=False):
+         ratios=None, batched_append=False, append_on_fetch=False, sm_split=0):
     ig, decoder = mods
     dev = "cuda:0"
     Lcap = w.lcap
@@ -58,7 +58,8 @@ def _run(mods, w, steps, rope=False, check_slots=False, fused_select=True, fused
     dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=ks if ratios else w.k,
                           Lcap=Lcap, pool_cap=cap, alpha=alpha, rope_theta=w.rope_theta,
                           fused_select=fused_select, fused_fetch=fused_fetch, graph=graph,
-                          batched_append=batched_append, append_on_fetch=append_on_fetch, device=dev)
+                          batched_append=batched_append, append_on_fetch=append_on_fetch, sm_split=sm_split,
+                          device=dev)
     try:
         data = [_layer_data(w, l, cap, rope, ratios[l] if ratios else None) for l in range(w.layers)]
         for l, dd in enumerate(data):
@@ -188,6 +189,33 @@ def test_decoder_fused_fetch_graph_replay(mods):
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-ffg", layers=3, batch=2, heads=4, hidden=512,
                      prompt=200, gen=10, pool_frac=0.95)
     _run(mods, w, steps=4, check_slots=True, fused_fetch=True, graph=True)
+
+
+@pytest.mark.parametrize("fetch", ["staged", "fused"])
+def test_decoder_on_an_sm_split(mods, fetch):
+    """The step on two green contexts (fetch stream on 16 SMs of its own, compute on the rest),
+    eager and under CUDA-graph replay, against the oracle."""
+    ig, _ = mods
+    w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-split", layers=3, batch=2, heads=4, hidden=512,
+                     prompt=200, gen=10, pool_frac=0.95)
+    _run(mods, w, steps=4, check_slots=True, fused_fetch=fetch == "fused", sm_split=16)
+    _run(mods, w, steps=4, check_slots=True, fused_fetch=fetch == "fused", graph=True, sm_split=16)
+
+
+def test_sm_split_sizes_and_errors(mods):
+    ig, _ = mods
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    h, cs, fs, nc, nf = ig.ig_sm_split_create(0, 20)
+    try:
+        assert cs and fs and cs != fs
+        assert nf >= 20 and nc >= 1 and nc + nf <= n
+    finally:
+        ig.ig_sm_split_destroy(h)
+    with pytest.raises(ig.IGError) as e:
+        ig.ig_sm_split_create(0, n)
+    assert e.value.status == ig.IG_ERR_INVALID
+    with pytest.raises(ig.IGError):
+        ig.ig_sm_split_create(0, 0)
 
 
 def test_decoder_llama13b_width_capped_pool(mods):
