@@ -78,9 +78,10 @@ namespace {
 // workspace regions: [main: speculation / selection-fused / S's attention][selection][fetch
 // stream's attention, fused fetch only]
 void ws_regions(const ig_decoder_config* c, size_t* main, size_t* sel, size_t* fetch) {
-  size_t a = c->rope_theta > 0.f ? ig_speculate_rope_workspace_bytes(c->B, c->D, c->H, c->d, c->k)
-                                  : ig_speculate_workspace_bytes(c->B, c->D, c->H, c->k);
-  const size_t f = ig_speculate_select_workspace_bytes(c->B, c->D, c->H, c->d, c->k, c->Lcap);
+  const bool rope = c->rope_theta > 0.f;
+  size_t a = rope ? ig_speculate_rope_workspace_bytes(c->B, c->D, c->H, c->d, c->k)
+                  : ig_speculate_workspace_bytes(c->B, c->D, c->H, c->k);
+  const size_t f = ig_speculate_select_workspace_bytes(c->B, c->D, c->H, c->d, c->k, rope ? 1 : 0);
   if (f > a) a = f;
   const size_t b = ig_attend_workspace_bytes(c->B, c->H, c->d, c->Lcap);
   *main = round_up(a > b ? a : b, 256);
