@@ -333,6 +333,9 @@ __device__ __forceinline__ int cta_of(long long r, long long R, int G) {
 // the current token, normalises.  NGP partials per (head, CTA): 1 for the staged attention;
 // the lane-group count for the fused fetch, where group g of CTA cc holds a partial for the
 // head iff one of the head's rows in that CTA's range is g's (rows go round-robin to groups).
+// The head's candidate partials are numbered t = (cc - c0) * NGP + g and taken D at a time,
+// one per thread, so their loads are issued together rather than one after another; the
+// sums still run over t in order.
 template <int D, int NGP>
 __global__ void __launch_bounds__(D) k5_combine(const float* __restrict__ ws, const int* __restrict__ gpre,
                                                 int units, int G, const __half* __restrict__ q,
@@ -340,6 +343,8 @@ __global__ void __launch_bounds__(D) k5_combine(const float* __restrict__ ws, co
                                                 const __half* __restrict__ v_new, float scale,
                                                 float* __restrict__ out) {
   __shared__ float red[D / 32];
+  __shared__ float sf[D], sl[D];
+  __shared__ int sw[D];
   const int u = blockIdx.x, dd = threadIdx.x;
   // rows before this head, its rows and all rows (the main kernel's clamped prefix)
   const long long lo = gpre[u], R = gpre[units];
@@ -347,26 +352,52 @@ __global__ void __launch_bounds__(D) k5_combine(const float* __restrict__ ws, co
   float M = -INFINITY, Ls = 0.f, o = 0.f;
   if (c > 0) {
     // CTAs c0..c1 cover this head's rows; those with an empty range (fewer rows than CTAs)
-    // wrote nothing and are skipped
+    // wrote nothing, and are skipped
     const int c0 = cta_of(lo, R, G), c1 = cta_of(lo + c - 1, R, G);
-    for (int pass = 0; pass < 2; ++pass) {
-      for (int cc = c0; cc <= c1; ++cc) {
-        const long long s0 = (R * cc) / G, s1 = (R * (cc + 1)) / G;
-        if (s0 == s1) continue;
+    const int P = (c1 - c0 + 1) * NGP;
+    // offset (in floats) of candidate t's partial, or -1 where it holds none
+    auto where = [&](int t) -> long long {
+      const int cc = c0 + t / NGP, gi = t % NGP;
+      const long long s0 = (R * cc) / G, s1 = (R * (cc + 1)) / G;
+      if (s0 == s1) return -1;
+      if (NGP > 1) {
         const long long a = lo > s0 ? lo : s0, e = (lo + c) < s1 ? (lo + c) : s1;
         const long long n = e - a, off = (a - s0) % NGP;
-        for (int gi = 0; gi < NGP; ++gi) {
-          if (NGP > 1 && n < NGP && (gi - off + NGP) % NGP >= n) continue;
-          const float* w = ws + (((size_t)u + cc) * NGP + gi) * (D + kPartHead);
-          if (pass == 0) {
-            M = fmaxf(M, w[0]);
-          } else if (w[0] != -INFINITY) {
-            const float f = __expf(w[0] - M);
-            Ls += w[1] * f;
-            o += w[kPartHead + dd] * f;
-          }
+        if (n < NGP && (gi - off + NGP) % NGP >= n) return -1;
+      }
+      return (((long long)u + cc) * NGP + gi) * (D + kPartHead);
+    };
+    for (int base = 0; base < P; base += D) {  // the head's maximum
+      const int t = base + dd;
+      const long long w = t < P ? where(t) : -1;
+      float mt = w >= 0 ? ws[w] : -INFINITY;
+      for (int off = 16; off; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+      if ((dd & 31) == 0) red[dd >> 5] = mt;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) M = fmaxf(M, red[i]);
+      __syncthreads();
+    }
+    for (int base = 0; base < P; base += D) {  // weights, then the sums in candidate order
+      const int t = base + dd;
+      const long long w = t < P ? where(t) : -1;
+      const float mt = w >= 0 ? ws[w] : -INFINITY;
+      const bool live = mt != -INFINITY;
+      sf[dd] = live ? __expf(mt - M) : 0.f;
+      sl[dd] = live ? ws[w + 1] : 0.f;
+      sw[dd] = live ? (int)(w / (D + kPartHead)) : -1;
+      __syncthreads();
+      const int n = min(D, P - base);
+#pragma unroll 4
+      for (int i = 0; i < n; ++i) {
+        const int wi = sw[i];
+        if (wi >= 0) {
+          const float f = sf[i];
+          Ls += sl[i] * f;
+          o += ws[(size_t)wi * (D + kPartHead) + kPartHead + dd] * f;
         }
       }
+      __syncthreads();
     }
   }
   if (k_new) {
