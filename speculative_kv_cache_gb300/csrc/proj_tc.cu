@@ -109,11 +109,13 @@ __global__ void __launch_bounds__(kTcThreads) k1_partial_q_tc(
   const uint32_t tmem = *tmem_slot;
 
   if (threadIdx.x == 0) {
-    // every stage's loads at once: the CTA's whole K range is in flight
+    // every stage's loads at once: the CTA's whole K range is in flight; the weight, read
+    // once per step, is marked first for eviction
+    const uint64_t pol = l2_evict_first();
     for (int i = 0; i < nst; ++i) {
       mbar_arrive_expect_tx(&full[i], kStageA + kStageB);
       const int kx = k_begin + i * kTcBK;
-      tma_load_2d(sA + i * kStageA, &map_w, kx, m0, &full[i]);
+      tma_load_2d_hint(sA + i * kStageA, &map_w, kx, m0, &full[i], pol);
       tma_load_2d(sB + i * kStageB, &map_x, kx, b0, &full[i]);
     }
     bool ok = true;

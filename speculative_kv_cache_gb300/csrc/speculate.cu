@@ -97,7 +97,8 @@ __global__ void k2_scores(const float* __restrict__ qsrc, int S, int B, int H, i
     fence_mbar_init();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive_expect_tx(bar, (uint32_t)(k * n_copy * 2));
-    for (int c = 0; c < k; ++c) bulk_g2s(Ks + (size_t)c * T, rows + (size_t)c * Lcap, n_copy * 2, bar);
+    const uint64_t pol = l2_evict_first();
+    for (int c = 0; c < k; ++c) bulk_g2s_hint(Ks + (size_t)c * T, rows + (size_t)c * Lcap, n_copy * 2, bar, pol);
   }
   for (int c = threadIdx.x; c < k; c += blockDim.x) {
     const int N = H * k;
