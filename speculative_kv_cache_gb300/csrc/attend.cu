@@ -23,7 +23,7 @@ namespace {
 
 constexpr int kAttThreads = 128;
 constexpr int kAttUnroll = 4;
-constexpr int kMaxAttCtas = 1024;   // upper bound of the balanced grid (sizes the workspace)
+constexpr int kMaxAttCtas = 2048;   // upper bound of the balanced grid (sizes the workspace)
 constexpr int kMaxAttUnits = 16384; // (units + 1) ints of shared memory for the scan
 constexpr int kFaThreads = 256;     // fused fetch + attention: as the gather (host-link bound)
 constexpr int kFaUnroll = 6;        // rows per batch and lane group (two batches in flight)
@@ -430,8 +430,10 @@ inline size_t fa_part_bytes(int B, int H, int d) {
 }
 inline size_t prefix_bytes(int B, int H) { return round_up((size_t)(B * H + 1) * sizeof(int), 256); }
 
+// 8 CTAs of 4 warps per SM (the register limit at 64 per thread): 32 warps, 8 rows in flight
+// each, to cover the memory latency
 inline int att_grid(cudaStream_t st) {
-  int g = 4 * sm_count(st);
+  int g = 8 * sm_count(st);
   return g > kMaxAttCtas ? kMaxAttCtas : g;
 }
 

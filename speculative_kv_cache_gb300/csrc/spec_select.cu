@@ -40,8 +40,10 @@ __global__ void __launch_bounds__(kFThreads) k23_score_select(
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ float red_f[kFThreads / 32];
   __shared__ int red_i[kFThreads / 32];
-  __shared__ float chunk_max;
-  __shared__ int chunk_cnt;
+  // every CTA's chunk maximum and count, pushed here by their CTAs through distributed shared
+  // memory, so that after each exchange every CTA reads only its own shared memory
+  __shared__ float chunk_max[kFMaxChunks];
+  __shared__ int chunk_cnt[kFMaxChunks];
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
   float* qs = reinterpret_cast<float*>(smem + 16);
   __half* Ks = reinterpret_cast<__half*>(smem + 16 + ((k * 4 + 127) & ~127));
@@ -55,6 +57,9 @@ __global__ void __launch_bounds__(kFThreads) k23_score_select(
     if (threadIdx.x == 0 && rank == 0) raise_error(err, IG_DEVERR_INDEX);
     L = L < 0 ? 0 : Lcap;
   }
+  // no CTA writes into another's shared memory before all of the cluster's CTAs run: arrive
+  // now, wait just before the first push (by then the wait is long satisfied)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const int n_tok = max(0, min(kFT, L - t0));
   const int n_copy = (n_tok + 7) & ~7;
   const __half* rows = Kpart + ((size_t)bh * k) * Lcap + t0;
@@ -110,14 +115,15 @@ __global__ void __launch_bounds__(kFThreads) k23_score_select(
   for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) red_f[warp] = mx;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float m = -INFINITY;
-    for (int w = 0; w < kFThreads / 32; ++w) m = fmaxf(m, red_f[w]);
-    chunk_max = m;
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (threadIdx.x < nranks) {
+    float cm = -INFINITY;
+    for (int w = 0; w < kFThreads / 32; ++w) cm = fmaxf(cm, red_f[w]);
+    *cluster.map_shared_rank(&chunk_max[rank], (unsigned)threadIdx.x) = cm;
   }
   cluster.sync();
   float m = -INFINITY;
-  for (int r = 0; r < nranks; ++r) m = fmaxf(m, *cluster.map_shared_rank(&chunk_max, r));
+  for (int r = 0; r < nranks; ++r) m = fmaxf(m, chunk_max[r]);
   // flags in token order; a token past L_valid scored -inf and is never kept (for alpha = inf,
   // (m - (-inf)) < inf is false, and with no valid token m - s is NaN)
   bool f[4];
@@ -137,15 +143,15 @@ __global__ void __launch_bounds__(kFThreads) k23_score_select(
   __syncthreads();
   int before = incl - mine;
   for (int w = 0; w < warp; ++w) before += red_i[w];
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < nranks) {
     int tot = 0;
     for (int w = 0; w < kFThreads / 32; ++w) tot += red_i[w];
-    chunk_cnt = tot;
+    *cluster.map_shared_rank(&chunk_cnt[rank], (unsigned)threadIdx.x) = tot;
   }
-  cluster.sync();
+  cluster.sync();  // the last access to another CTA's shared memory is before this barrier
   int offset = 0, total = 0;
   for (int r = 0; r < nranks; ++r) {
-    const int c = *cluster.map_shared_rank(&chunk_cnt, r);
+    const int c = chunk_cnt[r];
     if (r < rank) offset += c;
     total += c;
   }
@@ -160,7 +166,6 @@ __global__ void __launch_bounds__(kFThreads) k23_score_select(
     }
   }
   if (rank == 0 && threadIdx.x == 0) cnt[bh] = total;
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 size_t fused_smem(int k) { return 16 + round_up((size_t)k * 4, 128) + (size_t)k * kFT * 2; }
