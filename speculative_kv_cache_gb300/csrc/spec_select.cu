@@ -3,11 +3,13 @@
 //
 // One thread-block cluster per (sequence, head), one CTA per chunk of 512 tokens (at most 8
 // chunks: Lcap <= 4096).  Each CTA stages its chunk of the partial key cache with bulk (TMA)
-// copies, scores 4 tokens per thread into registers, and reduces its chunk maximum; the CTAs
-// read each other's maxima through distributed shared memory, so every CTA knows the head's
-// maximum m.  Each thread then flags its tokens with (m - s) < alpha, the CTA scans its flags
-// in token order, the CTAs read the counts of the lower-ranked chunks through distributed
-// shared memory, and each writes its indices at the right offset.  The comparisons are the
+// copies, scores 4 tokens per thread into registers, and reduces its chunk maximum, which it
+// writes into every CTA of the cluster (distributed shared memory); after one cluster barrier
+// every CTA knows the head's maximum m.  Each thread then flags its tokens with (m - s) < alpha,
+// the CTA scans its flags in token order and pushes its count the same way; after a second
+// barrier each CTA sums the counts of the lower-ranked chunks and writes its indices at that
+// offset.  No CTA touches another's shared memory after that barrier, so none waits for the
+// others to finish.  The comparisons are the
 // same fp32 operations as in the separate score and select kernels, so the result is
 // identical to theirs.
 #include <cooperative_groups.h>
