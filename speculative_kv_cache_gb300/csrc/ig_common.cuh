@@ -104,16 +104,6 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
-// Bulk (non-tensor TMA) copy global -> shared, completing on `bar` with `bytes` of tx.
-// src, dst 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // An L2 policy that marks the lines it touches first for eviction: for data read once per
 // step (the partial key cache, the projection weight), so that it does not push out data read
 // again soon (the staged rows the attention reads).  Speculation + selection of an OPT-30B
@@ -124,7 +114,8 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
   return pol;
 }
 
-// bulk_g2s with an L2 policy
+// Bulk (non-tensor TMA) copy global -> shared, completing on `bar` with `bytes` of tx, under
+// the L2 policy `pol`.  src, dst 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
                                               uint64_t pol) {
   asm volatile(
