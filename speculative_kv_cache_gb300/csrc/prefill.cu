@@ -8,13 +8,15 @@
 //   Step 3  the partial query weight (the chosen rows of W~_Q^T) and the partial key cache.
 //
 // The GEMM C[M][N] = A[M][K] . Bt[N][K]^T (both K-major, fp16 in, fp32 accumulate, fp16 out):
-// one 128 x 256 output tile per CTA, a ring of 4 TMA stages of 64-wide K (48 KB each), one
-// thread issuing the loads and another the tcgen05 MMAs (128x256x16, accumulator in 256 TMEM
-// columns), each stage released by a tcgen05.commit onto its "empty" mbarrier.  The epilogue
-// reads the accumulator with tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = rows), stores
-// fp16 rows, and, when asked, reduces |C| down each column of the tile (a shuffle transpose-
-// reduce in each warp, then the four warps in a fixed order) into per-tile partial sums, so the
-// column score is deterministic.
+// a persistent kernel, one CTA per SM, each taking 128 x 256 output tiles in turn.  One thread
+// issues the TMA loads into a ring of 4 stages of 64-wide K (48 KB each), another the tcgen05
+// MMAs (128x256x16) into one of two 256-column accumulators in tensor memory, each stage
+// released by a tcgen05.commit onto its "empty" mbarrier and each finished accumulator
+// announced on its "full" one; four epilogue warps read it with tcgen05.ld (warp w owns TMEM
+// lanes 32 (w % 4) .. + 31 = rows), hand it back, store fp16 rows, and, when asked, reduce |C|
+// down each column of the tile (a shuffle transpose-reduce in each warp, then the four row
+// quarters in a fixed order) into per-tile partial sums, so the column score is deterministic.
+// The MMAs of the next tile run while the epilogue drains the last one.
 #include <cuda.h>
 
 #include <mutex>
@@ -27,21 +29,47 @@ namespace ig {
 namespace {
 
 constexpr int kGM = 128;        // tile rows (tcgen05 M = TMEM lanes)
-constexpr int kGN = 256;        // tile columns (tcgen05 N = TMEM columns)
+constexpr int kGN = 256;        // tile columns (tcgen05 N = TMEM columns of one accumulator)
 constexpr int kGK = 64;         // K per stage: one 128-byte swizzle atom of fp16
 constexpr int kGStages = 4;
-constexpr int kGThreads = 128;
+constexpr int kGThreads = 192;  // warp 0: TMA loads, warp 1: MMAs, warps 2-5: epilogue
 constexpr uint32_t kGStageA = kGM * kGK * 2;  // 16 KB
 constexpr uint32_t kGStageB = kGN * kGK * 2;  // 32 KB
-constexpr uint32_t kGTmemCols = 256;
+constexpr uint32_t kGTmemCols = 2 * kGN;      // two accumulators: one fills while one drains
 constexpr int kGGroup = 16;     // row tiles per group of the tile order
 // kind::f16, D fp32, A/B fp16 K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28
 constexpr uint32_t kGIdesc = (1u << 4) | ((uint32_t)(kGN >> 3) << 17) | ((uint32_t)(kGM >> 4) << 24);
 
+// barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain
 size_t gemm_smem_bytes() {
-  return 1024 + kGStages * (kGStageA + kGStageB) + (2 * kGStages + 1) * 8 + 32 + 4 * kGN * sizeof(float);
+  return 1024 + kGStages * (kGStageA + kGStageB) + (2 * kGStages + 5) * 8 + 32 + 4 * kGN * sizeof(float);
 }
 
+// Tile t of the grouped order: runs of kGGroup row tiles take each column tile in turn, so a B
+// tile is reused by the CTAs working on neighbouring t and the group's A tiles stay in L2.
+__device__ __forceinline__ void gemm_tile(int t, int tiles_m, int tiles_n, int& mt, int& ntile) {
+  const int per_group = kGGroup * tiles_n;
+  const int gi = t / per_group, within = t % per_group;
+  const int first_m = gi * kGGroup;
+  const int gsize = min(tiles_m - first_m, kGGroup);
+  mt = first_m + within % gsize;
+  ntile = within / gsize;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+
+// Persistent: CTA b takes tiles b, b + G, b + 2G, ... of the grouped order.  The load ring
+// and the MMAs run on across tiles, and the accumulator alternates between two 256-column
+// halves of tensor memory, so the epilogue of one tile overlaps the MMAs of the next.
 __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant__ CUtensorMap map_a,
                                                            const __grid_constant__ CUtensorMap map_b,
                                                            __half* __restrict__ C, int M, int N, int K,
@@ -53,20 +81,16 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant_
   unsigned char* sB = smem + kGStages * kGStageA;
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + kGStages * kGStageB);
   uint64_t* empty = full + kGStages;
-  uint64_t* done = empty + kGStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  float* csum = reinterpret_cast<float*>(abort_flag + 3);  // [4][kGN] (scalar accesses only)
+  uint64_t* acc_full = empty + kGStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* epi_ok = reinterpret_cast<int*>(tmem_slot + 2);   // [2]: the epilogue warps' joint verdict
+  float* csum = reinterpret_cast<float*>(tmem_slot + 4);  // [4][kGN] (scalar accesses only)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // grouped tile order: runs of kGGroup row tiles take each column tile in turn, so a B tile is
-  // reused by consecutive CTAs and the group's A tiles stay in L2 while the group sweeps N
   const int tiles_n = (N + kGN - 1) / kGN, tiles_m = (M + kGM - 1) / kGM;
-  const int per_group = kGGroup * tiles_n;
-  const int gi = (int)blockIdx.x / per_group, within = (int)blockIdx.x % per_group;
-  const int first_m = gi * kGGroup;
-  const int gsize = min(tiles_m - first_m, kGGroup);
-  const int mt = first_m + within % gsize, ntile = within / gsize;
-  const int n0 = ntile * kGN, m0 = mt * kGM;
+  const int T = tiles_m * tiles_n;
   const int nk = (K + kGK - 1) / kGK;
 
   if (threadIdx.x == 0) {
@@ -74,12 +98,16 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant_
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
-  if (warp == 0) {
+  if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
                  "r"(kGTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -89,121 +117,163 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (threadIdx.x == 0) {
-    // producer: stage kb % S of round kb / S is free once the MMAs of the previous round on it
-    // have completed (their commit arrives on empty[stage])
-    for (int kb = 0; kb < nk; ++kb) {
-      const int st = kb % kGStages, r = kb / kGStages;
-      if (r > 0 && !mbar_wait_bounded(&empty[st], (uint32_t)((r - 1) & 1))) {
-        *abort_flag = 1;
-        break;
+  if (warp == 0) {
+    if (lane == 0) {
+      // producer: stage it % S of round it / S is free once the MMAs of the previous round on it
+      // have completed (their commit arrives on empty[stage])
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < T && !*abort_flag; t += gridDim.x) {
+        int mt, ntile;
+        gemm_tile(t, tiles_m, tiles_n, mt, ntile);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const uint32_t st = it % kGStages, r = it / kGStages;
+          if (r > 0 && !mbar_wait_bounded(&empty[st], (r - 1) & 1)) {
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[st], kGStageA + kGStageB);
+          tma_load_2d(sA + st * kGStageA, &map_a, kb * kGK, mt * kGM, &full[st]);
+          tma_load_2d(sB + st * kGStageB, &map_b, kb * kGK, ntile * kGN, &full[st]);
+        }
       }
-      mbar_arrive_expect_tx(&full[st], kGStageA + kGStageB);
-      tma_load_2d(sA + st * kGStageA, &map_a, kb * kGK, m0, &full[st]);
-      tma_load_2d(sB + st * kGStageB, &map_b, kb * kGK, n0, &full[st]);
+      if (*abort_flag) {
+        // let the loads already issued land before the shared memory is released
+        for (uint32_t st = 0; st < kGStages && st < it; ++st)
+          mbar_wait_bounded(&full[st], ((it - 1 - st) / kGStages) & 1, 1u << 16);
+      }
     }
-  } else if (threadIdx.x == 32) {
-    // MMA issuer
-    bool ok = true;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int st = kb % kGStages, r = kb / kGStages;
-      if (!mbar_wait_bounded(&full[st], (uint32_t)(r & 1))) {
-        ok = false;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      uint32_t it = 0, j = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < T && ok && !*abort_flag; t += gridDim.x, ++j) {
+        const uint32_t buf = j & 1, u = j >> 1;
+        // the epilogue has drained this accumulator's previous tile
+        if (u > 0 && !mbar_wait_bounded(&acc_empty[buf], (u - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc_tm = tmem + buf * kGN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const uint32_t st = it % kGStages, r = it / kGStages;
+          if (!mbar_wait_bounded(&full[st], r & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_addr(sA + st * kGStageA), b0 = smem_addr(sB + st * kGStageB);
+#pragma unroll
+          for (int kk = 0; kk < kGK / 16; ++kk) {
+            const uint64_t ad = sw128_desc(a0 + kk * 32), bd = sw128_desc(b0 + kk * 32);
+            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+            asm volatile(
+                "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(acc_tm),
+                "l"(ad), "l"(bd), "r"(kGIdesc), "r"(acc));
+          }
+          mma_commit(&empty[st]);
+        }
+        if (ok) mma_commit(&acc_full[buf]);
+      }
+      if (!ok || *abort_flag) {
+        *abort_flag = 1;
+        // the MMAs already issued finish before tensor memory is released
+        mma_commit(drain);
+        mbar_wait_bounded(drain, 0, 1u << 16);
+      }
+    }
+  } else {
+    // epilogue, warps 2-5: warp w reads TMEM lanes 32 (w % 4) .. + 31 = rows of that quarter
+    const int q = warp & 3, et = threadIdx.x - 64;
+    uint32_t j = 0;
+    for (int t = blockIdx.x; t < T; t += gridDim.x, ++j) {
+      const uint32_t buf = j & 1, u = j >> 1;
+      const bool mine = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_full[buf], u & 1) ? 1 : 0) != 0;
+      // one verdict for the four warps (the TMEM loads are warp-collective and the warps meet
+      // at named barriers below): all four saw the tile, and nothing aborted
+      // (the abort flag is read before the barrier, so no warp can see a later value than another)
+      if (lane == 0) epi_ok[(j & 1)] = 1;
+      epi_sync();
+      if (lane == 0 && (!mine || *abort_flag)) epi_ok[(j & 1)] = 0;
+      epi_sync();
+      const bool go = epi_ok[(j & 1)] != 0;
+      if (!go) {
+        if (et == 0) {
+          *abort_flag = 1;
+          raise_error(err, IG_DEVERR_TIMEOUT);
+        }
         break;
       }
       tc_fence_after();
-      const uint32_t a0 = smem_addr(sA + st * kGStageA), b0 = smem_addr(sB + st * kGStageB);
-#pragma unroll
-      for (int kk = 0; kk < kGK / 16; ++kk) {
-        const uint64_t ad = sw128_desc(a0 + kk * 32), bd = sw128_desc(b0 + kk * 32);
-        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+      int mt, ntile;
+      gemm_tile(t, tiles_m, tiles_n, mt, ntile);
+      const int m0 = mt * kGM, n0 = ntile * kGN;
+      const int row = m0 + q * 32 + lane;
+      for (int ch = 0; ch < kGN / 32; ++ch) {
+        const int c0 = n0 + ch * 32;
+        uint32_t r[32];
+        const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + buf * kGN + (uint32_t)(ch * 32);
         asm volatile(
-            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
-            "l"(ad), "l"(bd), "r"(kGIdesc), "r"(acc));
-      }
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_addr(&empty[st]))
-                   : "memory");
-    }
-    if (ok)
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_addr(done))
-                   : "memory");
-    else
-      *abort_flag = 1;
-  }
-  __syncthreads();
-  const bool aborted = *abort_flag != 0;
-  // every thread takes the same branch: the TMEM loads below are warp-collective
-  const bool landed = __syncthreads_and((!aborted && mbar_wait_bounded(done, 0)) ? 1 : 0) != 0;
-  if (!landed) {
-    if (threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
-    if (aborted && threadIdx.x == 0) {
-      // let the loads already issued land before the shared memory is released
-      for (int i = 0; i < kGStages; ++i) mbar_wait_bounded(&full[i], 0, 1u << 16);
-    }
-  } else {
-    tc_fence_after();
-    const int row = m0 + warp * 32 + lane;
-    for (int ch = 0; ch < kGN / 32; ++ch) {
-      const int c0 = n0 + ch * 32;
-      uint32_t r[32];
-      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(ch * 32);
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-          "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-            "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-            "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-            "=r"(r[30]), "=r"(r[31])
-          : "r"(taddr));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      if (c0 >= N) continue;  // warp-uniform: N is a multiple of 32
-      float v[32];
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+              "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+              "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+              "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+            : "r"(taddr));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        if (c0 >= N) continue;  // warp-uniform: N is a multiple of 32
+        float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-      if (row < M) {
-        uint32_t h[16];
+        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+        if (row < M) {
+          uint32_t h[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-          h[i] = *reinterpret_cast<const uint32_t*>(&p);
-        }
-        uint4* dst = reinterpret_cast<uint4*>(C + (size_t)row * N + c0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
-      }
-      if (colpart) {
-        // |C| of the stored fp16 values (rows past M are zero: the A tile is zero-filled there);
-        // transpose-reduce: after the steps 16, 8, 4, 2, 1 lane j holds column j's sum
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = row < M ? fabsf(__half2float(__float2half_rn(v[i]))) : 0.f;
-#pragma unroll
-        for (int s = 16; s >= 1; s >>= 1) {
-          const bool up = (lane & s) != 0;
-#pragma unroll
-          for (int i = 0; i < s; ++i) {
-            const float send = up ? v[i] : v[i + s];
-            const float keep = up ? v[i + s] : v[i];
-            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+          for (int i = 0; i < 16; ++i) {
+            const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+            h[i] = *reinterpret_cast<const uint32_t*>(&p);
           }
+          uint4* dst = reinterpret_cast<uint4*>(C + (size_t)row * N + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
         }
-        csum[warp * kGN + ch * 32 + lane] = v[0];
+        if (colpart) {
+          // |C| of the stored fp16 values (rows past M are zero: the A tile is zero-filled
+          // there); transpose-reduce: after the steps 16, 8, 4, 2, 1 lane j holds column j's sum
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = row < M ? fabsf(__half2float(__float2half_rn(v[i]))) : 0.f;
+#pragma unroll
+          for (int s2 = 16; s2 >= 1; s2 >>= 1) {
+            const bool up = (lane & s2) != 0;
+#pragma unroll
+            for (int i = 0; i < s2; ++i) {
+              const float send = up ? v[i] : v[i + s2];
+              const float keep = up ? v[i + s2] : v[i];
+              v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s2);
+            }
+          }
+          csum[q * kGN + ch * 32 + lane] = v[0];
+        }
       }
-    }
-  }
-  __syncthreads();
-  if (landed && colpart) {
-    for (int c = threadIdx.x; c < kGN; c += kGThreads) {
-      if (n0 + c >= N) continue;
-      colpart[(size_t)mt * N + n0 + c] = ((csum[c] + csum[kGN + c]) + csum[2 * kGN + c]) + csum[3 * kGN + c];
+      // this warp's reads of the accumulator are done: the MMAs may refill it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+      if (colpart) {
+        epi_sync();
+        for (int c = et; c < kGN; c += 128) {
+          if (n0 + c >= N) continue;
+          colpart[(size_t)mt * N + n0 + c] = ((csum[c] + csum[kGN + c]) + csum[2 * kGN + c]) + csum[3 * kGN + c];
+        }
+        epi_sync();  // csum is refilled by the next tile
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kGTmemCols));
   }
@@ -468,7 +538,9 @@ ig_status gemm(cudaStream_t st, const uint16_t* A, const uint16_t* Bt, uint16_t*
   if (e != cudaSuccess) return cuda_fail(e, "prefill GEMM smem attribute");
   const long long tiles = (long long)((N + kGN - 1) / kGN) * ((M + kGM - 1) / kGM);
   IG_REQUIRE(tiles < (1ll << 31), "GEMM too large for one launch");
-  k_gemm_tn<<<(unsigned)tiles, kGThreads, smem, st>>>(ma, mb, reinterpret_cast<__half*>(C), M, N, K, colpart, error_word());
+  // persistent: one CTA per SM (its 197 KB of shared memory admit no second one)
+  const int grid = (int)(tiles < sm_count(st) ? tiles : sm_count(st));
+  k_gemm_tn<<<grid, kGThreads, smem, st>>>(ma, mb, reinterpret_cast<__half*>(C), M, N, K, colpart, error_word());
   IG_CHECK_LAUNCH("prefill GEMM launch");
   return IG_OK;
 }

@@ -37,7 +37,10 @@ def _ulp16(x):
     return 2.0 ** (np.floor(np.log2(a)) - 10)
 
 
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 288, 72), (1000, 512, 1000), (129, 32, 8), (4096, 768, 2048)])
+# the last two have more tiles than SMs: each persistent CTA takes several, alternating its
+# two accumulators and reusing each (ragged M, N and K in the second)
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (200, 288, 72), (1000, 512, 1000), (129, 32, 8), (4096, 768, 2048),
+                                   (16384, 1024, 128), (20000, 288, 72)])
 def test_gemm_matches_float64(ig, M, N, K):
     g = np.random.default_rng(M + N + K)
     A = g.standard_normal((M, K)).astype(np.float16)
