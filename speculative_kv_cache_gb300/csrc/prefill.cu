@@ -40,10 +40,21 @@ constexpr int kGGroup = 16;     // row tiles per group of the tile order
 // kind::f16, D fp32, A/B fp16 K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28
 constexpr uint32_t kGIdesc = (1u << 4) | ((uint32_t)(kGN >> 3) << 17) | ((uint32_t)(kGM >> 4) << 24);
 
-// barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain
+constexpr int kGStageRow = 64 + 8;  // halves per row of an epilogue warp's staging (+8: banks)
+
+// barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain; then the tensor-memory slot,
+// flags, the column sums [4][kGN] and the epilogue warps' staging [4][32][kGStageRow] fp16
 size_t gemm_smem_bytes() {
-  return 1024 + kGStages * (kGStageA + kGStageB) + (2 * kGStages + 5) * 8 + 32 + 4 * kGN * sizeof(float);
+  return 1024 + kGStages * (kGStageA + kGStageB) + (2 * kGStages + 5) * 8 + 32 + 4 * kGN * sizeof(float) + 16 +
+         4 * 32 * kGStageRow * 2;
 }
+
+// Rows of the output that also go to a pinned pool, as the pool keeps them: output row
+// b * N + t (t >= N - cap) to slot t mod cap of [B][H][cap][d], column h * d + j to (h, j).
+struct PoolOut {
+  uint16_t* base;  // NULL: no pool output
+  int N, H, d, cap;
+};
 
 // Tile t of the grouped order: runs of kGGroup row tiles take each column tile in turn, so a B
 // tile is reused by the CTAs working on neighbouring t and the group's A tiles stay in L2.
@@ -73,7 +84,7 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant__ CUtensorMap map_a,
                                                            const __grid_constant__ CUtensorMap map_b,
                                                            __half* __restrict__ C, int M, int N, int K,
-                                                           float* __restrict__ colpart, int* err) {
+                                                           float* __restrict__ colpart, const PoolOut po, int* err) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -88,6 +99,9 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* epi_ok = reinterpret_cast<int*>(tmem_slot + 2);   // [2]: the epilogue warps' joint verdict
   float* csum = reinterpret_cast<float*>(tmem_slot + 4);  // [4][kGN] (scalar accesses only)
+  // [4][32][kGStageRow], on a 16-byte boundary (rows of 144 bytes keep every piece aligned)
+  __half* stage_all = reinterpret_cast<__half*>((reinterpret_cast<uintptr_t>(csum + 4 * kGN) + 15) &
+                                                ~static_cast<uintptr_t>(15));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_n = (N + kGN - 1) / kGN, tiles_m = (M + kGM - 1) / kGM;
   const int T = tiles_m * tiles_n;
@@ -210,6 +224,8 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant_
       gemm_tile(t, tiles_m, tiles_n, mt, ntile);
       const int m0 = mt * kGM, n0 = ntile * kGN;
       const int row = m0 + q * 32 + lane;
+      __half* stage = stage_all + (size_t)q * 32 * kGStageRow;
+      const int first = po.N > po.cap ? po.N - po.cap : 0;
       for (int ch = 0; ch < kGN / 32; ++ch) {
         const int c0 = n0 + ch * 32;
         uint32_t r[32];
@@ -228,16 +244,45 @@ __global__ void __launch_bounds__(kGThreads, 1) k_gemm_tn(const __grid_constant_
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-        if (row < M) {
-          uint32_t h[16];
+        uint32_t h[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
-            h[i] = *reinterpret_cast<const uint32_t*>(&p);
-          }
+        for (int i = 0; i < 16; ++i) {
+          const __half2 p = __floats2half2_rn(v[2 * i], v[2 * i + 1]);
+          h[i] = *reinterpret_cast<const uint32_t*>(&p);
+        }
+        if (C && row < M) {
           uint4* dst = reinterpret_cast<uint4*>(C + (size_t)row * N + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+        }
+        if (po.base) {
+          // 64 columns at a time through shared memory, so that the pool rows (far apart in
+          // host memory) go out as whole 128-byte pieces, eight lanes to a row
+          uint4* srow = reinterpret_cast<uint4*>(stage + (size_t)lane * kGStageRow + (ch & 1) * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) srow[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+          if ((ch & 1) || ch == kGN / 32 - 1 || c0 + 32 >= N) {
+            __syncwarp();
+            const int cb = c0 - (ch & 1) * 32;           // first column of the staged block
+            const int ncols = min(64, N - cb);           // 32 or 64 (N is a multiple of 32)
+            const int part = lane & 7;                   // 16-byte piece of a row
+            const int col = cb + part * 8;
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int rl = it * 4 + (lane >> 3);
+              const int grow = m0 + q * 32 + rl;
+              if (grow < M && part * 8 < ncols) {
+                const int t = grow % po.N, b = grow / po.N;
+                if (t >= first) {
+                  const int hh = col / po.d, j = col % po.d;
+                  uint4* dst = reinterpret_cast<uint4*>(
+                      po.base + ((((size_t)b * po.H + hh) * po.cap + t % po.cap) * po.d + j));
+                  *dst = *reinterpret_cast<const uint4*>(stage + (size_t)rl * kGStageRow + part * 8);
+                }
+              }
+            }
+            __syncwarp();
+          }
         }
         if (colpart) {
           // |C| of the stored fp16 values (rows past M are zero: the A tile is zero-filled
@@ -527,7 +572,7 @@ void prefill_layout(int B, int N, int H, int d, size_t* off_v, size_t* off_cp, s
 }
 
 ig_status gemm(cudaStream_t st, const uint16_t* A, const uint16_t* Bt, uint16_t* C, int M, int N, int K,
-               float* colpart) {
+               float* colpart, PoolOut po = PoolOut{nullptr, 1, 1, 1, 1}) {
   CUtensorMap ma, mb;
   ig_status r = make_map(&ma, A, M, K, kGM);
   if (r != IG_OK) return r;
@@ -540,7 +585,8 @@ ig_status gemm(cudaStream_t st, const uint16_t* A, const uint16_t* Bt, uint16_t*
   IG_REQUIRE(tiles < (1ll << 31), "GEMM too large for one launch");
   // persistent: one CTA per SM (its 197 KB of shared memory admit no second one)
   const int grid = (int)(tiles < sm_count(st) ? tiles : sm_count(st));
-  k_gemm_tn<<<grid, kGThreads, smem, st>>>(ma, mb, reinterpret_cast<__half*>(C), M, N, K, colpart, error_word());
+  k_gemm_tn<<<grid, kGThreads, smem, st>>>(ma, mb, reinterpret_cast<__half*>(C), M, N, K, colpart, po,
+                                           error_word());
   IG_CHECK_LAUNCH("prefill GEMM launch");
   return IG_OK;
 }
@@ -593,26 +639,20 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   const int M = B * N, Nn = H * d;
   const int mtiles = (M + kGM - 1) / kGM;
   IG_REQUIRE(mtiles <= 65535, "B*N too large for one launch");
-  SideStream* ss = nullptr;
-  ig_status r = side_stream(&ss);
-  if (r != IG_OK) return r;
-  std::lock_guard<std::mutex> lock(g_side_mu);
+  (void)Vt;
   const size_t le = (size_t)B * H * pool->cap * d;
-  // Step 1: K~ (with the per-tile column partials of |K~|); its pool rows go out on the side
-  // stream while V is projected, then V's while the columns are chosen
-  r = gemm(st, X, Wk_t, Kt, M, Nn, D, colpart);
+  // Step 1: K~ (with the per-tile column partials of |K~|) and V; the GEMMs' epilogues write the
+  // rows the pool keeps straight to it (V goes nowhere else)
+  ig_status r = gemm(st, X, Wk_t, Kt, M, Nn, D, colpart,
+                     PoolOut{pool->Kdev + (size_t)layer * le, N, H, d, pool->cap});
   if (r != IG_OK) return r;
-  r = fork_pool_rows(st, ss, 0, Kt, B, N, H, d, pool->cap, pool->Kdev + (size_t)layer * le);
-  if (r != IG_OK) return r;
-  r = gemm(st, X, Wv_t, Vt, M, Nn, D, nullptr);
-  if (r != IG_OK) return r;
-  r = fork_pool_rows(st, ss, 1, Vt, B, N, H, d, pool->cap, pool->Vdev + (size_t)layer * le);
+  r = gemm(st, X, Wv_t, nullptr, M, Nn, D, nullptr, PoolOut{pool->Vdev + (size_t)layer * le, N, H, d, pool->cap});
   if (r != IG_OK) return r;
   // Step 2: the columns
   k_choose_cols<<<H, d, d * sizeof(double), st>>>(reinterpret_cast<const __half*>(Wq_t), D, H, d, k, colpart, mtiles,
                                                   cols, nullptr);
   IG_CHECK_LAUNCH("column choice launch");
-  // Step 3: the partial weight and the partial key cache; then wait for the pool rows
+  // Step 3: the partial weight and the partial key cache
   k_extract_rows<<<H * k, 128, 0, st>>>(reinterpret_cast<const uint4*>(Wq_t), D, d, k, cols,
                                         reinterpret_cast<uint4*>(Wq_part_t), error_word());
   IG_CHECK_LAUNCH("partial weight launch");
@@ -620,7 +660,7 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   k_partial_keys<<<sg, 256, kScTok * d * 2, st>>>(reinterpret_cast<const __half*>(Kt), N, H, d, k, pool->cap, Lcap,
                                                  cols, reinterpret_cast<__half*>(Kpart), error_word());
   IG_CHECK_LAUNCH("partial keys launch");
-  return join_side(st, ss);
+  return IG_OK;
 }
 
 extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,
@@ -681,9 +721,8 @@ extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int laye
   IG_CHECK_LAUNCH("rope-skew launch");
   r = fork_pool_rows(st, ss, 0, Kt, B, N, H, d, pool->cap, pool->Kdev + (size_t)layer * le);
   if (r != IG_OK) return r;
-  r = gemm(st, X, Wv_t, Vt, M, Nn, D, nullptr);
-  if (r != IG_OK) return r;
-  r = fork_pool_rows(st, ss, 1, Vt, B, N, H, d, pool->cap, pool->Vdev + (size_t)layer * le);
+  (void)Vt;  // V's pool rows come from the GEMM's epilogue
+  r = gemm(st, X, Wv_t, nullptr, M, Nn, D, nullptr, PoolOut{pool->Vdev + (size_t)layer * le, N, H, d, pool->cap});
   if (r != IG_OK) return r;
   // Step 2: the columns (W~_Q from Wq_t, the keys' partials over 64-row tiles)
   k_choose_cols<<<H, d, d * sizeof(double), st>>>(reinterpret_cast<const __half*>(Wq_t), D, H, d, k, colpart, mt,
