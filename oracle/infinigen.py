@@ -36,6 +36,9 @@ Readings taken where the page is silent or garbled (each is listed in the design
     row of keys and values is stored as e4m3 codes with one float32 scale, amax / 448, the
     codes being round-to-nearest-even e4m3 (saturating at 448) of x * (448 / amax) in float32;
     a row of zeros keeps scale 0; the partial key cache stays float16;
+  * the INT4 pool: the same record idea with signed 4-bit codes in [-7, 7], scale amax / 7,
+    codes the nearest integers (ties to even) of x * (7 / amax) in float32, two codes per byte
+    (even element in the low nibble);
   * speculation fidelity: recall@c counts the speculated tokens whose real score is at least
     the c-th largest real score (c = the speculated count; ties at that score count as hits);
     the captured fraction is the share of sum_t sum_c |q_c k_tc| that the partial columns hold.
@@ -674,6 +677,57 @@ def fp8_dequantize_rows(codes, scales):
     codes = np.asarray(codes)
     table = np.array([0.0 if (c & 0x7F) == 0x7F else e4m3_decode(c) for c in range(256)], dtype=np.float32)
     vals = table[codes] * np.asarray(scales, dtype=np.float32)[..., None]
+    return vals.astype(np.float32).astype(np.float16)
+
+
+# ----------------------------------------------------------------------------------------
+# INT4 pool rows (the follow-up's own format: selective prefetch of a 4-bit pool)
+# ----------------------------------------------------------------------------------------
+INT4_MAX = 7
+
+
+def int4_quantize_rows(X):
+    """Rows (last axis) of float16 X -> (signed codes int8 in [-7, 7], float32 scales): the
+    row's scale is amax / 7, its codes the nearest integers (ties to even) to x * (7 / amax)
+    in float32; a row of zeros keeps scale 0 and zero codes."""
+    X = np.asarray(X, dtype=np.float16).astype(np.float32)
+    flat = X.reshape(-1, X.shape[-1])
+    codes = np.zeros(flat.shape, dtype=np.int8)
+    scales = np.zeros(flat.shape[0], dtype=np.float32)
+    for r in range(flat.shape[0]):
+        amax = np.float32(np.abs(flat[r]).max())
+        if amax == 0:
+            continue
+        inv = np.float32(np.float32(INT4_MAX) / amax)
+        scales[r] = np.float32(amax / np.float32(INT4_MAX))
+        v = (flat[r] * inv).astype(np.float32)
+        codes[r] = np.clip(np.rint(v), -INT4_MAX, INT4_MAX).astype(np.int8)
+    return codes.reshape(X.shape), scales.reshape(X.shape[:-1])
+
+
+def int4_pack(codes):
+    """Signed 4-bit codes (last axis even) -> bytes: element 2j in the low nibble of byte j,
+    element 2j + 1 in the high one, each as its two's-complement low four bits."""
+    c = (np.asarray(codes).astype(np.int16) & 0xF).astype(np.uint8)
+    return (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+
+
+def int4_unpack(packed):
+    """Inverse of int4_pack: bytes -> signed codes int8."""
+    p = np.asarray(packed, dtype=np.uint8)
+    lo = (p & 0xF).astype(np.int8)
+    hi = (p >> 4).astype(np.int8)
+    lo = np.where(lo > 7, lo - 16, lo).astype(np.int8)
+    hi = np.where(hi > 7, hi - 16, hi).astype(np.int8)
+    out = np.empty(p.shape[:-1] + (2 * p.shape[-1],), dtype=np.int8)
+    out[..., 0::2] = lo
+    out[..., 1::2] = hi
+    return out
+
+
+def int4_dequantize_rows(codes, scales):
+    """float16 rows: float32(code) * scale, rounded to float16."""
+    vals = np.asarray(codes, dtype=np.float32) * np.asarray(scales, dtype=np.float32)[..., None]
     return vals.astype(np.float32).astype(np.float16)
 
 

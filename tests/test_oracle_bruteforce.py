@@ -332,3 +332,55 @@ def test_fp8_rows_scale_and_error_bound():
     assert np.all(np.abs(Yf - Xf) <= np.maximum(np.abs(Xf) * 2.0 ** -4, amax / 448 * 2.0 ** -9) + 1e-3 * amax + 1e-6)
     r = np.unravel_index(np.abs(Xf[1, 2]).argmax(), (64,))
     assert ora.e4m3_decode(codes[1, 2][r]) in (448.0, -448.0)
+
+
+# --- INT4 pool rows -----------------------------------------------------------------------------
+def test_int4_rows_exact_on_integer_rows_and_zero_rows():
+    # amax = 7: the reciprocal 7/7 and the scale 7/7 are exactly 1, so integer rows in [-7, 7]
+    # are their own codes and decode back exactly
+    g = np.random.default_rng(2)
+    X = g.integers(-7, 8, size=(4, 32)).astype(np.float16)
+    X[:, 0] = 7
+    X[3] = 0
+    codes, scales = ora.int4_quantize_rows(X)
+    assert np.array_equal(scales[:3], np.ones(3, np.float32)) and scales[3] == 0
+    assert np.array_equal(codes[:3].astype(np.int64), X[:3].astype(np.int64)) and not codes[3].any()
+    assert np.array_equal(ora.int4_dequantize_rows(codes, scales), X)
+
+
+def test_int4_rows_rounding_symmetry_and_error_bound():
+    g = np.random.default_rng(3)
+    X = (g.standard_normal((6, 128)) * g.uniform(0.01, 50, (6, 1))).astype(np.float16)
+    codes, scales = ora.int4_quantize_rows(X)
+    codes_neg, scales_neg = ora.int4_quantize_rows(-X)
+    assert np.array_equal(scales, scales_neg) and np.array_equal(codes_neg, -codes)  # ties to even: symmetric
+    assert codes.min() >= -7 and codes.max() <= 7
+    Xf = X.astype(np.float64)
+    amax = np.abs(Xf).max(-1)
+    for r in range(6):  # the largest element maps to +-7
+        assert abs(int(codes[r, np.abs(Xf[r]).argmax()])) == 7
+    # brute force: each code is the integer nearest x / scale (within the float32 rounding of
+    # the reciprocal), so the reconstruction is within half a step
+    step = amax / 7
+    Y = ora.int4_dequantize_rows(codes, scales).astype(np.float64)
+    assert np.all(np.abs(Y - Xf) <= step[:, None] * (0.5 + 1e-5) + np.abs(Y) * 2.0 ** -11)
+    for r in range(6):
+        for i in range(128):
+            cand = [c for c in range(-7, 8)]
+            dist = [abs(c * step[r] - Xf[r, i]) for c in cand]
+            best = min(dist)
+            assert abs(int(codes[r, i]) * step[r] - Xf[r, i]) <= best + 1e-6 * step[r]
+
+
+def test_int4_packing_nibble_order():
+    codes = np.array([[1, -1, 7, -7, 0, -8 + 1, 3, -2]], dtype=np.int8)
+    packed = ora.int4_pack(codes)
+    # written out by hand: byte j = (code[2j] & 15) | (code[2j+1] & 15) << 4
+    want = []
+    for j in range(4):
+        a, b = int(codes[0, 2 * j]), int(codes[0, 2 * j + 1])
+        want.append((a & 15) | ((b & 15) << 4))
+    assert packed.tolist() == [want] == [[0xF1, 0x97, 0x90, 0xE3]]
+    g = np.random.default_rng(4)
+    c = g.integers(-7, 8, size=(5, 64)).astype(np.int8)
+    assert np.array_equal(ora.int4_unpack(ora.int4_pack(c)), c)
