@@ -57,6 +57,8 @@ def parse_args(argv=None):
                    help="1: each layer's append runs on the fetch stream right after its gather")
     p.add_argument("--pool-fp8", type=int, default=0,
                    help="1: the host pool holds e4m3 rows with a per-row scale (d + 4 bytes per row)")
+    p.add_argument("--pool-int4", type=int, default=0,
+                   help="1: the host pool holds signed 4-bit rows with a per-row scale (d/2 + 4 bytes per row)")
     p.add_argument("--fused-fetch", type=int, default=0,
                    help="1: layers 1.. attend straight from the pinned pool on the fetch stream (no staging)")
     p.add_argument("--sm-split", type=int, default=0,
@@ -319,7 +321,7 @@ def link_peak_gbs(torch) -> float:
 
 def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True,
                   fused_fetch=False, pool_policy=0, policy=0, pool_fp8=False, batched_append=False,
-                  append_on_fetch=False, sm_split=0):
+                  append_on_fetch=False, sm_split=0, pool_int4=False):
     from speculative_kv_cache_gb300.decoder import Decoder
 
     Lcap = w.lcap
@@ -328,7 +330,8 @@ def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False
                   stage_timing=True, graph=bool(graph), fused_select=bool(fused_select),
                   fused_fetch=bool(fused_fetch), pool_policy=pool_policy, policy=policy,
                   pool_fp8=bool(pool_fp8), batched_append=bool(batched_append),
-                  append_on_fetch=bool(append_on_fetch), sm_split=sm_split, device=device)
+                  append_on_fetch=bool(append_on_fetch), sm_split=sm_split, pool_int4=bool(pool_int4),
+                  device=device)
     gen = torch.Generator(device=device)
     shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
@@ -435,7 +438,8 @@ def run_ours(args, w, alpha):
               "normalized": ig.IG_SEL_NORMALIZED}[args.policy]
     dec, xs, qs, kns, vns = setup_decoder(torch, w, alpha, args.gather_ctas, device, steps_total, args.graph,
                                           args.fused_select, fused_fetch, pool_policy, policy, args.pool_fp8,
-                                          args.batched_append, args.append_on_fetch, args.sm_split)
+                                          args.batched_append, args.append_on_fetch, args.sm_split,
+                                          args.pool_int4)
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
@@ -484,7 +488,9 @@ def run_ours(args, w, alpha):
     sel_rows = cnts[:, 1:].sum()                                          # layers 1.. gather
     ctx = np.array([w.prompt + args.warmup + i for i in range(args.steps)], dtype=np.float64)
     f = sel_rows / (args.steps * (w.layers - 1) * w.batch * w.heads * ctx.mean())
-    row_link = 2 * (w.head_dim + 4) if args.pool_fp8 else 2 * w.head_dim * 2  # K + V bytes of a row
+    # K + V bytes of a row over the link (codes and scales of a quantized row)
+    row_link = (2 * (w.head_dim + 4) if args.pool_fp8 else 2 * (w.head_dim // 2 + 4) if args.pool_int4
+                else 2 * w.head_dim * 2)
     G_total = sel_rows * row_link                                         # over the link
     gather_ms_per_launch = stage[0] / max(stage_n[0], 1)
     G_per_launch = G_total / max(stage_n[0], 1)
@@ -539,7 +545,8 @@ def run_ours(args, w, alpha):
             "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph),
                            fused_select=bool(args.fused_select), fused_fetch=fused_fetch,
                            selection=args.policy, batched_append=bool(args.batched_append),
-                           append_on_fetch=bool(args.append_on_fetch), pool_dtype="fp8-e4m3 + fp32 row scale" if args.pool_fp8 else "fp16",
+                           append_on_fetch=bool(args.append_on_fetch), pool_dtype=("fp8-e4m3 + fp32 row scale" if args.pool_fp8 else
+                                       "int4 + fp32 row scale" if args.pool_int4 else "fp16"),
                            pool_policy=args.pool_policy if w.pool_frac < 1 else None,
                            sm_split=({"fetch_sms": dec.fetch_sms, "compute_sms": dec.compute_sms}
                                      if args.sm_split else None)),
@@ -556,11 +563,14 @@ def run_ours(args, w, alpha):
                                   ("append" if fused_fetch else "attend_append"): stage[2] / args.steps},
             "e2e": e2e,
             "gpu_launches": int(launches),
-            "roofline": {"kernel": ("k5_fetch_attend + combine (fused zero-copy fetch + attention)"
-                                    if fused_fetch else "k4_gather (zero-copy fetch of the selected K/V rows)"),
+            "roofline": {"kernel": ("k5_fetch_attend + combine (fused zero-copy fetch + attention)" if fused_fetch
+                                    else "k4_gather_q (zero-copy fetch and dequantization of the selected rows)"
+                                    if (args.pool_fp8 or args.pool_int4)
+                                    else "k4_gather (zero-copy fetch of the selected K/V rows)"),
                          "bound": "host-link", "achieved": achieved, "peak": link,
                          "unit": "GB/s", "frac": achieved / link,
-                         "traffic": None if fused_fetch else gather_traffic_bytes(),
+                         "traffic": (None if (fused_fetch or args.pool_fp8 or args.pool_int4)
+                                     else gather_traffic_bytes()),
                          "traffic_note": "DRAM read+write bytes per launch (ncu, same per-layer shape); "
                                          "the kernel's algorithmic bytes cross the host link, not DRAM",
                          "peak_source": "measured in this run: pinned host->device copy, best of 5 x 1 GiB",

@@ -235,12 +235,19 @@ typedef struct ig_pool ig_pool;
  * 0.  ig_gather_kv reads one contiguous record per selected row and dequantizes it (code value x
  * scale, rounded to fp16) into the usual fp16 staging rows, so the link carries 2d + 16 bytes
  * per row instead of 4d; the partial key cache (speculation) stays fp16.  d must be 64 or 128;
- * ig_pool_kv and ig_gather_attend refuse fp8 pools (use ig_pool_kv8). */
+ * ig_pool_kv, ig_gather_attend and the prefill refuse quantized pools (use ig_pool_kv8). */
 #define IG_POOL_FP8 2
+/* IG_POOL_INT4: the same record with signed 4-bit codes (the format the follow-up work names):
+ * d / 2 bytes of key codes, d / 2 of value codes, the two fp32 scales, 8 bytes of padding
+ * (d + 16 bytes).  scale = amax / 7, codes = the nearest integer (ties to even) of x * (7 / amax)
+ * in fp32, in [-7, 7], two per byte with element 2j in the low nibble of byte j (two's
+ * complement); a row of zeros has scale 0.  The gather dequantizes as for IG_POOL_FP8; the link
+ * carries d + 16 bytes per row.  Excludes IG_POOL_FP8; d must be 64 or 128. */
+#define IG_POOL_INT4 4
 
 ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out);
-/* ig_pool_create with a victim policy (IG_POOL_COUNTER/FIFO/LRU) and flags (0, IG_POOL_NO_STORAGE
- * or IG_POOL_FP8). */
+/* ig_pool_create with a victim policy (IG_POOL_COUNTER/FIFO/LRU) and flags (0, IG_POOL_NO_STORAGE,
+ * IG_POOL_FP8 or IG_POOL_INT4). */
 ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap, int policy, int flags,
                             ig_pool** out);
 ig_status ig_pool_destroy(ig_pool* pool);
@@ -248,13 +255,14 @@ ig_status ig_pool_destroy(ig_pool* pool);
 /* Host pointers (also valid on the device) to one layer's K and V arrays. */
 ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V);
 
-/* fp8 pools: host pointer (also valid on the device) to one layer's records
- * [B][H][cap][record_bytes] (layout under IG_POOL_FP8) and the record size (2d + 16). */
+/* Quantized (fp8 or int4) pools: host pointer (also valid on the device) to one layer's records
+ * [B][H][cap][record_bytes] (layouts under IG_POOL_FP8 and IG_POOL_INT4) and the record size
+ * (2d + 16 or d + 16). */
 ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** records, int* record_bytes);
 
 /* Copies one layer's K and V ([B][H][cap][d] fp16 each, from device or host memory) into
- * the pool, asynchronously on `stream`.  An fp8 pool quantizes them in a kernel, so for it the
- * source must be device memory or pinned host memory. */
+ * the pool, asynchronously on `stream`.  A quantized pool quantizes them in a kernel, so for it
+ * the source must be device memory or pinned host memory. */
 ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const uint16_t* K,
                         const uint16_t* V);
 
@@ -353,7 +361,7 @@ ig_status ig_gather_attend(void* stream, const ig_pool* pool, int layer, int B, 
  *   cols    host array [layers] of dev int32 [H][ks[l]] (entries may be NULL with Kpart[l])
  *   k_new, v_new  dev fp16 [layers][B][H][d]
  *   Kpart   host array [layers] of dev fp16 [B][H][ks[l]][Lcap] or NULL entries; may be NULL
- * At most 128 layers per call; fp8 pools quantize the rows as ig_append_kv does. */
+ * At most 128 layers per call; quantized pools quantize the rows as ig_append_kv does. */
 ig_status ig_append_kv_layers(void* stream, ig_pool* pool, int layers, int B, int H, int d,
                               const int* ks, int Lcap, const int32_t* slot,
                               const int32_t* const* cols, const uint16_t* k_new,

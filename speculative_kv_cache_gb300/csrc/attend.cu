@@ -546,7 +546,7 @@ extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int lay
                                       void* workspace, size_t workspace_bytes, int max_ctas) {
   IG_REQUIRE(pool, "null pool");
   IG_REQUIRE(pool->storage, "the pool was created without storage");
-  IG_REQUIRE(!pool->fp8, "fused fetch + attention reads fp16 pools only");
+  IG_REQUIRE(!pool->qbits, "fused fetch + attention reads fp16 pools only");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
   IG_REQUIRE(B > 0 && H > 0 && Lcap > 0, "B, H, Lcap must be positive");

@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kGatherThreads = 256;
 constexpr int kUnroll = 8;  // 8 rows x (K, V) in flight per lane: 205 GB/s alone at 38 CTAs
-constexpr int kUnroll8 = 16;  // fp8 records: one 16-byte load per lane and row, so twice the rows
+constexpr int kUnroll8 = 16;  // quantized records: one 16-byte load per lane and row, so twice the rows
 constexpr int kMaxGatherUnits = 32768;  // (units + 1) ints of shared memory: 128 KB
 
 __global__ void __launch_bounds__(kGatherThreads) k4_gather(
@@ -117,12 +117,15 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather(
   }
 }
 
-// FP8 pool (one record per (token, head): K codes, V codes, their two fp32 scales): the same
-// balanced row split; a row is one contiguous record of 2d + 16 bytes, read by 2d/16 lanes (16
-// codes each: the first d/16 lanes the key, the rest the value) plus each lane's 4-byte scale
-// from the same record, and dequantized to fp16 (code value x scale, rounded to nearest) into
-// the usual staging layout.
-__global__ void __launch_bounds__(kGatherThreads) k4_gather_fp8(
+// Quantized pool (one record per (token, head): K codes, V codes, their two fp32 scales): the
+// same balanced row split; a row is one contiguous record of 2 d BITS / 8 + 16 bytes, read by
+// vpr = 2 d BITS / 128 lanes (16 bytes of codes each: the first half of the lanes the key, the
+// rest the value) plus each lane's 4-byte scale from the same record, and dequantized to fp16
+// (code value x scale in fp32, rounded to nearest) into the usual staging layout.  BITS = 8:
+// 16 e4m3 codes per lane; BITS = 4: 32 signed 4-bit codes per lane (element 2j in the low
+// nibble of byte j).
+template <int BITS>
+__global__ void __launch_bounds__(kGatherThreads) k4_gather_q(
     const uint8_t* __restrict__ Rec, int rec, int units, int cap, int vpr, int Lcap, const int32_t* __restrict__ idx,
     const int32_t* __restrict__ cnt, uint4* __restrict__ Kg, uint4* __restrict__ Vg, int* err) {
   extern __shared__ int pre[];
@@ -169,9 +172,10 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather_fp8(
     }
     u = lo;
   }
+  constexpr int OUT = BITS == 8 ? 2 : 4;  // 16-byte fp16 pieces a lane writes
   const int half = vpr / 2;            // lanes of the key codes
   const bool is_v = v >= half;
-  const int cv = is_v ? v - half : v;   // chunk of 16 codes within K or V
+  const int cv = is_v ? v - half : v;   // 16-byte chunk of codes within K or V
   uint4* out = is_v ? Vg : Kg;
   for (int r = r0 + rg; r < r1; r += rpp * kUnroll8) {
     uint4 cd[kUnroll8];
@@ -203,21 +207,33 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather_fp8(
 #pragma unroll
     for (int q = 0; q < kUnroll8; ++q) {
       if (slot[q] < 0) continue;
-      const size_t dst = ((size_t)unit[q] * Lcap + row[q]) * (2 * half) + 2 * cv;
+      const size_t dst = ((size_t)unit[q] * Lcap + row[q]) * (OUT * half) + OUT * cv;
       const uint32_t w4[4] = {cd[q].x, cd[q].y, cd[q].z, cd[q].w};
-      uint32_t o[8];
+      uint32_t o[4 * OUT];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        // two codes at a time: exact fp16 values of the codes, then x scale in fp32
-        const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] & 0xffffu), __NV_E4M3);
-        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] >> 16), __NV_E4M3);
-        const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
-        const __half2 ra = __floats2half2_rn(a.x * sc[q], a.y * sc[q]), rb = __floats2half2_rn(b.x * sc[q], b.y * sc[q]);
-        o[2 * i] = *reinterpret_cast<const uint32_t*>(&ra);
-        o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&rb);
+        if constexpr (BITS == 8) {
+          // two codes at a time: exact fp16 values of the codes, then x scale in fp32
+          const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] & 0xffffu), __NV_E4M3);
+          const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w4[i] >> 16), __NV_E4M3);
+          const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+          const __half2 ra = __floats2half2_rn(a.x * sc[q], a.y * sc[q]);
+          const __half2 rb = __floats2half2_rn(b.x * sc[q], b.y * sc[q]);
+          o[2 * i] = *reinterpret_cast<const uint32_t*>(&ra);
+          o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&rb);
+        } else {
+          // eight signed nibbles: shift each to the top and back, sign-extending
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int c0 = (int)(w4[i] << (28 - 8 * j)) >> 28;
+            const int c1 = (int)(w4[i] << (24 - 8 * j)) >> 28;
+            const __half2 r = __floats2half2_rn((float)c0 * sc[q], (float)c1 * sc[q]);
+            o[4 * i + j] = *reinterpret_cast<const uint32_t*>(&r);
+          }
+        }
       }
-      out[dst] = make_uint4(o[0], o[1], o[2], o[3]);
-      out[dst + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+      for (int i = 0; i < OUT; ++i) out[dst + i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
     }
   }
 }
@@ -249,17 +265,18 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
     cudaError_t e = cudaFuncSetAttribute(k4_gather, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "gather smem attribute");
   }
-  if (pool->fp8) {
-    const int vpr8 = 2 * d / 16;  // lanes per fp8 record (16 codes each: K, then V)
+  if (pool->qbits) {
+    const int vprq = 2 * (d * pool->qbits / 8) / 16;  // lanes per record (16 bytes of codes each: K, then V)
+    auto kern = pool->qbits == 8 ? k4_gather_q<8> : k4_gather_q<4>;
     if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(k4_gather_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return cuda_fail(e, "gather smem attribute");
     }
     const size_t rows = (size_t)B * H * pool->cap, r0 = (size_t)layer * rows;
-    k4_gather_fp8<<<grid, kGatherThreads, smem, as_stream(stream)>>>(
-        pool->R + r0 * pool->rec, pool->rec, units, pool->cap, vpr8, Lcap, idx, cnt, reinterpret_cast<uint4*>(Kg),
+    kern<<<grid, kGatherThreads, smem, as_stream(stream)>>>(
+        pool->R + r0 * pool->rec, pool->rec, units, pool->cap, vprq, Lcap, idx, cnt, reinterpret_cast<uint4*>(Kg),
         reinterpret_cast<uint4*>(Vg), error_word());
-    IG_CHECK_LAUNCH("fp8 gather launch");
+    IG_CHECK_LAUNCH("quantized gather launch");
     return IG_OK;
   }
   const size_t layer_elems = (size_t)B * H * pool->cap * d;

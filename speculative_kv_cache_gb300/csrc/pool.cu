@@ -70,11 +70,15 @@ __global__ void k6_append(uint4* __restrict__ Kp, uint4* __restrict__ Vp, int ca
   }
 }
 
-// One warp quantizes one row of d fp16 values (d = 32 * PER) to e4m3 codes with the row's
-// scale amax / 448: codes = RN-even e4m3, saturating, of x * (448 / amax) in fp32; a row of
-// zeros gets scale 0 and zero codes.
-template <int PER>
+// One warp quantizes one row of d fp16 values (d = 32 * PER, lane i holding elements
+// PER i .. PER i + PER - 1) with one fp32 scale per row; a row of zeros gets scale 0 and zero
+// codes.  BITS = 8: e4m3 codes, scale amax / 448, codes = RN-even e4m3, saturating, of
+// x * (448 / amax) in fp32.  BITS = 4: signed codes in [-7, 7], scale amax / 7, codes = the
+// nearest integer (ties to even) of x * (7 / amax) in fp32, two per byte, element 2j in the low
+// nibble of byte j.  The codes take d * BITS / 8 bytes.
+template <int BITS, int PER>
 __device__ void quantize_row(const __half* __restrict__ x, uint8_t* __restrict__ codes, float* __restrict__ scale) {
+  constexpr float kMax = BITS == 8 ? 448.f : 7.f;
   const int lane = threadIdx.x & 31;
   float v[PER];
   float amax = 0.f;
@@ -86,37 +90,45 @@ __device__ void quantize_row(const __half* __restrict__ x, uint8_t* __restrict__
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   uint32_t packed = 0;
   if (amax > 0.f) {
-    const float inv = 448.f / amax;
+    const float inv = kMax / amax;
 #pragma unroll
-    for (int i = 0; i < PER; ++i)
-      packed |= (uint32_t)__nv_cvt_float_to_fp8(v[i] * inv, __NV_SATFINITE, __NV_E4M3) << (8 * i);
+    for (int i = 0; i < PER; ++i) {
+      if constexpr (BITS == 8) {
+        packed |= (uint32_t)__nv_cvt_float_to_fp8(v[i] * inv, __NV_SATFINITE, __NV_E4M3) << (8 * i);
+      } else {
+        const int c = min(7, max(-7, __float2int_rn(v[i] * inv)));
+        packed |= (uint32_t)(c & 0xF) << (4 * i);
+      }
+    }
   }
-  if (PER == 4) reinterpret_cast<uint32_t*>(codes)[lane] = packed;
-  else reinterpret_cast<uint16_t*>(codes)[lane] = (uint16_t)packed;
-  if (lane == 0) *scale = amax > 0.f ? amax / 448.f : 0.f;
+  constexpr int kBytes = PER * BITS / 8;  // per lane: 4 or 2 (fp8), 2 or 1 (int4)
+  if constexpr (kBytes == 4) reinterpret_cast<uint32_t*>(codes)[lane] = packed;
+  else if constexpr (kBytes == 2) reinterpret_cast<uint16_t*>(codes)[lane] = (uint16_t)packed;
+  else codes[lane] = (uint8_t)packed;
+  if (lane == 0) *scale = amax > 0.f ? amax / kMax : 0.f;
 }
 
-// Pool write of an fp8 pool: rows [rows][d] fp16 (device-accessible) -> records (K and V codes,
-// then their scales).
-template <int PER>
+// Pool write of a quantized pool: rows [rows][d] fp16 (device-accessible) -> records (K and V
+// codes, then their scales).
+template <int BITS, int PER>
 __global__ void k_quantize_rows(const __half* __restrict__ K, const __half* __restrict__ V, size_t rows,
                                 uint8_t* __restrict__ R, int rec) {
-  constexpr int D = 32 * PER;
+  constexpr int D = 32 * PER, CB = D * BITS / 8;
   const size_t r = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (r >= rows) return;
   uint8_t* rr = R + r * rec;
-  float* sc = reinterpret_cast<float*>(rr + 2 * D);
-  quantize_row<PER>(K + r * D, rr, sc);
-  quantize_row<PER>(V + r * D, rr + D, sc + 1);
+  float* sc = reinterpret_cast<float*>(rr + 2 * CB);
+  quantize_row<BITS, PER>(K + r * D, rr, sc);
+  quantize_row<BITS, PER>(V + r * D, rr + CB, sc + 1);
 }
 
-// Append into an fp8 pool: one warp per (b, h) quantizes the current token's key and value into
-// its record.
-template <int PER>
-__global__ void k6_append_fp8(uint8_t* __restrict__ R, int rec, int units, int cap, int H,
-                              const int32_t* __restrict__ slot, const __half* __restrict__ k_new,
-                              const __half* __restrict__ v_new, int* err) {
-  constexpr int D = 32 * PER;
+// Append into a quantized pool: one warp per (b, h) quantizes the current token's key and value
+// into its record.
+template <int BITS, int PER>
+__global__ void k6_append_q(uint8_t* __restrict__ R, int rec, int units, int cap, int H,
+                            const int32_t* __restrict__ slot, const __half* __restrict__ k_new,
+                            const __half* __restrict__ v_new, int* err) {
+  constexpr int D = 32 * PER, CB = D * BITS / 8;
   const int bh = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (bh >= units) return;
   const int sl = slot[bh / H];
@@ -126,14 +138,14 @@ __global__ void k6_append_fp8(uint8_t* __restrict__ R, int rec, int units, int c
     return;
   }
   uint8_t* rr = R + ((size_t)bh * cap + sl) * rec;
-  float* sc = reinterpret_cast<float*>(rr + 2 * D);
-  quantize_row<PER>(k_new + (size_t)bh * D, rr, sc);
-  quantize_row<PER>(v_new + (size_t)bh * D, rr + D, sc + 1);
+  float* sc = reinterpret_cast<float*>(rr + 2 * CB);
+  quantize_row<BITS, PER>(k_new + (size_t)bh * D, rr, sc);
+  quantize_row<BITS, PER>(v_new + (size_t)bh * D, rr + CB, sc + 1);
 }
 
 // Appends of every layer's current token in one launch (grid: (b, h) x layer), run once the
 // step's fetches are done: layer 0 to the dense rows when given, other layers to the pool
-// (Q = 0: fp16 rows by 16-byte copies; Q = 2 or 4: fp8 rows quantized by the first two warps),
+// (BITS = 0: fp16 rows by 16-byte copies; BITS = 8 or 4: quantized rows, the first two warps),
 // and each layer's chosen columns to its partial key cache.
 constexpr int kMaxAppendLayers = 128;
 struct AppendLayers {
@@ -142,7 +154,7 @@ struct AppendLayers {
   int k[kMaxAppendLayers];
 };
 
-template <int Q>
+template <int BITS, int PER>
 __global__ void __launch_bounds__(64) k6_append_layers(
     const AppendLayers P, uint4* __restrict__ Kp, uint4* __restrict__ Vp, uint8_t* __restrict__ R, int rec,
     int cap, int H, int d, int Lcap,
@@ -169,17 +181,17 @@ __global__ void __launch_bounds__(64) k6_append_layers(
       return;
     }
     const size_t row = ((size_t)l * units + bh) * cap + sl;
-    if (Q == 0) {
+    if constexpr (BITS == 0) {
       for (int v = threadIdx.x; v < vpr; v += blockDim.x) {
         Kp[row * vpr + v] = reinterpret_cast<const uint4*>(kn)[v];
         Vp[row * vpr + v] = reinterpret_cast<const uint4*>(vn)[v];
       }
     } else {
-      constexpr int PER = Q > 0 ? Q : 1;
+      constexpr int CB = 32 * PER * BITS / 8;
       uint8_t* rr = R + row * rec;
-      float* sc = reinterpret_cast<float*>(rr + 2 * d);
-      if (threadIdx.x < 32) quantize_row<PER>(kn, rr, sc);
-      else quantize_row<PER>(vn, rr + d, sc + 1);
+      float* sc = reinterpret_cast<float*>(rr + 2 * CB);
+      if (threadIdx.x < 32) quantize_row<BITS, PER>(kn, rr, sc);
+      else quantize_row<BITS, PER>(vn, rr + CB, sc + 1);
     }
   }
   __half* kp = P.Kpart[l];
@@ -212,10 +224,11 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
   *out = nullptr;
   IG_REQUIRE(policy == IG_POOL_COUNTER || policy == IG_POOL_FIFO || policy == IG_POOL_LRU,
              "unknown pool policy %d", policy);
-  IG_REQUIRE((flags & ~(IG_POOL_NO_STORAGE | IG_POOL_FP8)) == 0, "unknown pool flags 0x%x", flags);
+  IG_REQUIRE((flags & ~(IG_POOL_NO_STORAGE | IG_POOL_FP8 | IG_POOL_INT4)) == 0, "unknown pool flags 0x%x", flags);
+  IG_REQUIRE(!((flags & IG_POOL_FP8) && (flags & IG_POOL_INT4)), "IG_POOL_FP8 and IG_POOL_INT4 exclude each other");
   const bool storage = !(flags & IG_POOL_NO_STORAGE);
-  const bool fp8 = storage && (flags & IG_POOL_FP8);
-  IG_REQUIRE(!fp8 || d == 64 || d == 128, "an fp8 pool needs d = 64 or 128");
+  const int qbits = !storage ? 0 : (flags & IG_POOL_FP8) ? 8 : (flags & IG_POOL_INT4) ? 4 : 0;
+  IG_REQUIRE(!qbits || d == 64 || d == 128, "a quantized pool needs d = 64 or 128");
   IG_REQUIRE(layers > 0 && B > 0 && cap > 0, "pool sizes must be positive");
   IG_REQUIRE(!storage || (H > 0 && d > 0), "a pool with storage needs H, d > 0");
   IG_REQUIRE(!storage || d % 8 == 0, "d must be a multiple of 8 (16-byte rows)");
@@ -237,14 +250,14 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
     // it is still obtained through cudaHostGetDevicePointer below for the fp16 rows
     auto alloc = [&](void** p, size_t bytes) { return cudaHostAlloc(p, bytes, hflags); };
     cudaError_t e;
-    if (fp8) {
-      p->fp8 = true;
-      p->rec = 2 * d + 16;
+    if (qbits) {
+      p->qbits = qbits;
+      p->rec = 2 * (d * qbits / 8) + 16;
       e = alloc(reinterpret_cast<void**>(&p->R), nrows * (size_t)p->rec);
       if (e != cudaSuccess) {
         cudaGetLastError();
         delete p;
-        return fail(IG_ERR_OOM, "pinned allocation of the fp8 pool (%zu bytes) failed: %s", nrows * (size_t)p->rec,
+        return fail(IG_ERR_OOM, "pinned allocation of the quantized pool (%zu bytes) failed: %s", nrows * (size_t)p->rec,
                     cudaGetErrorString(e));
       }
     } else {
@@ -310,7 +323,7 @@ extern "C" ig_status ig_pool_destroy(ig_pool* pool) {
 extern "C" ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V) {
   IG_REQUIRE(pool && K && V, "null argument");
   IG_REQUIRE(pool->storage, "the pool was created without storage");
-  IG_REQUIRE(!pool->fp8, "an fp8 pool has no fp16 rows (use ig_pool_kv8)");
+  IG_REQUIRE(!pool->qbits, "a quantized pool has no fp16 rows (use ig_pool_kv8)");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
   *K = pool->K + (size_t)layer * le;
@@ -320,7 +333,7 @@ extern "C" ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, ui
 
 extern "C" ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** records, int* record_bytes) {
   IG_REQUIRE(pool && records && record_bytes, "null argument");
-  IG_REQUIRE(pool->fp8, "not an fp8 pool");
+  IG_REQUIRE(pool->qbits, "not a quantized pool");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t rows = (size_t)pool->B * pool->H * pool->cap;
   *records = pool->R + (size_t)layer * rows * pool->rec;
@@ -335,14 +348,14 @@ extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
   cudaStream_t s = as_stream(stream);
-  if (pool->fp8) {
+  if (pool->qbits) {
     // the rows are quantized by a kernel, so they must be readable by the device
     for (const void* src : {(const void*)K, (const void*)V}) {
       cudaPointerAttributes at{};
       const cudaError_t e = cudaPointerGetAttributes(&at, src);
       if (e != cudaSuccess || at.type == cudaMemoryTypeUnregistered) {
         cudaGetLastError();
-        return fail(IG_ERR_INVALID, "writing an fp8 pool needs device or pinned source rows");
+        return fail(IG_ERR_INVALID, "writing a quantized pool needs device or pinned source rows");
       }
     }
     const size_t rows = (size_t)pool->B * pool->H * pool->cap;
@@ -352,11 +365,15 @@ extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const
     auto Kh = reinterpret_cast<const __half*>(K);
     auto Vh = reinterpret_cast<const __half*>(V);
     uint8_t* R0 = pool->R + r0 * pool->rec;
-    if (pool->d == 128)
-      k_quantize_rows<4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
-    else
-      k_quantize_rows<2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
-    IG_CHECK_LAUNCH("fp8 pool write launch");
+    const bool d128 = pool->d == 128;
+    if (pool->qbits == 8) {
+      if (d128) k_quantize_rows<8, 4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
+      else k_quantize_rows<8, 2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
+    } else {
+      if (d128) k_quantize_rows<4, 4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
+      else k_quantize_rows<4, 2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
+    }
+    IG_CHECK_LAUNCH("quantized pool write launch");
     return IG_OK;
   }
   cudaError_t e = cudaMemcpyAsync(pool->K + (size_t)layer * le, K, le * 2, cudaMemcpyDefault, s);
@@ -382,19 +399,23 @@ extern "C" ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B,
     IG_REQUIRE(pool->storage, "the pool was created without storage");
     IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
     IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
-    if (pool->fp8) {  // the quantized row goes to the pool here; the kernel below does the rest
+    if (pool->qbits) {  // the quantized row goes to the pool here; the kernel below does the rest
       const size_t rows = (size_t)B * H * pool->cap, r0 = (size_t)layer * rows;
       const int units = B * H, wpb = 8;
       auto kn = reinterpret_cast<const __half*>(k_new);
       auto vn = reinterpret_cast<const __half*>(v_new);
       uint8_t* R0 = pool->R + r0 * pool->rec;
-      if (d == 128)
-        k6_append_fp8<4><<<(units + wpb - 1) / wpb, 32 * wpb, 0, as_stream(stream)>>>(R0, pool->rec, units, pool->cap,
-                                                                                     H, slot, kn, vn, error_word());
-      else
-        k6_append_fp8<2><<<(units + wpb - 1) / wpb, 32 * wpb, 0, as_stream(stream)>>>(R0, pool->rec, units, pool->cap,
-                                                                                     H, slot, kn, vn, error_word());
-      IG_CHECK_LAUNCH("fp8 append launch");
+      const unsigned g = (unsigned)((units + wpb - 1) / wpb);
+      cudaStream_t s = as_stream(stream);
+      int* err = error_word();
+      if (pool->qbits == 8) {
+        if (d == 128) k6_append_q<8, 4><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, units, pool->cap, H, slot, kn, vn, err);
+        else k6_append_q<8, 2><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, units, pool->cap, H, slot, kn, vn, err);
+      } else {
+        if (d == 128) k6_append_q<4, 4><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, units, pool->cap, H, slot, kn, vn, err);
+        else k6_append_q<4, 2><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, units, pool->cap, H, slot, kn, vn, err);
+      }
+      IG_CHECK_LAUNCH("quantized append launch");
       if (!Kpart && !Kdense) return IG_OK;
     } else {
       const size_t le = (size_t)B * H * pool->cap * d;
@@ -437,15 +458,25 @@ extern "C" ig_status ig_append_kv_layers(void* stream, ig_pool* pool, int layers
   auto vn = reinterpret_cast<const __half*>(v_new);
   auto Kd = reinterpret_cast<uint4*>(Kdense);
   auto Vd = reinterpret_cast<uint4*>(Vdense);
-  if (!pool->fp8) {
-    k6_append_layers<0><<<grid, 64, 0, st>>>(P, reinterpret_cast<uint4*>(pool->Kdev), reinterpret_cast<uint4*>(pool->Vdev),
-                                            nullptr, 0, pool->cap, H, d, Lcap, units, slot, kn, vn, Kd, Vd, error_word());
-  } else if (d == 128) {
-    k6_append_layers<4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
-                                            slot, kn, vn, Kd, Vd, error_word());
+  int* err = error_word();
+  if (!pool->qbits) {
+    k6_append_layers<0, 1><<<grid, 64, 0, st>>>(P, reinterpret_cast<uint4*>(pool->Kdev),
+                                               reinterpret_cast<uint4*>(pool->Vdev), nullptr, 0, pool->cap, H, d, Lcap,
+                                               units, slot, kn, vn, Kd, Vd, err);
+  } else if (pool->qbits == 8) {
+    if (d == 128)
+      k6_append_layers<8, 4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+                                                 slot, kn, vn, Kd, Vd, err);
+    else
+      k6_append_layers<8, 2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+                                                 slot, kn, vn, Kd, Vd, err);
   } else {
-    k6_append_layers<2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
-                                            slot, kn, vn, Kd, Vd, error_word());
+    if (d == 128)
+      k6_append_layers<4, 4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+                                                 slot, kn, vn, Kd, Vd, err);
+    else
+      k6_append_layers<4, 2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+                                                 slot, kn, vn, Kd, Vd, err);
   }
   IG_CHECK_LAUNCH("batched append launch");
   return IG_OK;

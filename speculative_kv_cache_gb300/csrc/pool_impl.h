@@ -9,9 +9,10 @@ struct ig_pool {
   int layers = 0, B = 0, H = 0, d = 0, cap = 0;
   int policy = 0;            // IG_POOL_COUNTER, IG_POOL_FIFO or IG_POOL_LRU
   bool storage = true;       // false: the slot manager only, no K/V rows
-  bool fp8 = false;          // rows stored as e4m3 codes with one fp32 scale per row
-  uint8_t* R = nullptr;      // fp8 pools: pinned, mapped records [layers][B][H][cap][rec]:
-  int rec = 0;               //   K codes [d], V codes [d], K scale, V scale (fp32), 8 B pad
+  int qbits = 0;             // 0: fp16 rows; 8: e4m3 codes, 4: int4 codes, one fp32 scale per row
+  uint8_t* R = nullptr;      // quantized pools: pinned, mapped records [layers][B][H][cap][rec]:
+  int rec = 0;               //   K codes, V codes (d * qbits / 8 bytes each), K scale, V scale
+                             //   (fp32), 8 B pad
   uint16_t* K = nullptr;     // pinned, mapped host memory [layers][B][H][cap][d]
   uint16_t* V = nullptr;
   uint16_t* Kdev = nullptr;  // the same memory as seen from the device

@@ -615,7 +615,7 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
                                       const uint16_t* Wv_t, int32_t* cols, uint16_t* Wq_part_t, uint16_t* Kpart,
                                       void* workspace, size_t workspace_bytes) {
   IG_REQUIRE(pool, "null pool");
-  IG_REQUIRE(pool->storage && !pool->fp8, "the prefill writes an fp16 pool with storage");
+  IG_REQUIRE(pool->storage && !pool->qbits, "the prefill writes an fp16 pool with storage");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
   IG_REQUIRE(N > 0 && D > 0 && D % 8 == 0, "N > 0 and D a positive multiple of 8");
@@ -669,7 +669,7 @@ extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int laye
                                            const float* A, int32_t* cols, float* A_cols, uint16_t* Kpart,
                                            void* workspace, size_t workspace_bytes) {
   IG_REQUIRE(pool, "null pool");
-  IG_REQUIRE(pool->storage && !pool->fp8, "the prefill writes an fp16 pool with storage");
+  IG_REQUIRE(pool->storage && !pool->qbits, "the prefill writes an fp16 pool with storage");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
   IG_REQUIRE(N > 0 && D > 0 && D % 8 == 0, "N > 0 and D a positive multiple of 8");

@@ -37,10 +37,13 @@ class Decoder:
     def __init__(self, *, layers, B, H, d, D, k, Lcap, pool_cap, alpha, policy=ig.IG_SEL_THRESHOLD,
                  cap_frac=1.0, score_scale=None, rope_theta=0.0, gather_ctas=0, stage_timing=False,
                  graph=False, fused_select=True, fused_fetch=False, pool_policy=ig.IG_POOL_COUNTER,
-                 pool_fp8=False, batched_append=False, append_on_fetch=False, sm_split=0, device="cuda:0"):
+                 pool_fp8=False, batched_append=False, append_on_fetch=False, sm_split=0, pool_int4=False,
+                 device="cuda:0"):
         if pool_cap > Lcap or Lcap % 8:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
-        if pool_fp8 and fused_fetch:
+        if pool_fp8 and pool_int4:
+            raise ValueError("one pool format: fp8 or int4")
+        if (pool_fp8 or pool_int4) and fused_fetch:
             raise ValueError("the fused fetch + attention reads fp16 pools only")
         # k: one partial width for every layer, or one per layer (e.g. from ig_ratio_from_spectrum)
         ks = [int(x) for x in k] if hasattr(k, "__len__") else [int(k)] * layers
@@ -56,8 +59,9 @@ class Decoder:
         f16, i32 = torch.float16, torch.int32
         e = lambda *s, dt=f16: torch.empty(*s, dtype=dt, device=self.dev)  # noqa: E731
         self.pool_fp8 = bool(pool_fp8)
+        self.pool_int4 = bool(pool_int4)
         self.pool = ig.ig_pool_create_ex(layers, B, H, d, pool_cap, pool_policy,
-                                         ig.IG_POOL_FP8 if pool_fp8 else 0)
+                                         ig.IG_POOL_FP8 if pool_fp8 else ig.IG_POOL_INT4 if pool_int4 else 0)
         self.cfg = ig.DecoderConfig(layers, B, H, d, D, k, Lcap, policy, float(alpha), float(cap_frac),
                                     float(score_scale if score_scale is not None else 1.0 / math.sqrt(d)),
                                     float(rope_theta), int(gather_ctas), int(bool(stage_timing)),

@@ -41,6 +41,7 @@ IG_POOL_FIFO = 1
 IG_POOL_LRU = 2
 IG_POOL_NO_STORAGE = 1
 IG_POOL_FP8 = 2
+IG_POOL_INT4 = 4
 
 _vp, _i, _f, _sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
 
@@ -280,6 +281,16 @@ def pool_layer_view_fp8(pool, layer, B, H, cap, d):
     raw = np.ctypeslib.as_array(C.cast(r, C.POINTER(C.c_uint8)), shape=(B * H * cap * rec,)).reshape(B, H, cap, rec)
     sc = raw[..., 2 * d:2 * d + 8].view(np.float32)
     return raw[..., :d], raw[..., d:2 * d], sc[..., 0], sc[..., 1]
+
+
+def pool_layer_view_int4(pool, layer, B, H, cap, d):
+    """NumPy views of one layer of an int4 pool: packed codes [B, H, cap, d/2] uint8 (K, V; two
+    codes per byte, element 2j in the low nibble) and scales [B, H, cap] float32 (K, V)."""
+    r, rec = ig_pool_kv8(pool, layer)
+    raw = np.ctypeslib.as_array(C.cast(r, C.POINTER(C.c_uint8)), shape=(B * H * cap * rec,)).reshape(B, H, cap, rec)
+    cb = d // 2
+    sc = raw[..., 2 * cb:2 * cb + 8].view(np.float32)
+    return raw[..., :cb], raw[..., cb:2 * cb], sc[..., 0], sc[..., 1]
 
 
 def ig_pool_slot_tokens(pool, layer, b, out):

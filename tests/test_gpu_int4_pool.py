@@ -1,0 +1,168 @@
+"""The INT4 pool (signed 4-bit rows + per-row scale) on the GPU against the oracle, bit for bit.
+
+As for the fp8 pool: the packed codes and scales that ig_pool_write, ig_append_kv and
+ig_append_kv_layers store, and the fp16 rows ig_gather_kv produces from them, must equal the
+oracle's (int4_quantize_rows, int4_pack, int4_dequantize_rows); then a few decoder steps with an
+int4 pool against the oracle's attention over the dequantized rows of the GPU's own index sets.
+"""
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import infinigen as ora  # noqa: E402
+from speculative_kv_cache_gb300 import synth  # noqa: E402
+from gpu_util import dev, host  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mods():
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA GPU is required for the -m gpu tests")
+    from speculative_kv_cache_gb300 import build
+
+    build.build()
+    from speculative_kv_cache_gb300 import decoder, ig
+
+    return ig, decoder
+
+
+def _rows(seed, B, H, cap, d):
+    g = np.random.default_rng(seed)
+    K = (g.standard_normal((B, H, cap, d)) * g.uniform(0.01, 30, (B, H, cap, 1))).astype(np.float16)
+    V = (g.standard_normal((B, H, cap, d)) * 2).astype(np.float16)
+    K[0, 0, 3] = 0                      # a zero row: scale 0, codes 0
+    K[0, 0, 4, :5] = -0.0               # negative zeros in a nonzero row
+    V[-1, -1, -1, 7] = 60000            # a large value (the row's amax)
+    K[0, 1, 5] = np.arange(d) % 15 - 7  # an integer row with amax 7: codes equal the values
+    return K, V
+
+
+def _packed(X):
+    codes, scales = ora.int4_quantize_rows(X)
+    return ora.int4_pack(codes), scales, codes
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_int4_pool_write_gather_append_bit_exact(mods, d):
+    ig, _ = mods
+    B, H, cap, Lcap = 2, 3, 40, 48
+    K, V = _rows(d + 1, B, H, cap, d)
+    pool = ig.ig_pool_create_ex(2, B, H, d, cap, ig.IG_POOL_COUNTER, ig.IG_POOL_INT4)
+    try:
+        ig.ig_pool_write(pool, None, 1, dev(K), dev(V))
+        torch.cuda.synchronize()
+        K4, V4, Ks, Vs = ig.pool_layer_view_int4(pool, 1, B, H, cap, d)
+        wk, wks, ck = _packed(K)
+        wv, wvs, cv = _packed(V)
+        assert np.array_equal(K4, wk) and np.array_equal(V4, wv)
+        assert np.array_equal(Ks.view(np.uint32), wks.view(np.uint32))
+        assert np.array_equal(Vs.view(np.uint32), wvs.view(np.uint32))
+        # gather: ragged counts, every slot at least once across heads
+        g = np.random.default_rng(1)
+        cnt = g.integers(0, cap + 1, size=(B, H)).astype(np.int32)
+        cnt[0, 0] = cap
+        idx = np.zeros((B, H, Lcap), np.int32)
+        for b in range(B):
+            for h in range(H):
+                idx[b, h, :cnt[b, h]] = np.sort(g.permutation(cap)[:cnt[b, h]])
+        Kg = torch.zeros((B, H, Lcap, d), dtype=torch.float16, device="cuda")
+        Vg = torch.zeros_like(Kg)
+        ig.ig_gather_kv(None, pool, 1, B, H, d, Lcap, dev(idx), dev(cnt), Kg, Vg, 0)
+        ig.ig_check()
+        Kd, Vd = ora.int4_dequantize_rows(ck, wks), ora.int4_dequantize_rows(cv, wvs)
+        Kh, Vh = host(Kg), host(Vg)
+        for b in range(B):
+            for h in range(H):
+                n = cnt[b, h]
+                assert Kh[b, h, :n].tobytes() == Kd[b, h, idx[b, h, :n]].tobytes()
+                assert Vh[b, h, :n].tobytes() == Vd[b, h, idx[b, h, :n]].tobytes()
+        assert np.array_equal(Kd[0, 1, 5], K[0, 1, 5])  # the integer row comes back exactly
+        # append: the new rows are quantized into their slots; the partial key stays fp16
+        k = 16
+        kn = (g.standard_normal((B, H, d)) * 3).astype(np.float16)
+        vn = (g.standard_normal((B, H, d)) * 3).astype(np.float16)
+        slot = np.array([7, -1][:B], np.int32)
+        cols = np.stack([np.sort(g.permutation(d)[:k]) for _ in range(H)]).astype(np.int32)
+        Kpart = torch.zeros((B, H, k, Lcap), dtype=torch.float16, device="cuda")
+        ig.ig_append_kv(None, pool, 1, B, H, d, k, Lcap, dev(slot), dev(cols), dev(kn), dev(vn), Kpart)
+        torch.cuda.synchronize()
+        ig.ig_check()
+        K4, V4, Ks, Vs = ig.pool_layer_view_int4(pool, 1, B, H, cap, d)
+        ak, aks, _ = _packed(kn[0])
+        av, avs, _ = _packed(vn[0])
+        assert np.array_equal(K4[0, :, 7], ak) and np.array_equal(V4[0, :, 7], av)
+        assert np.array_equal(Ks[0, :, 7], aks) and np.array_equal(Vs[0, :, 7], avs)
+        assert np.array_equal(K4[1], wk[1]) and np.array_equal(Ks[1], wks[1])  # slot -1: untouched
+        kp = host(Kpart)
+        for h in range(H):
+            assert np.array_equal(kp[0, h, :, 7], kn[0, h, cols[h]])
+        # the batched append of two layers quantizes the same way
+        kn2 = np.stack([kn, -kn]).astype(np.float16)
+        vn2 = np.stack([vn, vn * 2]).astype(np.float16)
+        slot2 = np.array([[-1] * B, [9, 11][:B]], np.int32)
+        ig.ig_append_kv_layers(None, pool, 2, B, H, d, [0, 0], Lcap, dev(slot2), [None, None], dev(kn2), dev(vn2),
+                               None)
+        torch.cuda.synchronize()
+        ig.ig_check()
+        K4, V4, Ks, Vs = ig.pool_layer_view_int4(pool, 1, B, H, cap, d)
+        for b in range(B):
+            bk, bks, _ = _packed(kn2[1, b])
+            bv, bvs, _ = _packed(vn2[1, b])
+            s_ = slot2[1, b]
+            assert np.array_equal(K4[b, :, s_], bk) and np.array_equal(Ks[b, :, s_], bks)
+            assert np.array_equal(V4[b, :, s_], bv) and np.array_equal(Vs[b, :, s_], bvs)
+        # the fp16-only calls refuse an int4 pool; the two formats exclude each other
+        with pytest.raises(ig.IGError):
+            ig.ig_pool_kv(pool, 1)
+        with pytest.raises(ig.IGError):
+            ig.ig_pool_create_ex(1, B, H, d, cap, ig.IG_POOL_COUNTER, ig.IG_POOL_INT4 | ig.IG_POOL_FP8)
+    finally:
+        ig.ig_pool_destroy(pool)
+
+
+def test_decoder_with_int4_pool(mods):
+    ig, decoder = mods
+    w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-int4", layers=3, batch=2, heads=4, hidden=512,
+                     prompt=200, gen=6)
+    devn = "cuda:0"
+    cap = w.pool_cap
+    scale = np.float32(1.0 / math.sqrt(w.head_dim))
+    dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=w.lcap,
+                          pool_cap=cap, alpha=4.0, pool_int4=True, device=devn)
+    try:
+        for l in range(w.layers):
+            K, V = synth.pool_layer(w, l, cap=cap)
+            cols = synth.skewed_columns(w, l)
+            Wqp = synth.skewed_partial_weight(w, l)
+            t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(devn)  # noqa: E731
+            dec.load_layer(l, t(K), t(V), cols, Wq_part=t(Wqp))
+        dec.prefill(w.prompt)
+        for s in range(2):
+            x = synth.layer_inputs(w, step=s)
+            qkv = [synth.token_inputs(w, l, s) for l in range(w.layers)]
+            q, kn, vn = (np.stack([a[i] for a in qkv]) for i in range(3))
+            out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=devn)
+            L_now = dec.step(*(torch.from_numpy(a).to(devn) for a in (x, q, kn, vn)), out)
+            dec.finish()
+            ig.ig_check(dec.S)
+            o, cnt, idx_buf = out.cpu().numpy(), dec.cnt.cpu().numpy(), dec.idx.cpu().numpy()
+            for l in range(1, w.layers):
+                K4, V4, Ks, Vs = ig.pool_layer_view_int4(dec.pool, l, w.batch, w.heads, cap, w.head_dim)
+                Kd = ora.int4_dequantize_rows(ora.int4_unpack(K4), Ks)
+                Vd = ora.int4_dequantize_rows(ora.int4_unpack(V4), Vs)
+                gi = idx_buf[l % 2]
+                sets = [[gi[b, h, :cnt[l, b, h]] for h in range(w.heads)] for b in range(w.batch)]
+                # the pool is not full, so this step's token went to slot L_now, beyond every
+                # selected slot: the rows the step read are the ones in the pool now
+                assert all(int(t) < L_now for r in sets for x in r for t in x)
+                Kg, Vg = ora.gather(Kd, Vd, sets, w.lcap)
+                ol = ora.attend(q[l], Kg, Vg, cnt[l], scale, kn[l], vn[l])
+                assert np.abs(o[l] - ol).max() <= 2e-3
+                assert cnt[l].sum() > 0
+    finally:
+        dec.close()
