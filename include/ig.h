@@ -295,8 +295,9 @@ ig_status ig_pool_evictions(const ig_pool* pool, int layer, int b, int64_t* out)
  * "Decoding Stage", Step 5 (fetch the selected tokens' full keys and values, all d columns,
  * asynchronously and overlapped with layer i-1's compute).  The kernel reads the mapped
  * pinned pool directly (16-byte zero-copy loads over the host link); issue it on a side
- * stream.  max_ctas bounds its grid (0 = library default) so that it leaves SMs to the
- * compute stream.
+ * stream.  max_ctas bounds its grid (0 = library default: a quarter of the SMs, or two CTAs
+ * per SM of the stream's own partition after ig_sm_split_create) so that it leaves SMs to the
+ * compute stream.  Quantized pools (IG_POOL_FP8, IG_POOL_INT4) are dequantized to fp16 here.
  *   idx, cnt  dev, from ig_select (slots must be < cap)
  *   Kg, Vg    dev fp16 [B][H][Lcap][d] out  rows j < cnt[b][h] = pool rows idx[b][h][j] */
 ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, int B, int H, int d,
@@ -337,7 +338,8 @@ ig_status ig_dense_attend(void* stream, int B, int H, int d, int Lcap, float sca
  * and folds it into a per-head online softmax.  This is the prefetch of section 3.4
  * (Inference Controller) with the copy and the attention that consumes it in one pass; the
  * pages stage the rows in GPU memory first.  Issue it on a side stream; max_ctas bounds the
- * grid (0 = library default, a quarter of the SMs; at most 256).
+ * grid (0 = library default: a quarter of the SMs, or two CTAs per SM of the stream's own
+ * partition after ig_sm_split_create; at most 256).
  *   pool, layer        as for ig_gather_kv (B, H, d must match the pool)
  *   q                  dev fp16 [B][H][d]
  *   idx, cnt           dev, from ig_select (slots must be < the pool's capacity; a slot
