@@ -286,16 +286,28 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def gather_kernel_key(src: str) -> str:
+    """The fp16 fetch kernel's source as the counters depend on it: the file's constants (code
+    without comments) and the text of the k4_gather function itself, so that edits elsewhere in
+    the file (the quantized fetch) do not void the counters."""
+    start = src.index("k4_gather(")
+    start = src.rfind("\n", 0, src.rfind("__global__", 0, start)) + 1
+    end = src.index("\n}\n", start) + 3
+    consts = [ln.split("//")[0].rstrip() for ln in src.splitlines() if ln.startswith("constexpr")]
+    return "\n".join(consts) + "\n" + src[start:end]
+
+
 def gather_traffic_bytes():
     """DRAM bytes per launch of the fetch kernel from the committed ncu summary, or None when
-    the kernel source has changed since those counters were taken."""
+    the kernel (gather_kernel_key) has changed since those counters were taken."""
     import hashlib
 
     prof = os.path.join(ROOT, "profiles", "k4_gather_opt30b_4layer.md")
     src = os.path.join(ROOT, "speculative_kv_cache_gb300", "csrc", "gather.cu")
     try:
         vals = dict(ln.split(":", 1) for ln in open(prof).read().splitlines() if ln.startswith("traffic_"))
-        if vals["traffic_source_sha1"].strip() != hashlib.sha1(open(src, "rb").read()).hexdigest():
+        key = hashlib.sha1(gather_kernel_key(open(src).read()).encode()).hexdigest()
+        if vals["traffic_kernel_sha1"].strip() != key:
             return None
         return float(vals["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):

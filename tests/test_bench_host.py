@@ -89,3 +89,17 @@ def test_fetch_stream_summary_charges_gaps():
     assert abs(got["gap_us_mean"] - 1e3 * (0.5 + 0.1) / 2) < 1e-3
     assert got["gated_by_select_frac"] == 0.5 and got["gated_by_buffer_frac"] == 0.0
     assert bench.fetch_stream_summary([T[:2]], fused_fetch=False) is None
+
+
+def test_gather_kernel_key_is_the_fp16_fetch_kernel():
+    import bench
+
+    src = open(os.path.join(ROOT, "speculative_kv_cache_gb300", "csrc", "gather.cu")).read()
+    key = bench.gather_kernel_key(src)
+    body = key[key.index("__global__"):]
+    assert body.startswith("__global__ void __launch_bounds__(kGatherThreads) k4_gather(")
+    assert "k4_gather_q" not in body and body.endswith("\n}\n")
+    assert "constexpr int kUnroll = 8;" in key
+    # an edit outside the kernel leaves the key unchanged; one inside changes it
+    assert bench.gather_kernel_key(src.replace("k4_gather_q", "k4_gather_x")) == key
+    assert bench.gather_kernel_key(src.replace("kv[q] = ld_nc_v4(Kp + src);", "kv[q] = ld_nc_v4(Kp + src + 0);")) != key
