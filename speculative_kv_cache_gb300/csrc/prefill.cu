@@ -515,6 +515,8 @@ namespace {
 
 size_t rup(size_t x) { return round_up(x, 256); }
 
+constexpr int kPrefillFreeSms = 16;  // SMs the V projection leaves to the column choice and partial keys
+
 // The side stream and events that let the pool writes run beside the projections (one set per
 // device, created on first use; the enqueue sequence of a call is serialised by a mutex).
 struct SideStream {
@@ -571,8 +573,10 @@ void prefill_layout(int B, int N, int H, int d, size_t* off_v, size_t* off_cp, s
   *total = *off_tab + rup((size_t)N * d * sizeof(float));
 }
 
+// max_ctas: at most this many persistent CTAs (0: one per SM), so that kernels on another
+// stream find SMs free
 ig_status gemm(cudaStream_t st, const uint16_t* A, const uint16_t* Bt, uint16_t* C, int M, int N, int K,
-               float* colpart, PoolOut po = PoolOut{nullptr, 1, 1, 1, 1}) {
+               float* colpart, PoolOut po = PoolOut{nullptr, 1, 1, 1, 1}, int max_ctas = 0) {
   CUtensorMap ma, mb;
   ig_status r = make_map(&ma, A, M, K, kGM);
   if (r != IG_OK) return r;
@@ -584,7 +588,8 @@ ig_status gemm(cudaStream_t st, const uint16_t* A, const uint16_t* Bt, uint16_t*
   const long long tiles = (long long)((N + kGN - 1) / kGN) * ((M + kGM - 1) / kGM);
   IG_REQUIRE(tiles < (1ll << 31), "GEMM too large for one launch");
   // persistent: one CTA per SM (its 197 KB of shared memory admit no second one)
-  const int grid = (int)(tiles < sm_count(st) ? tiles : sm_count(st));
+  const int slots = max_ctas > 0 && max_ctas < sm_count(st) ? max_ctas : sm_count(st);
+  const int grid = (int)(tiles < slots ? tiles : slots);
   k_gemm_tn<<<grid, kGThreads, smem, st>>>(ma, mb, reinterpret_cast<__half*>(C), M, N, K, colpart, po,
                                            error_word());
   IG_CHECK_LAUNCH("prefill GEMM launch");
@@ -641,12 +646,20 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   IG_REQUIRE(mtiles <= 65535, "B*N too large for one launch");
   (void)Vt;
   const size_t le = (size_t)B * H * pool->cap * d;
-  // Step 1: K~ (with the per-tile column partials of |K~|) and V; the GEMMs' epilogues write the
-  // rows the pool keeps straight to it (V goes nowhere else)
-  ig_status r = gemm(st, X, Wk_t, Kt, M, Nn, D, colpart,
-                     PoolOut{pool->Kdev + (size_t)layer * le, N, H, d, pool->cap});
+  SideStream* ss = nullptr;
+  ig_status r = side_stream(&ss);
   if (r != IG_OK) return r;
-  r = gemm(st, X, Wv_t, nullptr, M, Nn, D, nullptr, PoolOut{pool->Vdev + (size_t)layer * le, N, H, d, pool->cap});
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  // Step 1: K~ (with the per-tile column partials of |K~|) and V; the GEMMs' epilogues write the
+  // rows the pool keeps straight to it (V goes nowhere else).  V is projected on the side stream
+  // with kPrefillFreeSms SMs left free, where steps 2-3 (which need only K~) run meanwhile.
+  r = gemm(st, X, Wk_t, Kt, M, Nn, D, colpart, PoolOut{pool->Kdev + (size_t)layer * le, N, H, d, pool->cap});
+  if (r != IG_OK) return r;
+  cudaError_t fe = cudaEventRecord(ss->ev[0], st);
+  if (fe == cudaSuccess) fe = cudaStreamWaitEvent(ss->s, ss->ev[0], 0);
+  if (fe != cudaSuccess) return cuda_fail(fe, "prefill fork");
+  r = gemm(ss->s, X, Wv_t, nullptr, M, Nn, D, nullptr, PoolOut{pool->Vdev + (size_t)layer * le, N, H, d, pool->cap},
+           sm_count(st) - kPrefillFreeSms);
   if (r != IG_OK) return r;
   // Step 2: the columns
   k_choose_cols<<<H, d, d * sizeof(double), st>>>(reinterpret_cast<const __half*>(Wq_t), D, H, d, k, colpart, mtiles,
@@ -660,7 +673,7 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   k_partial_keys<<<sg, 256, kScTok * d * 2, st>>>(reinterpret_cast<const __half*>(Kt), N, H, d, k, pool->cap, Lcap,
                                                  cols, reinterpret_cast<__half*>(Kpart), error_word());
   IG_CHECK_LAUNCH("partial keys launch");
-  return IG_OK;
+  return join_side(st, ss);
 }
 
 extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,
