@@ -557,7 +557,8 @@ ig_status ig_captured_fraction(void* stream, int B, int H, int d, int k, int Lca
  *   Wq_part_t     dev fp16 [H*k][D] out
  *   Kpart         dev fp16 [B][H][k][Lcap] out (resident slots written; others untouched)
  *   workspace     dev, >= ig_prefill_workspace_bytes(B, N, H, d), 256-byte aligned (holds
- *                 K~ and V, 4 B N H d bytes, per-tile column sums and a RoPE table)
+ *                 K~, 2 B N H d bytes, per-tile column sums and a RoPE table; V goes from the
+ *                 GEMM straight to the pool)
  * The pool must have storage and fp16 rows; d must be 64 or 128; D a multiple of 8. */
 size_t ig_prefill_workspace_bytes(int B, int N, int H, int d);
 ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,

@@ -562,13 +562,13 @@ ig_status join_side(cudaStream_t st, SideStream* ss) {
   return e == cudaSuccess ? IG_OK : cuda_fail(e, "prefill join");
 }
 
-// workspace: K~ [B N][H d] fp16, V [B N][H d] fp16, column partials [ceil(B N / 64)][H d] fp32
-// (128-row tiles use the first half), the RoPE cos/sin table [N][d/2][2] fp32
-void prefill_layout(int B, int N, int H, int d, size_t* off_v, size_t* off_cp, size_t* off_tab, size_t* total) {
+// workspace: K~ [B N][H d] fp16, column partials [ceil(B N / 64)][H d] fp32 (128-row tiles
+// use the first half), the RoPE cos/sin table [N][d/2][2] fp32 (V needs none: its rows go from
+// the GEMM's epilogue to the pool)
+void prefill_layout(int B, int N, int H, int d, size_t* off_cp, size_t* off_tab, size_t* total) {
   const size_t M = (size_t)B * N, Nn = (size_t)H * d;
   const size_t mt = (M + kRsRows - 1) / kRsRows;
-  *off_v = rup(M * Nn * 2);
-  *off_cp = *off_v + rup(M * Nn * 2);
+  *off_cp = rup(M * Nn * 2);
   *off_tab = *off_cp + rup(mt * Nn * sizeof(float));
   *total = *off_tab + rup((size_t)N * d * sizeof(float));
 }
@@ -610,8 +610,8 @@ extern "C" ig_status ig_gemm_tn(void* stream, int M, int N, int K, const uint16_
 
 extern "C" size_t ig_prefill_workspace_bytes(int B, int N, int H, int d) {
   if (B <= 0 || N <= 0 || H <= 0 || d <= 0) return 0;
-  size_t ov, oc, ot, tot;
-  prefill_layout(B, N, H, d, &ov, &oc, &ot, &tot);
+  size_t oc, ot, tot;
+  prefill_layout(B, N, H, d, &oc, &ot, &tot);
   return tot;
 }
 
@@ -631,20 +631,18 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   IG_REQUIRE(aligned(X, 16) && aligned(Wq_t, 16) && aligned(Wk_t, 16) && aligned(Wv_t, 16) &&
                  aligned(Wq_part_t, 16),
              "X and the weights must be 16-byte aligned");
-  size_t ov, oc, ot, tot;
-  prefill_layout(B, N, H, d, &ov, &oc, &ot, &tot);
+  size_t oc, ot, tot;
+  prefill_layout(B, N, H, d, &oc, &ot, &tot);
   if (!workspace || workspace_bytes < tot)
     return fail(IG_ERR_CAPACITY, "the prefill needs %zu workspace bytes", tot);
   IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
   cudaStream_t st = as_stream(stream);
   char* ws = static_cast<char*>(workspace);
   uint16_t* Kt = reinterpret_cast<uint16_t*>(ws);
-  uint16_t* Vt = reinterpret_cast<uint16_t*>(ws + ov);
   float* colpart = reinterpret_cast<float*>(ws + oc);
   const int M = B * N, Nn = H * d;
   const int mtiles = (M + kGM - 1) / kGM;
   IG_REQUIRE(mtiles <= 65535, "B*N too large for one launch");
-  (void)Vt;
   const size_t le = (size_t)B * H * pool->cap * d;
   SideStream* ss = nullptr;
   ig_status r = side_stream(&ss);
@@ -693,15 +691,14 @@ extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int laye
   IG_REQUIRE(X && Wq_t && Wk_t && Wv_t && A && cols && A_cols && Kpart, "null pointer argument");
   IG_REQUIRE(aligned(X, 16) && aligned(Wq_t, 16) && aligned(Wk_t, 16) && aligned(Wv_t, 16),
              "X and the weights must be 16-byte aligned");
-  size_t ov, oc, ot, tot;
-  prefill_layout(B, N, H, d, &ov, &oc, &ot, &tot);
+  size_t oc, ot, tot;
+  prefill_layout(B, N, H, d, &oc, &ot, &tot);
   if (!workspace || workspace_bytes < tot)
     return fail(IG_ERR_CAPACITY, "the prefill needs %zu workspace bytes", tot);
   IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
   cudaStream_t st = as_stream(stream);
   char* ws = static_cast<char*>(workspace);
   uint16_t* Kt = reinterpret_cast<uint16_t*>(ws);
-  uint16_t* Vt = reinterpret_cast<uint16_t*>(ws + ov);
   float* colpart = reinterpret_cast<float*>(ws + oc);
   float* tab = reinterpret_cast<float*>(ws + ot);
   const int M = B * N, Nn = H * d;
@@ -734,7 +731,7 @@ extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int laye
   IG_CHECK_LAUNCH("rope-skew launch");
   r = fork_pool_rows(st, ss, 0, Kt, B, N, H, d, pool->cap, pool->Kdev + (size_t)layer * le);
   if (r != IG_OK) return r;
-  (void)Vt;  // V's pool rows come from the GEMM's epilogue
+  // V's pool rows come from the GEMM's epilogue
   r = gemm(st, X, Wv_t, nullptr, M, Nn, D, nullptr, PoolOut{pool->Vdev + (size_t)layer * le, N, H, d, pool->cap});
   if (r != IG_OK) return r;
   // Step 2: the columns (W~_Q from Wq_t, the keys' partials over 64-row tiles)
