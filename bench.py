@@ -65,7 +65,8 @@ def parse_args(argv=None):
                    help="N > 0: the fetch stream on N SMs of its own (green contexts), compute on the rest")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-layers", type=int, default=0, help="oracle sample: layers (0 = default)")
+    p.add_argument("--cpu-layers", type=int, default=0, help="reference arm: layers of its oracle sample (0 = 2)")
+    p.add_argument("--cpu-seqs", type=int, default=4, help="CPU baseline: sequences of the oracle's sample")
     p.add_argument("--oracle-layer-step", default=None, help=argparse.SUPPRESS)
     p.add_argument("--layers", type=int, default=0,
                    help="override the workload's layer count (small cases for profiling)")
@@ -314,21 +315,88 @@ def gather_traffic_bytes():
         return None
 
 
-def link_peak_gbs(torch) -> float:
-    """Pinned host -> device copy bandwidth (best of 5 x 1 GiB, CUDA events)."""
+def link_probes(torch, ig, device, reps: int = 5) -> dict:
+    """The host link's read bandwidth three ways (GB/s, best of ``reps`` over 1 GiB each):
+    a pinned host -> device copy (cudaMemcpyAsync), a zero-copy streaming read of mapped pinned
+    memory, and a zero-copy gather of 256-byte rows at random positions (the fetch's pattern);
+    the kernels at 1, 2 and 4 CTAs per SM.  The roofline takes the best of the three."""
     n = 1 << 30
+
+    def best_ms(fn):
+        best = 1e30
+        for _ in range(reps + 1):  # the first run warms up
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            best = min(best, a.elapsed_time(b))
+        return best
+
+    out = {}
     h = torch.empty(n, dtype=torch.uint8).pin_memory()
-    d = torch.empty(n, dtype=torch.uint8, device="cuda")
-    best = 1e9
-    for _ in range(6):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        d.copy_(h, non_blocking=True)
-        b.record()
-        b.synchronize()
-        best = min(best, a.elapsed_time(b))
-    del h, d
-    return n / (best * 1e-3) / 1e9
+    d = torch.empty(n, dtype=torch.uint8, device=device)
+    out["copy"] = n / (best_ms(lambda: d.copy_(h, non_blocking=True)) * 1e-3) / 1e9
+    del h
+    # mapped pinned memory from the library's own pool allocator: one layer of 2^22 rows x 256 B
+    rows = n // 256
+    pool = ig.ig_pool_create(1, 1, 1, 128, rows)
+    try:
+        src, _ = ig.ig_pool_kv(pool, 0)
+        sink = torch.zeros(4, dtype=torch.int32, device=device)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        idx = torch.randperm(rows, device=device, dtype=torch.int64).to(torch.int32)
+        read, gather = 0.0, 0.0
+        for per_sm in (1, 2, 4):
+            ctas = per_sm * sms
+            read = max(read, n / (best_ms(lambda: ig.ig_link_read(None, src, n, sink, ctas)) * 1e-3) / 1e9)
+            gather = max(gather, n / (best_ms(lambda: ig.ig_link_gather(None, src, rows, 256, idx, rows, d, ctas))
+                                      * 1e-3) / 1e9)
+        ig.ig_check()
+        out["zero_copy_read"] = read
+        out["zero_copy_gather_256B"] = gather
+    finally:
+        torch.cuda.synchronize()
+        ig.ig_pool_destroy(pool)
+    del d
+    out["best"] = max(out["copy"], out["zero_copy_read"], out["zero_copy_gather_256B"])
+    out["best_of"] = max(("copy", "zero_copy_read", "zero_copy_gather_256B"), key=lambda k: out[k])
+    return out
+
+
+def oracle_on_bench_data(torch, w, alpha, device, n_seq: int) -> tuple[float, int]:
+    """The oracle's time for one decode step (step 0) of every layer for the first ``n_seq``
+    sequences of the benchmark's own inputs (drawn on the GPU, copied to the host; only the
+    oracle's calls are timed): layer 0's dense attention, and for each later layer the partial
+    query, the speculated scores, the selection, the gather and the attention."""
+    from oracle import infinigen as ora
+
+    scale = 1.0 / math.sqrt(w.head_dim)
+    bs = list(range(n_seq))
+    L = np.full(n_seq, w.prompt, dtype=np.int32)
+    x, q, kn, vn = (t[:, bs].cpu().numpy() for t in synth.torch_step_inputs(w, 0, device))
+    total = 0.0
+    for l in range(w.layers):
+        t = synth.torch_layer(w, l, device)
+        K, V = t["K"][bs].cpu().numpy(), t["V"][bs].cpu().numpy()
+        cols = t["cols"].cpu().numpy()
+        W = (t["Wq"].cpu().numpy(), t["A"].cpu().numpy()) if w.rope_theta else t["Wqp"].cpu().numpy()
+        del t
+        Kpart = ora.partial_key_cache(K, cols) if l else None  # built by the prefill: not timed
+        t0 = time.perf_counter()
+        if l == 0:
+            ora.attend(q[0], K, V, np.full((n_seq, w.heads), w.prompt), scale, kn[0], vn[0])
+        else:
+            if w.rope_theta:
+                qp = ora.partial_query_rope(x[l - 1], W[0], W[1], cols, L, w.rope_theta)
+            else:
+                qp = ora.partial_query(x[l - 1], W, w.heads, w.k)
+            sc = ora.speculate(qp, Kpart, L, scale)
+            idx, cnt, _ = ora.select(sc, L, alpha)
+            Kg, Vg = ora.gather(K, V, idx, K.shape[2])
+            ora.attend(q[l], Kg, Vg, cnt, scale, kn[l], vn[l])
+        total += time.perf_counter() - t0
+    return total, n_seq
 
 
 def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False, fused_select=True,
@@ -344,43 +412,23 @@ def setup_decoder(torch, w, alpha, gather_ctas, device, steps_total, graph=False
                   pool_fp8=bool(pool_fp8), batched_append=bool(batched_append),
                   append_on_fetch=bool(append_on_fetch), sm_split=sm_split, pool_int4=bool(pool_int4),
                   device=device)
-    gen = torch.Generator(device=device)
-    shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
     for l in range(w.layers):
-        gen.manual_seed(1_000_003 * (l + 1))
-        K = torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * w.key_std
-        if w.planted_p > 0:
-            m = torch.rand(shape[:3], generator=gen, device=device) < w.planted_p
-            K = torch.where(m[..., None], K * w.planted_gamma, K)
-        K = K.half()
-        V = (torch.randn(shape, generator=gen, device=device) * w.key_std).half()
-        cols = torch.stack([torch.randperm(w.head_dim, generator=gen, device=device)[: w.k].sort().values
-                            for _ in range(w.heads)]).int()
+        t = synth.torch_layer(w, l, device)
         if w.rope_theta:
-            Wq = (torch.randn((w.hidden, w.heads * w.head_dim), generator=gen, device=device) * w.w_std).half()
-            g = np.random.default_rng(1_000_003 * (l + 1))  # orthogonal skew stand-in, built on the host
-            A = torch.from_numpy(np.stack([np.linalg.qr(g.standard_normal((w.head_dim, w.head_dim)))[0]
-                                           for _ in range(w.heads)]).astype(np.float32)).to(device)
-            A_cols = torch.stack([A[h][:, cols[h].long()] for h in range(w.heads)]).contiguous()
-            dec.load_layer(l, K, V, cols, Wq=Wq, A_cols=A_cols)
+            A_cols = torch.stack([t["A"][h][:, t["cols"][h].long()] for h in range(w.heads)]).contiguous()
+            dec.load_layer(l, t["K"], t["V"], t["cols"], Wq=t["Wq"], A_cols=A_cols)
         else:
-            Wqp = (torch.randn((w.hidden, w.heads * w.k), generator=gen, device=device) * w.w_std).half()
-            dec.load_layer(l, K, V, cols, Wq_part=Wqp)
-        del K, V
+            dec.load_layer(l, t["K"], t["V"], t["cols"], Wq_part=t["Wqp"])
+        del t
     dec.prefill(w.prompt)
     # per-step inputs: layer inputs with cross-layer drift, queries, new keys/values
     xs, qs, kns, vns = [], [], [], []
     for s in range(steps_total):
-        gen.manual_seed(7_000_001 + s)
-        x = torch.empty((w.layers, w.batch, w.hidden), device=device)
-        x[0] = torch.randn((w.batch, w.hidden), generator=gen, device=device)
-        for l in range(1, w.layers):
-            x[l] = (x[l - 1] + 0.4 * torch.randn((w.batch, w.hidden), generator=gen, device=device)) / math.sqrt(1.16)
-        xs.append(x.half())
-        t = (w.layers, w.batch, w.heads, w.head_dim)
-        qs.append((torch.randn(t, generator=gen, device=device) * w.key_std).half())
-        kns.append((torch.randn(t, generator=gen, device=device) * w.key_std).half())
-        vns.append((torch.randn(t, generator=gen, device=device) * w.key_std).half())
+        x, q, kn, vn = synth.torch_step_inputs(w, s, device)
+        xs.append(x)
+        qs.append(q)
+        kns.append(kn)
+        vns.append(vn)
     torch.cuda.synchronize()
     return dec, xs, qs, kns, vns
 
@@ -424,21 +472,21 @@ def run_ours(args, w, alpha):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # CPU baseline first (oracle on the host cores; no GPU state involved yet)
+    # CPU baseline: the oracle over every layer of one decode step of the benchmark's own data
+    # for a sample of the sequences (about 10 s of NumPy float64 at the OPT-30B shape)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        nl = min(w.layers - 1, args.cpu_layers or 16)
-        w1, L1, sample = oracle_sample(w, nl, alpha)
-        t_cpu = time_oracle(w1, L1, sample, alpha)
-        cpu = {"value": (nl / w.layers) / t_cpu, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-               "sample": f"1 of {w.batch} sequences, {nl} of {w.layers} layers, one decode step "
-                         f"({t_cpu:.1f} s of NumPy float64)"}
-        del sample
+        n_seq = max(1, min(w.batch, args.cpu_seqs))
+        t_cpu, n_tok = oracle_on_bench_data(torch, w, alpha, device, n_seq)
+        cpu = {"value": n_tok / t_cpu, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"one decode step (step 0, all {w.layers} layers) of {n_seq} of the {w.batch} "
+                         f"sequences ({t_cpu:.1f} s of NumPy float64 on the host cores)"}
         one = oracle_one_thread(w, alpha)
         if one is not None:
             cpu["one_thread"] = one
 
-    link = link_peak_gbs(torch)
+    probes = link_probes(torch, ig, device)
+    link = probes["best"]
     hbm_peak, hbm_src = measured_peaks()
     n_e2e = 0 if args.no_e2e else args.steps
     steps_total = args.warmup + args.steps + n_e2e
@@ -468,10 +516,13 @@ def run_ours(args, w, alpha):
     barrier()
     launches0 = ig.ig_launch_count()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event at the end of every step: the spread of the step times
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         t0.record(dec.S)
         for i in range(args.steps):
             dec.step(xs[s], qs[s], kns[s], vns[s], out)
+            step_ev[i].record(dec.S)
             with torch.cuda.stream(dec.S):
                 cnt_host[i].copy_(dec.cnt, non_blocking=True)
             if i > 0:  # the previous step's stage times, while this step is queued
@@ -491,6 +542,7 @@ def run_ours(args, w, alpha):
     barrier()
     launches = ig.ig_launch_count() - launches0
     elapsed = t0.elapsed_time(t1)
+    step_ms = [t0.elapsed_time(step_ev[0])] + [step_ev[i - 1].elapsed_time(step_ev[i]) for i in range(1, args.steps)]
     dec.finish()
     ig.ig_check(dec.S)
     elapsed_max, tokens_all = reduce_over_ranks(torch, elapsed, float(w.batch * args.steps), dist_on)
@@ -562,7 +614,10 @@ def run_ours(args, w, alpha):
                            pool_policy=args.pool_policy if w.pool_frac < 1 else None,
                            sm_split=({"fetch_sms": dec.fetch_sms, "compute_sms": dec.compute_sms}
                                      if args.sm_split else None)),
+            "step_ms": {"p50": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),
+                        "mean": statistics.fmean(step_ms)},
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
+            "us_per_layer_step_p50": 1000 * statistics.median(step_ms) / w.layers,
             "selected_fraction": float(f),
             "link_gbs": G_total / args.steps / (ms_per_step * 1e-3) / 1e9,
             "hbm_alg_gbs": hbm_gbs_alg,
@@ -585,12 +640,14 @@ def run_ours(args, w, alpha):
                                      else gather_traffic_bytes()),
                          "traffic_note": "DRAM read+write bytes per launch (ncu, same per-layer shape); "
                                          "the kernel's algorithmic bytes cross the host link, not DRAM",
-                         "peak_source": "measured in this run: pinned host->device copy, best of 5 x 1 GiB",
+                         "peak_source": f"measured in this run: best of three host-link probes "
+                                        f"({probes['best_of']}; best of 5 x 1 GiB each)",
                          "algorithmic_bytes_per_launch": G_per_launch,
                          "launch_ms": gather_ms_per_launch},
             "path_roofline": {"t_roof_ms": 1000 * t_roof_s, "t_step_ms": ms_per_step,
                               "frac": 1000 * t_roof_s / ms_per_step, "hbm_peak_gbs": hbm_peak,
                               "hbm_peak_source": hbm_src, "link_peak_gbs": link},
+            "link_probes_gbs": {k: v for k, v in probes.items() if k != "best"},
             "cpu_baseline": cpu,
             "clocks": clk.summary(),
         }

@@ -64,6 +64,16 @@ int ig_version(void);
  * Returns IG_OK, IG_ERR_INVALID (an index guard tripped), IG_ERR_TIMEOUT, or IG_ERR_CUDA. */
 ig_status ig_check(void* stream);
 
+/* Iteration limit of the score kernels' bounded waits for their staged copies (k2_scores,
+ * k23_score_select) on the current device: a wait that runs out records IG_DEVERR_TIMEOUT,
+ * the CTA then waits (with the fixed default limit) for its copies in flight to land and
+ * leaves without scoring, and the next ig_check returns IG_ERR_TIMEOUT.  max_iters < 0
+ * restores the default (2^22 probes, far more than a copy needs); 0 makes the first wait give
+ * up at once, which is how tests exercise the timeout path without faulting anything.
+ * Synchronous (a 4-byte copy to the device); not for use during stream capture.  No
+ * counterpart in the paper. */
+ig_status ig_set_wait_limit(int max_iters);
+
 /* ------------------------------------------------------------------------------------
  * Offline skew and partial-column choice.
  * Section 3.4, "Skewed Partial Weights" (Q = U S V^T, A = V, W~_Q = W_Q A, W~_K = W_K A) and
@@ -85,7 +95,8 @@ ig_status ig_check(void* stream);
  *   k_out   host int              out    k
  * Host-only and synchronous; uses up to `threads` host threads (0 = all cores).
  * Errors: IG_ERR_INVALID (d odd with RoPE, ratio outside (0,1], null required pointer),
- *         IG_ERR_NUMERIC (Jacobi sweeps did not converge). */
+ *         IG_ERR_NUMERIC (Jacobi sweeps did not converge within 80 sweeps; tests force it
+ *         with the environment variable IG_FAULT=svd_noconverge, which allows no sweeps). */
 ig_status ig_skew_weights(int D, int H, int d, float ratio, float rope_theta,
                           const uint16_t* Xs, int Ns, const uint16_t* Wq, const uint16_t* Wk,
                           const uint16_t* Kp, int Nk, float* A, uint16_t* Wq_skew,
@@ -416,6 +427,9 @@ typedef struct {
   int append_on_fetch; /* staged fetch, batched_append = 0: 1: layer l >= 1's append runs on the
                           fetch stream right after its gather (spares the compute stream where
                           that is the critical path); 0: on the compute stream after attention */
+  int keep_indices;    /* 1: idx is [layers][B][H][Lcap] and every layer's index list outlives the
+                          step (for inspection; the kernels and their grids are unchanged);
+                          0: idx is [2][B][H][Lcap], reused by layer parity */
 } ig_decoder_config;
 
 typedef struct {
@@ -427,7 +441,8 @@ typedef struct {
   uint16_t* K0;                    /* dev fp16 [B][H][Lcap][d]: layer 0's KV in HBM          */
   uint16_t* V0;
   float* scores;                   /* dev fp32 [B][H][Lcap]                                  */
-  int32_t* idx;                    /* dev int32 [2][B][H][Lcap]                              */
+  int32_t* idx;                    /* dev int32 [2][B][H][Lcap] ([layers][B][H][Lcap] with
+                                      config keep_indices)                                   */
   int32_t* cnt;                    /* dev int32 [layers][B][H]                               */
   uint8_t* used;                   /* dev uint8 [layers][B][Lcap] or NULL                    */
   uint16_t* Kg;                    /* dev fp16 [2][B][H][Lcap][d] (16-byte aligned); NULL
@@ -559,7 +574,11 @@ ig_status ig_captured_fraction(void* stream, int B, int H, int d, int k, int Lca
  *   workspace     dev, >= ig_prefill_workspace_bytes(B, N, H, d), 256-byte aligned (holds
  *                 K~, 2 B N H d bytes, per-tile column sums and a RoPE table; V goes from the
  *                 GEMM straight to the pool)
- * The pool must have storage and fp16 rows; d must be 64 or 128; D a multiple of 8. */
+ * The pool must have storage and fp16 rows; d must be 64 or 128; D a multiple of 8.
+ * V is projected on an internal side stream of the device's primary context (one per device,
+ * joined back into `stream` before the call's last work): it runs on the whole device even
+ * when `stream` belongs to an SM partition (ig_sm_split_create), so the prefill is not
+ * confined by such a stream.  Calls from several host threads are serialised internally. */
 size_t ig_prefill_workspace_bytes(int B, int N, int H, int d);
 ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, int B, int N, int D, int H,
                            int d, int k, int Lcap, const uint16_t* X, const uint16_t* Wq_t,
@@ -632,6 +651,23 @@ ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float* ms_out, in
  * draws this overlap of the prefetch with the previous layer's compute (section 3.2, Fig 8);
  * the timeline shows it.  Needs config.stage_timing = 1; waits for that step to finish. */
 ig_status ig_decoder_timeline(ig_decoder* dec, int steps_back, float* t_out);
+
+/* Host-link probes (measurement, not steps of the method).  The fetch of the selected rows
+ * (ig_gather_kv) is bound by the link between host memory and the GPU; the summary's critique
+ * (section 6.3) ties InfiniGen's gains to that link, so its speed is measured on the machine
+ * rather than assumed.  Both read mapped, pinned host memory in place (zero-copy), 16 bytes
+ * per load, many loads in flight; ctas = 0 picks 4 CTAs per SM.
+ *   ig_link_read:   streams `bytes` (a positive multiple of 16) of src; nothing is written
+ *                   (sink, dev 16 bytes, 16-byte aligned, receives a store only for a
+ *                   checksum no real buffer produces).
+ *   ig_link_gather: dst row j = src row idx[j] for j < n, rows of row_bytes (16 times a
+ *                   divisor of 256: 16 .. 4096); src [rows][row_bytes] mapped pinned host,
+ *                   idx dev int32 [n], dst dev [n][row_bytes]; an index outside [0, rows)
+ *                   sets IG_DEVERR_INDEX and its row is skipped.
+ * src, dst 16-byte aligned.  Asynchronous on `stream`.  No counterpart in the paper. */
+ig_status ig_link_read(void* stream, const void* src, size_t bytes, void* sink, int ctas);
+ig_status ig_link_gather(void* stream, const void* src, size_t rows, int row_bytes,
+                         const int32_t* idx, size_t n, void* dst, int ctas);
 
 #ifdef __cplusplus
 }

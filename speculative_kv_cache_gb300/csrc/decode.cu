@@ -22,7 +22,8 @@
 //     S: (l == 1) dense attention(0), append(0)
 //   S: wait att[L-2], append(L-2); wait att[L-1], append(L-1)
 // so the fetch stream does nothing but fetch and attend.  Selection l reuses index buffer
-// l % 2 only after attention(l-2) has finished with it.
+// l % 2 only after attention(l-2) has finished with it (config.keep_indices gives every layer
+// a list of its own instead).
 #include <limits>
 #include <vector>
 
@@ -54,6 +55,10 @@ namespace {
 
 size_t sz_scores(const ig_decoder_config& c) { return (size_t)c.B * c.H * c.Lcap; }
 size_t sz_kv(const ig_decoder_config& c) { return (size_t)c.B * c.H * c.Lcap * c.d; }
+// offset of layer l's index list: one list per layer, or two reused by layer parity
+size_t idx_off(const ig_decoder_config& c, int l) {
+  return (size_t)(c.keep_indices ? l : (l & 1)) * sz_scores(c);
+}
 
 void destroy_events(ig_decoder* d) {
   for (auto* v : {&d->ev_sel, &d->ev_got, &d->ev_att, &d->tg0, &d->tg1, &d->ts0, &d->ts1, &d->ta0,
@@ -257,7 +262,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
   // speculation + selection of layer l on S; G then waits for it
   auto spec_select = [&](int l) -> ig_status {
     float* sc = b.scores;
-    int32_t* idx = b.idx + (size_t)(l & 1) * sz_scores(c);
+    int32_t* idx = b.idx + idx_off(c, l);
     int32_t* cnt = b.cnt + (size_t)l * B * H;
     uint8_t* used = b.used ? b.used + (size_t)l * B * Lc : nullptr;
     cudaError_t se = rec(dec->ts0, l, S);
@@ -330,7 +335,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
       if (e != cudaSuccess) return cuda_fail(e, "timing event");
       const size_t off = (size_t)l * ts;
       st = ig_gather_attend(G, dec->pool, l, B, H, d, Lc, c.score_scale, io->q + off,
-                            b.idx + (size_t)(l & 1) * sz_scores(c), b.cnt + (size_t)l * B * H,
+                            b.idx + idx_off(c, l), b.cnt + (size_t)l * B * H,
                             io->k_new + off, io->v_new + off, io->out + off, fetch_ws, dec->ws_fetch,
                             c.gather_ctas);
       if (st != IG_OK) return st;
@@ -354,7 +359,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
   for (int l = 1; l < L; ++l) {
     st = spec_select(l);
     if (st != IG_OK) return st;
-    const int32_t* idx = b.idx + (size_t)(l & 1) * sz_scores(c);
+    const int32_t* idx = b.idx + idx_off(c, l);
     const int32_t* cnt = b.cnt + (size_t)l * B * H;
     if (l >= 3) e = cudaStreamWaitEvent(G, dec->ev_att[l - 2], 0);
     if (e == cudaSuccess) e = rec(dec->tg0, l, G);

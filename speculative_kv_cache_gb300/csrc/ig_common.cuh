@@ -19,8 +19,12 @@ ig_status fail(ig_status st, const char* fmt, ...);
 // Maps a CUDA error to IG_ERR_CUDA with a message naming `what`.
 ig_status cuda_fail(cudaError_t e, const char* what);
 
-// Device pointer of the error word of the current device.
+// Device pointer of the error word of the current device; the word after it holds the
+// iteration limit of the score kernels' first bounded wait (ig_set_wait_limit).
 int* error_word();
+
+// Default iteration limit of a bounded mbarrier wait (far longer than any copy takes).
+constexpr int kDefaultWaitIters = 1 << 22;
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
@@ -97,11 +101,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for phase `parity` with an iteration limit; false if the limit ran out.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
-                                                  uint32_t max_iters = (1u << 22)) {
+                                                  uint32_t max_iters = (uint32_t)kDefaultWaitIters) {
   for (uint32_t i = 0; i < max_iters; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   return false;
+}
+
+// The host-set limit of a score kernel's first wait for its copies (ig_set_wait_limit), read
+// from the word after the error word.  A give-up path must still drain its copies with the
+// default limit before the CTA leaves.
+__device__ __forceinline__ uint32_t wait_limit(const int* err) {
+  if (!err) return (uint32_t)kDefaultWaitIters;
+  const int v = *(reinterpret_cast<const volatile int*>(err) + 1);
+  return v < 0 ? (uint32_t)kDefaultWaitIters : (uint32_t)v;
 }
 
 // An L2 policy that marks the lines it touches first for eviction: for data read once per

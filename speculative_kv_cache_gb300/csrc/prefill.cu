@@ -518,7 +518,9 @@ size_t rup(size_t x) { return round_up(x, 256); }
 constexpr int kPrefillFreeSms = 16;  // SMs the V projection leaves to the column choice and partial keys
 
 // The side stream and events that let the pool writes run beside the projections (one set per
-// device, created on first use; the enqueue sequence of a call is serialised by a mutex).
+// device, created on first use; creation and the enqueue sequence of a call are serialised by
+// g_side_mu, which callers of side_stream hold).  The side stream belongs to the device's
+// primary context, so it runs on the whole device whatever SM partition the caller's stream has.
 struct SideStream {
   cudaStream_t s = nullptr;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
@@ -644,10 +646,11 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   const int mtiles = (M + kGM - 1) / kGM;
   IG_REQUIRE(mtiles <= 65535, "B*N too large for one launch");
   const size_t le = (size_t)B * H * pool->cap * d;
+  // the lock covers the side stream's creation on first use as well as the enqueue sequence
+  std::lock_guard<std::mutex> lock(g_side_mu);
   SideStream* ss = nullptr;
   ig_status r = side_stream(&ss);
   if (r != IG_OK) return r;
-  std::lock_guard<std::mutex> lock(g_side_mu);
   // Step 1: K~ (with the per-tile column partials of |K~|) and V; the GEMMs' epilogues write the
   // rows the pool keeps straight to it (V goes nowhere else).  V is projected on the side stream
   // with kPrefillFreeSms SMs left free, where steps 2-3 (which need only K~) run meanwhile.
@@ -656,8 +659,9 @@ extern "C" ig_status ig_prefill_layer(void* stream, ig_pool* pool, int layer, in
   cudaError_t fe = cudaEventRecord(ss->ev[0], st);
   if (fe == cudaSuccess) fe = cudaStreamWaitEvent(ss->s, ss->ev[0], 0);
   if (fe != cudaSuccess) return cuda_fail(fe, "prefill fork");
+  // the side stream spans the whole device, so its grid is sized by the device's SM count
   r = gemm(ss->s, X, Wv_t, nullptr, M, Nn, D, nullptr, PoolOut{pool->Vdev + (size_t)layer * le, N, H, d, pool->cap},
-           sm_count(st) - kPrefillFreeSms);
+           sm_count() - kPrefillFreeSms);
   if (r != IG_OK) return r;
   // Step 2: the columns
   k_choose_cols<<<H, d, d * sizeof(double), st>>>(reinterpret_cast<const __half*>(Wq_t), D, H, d, k, colpart, mtiles,
@@ -703,10 +707,11 @@ extern "C" ig_status ig_prefill_layer_rope(void* stream, ig_pool* pool, int laye
   float* tab = reinterpret_cast<float*>(ws + ot);
   const int M = B * N, Nn = H * d;
   IG_REQUIRE((M + kGM - 1) / kGM <= 65535, "B*N too large for one launch");
+  // the lock covers the side stream's creation on first use as well as the enqueue sequence
+  std::lock_guard<std::mutex> lock(g_side_mu);
   SideStream* ss = nullptr;
   ig_status r = side_stream(&ss);
   if (r != IG_OK) return r;
-  std::lock_guard<std::mutex> lock(g_side_mu);
   const size_t le = (size_t)B * H * pool->cap * d;
   // Step 1: K = X W_K, rotated and skewed row by row (with the column partials); its pool rows
   // go out on the side stream while V is projected

@@ -82,13 +82,14 @@ __global__ void __launch_bounds__(kFThreads) k23_score_select(
   __syncthreads();
   const int tl = threadIdx.x * 4;
   float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  bool landed = true;
   if (n_copy > 0) {
     // a copy that does not land is reported and its chunk selects nothing; the CTA still
     // takes part in every cluster barrier below
-    bool landed = mbar_wait_bounded(bar, 0);
+    landed = mbar_wait_bounded(bar, 0, wait_limit(err));
     if (!landed) {
       if (threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
-      landed = mbar_wait_bounded(bar, 0);
+      landed = mbar_wait_bounded(bar, 0);  // the default limit: copies land long before it
     }
     if (landed && tl < n_tok) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -168,6 +169,8 @@ __global__ void __launch_bounds__(kFThreads) k23_score_select(
     }
   }
   if (rank == 0 && threadIdx.x == 0) cnt[bh] = total;
+  // a CTA whose copies never landed waits for them once more (bounded) before it leaves
+  if (!landed) mbar_wait_bounded(bar, 0);
 }
 
 size_t fused_smem(int k) { return 16 + round_up((size_t)k * 4, 128) + (size_t)k * kFT * 2; }

@@ -110,9 +110,9 @@ __global__ void k2_scores(const float* __restrict__ qsrc, int S, int B, int H, i
   const int tl = threadIdx.x * 4;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   if (n_copy > 0) {
-    if (!mbar_wait_bounded(bar, 0)) {
+    if (!mbar_wait_bounded(bar, 0, wait_limit(err))) {
       if (threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
-      mbar_wait_bounded(bar, 0);  // give copies in flight one more bounded chance
+      mbar_wait_bounded(bar, 0);  // let the copies in flight land (default limit) before leaving
       return;
     }
     if (tl < n_tok) {

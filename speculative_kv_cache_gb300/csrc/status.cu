@@ -20,8 +20,9 @@ std::vector<std::pair<cudaStream_t, int>> g_stream_sms;
 std::atomic<int> g_n_stream_sms{0};
 }  // namespace
 
-// One error word per device: bits IG_DEVERR_* set by guarded kernels.
-__device__ int g_device_error_word;
+// Per device: [0] the error word (bits IG_DEVERR_* set by guarded kernels), [1] the iteration
+// limit of the score kernels' first bounded wait (ig_set_wait_limit).
+__device__ int g_device_error_word[2] = {0, kDefaultWaitIters};
 
 ig_status fail(ig_status st, const char* fmt, ...) {
   va_list ap;
@@ -111,6 +112,15 @@ extern "C" uint64_t ig_launch_count(void) { return ig::g_launches.load(); }
 extern "C" const char* ig_last_error(void) { return ig::g_msg; }
 
 extern "C" int ig_version(void) { return 100; }
+
+extern "C" ig_status ig_set_wait_limit(int max_iters) {
+  int* w = ig::error_word();
+  if (!w) return ig::fail(IG_ERR_CUDA, "ig_set_wait_limit: no device error word");
+  const int v = max_iters < 0 ? ig::kDefaultWaitIters : max_iters;
+  cudaError_t e = cudaMemcpy(w + 1, &v, sizeof(int), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return ig::cuda_fail(e, "ig_set_wait_limit");
+  return IG_OK;
+}
 
 extern "C" ig_status ig_check(void* stream) {
   cudaStream_t s = ig::as_stream(stream);

@@ -38,7 +38,7 @@ class Decoder:
                  cap_frac=1.0, score_scale=None, rope_theta=0.0, gather_ctas=0, stage_timing=False,
                  graph=False, fused_select=True, fused_fetch=False, pool_policy=ig.IG_POOL_COUNTER,
                  pool_fp8=False, batched_append=False, append_on_fetch=False, sm_split=0, pool_int4=False,
-                 device="cuda:0"):
+                 keep_indices=False, device="cuda:0"):
         if pool_cap > Lcap or Lcap % 8:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
         if pool_fp8 and pool_int4:
@@ -66,7 +66,7 @@ class Decoder:
                                     float(score_scale if score_scale is not None else 1.0 / math.sqrt(d)),
                                     float(rope_theta), int(gather_ctas), int(bool(stage_timing)),
                                     int(bool(fused_select)), int(bool(fused_fetch)), int(bool(batched_append)),
-                                    int(bool(append_on_fetch)))
+                                    int(bool(append_on_fetch)), int(bool(keep_indices)))
         # per-layer state: partial query weight (or full W_Q and A[:, S] for RoPE), columns,
         # partial key cache; layer 0 keeps its full KV in HBM instead
         self.Wq_part = [None] + [e(H * ks[l], D) for l in range(1, layers)] if not self.rope else None
@@ -76,7 +76,8 @@ class Decoder:
         self.Kpart = [None] + [e(B, H, ks[l], Lcap) for l in range(1, layers)]
         self.K0, self.V0 = e(B, H, Lcap, d), e(B, H, Lcap, d)
         self.scores = e(B, H, Lcap, dt=torch.float32)
-        self.idx = e(2, B, H, Lcap, dt=i32)
+        # index lists: two reused by layer parity, or (keep_indices) one per layer, kept after the step
+        self.idx = e(layers if keep_indices else 2, B, H, Lcap, dt=i32)
         self.cnt = torch.zeros(layers, B, H, dtype=i32, device=self.dev)
         self.used = torch.zeros(layers, B, Lcap, dtype=torch.uint8, device=self.dev)
         # staging buffers of the fetched rows (none when the fetch stream attends from the pool)

@@ -63,6 +63,9 @@ def _sig(name, restype, *argtypes):
 _sig("ig_last_error", C.c_char_p)
 _sig("ig_version", _i)
 _sig("ig_check", _i, _vp)
+_sig("ig_set_wait_limit", _i, _i)
+_sig("ig_link_read", _i, _vp, _vp, _sz, _vp, _i)
+_sig("ig_link_gather", _i, _vp, _vp, _sz, _i, _vp, _sz, _vp, _i)
 _sig("ig_skew_weights", _i, _i, _i, _i, _f, _f, _vp, _i, _vp, _vp, _vp, _i, _vp, _vp, _vp, _vp,
      _vp, _vp, _i)
 _sig("ig_skew_spectrum", _i, _i, _i, _i, _f, _vp, _i, _vp, _vp, _i)
@@ -156,6 +159,19 @@ def ig_last_error() -> str:
 
 def ig_check(stream=None):
     _ok(_lib.ig_check(_s(stream)), "ig_check")
+
+
+def ig_set_wait_limit(max_iters: int):
+    _ok(_lib.ig_set_wait_limit(int(max_iters)), "ig_set_wait_limit")
+
+
+def ig_link_read(stream, src, nbytes, sink, ctas=0):
+    _ok(_lib.ig_link_read(_s(stream), _p(src), int(nbytes), _p(sink), int(ctas)), "ig_link_read")
+
+
+def ig_link_gather(stream, src, rows, row_bytes, idx, n, dst, ctas=0):
+    _ok(_lib.ig_link_gather(_s(stream), _p(src), int(rows), int(row_bytes), _p(idx), int(n), _p(dst), int(ctas)),
+        "ig_link_gather")
 
 
 def ig_skew_weights(D, H, d, ratio, rope_theta, Xs, Ns, Wq, Wk, Kp, Nk, A, Wq_skew, Wk_skew,
@@ -408,7 +424,8 @@ class DecoderConfig(C.Structure):
     _fields_ = [("layers", _i), ("B", _i), ("H", _i), ("d", _i), ("D", _i), ("k", _i), ("Lcap", _i),
                 ("policy", _i), ("alpha", _f), ("cap_frac", _f), ("score_scale", _f),
                 ("rope_theta", _f), ("gather_ctas", _i), ("stage_timing", _i), ("fused_select", _i),
-                ("fused_fetch", _i), ("batched_append", _i), ("append_on_fetch", _i)]
+                ("fused_fetch", _i), ("batched_append", _i), ("append_on_fetch", _i),
+                ("keep_indices", _i)]
 
 
 class DecoderBuffers(C.Structure):

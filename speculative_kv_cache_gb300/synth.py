@@ -224,3 +224,56 @@ def scaled(w: Workload, **over) -> Workload:
     d = dict(w.__dict__)
     d.update(over)
     return Workload(**d)
+
+
+# ---------------------------------------------------------------------------------------
+# The same recipe drawn on the GPU (torch.Generator): the full-size workloads, whose pools
+# (up to 45 GB) are too large to draw on the host in reasonable time.  The benchmark and the
+# full-size tests both take their inputs from here, so they see identical bytes.
+# ---------------------------------------------------------------------------------------
+def torch_layer(w: Workload, layer: int, device):
+    """One layer's data on ``device``: skewed keys K and values V [B, H, pool_cap, d] fp16
+    (planted rows for the OPT-30B shape), a column set per head cols [H, k] int32 (ascending),
+    and either the partial query weight Wqp [D, H*k] fp16 (drawn in the skewed basis) or, for
+    RoPE workloads, the unskewed W_Q [D, H*d] fp16 and an orthogonal stand-in skew A
+    [H, d, d] fp32 (QR of a Gaussian matrix, drawn on the host)."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1_000_003 * (layer + 1))
+    shape = (w.batch, w.heads, w.pool_cap, w.head_dim)
+    K = torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * w.key_std
+    if w.planted_p > 0:
+        m = torch.rand(shape[:3], generator=gen, device=device) < w.planted_p
+        K = torch.where(m[..., None], K * w.planted_gamma, K)
+    K = K.half()
+    V = (torch.randn(shape, generator=gen, device=device) * w.key_std).half()
+    cols = torch.stack([torch.randperm(w.head_dim, generator=gen, device=device)[: w.k].sort().values
+                        for _ in range(w.heads)]).int()
+    out = dict(K=K, V=V, cols=cols)
+    if w.rope_theta:
+        out["Wq"] = (torch.randn((w.hidden, w.heads * w.head_dim), generator=gen, device=device) * w.w_std).half()
+        g = np.random.default_rng(1_000_003 * (layer + 1))
+        A = np.stack([np.linalg.qr(g.standard_normal((w.head_dim, w.head_dim)))[0] for _ in range(w.heads)])
+        out["A"] = torch.from_numpy(A.astype(np.float32)).to(device)
+    else:
+        out["Wqp"] = (torch.randn((w.hidden, w.heads * w.k), generator=gen, device=device) * w.w_std).half()
+    return out
+
+
+def torch_step_inputs(w: Workload, step: int, device):
+    """One decode step's inputs on ``device``: layer inputs x [L, B, D] with the cross-layer
+    drift, and the current token's query, key and value [L, B, H, d], all fp16."""
+    import torch
+
+    gen = torch.Generator(device=device)
+    gen.manual_seed(7_000_001 + step)
+    x = torch.empty((w.layers, w.batch, w.hidden), device=device)
+    x[0] = torch.randn((w.batch, w.hidden), generator=gen, device=device)
+    for l in range(1, w.layers):
+        x[l] = (x[l - 1] + 0.4 * torch.randn((w.batch, w.hidden), generator=gen, device=device)) / math.sqrt(1.16)
+    t = (w.layers, w.batch, w.heads, w.head_dim)
+    q = (torch.randn(t, generator=gen, device=device) * w.key_std).half()
+    kn = (torch.randn(t, generator=gen, device=device) * w.key_std).half()
+    vn = (torch.randn(t, generator=gen, device=device) * w.key_std).half()
+    return x.half(), q, kn, vn

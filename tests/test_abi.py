@@ -84,3 +84,52 @@ def test_injected_pinned_allocation_failure():
             "sys.exit(4)")
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_build_reuses_the_library_only_for_identical_inputs(tmp_path, monkeypatch):
+    """The up-to-date check is a hash of the inputs' bytes, flags and tools, not of mtimes."""
+    from speculative_kv_cache_gb300 import build
+
+    extra = tmp_path / "extra.cuh"
+    extra.write_text("// a header\n")
+    real_inputs = build._inputs
+    monkeypatch.setattr(build, "_inputs", lambda: real_inputs() + [str(extra)])
+    h0 = build.build_hash()
+    assert build.build_hash() == h0
+    extra.write_text("// a header, edited\n")
+    h1 = build.build_hash()
+    assert h1 != h0
+    os.utime(extra, (0, 0))  # an old mtime does not hide the edit
+    assert build.build_hash() == h1
+    monkeypatch.setattr(build, "NVCC_FLAGS", build.NVCC_FLAGS + ["-DIG_SOMETHING"])
+    assert build.build_hash() != h1
+    # a stamp from other inputs never counts as up to date
+    monkeypatch.setattr(build, "STAMP", str(tmp_path / "libig.so.sha256"))
+    (tmp_path / "libig.so.sha256").write_text(h0 + "\n")
+    assert not build.up_to_date(h1)
+    assert build.up_to_date(h0) == os.path.exists(build.LIB)
+
+
+def test_injected_svd_non_convergence():
+    """IG_FAULT=svd_noconverge leaves the Jacobi iteration no sweeps: ig_skew_weights (a host
+    call) must report IG_ERR_NUMERIC, and the same call without the fault must succeed."""
+    code = ("import os, sys\n"
+            "import numpy as np\n"
+            "from speculative_kv_cache_gb300 import ig\n"
+            "D, H, d, Ns = 32, 2, 8, 16\n"
+            "g = np.random.default_rng(0)\n"
+            "X = g.standard_normal((Ns, D)).astype(np.float16)\n"
+            "W = (0.1 * g.standard_normal((D, H * d))).astype(np.float16)\n"
+            "A = np.zeros((H, d, d), np.float32); cols = np.zeros((H, 4), np.int32)\n"
+            "args = (D, H, d, 0.5, 0.0, X, Ns, W, W, None, 0, A, None, None, None, cols)\n"
+            "if os.environ.get('IG_FAULT'):\n"
+            "    try:\n"
+            "        ig.ig_skew_weights(*args)\n"
+            "    except ig.IGError as e:\n"
+            "        sys.exit(0 if e.status == ig.IG_ERR_NUMERIC and 'converge' in str(e) else 3)\n"
+            "    sys.exit(4)\n"
+            "sys.exit(0 if ig.ig_skew_weights(*args) == 4 else 5)\n")
+    for fault in ("svd_noconverge", ""):
+        env = dict(os.environ, IG_FAULT=fault)
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, env=env)
+        assert r.returncode == 0, (fault, r.returncode, r.stderr)

@@ -478,3 +478,37 @@ def test_prefill_rope_keys_are_the_skews_rotated_prompt_keys():
         kp = o["K_part"][0, h].astype(np.float64)  # [k, cap]
         assert np.allclose(qp[0, h] @ kp, qp[0, h] @ o["K"][0, :, h][:, o["cols"][h]].T.astype(np.float64))
         assert np.array_equal(o["A_cols"][h], A[h][:, o["cols"][h]])
+
+
+# --- Prefill Step 3 (extract the partial weight): a hand-written two-head case -------------
+def test_partial_weight_hand_written_two_heads():
+    """W~_Q is 3 x 8 (D = 3, H = 2 heads of d = 4); head 0 keeps columns {1, 3}, head 1 keeps
+    {0, 2}.  Entry (r, c) of W~_Q is 10 * r + c, so every column's origin can be read off its
+    values.  Head 1's columns sit at offset h * d = 4 in W~_Q: columns 4 and 6, not 0 and 2."""
+    W = np.array([[10 * r + c for c in range(8)] for r in range(3)], dtype=np.float16)
+    cols = np.array([[1, 3], [0, 2]], dtype=np.int32)
+    got = ora.partial_weight(W, cols, H=2, d=4)
+    want = np.array([[1, 3, 4, 6],
+                     [11, 13, 14, 16],
+                     [21, 23, 24, 26]], dtype=np.float16)
+    assert got.shape == (3, 4) and got.dtype == np.float16
+    assert np.array_equal(got, want)
+    # the partial query through it is x . W~_Q restricted to those columns, by hand
+    x = np.array([[1.0, -2.0, 0.5]], dtype=np.float16)
+    q = ora.partial_query(x, got, H=2, k=2)
+    assert q.shape == (1, 2, 2)
+    assert np.array_equal(q[0], [[1 - 22 + 10.5, 3 - 26 + 11.5], [4 - 28 + 12.0, 6 - 32 + 13.0]])
+
+
+# --- Speculation fidelity: real logits of a two-token case --------------------------------
+def test_real_scores_two_token_closed_form():
+    """q = (1, 2), keys (3, 4) and (-1, 0.5), scale 0.5: logits 0.5 * 11 = 5.5 and
+    0.5 * 0 = 0; the third slot is past L and must read -inf.  A second sequence with L = 1
+    checks that L is taken per sequence."""
+    q = np.array([[[1.0, 2.0]], [[2.0, 0.0]]])           # [B=2, H=1, d=2]
+    K = np.array([[[[3.0, 4.0], [-1.0, 0.5], [7.0, 7.0]]],
+                  [[[1.0, 9.0], [5.0, 5.0], [0.0, 0.0]]]])  # [B=2, H=1, T=3, d=2]
+    z = ora.real_scores(q, K, np.array([2, 1]), 0.5)
+    assert z.shape == (2, 1, 3)
+    assert z[0, 0, 0] == 5.5 and z[0, 0, 1] == 0.0 and np.isneginf(z[0, 0, 2])
+    assert z[1, 0, 0] == 1.0 and np.isneginf(z[1, 0, 1]) and np.isneginf(z[1, 0, 2])
