@@ -15,6 +15,7 @@ Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle instea
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -218,6 +219,11 @@ class ClockSampler:
             self.th.start()
         except OSError:
             self.proc = None
+        # nvidia-smi's first query (its NVML start-up) is the costly one: let it finish before
+        # the timed region opens, so that it does not land inside a timed step
+        t_end = time.time() + 10.0
+        while self.proc is not None and not self.lines and time.time() < t_end and self.proc.poll() is None:
+            time.sleep(0.05)
         time.sleep(0.3)
         return self
 
@@ -513,6 +519,11 @@ def run_ours(args, w, alpha):
     stage = [0.0, 0.0, 0.0, 0.0]
     stage_n = [0, 0, 0, 0]
     timelines = []
+    # the host stays about one step ahead of the GPU (it reads each step's stage timeline one
+    # step back), so a collector pause inside the timed region would idle the GPU: collect now
+    # and hold the collector off until the timed steps are done
+    gc.collect()
+    gc.disable()
     barrier()
     launches0 = ig.ig_launch_count()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -540,6 +551,7 @@ def run_ours(args, w, alpha):
             stage_n[j] += n[j]
         timelines.append(dec.timeline(steps_back=0))
     barrier()
+    gc.enable()
     launches = ig.ig_launch_count() - launches0
     elapsed = t0.elapsed_time(t1)
     step_ms = [t0.elapsed_time(step_ev[0])] + [step_ev[i - 1].elapsed_time(step_ev[i]) for i in range(1, args.steps)]
@@ -579,6 +591,8 @@ def run_ours(args, w, alpha):
         hv = [t.cpu().pin_memory() for t in vns[s:s + n_e2e]]
         dx, dq, dk, dv = (torch.empty_like(t) for t in (xs[0], qs[0], kns[0], vns[0]))
         hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        gc.collect()
+        gc.disable()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(dec.S)
@@ -594,6 +608,7 @@ def run_ours(args, w, alpha):
         e1.record(dec.S)
         e1.synchronize()
         barrier()
+        gc.enable()
         dec.finish()
         e_ms, e_tok = reduce_over_ranks(torch, e0.elapsed_time(e1), float(w.batch * n_e2e), dist_on)
         bi = sum(t.numel() * t.element_size() for t in (hx[0], hq[0], hk[0], hv[0]))
@@ -615,7 +630,7 @@ def run_ours(args, w, alpha):
                            sm_split=({"fetch_sms": dec.fetch_sms, "compute_sms": dec.compute_sms}
                                      if args.sm_split else None)),
             "step_ms": {"p50": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),
-                        "mean": statistics.fmean(step_ms)},
+                        "mean": statistics.fmean(step_ms), "each": [round(t, 3) for t in step_ms]},
             "us_per_layer_step": 1000 * ms_per_step / w.layers,
             "us_per_layer_step_p50": 1000 * statistics.median(step_ms) / w.layers,
             "selected_fraction": float(f),

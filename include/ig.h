@@ -198,16 +198,17 @@ ig_status ig_select(void* stream, int B, int H, int Lcap, const float* scores,
 /* ------------------------------------------------------------------------------------
  * Fused speculation + threshold selection: ig_speculate followed by ig_select with
  * IG_SEL_THRESHOLD and no cap, with the scores kept on chip.  Section 3.4, "Decoding Stage",
- * Steps 1-3.  One thread-block cluster per (sequence, head) and one CTA per 512-token chunk;
- * the head's maximum and the compaction offsets cross the cluster through distributed
- * shared memory.  Identical results to the two calls (same fp32 operations).
+ * Steps 1-3.  Persistent CTAs stream whole heads (two CTAs per SM at the OPT-30B shape): the
+ * partial-key rows go through a two-stage ring of bulk copies that runs ahead into the next
+ * head, the head's scores stay in shared memory, and each warp compacts a contiguous run of
+ * tokens in order.  Identical results to the two calls (same fp32 operations).
  *   Wq        dev fp16 [H*k][D] (rope_theta == 0) or [H*d][D] (RoPE: then A_cols [H][d][k] and
  *             positions [B] are required, as in ig_speculate_rope)
  *   idx, cnt, used   as ig_select (used may be NULL)
  *   scores    dev fp32 [B][H][Lcap] or NULL: the scores, written only when asked for
  *   q_part    dev fp32 [B][H][k] or NULL
  *   workspace >= ig_speculate_select_workspace_bytes(B, D, H, d, k, rope != 0)
- * Lcap must be <= 4096 (at most 8 chunks per cluster); else IG_ERR_INVALID. */
+ * Lcap must be <= 8192 (the on-chip score row); else IG_ERR_INVALID. */
 size_t ig_speculate_select_workspace_bytes(int B, int D, int H, int d, int k, int rope);
 ig_status ig_speculate_select(void* stream, int B, int D, int H, int d, int k, int Lcap,
                               const uint16_t* x, const uint16_t* Wq, const float* A_cols,
@@ -417,7 +418,7 @@ typedef struct {
   int gather_ctas;     /* grid of the fetch kernel; 0 = library default */
   int stage_timing;    /* 1: record timing events around each stage (ig_decoder_stage_ms) */
   int fused_select;    /* 1: use ig_speculate_select when policy = IG_SEL_THRESHOLD, cap_frac >= 1
-                          and Lcap <= 4096 (scores stay on chip); 0: separate calls */
+                          and Lcap <= 8192 (scores stay on chip); 0: separate calls */
   int fused_fetch;     /* 1: layers 1.. attend straight from the pool on the fetch stream
                           (ig_gather_attend), no staging in HBM, Kg/Vg unused (may be NULL);
                           0: gather into Kg/Vg on the fetch stream, attend on the compute stream */

@@ -267,7 +267,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     uint8_t* used = b.used ? b.used + (size_t)l * B * Lc : nullptr;
     cudaError_t se = rec(dec->ts0, l, S);
     if (se != cudaSuccess) return cuda_fail(se, "timing event");
-    const bool fused = c.fused_select && c.policy == IG_SEL_THRESHOLD && c.cap_frac >= 1.f && Lc <= 4096;
+    const bool fused = c.fused_select && c.policy == IG_SEL_THRESHOLD && c.cap_frac >= 1.f && Lc <= 8192;
     ig_status r;
     if (fused) {
       const bool rope = c.rope_theta > 0.f;

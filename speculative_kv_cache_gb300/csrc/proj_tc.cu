@@ -5,13 +5,15 @@
 //   A = Wt tile  (M = 128 output components x K, K-major: row n of Wt holds its D weights)
 //   B = x tile   (N = 16 batch rows x K, K-major)
 // so the batch (1..16 rows) is the MMA's N and the 128 components fill its M (swap-AB).
-// One CTA per (128-component tile, reduction split, 16-row batch chunk).  Thread 0 issues every
-// TMA load of the CTA's K range up front (64-wide 128B-swizzled stages, one mbarrier each),
-// then one tcgen05.mma (128x16x16, fp16 in, fp32 accumulate in tensor memory) per 16-wide
-// K step as the stages land, and commits to an mbarrier; the four warps then read the
+// One CTA per (128-component tile, reduction split, 16-row batch chunk); the reduction is
+// split so that the grid holds about two CTAs per SM and runs in one wave.  Thread 0 streams
+// the CTA's K range through a ring of four 64-wide 128B-swizzled stages (TMA, one "full"
+// mbarrier each), issues one tcgen05.mma (128x16x16, fp16 in, fp32 accumulate in tensor
+// memory) per 16-wide K step as the stages land, and refills a stage once the MMAs that read
+// it have completed (tcgen05.commit onto its "empty" mbarrier), one stage behind, so loads
+// stay in flight; a final commit signals the accumulator.  The four warps then read the
 // accumulator rows of their TMEM sub-partition with tcgen05.ld and write the fp32 partials.
-// The weight stream is the whole cost (30.5 MB per layer at the OPT-30B shape), so the CTA
-// keeps every stage in flight at once instead of running a ring.
+// The weight stream is the whole cost (30.5 MB per layer at the OPT-30B shape).
 #include <cuda.h>
 
 #include <mutex>
@@ -61,7 +63,7 @@ constexpr int kTcM = 128;       // output components per CTA (tcgen05 M)
 constexpr int kTcN = 16;        // batch rows per CTA (tcgen05 N)
 constexpr int kTcBK = 64;       // K per stage: one 128-byte swizzle atom of fp16
 constexpr int kTcThreads = 128;
-constexpr int kTcMaxStages = 10;
+constexpr int kTcRing = 4;      // stages in the ring
 constexpr uint32_t kStageA = kTcM * kTcBK * 2;  // 16 KB
 constexpr uint32_t kStageB = kTcN * kTcBK * 2;  // 2 KB
 constexpr uint32_t kTmemCols = 32;              // minimum allocation; 16 columns used
@@ -72,7 +74,7 @@ constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kTcN >> 3) << 17) | ((uint32
 
 __global__ void __launch_bounds__(kTcThreads) k1_partial_q_tc(
     const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-    float* __restrict__ part, int B, int D, int N, int split_k, int max_st, int* err) {
+    float* __restrict__ part, int B, int D, int N, int split_k, int* err) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // 1024-byte alignment for the swizzled stages
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -82,17 +84,22 @@ __global__ void __launch_bounds__(kTcThreads) k1_partial_q_tc(
   const int b0 = blockIdx.z * kTcN;
   const int k_begin = s * split_k;
   const int k_end = min(D, k_begin + split_k);
-  const int nst = (k_end - k_begin + kTcBK - 1) / kTcBK;  // 1..max_st stages of this CTA
-  unsigned char* sA = smem;                              // max_st weight stages
-  unsigned char* sB = smem + max_st * kStageA;           // max_st x stages
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + max_st * kStageB);
-  uint64_t* done = full + max_st;
+  const int nst = (k_end - k_begin + kTcBK - 1) / kTcBK;  // stages of this CTA's K range
+  const int R = nst < kTcRing ? nst : kTcRing;            // slots of the ring in use
+  unsigned char* sA = smem;                               // kTcRing weight stages
+  unsigned char* sB = smem + kTcRing * kStageA;           // kTcRing x stages
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kTcRing * kStageB);
+  uint64_t* empty = full + kTcRing;
+  uint64_t* done = empty + kTcRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < nst; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kTcRing; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -109,23 +116,27 @@ __global__ void __launch_bounds__(kTcThreads) k1_partial_q_tc(
   const uint32_t tmem = *tmem_slot;
 
   if (threadIdx.x == 0) {
-    // every stage's loads at once: the CTA's whole K range is in flight; the weight, read
-    // once per step, is marked first for eviction
+    // the weight, read once per step, is marked first for eviction
     const uint64_t pol = l2_evict_first();
-    for (int i = 0; i < nst; ++i) {
-      mbar_arrive_expect_tx(&full[i], kStageA + kStageB);
+    auto load = [&](int i) {  // stage i into slot i % R
+      const int slot = i % R;
+      mbar_arrive_expect_tx(&full[slot], kStageA + kStageB);
       const int kx = k_begin + i * kTcBK;
-      tma_load_2d_hint(sA + i * kStageA, &map_w, kx, m0, &full[i], pol);
-      tma_load_2d(sB + i * kStageB, &map_x, kx, b0, &full[i]);
-    }
+      tma_load_2d_hint(sA + slot * kStageA, &map_w, kx, m0, &full[slot], pol);
+      tma_load_2d(sB + slot * kStageB, &map_x, kx, b0, &full[slot]);
+    };
+    int issued = 0, consumed = 0;
+    for (; issued < R; ++issued) load(issued);
     bool ok = true;
-    for (int i = 0; i < nst && ok; ++i) {
-      if (!mbar_wait_bounded(&full[i], 0)) {
+    for (int i = 0; i < nst; ++i) {
+      const int slot = i % R;
+      if (!mbar_wait_bounded(&full[slot], (uint32_t)(i / R) & 1u)) {
         ok = false;
         break;
       }
+      consumed = i + 1;
       tc_fence_after();
-      const uint32_t a0 = smem_addr(sA + i * kStageA), bb0 = smem_addr(sB + i * kStageB);
+      const uint32_t a0 = smem_addr(sA + slot * kStageA), bb0 = smem_addr(sB + slot * kStageB);
 #pragma unroll
       for (int kk = 0; kk < kTcBK / 16; ++kk) {
         const uint64_t ad = sw128_desc(a0 + kk * 32), bd = sw128_desc(bb0 + kk * 32);
@@ -135,42 +146,54 @@ __global__ void __launch_bounds__(kTcThreads) k1_partial_q_tc(
             " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
             "l"(ad), "l"(bd), "r"(kIdesc), "r"(acc));
       }
-    }
-    if (ok) {
+      // the slot is free once these MMAs have read it
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_addr(done))
+                       smem_addr(&empty[slot]))
                    : "memory");
-    } else {
+      // refill the previous stage's slot (its MMAs were issued one step earlier)
+      if (i >= 1 && issued < nst) {
+        const int ps = (i - 1) % R;
+        if (!mbar_wait_bounded(&empty[ps], (uint32_t)((i - 1) / R) & 1u)) {
+          ok = false;
+          break;
+        }
+        load(issued++);
+      }
+    }
+    if (!ok) {
       *abort_flag = 1;
       raise_error(err, IG_DEVERR_TIMEOUT);
-      for (int i = 0; i < nst; ++i) mbar_wait_bounded(&full[i], 0);  // let copies in flight land
+      // let the copies in flight land before the CTA leaves
+      for (int u = consumed; u < issued; ++u) mbar_wait_bounded(&full[u % R], (uint32_t)(u / R) & 1u);
     }
+    // the accumulator (and every issued MMA) is complete when `done` fires
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(done))
+                 : "memory");
   }
   __syncthreads();
   const bool aborted = *abort_flag != 0;
-  if (!aborted) {
-    // every thread must take the same branch: the TMEM load below is warp-collective
-    const bool landed = __syncthreads_and(mbar_wait_bounded(done, 0) ? 1 : 0) != 0;
-    if (!landed) {
-      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
-    } else {
-      tc_fence_after();
-      // warp w reads TMEM lanes 32w..32w+31 = output components m0 + 32w + lane, 16 batch columns
-      uint32_t r[16];
-      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-          "[%16];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-            "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-          : "r"(taddr));
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      const int n = m0 + warp * 32 + lane;
-      if (n < N) {
+  // every thread must take the same branch: the TMEM load below is warp-collective
+  const bool landed = __syncthreads_and(mbar_wait_bounded(done, 0) ? 1 : 0) != 0;
+  if (!landed) {
+    if (threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
+  } else if (!aborted) {
+    tc_fence_after();
+    // warp w reads TMEM lanes 32w..32w+31 = output components m0 + 32w + lane, 16 batch columns
+    uint32_t r[16];
+    const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+        "[%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    const int n = m0 + warp * 32 + lane;
+    if (n < N) {
 #pragma unroll
-        for (int j = 0; j < kTcN; ++j)
-          if (b0 + j < B) part[((size_t)s * B + b0 + j) * N + n] = __uint_as_float(r[j]);
-      }
+      for (int j = 0; j < kTcN; ++j)
+        if (b0 + j < B) part[((size_t)s * B + b0 + j) * N + n] = __uint_as_float(r[j]);
     }
   }
   tc_fence_before();
@@ -181,18 +204,19 @@ __global__ void __launch_bounds__(kTcThreads) k1_partial_q_tc(
   }
 }
 
-// shared memory for max_st stages (sized per launch: 4 stages of a 256-wide split take 73 KB, so
-// three CTAs share an SM)
-size_t tc_smem_bytes(int max_st) { return 1024 + max_st * (kStageA + kStageB) + (max_st + 1) * 8 + 16; }
+// shared memory of the ring: 4 stages of 18 KB (three CTAs share an SM)
+size_t tc_smem_bytes() { return 1024 + kTcRing * (kStageA + kStageB) + (2 * kTcRing + 1) * 8 + 16; }
 
 }  // namespace
 
-// Split of the reduction axis for the tensor-core projection: S pieces of a multiple of 64.
-int tc_split_k(int D, int S) {
-  int per = (D + S - 1) / S;
-  per = (per + kTcBK - 1) / kTcBK * kTcBK;
-  if (per > kTcMaxStages * kTcBK) per = kTcMaxStages * kTcBK;
-  return per;
+// Split of the reduction axis: about two CTAs per SM over the (component tile, batch chunk)
+// grid, at most S splits (the workspace's), each a multiple of 64 wide.
+int tc_split_k(int D, int S, int tiles, int sms) {
+  int want = (2 * sms + tiles / 2) / (tiles > 0 ? tiles : 1);
+  if (want < 1) want = 1;
+  if (want > S) want = S;
+  int per = (D + want - 1) / want;
+  return (per + kTcBK - 1) / kTcBK * kTcBK;
 }
 
 // part[s][b][n] for s < S_eff = ceil(D / split_k); returns S_eff through *s_eff.
@@ -200,7 +224,8 @@ ig_status launch_partial_q_tc(cudaStream_t st, const __half* x, const __half* Wt
                               int N, int S, int* s_eff) {
   IG_REQUIRE(D % 8 == 0, "D must be a multiple of 8 (16-byte rows for the tensor maps)");
   IG_REQUIRE(aligned(x, 16) && aligned(Wt, 16), "x and the weight must be 16-byte aligned");
-  const int split_k = tc_split_k(D, S);
+  const int tiles = ((N + kTcM - 1) / kTcM) * ((B + kTcN - 1) / kTcN);
+  const int split_k = tc_split_k(D, S, tiles, sm_count(st));
   const int se = (D + split_k - 1) / split_k;
   IG_REQUIRE(se <= S, "reduction split exceeds the workspace");
   CUtensorMap mw, mx;
@@ -208,12 +233,11 @@ ig_status launch_partial_q_tc(cudaStream_t st, const __half* x, const __half* Wt
   if (r != IG_OK) return r;
   r = make_map(&mx, x, B, D, kTcN);
   if (r != IG_OK) return r;
-  const int max_st = split_k / kTcBK;
-  const size_t smem = tc_smem_bytes(max_st);
+  const size_t smem = tc_smem_bytes();
   cudaError_t ae = cudaFuncSetAttribute(k1_partial_q_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ae != cudaSuccess) return cuda_fail(ae, "tensor-core projection smem attribute");
   dim3 grid((N + kTcM - 1) / kTcM, se, (B + kTcN - 1) / kTcN);
-  k1_partial_q_tc<<<grid, kTcThreads, smem, st>>>(mw, mx, part, B, D, N, split_k, max_st, error_word());
+  k1_partial_q_tc<<<grid, kTcThreads, smem, st>>>(mw, mx, part, B, D, N, split_k, error_word());
   IG_CHECK_LAUNCH("tensor-core projection launch");
   *s_eff = se;
   return IG_OK;

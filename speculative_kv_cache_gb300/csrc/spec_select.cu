@@ -1,23 +1,24 @@
 // Fused speculated scores + threshold selection (InfiniGen paper-graph summary, section 3.4,
 // "Decoding Stage", Steps 2-3), with the scores kept on chip.
 //
-// One thread-block cluster per (sequence, head), one CTA per chunk of 512 tokens (at most 8
-// chunks: Lcap <= 4096).  Each CTA stages its chunk of the partial key cache with bulk (TMA)
-// copies, scores 4 tokens per thread into registers, and reduces its chunk maximum, which it
-// writes into every CTA of the cluster (distributed shared memory); after one cluster barrier
-// every CTA knows the head's maximum m.  Each thread then flags its tokens with (m - s) < alpha,
-// the CTA scans its flags in token order and pushes its count the same way; after a second
-// barrier each CTA sums the counts of the lower-ranked chunks and writes its indices at that
-// offset.  No CTA touches another's shared memory after that barrier, so none waits for the
-// others to finish.  The comparisons are the
-// same fp32 operations as in the separate score and select kernels, so the result is
-// identical to theirs.
-#include <cooperative_groups.h>
+// Persistent CTAs, each streaming whole heads (sequence, head) one after another: CTA i takes
+// heads i, i + grid, i + 2 grid, ...  A head's partial keys are k rows of Lcap tokens, adjacent
+// in memory (the cache is [B][H][k][Lcap]).  The warps have two roles.  A producer warp stages
+// the rows R at a time (its lanes issue one bulk copy per row, of the head's L resident tokens)
+// into a ring of stages, running ahead into the next head, so that loads stay in flight
+// while the consumers reduce and compact.  Eight consumer warps each own a fixed set of the
+// head's tokens (runs of eight, 8 p .. 8 p + 7 for p = thread + 256 m) and keep their scores in
+// registers (one 16-byte shared-memory load per run and row):
+// every stage adds its R rows' terms q_c K_ct in row order, so each score is the same fp32 fmaf
+// chain over c = 0..k-1 as in the separate score kernel; a consumer warp hands a stage back
+// through an "empty" mbarrier.  The next head's split partials of the projection are fetched
+// with cp.async meanwhile.  At the head's end the scores go to an on-chip score row, the
+// consumers reduce the maximum m, and each warp compacts a contiguous run of tokens with
+// (m - s) < alpha in token order (ballot + popc: a count pass, then a write pass at the warp's
+// offset), so the result is identical to the separate score and select kernels'.
 #include <math.h>
 
 #include "ig_common.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace ig {
 
@@ -29,187 +30,318 @@ int projection_splits(int D);
 
 namespace {
 
-constexpr int kFT = 512;             // tokens per CTA
-constexpr int kFThreads = kFT / 4;   // 4 tokens per thread
-constexpr int kFMaxChunks = 8;       // portable cluster size
+constexpr int kSConsumerWarps = 8;
+constexpr int kSConsumers = kSConsumerWarps * 32;
+constexpr int kSThreads = kSConsumers + 32;         // + the producer warp
+#ifndef IG_K23_STAGES
+#define IG_K23_STAGES 3
+#endif
+#ifndef IG_K23_STAGE_KB
+#define IG_K23_STAGE_KB 32
+#endif
+#ifndef IG_K23_MIN_CTAS
+#define IG_K23_MIN_CTAS 2
+#endif
+constexpr int kSMaxStages = IG_K23_STAGES;          // ring of staged row groups
+constexpr int kSRun = 8;                            // consecutive tokens a consumer thread owns
+constexpr int kSBlock = kSRun * kSConsumers;        // 2048 tokens: one run per thread
+constexpr int kSMaxLcap = 4 * kSBlock;              // 8192 tokens: four runs per thread
+constexpr int kSStageTarget = IG_K23_STAGE_KB * 1024;  // bytes of rows per stage (at least one row)
 
-__global__ void __launch_bounds__(kFThreads) k23_score_select(
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// barrier 1 among the consumer warps only (the producer never joins it)
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSConsumers) : "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Shared-memory layout of one CTA (all offsets 128-byte aligned).
+struct SelLayout {
+  int R;   // rows per stage
+  int NS;  // stages in the ring
+  size_t qs, qbuf, sc, stage, stage_bytes, total;
+};
+
+__host__ __device__ inline size_t al128(size_t x) { return (x + 127) / 128 * 128; }
+
+__host__ __device__ inline SelLayout sel_layout(int S, int k, int Lcap, int NS) {
+  SelLayout l;
+  l.NS = NS;
+  l.R = kSStageTarget / (Lcap * 2);
+  if (l.R < 1) l.R = 1;
+  if (l.R > k) l.R = k;
+  if (l.R > 32) l.R = 32;                          // one row per producer lane
+  l.qs = 256;                                      // [0, 256): full[] and empty[] mbarriers, flags
+  l.qbuf = l.qs + al128((size_t)k * 4);            // scaled query, k floats
+  l.sc = l.qbuf + al128((size_t)2 * S * k * 4);    // split partials of two heads
+  l.stage = l.sc + al128((size_t)Lcap * 4);        // the head's scores
+  l.stage_bytes = al128((size_t)l.R * Lcap * 2);
+  l.total = l.stage + (size_t)NS * l.stage_bytes;
+  return l;
+}
+
+
+// MAXB runs of kSRun tokens per consumer thread: Lcap <= kSBlock * MAXB.
+template <int MAXB>
+__global__ void __launch_bounds__(kSThreads, IG_K23_MIN_CTAS) k23_score_select(
     const float* __restrict__ qsrc, int S, int B, int H, int k, const __half* __restrict__ Kpart,
     const int* __restrict__ L_valid, int Lcap, float scale, float alpha, int32_t* __restrict__ idx,
     int32_t* __restrict__ cnt, uint8_t* __restrict__ used, float* __restrict__ scores_out,
-    float* __restrict__ q_out, int* err) {
-  cg::cluster_group cluster = cg::this_cluster();
+    float* __restrict__ q_out, int NS, int* err) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ float red_f[kFThreads / 32];
-  __shared__ int red_i[kFThreads / 32];
-  // every CTA's chunk maximum and count, pushed here by their CTAs through distributed shared
-  // memory, so that after each exchange every CTA reads only its own shared memory
-  __shared__ float chunk_max[kFMaxChunks];
-  __shared__ int chunk_cnt[kFMaxChunks];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-  float* qs = reinterpret_cast<float*>(smem + 16);
-  __half* Ks = reinterpret_cast<__half*>(smem + 16 + ((k * 4 + 127) & ~127));
-  const int rank = (int)cluster.block_rank();
-  const int nranks = (int)cluster.num_blocks();
-  const int bh = blockIdx.y, b = bh / H, h = bh % H;
-  const int t0 = rank * kFT;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int L = L_valid[b];
-  if (L < 0 || L > Lcap) {
-    if (threadIdx.x == 0 && rank == 0) raise_error(err, IG_DEVERR_INDEX);
-    L = L < 0 ? 0 : Lcap;
-  }
-  // no CTA writes into another's shared memory before all of the cluster's CTAs run: arrive
-  // now, wait just before the first push (by then the wait is long satisfied)
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-  const int n_tok = max(0, min(kFT, L - t0));
-  const int n_copy = (n_tok + 7) & ~7;
-  const __half* rows = Kpart + ((size_t)bh * k) * Lcap + t0;
-  if (threadIdx.x == 0 && n_copy > 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_arrive_expect_tx(bar, (uint32_t)(k * n_copy * 2));
-    const uint64_t pol = l2_evict_first();
-    for (int c = 0; c < k; ++c) bulk_g2s_hint(Ks + (size_t)c * kFT, rows + (size_t)c * Lcap, n_copy * 2, bar, pol);
-  }
-  for (int c = threadIdx.x; c < k; c += blockDim.x) {
-    const int N = H * k;
-    const float a = sum_splits(qsrc + (size_t)b * N + h * k + c, (size_t)B * N, S);
-    qs[c] = a * scale;
-    if (q_out && rank == 0) q_out[(size_t)bh * k + c] = a;
-  }
-  __syncthreads();
-  const int tl = threadIdx.x * 4;
-  float sc[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  bool landed = true;
-  if (n_copy > 0) {
-    // a copy that does not land is reported and its chunk selects nothing; the CTA still
-    // takes part in every cluster barrier below
-    landed = mbar_wait_bounded(bar, 0, wait_limit(err));
-    if (!landed) {
-      if (threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
-      landed = mbar_wait_bounded(bar, 0);  // the default limit: copies land long before it
-    }
-    if (landed && tl < n_tok) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int c = 0; c < k; ++c) {
-        uint2 v = *reinterpret_cast<const uint2*>(Ks + (size_t)c * kFT + tl);
-        float2 f0 = h2_to_f2(v.x), f1 = h2_to_f2(v.y);
-        const float qc = qs[c];
-        acc[0] = fmaf(qc, f0.x, acc[0]);
-        acc[1] = fmaf(qc, f0.y, acc[1]);
-        acc[2] = fmaf(qc, f1.x, acc[2]);
-        acc[3] = fmaf(qc, f1.y, acc[3]);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) sc[j] = (t0 + tl + j < L) ? acc[j] : -INFINITY;
-    }
-  }
-  if (scores_out) {
-    const int t = t0 + tl;
-    if (t < Lcap) {
-      float4 o = make_float4(sc[0], sc[1], sc[2], sc[3]);
-      *reinterpret_cast<float4*>(scores_out + (size_t)bh * Lcap + t) = o;
-    }
-  }
-  // chunk maximum (fmaxf ignores NaN), then the head's maximum across the cluster
-  float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red_f[warp] = mx;
-  __syncthreads();
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  if (threadIdx.x < nranks) {
-    float cm = -INFINITY;
-    for (int w = 0; w < kFThreads / 32; ++w) cm = fmaxf(cm, red_f[w]);
-    *cluster.map_shared_rank(&chunk_max[rank], (unsigned)threadIdx.x) = cm;
-  }
-  cluster.sync();
-  float m = -INFINITY;
-  for (int r = 0; r < nranks; ++r) m = fmaxf(m, chunk_max[r]);
-  // flags in token order; a token past L_valid scored -inf and is never kept (for alpha = inf,
-  // (m - (-inf)) < inf is false, and with no valid token m - s is NaN)
-  bool f[4];
-  int mine = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int t = t0 + tl + j;
-    f[j] = (t < L) && !isnan(sc[j]) && ((m - sc[j]) < alpha);
-    mine += f[j] ? 1 : 0;
-  }
-  int incl = mine;
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) red_i[warp] = incl;
-  __syncthreads();
-  int before = incl - mine;
-  for (int w = 0; w < warp; ++w) before += red_i[w];
-  if (threadIdx.x < nranks) {
-    int tot = 0;
-    for (int w = 0; w < kFThreads / 32; ++w) tot += red_i[w];
-    *cluster.map_shared_rank(&chunk_cnt[rank], (unsigned)threadIdx.x) = tot;
-  }
-  cluster.sync();  // the last access to another CTA's shared memory is before this barrier
-  int offset = 0, total = 0;
-  for (int r = 0; r < nranks; ++r) {
-    const int c = chunk_cnt[r];
-    if (r < rank) offset += c;
-    total += c;
-  }
-  int pos = offset + before;
-  int32_t* io = idx + (size_t)bh * Lcap;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    if (f[j]) {
-      const int t = t0 + tl + j;
-      io[pos++] = t;
-      if (used) used[(size_t)b * Lcap + t] = 1;
-    }
-  }
-  if (rank == 0 && threadIdx.x == 0) cnt[bh] = total;
-  // a CTA whose copies never landed waits for them once more (bounded) before it leaves
-  if (!landed) mbar_wait_bounded(bar, 0);
-}
+  __shared__ float red_f[kSConsumerWarps];
+  __shared__ int red_i[kSConsumerWarps];
+  const SelLayout lay = sel_layout(S, k, Lcap, NS);
+  const int R = lay.R;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + kSMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kSMaxStages);
+  float* qs = reinterpret_cast<float*>(smem + lay.qs);
+  float* qbuf = reinterpret_cast<float*>(smem + lay.qbuf);
+  float* sc = reinterpret_cast<float*>(smem + lay.sc);
+  const int BH = B * H, N = H * k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto head_of = [&](int i) { return (int)blockIdx.x + i * (int)gridDim.x; };
+  auto len_of = [&](int bh) {
+    const int L = L_valid[bh / H];
+    return L < 0 ? 0 : (L > Lcap ? Lcap : L);
+  };
+  auto stage_ptr = [&](int st) { return reinterpret_cast<__half*>(smem + lay.stage + (size_t)st * lay.stage_bytes); };
 
-size_t fused_smem(int k) { return 16 + round_up((size_t)k * 4, 128) + (size_t)k * kFT * 2; }
+  if (head_of(0) >= BH) return;
+  if (tid == 0) {
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kSConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kSConsumerWarps) {
+    // ---------------- producer warp ----------------
+    const uint64_t pol = l2_evict_first();
+    int issued = 0;
+    for (int i = 0; head_of(i) < BH; ++i) {
+      const int bh = head_of(i);
+      const int L = len_of(bh);
+      if (L == 0) continue;
+      const int n_copy = (L + 7) & ~7;  // within Lcap: L <= Lcap, Lcap % 8 == 0
+      const __half* head_rows = Kpart + (size_t)bh * k * Lcap;
+      for (int c0 = 0; c0 < k; c0 += R) {
+        const int rows = min(R, k - c0);
+        const int st = issued % NS, use = issued / NS;
+        if (use > 0 && !mbar_wait_bounded(&empty[st], (uint32_t)(use - 1) & 1u)) {
+          // the consumers never released the stage: stop staging (their bounded waits end too)
+          if (lane == 0) {
+            raise_error(err, IG_DEVERR_TIMEOUT);
+            *abort_flag = 1;
+          }
+          return;
+        }
+        __half* dst = stage_ptr(st);
+        if (lane == 0) {
+          // the stage was last read through the generic proxy; order that before the async writes
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive_expect_tx(&full[st], (uint32_t)(rows * n_copy * 2));
+        }
+        __syncwarp();
+        if (lane < rows)
+          bulk_g2s_hint(dst + (size_t)lane * Lcap, head_rows + (size_t)(c0 + lane) * Lcap, n_copy * 2, &full[st], pol);
+        ++issued;
+      }
+    }
+    // stay until the consumers have released every stage that was filled
+    for (int u = issued > NS ? issued - NS : 0; u < issued; ++u)
+      mbar_wait_bounded(&empty[u % NS], (uint32_t)(u / NS) & 1u);
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  const uint32_t lim = wait_limit(err);
+  auto prefetch_q = [&](int bh, int half) {
+    const int b = bh / H, h = bh % H;
+    float* dst = qbuf + (size_t)half * S * k;
+    for (int e = tid; e < S * k; e += kSConsumers) {
+      const int sp = e / k, c = e - sp * k;
+      cp_async4(dst + e, qsrc + ((size_t)sp * B + b) * N + (size_t)h * k + c);
+    }
+    cp_async_commit();
+  };
+  prefetch_q(head_of(0), 0);
+  int g = 0;                          // stages consumed so far
+  for (int i = 0; head_of(i) < BH; ++i) {
+    const int bh = head_of(i), b = bh / H;
+    int L = L_valid[b];
+    if (L < 0 || L > Lcap) {
+      if (tid == 0) raise_error(err, IG_DEVERR_INDEX);
+      L = L < 0 ? 0 : Lcap;
+    }
+    // this head's query: the split partials summed in order, scaled once
+    cp_async_wait_all();
+    consumer_sync();
+    const float* qb = qbuf + (size_t)(i & 1) * S * k;
+    for (int c = tid; c < k; c += kSConsumers) {
+      float a = 0.f;
+      for (int sp = 0; sp < S; ++sp) a += qb[(size_t)sp * k + c];
+      qs[c] = a * scale;
+      if (q_out) q_out[(size_t)bh * k + c] = a;
+    }
+    consumer_sync();
+    if (head_of(i + 1) < BH) prefetch_q(head_of(i + 1), (i + 1) & 1);
+
+    // scores of this thread's token runs, row group by row group
+    float acc[kSRun * MAXB];
+#pragma unroll
+    for (int m = 0; m < kSRun * MAXB; ++m) acc[m] = 0.f;
+    bool ok = L > 0;
+    for (int c0 = 0; L > 0 && c0 < k; c0 += R, ++g) {
+      const int st = g % NS;
+      const uint32_t par = (uint32_t)(g / NS) & 1u;
+      bool landed = ok && !*abort_flag;
+      if (landed && !mbar_wait_bounded(&full[st], par, lim)) {
+        if (lane == 0) raise_error(err, IG_DEVERR_TIMEOUT);
+        landed = mbar_wait_bounded(&full[st], par);  // the default limit: copies land long before it
+        if (!landed) *abort_flag = 1;               // nothing more is waited for or released
+      }
+      ok = ok && landed;
+      if (landed) {
+        const __half* Ks = stage_ptr(st) + kSRun * tid;
+        const int rows = min(R, k - c0);
+        for (int r = 0; r < rows; ++r) {
+          const float qc = qs[c0 + r];
+          const __half* row = Ks + (size_t)r * Lcap;
+#pragma unroll
+          for (int m = 0; m < MAXB; ++m) {
+            // a run that starts below L lies within the copied ceil8(L) tokens
+            if (kSRun * tid + kSBlock * m < L) {
+              const uint4 v = *reinterpret_cast<const uint4*>(row + kSBlock * m);
+              const float2 f0 = h2_to_f2(v.x), f1 = h2_to_f2(v.y), f2 = h2_to_f2(v.z), f3 = h2_to_f2(v.w);
+              float* a = acc + kSRun * m;
+              a[0] = fmaf(qc, f0.x, a[0]);
+              a[1] = fmaf(qc, f0.y, a[1]);
+              a[2] = fmaf(qc, f1.x, a[2]);
+              a[3] = fmaf(qc, f1.y, a[3]);
+              a[4] = fmaf(qc, f2.x, a[4]);
+              a[5] = fmaf(qc, f2.y, a[5]);
+              a[6] = fmaf(qc, f3.x, a[6]);
+              a[7] = fmaf(qc, f3.y, a[7]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
+      }
+    }
+    // the scores to the score row (and out, when asked for), with the running maximum
+    float mx = -INFINITY;
+#pragma unroll
+    for (int m = 0; m < MAXB; ++m) {
+      const int t0 = kSRun * tid + kSBlock * m;
+      if (t0 < L) {
+#pragma unroll
+        for (int j = 0; j < kSRun; ++j) {
+          const float sj = (ok && t0 + j < L) ? acc[kSRun * m + j] : -INFINITY;
+          mx = fmaxf(mx, sj);  // fmaxf ignores NaN
+          if (t0 + j < L) {
+            sc[t0 + j] = sj;
+            if (scores_out) scores_out[(size_t)bh * Lcap + t0 + j] = sj;
+          }
+        }
+      }
+    }
+    // the head's maximum
+    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red_f[warp] = mx;
+    consumer_sync();
+    float m = -INFINITY;
+    for (int w = 0; w < kSConsumerWarps; ++w) m = fmaxf(m, red_f[w]);
+    // ordered compaction: warp w owns tokens [w seg, (w + 1) seg); a count pass, the warps'
+    // offsets, then a write pass.  With no valid token m is -inf and m - s is NaN: nothing kept.
+    const int seg = ((L + kSConsumerWarps - 1) / kSConsumerWarps + 31) / 32 * 32;
+    const int wa = min(L, warp * seg), we = min(L, wa + seg);
+    int wcount = 0;
+    for (int t0 = wa; t0 < we; t0 += 32) {
+      const int t = t0 + lane;
+      const bool f = t < we && !isnan(sc[t]) && (m - sc[t]) < alpha;
+      wcount += __popc(__ballot_sync(0xffffffffu, f));
+    }
+    if (lane == 0) red_i[warp] = wcount;
+    consumer_sync();
+    int pos = 0, total = 0;
+    for (int w = 0; w < kSConsumerWarps; ++w) {
+      if (w < warp) pos += red_i[w];
+      total += red_i[w];
+    }
+    int32_t* io = idx + (size_t)bh * Lcap;
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int t0 = wa; t0 < we; t0 += 32) {
+      const int t = t0 + lane;
+      const bool f = t < we && !isnan(sc[t]) && (m - sc[t]) < alpha;
+      const uint32_t bal = __ballot_sync(0xffffffffu, f);
+      if (f) {
+        io[pos + __popc(bal & lt)] = t;
+        if (used) used[(size_t)b * Lcap + t] = 1;
+      }
+      pos += __popc(bal);
+    }
+    if (tid == 0) cnt[bh] = total;
+    if (scores_out)
+      for (int t = L + tid; t < Lcap; t += kSConsumers) scores_out[(size_t)bh * Lcap + t] = -INFINITY;
+    consumer_sync();  // the score row and the reduction slots are reused by the next head
+  }
+  cp_async_wait_all();
+}
 
 }  // namespace
 
 // Fused score + select on the split partials qsrc [S][B][H*k] (the projection's output, or the
-// RoPE epilogue's [1][B][H*k]).  Requires Lcap <= 8 * 512.
+// RoPE epilogue's [1][B][H*k]).  Requires Lcap <= kSMaxLcap.
+template <int MAXB>
+ig_status launch_k23(cudaStream_t st, const float* qsrc, int S, int B, int H, int k, const uint16_t* Kpart,
+                     const int32_t* L_valid, int Lcap, float scale, float alpha, int32_t* idx, int32_t* cnt,
+                     uint8_t* used, float* scores, float* q_part) {
+  const long long heads = (long long)B * H;
+  const int sms = sm_count(st);
+  const int NS = kSMaxStages;
+  const SelLayout lay = sel_layout(S, k, Lcap, NS);
+  IG_REQUIRE(lay.total <= 220 * 1024, "k or Lcap too large for the fused selection (%zu bytes of shared memory)",
+             lay.total);
+  cudaError_t e = cudaFuncSetAttribute(k23_score_select<MAXB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)lay.total);
+  if (e != cudaSuccess) return cuda_fail(e, "fused select smem attribute");
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k23_score_select<MAXB>, kSThreads, lay.total);
+  if (e != cudaSuccess) return cuda_fail(e, "fused select occupancy");
+  if (per_sm < 1) per_sm = 1;
+  const long long slots = (long long)per_sm * sms;
+  const int grid = (int)(heads < slots ? heads : slots);
+  k23_score_select<MAXB><<<grid, kSThreads, lay.total, st>>>(qsrc, S, B, H, k, reinterpret_cast<const __half*>(Kpart),
+                                                            L_valid, Lcap, scale, alpha, idx, cnt, used, scores,
+                                                            q_part, NS, error_word());
+  IG_CHECK_LAUNCH("fused select launch");
+  return IG_OK;
+}
+
 ig_status launch_score_select(cudaStream_t st, const float* qsrc, int S, int B, int H, int k,
                               const uint16_t* Kpart, const int32_t* L_valid, int Lcap, float scale,
                               float alpha, int32_t* idx, int32_t* cnt, uint8_t* used, float* scores,
                               float* q_part) {
-  const int nch = (Lcap + kFT - 1) / kFT;
-  IG_REQUIRE(nch <= kFMaxChunks, "fused selection needs Lcap <= %d (got %d)", kFMaxChunks * kFT, Lcap);
-  const size_t sm = fused_smem(k);
-  IG_REQUIRE(sm <= 200 * 1024, "k too large for the fused selection");
-  cudaError_t e = cudaFuncSetAttribute(k23_score_select, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-  if (e != cudaSuccess) return cuda_fail(e, "fused select smem attribute");
+  IG_REQUIRE(Lcap <= kSMaxLcap, "fused selection needs Lcap <= %d (got %d)", kSMaxLcap, Lcap);
   if (used) {
-    e = cudaMemsetAsync(used, 0, (size_t)B * Lcap, st);
+    cudaError_t e = cudaMemsetAsync(used, 0, (size_t)B * Lcap, st);
     if (e != cudaSuccess) return cuda_fail(e, "clear used flags");
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(nch, B * H, 1);
-  cfg.blockDim = dim3(kFThreads, 1, 1);
-  cfg.dynamicSmemBytes = sm;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = nch;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, k23_score_select, qsrc, S, B, H, k, reinterpret_cast<const __half*>(Kpart),
-                         L_valid, Lcap, scale, alpha, idx, cnt, used, scores, q_part, error_word());
-  if (e != cudaSuccess) return cuda_fail(e, "fused select launch");
-  IG_CHECK_LAUNCH("fused select launch");
-  return IG_OK;
+  if (Lcap <= kSBlock)
+    return launch_k23<1>(st, qsrc, S, B, H, k, Kpart, L_valid, Lcap, scale, alpha, idx, cnt, used, scores, q_part);
+  if (Lcap <= 2 * kSBlock)
+    return launch_k23<2>(st, qsrc, S, B, H, k, Kpart, L_valid, Lcap, scale, alpha, idx, cnt, used, scores, q_part);
+  return launch_k23<4>(st, qsrc, S, B, H, k, Kpart, L_valid, Lcap, scale, alpha, idx, cnt, used, scores, q_part);
 }
 
 }  // namespace ig

@@ -33,34 +33,76 @@ ig_status launch_k1(cudaStream_t st, const __half* x, const __half* Wt, float* p
 
 
 // K1b: RoPE epilogue for one (b, h): q = sum of the split partials of x W_Q,h; rotate the
-// pairs (j, j + d/2) by p * theta^(-2j/d) (angle in float64); then q~p[c] = sum_j q_rot[j] A[h][j][c]
-// with A[h][:, S_h] staged in shared memory by coalesced loads and one warp per output c.
+// pairs (j, j + d/2) by the angle p * theta^(-2j/d) (the inverse frequencies come from the host
+// in float64; the angle is formed and reduced to [-pi, pi] in float64, then rotated in
+// float64); then q~p[c] = sum_j q_rot[j] A[h][j][c] with A[h][:, S_h] (a contiguous d x k
+// block) staged in shared memory by one bulk copy that overlaps the split sums, and one warp
+// per output c.
+constexpr int kRopeMaxHalf = 128;  // d <= 256
+struct InvFreq {
+  double v[kRopeMaxHalf];
+};
+
 __global__ void k1b_rope_project(const float* __restrict__ part, int S, int B, int H, int d, int k,
                                  const float* __restrict__ A_cols, const int* __restrict__ pos,
-                                 double theta, float* __restrict__ qp) {
-  extern __shared__ float sh[];
-  float* q = sh;           // d
-  float* qr = sh + d;      // d
-  float* As = sh + 2 * d;  // d * k
+                                 const __grid_constant__ InvFreq inv, float* __restrict__ qp, int* err) {
+  extern __shared__ __align__(16) float sh[];
+  const int dk = d * k;
+  float* As = sh;                                    // d * k (16-byte aligned: first)
+  float* q = sh + ((dk + 3) & ~3);                   // d
+  float* qr = q + d;                                 // d
+  uint64_t* bar = reinterpret_cast<uint64_t*>(qr + ((d + 1) & ~1));
   const int bh = blockIdx.x, b = bh / H, h = bh % H;
   const int N = H * d;
+  const float* Ah = A_cols + (size_t)h * dk;
+  // one bulk copy when the block is 16-byte aligned and a multiple of 16 bytes, else plain loads
+  const bool bulk = (reinterpret_cast<uintptr_t>(Ah) % 16) == 0 && (dk % 4) == 0;
+  if (bulk && threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(bar, (uint32_t)(dk * 4));
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(As)),
+        "l"(Ah), "r"(dk * 4), "r"(smem_addr(bar))
+        : "memory");
+  }
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
     q[j] = sum_splits(part + (size_t)b * N + h * d + j, (size_t)B * N, S);
   }
-  const float* Ah = A_cols + (size_t)h * d * k;
-  for (int i = threadIdx.x; i < d * k; i += blockDim.x) As[i] = Ah[i];
+  if (!bulk) {
+    for (int i0 = threadIdx.x; i0 < dk; i0 += 8 * blockDim.x) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = i0 + u * (int)blockDim.x < dk ? __ldg(Ah + i0 + u * blockDim.x) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * (int)blockDim.x < dk) As[i0 + u * blockDim.x] = v[u];
+    }
+  }
   __syncthreads();
   const int half = d / 2;
   const double p = (double)pos[b];
+  const double two_pi = 6.283185307179586476925286766559;
   for (int j = threadIdx.x; j < half; j += blockDim.x) {
-    double inv = pow(theta, -2.0 * (double)j / (double)d);
+    const double a = p * inv.v[j];
+    const double r = a - two_pi * rint(a / two_pi);
     double sn, cs;
-    sincos(p * inv, &sn, &cs);
+    sincos(r, &sn, &cs);
     const float lo = q[j], hi = q[j + half];
     qr[j] = (float)((double)lo * cs - (double)hi * sn);
     qr[j + half] = (float)((double)lo * sn + (double)hi * cs);
   }
-  __syncthreads();
+  bool landed = true;
+  if (bulk) {
+    landed = mbar_wait_bounded(bar, 0);
+    if (!landed && threadIdx.x == 0) raise_error(err, IG_DEVERR_TIMEOUT);
+  }
+  landed = __syncthreads_and(landed ? 1 : 0) != 0;
+  if (!landed) {
+    mbar_wait_bounded(bar, 0);  // let the copy land (bounded) before the CTA leaves
+    return;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int c = warp; c < k; c += nw) {
     float a = 0.f;
@@ -179,13 +221,16 @@ int projection_splits(int D) { return proj_splits(D); }
 
 ig_status launch_rope_project(cudaStream_t st, const float* part, int S, int B, int H, int d, int k,
                               const float* A_cols, const int* pos, float theta, float* qp) {
-  const size_t rope_smem = (size_t)(2 * d + d * k) * sizeof(float);
+  IG_REQUIRE(d / 2 <= kRopeMaxHalf, "RoPE head width d must be <= %d", 2 * kRopeMaxHalf);
+  InvFreq inv = {};
+  for (int j = 0; j < d / 2; ++j) inv.v[j] = pow((double)theta, -2.0 * (double)j / (double)d);
+  const size_t rope_smem = (size_t)(((d * k + 3) & ~3) + 2 * ((d + 1) & ~1)) * sizeof(float) + 16;
   if (rope_smem > 48 * 1024) {
     cudaError_t ae = cudaFuncSetAttribute(k1b_rope_project, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)rope_smem);
     if (ae != cudaSuccess) return cuda_fail(ae, "rope epilogue smem attribute");
   }
-  k1b_rope_project<<<B * H, 128, rope_smem, st>>>(part, S, B, H, d, k, A_cols, pos, (double)theta, qp);
+  k1b_rope_project<<<B * H, 128, rope_smem, st>>>(part, S, B, H, d, k, A_cols, pos, inv, qp, error_word());
   IG_CHECK_LAUNCH("rope epilogue launch");
   return IG_OK;
 }

@@ -512,3 +512,53 @@ def test_fused_speculate_select_rope(ig, alpha):
     for b in range(B):
         for h in range(H):
             assert np.array_equal(a1[b, h, :cn1[b, h]], a2[b, h, :cn2[b, h]])
+
+
+# the fused kernel against the oracle directly: its index sets, counts and use flags against
+# ora.select(ora.speculate(...)) in float64 (exempt: tokens within 1e-3 of the threshold), and
+# its scores (asked for) within the score tolerance; also a long context (Lcap 8192) and
+# lengths that end inside a chunk and inside a token pair
+FUSED_SHAPES = dict(SHAPES)
+FUSED_SHAPES["long-odd"] = (synth.scaled(synth.WORKLOADS["opt-6.7b"], name="long-odd", batch=3, heads=3,
+                                         hidden=384, prompt=8000, gen=0), 8192, [8191, 4097, 513])
+
+
+@functools.lru_cache(maxsize=2)
+def make_fused_case(name):
+    if name in SHAPES:
+        return make_case(name)
+    w, Lcap, Ls = FUSED_SHAPES[name]
+    L = np.array(Ls, dtype=np.int32)
+    K, _ = synth.pool_layer(w, 1, cap=Lcap)
+    cols = synth.skewed_columns(w, 1)
+    return dict(w=w, Lcap=Lcap, L=L, cols=cols, x=synth.layer_inputs(w, layers=1)[0],
+                Wqp=synth.skewed_partial_weight(w, 1), Kpart=ora.partial_key_cache(K, cols),
+                scale=np.float32(1.0 / math.sqrt(w.head_dim)))
+
+
+@pytest.mark.parametrize("name", list(FUSED_SHAPES))
+@pytest.mark.parametrize("alpha", [2.0, 4.0])
+def test_fused_speculate_select_matches_oracle(ig, name, alpha):
+    c = make_fused_case(name)
+    w = c["w"]
+    B, H, d, k, D, Lcap = w.batch, w.heads, w.head_dim, w.k, w.hidden, c["Lcap"]
+    ws = workspace(ig.ig_speculate_select_workspace_bytes(B, D, H, d, k, 0))
+    idx, cnt = empty((B, H, Lcap), torch.int32), empty((B, H), torch.int32)
+    used, scores = empty((B, Lcap), torch.uint8), empty((B, H, Lcap), torch.float32)
+    ig.ig_speculate_select(None, B, D, H, d, k, Lcap, dev(c["x"]), dev(c["Wqp"].T), None, None, 0.0,
+                           dev(c["Kpart"]), dev(c["L"]), float(c["scale"]), alpha, idx, cnt, used, scores, None, ws,
+                           ws.numel())
+    ig.ig_check()
+    qp = ora.partial_query(c["x"], c["Wqp"], H, k)
+    s_o = ora.speculate(qp, c["Kpart"], c["L"], c["scale"])
+    assert score_ok(host(scores), s_o, c["L"]) <= SCORE_TOL
+    want, want_cnt, want_used = ora.select(s_o, c["L"], alpha)
+    idx_g, cnt_g, used_g = host(idx), host(cnt), host(used)
+    exempt = index_sets_ok(idx_g, cnt_g, s_o, c["L"], alpha)
+    if exempt == 0:
+        assert np.array_equal(cnt_g, want_cnt)
+        for b in range(B):
+            for h in range(H):
+                assert np.array_equal(idx_g[b, h, :cnt_g[b, h]], want[b][h])
+        assert np.array_equal(used_g, want_used)
+    assert exempt <= 1e-3 * max(1, int(cnt_g.sum()))
