@@ -564,9 +564,8 @@ def run_ours(args, w, alpha):
     sel_rows = cnts[:, 1:].sum()                                          # layers 1.. gather
     ctx = np.array([w.prompt + args.warmup + i for i in range(args.steps)], dtype=np.float64)
     f = sel_rows / (args.steps * (w.layers - 1) * w.batch * w.heads * ctx.mean())
-    # K + V bytes of a row over the link (codes and scales of a quantized row)
-    row_link = (2 * (w.head_dim + 4) if args.pool_fp8 else 2 * (w.head_dim // 2 + 4) if args.pool_int4
-                else 2 * w.head_dim * 2)
+    # K + V bytes of a row over the link (a quantized row's codes; its scales are read from HBM)
+    row_link = (2 * w.head_dim if args.pool_fp8 else w.head_dim if args.pool_int4 else 2 * w.head_dim * 2)
     G_total = sel_rows * row_link                                         # over the link
     gather_ms_per_launch = stage[0] / max(stage_n[0], 1)
     G_per_launch = G_total / max(stage_n[0], 1)
@@ -624,8 +623,9 @@ def run_ours(args, w, alpha):
             "config": dict(workload_config(w, alpha), cuda_graph=bool(args.graph),
                            fused_select=bool(args.fused_select), fused_fetch=fused_fetch,
                            selection=args.policy, batched_append=bool(args.batched_append),
-                           append_on_fetch=bool(args.append_on_fetch), pool_dtype=("fp8-e4m3 + fp32 row scale" if args.pool_fp8 else
-                                       "int4 + fp32 row scale" if args.pool_int4 else "fp16"),
+                           append_on_fetch=bool(args.append_on_fetch), pool_dtype=("fp8-e4m3 codes in the pinned pool, fp32 row scales in HBM" if args.pool_fp8 else
+                                       "int4 codes in the pinned pool, fp32 row scales in HBM" if args.pool_int4
+                                       else "fp16"),
                            pool_policy=args.pool_policy if w.pool_frac < 1 else None,
                            sm_split=({"fetch_sms": dec.fetch_sms, "compute_sms": dec.compute_sms}
                                      if args.sm_split else None)),

@@ -12,7 +12,8 @@
  *     for the calling thread.  Nothing aborts the process or traps the GPU.
  *   - "dev" pointers are device memory (or, where stated, host memory the GPU can map);
  *     "host" pointers are ordinary host memory.  The caller owns every buffer it passes.
- *     The library owns only the pinned KV pool (ig_pool_create / ig_pool_destroy).
+ *     The library owns only the KV pool (ig_pool_create / ig_pool_destroy): its pinned host
+ *     rows and, for a quantized pool, the device-memory array of the rows' scales.
  *   - Device calls are asynchronous on the caller's cudaStream_t, passed as void* (NULL =
  *     legacy default stream).  Argument and launch errors are returned at once; a guard
  *     that trips inside a kernel (an index out of range, a bounded wait that ran out) is
@@ -239,22 +240,28 @@ typedef struct ig_pool ig_pool;
  * rows (ig_pool_kv, ig_pool_write, ig_gather_kv, ig_gather_attend, ig_append_kv with this
  * pool) then return IG_ERR_INVALID. */
 #define IG_POOL_NO_STORAGE 1
-/* IG_POOL_FP8: each (token, head) row stored as one record of 2d + 16 bytes: the key's d e4m3
- * codes, the value's d codes, the key's and the value's fp32 scale, 8 bytes of padding (the
- * combination of a quantized pool with selective prefetch proposed as follow-up work).  Each
- * row is quantized on its way in (ig_pool_write, ig_append_kv): scale = amax / 448, codes =
- * round-to-nearest-even e4m3 of x * (448 / amax) in fp32, saturating; a row of zeros has scale
- * 0.  ig_gather_kv reads one contiguous record per selected row and dequantizes it (code value x
- * scale, rounded to fp16) into the usual fp16 staging rows, so the link carries 2d + 16 bytes
- * per row instead of 4d; the partial key cache (speculation) stays fp16.  d must be 64 or 128;
- * ig_pool_kv, ig_gather_attend and the prefill refuse quantized pools (use ig_pool_kv8). */
+/* IG_POOL_FP8: each (token, head) row stored as one record of 2d bytes of codes in the pinned
+ * pool, the key's d e4m3 codes then the value's d codes, and the row's two fp32 scales (key,
+ * value) in a device-memory array the pool allocates on the device current at creation (the
+ * combination of a quantized pool with selective prefetch proposed as follow-up work).  A
+ * record is whole 128-byte lines (256 bytes at d = 128), so each fetched row is two full lines
+ * over the host link; the 8 bytes of scales per row stay resident in HBM (0.7 GB at the
+ * OPT-30B shape).  Each row is quantized on its way in (ig_pool_write, ig_append_kv): scale =
+ * amax / 448, codes = round-to-nearest-even e4m3 of x * (448 / amax) in fp32, saturating; a
+ * row of zeros has scale 0.  ig_gather_kv reads one record per selected row and its scales
+ * and dequantizes (code value x scale, rounded to fp16) into the usual fp16 staging rows, so
+ * the link carries 2d bytes per row instead of 4d; the partial key cache (speculation) stays
+ * fp16.  d must be 64 or 128; the pool's kernels must run on the device that holds its scales
+ * (else IG_ERR_INVALID); ig_pool_kv, ig_gather_attend and the prefill refuse quantized pools
+ * (use ig_pool_kv8). */
 #define IG_POOL_FP8 2
-/* IG_POOL_INT4: the same record with signed 4-bit codes (the format the follow-up work names):
- * d / 2 bytes of key codes, d / 2 of value codes, the two fp32 scales, 8 bytes of padding
- * (d + 16 bytes).  scale = amax / 7, codes = the nearest integer (ties to even) of x * (7 / amax)
- * in fp32, in [-7, 7], two per byte with element 2j in the low nibble of byte j (two's
- * complement); a row of zeros has scale 0.  The gather dequantizes as for IG_POOL_FP8; the link
- * carries d + 16 bytes per row.  Excludes IG_POOL_FP8; d must be 64 or 128. */
+/* IG_POOL_INT4: the same split with signed 4-bit codes (the format the follow-up work names):
+ * a record of d / 2 bytes of key codes then d / 2 of value codes (d bytes: one 128-byte line at
+ * d = 128) in the pinned pool, the two fp32 scales in device memory.  scale = amax / 7, codes =
+ * the nearest integer (ties to even) of x * (7 / amax) in fp32, in [-7, 7], two per byte with
+ * element 2j in the low nibble of byte j (two's complement); a row of zeros has scale 0.  The
+ * gather dequantizes as for IG_POOL_FP8; the link carries d bytes per row.  Excludes
+ * IG_POOL_FP8; d must be 64 or 128. */
 #define IG_POOL_INT4 4
 
 ig_status ig_pool_create(int layers, int B, int H, int d, int cap, ig_pool** out);
@@ -267,10 +274,15 @@ ig_status ig_pool_destroy(ig_pool* pool);
 /* Host pointers (also valid on the device) to one layer's K and V arrays. */
 ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, uint16_t** V);
 
-/* Quantized (fp8 or int4) pools: host pointer (also valid on the device) to one layer's records
- * [B][H][cap][record_bytes] (layouts under IG_POOL_FP8 and IG_POOL_INT4) and the record size
- * (2d + 16 or d + 16). */
-ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** records, int* record_bytes);
+/* Quantized (fp8 or int4) pools: host pointer (also valid on the device) to one layer's code
+ * records [B][H][cap][record_bytes] (layouts under IG_POOL_FP8 and IG_POOL_INT4), the record
+ * size (2d or d), and (when scales is not NULL) the device pointer to that layer's scales
+ * [B][H][cap][2] fp32 (key, value). */
+ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** records, int* record_bytes,
+                      float** scales);
+/* Copies one layer's scales of a quantized pool to host memory out [B][H][cap][2] fp32
+ * (synchronous). */
+ig_status ig_pool_read_scales(const ig_pool* pool, int layer, float* out);
 
 /* Copies one layer's K and V ([B][H][cap][d] fp16 each, from device or host memory) into
  * the pool, asynchronously on `stream`.  A quantized pool quantizes them in a kernel, so for it
@@ -308,8 +320,9 @@ ig_status ig_pool_evictions(const ig_pool* pool, int layer, int b, int64_t* out)
  * asynchronously and overlapped with layer i-1's compute).  The kernel reads the mapped
  * pinned pool directly (16-byte zero-copy loads over the host link); issue it on a side
  * stream.  max_ctas bounds its grid (0 = library default: a quarter of the SMs, or two CTAs
- * per SM of the stream's own partition after ig_sm_split_create) so that it leaves SMs to the
- * compute stream.  Quantized pools (IG_POOL_FP8, IG_POOL_INT4) are dequantized to fp16 here.
+ * per SM of the stream's own partition after ig_sm_split_create, twice that for a quantized
+ * pool) so that it leaves SMs to the compute stream.  Quantized pools (IG_POOL_FP8,
+ * IG_POOL_INT4) are dequantized to fp16 here (codes over the link, scales from HBM).
  *   idx, cnt  dev, from ig_select (slots must be < cap)
  *   Kg, Vg    dev fp16 [B][H][Lcap][d] out  rows j < cnt[b][h] = pool rows idx[b][h][j] */
 ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, int B, int H, int d,

@@ -21,7 +21,13 @@ namespace {
 
 constexpr int kGatherThreads = 256;
 constexpr int kUnroll = 8;  // 8 rows x (K, V) in flight per lane: 205 GB/s alone at 38 CTAs
-constexpr int kUnroll8 = 16;  // quantized records: one 16-byte load per lane and row, so twice the rows
+#ifndef IG_GQ_UNROLL
+#define IG_GQ_UNROLL 4
+#endif
+#ifndef IG_GQ_MIN_CTAS
+#define IG_GQ_MIN_CTAS 4
+#endif
+constexpr int kUnroll8 = IG_GQ_UNROLL;  // quantized records: one 16-byte load per lane and row, so more rows
 constexpr int kMaxGatherUnits = 32768;  // (units + 1) ints of shared memory: 128 KB
 
 __global__ void __launch_bounds__(kGatherThreads) k4_gather(
@@ -117,16 +123,18 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather(
   }
 }
 
-// Quantized pool (one record per (token, head): K codes, V codes, their two fp32 scales): the
-// same balanced row split; a row is one contiguous record of 2 d BITS / 8 + 16 bytes, read by
+// Quantized pool (one record of codes per (token, head) in the pinned pool: K codes, then V
+// codes; the two fp32 scales of the row in device memory): the same balanced row split; a row
+// is one contiguous record of 2 d BITS / 8 bytes (whole 128-byte lines at d = 128), read by
 // vpr = 2 d BITS / 128 lanes (16 bytes of codes each: the first half of the lanes the key, the
-// rest the value) plus each lane's 4-byte scale from the same record, and dequantized to fp16
-// (code value x scale in fp32, rounded to nearest) into the usual staging layout.  BITS = 8:
-// 16 e4m3 codes per lane; BITS = 4: 32 signed 4-bit codes per lane (element 2j in the low
-// nibble of byte j).
+// rest the value) plus each lane's scale from the device-resident scale array, and
+// dequantized to fp16 (code value x scale in fp32, rounded to nearest) into the usual staging
+// layout.  BITS = 8: 16 e4m3 codes per lane; BITS = 4: 32 signed 4-bit codes per lane
+// (element 2j in the low nibble of byte j).
 template <int BITS>
-__global__ void __launch_bounds__(kGatherThreads) k4_gather_q(
-    const uint8_t* __restrict__ Rec, int rec, int units, int cap, int vpr, int Lcap, const int32_t* __restrict__ idx,
+__global__ void __launch_bounds__(kGatherThreads, IG_GQ_MIN_CTAS) k4_gather_q(
+    const uint8_t* __restrict__ Rec, int rec, const float* __restrict__ Sc, int units, int cap, int vpr, int Lcap,
+    const int32_t* __restrict__ idx,
     const int32_t* __restrict__ cnt, uint4* __restrict__ Kg, uint4* __restrict__ Vg, int* err) {
   extern __shared__ int pre[];
   __shared__ int wsum[kGatherThreads / 32];
@@ -199,9 +207,9 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather_q(
 #pragma unroll
     for (int q = 0; q < kUnroll8; ++q) {
       if (slot[q] >= 0) {
-        const uint8_t* rp = Rec + ((size_t)unit[q] * cap + slot[q]) * rec;
-        cd[q] = ld_nc_v4(rp + (size_t)v * 16);
-        sc[q] = __ldg(reinterpret_cast<const float*>(rp + 2 * 16 * half) + (is_v ? 1 : 0));
+        const size_t rw = (size_t)unit[q] * cap + slot[q];
+        cd[q] = ld_nc_v4(Rec + rw * rec + (size_t)v * 16);
+        sc[q] = __ldg(Sc + 2 * rw + (is_v ? 1 : 0));
       }
     }
 #pragma unroll
@@ -241,6 +249,10 @@ __global__ void __launch_bounds__(kGatherThreads) k4_gather_q(
 }  // namespace
 }  // namespace ig
 
+namespace ig {
+ig_status check_pool_device(const ig_pool* pool);
+}
+
 using namespace ig;
 
 extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, int B, int H,
@@ -258,7 +270,9 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
   const int units = B * H;
   IG_REQUIRE(units <= kMaxGatherUnits, "B*H = %d exceeds %d", units, kMaxGatherUnits);
   IG_REQUIRE((long long)units * Lcap < (1ll << 31), "B*H*Lcap must stay below 2^31 rows");
-  int grid = max_ctas > 0 ? max_ctas : fetch_grid(as_stream(stream));
+  // a quantized fetch also dequantizes every row: by default it takes twice the CTAs of the
+  // fp16 fetch (OPT-30B, int4 pool: 76 CTAs move 138 GB/s live against 116 for 38)
+  int grid = max_ctas > 0 ? max_ctas : (pool->qbits ? 2 : 1) * fetch_grid(as_stream(stream));
   if (grid < 1) grid = 1;
   const size_t smem = (size_t)(units + 1) * sizeof(int);
   if (smem > 48 * 1024) {
@@ -266,6 +280,7 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
     if (e != cudaSuccess) return cuda_fail(e, "gather smem attribute");
   }
   if (pool->qbits) {
+    if (ig_status dst = check_pool_device(pool); dst != IG_OK) return dst;
     const int vprq = 2 * (d * pool->qbits / 8) / 16;  // lanes per record (16 bytes of codes each: K, then V)
     auto kern = pool->qbits == 8 ? k4_gather_q<8> : k4_gather_q<4>;
     if (smem > 48 * 1024) {
@@ -274,8 +289,8 @@ extern "C" ig_status ig_gather_kv(void* stream, const ig_pool* pool, int layer, 
     }
     const size_t rows = (size_t)B * H * pool->cap, r0 = (size_t)layer * rows;
     kern<<<grid, kGatherThreads, smem, as_stream(stream)>>>(
-        pool->R + r0 * pool->rec, pool->rec, units, pool->cap, vprq, Lcap, idx, cnt, reinterpret_cast<uint4*>(Kg),
-        reinterpret_cast<uint4*>(Vg), error_word());
+        pool->R + r0 * pool->rec, pool->rec, pool->S + r0 * 2, units, pool->cap, vprq, Lcap, idx, cnt,
+        reinterpret_cast<uint4*>(Kg), reinterpret_cast<uint4*>(Vg), error_word());
     IG_CHECK_LAUNCH("quantized gather launch");
     return IG_OK;
   }

@@ -108,24 +108,23 @@ __device__ void quantize_row(const __half* __restrict__ x, uint8_t* __restrict__
   if (lane == 0) *scale = amax > 0.f ? amax / kMax : 0.f;
 }
 
-// Pool write of a quantized pool: rows [rows][d] fp16 (device-accessible) -> records (K and V
-// codes, then their scales).
+// Pool write of a quantized pool: rows [rows][d] fp16 (device-accessible) -> code records (K,
+// then V codes) in the pinned pool and the two scales of each row in device memory.
 template <int BITS, int PER>
 __global__ void k_quantize_rows(const __half* __restrict__ K, const __half* __restrict__ V, size_t rows,
-                                uint8_t* __restrict__ R, int rec) {
+                                uint8_t* __restrict__ R, int rec, float* __restrict__ S) {
   constexpr int D = 32 * PER, CB = D * BITS / 8;
   const size_t r = (size_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
   if (r >= rows) return;
   uint8_t* rr = R + r * rec;
-  float* sc = reinterpret_cast<float*>(rr + 2 * CB);
-  quantize_row<BITS, PER>(K + r * D, rr, sc);
-  quantize_row<BITS, PER>(V + r * D, rr + CB, sc + 1);
+  quantize_row<BITS, PER>(K + r * D, rr, S + 2 * r);
+  quantize_row<BITS, PER>(V + r * D, rr + CB, S + 2 * r + 1);
 }
 
 // Append into a quantized pool: one warp per (b, h) quantizes the current token's key and value
 // into its record.
 template <int BITS, int PER>
-__global__ void k6_append_q(uint8_t* __restrict__ R, int rec, int units, int cap, int H,
+__global__ void k6_append_q(uint8_t* __restrict__ R, int rec, float* __restrict__ S, int units, int cap, int H,
                             const int32_t* __restrict__ slot, const __half* __restrict__ k_new,
                             const __half* __restrict__ v_new, int* err) {
   constexpr int D = 32 * PER, CB = D * BITS / 8;
@@ -137,10 +136,10 @@ __global__ void k6_append_q(uint8_t* __restrict__ R, int rec, int units, int cap
     if ((threadIdx.x & 31) == 0) raise_error(err, IG_DEVERR_INDEX);
     return;
   }
-  uint8_t* rr = R + ((size_t)bh * cap + sl) * rec;
-  float* sc = reinterpret_cast<float*>(rr + 2 * CB);
-  quantize_row<BITS, PER>(k_new + (size_t)bh * D, rr, sc);
-  quantize_row<BITS, PER>(v_new + (size_t)bh * D, rr + CB, sc + 1);
+  const size_t row = (size_t)bh * cap + sl;
+  uint8_t* rr = R + row * rec;
+  quantize_row<BITS, PER>(k_new + (size_t)bh * D, rr, S + 2 * row);
+  quantize_row<BITS, PER>(v_new + (size_t)bh * D, rr + CB, S + 2 * row + 1);
 }
 
 // Appends of every layer's current token in one launch (grid: (b, h) x layer), run once the
@@ -157,7 +156,7 @@ struct AppendLayers {
 template <int BITS, int PER>
 __global__ void __launch_bounds__(64) k6_append_layers(
     const AppendLayers P, uint4* __restrict__ Kp, uint4* __restrict__ Vp, uint8_t* __restrict__ R, int rec,
-    int cap, int H, int d, int Lcap,
+    float* __restrict__ S, int cap, int H, int d, int Lcap,
     int units, const int32_t* __restrict__ slot, const __half* __restrict__ k_new,
     const __half* __restrict__ v_new, uint4* __restrict__ Kd, uint4* __restrict__ Vd, int* err) {
   const int bh = blockIdx.x, l = blockIdx.y, b = bh / H, h = bh % H;
@@ -189,9 +188,8 @@ __global__ void __launch_bounds__(64) k6_append_layers(
     } else {
       constexpr int CB = 32 * PER * BITS / 8;
       uint8_t* rr = R + row * rec;
-      float* sc = reinterpret_cast<float*>(rr + 2 * CB);
-      if (threadIdx.x < 32) quantize_row<BITS, PER>(kn, rr, sc);
-      else quantize_row<BITS, PER>(vn, rr + CB, sc + 1);
+      if (threadIdx.x < 32) quantize_row<BITS, PER>(kn, rr, S + 2 * row);
+      else quantize_row<BITS, PER>(vn, rr + CB, S + 2 * row + 1);
     }
   }
   __half* kp = P.Kpart[l];
@@ -252,13 +250,25 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
     cudaError_t e;
     if (qbits) {
       p->qbits = qbits;
-      p->rec = 2 * (d * qbits / 8) + 16;
+      p->rec = 2 * (d * qbits / 8);
       e = alloc(reinterpret_cast<void**>(&p->R), nrows * (size_t)p->rec);
       if (e != cudaSuccess) {
         cudaGetLastError();
         delete p;
         return fail(IG_ERR_OOM, "pinned allocation of the quantized pool (%zu bytes) failed: %s", nrows * (size_t)p->rec,
                     cudaGetErrorString(e));
+      }
+      // the scales stay in device memory, so that the link carries whole lines of codes only
+      e = cudaGetDevice(&p->sdev);
+      if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&p->S), nrows * 2 * sizeof(float));
+      if (e == cudaSuccess) e = cudaMemset(p->S, 0, nrows * 2 * sizeof(float));
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        cudaFreeHost(p->R);
+        if (p->S) cudaFree(p->S);
+        delete p;
+        return fail(IG_ERR_OOM, "device allocation of the quantized pool's scales (%zu bytes) failed: %s",
+                    nrows * 2 * sizeof(float), cudaGetErrorString(e));
       }
     } else {
       e = alloc(reinterpret_cast<void**>(&p->K), elems * 2);
@@ -296,6 +306,7 @@ extern "C" ig_status ig_pool_create_ex(int layers, int B, int H, int d, int cap,
   } catch (...) {
     for (void* q : {(void*)p->K, (void*)p->V, (void*)p->R})
       if (q) cudaFreeHost(q);
+    if (p->S) cudaFree(p->S);
     delete p;
     return fail(IG_ERR_OOM, "host allocation of the pool manager failed");
   }
@@ -315,6 +326,14 @@ extern "C" ig_status ig_pool_destroy(ig_pool* pool) {
     const cudaError_t e = cudaFreeHost(q);
     if (first == cudaSuccess) first = e;
   }
+  if (pool->S) {
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e == cudaSuccess && cur != pool->sdev) e = cudaSetDevice(pool->sdev);
+    if (e == cudaSuccess) e = cudaFree(pool->S);
+    if (cur != pool->sdev) cudaSetDevice(cur);
+    if (first == cudaSuccess) first = e;
+  }
   delete pool;
   if (first != cudaSuccess) return cuda_fail(first, "free pool memory");
   return IG_OK;
@@ -331,19 +350,45 @@ extern "C" ig_status ig_pool_kv(const ig_pool* pool, int layer, uint16_t** K, ui
   return IG_OK;
 }
 
-extern "C" ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** records, int* record_bytes) {
+extern "C" ig_status ig_pool_kv8(const ig_pool* pool, int layer, uint8_t** records, int* record_bytes,
+                                  float** scales) {
   IG_REQUIRE(pool && records && record_bytes, "null argument");
   IG_REQUIRE(pool->qbits, "not a quantized pool");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t rows = (size_t)pool->B * pool->H * pool->cap;
   *records = pool->R + (size_t)layer * rows * pool->rec;
   *record_bytes = pool->rec;
+  if (scales) *scales = pool->S + (size_t)layer * rows * 2;
   return IG_OK;
 }
+
+extern "C" ig_status ig_pool_read_scales(const ig_pool* pool, int layer, float* out) {
+  IG_REQUIRE(pool && out, "null argument");
+  IG_REQUIRE(pool->qbits, "not a quantized pool");
+  IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+  const size_t rows = (size_t)pool->B * pool->H * pool->cap;
+  cudaError_t e = cudaMemcpy(out, pool->S + (size_t)layer * rows * 2, rows * 2 * sizeof(float), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read the pool's scales");
+  return IG_OK;
+}
+
+namespace ig {
+// A quantized pool's scales live on one device: its kernels must run there.
+ig_status check_pool_device(const ig_pool* pool) {
+  if (!pool || !pool->qbits) return IG_OK;
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "current device");
+  IG_REQUIRE(cur == pool->sdev, "the quantized pool's scales are on device %d, the current device is %d", pool->sdev,
+             cur);
+  return IG_OK;
+}
+}  // namespace ig
 
 extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const uint16_t* K,
                                    const uint16_t* V) {
   IG_REQUIRE(pool && K && V, "null argument");
+  if (ig_status dst = check_pool_device(pool); dst != IG_OK) return dst;
   IG_REQUIRE(pool->storage, "the pool was created without storage");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
   const size_t le = (size_t)pool->B * pool->H * pool->cap * pool->d;
@@ -365,13 +410,14 @@ extern "C" ig_status ig_pool_write(ig_pool* pool, void* stream, int layer, const
     auto Kh = reinterpret_cast<const __half*>(K);
     auto Vh = reinterpret_cast<const __half*>(V);
     uint8_t* R0 = pool->R + r0 * pool->rec;
+    float* S0 = pool->S + r0 * 2;
     const bool d128 = pool->d == 128;
     if (pool->qbits == 8) {
-      if (d128) k_quantize_rows<8, 4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
-      else k_quantize_rows<8, 2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
+      if (d128) k_quantize_rows<8, 4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec, S0);
+      else k_quantize_rows<8, 2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec, S0);
     } else {
-      if (d128) k_quantize_rows<4, 4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
-      else k_quantize_rows<4, 2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec);
+      if (d128) k_quantize_rows<4, 4><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec, S0);
+      else k_quantize_rows<4, 2><<<blocks, 32 * wpb, 0, s>>>(Kh, Vh, rows, R0, pool->rec, S0);
     }
     IG_CHECK_LAUNCH("quantized pool write launch");
     return IG_OK;
@@ -399,21 +445,23 @@ extern "C" ig_status ig_append_kv(void* stream, ig_pool* pool, int layer, int B,
     IG_REQUIRE(pool->storage, "the pool was created without storage");
     IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
     IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
+    if (ig_status dst = check_pool_device(pool); dst != IG_OK) return dst;
     if (pool->qbits) {  // the quantized row goes to the pool here; the kernel below does the rest
       const size_t rows = (size_t)B * H * pool->cap, r0 = (size_t)layer * rows;
       const int units = B * H, wpb = 8;
       auto kn = reinterpret_cast<const __half*>(k_new);
       auto vn = reinterpret_cast<const __half*>(v_new);
       uint8_t* R0 = pool->R + r0 * pool->rec;
+      float* S0 = pool->S + r0 * 2;
       const unsigned g = (unsigned)((units + wpb - 1) / wpb);
       cudaStream_t s = as_stream(stream);
       int* err = error_word();
       if (pool->qbits == 8) {
-        if (d == 128) k6_append_q<8, 4><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, units, pool->cap, H, slot, kn, vn, err);
-        else k6_append_q<8, 2><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, units, pool->cap, H, slot, kn, vn, err);
+        if (d == 128) k6_append_q<8, 4><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, S0, units, pool->cap, H, slot, kn, vn, err);
+        else k6_append_q<8, 2><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, S0, units, pool->cap, H, slot, kn, vn, err);
       } else {
-        if (d == 128) k6_append_q<4, 4><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, units, pool->cap, H, slot, kn, vn, err);
-        else k6_append_q<4, 2><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, units, pool->cap, H, slot, kn, vn, err);
+        if (d == 128) k6_append_q<4, 4><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, S0, units, pool->cap, H, slot, kn, vn, err);
+        else k6_append_q<4, 2><<<g, 32 * wpb, 0, s>>>(R0, pool->rec, S0, units, pool->cap, H, slot, kn, vn, err);
       }
       IG_CHECK_LAUNCH("quantized append launch");
       if (!Kpart && !Kdense) return IG_OK;
@@ -440,6 +488,7 @@ extern "C" ig_status ig_append_kv_layers(void* stream, ig_pool* pool, int layers
   IG_REQUIRE(pool && pool->storage, "a pool with storage is needed");
   IG_REQUIRE(layers >= 1 && layers <= pool->layers && layers <= kMaxAppendLayers, "bad layer count %d", layers);
   IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
+  if (ig_status dst = check_pool_device(pool); dst != IG_OK) return dst;
   IG_REQUIRE(Lcap > 0 && slot && k_new && v_new, "bad Lcap or null pointer");
   IG_REQUIRE((Kdense == nullptr) == (Vdense == nullptr), "Kdense and Vdense go together");
   IG_REQUIRE(aligned(k_new, 16) && aligned(v_new, 16), "k_new, v_new must be 16-byte aligned");
@@ -461,21 +510,22 @@ extern "C" ig_status ig_append_kv_layers(void* stream, ig_pool* pool, int layers
   int* err = error_word();
   if (!pool->qbits) {
     k6_append_layers<0, 1><<<grid, 64, 0, st>>>(P, reinterpret_cast<uint4*>(pool->Kdev),
-                                               reinterpret_cast<uint4*>(pool->Vdev), nullptr, 0, pool->cap, H, d, Lcap,
+                                               reinterpret_cast<uint4*>(pool->Vdev), nullptr, 0, nullptr, pool->cap, H, d,
+                                               Lcap,
                                                units, slot, kn, vn, Kd, Vd, err);
   } else if (pool->qbits == 8) {
     if (d == 128)
-      k6_append_layers<8, 4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+      k6_append_layers<8, 4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->S, pool->cap, H, d, Lcap, units,
                                                  slot, kn, vn, Kd, Vd, err);
     else
-      k6_append_layers<8, 2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+      k6_append_layers<8, 2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->S, pool->cap, H, d, Lcap, units,
                                                  slot, kn, vn, Kd, Vd, err);
   } else {
     if (d == 128)
-      k6_append_layers<4, 4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+      k6_append_layers<4, 4><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->S, pool->cap, H, d, Lcap, units,
                                                  slot, kn, vn, Kd, Vd, err);
     else
-      k6_append_layers<4, 2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->cap, H, d, Lcap, units,
+      k6_append_layers<4, 2><<<grid, 64, 0, st>>>(P, nullptr, nullptr, pool->R, pool->rec, pool->S, pool->cap, H, d, Lcap, units,
                                                  slot, kn, vn, Kd, Vd, err);
   }
   IG_CHECK_LAUNCH("batched append launch");

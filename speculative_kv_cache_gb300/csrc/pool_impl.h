@@ -10,9 +10,12 @@ struct ig_pool {
   int policy = 0;            // IG_POOL_COUNTER, IG_POOL_FIFO or IG_POOL_LRU
   bool storage = true;       // false: the slot manager only, no K/V rows
   int qbits = 0;             // 0: fp16 rows; 8: e4m3 codes, 4: int4 codes, one fp32 scale per row
-  uint8_t* R = nullptr;      // quantized pools: pinned, mapped records [layers][B][H][cap][rec]:
-  int rec = 0;               //   K codes, V codes (d * qbits / 8 bytes each), K scale, V scale
-                             //   (fp32), 8 B pad
+  uint8_t* R = nullptr;      // quantized pools: pinned, mapped code records [layers][B][H][cap][rec]:
+  int rec = 0;               //   K codes, then V codes (d * qbits / 8 bytes each; rec = 128 or 256
+                             //   bytes at d = 128, whole 128-byte lines)
+  float* S = nullptr;        // quantized pools: the rows' fp32 scales in device memory
+                             //   [layers][B][H][cap][2] (K, V)
+  int sdev = -1;             // the device that holds S
   uint16_t* K = nullptr;     // pinned, mapped host memory [layers][B][H][cap][d]
   uint16_t* V = nullptr;
   uint16_t* Kdev = nullptr;  // the same memory as seen from the device

@@ -84,7 +84,8 @@ _sig("ig_select", _i, _vp, _i, _i, _i, _vp, _vp, _f, _i, _f, _vp, _vp, _vp, _vp,
 _sig("ig_pool_create", _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_create_ex", _i, _i, _i, _i, _i, _i, _i, _i, C.POINTER(_vp))
 _sig("ig_pool_slot_tokens", _i, _vp, _i, _i, _vp)
-_sig("ig_pool_kv8", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_i))
+_sig("ig_pool_kv8", _i, _vp, _i, C.POINTER(_vp), C.POINTER(_i), C.POINTER(_vp))
+_sig("ig_pool_read_scales", _i, _vp, _i, _vp)
 _sig("ig_pool_evictions", _i, _vp, _i, _i, C.POINTER(C.c_int64))
 _sig("ig_append_kv_layers", _i, _vp, _vp, _i, _i, _i, _i, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp)
 _sig("ig_eviction_misses", _i, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp)
@@ -284,29 +285,36 @@ def ig_pool_counters(pool, layer, b, out):
 
 
 def ig_pool_kv8(pool, layer):
-    """fp8 pools: host address (also valid on the device) of one layer's records, and their size."""
-    r, n = _vp(), _i(0)
-    _ok(_lib.ig_pool_kv8(pool, layer, C.byref(r), C.byref(n)), "ig_pool_kv8")
-    return r.value, n.value
+    """Quantized pools: host address (also valid on the device) of one layer's code records, the
+    record size, and the device address of that layer's scales [B][H][cap][2]."""
+    r, n, sp = _vp(), _i(0), _vp()
+    _ok(_lib.ig_pool_kv8(pool, layer, C.byref(r), C.byref(n), C.byref(sp)), "ig_pool_kv8")
+    return r.value, n.value, sp.value
+
+
+def ig_pool_read_scales(pool, layer, out):
+    _ok(_lib.ig_pool_read_scales(pool, layer, _p(out)), "ig_pool_read_scales")
+
+
+def _pool_layer_view_q(pool, layer, B, H, cap, cb):
+    r, rec, _ = ig_pool_kv8(pool, layer)
+    raw = np.ctypeslib.as_array(C.cast(r, C.POINTER(C.c_uint8)), shape=(B * H * cap * rec,)).reshape(B, H, cap, rec)
+    sc = np.zeros((B, H, cap, 2), dtype=np.float32)
+    ig_pool_read_scales(pool, layer, sc)
+    return raw[..., :cb], raw[..., cb:2 * cb], sc[..., 0], sc[..., 1]
 
 
 def pool_layer_view_fp8(pool, layer, B, H, cap, d):
-    """NumPy views of one layer of an fp8 pool: codes [B, H, cap, d] uint8 (K, V) and scales
-    [B, H, cap] float32 (K, V), all views into the records."""
-    r, rec = ig_pool_kv8(pool, layer)
-    raw = np.ctypeslib.as_array(C.cast(r, C.POINTER(C.c_uint8)), shape=(B * H * cap * rec,)).reshape(B, H, cap, rec)
-    sc = raw[..., 2 * d:2 * d + 8].view(np.float32)
-    return raw[..., :d], raw[..., d:2 * d], sc[..., 0], sc[..., 1]
+    """One layer of an fp8 pool: codes [B, H, cap, d] uint8 (K, V; views into the pinned
+    records) and scales [B, H, cap] float32 (K, V; a copy of the device-resident scales)."""
+    return _pool_layer_view_q(pool, layer, B, H, cap, d)
 
 
 def pool_layer_view_int4(pool, layer, B, H, cap, d):
-    """NumPy views of one layer of an int4 pool: packed codes [B, H, cap, d/2] uint8 (K, V; two
-    codes per byte, element 2j in the low nibble) and scales [B, H, cap] float32 (K, V)."""
-    r, rec = ig_pool_kv8(pool, layer)
-    raw = np.ctypeslib.as_array(C.cast(r, C.POINTER(C.c_uint8)), shape=(B * H * cap * rec,)).reshape(B, H, cap, rec)
-    cb = d // 2
-    sc = raw[..., 2 * cb:2 * cb + 8].view(np.float32)
-    return raw[..., :cb], raw[..., cb:2 * cb], sc[..., 0], sc[..., 1]
+    """One layer of an int4 pool: packed codes [B, H, cap, d/2] uint8 (K, V; two codes per byte,
+    element 2j in the low nibble; views into the pinned records) and scales [B, H, cap] float32
+    (K, V; a copy of the device-resident scales)."""
+    return _pool_layer_view_q(pool, layer, B, H, cap, d // 2)
 
 
 def ig_pool_slot_tokens(pool, layer, b, out):
