@@ -233,6 +233,55 @@ class Decoder:
         self.t += 1
         return L_now
 
+    def step_host(self, x, q, k_new, v_new, out, positions=None):
+        """One decode step from pinned host inputs to a pinned host output, with the transfers
+        overlapped with the neighbouring steps (returns at once).
+
+        x [L, B, D], q / k_new / v_new [L, B, H, d] fp16 and out [L, B, H, d] fp32, all pinned host
+        tensors.  The inputs go up on a copy stream into one of two device input sets while the
+        previous step runs; the step's output is copied to one of two device buffers at the end
+        of the step and comes down on the copy stream while the next step runs.  ``out`` is
+        complete after ``finish_host()`` (or once the event ``host_events[-1]`` has completed).
+        """
+        if not hasattr(self, "_host_io"):
+            e = lambda *s, dt=torch.float16: torch.empty(*s, dtype=dt, device=self.dev)  # noqa: E731
+            L, B, H, d, D = self.layers, self.B, self.H, self.d, self.D
+            self._copy_stream = torch.cuda.Stream(self.dev)
+            self._host_io = [dict(x=e(L, B, D), q=e(L, B, H, d), k=e(L, B, H, d), v=e(L, B, H, d),
+                                  out=e(L, B, H, d, dt=torch.float32),
+                                  consumed=torch.cuda.Event(), result=torch.cuda.Event(), down=torch.cuda.Event())
+                             for _ in range(2)]
+            self._host_calls = 0
+            self.host_events = []
+        buf = self._host_io[self._host_calls % 2]
+        C = self._copy_stream
+        with torch.cuda.stream(C):
+            if self._host_calls >= 2:
+                C.wait_event(buf["consumed"])  # the step two calls back has read this input set
+            for name, src in (("x", x), ("q", q), ("k", k_new), ("v", v_new)):
+                buf[name].copy_(src, non_blocking=True)
+            ready = torch.cuda.Event()
+            ready.record(C)
+        torch.cuda.current_stream(self.dev).wait_event(ready)
+        if self._host_calls >= 2:  # the previous download from this output buffer is done
+            torch.cuda.current_stream(self.dev).wait_event(buf["down"])
+        L_now = self.step(buf["x"], buf["q"], buf["k"], buf["v"], buf["out"], positions=positions)
+        buf["consumed"].record(self.S)
+        buf["result"].record(self.S)
+        with torch.cuda.stream(C):
+            C.wait_event(buf["result"])
+            out.copy_(buf["out"], non_blocking=True)
+            buf["down"].record(C)
+        self.host_events.append(buf["down"])
+        self._host_calls += 1
+        return L_now
+
+    def finish_host(self):
+        """Waits for every step_host call's output to have arrived in host memory."""
+        if getattr(self, "_copy_stream", None) is not None:
+            self._copy_stream.synchronize()
+        self.finish()
+
     def stage_ms(self, steps_back=0):
         """Per-stage device times of a recent step (see ig_decoder_stage_ms); waits for it."""
         return ig.ig_decoder_stage_ms(self.handle, steps_back)

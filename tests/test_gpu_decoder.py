@@ -279,3 +279,44 @@ def test_graph_replay_matches_eager_step(mods, fused_fetch):
     for (o0, c0, s0), (o1, c1, s1) in zip(outs[False], outs[True]):
         assert np.array_equal(s0, s1) and np.array_equal(c0, c1)
         assert np.array_equal(o0, o1)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_step_from_host_buffers_equals_device_step(mods, graph):
+    """Decoder.step_host (pinned host inputs and output, transfers on a copy stream overlapping
+    the neighbouring steps) gives the same bytes as Decoder.step on device tensors, step after
+    step, across graph capture and eviction."""
+    ig, decoder = mods
+    w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-host", layers=3, batch=2, heads=4, hidden=512,
+                     prompt=200, gen=10, pool_frac=0.95)
+    dev = "cuda:0"
+    decs = []
+    for _ in range(2):
+        dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k,
+                              Lcap=w.lcap, pool_cap=w.pool_cap, alpha=4.0, graph=graph, device=dev)
+        for l in range(w.layers):
+            dd = _layer_data(w, l, w.pool_cap, False)
+            t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+            dec.load_layer(l, t(dd["K"]), t(dd["V"]), dd["cols"], Wq_part=t(dd["Wqp"]))
+        dec.prefill(w.prompt)
+        decs.append(dec)
+    try:
+        shape = (w.layers, w.batch, w.heads, w.head_dim)
+        hout = [torch.empty(shape, dtype=torch.float32).pin_memory() for _ in range(5)]
+        ref = []
+        for s in range(5):
+            x = synth.layer_inputs(w, step=s)
+            qkv = [synth.token_inputs(w, l, s) for l in range(w.layers)]
+            q, kn, vn = (np.stack([a[i] for a in qkv]) for i in range(3))
+            out = torch.empty(shape, dtype=torch.float32, device=dev)
+            decs[0].step(*(torch.from_numpy(a).to(dev) for a in (x, q, kn, vn)), out)
+            decs[0].finish()
+            ref.append(out.cpu().numpy())
+            decs[1].step_host(*(torch.from_numpy(a).pin_memory() for a in (x, q, kn, vn)), hout[s])
+        decs[1].finish_host()
+        ig.ig_check()
+        for s in range(5):
+            assert np.array_equal(hout[s].numpy(), ref[s]), f"step {s}"
+    finally:
+        for dec in decs:
+            dec.close()
