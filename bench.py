@@ -229,7 +229,7 @@ class ClockSampler:
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.time(), ln.strip()))
 
     def __exit__(self, *a):
         if self.proc:
@@ -240,10 +240,14 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t_start=None, t_end=None):
+        """Median SM clock, its maximum and the throttle reasons seen, from the samples that arrived
+        between t_start and t_end (host time; all samples when not given)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
+            if (t_start is not None and t < t_start) or (t_end is not None and t > t_end):
+                continue
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
@@ -509,6 +513,11 @@ def run_ours(args, w, alpha):
     out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=device)
     cnt_host = [torch.empty_like(dec.cnt, device="cpu").pin_memory() for _ in range(args.steps)]
 
+    # the clock sampler starts (and takes its first, slow sample) before the warm-up, so that the
+    # GPU is not left idle between the warm-up and the timed steps; only the samples that arrive
+    # within the timed region are summarised
+    clk = ClockSampler(local).__enter__()
+    gc.collect()
     s = 0
     for _ in range(args.warmup):
         dec.step(xs[s], qs[s], kns[s], vns[s], out)
@@ -520,38 +529,39 @@ def run_ours(args, w, alpha):
     stage_n = [0, 0, 0, 0]
     timelines = []
     # the host stays about one step ahead of the GPU (it reads each step's stage timeline one
-    # step back), so a collector pause inside the timed region would idle the GPU: collect now
-    # and hold the collector off until the timed steps are done
-    gc.collect()
-    gc.disable()
-    barrier()
-    launches0 = ig.ig_launch_count()
+    # step back), so a collector pause inside the timed region would idle the GPU: the collector
+    # is held off until the timed steps are done
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     # one event at the end of every step: the spread of the step times
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
-        t0.record(dec.S)
-        for i in range(args.steps):
-            dec.step(xs[s], qs[s], kns[s], vns[s], out)
-            step_ev[i].record(dec.S)
-            with torch.cuda.stream(dec.S):
-                cnt_host[i].copy_(dec.cnt, non_blocking=True)
-            if i > 0:  # the previous step's stage times, while this step is queued
-                ms, n = dec.stage_ms(steps_back=1)
-                for j in range(4):
-                    stage[j] += ms[j]
-                    stage_n[j] += n[j]
-                timelines.append(dec.timeline(steps_back=1))
-            s += 1
-        t1.record(dec.S)
-        t1.synchronize()
-        ms, n = dec.stage_ms(steps_back=0)
-        for j in range(4):
-            stage[j] += ms[j]
-            stage_n[j] += n[j]
-        timelines.append(dec.timeline(steps_back=0))
+    gc.disable()
     barrier()
+    launches0 = ig.ig_launch_count()
+    t_clock0 = time.time()
+    t0.record(dec.S)
+    for i in range(args.steps):
+        dec.step(xs[s], qs[s], kns[s], vns[s], out)
+        step_ev[i].record(dec.S)
+        with torch.cuda.stream(dec.S):
+            cnt_host[i].copy_(dec.cnt, non_blocking=True)
+        if i > 0:  # the previous step's stage times, while this step is queued
+            ms, n = dec.stage_ms(steps_back=1)
+            for j in range(4):
+                stage[j] += ms[j]
+                stage_n[j] += n[j]
+            timelines.append(dec.timeline(steps_back=1))
+        s += 1
+    t1.record(dec.S)
+    t1.synchronize()
+    ms, n = dec.stage_ms(steps_back=0)
+    for j in range(4):
+        stage[j] += ms[j]
+        stage_n[j] += n[j]
+    timelines.append(dec.timeline(steps_back=0))
+    barrier()
+    t_clock1 = time.time()
     gc.enable()
+    clk.__exit__(None, None, None)
     launches = ig.ig_launch_count() - launches0
     elapsed = t0.elapsed_time(t1)
     step_ms = [t0.elapsed_time(step_ev[0])] + [step_ev[i - 1].elapsed_time(step_ev[i]) for i in range(1, args.steps)]
@@ -590,11 +600,13 @@ def run_ours(args, w, alpha):
         hk = [t.cpu().pin_memory() for t in kns[s:s + n_e2e]]
         hv = [t.cpu().pin_memory() for t in vns[s:s + n_e2e]]
         hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
-        dec.step_host(hx[0], hq[0], hk[0], hv[0], hout[0])  # sets up the copy stream and buffers
+        gc.collect()
+        # one untimed call sets up the copy stream and buffers and brings the GPU back from the
+        # host-side preparation above
+        dec.step_host(hx[0], hq[0], hk[0], hv[0], hout[0])
         dec.finish_host()
         hx, hq, hk, hv = hx[1:], hq[1:], hk[1:], hv[1:]
         n_e2e -= 1
-        gc.collect()
         gc.disable()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -663,7 +675,7 @@ def run_ours(args, w, alpha):
                               "hbm_peak_source": hbm_src, "link_peak_gbs": link},
             "link_probes_gbs": {k: v for k, v in probes.items() if k != "best"},
             "cpu_baseline": cpu,
-            "clocks": clk.summary(),
+            "clocks": clk.summary(t_clock0, t_clock1),
         }
         print(json.dumps(line), flush=True)
     dec.close()

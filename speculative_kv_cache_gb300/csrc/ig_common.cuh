@@ -62,9 +62,35 @@ void count_launches(int64_t n);
     if (!(cond)) return ::ig::fail(IG_ERR_INVALID, __VA_ARGS__); \
   } while (0)
 
+// Launches `kern` with programmatic stream serialization: it may start while the kernel before
+// it in the stream is still running (which lets it begin once that kernel's CTAs have signalled
+// pdl_trigger()), so it must call pdl_wait() before reading anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ----------------------------------------------------------------------------------------
 // Device side
 // ----------------------------------------------------------------------------------------
+// Programmatic dependent launch: the kernel after this one in the stream (launched with
+// launch_pdl) may be scheduled once every CTA of this grid has issued pdl_trigger() ...
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// ... and a kernel launched that way waits here until the grid before it has completed and its
+// memory operations are visible (a no-op for a kernel launched without the attribute).  Every
+// such kernel waits before it exits, so that completion stays transitive along the stream.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void raise_error(int* err, int bit) {
   if (err) atomicOr(err, bit);
 }

@@ -94,6 +94,9 @@ __global__ void __launch_bounds__(kTcThreads) k1_partial_q_tc(
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the kernel after this one (the RoPE epilogue or the selection) may start now: it reads
+  // this kernel's output only after its own pdl_wait()
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcRing; ++i) {

@@ -173,6 +173,9 @@ __global__ void __launch_bounds__(kSThreads, IG_K23_MIN_CTAS) k23_score_select(
     }
     cp_async_commit();
   };
+  // the kernel may start while the projection (or the RoPE epilogue) still runs: the producer's
+  // partial-key copies do not depend on it, the query does
+  pdl_wait();
   prefetch_q(head_of(0), 0);
   int g = 0;                          // stages consumed so far
   for (int i = 0; head_of(i) < BH; ++i) {
@@ -321,9 +324,11 @@ ig_status launch_k23(cudaStream_t st, const float* qsrc, int S, int B, int H, in
   if (per_sm < 1) per_sm = 1;
   const long long slots = (long long)per_sm * sms;
   const int grid = (int)(heads < slots ? heads : slots);
-  k23_score_select<MAXB><<<grid, kSThreads, lay.total, st>>>(qsrc, S, B, H, k, reinterpret_cast<const __half*>(Kpart),
-                                                            L_valid, Lcap, scale, alpha, idx, cnt, used, scores,
-                                                            q_part, NS, error_word());
+  // programmatic launch: the partial keys stream while the query's producer finishes
+  e = launch_pdl(k23_score_select<MAXB>, dim3(grid), dim3(kSThreads), lay.total, st, qsrc, S, B, H, k,
+                 reinterpret_cast<const __half*>(Kpart), L_valid, Lcap, scale, alpha, idx, cnt, used, scores, q_part,
+                 NS, error_word());
+  if (e != cudaSuccess) return cuda_fail(e, "fused select launch");
   IG_CHECK_LAUNCH("fused select launch");
   return IG_OK;
 }
@@ -333,10 +338,6 @@ ig_status launch_score_select(cudaStream_t st, const float* qsrc, int S, int B, 
                               float alpha, int32_t* idx, int32_t* cnt, uint8_t* used, float* scores,
                               float* q_part) {
   IG_REQUIRE(Lcap <= kSMaxLcap, "fused selection needs Lcap <= %d (got %d)", kSMaxLcap, Lcap);
-  if (used) {
-    cudaError_t e = cudaMemsetAsync(used, 0, (size_t)B * Lcap, st);
-    if (e != cudaSuccess) return cuda_fail(e, "clear used flags");
-  }
   if (Lcap <= kSBlock)
     return launch_k23<1>(st, qsrc, S, B, H, k, Kpart, L_valid, Lcap, scale, alpha, idx, cnt, used, scores, q_part);
   if (Lcap <= 2 * kSBlock)
@@ -370,7 +371,14 @@ extern "C" ig_status ig_speculate_select(void* stream, int B, int D, int H, int 
   IG_REQUIRE(!rope || (A_cols && positions && d % 2 == 0), "RoPE needs A_cols, positions and an even d");
   const size_t need = ig_speculate_select_workspace_bytes(B, D, H, d, k, rope ? 1 : 0);
   if (workspace_bytes < need) return fail(IG_ERR_CAPACITY, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+  IG_REQUIRE(Lcap <= kSMaxLcap, "fused selection needs Lcap <= %d (got %d)", kSMaxLcap, Lcap);
   cudaStream_t s = as_stream(stream);
+  // the use flags are cleared before the projection, so that the selection follows the
+  // projection (or the RoPE epilogue) directly and may overlap it
+  if (used) {
+    cudaError_t e = cudaMemsetAsync(used, 0, (size_t)B * Lcap, s);
+    if (e != cudaSuccess) return cuda_fail(e, "clear used flags");
+  }
   int S = projection_splits(D);
   float* part = static_cast<float*>(workspace);
   const int N = rope ? H * d : H * k;

@@ -32,7 +32,9 @@ ig_status launch_k1(cudaStream_t st, const __half* x, const __half* Wt, float* p
 }
 
 
-// K1b: RoPE epilogue for one (b, h): q = sum of the split partials of x W_Q,h; rotate the
+// K1b: RoPE epilogue for one (b, h) (launched so that it may start during the projection: the
+// copy of A[:, S] is issued first, the partials are read after pdl_wait): q = sum of the split
+// partials of x W_Q,h; rotate the
 // pairs (j, j + d/2) by the angle p * theta^(-2j/d) (the inverse frequencies come from the host
 // in float64; the angle is formed and reduced to [-pi, pi] in float64, then rotated in
 // float64); then q~p[c] = sum_j q_rot[j] A[h][j][c] with A[h][:, S_h] (a contiguous d x k
@@ -67,6 +69,8 @@ __global__ void k1b_rope_project(const float* __restrict__ part, int S, int B, i
         "l"(Ah), "r"(dk * 4), "r"(smem_addr(bar))
         : "memory");
   }
+  pdl_trigger();
+  pdl_wait();  // the projection's partials are complete and visible from here on
   for (int j = threadIdx.x; j < d; j += blockDim.x) {
     q[j] = sum_splits(part + (size_t)b * N + h * d + j, (size_t)B * N, S);
   }
@@ -230,7 +234,10 @@ ig_status launch_rope_project(cudaStream_t st, const float* part, int S, int B, 
                                           (int)rope_smem);
     if (ae != cudaSuccess) return cuda_fail(ae, "rope epilogue smem attribute");
   }
-  k1b_rope_project<<<B * H, 128, rope_smem, st>>>(part, S, B, H, d, k, A_cols, pos, inv, qp, error_word());
+  // may start during the projection: A's copy overlaps it, the partials are read after pdl_wait
+  cudaError_t le = launch_pdl(k1b_rope_project, dim3(B * H), dim3(128), rope_smem, st, part, S, B, H, d, k, A_cols,
+                              pos, inv, qp, error_word());
+  if (le != cudaSuccess) return cuda_fail(le, "rope epilogue launch");
   IG_CHECK_LAUNCH("rope epilogue launch");
   return IG_OK;
 }
