@@ -115,13 +115,22 @@ def oracle_sample(w: synth.Workload, n_layers: int, alpha: float, batch: int = 1
     return w1, L, layers
 
 
-def time_oracle(w1, L, layers, alpha) -> float:
+def partial_caches(layers):
+    """The partial key cache of each sampled layer (built by the prefill: not timed)."""
+    from oracle import infinigen as ora
+
+    return [ora.partial_key_cache(K, cols) for (_, _, K, _, cols, _, _, _) in layers]
+
+
+def time_oracle(w1, L, layers, alpha, kparts=None) -> float:
+    """The oracle's decode layer-steps over the sample: partial query, scores, selection, gather
+    and attention (the partial key caches, the prefill's product, are built beforehand)."""
     from oracle import infinigen as ora
 
     scale = 1.0 / math.sqrt(w1.head_dim)
+    kparts = kparts if kparts is not None else partial_caches(layers)
     t0 = time.perf_counter()
-    for x, W, K, V, cols, q, kn, vn in layers:
-        Kpart = ora.partial_key_cache(K, cols)
+    for (x, W, K, V, cols, q, kn, vn), Kpart in zip(layers, kparts):
         if w1.rope_theta:
             qp = ora.partial_query_rope(x, W[0], W[1], cols, L, w1.rope_theta)
         else:
@@ -144,8 +153,9 @@ def oracle_layer_step_child(names, alpha) -> int:
         w = synth.WORKLOADS[name]
         a = alpha if alpha in w.alphas else w.alphas[0]
         w1, L, layers = oracle_sample(w, 1, a, batch=w.batch)
-        time_oracle(w1, L, layers, a)  # warm
-        out[name] = time_oracle(w1, L, layers, a)
+        kp = partial_caches(layers)
+        time_oracle(w1, L, layers, a, kp)  # warm
+        out[name] = time_oracle(w1, L, layers, a, kp)
     print(json.dumps(out), flush=True)
     return 0
 
@@ -174,9 +184,10 @@ def run_reference(args, w, alpha):
         return 0
     n_layers = max(1, min(w.layers - 1, args.cpu_layers or 2))
     w1, L, layers = oracle_sample(w, n_layers, alpha)
+    kp = partial_caches(layers)
     for _ in range(args.warmup):
-        time_oracle(w1, L, layers, alpha)
-    times = [time_oracle(w1, L, layers, alpha) for _ in range(args.steps)]
+        time_oracle(w1, L, layers, alpha, kp)
+    times = [time_oracle(w1, L, layers, alpha, kp) for _ in range(args.steps)]
     total = sum(times)
     # tokens: one sequence through n_layers of the w.layers layers, per step
     tokens = args.steps * (n_layers / w.layers)
