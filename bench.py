@@ -572,7 +572,6 @@ def run_ours(args, w, alpha):
     barrier()
     t_clock1 = time.time()
     gc.enable()
-    clk.__exit__(None, None, None)
     launches = ig.ig_launch_count() - launches0
     elapsed = t0.elapsed_time(t1)
     step_ms = [t0.elapsed_time(step_ev[0])] + [step_ev[i - 1].elapsed_time(step_ev[i]) for i in range(1, args.steps)]
@@ -603,7 +602,8 @@ def run_ours(args, w, alpha):
     hbm_gbs_alg = float(hbm_l.sum() + w.batch * w.heads * ctx.mean() * w.head_dim * 4) / (ms_per_step * 1e-3) / 1e9
 
     # end to end through host buffers (pinned): inputs up, outputs down, every step, through the
-    # decoder's host-buffer call (its transfers overlap the neighbouring steps on a copy stream)
+    # decoder's host-buffer call (its uploads and downloads overlap the neighbouring steps on two
+    # copy streams)
     e2e = None
     if n_e2e:
         hx = [t.cpu().pin_memory() for t in xs[s:s + n_e2e]]
@@ -621,20 +621,29 @@ def run_ours(args, w, alpha):
         gc.disable()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        up, down = dec.host_streams()
+        e_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_e2e)]
         e0.record(dec.S)
-        dec._copy_stream.wait_event(e0)
+        up.wait_event(e0)
         for i in range(n_e2e):
             dec.step_host(hx[i], hq[i], hk[i], hv[i], hout[i % 2])
-        e1.record(dec._copy_stream)  # after the last step's output has come down
+            e_ev[i].record(down)  # this step's output is in host memory
+        e1.record(down)  # after the last step's output has come down
         e1.synchronize()
         barrier()
         gc.enable()
         dec.finish_host()
+        e_each = [e0.elapsed_time(e_ev[0])] + [e_ev[i - 1].elapsed_time(e_ev[i]) for i in range(1, n_e2e)]
         e_ms, e_tok = reduce_over_ranks(torch, e0.elapsed_time(e1), float(w.batch * n_e2e), dist_on)
         bi = sum(t.numel() * t.element_size() for t in (hx[0], hq[0], hk[0], hv[0]))
         e2e = {"value": e_tok / (e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": out.numel() * out.element_size(),
-               "api": "Decoder.step_host (pinned host inputs and output; transfers overlap the steps)"}
+               "api": "Decoder.step_host (pinned host inputs and output; transfers overlap the steps)",
+               "step_ms_each": [round(x, 3) for x in e_each]}
+
+    # the sampler runs on through the end-to-end steps (stopping nvidia-smi is not free either);
+    # only the samples of the device-timed region are summarised
+    clk.__exit__(None, None, None)
 
     if rank == 0:
         line = {

@@ -252,8 +252,7 @@ typedef struct ig_pool ig_pool;
  * and dequantizes (code value x scale, rounded to fp16) into the usual fp16 staging rows, so
  * the link carries 2d bytes per row instead of 4d; the partial key cache (speculation) stays
  * fp16.  d must be 64 or 128; the pool's kernels must run on the device that holds its scales
- * (else IG_ERR_INVALID); ig_pool_kv, ig_gather_attend and the prefill refuse quantized pools
- * (use ig_pool_kv8). */
+ * (else IG_ERR_INVALID); ig_pool_kv and the prefill refuse quantized pools (use ig_pool_kv8). */
 #define IG_POOL_FP8 2
 /* IG_POOL_INT4: the same split with signed 4-bit codes (the format the follow-up work names):
  * a record of d / 2 bytes of key codes then d / 2 of value codes (d bytes: one 128-byte line at
@@ -362,9 +361,12 @@ ig_status ig_dense_attend(void* stream, int B, int H, int d, int Lcap, float sca
  * row straight from the pinned pool (16-byte zero-copy loads over the host link) through idx
  * and folds it into a per-head online softmax.  This is the prefetch of section 3.4
  * (Inference Controller) with the copy and the attention that consumes it in one pass; the
- * pages stage the rows in GPU memory first.  Issue it on a side stream; max_ctas bounds the
- * grid (0 = library default: a quarter of the SMs, or two CTAs per SM of the stream's own
- * partition after ig_sm_split_create; at most 256).
+ * pages stage the rows in GPU memory first.  A quantized pool (IG_POOL_FP8, IG_POOL_INT4) is
+ * read as its code records (each lane its 8 or 4 bytes of codes) with the rows' scales from
+ * HBM, dequantized in registers as ig_gather_kv dequantizes them (code value x scale in fp32,
+ * rounded to fp16).  Issue it on a side stream; max_ctas bounds the grid (0 = library default:
+ * a quarter of the SMs, or two CTAs per SM of the stream's own partition after
+ * ig_sm_split_create, twice that for a quantized pool; at most 256).
  *   pool, layer        as for ig_gather_kv (B, H, d must match the pool)
  *   q                  dev fp16 [B][H][d]
  *   idx, cnt           dev, from ig_select (slots must be < the pool's capacity; a slot

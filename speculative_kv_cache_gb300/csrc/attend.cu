@@ -13,6 +13,7 @@
 // to the workspace at index head + CTA (unique: CTA ranges and head ranges are both
 // increasing).  A combine kernel merges each head's partials, adds the current token's own
 // key/value, and normalises.  No atomics; the result does not depend on timing.
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "ig_common.cuh"
@@ -203,9 +204,60 @@ __global__ void __launch_bounds__(kAttThreads) k5_attend(
 // row belongs to another head it writes its partial to ws[(head + CTA) * NG + g] and starts
 // afresh, so a group writes one partial per head it touches and no CTA-wide barrier sits on
 // the load path.  Every slot is range-checked; a bad one is skipped and flagged.
-template <int D>
+// BITS = 0: fp16 rows (Kp, Vp); BITS = 8 or 4: a quantized pool's code records (Rec, rec bytes
+// each: K codes then V codes) and the rows' scales in device memory (Sc, [row][2]).  A lane
+// loads the 8 codes of its 8 elements (8 or 4 bytes) of the key and of the value and dequantizes
+// them when the row is folded in, exactly as the staged fetch does (code value x scale in fp32,
+// rounded to fp16), so the attention sees the same values.
+template <int BITS>
+struct FaRow;  // the raw data a lane holds for one row in flight
+template <>
+struct FaRow<0> {
+  uint4 k, v;
+};
+template <>
+struct FaRow<8> {
+  uint2 k, v;
+  float2 s;
+};
+template <>
+struct FaRow<4> {
+  uint32_t k, v;
+  float2 s;
+};
+
+// 8 codes (one lane's share of a row) and their scale -> 8 fp16 values packed in a uint4
+__device__ __forceinline__ uint4 dq8(uint2 c, float sc) {
+  const uint32_t w[2] = {c.x, c.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> 16), __NV_E4M3);
+    const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+    const __half2 ra = __floats2half2_rn(a.x * sc, a.y * sc);
+    const __half2 rb = __floats2half2_rn(b.x * sc, b.y * sc);
+    o[2 * i] = *reinterpret_cast<const uint32_t*>(&ra);
+    o[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&rb);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+__device__ __forceinline__ uint4 dq4(uint32_t c, float sc) {
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int c0 = (int)(c << (28 - 8 * j)) >> 28;
+    const int c1 = (int)(c << (24 - 8 * j)) >> 28;
+    const __half2 r = __floats2half2_rn((float)c0 * sc, (float)c1 * sc);
+    o[j] = *reinterpret_cast<const uint32_t*>(&r);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int D, int BITS>
 __global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
     const __half* __restrict__ q, const uint4* __restrict__ Kp, const uint4* __restrict__ Vp,
+    const uint8_t* __restrict__ Rec, int rec, const float* __restrict__ Sc,
     const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int H, int Lcap, int units,
     int cap, float scale, float* __restrict__ ws, int* __restrict__ gpre, int* err) {
   constexpr int VPR = D / 8;                  // lanes per row
@@ -264,25 +316,49 @@ __global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
     }
   };
   // the query chunk is loaded only where the head changes (a group's rows mostly share one)
-  auto issue = [&](const int (&hu)[kFaUnroll], const int (&slot)[kFaUnroll], int prev, uint4 (&kv)[kFaUnroll],
-                   uint4 (&vv)[kFaUnroll], uint4 (&qv)[kFaUnroll]) {
+  auto issue = [&](const int (&hu)[kFaUnroll], const int (&slot)[kFaUnroll], int prev, FaRow<BITS> (&rw_)[kFaUnroll],
+                   uint4 (&qv)[kFaUnroll]) {
 #pragma unroll
     for (int x = 0; x < kFaUnroll; ++x) {
-      kv[x] = vv[x] = qv[x] = make_uint4(0, 0, 0, 0);
+      rw_[x] = FaRow<BITS>{};
+      qv[x] = make_uint4(0, 0, 0, 0);
       if (hu[x] >= 0 && hu[x] != (x == 0 ? prev : hu[x - 1]))
         qv[x] = *reinterpret_cast<const uint4*>(q + (size_t)hu[x] * D + v * 8);
       if (slot[x] >= 0) {
-        const size_t src = ((size_t)hu[x] * cap + slot[x]) * VPR + v;
-        kv[x] = ld_nc_v4(Kp + src);
-        vv[x] = ld_nc_v4(Vp + src);
+        const size_t row = (size_t)hu[x] * cap + slot[x];
+        if constexpr (BITS == 0) {
+          rw_[x].k = ld_nc_v4(Kp + row * VPR + v);
+          rw_[x].v = ld_nc_v4(Vp + row * VPR + v);
+        } else if constexpr (BITS == 8) {
+          const uint8_t* rp = Rec + row * rec;
+          rw_[x].k = ld_nc_v2(rp + (size_t)v * 8);
+          rw_[x].v = ld_nc_v2(rp + D + (size_t)v * 8);
+          rw_[x].s = __ldg(reinterpret_cast<const float2*>(Sc) + row);
+        } else {
+          const uint8_t* rp = Rec + row * rec;
+          rw_[x].k = ld_nc_u32(rp + (size_t)v * 4);
+          rw_[x].v = ld_nc_u32(rp + D / 2 + (size_t)v * 4);
+          rw_[x].s = __ldg(reinterpret_cast<const float2*>(Sc) + row);
+        }
       }
     }
   };
+  auto key_of = [&](const FaRow<BITS>& r) -> uint4 {
+    if constexpr (BITS == 0) return r.k;
+    else if constexpr (BITS == 8) return dq8(r.k, r.s.x);
+    else return dq4(r.k, r.s.x);
+  };
+  auto value_of = [&](const FaRow<BITS>& r) -> uint4 {
+    if constexpr (BITS == 0) return r.v;
+    else if constexpr (BITS == 8) return dq8(r.v, r.s.y);
+    else return dq4(r.v, r.s.y);
+  };
   int hu[kFaUnroll], slot[kFaUnroll], hn[kFaUnroll], sn[kFaUnroll];
-  uint4 kv[kFaUnroll], vv[kFaUnroll], qv[kFaUnroll], kn[kFaUnroll], vn[kFaUnroll], qn[kFaUnroll];
+  FaRow<BITS> cu[kFaUnroll], nx[kFaUnroll];
+  uint4 qv[kFaUnroll], qn[kFaUnroll];
   int rw = r0 + warp * RPW;
   prepare(rw, hu, slot);
-  issue(hu, slot, -1, kv, vv, qv);
+  issue(hu, slot, -1, cu, qv);
   // warp-uniform trip count (the shuffles take the full mask); rows past the end compute on
   // zeros and change nothing
   while (rw < r1) {
@@ -291,7 +367,7 @@ __global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
 #pragma unroll
     for (int x = 0; x < kFaUnroll; ++x) last = hu[x] >= 0 ? hu[x] : last;
     prepare(rnext, hn, sn);
-    issue(hn, sn, last, kn, vn, qn);
+    issue(hn, sn, last, nx, qn);
 #pragma unroll
     for (int x = 0; x < kFaUnroll; ++x) {
       if (hu[x] >= 0 && hu[x] != cur) {  // a new head: hand over the previous one's partial
@@ -305,15 +381,14 @@ __global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
       }
-      const float z = group_sum<VPR>(lane_dot(qf, kv[x]));
-      if (slot[x] >= 0) online_add(z, vv[x], m, l, acc);
+      const float z = group_sum<VPR>(lane_dot(qf, key_of(cu[x])));
+      if (slot[x] >= 0) online_add(z, value_of(cu[x]), m, l, acc);
     }
 #pragma unroll
     for (int x = 0; x < kFaUnroll; ++x) {
       hu[x] = hn[x];
       slot[x] = sn[x];
-      kv[x] = kn[x];
-      vv[x] = vn[x];
+      cu[x] = nx[x];
       qv[x] = qn[x];
     }
     rw = rnext;
@@ -460,20 +535,22 @@ ig_status launch_attend(cudaStream_t st, int B, int H, int Lcap, float scale, co
   return IG_OK;
 }
 
-template <int D>
+template <int D, int BITS>
 ig_status launch_fetch_attend(cudaStream_t st, int B, int H, int Lcap, int cap, float scale, const uint16_t* q,
-                              const uint16_t* Kp, const uint16_t* Vp, const int32_t* idx, const int32_t* cnt,
-                              const uint16_t* kn, const uint16_t* vn, float* out, void* ws, int grid) {
+                              const uint16_t* Kp, const uint16_t* Vp, const uint8_t* Rec, int rec, const float* Sc,
+                              const int32_t* idx, const int32_t* cnt, const uint16_t* kn, const uint16_t* vn,
+                              float* out, void* ws, int grid) {
   const int units = B * H;
   const size_t smem = (size_t)(units + 1) * sizeof(int);
   if (smem > 32 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k5_fetch_attend<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k5_fetch_attend<D, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "fetch-attention smem attribute");
   }
   int* gpre = reinterpret_cast<int*>(static_cast<char*>(ws) + fa_part_bytes(B, H, D));
-  k5_fetch_attend<D><<<grid, kFaThreads, smem, st>>>(
-      reinterpret_cast<const __half*>(q), reinterpret_cast<const uint4*>(Kp), reinterpret_cast<const uint4*>(Vp),
-      idx, cnt, H, Lcap, units, cap, scale, static_cast<float*>(ws), gpre, error_word());
+  k5_fetch_attend<D, BITS><<<grid, kFaThreads, smem, st>>>(
+      reinterpret_cast<const __half*>(q), reinterpret_cast<const uint4*>(Kp), reinterpret_cast<const uint4*>(Vp), Rec,
+      rec, Sc, idx, cnt, H, Lcap, units, cap, scale, static_cast<float*>(ws), gpre, error_word());
   IG_CHECK_LAUNCH("fetch-attention launch");
   k5_combine<D, fa_groups<D>()><<<units, D, 0, st>>>(
       static_cast<const float*>(ws), gpre, units, grid, reinterpret_cast<const __half*>(q),
@@ -507,6 +584,7 @@ ig_status attend_common(void* stream, int B, int H, int d, int Lcap, float scale
 }
 
 }  // namespace
+ig_status check_pool_device(const ig_pool* pool);
 }  // namespace ig
 
 using namespace ig;
@@ -546,8 +624,8 @@ extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int lay
                                       void* workspace, size_t workspace_bytes, int max_ctas) {
   IG_REQUIRE(pool, "null pool");
   IG_REQUIRE(pool->storage, "the pool was created without storage");
-  IG_REQUIRE(!pool->qbits, "fused fetch + attention reads fp16 pools only");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
+  if (ig_status dst = check_pool_device(pool); dst != IG_OK) return dst;
   IG_REQUIRE(B == pool->B && H == pool->H && d == pool->d, "B/H/d do not match the pool");
   IG_REQUIRE(B > 0 && H > 0 && Lcap > 0, "B, H, Lcap must be positive");
   IG_REQUIRE(d == 64 || d == 128, "d must be 64 or 128 (got %d)", d);
@@ -562,17 +640,31 @@ extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int lay
   if (!workspace || workspace_bytes < need)
     return fail(IG_ERR_CAPACITY, "fused fetch + attention needs %zu workspace bytes", need);
   IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
-  // the same default as the gather
-  int grid = max_ctas > 0 ? max_ctas : fetch_grid(as_stream(stream));
+  // the same default as the gather (twice it for a quantized pool, whose rows need dequantizing)
+  int grid = max_ctas > 0 ? max_ctas : (pool->qbits ? 2 : 1) * fetch_grid(as_stream(stream));
   if (grid < 1) grid = 1;
   if (grid > kMaxFaCtas) grid = kMaxFaCtas;
-  const size_t layer_elems = (size_t)B * H * pool->cap * d;
-  const uint16_t* Kp = pool->Kdev + (size_t)layer * layer_elems;
-  const uint16_t* Vp = pool->Vdev + (size_t)layer * layer_elems;
   cudaStream_t s = as_stream(stream);
+  const size_t rows = (size_t)B * H * pool->cap;
+  if (pool->qbits) {
+    const uint8_t* Rec = pool->R + (size_t)layer * rows * pool->rec;
+    const float* Sc = pool->S + (size_t)layer * rows * 2;
+#define IG_FA_Q(DD, BB)                                                                                     \
+  return launch_fetch_attend<DD, BB>(s, B, H, Lcap, pool->cap, scale, q, nullptr, nullptr, Rec, pool->rec, Sc, idx, \
+                                     cnt, k_new, v_new, out, workspace, grid)
+    if (pool->qbits == 8) {
+      if (d == 128) IG_FA_Q(128, 8);
+      IG_FA_Q(64, 8);
+    }
+    if (d == 128) IG_FA_Q(128, 4);
+    IG_FA_Q(64, 4);
+#undef IG_FA_Q
+  }
+  const uint16_t* Kp = pool->Kdev + (size_t)layer * rows * d;
+  const uint16_t* Vp = pool->Vdev + (size_t)layer * rows * d;
   if (d == 128)
-    return launch_fetch_attend<128>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, idx, cnt, k_new, v_new, out,
-                                    workspace, grid);
-  return launch_fetch_attend<64>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, idx, cnt, k_new, v_new, out,
-                                 workspace, grid);
+    return launch_fetch_attend<128, 0>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, nullptr, 0, nullptr, idx, cnt,
+                                       k_new, v_new, out, workspace, grid);
+  return launch_fetch_attend<64, 0>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, nullptr, 0, nullptr, idx, cnt,
+                                    k_new, v_new, out, workspace, grid);
 }

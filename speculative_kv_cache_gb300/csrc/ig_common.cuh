@@ -173,6 +173,18 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
+// 8- and 4-byte read-only loads that do not allocate in L1
+__device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_nc_u32(const void* p) {
+  uint32_t r;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
 // Sum of S split partials p[0], p[stride], ... added in that order (the same fp32 sum as a
 // plain loop): the loads are issued 8 at a time before their adds, so they overlap.
 __device__ __forceinline__ float sum_splits(const float* __restrict__ p, size_t stride, int S) {

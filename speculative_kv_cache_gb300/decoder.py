@@ -43,8 +43,6 @@ class Decoder:
             raise ValueError("Lcap must be a multiple of 8 covering the pool capacity")
         if pool_fp8 and pool_int4:
             raise ValueError("one pool format: fp8 or int4")
-        if (pool_fp8 or pool_int4) and fused_fetch:
-            raise ValueError("the fused fetch + attention reads fp16 pools only")
         # k: one partial width for every layer, or one per layer (e.g. from ig_ratio_from_spectrum)
         ks = [int(x) for x in k] if hasattr(k, "__len__") else [int(k)] * layers
         if len(ks) != layers:
@@ -238,15 +236,18 @@ class Decoder:
         overlapped with the neighbouring steps (returns at once).
 
         x [L, B, D], q / k_new / v_new [L, B, H, d] fp16 and out [L, B, H, d] fp32, all pinned host
-        tensors.  The inputs go up on a copy stream into one of two device input sets while the
-        previous step runs; the step's output is copied to one of two device buffers at the end
-        of the step and comes down on the copy stream while the next step runs.  ``out`` is
-        complete after ``finish_host()`` (or once the event ``host_events[-1]`` has completed).
+        tensors.  The inputs go up on an upload stream into one of two device input sets while
+        the previous step runs; the step's output is copied to one of two device buffers at the
+        end of the step and comes down on a download stream while the next step runs.  Up and
+        down have a stream each, so the next step's upload never queues behind this step's
+        download.  ``out`` is complete after ``finish_host()`` (or once the event
+        ``host_events[-1]`` has completed).
         """
         if not hasattr(self, "_host_io"):
             e = lambda *s, dt=torch.float16: torch.empty(*s, dtype=dt, device=self.dev)  # noqa: E731
             L, B, H, d, D = self.layers, self.B, self.H, self.d, self.D
-            self._copy_stream = torch.cuda.Stream(self.dev)
+            self._up_stream = torch.cuda.Stream(self.dev)
+            self._down_stream = torch.cuda.Stream(self.dev)
             self._host_io = [dict(x=e(L, B, D), q=e(L, B, H, d), k=e(L, B, H, d), v=e(L, B, H, d),
                                   out=e(L, B, H, d, dt=torch.float32),
                                   consumed=torch.cuda.Event(), result=torch.cuda.Event(), down=torch.cuda.Event())
@@ -254,32 +255,39 @@ class Decoder:
             self._host_calls = 0
             self.host_events = []
         buf = self._host_io[self._host_calls % 2]
-        C = self._copy_stream
-        with torch.cuda.stream(C):
+        U, Dn = self._up_stream, self._down_stream
+        with torch.cuda.stream(U):
             if self._host_calls >= 2:
-                C.wait_event(buf["consumed"])  # the step two calls back has read this input set
+                U.wait_event(buf["consumed"])  # the step two calls back has read this input set
             for name, src in (("x", x), ("q", q), ("k", k_new), ("v", v_new)):
                 buf[name].copy_(src, non_blocking=True)
             ready = torch.cuda.Event()
-            ready.record(C)
+            ready.record(U)
         torch.cuda.current_stream(self.dev).wait_event(ready)
         if self._host_calls >= 2:  # the previous download from this output buffer is done
             torch.cuda.current_stream(self.dev).wait_event(buf["down"])
         L_now = self.step(buf["x"], buf["q"], buf["k"], buf["v"], buf["out"], positions=positions)
         buf["consumed"].record(self.S)
         buf["result"].record(self.S)
-        with torch.cuda.stream(C):
-            C.wait_event(buf["result"])
+        with torch.cuda.stream(Dn):
+            Dn.wait_event(buf["result"])
             out.copy_(buf["out"], non_blocking=True)
-            buf["down"].record(C)
+            buf["down"].record(Dn)
         self.host_events.append(buf["down"])
         self._host_calls += 1
         return L_now
 
+    def host_streams(self):
+        """The (upload, download) streams of step_host (None before its first call)."""
+        if not hasattr(self, "_host_io"):
+            return None, None
+        return self._up_stream, self._down_stream
+
     def finish_host(self):
         """Waits for every step_host call's output to have arrived in host memory."""
-        if getattr(self, "_copy_stream", None) is not None:
-            self._copy_stream.synchronize()
+        if hasattr(self, "_host_io"):
+            self._up_stream.synchronize()
+            self._down_stream.synchronize()
         self.finish()
 
     def stage_ms(self, steps_back=0):

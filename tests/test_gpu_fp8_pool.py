@@ -102,7 +102,8 @@ def test_fp8_pool_write_gather_append_bit_exact(mods, d):
         ig.ig_pool_destroy(pool)
 
 
-def test_decoder_with_fp8_pool(mods):
+@pytest.mark.parametrize("fused_fetch", [False, True])
+def test_decoder_with_fp8_pool(mods, fused_fetch):
     ig, decoder = mods
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-fp8", layers=3, batch=2, heads=4, hidden=512,
                      prompt=200, gen=6)
@@ -110,7 +111,7 @@ def test_decoder_with_fp8_pool(mods):
     cap = w.pool_cap
     scale = np.float32(1.0 / math.sqrt(w.head_dim))
     dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=w.lcap,
-                          pool_cap=cap, alpha=4.0, pool_fp8=True, device=devn)
+                          pool_cap=cap, alpha=4.0, pool_fp8=True, fused_fetch=fused_fetch, device=devn)
     try:
         for l in range(w.layers):
             K, V = synth.pool_layer(w, l, cap=cap)

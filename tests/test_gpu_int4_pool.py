@@ -125,7 +125,11 @@ def test_int4_pool_write_gather_append_bit_exact(mods, d):
         ig.ig_pool_destroy(pool)
 
 
-def test_decoder_with_int4_pool(mods):
+@pytest.mark.parametrize("fused_fetch", [False, True])
+def test_decoder_with_int4_pool(mods, fused_fetch):
+    """Decode steps over an int4 pool, staged (the fetch dequantizes into HBM) or fused (the
+    fetch stream's attention dequantizes in registers), against the oracle's attention over the
+    oracle-dequantized rows of the GPU's sets."""
     ig, decoder = mods
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-int4", layers=3, batch=2, heads=4, hidden=512,
                      prompt=200, gen=6)
@@ -133,7 +137,7 @@ def test_decoder_with_int4_pool(mods):
     cap = w.pool_cap
     scale = np.float32(1.0 / math.sqrt(w.head_dim))
     dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=w.lcap,
-                          pool_cap=cap, alpha=4.0, pool_int4=True, device=devn)
+                          pool_cap=cap, alpha=4.0, pool_int4=True, fused_fetch=fused_fetch, device=devn)
     try:
         for l in range(w.layers):
             K, V = synth.pool_layer(w, l, cap=cap)
@@ -166,3 +170,49 @@ def test_decoder_with_int4_pool(mods):
                 assert cnt[l].sum() > 0
     finally:
         dec.close()
+
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "int4"])
+@pytest.mark.parametrize("with_new", [False, True])
+def test_fused_fetch_attend_on_quantized_pools(mods, fmt, with_new):
+    """ig_gather_attend on a quantized pool (codes over the host link, scales from HBM,
+    dequantized in registers) against the oracle: its own quantization of the same seeded rows,
+    dequantized, then its attention over the same index sets.  The OPT-30B recipe (head
+    dimension, key scale, planted rows) at 2 sequences x 8 heads, so the pure-Python e4m3
+    encoder finishes in seconds; quantization is row by row, so quantizing only the gathered
+    rows equals quantizing the pool."""
+    ig, _ = mods
+    w = synth.scaled(synth.WORKLOADS["opt-30b"], batch=2, heads=8)
+    B, H, d, cap, Lcap = w.batch, w.heads, w.head_dim, 2048, 2048
+    K, V = synth.pool_layer(w, 1, cap=cap)
+    q, kn, vn = synth.token_inputs(w, 1, 0)
+    g = np.random.default_rng(5)
+    cnt = np.clip(np.round(np.exp(g.normal(np.log(120), 0.9, size=(B, H)))), 0, 1900).astype(np.int32)
+    cnt[0, 0], cnt[0, 1], cnt[1, 2] = 0, 1900, 1
+    idx = np.zeros((B, H, Lcap), np.int32)
+    for b in range(B):
+        for h in range(H):
+            idx[b, h, :cnt[b, h]] = np.sort(g.permutation(cap)[:cnt[b, h]])
+    flag = ig.IG_POOL_FP8 if fmt == "fp8" else ig.IG_POOL_INT4
+    pool = ig.ig_pool_create_ex(1, B, H, d, cap, ig.IG_POOL_COUNTER, flag)
+    try:
+        ig.ig_pool_write(pool, None, 0, dev(K), dev(V))
+        ws = torch.empty(ig.ig_gather_attend_workspace_bytes(B, H, d, Lcap), dtype=torch.uint8, device="cuda")
+        out = torch.empty((B, H, d), dtype=torch.float32, device="cuda")
+        scale = float(np.float32(1.0 / math.sqrt(d)))
+        ig.ig_gather_attend(None, pool, 0, B, H, d, Lcap, scale, dev(q), dev(idx), dev(cnt),
+                            dev(kn) if with_new else None, dev(vn) if with_new else None, out, ws, ws.numel(), 0)
+        ig.ig_check()
+        sets = [[idx[b, h, :cnt[b, h]] for h in range(H)] for b in range(B)]
+        Kg, Vg = ora.gather(K, V, sets, Lcap)
+        if fmt == "fp8":
+            Kg = ora.fp8_dequantize_rows(*ora.fp8_quantize_rows(Kg))
+            Vg = ora.fp8_dequantize_rows(*ora.fp8_quantize_rows(Vg))
+        else:
+            Kg = ora.int4_dequantize_rows(*ora.int4_quantize_rows(Kg))
+            Vg = ora.int4_dequantize_rows(*ora.int4_quantize_rows(Vg))
+        want = ora.attend(q, Kg, Vg, cnt, scale, kn if with_new else None, vn if with_new else None)
+        assert np.abs(host(out) - want).max() <= 2e-3
+    finally:
+        ig.ig_pool_destroy(pool)
