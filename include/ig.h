@@ -435,8 +435,9 @@ typedef struct {
   int fused_select;    /* 1: use ig_speculate_select when policy = IG_SEL_THRESHOLD, cap_frac >= 1
                           and Lcap <= 8192 (scores stay on chip); 0: separate calls */
   int fused_fetch;     /* 1: layers 1.. attend straight from the pool on the fetch stream
-                          (ig_gather_attend), no staging in HBM, Kg/Vg unused (may be NULL);
-                          0: gather into Kg/Vg on the fetch stream, attend on the compute stream */
+                          (ig_gather_attend's partials; its combine runs on the compute stream),
+                          no staging in HBM, Kg/Vg unused (may be NULL); 0: gather into Kg/Vg on
+                          the fetch stream, attend on the compute stream */
   int batched_append;  /* 1: every layer's new token is appended in one launch at the end of the
                           step (ig_append_kv_layers), after the fetches; 0: each layer's append
                           follows its attention */
@@ -651,9 +652,9 @@ uint64_t ig_launch_count(void);
 
 /* Stage timing of a recent ig_decode_step (steps_back = 0: the last one, 1: the one before),
  * when the decoder was created with config.stage_timing = 1: ms_out[0] = sum of gather kernel
- * times (fetch stream; with fused_fetch, of fetch + attention), ms_out[1] = speculate +
+ * times (fetch stream; with fused_fetch, of fetch + partial attention), ms_out[1] = speculate +
  * select, ms_out[2] = attention + append of layers 1.. (compute stream; with fused_fetch, the
- * appends alone), ms_out[3] = layer 0's dense attention + append; counts_out[0..3] = the
+ * combines of the partials and the appends), ms_out[3] = layer 0's dense attention + append; counts_out[0..3] = the
  * number of timed intervals of each (both arrays hold 4 entries).  Waits for that
  * step to finish; reading step t-1 while step t is queued keeps the GPU busy. */
 ig_status ig_decoder_stage_ms(ig_decoder* dec, int steps_back, float* ms_out, int* counts_out);

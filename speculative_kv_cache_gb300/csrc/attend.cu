@@ -27,7 +27,10 @@ constexpr int kAttUnroll = 4;
 constexpr int kMaxAttCtas = 2048;   // upper bound of the balanced grid (sizes the workspace)
 constexpr int kMaxAttUnits = 16384; // (units + 1) ints of shared memory for the scan
 constexpr int kFaThreads = 256;     // fused fetch + attention: as the gather (host-link bound)
-constexpr int kFaUnroll = 6;        // rows per batch and lane group (two batches in flight)
+#ifndef IG_FA_UNROLL
+#define IG_FA_UNROLL 6
+#endif
+constexpr int kFaUnroll = IG_FA_UNROLL;  // rows per batch and lane group (two batches in flight)
 constexpr int kMaxFaCtas = 256;     // upper bound of its grid (sizes its workspace)
 // a partial in the workspace: [max, sum, -, -, unnormalised output[D]] (D + 4 floats, so
 // that the output part of every partial starts on a 16-byte boundary)
@@ -536,10 +539,9 @@ ig_status launch_attend(cudaStream_t st, int B, int H, int Lcap, float scale, co
 }
 
 template <int D, int BITS>
-ig_status launch_fetch_attend(cudaStream_t st, int B, int H, int Lcap, int cap, float scale, const uint16_t* q,
-                              const uint16_t* Kp, const uint16_t* Vp, const uint8_t* Rec, int rec, const float* Sc,
-                              const int32_t* idx, const int32_t* cnt, const uint16_t* kn, const uint16_t* vn,
-                              float* out, void* ws, int grid) {
+ig_status launch_fetch_partials(cudaStream_t st, int B, int H, int Lcap, int cap, float scale, const uint16_t* q,
+                                const uint16_t* Kp, const uint16_t* Vp, const uint8_t* Rec, int rec, const float* Sc,
+                                const int32_t* idx, const int32_t* cnt, void* ws, int grid) {
   const int units = B * H;
   const size_t smem = (size_t)(units + 1) * sizeof(int);
   if (smem > 32 * 1024) {
@@ -552,6 +554,14 @@ ig_status launch_fetch_attend(cudaStream_t st, int B, int H, int Lcap, int cap, 
       reinterpret_cast<const __half*>(q), reinterpret_cast<const uint4*>(Kp), reinterpret_cast<const uint4*>(Vp), Rec,
       rec, Sc, idx, cnt, H, Lcap, units, cap, scale, static_cast<float*>(ws), gpre, error_word());
   IG_CHECK_LAUNCH("fetch-attention launch");
+  return IG_OK;
+}
+
+template <int D>
+ig_status launch_fetch_combine(cudaStream_t st, int B, int H, float scale, const uint16_t* q, const uint16_t* kn,
+                               const uint16_t* vn, float* out, const void* ws, int grid) {
+  const int units = B * H;
+  const int* gpre = reinterpret_cast<const int*>(static_cast<const char*>(ws) + fa_part_bytes(B, H, D));
   k5_combine<D, fa_groups<D>()><<<units, D, 0, st>>>(
       static_cast<const float*>(ws), gpre, units, grid, reinterpret_cast<const __half*>(q),
       reinterpret_cast<const __half*>(kn), reinterpret_cast<const __half*>(vn), scale, out);
@@ -617,11 +627,17 @@ extern "C" size_t ig_gather_attend_workspace_bytes(int B, int H, int d, int Lcap
   return fetch_attend_ws_bytes(B, H, d);
 }
 
-extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int layer, int B, int H,
-                                      int d, int Lcap, float scale, const uint16_t* q,
-                                      const int32_t* idx, const int32_t* cnt,
-                                      const uint16_t* k_new, const uint16_t* v_new, float* out,
-                                      void* workspace, size_t workspace_bytes, int max_ctas) {
+namespace ig {
+
+// The fused fetch + attention in its two launches: the partials (the pool read over the host
+// link, on `st`) and the combine (a CTA per head merges them, adds the current token and
+// normalises).  The decode step puts the combine on its compute stream so that the fetch
+// stream moves straight on to the next layer's rows; *grid_out is the partials' grid, which
+// the combine needs.
+ig_status fetch_attend_partials(cudaStream_t s, const ig_pool* pool, int layer, int B, int H, int d, int Lcap,
+                                float scale, const uint16_t* q, const int32_t* idx, const int32_t* cnt,
+                                const uint16_t* k_new, const uint16_t* v_new, const float* out, void* workspace,
+                                size_t workspace_bytes, int max_ctas, int* grid_out) {
   IG_REQUIRE(pool, "null pool");
   IG_REQUIRE(pool->storage, "the pool was created without storage");
   IG_REQUIRE(layer >= 0 && layer < pool->layers, "layer %d out of range", layer);
@@ -641,17 +657,17 @@ extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int lay
     return fail(IG_ERR_CAPACITY, "fused fetch + attention needs %zu workspace bytes", need);
   IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
   // the same default as the gather (twice it for a quantized pool, whose rows need dequantizing)
-  int grid = max_ctas > 0 ? max_ctas : (pool->qbits ? 2 : 1) * fetch_grid(as_stream(stream));
+  int grid = max_ctas > 0 ? max_ctas : (pool->qbits ? 2 : 1) * fetch_grid(s);
   if (grid < 1) grid = 1;
   if (grid > kMaxFaCtas) grid = kMaxFaCtas;
-  cudaStream_t s = as_stream(stream);
+  *grid_out = grid;
   const size_t rows = (size_t)B * H * pool->cap;
   if (pool->qbits) {
     const uint8_t* Rec = pool->R + (size_t)layer * rows * pool->rec;
     const float* Sc = pool->S + (size_t)layer * rows * 2;
-#define IG_FA_Q(DD, BB)                                                                                     \
-  return launch_fetch_attend<DD, BB>(s, B, H, Lcap, pool->cap, scale, q, nullptr, nullptr, Rec, pool->rec, Sc, idx, \
-                                     cnt, k_new, v_new, out, workspace, grid)
+#define IG_FA_Q(DD, BB)                                                                                      \
+  return launch_fetch_partials<DD, BB>(s, B, H, Lcap, pool->cap, scale, q, nullptr, nullptr, Rec, pool->rec, Sc, \
+                                       idx, cnt, workspace, grid)
     if (pool->qbits == 8) {
       if (d == 128) IG_FA_Q(128, 8);
       IG_FA_Q(64, 8);
@@ -663,8 +679,32 @@ extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int lay
   const uint16_t* Kp = pool->Kdev + (size_t)layer * rows * d;
   const uint16_t* Vp = pool->Vdev + (size_t)layer * rows * d;
   if (d == 128)
-    return launch_fetch_attend<128, 0>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, nullptr, 0, nullptr, idx, cnt,
-                                       k_new, v_new, out, workspace, grid);
-  return launch_fetch_attend<64, 0>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, nullptr, 0, nullptr, idx, cnt,
-                                    k_new, v_new, out, workspace, grid);
+    return launch_fetch_partials<128, 0>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, nullptr, 0, nullptr, idx, cnt,
+                                         workspace, grid);
+  return launch_fetch_partials<64, 0>(s, B, H, Lcap, pool->cap, scale, q, Kp, Vp, nullptr, 0, nullptr, idx, cnt,
+                                      workspace, grid);
+}
+
+// The combine of fetch_attend_partials' launch (same B, H, d, workspace and grid); the caller
+// orders it after the partials.
+ig_status fetch_attend_combine(cudaStream_t s, int B, int H, int d, float scale, const uint16_t* q,
+                               const uint16_t* k_new, const uint16_t* v_new, float* out, const void* workspace,
+                               int grid) {
+  if (d == 128) return launch_fetch_combine<128>(s, B, H, scale, q, k_new, v_new, out, workspace, grid);
+  return launch_fetch_combine<64>(s, B, H, scale, q, k_new, v_new, out, workspace, grid);
+}
+
+}  // namespace ig
+
+extern "C" ig_status ig_gather_attend(void* stream, const ig_pool* pool, int layer, int B, int H,
+                                      int d, int Lcap, float scale, const uint16_t* q,
+                                      const int32_t* idx, const int32_t* cnt,
+                                      const uint16_t* k_new, const uint16_t* v_new, float* out,
+                                      void* workspace, size_t workspace_bytes, int max_ctas) {
+  cudaStream_t s = as_stream(stream);
+  int grid = 0;
+  ig_status st = fetch_attend_partials(s, pool, layer, B, H, d, Lcap, scale, q, idx, cnt, k_new, v_new, out,
+                                       workspace, workspace_bytes, max_ctas, &grid);
+  if (st != IG_OK) return st;
+  return fetch_attend_combine(s, B, H, d, scale, q, k_new, v_new, out, workspace, grid);
 }

@@ -13,22 +13,35 @@
 //   S: wait got[L-1], attention(L-1), append(L-1)
 // so layer 1 is speculated and its fetch starts before layer 0 attends.
 //
-// With config.fused_fetch the selected rows are not staged in HBM: the fetch stream runs the
-// attention itself, reading the rows from the pinned pool (ig_gather_attend):
+// With config.fused_fetch the selected rows are not staged in HBM: the fetch stream reads them
+// from the pinned pool and folds them into per-head partial attention (the partials of
+// ig_gather_attend), and the compute stream merges them (its combine):
 //   for l = 1 .. L-1:
-//     S: (l >= 3: wait att[l-2], the attention that yields layer l-1's input; append(l-2))
+//     S: (l >= 3: wait att[l-2]; combine(l-2), the attention that yields layer l-1's input;
+//        append(l-2))
 //        speculate(l), select(l), record sel[l]
-//     G: wait sel[l], fetch + attention(l), record att[l]
+//     G: wait sel[l], fetch + partial attention(l) into partial set l % 2, record att[l]
 //     S: (l == 1) dense attention(0), append(0)
-//   S: wait att[L-2], append(L-2); wait att[L-1], append(L-1)
+//   S: wait att[L-2], combine + append(L-2); wait att[L-1], combine + append(L-1)
 // so the fetch stream does nothing but fetch and attend.  Selection l reuses index buffer
-// l % 2 only after attention(l-2) has finished with it (config.keep_indices gives every layer
-// a list of its own instead).
+// l % 2, and the fetch of layer l partial set l % 2, only after combine(l-2) (which S runs
+// before selection l) is done with them (config.keep_indices gives every layer an index list
+// of its own instead).
 #include <limits>
 #include <vector>
 
 #include "ig_common.cuh"
 #include "pool_impl.h"
+
+namespace ig {
+ig_status fetch_attend_partials(cudaStream_t s, const ig_pool* pool, int layer, int B, int H, int d, int Lcap,
+                                float scale, const uint16_t* q, const int32_t* idx, const int32_t* cnt,
+                                const uint16_t* k_new, const uint16_t* v_new, const float* out, void* workspace,
+                                size_t workspace_bytes, int max_ctas, int* grid_out);
+ig_status fetch_attend_combine(cudaStream_t s, int B, int H, int d, float scale, const uint16_t* q,
+                               const uint16_t* k_new, const uint16_t* v_new, float* out, const void* workspace,
+                               int grid);
+}  // namespace ig
 
 struct ig_decoder {
   ig_decoder_config cfg{};
@@ -91,7 +104,9 @@ void ws_regions(const ig_decoder_config* c, size_t* main, size_t* sel, size_t* f
   const size_t b = ig_attend_workspace_bytes(c->B, c->H, c->d, c->Lcap);
   *main = round_up(a > b ? a : b, 256);
   *sel = round_up(ig_select_workspace_bytes(c->B, c->H), 256);
-  *fetch = c->fused_fetch ? round_up(ig_gather_attend_workspace_bytes(c->B, c->H, c->d, c->Lcap), 256) : 0;
+  // fused fetch: two partial sets, by layer parity (the combine of layer l runs on the compute
+  // stream while the fetch stream writes layer l+1's partials)
+  *fetch = c->fused_fetch ? 2 * round_up(ig_gather_attend_workspace_bytes(c->B, c->H, c->d, c->Lcap), 256) : 0;
 }
 
 }  // namespace
@@ -204,7 +219,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
   const size_t spec_att_ws = dec->ws_main;
   void* sel_ws = ws + dec->ws_main;
   const size_t sel_ws_bytes = dec->ws_sel;
-  void* fetch_ws = ws + dec->ws_main + dec->ws_sel;
+  char* fetch_ws = ws + dec->ws_main + dec->ws_sel;
   ig_status st;
   cudaError_t e;
 
@@ -309,16 +324,22 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     return st != IG_OK ? st : batched_tail();
   }
   if (c.fused_fetch) {
-    // append(l) on S once the fetch stream's attention(l) has read the pool (the new token may
-    // overwrite an evicted slot) and speculation(l) has read the partial cache
-    auto append_after_fetch = [&](int l) -> ig_status {
+    // combine(l) and append(l) on S once the fetch stream's partials of layer l are done: the
+    // append only then, because the new token may overwrite an evicted slot that the fetch read
+    // (speculation(l) has read the partial cache before)
+    const size_t fetch_half = dec->ws_fetch / 2;
+    std::vector<int> fa_grid(L, 0);
+    auto combine_append = [&](int l) -> ig_status {
       cudaError_t ae = cudaStreamWaitEvent(S, dec->ev_att[l], 0);
       if (ae == cudaSuccess) ae = rec(dec->ta0, l, S);
       if (ae != cudaSuccess) return cuda_fail(ae, "decode step wait");
+      const size_t off = (size_t)l * ts;
+      ig_status r = fetch_attend_combine(S, B, H, d, c.score_scale, io->q + off, io->k_new + off, io->v_new + off,
+                                         io->out + off, fetch_ws + (size_t)(l & 1) * fetch_half, fa_grid[l]);
+      if (r != IG_OK) return r;
       if (io->slot && !c.batched_append) {
-        const size_t off = (size_t)l * ts;
-        ig_status r = ig_append_kv(S, dec->pool, l, B, H, d, ks[l], Lc, io->slot + (size_t)l * B, dec->cols[l],
-                                   io->k_new + off, io->v_new + off, dec->Kpart[l], nullptr, nullptr);
+        r = ig_append_kv(S, dec->pool, l, B, H, d, ks[l], Lc, io->slot + (size_t)l * B, dec->cols[l],
+                         io->k_new + off, io->v_new + off, dec->Kpart[l], nullptr, nullptr);
         if (r != IG_OK) return r;
       }
       ae = rec(dec->ta1, l, S);
@@ -326,18 +347,18 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
     };
     for (int l = 1; l < L; ++l) {
       if (l >= 3) {  // attention(l-2) yields layer l-1's input, which speculation(l) reads
-        st = append_after_fetch(l - 2);
+        st = combine_append(l - 2);
         if (st != IG_OK) return st;
       }
       st = spec_select(l);
       if (st != IG_OK) return st;
+      // the partial set l % 2 was last read by combine(l-2), which S ran before selection(l)
       e = rec(dec->tg0, l, G);
       if (e != cudaSuccess) return cuda_fail(e, "timing event");
       const size_t off = (size_t)l * ts;
-      st = ig_gather_attend(G, dec->pool, l, B, H, d, Lc, c.score_scale, io->q + off,
-                            b.idx + idx_off(c, l), b.cnt + (size_t)l * B * H,
-                            io->k_new + off, io->v_new + off, io->out + off, fetch_ws, dec->ws_fetch,
-                            c.gather_ctas);
+      st = fetch_attend_partials(G, dec->pool, l, B, H, d, Lc, c.score_scale, io->q + off, b.idx + idx_off(c, l),
+                                 b.cnt + (size_t)l * B * H, io->k_new + off, io->v_new + off, io->out + off,
+                                 fetch_ws + (size_t)(l & 1) * fetch_half, fetch_half, c.gather_ctas, &fa_grid[l]);
       if (st != IG_OK) return st;
       e = rec(dec->tg1, l, G);
       if (e == cudaSuccess) e = cudaEventRecord(dec->ev_att[l], G);
@@ -348,7 +369,7 @@ extern "C" ig_status ig_decode_step(ig_decoder* dec, const ig_step_io* io, void*
       }
     }
     for (int l = L - 2 > 1 ? L - 2 : 1; l < L; ++l) {
-      st = append_after_fetch(l);
+      st = combine_append(l);
       if (st != IG_OK) return st;
     }
     e = cudaEventRecord(dec->ev_join, G);

@@ -61,8 +61,9 @@ def test_decoder_fused_fetch_needs_no_staging_buffers_and_a_fetch_workspace(ig):
                 score_scale=0.125, rope_theta=0.0, gather_ctas=0, stage_timing=0, fused_select=1)
     staged = ig.ig_decoder_workspace_bytes(ig.DecoderConfig(**base, fused_fetch=0))
     fused = ig.ig_decoder_workspace_bytes(ig.DecoderConfig(**base, fused_fetch=1))
-    # the fetch stream's attention gets a region of its own
-    assert fused - staged == ig.ig_gather_attend_workspace_bytes(2, 4, 64, 64)
+    # the fetch stream's partial attention gets two regions of its own (by layer parity: the
+    # compute stream combines layer l's partials while the fetch stream writes layer l+1's)
+    assert fused - staged == 2 * ig.ig_gather_attend_workspace_bytes(2, 4, 64, 64)
     # per-head partials of every lane group: (B*H + 256 CTAs) x 32 groups x (d + 2) floats
     assert ig.ig_gather_attend_workspace_bytes(2, 4, 64, 64) >= (8 + 256) * 32 * 66 * 4
     assert ig.ig_gather_attend_workspace_bytes(2, 4, 96, 64) == 0
