@@ -513,8 +513,11 @@ inline size_t prefix_bytes(int B, int H) { return round_up((size_t)(B * H + 1) *
 
 // 8 CTAs of 4 warps per SM (the register limit at 64 per thread): 32 warps, 8 rows in flight
 // each, to cover the memory latency
+#ifndef IG_ATT_CTAS_PER_SM
+#define IG_ATT_CTAS_PER_SM 8
+#endif
 inline int att_grid(cudaStream_t st) {
-  int g = 8 * sm_count(st);
+  int g = IG_ATT_CTAS_PER_SM * sm_count(st);
   return g > kMaxAttCtas ? kMaxAttCtas : g;
 }
 

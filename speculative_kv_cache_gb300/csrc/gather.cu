@@ -20,7 +20,17 @@ namespace ig {
 namespace {
 
 constexpr int kGatherThreads = 256;
-constexpr int kUnroll = 8;  // 8 rows x (K, V) in flight per lane: 205 GB/s alone at 38 CTAs
+// 4 rows x (K, V) in flight per lane at 64 registers (4 CTAs' worth per SM): a gather CTA then
+// fits beside the compute stream's kernels, which leave it 16 K registers but not the 27 K it
+// took at 8 rows and 106 registers.  Live, Llama-2-7B alpha = 2: 5.2-5.4 -> 4.93 ms per step (the
+// fetch no longer waits for SMs to drain before it starts); OPT-30B unchanged at 195 GB/s.
+#ifndef IG_G_UNROLL
+#define IG_G_UNROLL 4
+#endif
+#ifndef IG_G_MIN_CTAS
+#define IG_G_MIN_CTAS 4
+#endif
+constexpr int kUnroll = IG_G_UNROLL;  // rows x (K, V) in flight per lane
 #ifndef IG_GQ_UNROLL
 #define IG_GQ_UNROLL 4
 #endif
@@ -30,7 +40,7 @@ constexpr int kUnroll = 8;  // 8 rows x (K, V) in flight per lane: 205 GB/s alon
 constexpr int kUnroll8 = IG_GQ_UNROLL;  // quantized records: one 16-byte load per lane and row, so more rows
 constexpr int kMaxGatherUnits = 32768;  // (units + 1) ints of shared memory: 128 KB
 
-__global__ void __launch_bounds__(kGatherThreads) k4_gather(
+__global__ void __launch_bounds__(kGatherThreads, IG_G_MIN_CTAS) k4_gather(
     const uint4* __restrict__ Kp, const uint4* __restrict__ Vp, int units, int cap, int vpr,
     int Lcap, const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt,
     uint4* __restrict__ Kg, uint4* __restrict__ Vg, int* err) {
