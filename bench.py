@@ -311,13 +311,14 @@ def measured_peaks():
 
 
 def gather_kernel_key(src: str) -> str:
-    """The fp16 fetch kernel's source as the counters depend on it: the file's constants (code
-    without comments) and the text of the k4_gather function itself, so that edits elsewhere in
+    """The fp16 fetch kernel's source as the counters depend on it: the file's constants and macro
+    defaults (code without comments) and the text of the k4_gather function itself, so that edits elsewhere in
     the file (the quantized fetch) do not void the counters."""
     start = src.index("k4_gather(")
     start = src.rfind("\n", 0, src.rfind("__global__", 0, start)) + 1
     end = src.index("\n}\n", start) + 3
-    consts = [ln.split("//")[0].rstrip() for ln in src.splitlines() if ln.startswith("constexpr")]
+    consts = [ln.split("//")[0].rstrip() for ln in src.splitlines()
+              if ln.startswith("constexpr") or ln.startswith("#define")]
     return "\n".join(consts) + "\n" + src[start:end]
 
 

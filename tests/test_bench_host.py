@@ -97,9 +97,11 @@ def test_gather_kernel_key_is_the_fp16_fetch_kernel():
     src = open(os.path.join(ROOT, "speculative_kv_cache_gb300", "csrc", "gather.cu")).read()
     key = bench.gather_kernel_key(src)
     body = key[key.index("__global__"):]
-    assert body.startswith("__global__ void __launch_bounds__(kGatherThreads) k4_gather(")
+    assert body.startswith("__global__ void __launch_bounds__(kGatherThreads, IG_G_MIN_CTAS) k4_gather(")
     assert "k4_gather_q" not in body and body.endswith("\n}\n")
-    assert "constexpr int kUnroll = 8;" in key
+    assert "constexpr int kUnroll = IG_G_UNROLL;" in key and "#define IG_G_UNROLL 4" in key
+    # the rows in flight are part of the key
+    assert bench.gather_kernel_key(src.replace("#define IG_G_UNROLL 4", "#define IG_G_UNROLL 8")) != key
     # an edit outside the kernel leaves the key unchanged; one inside changes it
     assert bench.gather_kernel_key(src.replace("k4_gather_q", "k4_gather_x")) == key
     assert bench.gather_kernel_key(src.replace("kv[q] = ld_nc_v4(Kp + src);", "kv[q] = ld_nc_v4(Kp + src + 0);")) != key
