@@ -26,11 +26,21 @@ constexpr int kAttThreads = 128;
 constexpr int kAttUnroll = 4;
 constexpr int kMaxAttCtas = 2048;   // upper bound of the balanced grid (sizes the workspace)
 constexpr int kMaxAttUnits = 16384; // (units + 1) ints of shared memory for the scan
-constexpr int kFaThreads = 256;     // fused fetch + attention: as the gather (host-link bound)
+#ifndef IG_FA_THREADS
+#define IG_FA_THREADS 256
+#endif
+#ifndef IG_FA_MIN_CTAS
+#define IG_FA_MIN_CTAS 1
+#endif
+constexpr int kFaThreads = IG_FA_THREADS;  // fused fetch + attention: as the gather (host-link bound)
 #ifndef IG_FA_UNROLL
 #define IG_FA_UNROLL 6
 #endif
-constexpr int kFaUnroll = IG_FA_UNROLL;  // rows per batch and lane group (two batches in flight)
+#ifndef IG_FA_UNROLL_Q
+#define IG_FA_UNROLL_Q IG_FA_UNROLL
+#endif
+// rows per batch and lane group (two batches in flight): fp16 rows, quantized rows
+__host__ __device__ constexpr int fa_unroll(int bits) { return bits ? IG_FA_UNROLL_Q : IG_FA_UNROLL; }
 constexpr int kMaxFaCtas = 256;     // upper bound of its grid (sizes its workspace)
 // a partial in the workspace: [max, sum, -, -, unnormalised output[D]] (D + 4 floats, so
 // that the output part of every partial starts on a 16-byte boundary)
@@ -202,7 +212,7 @@ __global__ void __launch_bounds__(kAttThreads) k5_attend(
 
 // Fused fetch + attention straight from the pinned pool.  The CTA's rows (the same balanced
 // split as above) are streamed as in the gather, without stopping at head boundaries: lane
-// group g takes rows start + g, start + g + NG, ..., kFaUnroll of them in flight, each with
+// group g takes rows start + g, start + g + NG, ..., fa_unroll(BITS) of them in flight, each with
 // its head's query chunk (loaded where the head changes), and keeps one online softmax for its
 // current head.  When its next
 // row belongs to another head it writes its partial to ws[(head + CTA) * NG + g] and starts
@@ -259,7 +269,7 @@ __device__ __forceinline__ uint4 dq4(uint32_t c, float sc) {
 }
 
 template <int D, int BITS>
-__global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
+__global__ void __launch_bounds__(kFaThreads, IG_FA_MIN_CTAS) k5_fetch_attend(
     const __half* __restrict__ q, const uint4* __restrict__ Kp, const uint4* __restrict__ Vp,
     const uint8_t* __restrict__ Rec, int rec, const float* __restrict__ Sc,
     const int32_t* __restrict__ idx, const int32_t* __restrict__ cnt, int H, int Lcap, int units,
@@ -301,12 +311,13 @@ __global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
       w[1] = l;
     }
   };
-  // Software pipeline over batches of kFaUnroll rows per group: the loads of batch n + 1
+  constexpr int kFaU = fa_unroll(BITS);
+  // Software pipeline over batches of kFaU rows per group: the loads of batch n + 1
   // (index, then pool rows and, where the head changes, the query chunk) are issued before
   // batch n is folded in, so the host link always has this group's rows in flight.
-  auto prepare = [&](int rw, int (&hu)[kFaUnroll], int (&slot)[kFaUnroll]) {
+  auto prepare = [&](int rw, int (&hu)[kFaU], int (&slot)[kFaU]) {
 #pragma unroll
-    for (int x = 0; x < kFaUnroll; ++x) {
+    for (int x = 0; x < kFaU; ++x) {
       const int rr = rw + sub + x * NG;
       hu[x] = -1;
       slot[x] = -1;
@@ -320,10 +331,10 @@ __global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
     }
   };
   // the query chunk is loaded only where the head changes (a group's rows mostly share one)
-  auto issue = [&](const int (&hu)[kFaUnroll], const int (&slot)[kFaUnroll], int prev, FaRow<BITS> (&rw_)[kFaUnroll],
-                   uint4 (&qv)[kFaUnroll]) {
+  auto issue = [&](const int (&hu)[kFaU], const int (&slot)[kFaU], int prev, FaRow<BITS> (&rw_)[kFaU],
+                   uint4 (&qv)[kFaU]) {
 #pragma unroll
-    for (int x = 0; x < kFaUnroll; ++x) {
+    for (int x = 0; x < kFaU; ++x) {
       rw_[x] = FaRow<BITS>{};
       qv[x] = make_uint4(0, 0, 0, 0);
       if (hu[x] >= 0 && hu[x] != (x == 0 ? prev : hu[x - 1]))
@@ -357,23 +368,23 @@ __global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
     else if constexpr (BITS == 8) return dq8(r.v, r.s.y);
     else return dq4(r.v, r.s.y);
   };
-  int hu[kFaUnroll], slot[kFaUnroll], hn[kFaUnroll], sn[kFaUnroll];
-  FaRow<BITS> cu[kFaUnroll], nx[kFaUnroll];
-  uint4 qv[kFaUnroll], qn[kFaUnroll];
+  int hu[kFaU], slot[kFaU], hn[kFaU], sn[kFaU];
+  FaRow<BITS> cu[kFaU], nx[kFaU];
+  uint4 qv[kFaU], qn[kFaU];
   int rw = r0 + warp * RPW;
   prepare(rw, hu, slot);
   issue(hu, slot, -1, cu, qv);
   // warp-uniform trip count (the shuffles take the full mask); rows past the end compute on
   // zeros and change nothing
   while (rw < r1) {
-    const int rnext = rw + NG * kFaUnroll;
+    const int rnext = rw + NG * kFaU;
     int last = cur;  // head of the last row of this batch (the query in use when the next starts)
 #pragma unroll
-    for (int x = 0; x < kFaUnroll; ++x) last = hu[x] >= 0 ? hu[x] : last;
+    for (int x = 0; x < kFaU; ++x) last = hu[x] >= 0 ? hu[x] : last;
     prepare(rnext, hn, sn);
     issue(hn, sn, last, nx, qn);
 #pragma unroll
-    for (int x = 0; x < kFaUnroll; ++x) {
+    for (int x = 0; x < kFaU; ++x) {
       if (hu[x] >= 0 && hu[x] != cur) {  // a new head: hand over the previous one's partial
         if (cur >= 0) flush();
         cur = hu[x];
@@ -389,7 +400,7 @@ __global__ void __launch_bounds__(kFaThreads) k5_fetch_attend(
       if (slot[x] >= 0) online_add(z, value_of(cu[x]), m, l, acc);
     }
 #pragma unroll
-    for (int x = 0; x < kFaUnroll; ++x) {
+    for (int x = 0; x < kFaU; ++x) {
       hu[x] = hn[x];
       slot[x] = sn[x];
       cu[x] = nx[x];
@@ -668,7 +679,7 @@ ig_status fetch_attend_partials(cudaStream_t s, const ig_pool* pool, int layer, 
     return fail(IG_ERR_CAPACITY, "fused fetch + attention needs %zu workspace bytes", need);
   IG_REQUIRE(aligned(workspace, 256), "workspace must be 256-byte aligned");
   // the same default as the gather (twice it for a quantized pool, whose rows need dequantizing)
-  int grid = max_ctas > 0 ? max_ctas : (pool->qbits ? 2 : 1) * fetch_grid(s);
+  int grid = max_ctas > 0 ? max_ctas : (pool->qbits ? 2 : 1) * (256 / kFaThreads) * fetch_grid(s);
   if (grid < 1) grid = 1;
   if (grid > kMaxFaCtas) grid = kMaxFaCtas;
   *grid_out = grid;
