@@ -81,21 +81,39 @@ __device__ __forceinline__ void online_add(float z, uint4 vv, float& m, float& l
 
 // Exclusive scan of the clamped per-unit row counts into pre[0..units] (pre[units] = R).
 // cnt_per_seq: the count of unit u is cnt[u / H] (dense attention) instead of cnt[u].
+// The counts are first copied to shared memory with coalesced loads, kScanBatch of them in
+// flight per thread (one round trip for up to kScanBatch * THREADS units: this prologue is on
+// every CTA's critical path), then each thread sums a contiguous chunk and the chunk sums are
+// scanned across the block.
+constexpr int kScanBatch = 8;
 template <int THREADS>
 __device__ void scan_counts(const int32_t* cnt, int cnt_per_seq, int H, int units, int Lcap, int* pre,
                             int* wsum, int* err) {
+  for (int base = 0; base < units; base += kScanBatch * THREADS) {
+    int c[kScanBatch];
+#pragma unroll
+    for (int x = 0; x < kScanBatch; ++x) {
+      const int u = base + x * THREADS + (int)threadIdx.x;
+      c[x] = u < units ? (cnt_per_seq ? cnt[u / H] : cnt[u]) : 0;
+    }
+#pragma unroll
+    for (int x = 0; x < kScanBatch; ++x) {
+      const int u = base + x * THREADS + (int)threadIdx.x;
+      if (u < units) {
+        int v = c[x];
+        if (v < 0 || v > Lcap) {
+          raise_error(err, IG_DEVERR_INDEX);
+          v = v < 0 ? 0 : Lcap;
+        }
+        pre[u + 1] = v;
+      }
+    }
+  }
+  __syncthreads();
   const int per = (units + THREADS - 1) / THREADS;
   const int u0 = threadIdx.x * per;
   int local = 0;
-  for (int u = u0; u < min(units, u0 + per); ++u) {
-    int c = cnt_per_seq ? cnt[u / H] : cnt[u];
-    if (c < 0 || c > Lcap) {
-      raise_error(err, IG_DEVERR_INDEX);
-      c = c < 0 ? 0 : Lcap;
-    }
-    pre[u + 1] = c;
-    local += c;
-  }
+  for (int u = u0; u < min(units, u0 + per); ++u) local += pre[u + 1];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = local;
   for (int o = 1; o < 32; o <<= 1) {
