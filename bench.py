@@ -397,7 +397,10 @@ def oracle_on_bench_data(torch, w, alpha, device, n_seq: int) -> tuple[float, in
 
     scale = 1.0 / math.sqrt(w.head_dim)
     bs = list(range(n_seq))
-    L = np.full(n_seq, w.prompt, dtype=np.int32)
+    # resident tokens after the prompt: all of it, or the pool's capacity when the pool is
+    # smaller (the decoder's positions default to the same count)
+    n_res = min(w.prompt, w.pool_cap)
+    L = np.full(n_seq, n_res, dtype=np.int32)
     x, q, kn, vn = (t[:, bs].cpu().numpy() for t in synth.torch_step_inputs(w, 0, device))
     total = 0.0
     for l in range(w.layers):
@@ -409,7 +412,7 @@ def oracle_on_bench_data(torch, w, alpha, device, n_seq: int) -> tuple[float, in
         Kpart = ora.partial_key_cache(K, cols) if l else None  # built by the prefill: not timed
         t0 = time.perf_counter()
         if l == 0:
-            ora.attend(q[0], K, V, np.full((n_seq, w.heads), w.prompt), scale, kn[0], vn[0])
+            ora.attend(q[0], K, V, np.full((n_seq, w.heads), n_res), scale, kn[0], vn[0])
         else:
             if w.rope_theta:
                 qp = ora.partial_query_rope(x[l - 1], W[0], W[1], cols, L, w.rope_theta)

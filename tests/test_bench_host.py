@@ -105,3 +105,18 @@ def test_gather_kernel_key_is_the_fp16_fetch_kernel():
     # an edit outside the kernel leaves the key unchanged; one inside changes it
     assert bench.gather_kernel_key(src.replace("k4_gather_q", "k4_gather_x")) == key
     assert bench.gather_kernel_key(src.replace("kv[q] = ld_nc_v4(Kp + src);", "kv[q] = ld_nc_v4(Kp + src + 0);")) != key
+
+
+@pytest.mark.parametrize("name,over", [
+    ("opt-30b", dict(layers=2, heads=2, hidden=256, batch=2, prompt=96, gen=8)),
+    # a pool smaller than the prompt (the Llama-2-13B 60 % pool): the oracle sees the resident rows
+    ("llama-2-13b", dict(layers=2, heads=2, hidden=256, batch=2, prompt=200, gen=20)),
+])
+def test_cpu_baseline_runs_on_small_copies_of_the_workloads(name, over):
+    import bench
+    from speculative_kv_cache_gb300 import synth
+
+    w = synth.scaled(synth.WORKLOADS[name], **over)
+    assert (w.pool_cap < w.prompt) == (name == "llama-2-13b")
+    secs, n = bench.oracle_on_bench_data(torch, w, w.alphas[0], "cpu", 1)
+    assert n == 1 and secs > 0
