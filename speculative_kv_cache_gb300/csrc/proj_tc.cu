@@ -63,7 +63,13 @@ constexpr int kTcM = 128;       // output components per CTA (tcgen05 M)
 constexpr int kTcN = 16;        // batch rows per CTA (tcgen05 N)
 constexpr int kTcBK = 64;       // K per stage: one 128-byte swizzle atom of fp16
 constexpr int kTcThreads = 128;
-constexpr int kTcRing = 4;      // stages in the ring
+#ifndef IG_TC_RING
+#define IG_TC_RING 4
+#endif
+#ifndef IG_TC_CTAS_PER_SM
+#define IG_TC_CTAS_PER_SM 2
+#endif
+constexpr int kTcRing = IG_TC_RING;  // stages in the ring
 constexpr uint32_t kStageA = kTcM * kTcBK * 2;  // 16 KB
 constexpr uint32_t kStageB = kTcN * kTcBK * 2;  // 2 KB
 constexpr uint32_t kTmemCols = 32;              // minimum allocation; 16 columns used
@@ -215,7 +221,7 @@ size_t tc_smem_bytes() { return 1024 + kTcRing * (kStageA + kStageB) + (2 * kTcR
 // Split of the reduction axis: about two CTAs per SM over the (component tile, batch chunk)
 // grid, at most S splits (the workspace's), each a multiple of 64 wide.
 int tc_split_k(int D, int S, int tiles, int sms) {
-  int want = (2 * sms + tiles / 2) / (tiles > 0 ? tiles : 1);
+  int want = (IG_TC_CTAS_PER_SM * sms + tiles / 2) / (tiles > 0 ? tiles : 1);
   if (want < 1) want = 1;
   if (want > S) want = S;
   int per = (D + want - 1) / want;
