@@ -664,6 +664,10 @@ def run_ours(args, w, alpha):
                                        "int4 codes in the pinned pool, fp32 row scales in HBM" if args.pool_int4
                                        else "fp16"),
                            pool_policy=args.pool_policy if w.pool_frac < 1 else None,
+                           # the pinned pool as allocated: fp16 rows, or one record of codes per row
+                           pinned_pool_gb=round(w.layers * w.batch * w.heads * w.pool_cap
+                                                * (2 * w.head_dim if args.pool_fp8 else w.head_dim if args.pool_int4
+                                                   else 4 * w.head_dim) / 1e9, 2),
                            sm_split=({"fetch_sms": dec.fetch_sms, "compute_sms": dec.compute_sms}
                                      if args.sm_split else None)),
             "step_ms": {"p50": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms),

@@ -175,16 +175,17 @@ def test_decoder_with_int4_pool(mods, fused_fetch):
 
 @pytest.mark.parametrize("fmt", ["fp8", "int4"])
 @pytest.mark.parametrize("with_new", [False, True])
-def test_fused_fetch_attend_on_quantized_pools(mods, fmt, with_new):
+@pytest.mark.parametrize("d", [128, 64])
+def test_fused_fetch_attend_on_quantized_pools(mods, fmt, with_new, d):
     """ig_gather_attend on a quantized pool (codes over the host link, scales from HBM,
     dequantized in registers) against the oracle: its own quantization of the same seeded rows,
-    dequantized, then its attention over the same index sets.  The OPT-30B recipe (head
-    dimension, key scale, planted rows) at 2 sequences x 8 heads, so the pure-Python e4m3
-    encoder finishes in seconds; quantization is row by row, so quantizing only the gathered
-    rows equals quantizing the pool."""
+    dequantized, then its attention over the same index sets.  The OPT-30B recipe (key scale,
+    planted rows) at 2 sequences x 8 heads and head dimensions 128 and 64, so that the
+    pure-Python e4m3 encoder finishes in seconds; quantization is row by row, so quantizing only
+    the gathered rows equals quantizing the pool."""
     ig, _ = mods
-    w = synth.scaled(synth.WORKLOADS["opt-30b"], batch=2, heads=8)
-    B, H, d, cap, Lcap = w.batch, w.heads, w.head_dim, 2048, 2048
+    w = synth.scaled(synth.WORKLOADS["opt-30b"], batch=2, heads=8, head_dim=d)
+    B, H, cap, Lcap = w.batch, w.heads, 2048, 2048
     K, V = synth.pool_layer(w, 1, cap=cap)
     q, kn, vn = synth.token_inputs(w, 1, 0)
     g = np.random.default_rng(5)
