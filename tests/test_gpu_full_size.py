@@ -1,14 +1,15 @@
 """The benchmarked decode step at each workload's full size, every layer, against the oracle.
 
-The decoder runs exactly as the benchmark runs it (CUDA-graph replay, fused score + select on
-thread-block clusters, the fetch staged in HBM on a side stream, the fp16 pool in pinned host
-memory, stage timing on), over the benchmark's own seeded inputs, for every generated token of
+The decoder runs exactly as the benchmark runs it (CUDA-graph replay, fused score + select, the
+fetch staged in HBM on a side stream, the fp16 pool in pinned host memory, stage timing on; and
+the benchmark's INT4 variant: INT4 codes in the pool, fetch and attention fused), over the benchmark's own seeded inputs, for every generated token of
 the workload (128 steps, appends and, for the capped Llama-2-13B pool, evictions included).
 At the first and the last step the oracle replays every layer for the first and the last
 sequence, all heads, from the same input bytes and its own copy of the pool (the seeded rows
 plus the tokens appended at the slots its own counter pool chose): speculation, threshold
 selection and attention, each as the InfiniGen summary's section 3.4 "Decoding Stage" states
-it (Steps 1-5), plus the dense layer 0.  The decoder keeps every layer's index list
+it (Steps 1-5), plus the dense layer 0 (HBM-resident, fp16 either way); with the INT4 pool the
+attention's rows are the oracle's own INT4 quantization of its pool rows, dequantized.  The decoder keeps every layer's index list
 (``keep_indices``; the kernels and grids are those of the benchmark).
 
 Tolerances (the stated ones): index sets equal except tokens whose oracle score lies within
@@ -33,8 +34,10 @@ from speculative_kv_cache_gb300 import synth  # noqa: E402
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 DEV = "cuda:0"
-CASES = [("opt-30b", 4.0), ("opt-6.7b", 4.0), ("llama-2-7b", 2.0), ("llama-2-7b", 4.0),
-         ("llama-2-7b", 6.0), ("llama-2-13b", 4.0)]
+CASES = [("opt-30b", 4.0, "fp16"), ("opt-6.7b", 4.0, "fp16"), ("llama-2-7b", 2.0, "fp16"),
+         ("llama-2-7b", 4.0, "fp16"), ("llama-2-7b", 6.0, "fp16"), ("llama-2-13b", 4.0, "fp16"),
+         # the benchmark's INT4 variant: INT4 codes in the pool, fetch and attention fused
+         ("opt-30b", 4.0, "int4")]
 
 
 @pytest.fixture(scope="module")
@@ -49,12 +52,28 @@ def mods():
     return ig, decoder
 
 
-def _bench_decoder(decoder, w, alpha):
-    """The decoder with the benchmark's default options."""
+def _bench_decoder(decoder, w, alpha, pool):
+    """The decoder with the benchmark's default options (for an INT4 pool: the fused fetch)."""
+    int4 = pool == "int4"
     return decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k,
                            Lcap=w.lcap, pool_cap=w.pool_cap, alpha=alpha, rope_theta=w.rope_theta,
                            gather_ctas=0, stage_timing=True, graph=True, fused_select=True,
-                           fused_fetch=False, keep_indices=True, device=DEV)
+                           fused_fetch=int4, pool_int4=int4, keep_indices=True, device=DEV)
+
+
+def _pool_rows(Kg, Vg, cnt, pool):
+    """The rows the attention sees: the pool's own (fp16), or the oracle's INT4 quantization of
+    them, dequantized (row by row, so quantizing the gathered rows equals quantizing the pool;
+    only the first cnt[b, h] rows of each head are used, and only they are quantized)."""
+    if pool == "fp16":
+        return Kg, Vg
+    valid = np.arange(Kg.shape[2])[None, None, :] < np.asarray(cnt)[:, :, None]
+    out = []
+    for X in (Kg, Vg):
+        Y = X.copy()
+        Y[valid] = ora.int4_dequantize_rows(*ora.int4_quantize_rows(X[valid]))
+        out.append(Y)
+    return out[0], out[1]
 
 
 def _load(dec, w):
@@ -86,7 +105,7 @@ def _oracle_layer_state(w, l, bs, appends):
     return host
 
 
-def _check_step(w, alpha, dec, s, x, q, kn, vn, out, used, L_now, bs, appends):
+def _check_step(w, alpha, dec, s, x, q, kn, vn, out, used, L_now, bs, appends, pool):
     """Every layer of step s for sequences ``bs`` against the oracle; returns (exempt, selected)."""
     scale = np.float32(1.0 / math.sqrt(w.head_dim))
     nb = len(bs)
@@ -127,12 +146,12 @@ def _check_step(w, alpha, dec, s, x, q, kn, vn, out, used, L_now, bs, appends):
                 same[j, h] = not diff
                 selected += g.size
         # attention: over the oracle's own sets where they match, over the GPU's where they differ
-        Kg, Vg = ora.gather(st["K"], st["V"], want, w.lcap)
+        Kg, Vg = _pool_rows(*ora.gather(st["K"], st["V"], want, w.lcap), want_cnt, pool)
         o_own = ora.attend(q_h[l], Kg, Vg, want_cnt, scale, kn_h[l], vn_h[l])
         err = np.abs(o_gpu[l] - o_own).max(axis=2)
         assert err[same].max(initial=0.0) <= 2e-3, f"step {s} layer {l}: output error {err[same].max()}"
         if not same.all():
-            Kg, Vg = ora.gather(st["K"], st["V"], gpu_sets, w.lcap)
+            Kg, Vg = _pool_rows(*ora.gather(st["K"], st["V"], gpu_sets, w.lcap), cnt_gpu[l], pool)
             o_gs = ora.attend(q_h[l], Kg, Vg, cnt_gpu[l], scale, kn_h[l], vn_h[l])
             assert np.abs(o_gpu[l] - o_gs)[~same].max() <= 2e-3
         # the per-slot use flags the pool manager reads: the union of the heads' sets
@@ -146,13 +165,14 @@ def _check_step(w, alpha, dec, s, x, q, kn, vn, out, used, L_now, bs, appends):
     return exempt, selected
 
 
-@pytest.mark.parametrize("name,alpha", CASES, ids=[f"{n}-a{a:g}" for n, a in CASES])
-def test_benched_step_at_full_size(mods, name, alpha):
+@pytest.mark.parametrize("name,alpha,pool", CASES,
+                         ids=[f"{n}-a{a:g}" + ("" if p == "fp16" else f"-{p}") for n, a, p in CASES])
+def test_benched_step_at_full_size(mods, name, alpha, pool):
     ig, decoder = mods
     w = synth.WORKLOADS[name]
     assert alpha in w.alphas
     bs = [0, w.batch - 1]
-    dec = _bench_decoder(decoder, w, alpha)
+    dec = _bench_decoder(decoder, w, alpha, pool)
     try:
         _load(dec, w)
         capped = w.pool_cap < w.context
@@ -183,7 +203,7 @@ def test_benched_step_at_full_size(mods, name, alpha):
             if not capped:
                 assert np.all(want_slots == w.prompt + s)
             if s in (0, w.gen - 1):
-                e, n = _check_step(w, alpha, dec, s, x, q, kn, vn, out, used, L_now, bs, appends)
+                e, n = _check_step(w, alpha, dec, s, x, q, kn, vn, out, used, L_now, bs, appends, pool)
                 exempt += e
                 selected += n
             appends.append((want_slots, kn[:, bs].cpu().numpy(), vn[:, bs].cpu().numpy()))
