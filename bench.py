@@ -47,7 +47,7 @@ def parse_args(argv=None):
     p.add_argument("--alpha", type=float, default=None)
     p.add_argument("--gather-ctas", type=int, default=0)
     p.add_argument("--graph", type=int, default=1, help="1: replay each step from a CUDA graph")
-    p.add_argument("--fused-select", type=int, default=1, help="1: fused cluster score+select kernel")
+    p.add_argument("--fused-select", type=int, default=1, help="1: fused score + select kernel (persistent, scores stay on chip)")
     p.add_argument("--policy", default="threshold", choices=["threshold", "head_avg", "normalized"],
                    help="selection policy (normalized: alpha in units of each head's score std)")
     p.add_argument("--pool-policy", default="counter", choices=["counter", "fifo", "lru"],

@@ -464,7 +464,7 @@ def test_rope_layer_step_end_to_end(ig, pools, name, step, alpha):
 @pytest.mark.parametrize("name", list(SHAPES))
 @pytest.mark.parametrize("alpha", [1e-6, 4.0, float("inf")])
 def test_fused_speculate_select_equals_separate_calls(ig, name, alpha):
-    """The cluster-fused score+select gives the same bytes as ig_speculate then ig_select."""
+    """The fused score + select gives the same bytes as ig_speculate then ig_select."""
     c = make_case(name)
     w = c["w"]
     B, H, d, k, D, Lcap = w.batch, w.heads, w.head_dim, w.k, w.hidden, c["Lcap"]
