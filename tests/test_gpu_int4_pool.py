@@ -175,8 +175,8 @@ def test_decoder_with_int4_pool(mods, fused_fetch):
 
 @pytest.mark.parametrize("fmt", ["fp8", "int4"])
 @pytest.mark.parametrize("with_new", [False, True])
-@pytest.mark.parametrize("d", [128, 64])
-def test_fused_fetch_attend_on_quantized_pools(mods, fmt, with_new, d):
+@pytest.mark.parametrize("d,grid", [(128, 0), (64, 0), (128, 1), (128, 7), (128, 256)])
+def test_fused_fetch_attend_on_quantized_pools(mods, fmt, with_new, d, grid):
     """ig_gather_attend on a quantized pool (codes over the host link, scales from HBM,
     dequantized in registers) against the oracle: its own quantization of the same seeded rows,
     dequantized, then its attention over the same index sets.  The OPT-30B recipe (key scale,
@@ -202,8 +202,10 @@ def test_fused_fetch_attend_on_quantized_pools(mods, fmt, with_new, d):
         ws = torch.empty(ig.ig_gather_attend_workspace_bytes(B, H, d, Lcap), dtype=torch.uint8, device="cuda")
         out = torch.empty((B, H, d), dtype=torch.float32, device="cuda")
         scale = float(np.float32(1.0 / math.sqrt(d)))
+        # grid 0: the library's default; 1, 7, 256: one CTA for every row, ragged CTA ranges that
+        # split heads at odd rows, more CTAs than the small heads need
         ig.ig_gather_attend(None, pool, 0, B, H, d, Lcap, scale, dev(q), dev(idx), dev(cnt),
-                            dev(kn) if with_new else None, dev(vn) if with_new else None, out, ws, ws.numel(), 0)
+                            dev(kn) if with_new else None, dev(vn) if with_new else None, out, ws, ws.numel(), grid)
         ig.ig_check()
         sets = [[idx[b, h, :cnt[b, h]] for h in range(H)] for b in range(B)]
         Kg, Vg = ora.gather(K, V, sets, Lcap)
