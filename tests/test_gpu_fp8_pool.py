@@ -16,6 +16,7 @@ torch = pytest.importorskip("torch")
 from oracle import infinigen as ora  # noqa: E402
 from speculative_kv_cache_gb300 import synth  # noqa: E402
 from gpu_util import dev, host  # noqa: E402
+import quant_decode_check  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -104,42 +105,10 @@ def test_fp8_pool_write_gather_append_bit_exact(mods, d):
 
 @pytest.mark.parametrize("fused_fetch", [False, True])
 def test_decoder_with_fp8_pool(mods, fused_fetch):
+    """Decode steps over an FP8 pool, staged (the fetch dequantizes into HBM) or fused (the
+    fetch stream's attention dequantizes in registers), against the oracle's own selection and its
+    attention over its own quantization of its own pool rows (tests/quant_decode_check.py)."""
     ig, decoder = mods
     w = synth.scaled(synth.WORKLOADS["opt-30b"], name="dec-fp8", layers=3, batch=2, heads=4, hidden=512,
                      prompt=200, gen=6)
-    devn = "cuda:0"
-    cap = w.pool_cap
-    scale = np.float32(1.0 / math.sqrt(w.head_dim))
-    dec = decoder.Decoder(layers=w.layers, B=w.batch, H=w.heads, d=w.head_dim, D=w.hidden, k=w.k, Lcap=w.lcap,
-                          pool_cap=cap, alpha=4.0, pool_fp8=True, fused_fetch=fused_fetch, device=devn)
-    try:
-        for l in range(w.layers):
-            K, V = synth.pool_layer(w, l, cap=cap)
-            cols = synth.skewed_columns(w, l)
-            Wqp = synth.skewed_partial_weight(w, l)
-            t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(devn)  # noqa: E731
-            dec.load_layer(l, t(K), t(V), cols, Wq_part=t(Wqp))
-        dec.prefill(w.prompt)
-        for s in range(2):
-            x = synth.layer_inputs(w, step=s)
-            qkv = [synth.token_inputs(w, l, s) for l in range(w.layers)]
-            q, kn, vn = (np.stack([a[i] for a in qkv]) for i in range(3))
-            out = torch.empty((w.layers, w.batch, w.heads, w.head_dim), dtype=torch.float32, device=devn)
-            L_now = dec.step(*(torch.from_numpy(a).to(devn) for a in (x, q, kn, vn)), out)
-            dec.finish()
-            ig.ig_check(dec.S)
-            o, cnt, idx_buf = out.cpu().numpy(), dec.cnt.cpu().numpy(), dec.idx.cpu().numpy()
-            for l in range(1, w.layers):
-                K8, V8, Ks, Vs = ig.pool_layer_view_fp8(dec.pool, l, w.batch, w.heads, cap, w.head_dim)
-                Kd, Vd = ora.fp8_dequantize_rows(K8, Ks), ora.fp8_dequantize_rows(V8, Vs)
-                gi = idx_buf[l % 2]
-                sets = [[gi[b, h, :cnt[l, b, h]] for h in range(w.heads)] for b in range(w.batch)]
-                # the pool is not full, so this step's token went to slot L_now, beyond every
-                # selected slot: the rows the step read are the ones in the pool now
-                assert all(int(t) < L_now for r in sets for x in r for t in x)
-                Kg, Vg = ora.gather(Kd, Vd, sets, w.lcap)
-                ol = ora.attend(q[l], Kg, Vg, cnt[l], scale, kn[l], vn[l])
-                assert np.abs(o[l] - ol).max() <= 2e-3
-                assert cnt[l].sum() > 0
-    finally:
-        dec.close()
+    quant_decode_check.run(ig, decoder, w, "fp8", "pool_fp8", fused_fetch)
