@@ -57,9 +57,9 @@ def parse_args(argv=None):
     p.add_argument("--append-on-fetch", type=int, default=0,
                    help="1: each layer's append runs on the fetch stream right after its gather")
     p.add_argument("--pool-fp8", type=int, default=0,
-                   help="1: the host pool holds e4m3 rows with a per-row scale (d + 4 bytes per row)")
+                   help="1: the host pool holds e4m3 codes (2d bytes per row, K then V; the row scales in HBM)")
     p.add_argument("--pool-int4", type=int, default=0,
-                   help="1: the host pool holds signed 4-bit rows with a per-row scale (d/2 + 4 bytes per row)")
+                   help="1: the host pool holds signed 4-bit codes (d bytes per row, K then V; the row scales in HBM)")
     p.add_argument("--fused-fetch", type=int, default=-1,
                    help="1: layers 1.. attend straight from the pinned pool on the fetch stream (no staging); "
                         "0: stage the rows in HBM; -1 (default): fused for an int4 pool (measured faster there), "
