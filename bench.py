@@ -652,7 +652,11 @@ def run_ours(args, w, alpha):
 
     # the sampler runs on through the end-to-end steps (stopping nvidia-smi is not free either);
     # only the samples of the device-timed region are summarised
+    t_clock2 = time.time()
     clk.__exit__(None, None, None)
+    clocks = clk.summary(t_clock0, t_clock1)
+    if not clocks["samples"]:  # a timed region shorter than the sampling period
+        clocks = dict(clk.summary(t_clock0, t_clock2), window="the device-timed and end-to-end steps")
 
     if rank == 0:
         line = {
@@ -708,7 +712,7 @@ def run_ours(args, w, alpha):
                               "hbm_peak_source": hbm_src, "link_peak_gbs": link},
             "link_probes_gbs": {k: v for k, v in probes.items() if k != "best"},
             "cpu_baseline": cpu,
-            "clocks": clk.summary(t_clock0, t_clock1),
+            "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     dec.close()

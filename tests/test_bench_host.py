@@ -120,3 +120,18 @@ def test_cpu_baseline_runs_on_small_copies_of_the_workloads(name, over):
     assert (w.pool_cap < w.prompt) == (name == "llama-2-13b")
     secs, n = bench.oracle_on_bench_data(torch, w, w.alphas[0], "cpu", 1)
     assert n == 1 and secs > 0
+
+
+def test_clock_summary_reads_the_timed_window_and_the_throttle_reasons():
+    import bench
+
+    clk = bench.ClockSampler(0)
+    row = "0, {sm}, 2070, 900.5, 0x0, {hw}, Not Active, Not Active, {cap}"
+    clk.lines = [(1.0, row.format(sm=1000, hw="Not Active", cap="Not Active")),  # before the window
+                 (2.0, row.format(sm=2070, hw="Not Active", cap="Active")),
+                 (2.5, row.format(sm=2040, hw="Not Active", cap="Not Active")),
+                 (3.0, row.format(sm=2070, hw="Active", cap="Not Active")),
+                 (9.0, "garbled line")]
+    s = clk.summary(1.5, 3.5)
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["hw_slowdown", "sw_power_cap"], "samples": 3}
+    assert clk.summary(4.0, 5.0)["samples"] == 0
