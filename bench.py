@@ -506,8 +506,9 @@ def run_ours(args, w, alpha):
 
     # CPU baseline: the oracle over every layer of one decode step of the benchmark's own data
     # for a sample of the sequences (about 10 s of NumPy float64 at the OPT-30B shape)
+    # (on rank 0 of a one-GPU run only: with more ranks it would slow the others' setup)
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_seq = max(1, min(w.batch, args.cpu_seqs))
         t_cpu, n_tok = oracle_on_bench_data(torch, w, alpha, device, n_seq)
         cpu = {"value": n_tok / t_cpu, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
